@@ -1,0 +1,371 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+No GPU.  Each test checks the oracle against something other than itself:
+worked numbers printed on the pages (tests/golden/), closed forms, invariants of
+the affine formula, and brute force on tiny inputs written here independently
+(plain Python loops, ``math.exp``, exhaustive candidate search).
+"""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+from oracle import kvq_oracle as O
+
+F32 = np.float32
+
+
+# --------------------------------------------------------------------------- #
+# byte accounting: worked numbers on the pages
+# --------------------------------------------------------------------------- #
+
+
+def test_kv_size_closed_form_llama3_70b():
+    g = read_golden("kv_size_llama3_70b.txt")
+    args = (g["layers"], g["kv_heads"], g["head_dim"], g["seq_len"], g["batch"])
+    bf16 = O.kv_cache_bytes(*args, 2)
+    assert bf16 == g["bf16_bytes"]
+    assert bf16 == g["bf16_gib"] * 2 ** 30
+    assert O.kv_cache_bytes(*args, 1) == g["fp8_gib"] * 2 ** 30
+    assert O.kv_cache_bytes(*args, 0.5) == g["int4_gib"] * 2 ** 30
+    assert O.kv_cache_bytes(*args, 0.25) == g["int2_gib"] * 2 ** 30
+
+
+def test_per_token_bytes_table():
+    g = read_golden("per_token_kv_bytes.txt")
+    # the fp8 row fixes the number of cached elements per token (1 byte each)
+    elems = g["fp8_e4m3_kib"] * 1024
+    q8 = O.block_format_bits_per_element(8, g["block"], g["scale_bits"])
+    q4 = O.block_format_bits_per_element(4, g["block"], g["scale_bits"])
+    assert q8 == 8.5 and q4 == 4.5
+    assert elems * q8 / 8 == g["q8_0_kib"] * 1024
+    assert elems * q4 / 8 == g["q4_0_kib"] * 1024
+    ctx = g["context_tokens"]
+    for kib, gib in ((g["q8_0_kib"], g["q8_0_gib_64k"]), (g["fp8_e4m3_kib"], g["fp8_e4m3_gib_64k"]),
+                     (g["q4_0_kib"], g["q4_0_gib_64k"])):
+        size = kib * 1024 * ctx / 2 ** 30
+        assert abs(size - gib) <= 0.005 + 1e-12
+
+
+# --------------------------------------------------------------------------- #
+# affine quantizer
+# --------------------------------------------------------------------------- #
+
+
+def _groups(seed, shape, scale=1.0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape).astype(F32) * F32(scale)
+    x[..., 0] += F32(3.0)   # off-centre groups (asymmetric case)
+    return x
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_codes_in_range_and_endpoints(bits):
+    x = _groups(bits, (300, 37), 5.0)
+    q, s, z = O.affine_quantize(x, bits)
+    assert q.dtype == np.uint8 and q.max() <= 2 ** bits - 1
+    rows = np.arange(x.shape[0])
+    assert np.all(q[rows, x.argmin(axis=1)] == 0)
+    assert np.all(q[rows, x.argmax(axis=1)] == 2 ** bits - 1)
+    assert s.dtype == np.float32 and z.dtype == np.float32
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_reconstruction_error_bound(bits):
+    # |x - x_hat| <= s/2 inside the clamp range (the group's own [min, max]),
+    # plus the fp32 rounding of x/s + z (a few ulps of 2^b)
+    x = _groups(10 + bits, (500, 64), 3.0)
+    q, s, z = O.affine_quantize(x, bits)
+    xh = O.affine_dequantize_f64(q, s[:, None], z[:, None])
+    slack = s.astype(np.float64)[:, None] * (2.0 ** (bits - 20))
+    assert np.all(np.abs(x - xh) <= s.astype(np.float64)[:, None] / 2 + slack)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_rounding_brute_force(bits):
+    # every code is the nearest integer of fl(fl(x/s) + z) in [0, 2^b-1], ties to even,
+    # found by trying every candidate code
+    x = _groups(20 + bits, (40, 9), 2.0)
+    q, s, z = O.affine_quantize(x, bits)
+    for i in range(x.shape[0]):
+        for j in range(x.shape[1]):
+            t = float(F32(F32(x[i, j] / s[i]) + z[i]))
+            # smallest distance first, then the even code among equally near ones
+            best = min((abs(t - c), c % 2, c) for c in range(2 ** bits))
+            assert q[i, j] == best[2], (i, j, t, q[i, j], best)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_on_grid_values_reconstruct_exactly(bits):
+    # power-of-two s and an integer zero-point: a group holding codes 0 and 2^b-1
+    # (so that min/max fix s and z) reconstructs exactly
+    levels = 2 ** bits - 1
+    rng = np.random.default_rng(bits)
+    for s0 in (2.0 ** -3, 0.5, 4.0):
+        z0 = int(rng.integers(0, levels + 1))
+        codes = rng.integers(0, levels + 1, size=30)
+        codes[0], codes[1] = 0, levels
+        x = (s0 * (codes - z0)).astype(F32)
+        q, s, z = O.affine_quantize(x, bits)
+        assert s == F32(s0) and z == F32(z0)
+        assert np.array_equal(q, codes.astype(np.uint8))
+        assert np.array_equal(O.affine_dequantize_f32(q, s, z), x)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_ties_round_to_even(bits):
+    levels = 2 ** bits - 1
+    s0, z0 = 0.25, 1
+    ks = np.arange(0, levels)                    # x/s + z = k + 1/2 exactly
+    x = np.concatenate([[s0 * (0 - z0), s0 * (levels - z0)], s0 * (ks + 0.5 - z0)]).astype(F32)
+    q, s, z = O.affine_quantize(x, bits)
+    assert s == F32(s0) and z == F32(z0)
+    expect = np.where(ks % 2 == 0, ks, ks + 1)
+    assert np.array_equal(q[2:], expect.astype(np.uint8))
+
+
+def test_constant_group():
+    for c in (0.0, -1.5, 3.0e-3):
+        x = np.full(16, c, F32)
+        q, s, z = O.affine_quantize(x, 4)
+        assert s == F32(1.0) and np.all(q == 0)
+        assert np.array_equal(O.affine_dequantize_f32(q, s, z), x)
+
+
+def test_key_per_channel_value_per_token_axes():
+    # Keys: every channel of every G-token group has its own (s, z);
+    # Values: every Gv-slice of every token has its own (s, z).
+    spec = O.Spec("int4", d=16, G=8, Gv=4)
+    rng = np.random.default_rng(5)
+    k = rng.standard_normal((24, 16)).astype(F32)
+    k[:, 3] *= 50
+    kc, ks, kz = O.quantize_key_groups(k, spec)
+    assert ks.shape == (3, 16)
+    for gi in range(3):
+        blk = k[gi * 8:(gi + 1) * 8]
+        for c in range(16):
+            col = kc[gi * 8:(gi + 1) * 8, c]
+            assert col[blk[:, c].argmin()] == 0 and col[blk[:, c].argmax()] == 15
+            assert ks[gi, c] == F32(F32(blk[:, c].max() - blk[:, c].min()) / F32(15))
+    v = rng.standard_normal((24, 16)).astype(F32)
+    vc, vs, vz = O.quantize_value_tokens(v, spec)
+    assert vs.shape == (24, 4)
+    for t in range(24):
+        for j in range(4):
+            seg = v[t, 4 * j:4 * j + 4]
+            cs = vc[t, 4 * j:4 * j + 4]
+            assert cs[seg.argmin()] == 0 and cs[seg.argmax()] == 15
+
+
+# --------------------------------------------------------------------------- #
+# FP8 E4M3 (OCP E4M3FN)
+# --------------------------------------------------------------------------- #
+
+
+def test_e4m3_known_values():
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3F: 1.875,
+             0x40: 2.0, 0x7E: 448.0, 0x7D: 416.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in cases.items():
+        assert O.e4m3_decode(np.array([c]))[0] == v
+    assert np.isnan(O.e4m3_decode(np.array([0x7F, 0xFF]))).all()
+    assert math.copysign(1.0, O.e4m3_decode(np.array([0x80]))[0]) == -1.0
+
+
+def test_e4m3_roundtrip_all_finite_codes():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = O.e4m3_decode(codes).astype(F32)
+    assert np.array_equal(O.e4m3_encode(vals), codes)
+
+
+def _bf16_all_finite():
+    bits = np.arange(65536, dtype=np.uint32)
+    f = (bits << 16).view(np.float32)
+    return f[np.isfinite(f)]
+
+
+def test_e4m3_encode_exhaustive_bf16_brute_force():
+    # nearest finite value, ties to the even code, saturate to +-448, keep the sign of zero;
+    # found by comparing against every one of the 127 non-negative finite codes
+    xs = _bf16_all_finite()
+    for scale in (1.0, 0.37, 3.0e-3, 61.0):
+        with np.errstate(over="ignore"):
+            v = (xs / F32(scale)).astype(F32)
+        got = O.e4m3_encode(v)
+        table = [(c, float(O.e4m3_decode(np.array([c]))[0])) for c in range(0x7F)]
+        a = np.abs(v.astype(np.float64))
+        best_d = np.full(a.shape, np.inf)
+        best_c = np.zeros(a.shape, np.int64)
+        for c, val in table:
+            d = np.abs(a - val)
+            better = (d < best_d) | ((d == best_d) & (c % 2 == 0))
+            best_d = np.where(better, d, best_d)
+            best_c = np.where(better, c, best_c)
+        best_c = np.where(a > 448.0, 0x7E, best_c)
+        best_c |= np.signbit(v).astype(np.int64) << 7
+        assert np.array_equal(got, best_c.astype(np.uint8)), scale
+
+
+def test_fp8_tensor_scale():
+    x = np.array([-3.5, 1.0, 2.0], F32)
+    assert O.fp8_tensor_scale(x) == F32(F32(3.5) / F32(448))
+    assert O.fp8_tensor_scale(np.zeros(4, F32)) == F32(1.0)
+    # the calibration tensor's amax maps to the largest finite code
+    s = O.fp8_tensor_scale(x)
+    assert O.fp8_quantize(x, s)[0] == 0xFE
+
+
+# --------------------------------------------------------------------------- #
+# cache state machine
+# --------------------------------------------------------------------------- #
+
+
+def test_token_split_workloads():
+    assert O.token_split(512, O.Spec("int4", G=32, Gv=128, R=32, S=0)) == (0, 480, 32)
+    assert O.token_split(8192, O.Spec("int4", G=128, Gv=128, R=128, S=0)) == (0, 8064, 128)
+    sp = O.Spec("int2", G=32, Gv=32, R=128, S=0)
+    assert O.token_split(32767, sp) == (0, 32608, 159)
+    assert O.token_split(32768, sp) == (0, 32640, 128)
+    sp5 = O.Spec("int4", G=16, Gv=128, R=64, S=1)
+    assert O.token_split(1, sp5) == (1, 0, 0)
+    assert O.token_split(80, sp5) == (1, 0, 79)
+    assert O.token_split(81, sp5) == (1, 16, 64)
+    assert O.token_split(9, O.Spec("fp8_e4m3", G=1, R=0, S=0)) == (0, 9, 0)
+
+
+def _same_cache(a, b):
+    for f in ("sink_k", "sink_v", "k_codes", "v_codes", "resid_k", "resid_v", "k_s", "k_z", "v_s", "v_z"):
+        x, y = getattr(a, f), getattr(b, f)
+        if x is None:
+            assert y is None
+            continue
+        assert x.shape == y.shape and np.array_equal(x, y), f
+
+
+@pytest.mark.parametrize("spec", [
+    O.Spec("int4", d=16, G=8, Gv=8, R=4, S=0),
+    O.Spec("int2", d=16, G=4, Gv=16, R=8, S=1),
+    O.Spec("int8", d=16, G=16, Gv=4, R=0, S=2),
+    O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=1),
+])
+def test_bulk_build_equals_appends(spec):
+    rng = np.random.default_rng(7)
+    T = 61
+    k = rng.standard_normal((T, 16)).astype(F32)
+    v = rng.standard_normal((T, 16)).astype(F32)
+    ks = O.fp8_tensor_scale(k) if spec.is_fp8 else None
+    vs = O.fp8_tensor_scale(v) if spec.is_fp8 else None
+    hc = O.empty_head_cache(spec, ks, vs)
+    for t in range(T):
+        O.append_token(hc, k[t], v[t])
+        bulk = O.build_head_cache(k[:t + 1], v[:t + 1], spec, ks, vs)
+        _same_cache(hc, bulk)
+        n_sink, qn, r = O.token_split(t + 1, spec)
+        assert (len(hc.sink_k), len(hc.k_codes), len(hc.resid_k)) == (n_sink, qn, r)
+        if not spec.is_fp8:
+            assert r < spec.R + spec.G
+
+
+# --------------------------------------------------------------------------- #
+# attention
+# --------------------------------------------------------------------------- #
+
+
+def _brute_attention(q, K, V, scale):
+    """Plain-Python softmax(q K^T * scale) V and its log-sum-exp."""
+    scores = [sum(float(a) * float(b) for a, b in zip(q, krow)) * scale for krow in K]
+    mx = max(scores)
+    w = [math.exp(s - mx) for s in scores]
+    tot = sum(w)
+    out = [sum(w[t] * float(V[t][c]) for t in range(len(V))) / tot for c in range(len(V[0]))]
+    return out, mx + math.log(tot)
+
+
+def _dequant_brute(hc):
+    """x_hat = s (q - z) element by element in Python floats (fp64)."""
+    sp = hc.spec
+    ks, vs = [], []
+    for t in range(len(hc.sink_k)):
+        ks.append(list(map(float, hc.sink_k[t])))
+        vs.append(list(map(float, hc.sink_v[t])))
+    for t in range(len(hc.k_codes)):
+        if sp.is_fp8:
+            ks.append([float(hc.k_scale) * float(O.e4m3_decode(np.array([c]))[0]) for c in hc.k_codes[t]])
+            vs.append([float(hc.v_scale) * float(O.e4m3_decode(np.array([c]))[0]) for c in hc.v_codes[t]])
+        else:
+            g = t // sp.G
+            ks.append([float(hc.k_s[g, c]) * (int(hc.k_codes[t, c]) - float(hc.k_z[g, c])) for c in range(sp.d)])
+            vs.append([float(hc.v_s[t, c // sp.Gv]) * (int(hc.v_codes[t, c]) - float(hc.v_z[t, c // sp.Gv]))
+                       for c in range(sp.d)])
+    for t in range(len(hc.resid_k)):
+        ks.append(list(map(float, hc.resid_k[t])))
+        vs.append(list(map(float, hc.resid_v[t])))
+    return ks, vs
+
+
+@pytest.mark.parametrize("spec", [
+    O.Spec("int4", d=16, G=8, Gv=8, R=4, S=1),
+    O.Spec("int2", d=16, G=4, Gv=16, R=8, S=0),
+    O.Spec("int8", d=16, G=16, Gv=4, R=2, S=0),
+    O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=1),
+])
+def test_attention_brute_force(spec):
+    rng = np.random.default_rng(11)
+    B, Hkv, g, T = 2, 2, 3, 37
+    q = rng.standard_normal((B, Hkv * g, 16)).astype(F32)
+    caches = []
+    for b in range(B):
+        row = []
+        for h in range(Hkv):
+            k = (rng.standard_normal((T, 16)) * 2).astype(F32)
+            v = rng.standard_normal((T, 16)).astype(F32)
+            ks = O.fp8_tensor_scale(k) if spec.is_fp8 else None
+            vs = O.fp8_tensor_scale(v) if spec.is_fp8 else None
+            row.append(O.build_head_cache(k, v, spec, ks, vs))
+        caches.append(row)
+    out, lse = O.decode_attention(q, caches)
+    for b in range(B):
+        for hq in range(Hkv * g):
+            K, V = _dequant_brute(caches[b][hq // g])
+            o, l = _brute_attention(q[b, hq], K, V, 1 / math.sqrt(16))
+            assert np.allclose(out[b, hq], o, rtol=0, atol=1e-12)
+            assert abs(lse[b, hq] - l) < 1e-12
+
+
+def test_attention_single_token_and_uniform():
+    spec = O.Spec("int4", d=8, G=4, Gv=8, R=4, S=0)
+    k = np.array([[1, -2, 0.5, 0, 3, 1, 1, -1]], F32)
+    v = np.array([[0.25, 1, -1, 2, 0, 0, 3, 4]], F32)
+    hc = O.build_head_cache(k, v, spec)
+    q = np.ones((1, 1, 8), F32)
+    out, lse = O.decode_attention(q, [[hc]])
+    assert np.allclose(out[0, 0], v[0], atol=0, rtol=0)
+    assert lse[0, 0] == pytest.approx(float(k[0] @ q[0, 0]) / math.sqrt(8), abs=1e-15)
+    # every token has the same key -> every score equal: out = mean(v), lse = score + ln T
+    T = 6
+    kk = np.repeat(k, T, axis=0)
+    vv = np.arange(T * 8, dtype=F32).reshape(T, 8)
+    hc = O.build_head_cache(kk, vv, spec)
+    assert len(hc.k_codes) == 0                     # T < R + G: all bf16
+    out, lse = O.decode_attention(q, [[hc]])
+    assert np.allclose(out[0, 0], vv.mean(axis=0), atol=1e-12)
+    assert lse[0, 0] == pytest.approx(float(k[0] @ q[0, 0]) / math.sqrt(8) + math.log(T), abs=1e-12)
+
+
+def test_gqa_equals_replicated_mha_and_token_order():
+    spec = O.Spec("int4", d=16, G=8, Gv=16, R=8, S=0)
+    rng = np.random.default_rng(3)
+    T = 40
+    k = rng.standard_normal((T, 16)).astype(F32)
+    v = rng.standard_normal((T, 16)).astype(F32)
+    hc = O.build_head_cache(k, v, spec)
+    q = rng.standard_normal((1, 4, 16)).astype(F32)
+    out_gqa, lse_gqa = O.decode_attention(q, [[hc]])
+    out_mha, lse_mha = O.decode_attention(q, [[hc, hc, hc, hc]])
+    assert np.array_equal(out_gqa, out_mha) and np.array_equal(lse_gqa, lse_mha)
+    kh, vh = O.dequantized_f64(hc)
+    perm = rng.permutation(T)
+    for j in range(4):
+        o1, l1 = O.attend_head(q[0, j], kh, vh, 0.25)
+        o2, l2 = O.attend_head(q[0, j], kh[perm], vh[perm], 0.25)
+        assert np.allclose(o1, o2, atol=1e-13) and abs(l1 - l2) < 1e-13
