@@ -1,0 +1,249 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) quantized KV-cache decode library (libkvq.so).
+ *
+ * The library implements attention decode over a KV cache stored with
+ * asymmetric affine quantization (Keys per channel over groups of tokens,
+ * Values per token over groups of channels) at 2, 4 or 8 bits, or as FP8 E4M3
+ * with a per-tensor fp32 scale; a bf16 residual window of recent tokens and
+ * bf16 attention-sink tokens; per-layer formats; contiguous or paged storage.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [KVQA] "KV Cache Quantization Analysis" (ryotta.opik.net, KV 캐시 양자화 심층 분석)
+ *          s2 "양자화 기초 / 핵심 개념"       q = round(x/s + z), x_hat = s(q - z); asymmetric z
+ *          s3 "Key=per-channel, Value=per-token" Key per channel, Value per token, residual window
+ *          s4 "FP8 / INT8"                    E4M3 with an fp32 scale; INT8 needs scale storage
+ *          s5 "구현·시스템 고려사항"          quantize the new K,V at write; dequantize right before
+ *                                             attention, fused with the matmul; paging is orthogonal
+ *          box "메모리 크기 감각"             KV bytes = 2 L H_kv d T B bytes
+ *   [W4KV] "W4A16 + KV cache quantization combined accuracy" (hrletsgo.me)
+ *          "오차가 어디서 만나는가"           softmax(Q K^T / sqrt(d))
+ *          "어떤 레이어가 더 민감한가"        sink token K/V kept 16-bit; FP8/INT8 early/late, INT4 middle
+ *   [AIQK] "양자화와 KV 캐시" (ai-trend.me)    PagedAttention: fixed-size blocks and a per-request table
+ *
+ * Conventions for every entry point
+ *   - All buffers are owned by the caller.  The library allocates no memory and
+ *     keeps no global state.  Pointers marked "device" are CUDA device pointers.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL =
+ *     the legacy default stream).  They return once the work is enqueued.
+ *   - A host-detectable error (bad sizes, unsupported combination, null pointer,
+ *     workspace too small) returns a negative kvq_status and enqueues nothing.
+ *     A failed launch returns KVQ_ERR_CUDA.
+ *   - Data-dependent errors found on the device (a block id outside the pool, a
+ *     length beyond the capacity, a bounded wait that gave up) are OR-ed as
+ *     KVQ_DEV_* bits into *dev_status (device uint32; may be NULL to drop them).
+ *     The offending load or store is skipped; kernels never trap and never wait
+ *     without a bound.  The caller clears *dev_status.
+ *   - head_dim must be 128; 1 <= num_q_heads / num_kv_heads <= 8.
+ *
+ * Token accounting of one (sequence, kv head) holding T tokens (S sink tokens,
+ * R residual tokens, K group G):  the first min(T, S) tokens are the sink (bf16);
+ * Q_n = max(0, floor((T - S - R) / G)) * G tokens are quantized; the last
+ * r = T - S - Q_n tokens are the residual window (bf16).  FP8 layers use G = 1
+ * and R = 0 (every token after the sink is quantized at once).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = -1, /* argument outside its documented range, null pointer */
+  KVQ_ERR_UNSUPPORTED = -2, /* valid but not implemented combination (e.g. head_dim != 128) */
+  KVQ_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  KVQ_ERR_WORKSPACE = -4    /* workspace smaller than kvq_decode_workspace_size() */
+} kvq_status;
+
+typedef enum {
+  KVQ_FMT_INT2 = 2,     /* 2-bit affine codes, fp32 scale + fp32 zero-point per group */
+  KVQ_FMT_INT4 = 4,     /* 4-bit affine codes */
+  KVQ_FMT_INT8 = 8,     /* 8-bit affine codes */
+  KVQ_FMT_FP8_E4M3 = 16 /* OCP E4M3FN codes, one fp32 scale per tensor (K and V each) */
+} kvq_format;
+
+/* bits OR-ed into *dev_status */
+#define KVQ_DEV_BAD_BLOCK 0x1u  /* a block-table entry outside [0, num_blocks) */
+#define KVQ_DEV_CAPACITY 0x2u   /* a sequence longer than the store can hold */
+#define KVQ_DEV_TIMEOUT 0x4u    /* a bounded wait for an asynchronous copy gave up */
+
+/* Per-layer configuration (host struct, read during the call only). */
+typedef struct {
+  int32_t num_kv_heads;       /* H_kv >= 1 */
+  int32_t head_dim;           /* d, must be 128 */
+  int32_t format;             /* kvq_format */
+  int32_t k_group_tokens;     /* G: tokens per Key group (per-channel scale); multiple of 16; 1 for FP8 */
+  int32_t v_group_dims;       /* Gv: channels per Value group (per-token scale); 8,16,32,64,128; FP8: 128 */
+  int32_t residual_tokens;    /* R >= 0 bf16 recent tokens kept (0 for FP8) */
+  int32_t sink_tokens;        /* S >= 0 bf16 first tokens kept */
+  int32_t paged;              /* 0: contiguous store, 1: paged store */
+  int32_t block_tokens;       /* paged: tokens per block P (INT: P == G; FP8: multiple of 16) */
+  int32_t capacity_tokens;    /* contiguous: quantized tokens per (seq, head); multiple of 16 and of G */
+  int32_t num_blocks;         /* paged: blocks in the pool */
+  int32_t max_blocks_per_seq; /* paged: row length of the block table */
+} kvq_layer_config;
+
+/*
+ * Device buffers of one layer's cache.  Which fields are used depends on the
+ * config; unused fields may be NULL.  With B = sequences, H = num_kv_heads,
+ * d = 128, b = bits (8 for FP8), rb = d*b/8 bytes per token row, W = R + G:
+ *
+ * Contiguous store (paged == 0), cap = capacity_tokens, per (seq, head) in
+ * [B][H] order:
+ *   k_codes  u8  [B][H][cap][rb]       token x's row; channel c in byte c/(8/b) at bit (c mod (8/b))*b
+ *   v_codes  u8  [B][H][cap/16][16*rb] 16-token tiles in "fragment order" (below)
+ *   k_scale  f32 [B][H][cap/G][d]      per-channel scale of each G-token Key group   (INT only)
+ *   k_zero   f32 [B][H][cap/G][d]      per-channel zero-point                         (INT only)
+ *   v_scale  f32 [B][H][cap][d/Gv]     per-token scale of each Gv-channel Value group (INT only)
+ *   v_zero   f32 [B][H][cap][d/Gv]                                                    (INT only)
+ * Paged store (paged == 1), P = block_tokens: block_pool holds num_blocks blocks
+ * of H head slabs; a slab is, in this order:
+ *   K codes [P][rb], V codes [P/16][16*rb] (fragment order),
+ *   K scale [P/G][d] f32, K zero [P/G][d] f32, V scale [P][d/Gv] f32, V zero [P][d/Gv] f32
+ *   (scales and zeros only for INT formats).  Quantized token x (= t - S) of
+ *   sequence b lives in block block_table[b*max_blocks_per_seq + x/P], row x mod P.
+ * Both stores index quantized tokens x = t - S only.
+ * bf16 parts (both stores):
+ *   resid_k, resid_v  bf16 [B][H][W][d]  residual token t in slot (t - S) mod W
+ *   sink_k,  sink_v   bf16 [B][H][S][d]
+ * FP8: k_tensor_scale, v_tensor_scale point to one device float each (amax/448,
+ * see kvq_fp8_calibrate); they stay fixed for later appends.
+ *
+ * Fragment order of a 16-token Value tile (token t in [0,16), channel c in
+ * [0,128)): n = c mod 8, j = c / 8, lane = 4n + (t mod 8)/2, e = (t mod 2) + 2(t / 8).
+ *   INT4: byte lane*32 + 4(j/2) + o/8, bits o mod 8, o = {0,16,4,20}[e] + 8(j mod 2)
+ *   INT2: byte lane*16 + 4(j/4) + o/8, bits o mod 8, o = 2(2(j mod 4) + e/2) + 16(e mod 2)
+ *   INT8: byte lane*64 + 4j + {0,2,1,3}[e]
+ *   FP8:  byte lane*64 + 4j + e
+ * i.e. each lane of a decode warp reads one contiguous run whose words unpack
+ * directly into tensor-core operand registers.
+ */
+typedef struct {
+  void* k_codes;
+  void* v_codes;
+  float* k_scale;
+  float* k_zero;
+  float* v_scale;
+  float* v_zero;
+  void* block_pool;
+  const int32_t* block_table;
+  void* resid_k;
+  void* resid_v;
+  void* sink_k;
+  void* sink_v;
+  const float* k_tensor_scale;
+  const float* v_tensor_scale;
+} kvq_layer_cache;
+
+/* Indices of kvq_cache_layout()'s output array. */
+enum {
+  KVQ_FIELD_K_CODES = 0,
+  KVQ_FIELD_V_CODES,
+  KVQ_FIELD_K_SCALE,
+  KVQ_FIELD_K_ZERO,
+  KVQ_FIELD_V_SCALE,
+  KVQ_FIELD_V_ZERO,
+  KVQ_FIELD_BLOCK_POOL,
+  KVQ_FIELD_RESID_K,
+  KVQ_FIELD_RESID_V,
+  KVQ_FIELD_SINK_K,
+  KVQ_FIELD_SINK_V,
+  KVQ_FIELD_COUNT
+};
+
+/*
+ * kvq_cache_layout -- bytes of each cache buffer for `num_seqs` sequences.
+ * Validates `cfg` (same rules as the other calls).  bytes[i] is 0 for a field
+ * the config does not use.  Host only; no CUDA call.
+ * Layout: see kvq_layer_cache.  Source: [KVQA] box "메모리 크기 감각" (sizes),
+ * s3 (per-channel K / per-token V groups), [AIQK] (blocks and block table).
+ */
+kvq_status kvq_cache_layout(const kvq_layer_config* cfg, int32_t num_seqs, size_t bytes[KVQ_FIELD_COUNT]);
+
+/*
+ * kvq_fp8_calibrate -- per-tensor FP8 scale s = amax/448 (fp32 division; s = 1
+ * when amax == 0) of `n` bf16 values at device pointer x; written to the device
+ * float *scale_out.  Source: [KVQA] s4 (E4M3 needs an fp32 scale) and s5
+ * (calibrated scales).  448 is the largest finite OCP E4M3FN value.
+ */
+kvq_status kvq_fp8_calibrate(const void* x, size_t n, float* scale_out, void* stream);
+
+/*
+ * kvq_quantize_append -- write `n_new` new tokens per (sequence, kv head).
+ * Source: [KVQA] s5 (quantize the new K,V right after they are computed and
+ * store them), s2 (affine formula), s3 (Key per channel over G tokens, Value
+ * per token over Gv channels, full-precision residual window), s4 (FP8);
+ * [W4KV] (sink tokens kept 16-bit).
+ *   k_new, v_new  device bf16 [batch][H][n_new][d]
+ *   seq_lens      device int32 [batch]: tokens already in the cache (before)
+ * Tokens t < S go to the sink; otherwise to the residual ring; every time the
+ * ring reaches R + G tokens its oldest G are quantized as one Key group (per
+ * channel: s = (max - min)/(2^b - 1), z = -(min/s), q = clamp(rne(x/s + z))
+ * in IEEE fp32, s = 1 for a constant group) and G Value tokens (per token and
+ * Gv-channel group, same formula).  FP8: code = E4M3 RNE satfinite of
+ * fp32(x / s_tensor).  Result identical to n_new single-token appends.
+ * The caller advances seq_lens by n_new afterwards, and for a paged store has
+ * the blocks of every group that spills already in the block table.
+ * Device errors: KVQ_DEV_CAPACITY (store full: nothing written for that
+ * sequence), KVQ_DEV_BAD_BLOCK (that group skipped).
+ */
+kvq_status kvq_quantize_append(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* k_new,
+                               const void* v_new, int32_t n_new, const int32_t* seq_lens, int32_t batch,
+                               uint32_t* dev_status, void* stream);
+
+/*
+ * kvq_decode_workspace_size -- device workspace bytes kvq_decode_attention
+ * needs for this config, batch and query-head count on the current device.
+ */
+kvq_status kvq_decode_workspace_size(const kvq_layer_config* cfg, int32_t batch, int32_t num_q_heads,
+                                     size_t* bytes);
+
+/*
+ * kvq_decode_attention -- one decode step of attention over the quantized cache.
+ * Source: [W4KV] "오차가 어디서 만나는가" (softmax(q K^T / sqrt(d)) V);
+ * [KVQA] s5 (dequantize right before attention, fused with the matmul, else
+ * the bandwidth saving is lost) and s1 (decode is bound by reading the cache).
+ *   q         device bf16 [batch][num_q_heads][d]; query head h reads kv head
+ *             h / (num_q_heads / H) (grouped-query attention)
+ *   seq_lens  device int32 [batch]: tokens in the cache (after this step's append)
+ *   softmax_scale  multiplies q.k (1/sqrt(d) for the plain formula)
+ *   out       device [batch][num_q_heads][d], fp32 (out_bf16 == 0) or bf16
+ *             (out_bf16 == 1: the round-to-nearest-even of the fp32 result)
+ *   lse       device f32 [batch][num_q_heads] natural-log log-sum-exp of the
+ *             scaled scores, or NULL
+ *   workspace device, at least kvq_decode_workspace_size() bytes, no alignment
+ *             beyond 16 bytes, contents need not be initialised
+ * A sequence with 0 tokens gets out = 0, lse = -inf.  Device errors:
+ * KVQ_DEV_BAD_BLOCK (tile skipped), KVQ_DEV_CAPACITY (length clamped to the
+ * capacity), KVQ_DEV_TIMEOUT.
+ */
+kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
+                                void* out, int32_t out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, void* stream);
+
+/*
+ * kvq_dequantize -- export the dequantized cache as fp32.
+ * Source: [KVQA] s2 (x_hat = s(q - z)), s4 (FP8 value times its scale).
+ *   k_out, v_out  device f32 [batch][H][max_tokens][d]; token t < seq_lens[b]
+ *   gets x_hat (sink / residual: the bf16 value; INT: s*(q - z) as two fp32
+ *   operations; FP8: s * E4M3 value in fp32), tokens t >= seq_lens[b] get 0.
+ *   seq_lens      device int32 [batch]; a length above max_tokens is an error
+ *   (KVQ_DEV_CAPACITY) and is clamped.
+ */
+kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const int32_t* seq_lens,
+                          int32_t batch, int32_t max_tokens, float* k_out, float* v_out, uint32_t* dev_status,
+                          void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

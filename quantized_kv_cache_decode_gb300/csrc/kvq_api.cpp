@@ -1,0 +1,345 @@
+// Host side of the libkvq C ABI: argument validation, cache layout, launch
+// configuration and dispatch.  See include/kvq.h for the contract.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreadsDecode = 128;  // 4 warps (kvq_decode.cuh)
+constexpr int kMaxStages = 4;
+constexpr int kWarpScratch = 16 * 272;
+constexpr int kSmemPerCtaTarget = 110 * 1024;  // two resident CTAs per SM
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
+  if (!cfg || !L) return KVQ_ERR_INVALID_ARG;
+  memset(L, 0, sizeof(*L));
+  if (cfg->num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;
+  if (cfg->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  const int f = cfg->format;
+  if (f != KVQ_FMT_INT2 && f != KVQ_FMT_INT4 && f != KVQ_FMT_INT8 && f != KVQ_FMT_FP8_E4M3)
+    return KVQ_ERR_INVALID_ARG;
+  L->H = cfg->num_kv_heads;
+  L->d = kHeadDim;
+  L->fmt = f;
+  L->fp8 = (f == KVQ_FMT_FP8_E4M3);
+  L->bits = L->fp8 ? 8 : f;
+  L->rb = L->d * L->bits / 8;
+  L->S = cfg->sink_tokens;
+  if (L->S < 0) return KVQ_ERR_INVALID_ARG;
+  if (L->fp8) {
+    if (cfg->k_group_tokens != 1 || cfg->residual_tokens != 0) return KVQ_ERR_INVALID_ARG;
+    L->G = 1;
+    L->Gv = kHeadDim;
+    L->R = 0;
+    L->W = 0;
+  } else {
+    L->G = cfg->k_group_tokens;
+    L->Gv = cfg->v_group_dims;
+    L->R = cfg->residual_tokens;
+    if (L->G < 16 || L->G % 16 != 0 || L->R < 0) return KVQ_ERR_INVALID_ARG;
+    if (L->Gv != 16 && L->Gv != 32 && L->Gv != 64 && L->Gv != 128) return KVQ_ERR_INVALID_ARG;
+    L->W = L->R + L->G;
+  }
+  L->ngv = L->d / L->Gv;
+  L->paged = cfg->paged ? 1 : 0;
+  if (L->paged) {
+    L->P = cfg->block_tokens;
+    L->num_blocks = cfg->num_blocks;
+    L->mbps = cfg->max_blocks_per_seq;
+    if (L->P < 16 || L->P % 16 != 0 || L->num_blocks < 1 || L->mbps < 1) return KVQ_ERR_INVALID_ARG;
+    if (!L->fp8 && L->P != L->G) return KVQ_ERR_INVALID_ARG;
+    long long off = 0;
+    L->off_kc = 0;
+    off += (long long)L->P * L->rb;
+    L->off_vc = (int)off;
+    off += (long long)L->P * L->rb;
+    if (!L->fp8) {
+      L->off_ks = (int)off;
+      off += (long long)(L->P / L->G) * L->d * 4;
+      L->off_kz = (int)off;
+      off += (long long)(L->P / L->G) * L->d * 4;
+      L->off_vs = (int)off;
+      off += (long long)L->P * L->ngv * 4;
+      L->off_vz = (int)off;
+      off += (long long)L->P * L->ngv * 4;
+    }
+    L->slab_bytes = (off + 15) / 16 * 16;
+    L->block_bytes = L->slab_bytes * L->H;
+  } else {
+    L->cap = cfg->capacity_tokens;
+    if (L->cap < 0 || L->cap % 16 != 0 || (!L->fp8 && L->cap % L->G != 0)) return KVQ_ERR_INVALID_ARG;
+  }
+  return KVQ_OK;
+}
+
+CachePtrs make_ptrs(const kvq_layer_cache* c) {
+  CachePtrs p;
+  p.k_codes = c->k_codes;
+  p.v_codes = c->v_codes;
+  p.k_scale = c->k_scale;
+  p.k_zero = c->k_zero;
+  p.v_scale = c->v_scale;
+  p.v_zero = c->v_zero;
+  p.block_pool = c->block_pool;
+  p.block_table = c->block_table;
+  p.resid_k = c->resid_k;
+  p.resid_v = c->resid_v;
+  p.sink_k = c->sink_k;
+  p.sink_v = c->sink_v;
+  p.k_tscale = c->k_tensor_scale;
+  p.v_tscale = c->v_tensor_scale;
+  return p;
+}
+
+// The buffers a config uses must be present and 16-byte aligned (bulk copies).
+kvq_status check_cache(const LayerDesc& L, const kvq_layer_cache* c) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  auto need = [](const void* p) { return p != nullptr && aligned16(p); };
+  if (L.paged) {
+    if (!need(c->block_pool) || !c->block_table) return KVQ_ERR_INVALID_ARG;
+  } else if (L.cap > 0) {
+    if (!need(c->k_codes) || !need(c->v_codes)) return KVQ_ERR_INVALID_ARG;
+    if (!L.fp8 && (!need(c->k_scale) || !need(c->k_zero) || !need(c->v_scale) || !need(c->v_zero)))
+      return KVQ_ERR_INVALID_ARG;
+  }
+  if (!L.fp8 && (!need(c->resid_k) || !need(c->resid_v))) return KVQ_ERR_INVALID_ARG;
+  if (L.S > 0 && (!need(c->sink_k) || !need(c->sink_v))) return KVQ_ERR_INVALID_ARG;
+  if (L.fp8 && (!c->k_tensor_scale || !c->v_tensor_scale)) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+int stage_bytes_of(const LayerDesc& L) {
+  int b = 2 * 16 * L.rb;
+  if (!L.fp8) b += 128 * L.ngv + 1024;
+  return b;
+}
+
+int fixed_smem(int batch) {
+  int prefix = ((batch + 1) * 4 + 15) / 16 * 16;
+  return kThreadsDecode / 32 * kMaxStages * 8 + 8 * 4 * 36 * 4 + kThreadsDecode / 32 * kWarpScratch + prefix;
+}
+
+cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
+  switch (L.fmt) {
+    case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, smem, n);
+    case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, smem, n);
+    case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, smem, n);
+    default: return occupancy_decode_fp8(L.ngv, smem, n);
+  }
+}
+
+struct DecodeGeom {
+  int smem, nst, stage_bytes, num_ctas;
+  size_t ws_bytes, off_lse, off_prefix;
+};
+
+kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) {
+  const int sb = stage_bytes_of(L);
+  const int fixed = fixed_smem(batch);
+  int nst = kMaxStages;
+  while (nst > 2 && fixed + (kThreadsDecode / 32) * nst * sb > kSmemPerCtaTarget) --nst;
+  const int smem = fixed + (kThreadsDecode / 32) * nst * sb;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (occupancy(L, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (per_sm < 1) return KVQ_ERR_UNSUPPORTED;
+  G->smem = smem;
+  G->nst = nst;
+  G->stage_bytes = sb;
+  G->num_ctas = sms * per_sm;
+  const size_t slots = (size_t)G->num_ctas + (size_t)batch * L.H;
+  const size_t o_bytes = slots * g * kHeadDim * sizeof(float);
+  const size_t l_bytes = slots * g * sizeof(float);
+  G->off_lse = (o_bytes + 255) / 256 * 256;
+  G->off_prefix = G->off_lse + (l_bytes + 255) / 256 * 256;
+  G->ws_bytes = G->off_prefix + (size_t)(batch + 1) * sizeof(int);
+  return KVQ_OK;
+}
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+kvq_status kvq_cache_layout(const kvq_layer_config* cfg, int32_t num_seqs, size_t bytes[KVQ_FIELD_COUNT]) {
+  LayerDesc L;
+  kvq_status st = make_desc(cfg, &L);
+  if (st != KVQ_OK) return st;
+  if (num_seqs < 0 || !bytes) return KVQ_ERR_INVALID_ARG;
+  for (int i = 0; i < KVQ_FIELD_COUNT; ++i) bytes[i] = 0;
+  const size_t pairs = (size_t)num_seqs * L.H;
+  if (L.paged) {
+    bytes[KVQ_FIELD_BLOCK_POOL] = (size_t)L.num_blocks * L.block_bytes;
+  } else {
+    bytes[KVQ_FIELD_K_CODES] = pairs * L.cap * L.rb;
+    bytes[KVQ_FIELD_V_CODES] = pairs * L.cap * L.rb;
+    if (!L.fp8) {
+      bytes[KVQ_FIELD_K_SCALE] = pairs * (L.cap / L.G) * L.d * sizeof(float);
+      bytes[KVQ_FIELD_K_ZERO] = bytes[KVQ_FIELD_K_SCALE];
+      bytes[KVQ_FIELD_V_SCALE] = pairs * L.cap * L.ngv * sizeof(float);
+      bytes[KVQ_FIELD_V_ZERO] = bytes[KVQ_FIELD_V_SCALE];
+    }
+  }
+  if (!L.fp8) {
+    bytes[KVQ_FIELD_RESID_K] = pairs * L.W * L.d * 2;
+    bytes[KVQ_FIELD_RESID_V] = bytes[KVQ_FIELD_RESID_K];
+  }
+  bytes[KVQ_FIELD_SINK_K] = pairs * L.S * L.d * 2;
+  bytes[KVQ_FIELD_SINK_V] = bytes[KVQ_FIELD_SINK_K];
+  return KVQ_OK;
+}
+
+kvq_status kvq_fp8_calibrate(const void* x, size_t n, float* scale_out, void* stream) {
+  if (!scale_out || (n > 0 && !x)) return KVQ_ERR_INVALID_ARG;
+  if (launch_fp8_calibrate(x, n, scale_out, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_append(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* k_new,
+                               const void* v_new, int32_t n_new, const int32_t* seq_lens, int32_t batch,
+                               uint32_t* dev_status, void* stream) {
+  LayerDesc L;
+  kvq_status st = make_desc(cfg, &L);
+  if (st != KVQ_OK) return st;
+  if ((st = check_cache(L, cache)) != KVQ_OK) return st;
+  if (batch < 0 || batch > kMaxBatch || n_new < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0 || n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !seq_lens) return KVQ_ERR_INVALID_ARG;
+  AppendParams p;
+  p.L = L;
+  p.C = make_ptrs(cache);
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.n_new = n_new;
+  p.batch = batch;
+  p.seq_lens = seq_lens;
+  p.status = dev_status;
+  if (launch_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_workspace_size(const kvq_layer_config* cfg, int32_t batch, int32_t num_q_heads,
+                                     size_t* bytes) {
+  LayerDesc L;
+  kvq_status st = make_desc(cfg, &L);
+  if (st != KVQ_OK) return st;
+  if (!bytes || batch < 0 || batch > kMaxBatch || num_q_heads < L.H || num_q_heads % L.H != 0 ||
+      num_q_heads / L.H > kMaxGqa)
+    return KVQ_ERR_INVALID_ARG;
+  DecodeGeom G;
+  if ((st = decode_geometry(L, batch, num_q_heads / L.H, &G)) != KVQ_OK) return st;
+  *bytes = G.ws_bytes;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
+                                void* out, int32_t out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, void* stream) {
+  LayerDesc L;
+  kvq_status st = make_desc(cfg, &L);
+  if (st != KVQ_OK) return st;
+  if ((st = check_cache(L, cache)) != KVQ_OK) return st;
+  if (batch < 0 || batch > kMaxBatch || num_q_heads < L.H || num_q_heads % L.H != 0 ||
+      num_q_heads / L.H > kMaxGqa || (out_bf16 != 0 && out_bf16 != 1))
+    return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (!q || !seq_lens || !out || !workspace || !aligned16(workspace) || !(softmax_scale == softmax_scale))
+    return KVQ_ERR_INVALID_ARG;
+  const int g = num_q_heads / L.H;
+  DecodeGeom G;
+  if ((st = decode_geometry(L, batch, g, &G)) != KVQ_OK) return st;
+  if (workspace_bytes < G.ws_bytes) return KVQ_ERR_WORKSPACE;
+  DecodeParams p;
+  p.L = L;
+  p.C = make_ptrs(cache);
+  p.q = q;
+  p.Hq = num_q_heads;
+  p.g = g;
+  p.batch = batch;
+  p.seq_lens = seq_lens;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.num_ctas = G.num_ctas;
+  p.nst = G.nst;
+  p.stage_bytes = G.stage_bytes;
+  // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
+  const int qbytes = 2 * 16 * L.rb + (L.fp8 ? 0 : 128 * L.ngv);
+  p.bf_weight = std::max(1, (8192 + qbytes / 2) / qbytes);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_o = reinterpret_cast<float*>(ws);
+  p.ws_lse = reinterpret_cast<float*>(ws + G.off_lse);
+  p.ws_prefix = reinterpret_cast<int*>(ws + G.off_prefix);
+  p.status = dev_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (L.fmt) {
+    case KVQ_FMT_INT2: e = launch_decode_int2(p, G.smem, s); break;
+    case KVQ_FMT_INT4: e = launch_decode_int4(p, G.smem, s); break;
+    case KVQ_FMT_INT8: e = launch_decode_int8(p, G.smem, s); break;
+    default: e = launch_decode_fp8(p, G.smem, s); break;
+  }
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  CombineParams c;
+  c.H = L.H;
+  c.g = g;
+  c.Hq = num_q_heads;
+  c.batch = batch;
+  c.num_ctas = G.num_ctas;
+  c.ws_prefix = p.ws_prefix;
+  c.ws_o = p.ws_o;
+  c.ws_lse = p.ws_lse;
+  c.out = out;
+  c.out_bf16 = out_bf16;
+  c.lse = lse;
+  if (launch_combine(c, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const int32_t* seq_lens,
+                          int32_t batch, int32_t max_tokens, float* k_out, float* v_out, uint32_t* dev_status,
+                          void* stream) {
+  LayerDesc L;
+  kvq_status st = make_desc(cfg, &L);
+  if (st != KVQ_OK) return st;
+  if ((st = check_cache(L, cache)) != KVQ_OK) return st;
+  if (batch < 0 || batch > kMaxBatch || max_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0 || max_tokens == 0) return KVQ_OK;
+  if (!seq_lens || !k_out || !v_out) return KVQ_ERR_INVALID_ARG;
+  if ((max_tokens + 15) / 16 > 65535) return KVQ_ERR_UNSUPPORTED;
+  DequantParams p;
+  p.L = L;
+  p.C = make_ptrs(cache);
+  p.seq_lens = seq_lens;
+  p.batch = batch;
+  p.max_tokens = max_tokens;
+  p.k_out = k_out;
+  p.v_out = v_out;
+  p.status = dev_status;
+  if (launch_dequantize(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG: an argument is outside its documented range";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED: valid but unsupported combination";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE: workspace smaller than kvq_decode_workspace_size()";
+    default: return "unknown kvq_status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,256 @@
+// Device helpers shared by the libkvq kernels (sm_103a): inline PTX for the
+// tensor-core MMA, bulk asynchronous copies (TMA engine), mbarriers, packed
+// f16/bf16 conversions, and the layout arithmetic of the cache.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// --------------------------------------------------------------------------
+// small PTX wrappers
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// d = (a & b) | c
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// packed f16 fused multiply-add, one rounding
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// two E4M3FN bytes (low byte -> low half) to two f16 values, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t lo16) {
+  uint32_t d;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(d) : "r"(lo16));
+  return d;
+}
+
+// f32 pair -> packed f16 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
+  __half2 h = *reinterpret_cast<__half2*>(&v);
+  return __half22float2(h);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+  float2 r;
+  r.x = __uint_as_float(v << 16);
+  r.y = __uint_as_float(v & 0xFFFF0000u);
+  return r;
+}
+
+// split two f32 values into hi + lo 16-bit pairs (hi = rn(x), lo = rn(x - hi))
+__device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_f16(x0, x1);
+  float2 h = unpack_f16(hi);
+  lo = pack_f16(x0 - h.x, x1 - h.y);
+}
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  float2 h = unpack_bf16(hi);
+  lo = pack_bf16(x0 - h.x, x1 - h.y);
+}
+
+// D += A * B, m16n8k16, fp32 accumulate
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// --------------------------------------------------------------------------
+// mbarrier + bulk copy (global -> shared through the TMA engine)
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of the barrier to complete, at most ~`limit` SM cycles.
+// Returns false when the bound ran out (the caller records KVQ_DEV_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// about one second at GB300 clocks
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+__device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// --------------------------------------------------------------------------
+// token accounting of one (sequence, head)
+// --------------------------------------------------------------------------
+struct TokenSplit {
+  int n_sink;  // bf16 sink tokens
+  int qn;      // quantized tokens
+  int r;       // bf16 residual tokens
+};
+
+__host__ __device__ __forceinline__ TokenSplit split_tokens(int T, const LayerDesc& L) {
+  TokenSplit s;
+  s.n_sink = T < L.S ? T : L.S;
+  int n = T - s.n_sink;
+  if (L.fp8) {
+    s.qn = n;
+    s.r = 0;
+  } else {
+    int k = (n - L.R) >= 0 ? (n - L.R) / L.G : 0;
+    s.qn = k * L.G;
+    s.r = n - s.qn;
+  }
+  return s;
+}
+
+// Largest token count one (sequence, head) can hold.
+__host__ __device__ __forceinline__ long long max_tokens(const LayerDesc& L) {
+  long long qcap = L.paged ? (long long)L.mbps * L.P : (long long)L.cap;
+  if (L.fp8) return L.S + qcap;
+  return L.S + qcap + L.R + L.G - 1;
+}
+
+// Addresses of quantized token x of (b, h): codes row, V tile, scale rows.
+struct QuantAddr {
+  const uint8_t* kc;  // K codes row of token x
+  const uint8_t* vt;  // V tile holding x (fragment order)
+  const float* ks;    // K scale row of x's group (INT)
+  const float* kz;
+  const float* vs;  // V scale row of token x (INT)
+  const float* vz;
+  bool ok;
+};
+
+__device__ __forceinline__ QuantAddr quant_addr(const LayerDesc& L, const CachePtrs& C, int b, int h, long long x,
+                                                uint32_t* status) {
+  QuantAddr a;
+  a.ok = true;
+  if (L.paged) {
+    const long long bi = x / L.P;
+    const int row = (int)(x - bi * L.P);
+    const int blk = C.block_table[(long long)b * L.mbps + bi];
+    if (blk < 0 || blk >= L.num_blocks) {
+      report(status, KVQ_DEV_BAD_BLOCK);
+      a.ok = false;
+      a.kc = a.vt = nullptr;
+      a.ks = a.kz = a.vs = a.vz = nullptr;
+      return a;
+    }
+    const uint8_t* slab = reinterpret_cast<const uint8_t*>(C.block_pool) + (long long)blk * L.block_bytes +
+                          (long long)h * L.slab_bytes;
+    a.kc = slab + L.off_kc + (long long)row * L.rb;
+    a.vt = slab + L.off_vc + (long long)(row / 16) * 16 * L.rb;
+    a.ks = reinterpret_cast<const float*>(slab + L.off_ks) + (long long)(row / L.G) * L.d;
+    a.kz = reinterpret_cast<const float*>(slab + L.off_kz) + (long long)(row / L.G) * L.d;
+    a.vs = reinterpret_cast<const float*>(slab + L.off_vs) + (long long)row * L.ngv;
+    a.vz = reinterpret_cast<const float*>(slab + L.off_vz) + (long long)row * L.ngv;
+  } else {
+    const long long pair = (long long)b * L.H + h;
+    a.kc = reinterpret_cast<const uint8_t*>(C.k_codes) + (pair * L.cap + x) * L.rb;
+    a.vt = reinterpret_cast<const uint8_t*>(C.v_codes) + (pair * L.cap + (x / 16) * 16) * L.rb;
+    a.ks = C.k_scale ? C.k_scale + (pair * (L.cap / L.G) + x / L.G) * L.d : nullptr;
+    a.kz = C.k_zero ? C.k_zero + (pair * (L.cap / L.G) + x / L.G) * L.d : nullptr;
+    a.vs = C.v_scale ? C.v_scale + (pair * L.cap + x) * L.ngv : nullptr;
+    a.vz = C.v_zero ? C.v_zero + (pair * L.cap + x) * L.ngv : nullptr;
+  }
+  return a;
+}
+
+// bf16 row of bf16-list token index xb (sink tokens first, then residual tokens in order)
+__device__ __forceinline__ const __nv_bfloat16* bf16_row(const LayerDesc& L, const __nv_bfloat16* sink,
+                                                         const __nv_bfloat16* ring, int b, int h, int xb,
+                                                         const TokenSplit& ts) {
+  const long long pair = (long long)b * L.H + h;
+  if (xb < ts.n_sink) return sink + (pair * L.S + xb) * L.d;
+  const int slot = (ts.qn + (xb - ts.n_sink)) % L.W;
+  return ring + (pair * L.W + slot) * L.d;
+}
+
+// Byte offset (inside a 16-token V tile in fragment order) and bit position of
+// element (token t, channel c).  Matches the decode kernel's operand unpacking.
+__host__ __device__ __forceinline__ void vtile_pos(int bits, bool fp8, int t, int c, int& byte, int& bit) {
+  const int n = c & 7, j = c >> 3, q = (t & 7) >> 1, e = (t & 1) + 2 * (t >> 3);
+  const int lane = 4 * n + q;
+  if (fp8) {
+    byte = lane * 64 + 4 * j + e;
+    bit = 0;
+  } else if (bits == 8) {
+    const int m[4] = {0, 2, 1, 3};
+    byte = lane * 64 + 4 * j + m[e];
+    bit = 0;
+  } else if (bits == 4) {
+    const int m[4] = {0, 16, 4, 20};
+    const int o = m[e] + 8 * (j & 1);
+    byte = lane * 32 + 4 * (j >> 1) + (o >> 3);
+    bit = o & 7;
+  } else {  // 2 bits
+    const int o = 2 * (2 * (j & 3) + (e >> 1)) + 16 * (e & 1);
+    byte = lane * 16 + 4 * (j >> 2) + (o >> 3);
+    bit = o & 7;
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,802 @@
+// Fused decode attention over a quantized KV cache (sm_103a).
+//
+// softmax(q K^T / sqrt(d)) V for one new query per head, reading the compressed
+// cache once ("W4A16 + KV cache quantization combined accuracy", section
+// "오차가 어디서 만나는가"; dequantization fused with the matmuls as "KV Cache
+// Quantization Analysis" section 5 asks, since decode is bound by reading the
+// cache, section 1).
+//
+// Work decomposition.  Every (sequence, kv head) pair is a list of work units:
+// 16-token bf16 tiles (sink + residual window, charged `bf_weight` units) and
+// 16-token quantized tiles (1 unit).  The pairs' lists are concatenated and cut
+// into num_ctas equal ranges, one per CTA (num_ctas = SMs x resident CTAs), so
+// every CTA moves the same number of bytes whatever the sequence lengths.  A
+// CTA writes one partial (normalised output + log-sum-exp) per pair it touches,
+// into slot cta + pair; a second kernel merges the partials of each pair.
+//
+// Inside a CTA each of the 4 warps takes a contiguous sub-range and runs its
+// own pipeline: its lane 0 streams 16-token tiles (codes, scales) into shared
+// memory with bulk asynchronous copies (cp.async.bulk, TMA engine) completing
+// on per-stage mbarriers, several stages ahead of the compute.
+//
+// Tensor-core mapping (mma.sync m16n8k16, fp32 accumulate).  The 16 MMA rows
+// are the g <= 8 query heads of the kv head (row r) and, in rows r + 8, the
+// low-order half of a two-term split of the same operand, so operands that are
+// not exactly representable in 16 bits keep ~22 bits:
+//   QK:  D[head][token] += A[head][channel] * B[channel][token]
+//        A = q_c * s_c (Key scale of the channel, hi/lo split), B = centred Key
+//        codes (exact in f16); the zero-point term sum_c q_c s_c (2^(b-1) - z_c)
+//        is added per group in fp32.  FP8: A = q (exact in f16 after a power-of-
+//        two rescale), B = E4M3 codes (exact in f16).  bf16 tiles: A = q, B = K.
+//   PV:  D[head][channel] += A[head][token] * B[token][channel]
+//        A = p_t * s_t (Value scale of the token, hi/lo split), B = centred Value
+//        codes; zero-point term accumulated per Value group in fp32.
+// The score tile of QK comes out of the MMA in exactly the register layout the
+// PV A operand needs, so probabilities never leave registers.  Values are
+// stored in "fragment order" so that each lane's 32-bit words unpack with one
+// lop3 + one fma.f16x2 into B-operand registers.
+#pragma once
+
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+constexpr int kNW = 4;                 // warps per CTA
+constexpr int kThreads = kNW * 32;
+constexpr int kMaxStages = 4;
+constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 range is safe
+constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
+constexpr float kSTau = 4.f;           // a Value scale may exceed its reference 4x before a rescale
+constexpr int kQStride = 36;           // floats per (head, lane-group) chunk of the query in smem
+constexpr int kBfRow = 272;            // bytes per bf16 row in the warp scratch (256 + 16 pad)
+constexpr int kWarpScratch = 16 * kBfRow;   // 4352 B: bf16 V tile, later the warp's merge record
+constexpr int kMergeStride = 132;      // floats per head in the merge record: m, l, -, -, o[128]
+constexpr unsigned kFull = 0xffffffffu;
+
+__host__ __device__ constexpr uint32_t f16_bits_of_int(int v) {
+  // exact f16 encoding of an integer with |v| < 2048
+  uint32_t s = v < 0 ? 0x8000u : 0u;
+  uint32_t a = (uint32_t)(v < 0 ? -v : v);
+  if (a == 0) return s;
+  int e = 0;
+  while ((a >> (e + 1)) != 0) ++e;
+  return s | ((uint32_t)(e + 15) << 10) | ((a << (10 - e)) & 0x3FFu);
+}
+__host__ __device__ constexpr uint32_t f16_bits_pow2(int k) { return (uint32_t)(k + 15) << 10; }
+__host__ __device__ constexpr uint32_t dup16(uint32_t h) { return h | (h << 16); }
+
+constexpr uint32_t kMagic = 0x64006400u;  // f16 1024.0 in both halves: (1024 | field) = 1024 + field
+
+template <int FMT>
+struct FT {
+  static constexpr bool kFp8 = FMT == 16;
+  static constexpr bool kInt = !kFp8;
+  static constexpr int kBits = kFp8 ? 8 : FMT;
+  static constexpr int kRB = 128 * kBits / 8;   // bytes of one token row of codes
+  static constexpr int kTile = 16 * kRB;        // bytes of 16 rows
+  static constexpr int kKChunk = kRB / 4;       // bytes of a lane's 32 channels in a row
+  static constexpr int kVChunk = kTile / 32;    // bytes of a lane's share of a V tile
+  static constexpr int kHalf = kFp8 ? 0 : (1 << (kBits - 1));
+};
+
+// Channels (relative to the lane's 32-channel window) held in the low / high
+// half of unpacked Key register j.
+template <int FMT>
+__host__ __device__ constexpr int kchan0(int j) {
+  return FMT == 4 ? 8 * (j / 4) + (j % 4)
+       : FMT == 2 ? 16 * (j / 8) + (j % 8)
+       : FMT == 8 ? 4 * (j / 2) + (j % 2)
+                  : 2 * j;  // FP8 and bf16: natural pairs
+}
+template <int FMT>
+__host__ __device__ constexpr int kchan1(int j) {
+  return FMT == 4 ? kchan0<FMT>(j) + 4 : FMT == 2 ? kchan0<FMT>(j) + 8 : FMT == 8 ? kchan0<FMT>(j) + 2
+                                                                                  : kchan0<FMT>(j) + 1;
+}
+
+// --------------------------------------------------------------------------
+// operand unpacking
+// --------------------------------------------------------------------------
+template <int P>  // 2-bit field at bit 2P of each half -> (n - 2)
+__device__ __forceinline__ uint32_t int2_pair(uint32_t w) {
+  constexpr uint32_t mask = (3u << (2 * P)) | (3u << (2 * P + 16));
+  return hfma2(lop3_and_or(w, mask, kMagic), dup16(f16_bits_pow2(-2 * P)),
+               dup16(f16_bits_of_int(-((1024 >> (2 * P)) + 2))));
+}
+__device__ __forceinline__ uint32_t int4_lo(uint32_t w) {  // nibbles at bits 0, 16 -> (n - 8)
+  return hfma2(lop3_and_or(w, 0x000F000Fu, kMagic), dup16(f16_bits_of_int(1)), dup16(f16_bits_of_int(-1032)));
+}
+__device__ __forceinline__ uint32_t int4_hi(uint32_t w) {  // nibbles at bits 4, 20 -> (n - 8)
+  return hfma2(lop3_and_or(w, 0x00F000F0u, kMagic), dup16(f16_bits_pow2(-4)), dup16(f16_bits_of_int(-72)));
+}
+__device__ __forceinline__ uint32_t int8_lo(uint32_t w) {  // bytes 0, 2 -> (n - 128)
+  return hfma2(lop3_and_or(w, 0x00FF00FFu, kMagic), dup16(f16_bits_of_int(1)), dup16(f16_bits_of_int(-1152)));
+}
+
+// Key row: the lane's 32 channels -> 16 packed f16 pairs (channels kchan0/1(j)).
+template <int FMT>
+__device__ __forceinline__ void unpack_k(const uint8_t* p, uint32_t (&R)[16]) {
+  if constexpr (FMT == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t s = w[i] >> 8;
+      R[4 * i + 0] = int4_lo(w[i]);
+      R[4 * i + 1] = int4_hi(w[i]);
+      R[4 * i + 2] = int4_lo(s);
+      R[4 * i + 3] = int4_hi(s);
+    }
+  } else if constexpr (FMT == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t s = w[i] >> 8;
+      R[8 * i + 0] = int2_pair<0>(w[i]);
+      R[8 * i + 1] = int2_pair<1>(w[i]);
+      R[8 * i + 2] = int2_pair<2>(w[i]);
+      R[8 * i + 3] = int2_pair<3>(w[i]);
+      R[8 * i + 4] = int2_pair<0>(s);
+      R[8 * i + 5] = int2_pair<1>(s);
+      R[8 * i + 6] = int2_pair<2>(s);
+      R[8 * i + 7] = int2_pair<3>(s);
+    }
+  } else if constexpr (FMT == 8) {
+    const uint4 v0 = *reinterpret_cast<const uint4*>(p);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(p + 16);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      R[2 * i + 0] = int8_lo(w[i]);
+      R[2 * i + 1] = int8_lo(w[i] >> 8);
+    }
+  } else {  // FP8 E4M3
+    const uint4 v0 = *reinterpret_cast<const uint4*>(p);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(p + 16);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      R[2 * i + 0] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+      R[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+    }
+  }
+}
+
+// Value tile: B-operand registers of n-tile jt from the lane's words W.
+template <int FMT, int JT, int NWORDS>
+__device__ __forceinline__ void unpack_v(const uint32_t (&W)[NWORDS], uint32_t& b01, uint32_t& b23) {
+  if constexpr (FMT == 4) {
+    const uint32_t src = (JT & 1) ? (W[JT / 2] >> 8) : W[JT / 2];
+    b01 = int4_lo(src);
+    b23 = int4_hi(src);
+  } else if constexpr (FMT == 2) {
+    constexpr int a = JT & 3;
+    constexpr int p0 = 2 * a, p1 = 2 * a + 1;
+    const uint32_t w = W[JT / 4];
+    const uint32_t s = w >> 8;
+    b01 = int2_pair<(p0 & 3)>(p0 < 4 ? w : s);
+    b23 = int2_pair<(p1 & 3)>(p1 < 4 ? w : s);
+  } else if constexpr (FMT == 8) {
+    b01 = int8_lo(W[JT]);
+    b23 = int8_lo(W[JT] >> 8);
+  } else {
+    b01 = e4m3x2_to_f16x2(W[JT] & 0xFFFFu);
+    b23 = e4m3x2_to_f16x2(W[JT] >> 16);
+  }
+}
+
+// --------------------------------------------------------------------------
+// per-warp online-softmax state (thread (r, q) holds head r)
+// --------------------------------------------------------------------------
+template <int NGV>
+struct WarpState {
+  float o[16][4];    // PV accumulators: rows r (hi) in [0..1], rows r+8 (lo) in [2..3]
+  float zacc[NGV];   // zero-point terms per Value group (thread-partial)
+  float m;           // reference max (log2 domain)
+  float l;           // sum of p (thread-partial)
+  float S;           // reference Value scale
+};
+
+template <int NGV>
+__device__ __forceinline__ void state_init(WarpState<NGV>& st) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < NGV; ++j) st.zacc[j] = 0.f;
+  st.m = -INFINITY;
+  st.l = 0.f;
+  st.S = 0.f;
+}
+
+// Update the running max / scale references for a tile with scores sig[4]
+// (tokens 2q, 2q+1, 8+2q, 9+2q of head r; -inf when masked) and the lane's
+// largest Value scale smax; return p[4] * kPrescale and 1 / S.  A token's PV
+// weight is then (s_t / S) * (p_t * kPrescale) <= 4 * 2^6 * 64 = 2^14.
+template <int NGV>
+__device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&sig)[4], float smax, float (&pr)[4]) {
+  float tmax = fmaxf(fmaxf(sig[0], sig[1]), fmaxf(sig[2], sig[3]));
+  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
+  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
+  smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
+  smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 2));
+  const bool bump_m = tmax > st.m + kTau;
+  const bool bump_s = smax > st.S * kSTau;
+  if (__any_sync(kFull, bump_m || bump_s)) {
+    const float m_new = bump_m ? tmax : st.m;
+    const float S_new = bump_s ? smax : st.S;
+    const float a = (st.m == -INFINITY) ? 0.f : exp2f(st.m - m_new);
+    const float ao = (S_new > 0.f) ? a * (st.S / S_new) : 0.f;
+    st.l *= a;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.o[j][e] *= ao;
+#pragma unroll
+    for (int j = 0; j < NGV; ++j) st.zacc[j] *= ao;
+    st.m = m_new;
+    st.S = S_new;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) pr[e] = (sig[e] == -INFINITY) ? 0.f : exp2f(sig[e] - st.m);
+  st.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) pr[e] *= kPrescale;
+  return 1.f / st.S;
+}
+
+// --------------------------------------------------------------------------
+// A operands built from the query
+// --------------------------------------------------------------------------
+// INT: A = q_c * s_c (this group's Key scales) split hi/lo, plus the group's
+// zero-point term and the score multiplier.  qv: the lane's 32 query values of
+// head r; ks/kz: this group's Key scale / zero row (smem, 128 floats).
+template <int FMT>
+__device__ __forceinline__ void build_a_int(const float* qrow, const float* ks, const float* kz, int q,
+                                            float scale_log2, uint32_t (&A)[8][4], float& kfac, float& cterm) {
+  float qv[32], sv[32], zv[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 q4 = *reinterpret_cast<const float4*>(qrow + 4 * i);
+    qv[4 * i + 0] = q4.x; qv[4 * i + 1] = q4.y; qv[4 * i + 2] = q4.z; qv[4 * i + 3] = q4.w;
+    const float4 s4 = *reinterpret_cast<const float4*>(ks + 32 * q + 4 * i);
+    const float4 z4 = *reinterpret_cast<const float4*>(kz + 32 * q + 4 * i);
+    sv[4 * i + 0] = s4.x; sv[4 * i + 1] = s4.y; sv[4 * i + 2] = s4.z; sv[4 * i + 3] = s4.w;
+    zv[4 * i + 0] = z4.x; zv[4 * i + 1] = z4.y; zv[4 * i + 2] = z4.z; zv[4 * i + 3] = z4.w;
+  }
+  constexpr float kH = (float)FT<FMT>::kHalf;
+  float x[32];
+  float mx = 0.f, cz = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int c0 = kchan0<FMT>(j), c1 = kchan1<FMT>(j);
+    const float x0 = qv[c0] * sv[c0];
+    const float x1 = qv[c1] * sv[c1];
+    x[2 * j] = x0;
+    x[2 * j + 1] = x1;
+    mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
+    cz = fmaf(x0, kH - zv[c0], cz);
+    cz = fmaf(x1, kH - zv[c1], cz);
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  cz += __shfl_xor_sync(kFull, cz, 1);
+  cz += __shfl_xor_sync(kFull, cz, 2);
+  const float kappa = mx > 0.f ? 16384.f / mx : 1.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    uint32_t hi, lo;
+    split_f16(x[2 * j] * kappa, x[2 * j + 1] * kappa, hi, lo);
+    if ((j & 1) == 0) {
+      A[j >> 1][0] = hi;
+      A[j >> 1][1] = lo;
+    } else {
+      A[j >> 1][2] = hi;
+      A[j >> 1][3] = lo;
+    }
+  }
+  kfac = scale_log2 / kappa;
+  cterm = scale_log2 * cz;
+}
+
+// --------------------------------------------------------------------------
+// the kernel
+// --------------------------------------------------------------------------
+struct SegInfo {
+  int b, h;
+  TokenSplit ts;
+  int nbf, nq;  // bf16 tiles, quantized tiles
+};
+
+template <int FMT, int NGV>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p) {
+  using F = FT<FMT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const LayerDesc& L = p.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = lane >> 2, q = lane & 3;
+  const int B = p.batch, H = L.H, g = p.g;
+
+  // ---- shared memory carve-up ----
+  uint8_t* stage_base = smem;
+  size_t off = (size_t)kNW * p.nst * p.stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
+  off += kNW * kMaxStages * sizeof(uint64_t);
+  float* q_s = reinterpret_cast<float*>(smem + off);
+  off += 8 * 4 * kQStride * sizeof(float);
+  uint8_t* scratch = smem + off;
+  off += kNW * kWarpScratch;
+  int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
+
+  if (tid == 0) {
+    for (int i = 0; i < kNW * kMaxStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    fence_barrier_init();
+  }
+
+  // ---- per-sequence work units and their prefix (units of all H heads) ----
+  const long long tmax_tok = max_tokens(L);
+  auto seq_tokens = [&](int b) -> int {
+    long long T = p.seq_lens[b];
+    if (T < 0) T = 0;
+    if (T > tmax_tok) T = tmax_tok;
+    return (int)T;
+  };
+  auto seq_units = [&](int b) -> int {
+    const TokenSplit ts = split_tokens(seq_tokens(b), L);
+    const int nbf = (ts.n_sink + ts.r + 15) >> 4;
+    const int nq = (ts.qn + 15) >> 4;
+    return nbf * p.bf_weight + nq;
+  };
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      prefix[b] = local;
+      local += seq_units(b) * H;
+    }
+    // exclusive scan of `local` over the block
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __shared__ int warp_tot[kNW];
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+    const int excl = wbase + incl - local;
+    for (int b = b0; b < b1; ++b) prefix[b] += excl;
+    if (tid == kThreads - 1) prefix[B] = wbase + incl;
+    // lengths beyond the capacity are reported once, by CTA 0
+    if (blockIdx.x == 0) {
+      for (int b = tid; b < B; b += kThreads)
+        if (p.seq_lens[b] > tmax_tok) report(p.status, KVQ_DEV_CAPACITY);
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int b = tid; b <= B; b += kThreads) p.ws_prefix[b] = prefix[b];
+  }
+
+  const long long U = prefix[B];
+  const long long C = p.num_ctas;
+  const long long st = (long long)blockIdx.x * U / C;
+  const long long en = (long long)(blockIdx.x + 1) * U / C;
+
+  const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  const __nv_bfloat16* sink_k = reinterpret_cast<const __nv_bfloat16*>(p.C.sink_k);
+  const __nv_bfloat16* sink_v = reinterpret_cast<const __nv_bfloat16*>(p.C.sink_v);
+  const __nv_bfloat16* ring_k = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_k);
+  const __nv_bfloat16* ring_v = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_v);
+
+  uint8_t* my_stages = stage_base + (size_t)warp * p.nst * p.stage_bytes;
+  uint64_t* my_bars = bars + warp * kMaxStages;
+  uint8_t* my_scratch = scratch + warp * kWarpScratch;
+  uint32_t phase_bits = 0;  // expected parity of each of this warp's stage barriers
+
+  // stage sub-buffer offsets
+  const int o_vc = F::kTile;
+  const int o_vs = 2 * F::kTile;
+  const int o_vz = o_vs + 64 * NGV;
+  const int o_ks = o_vz + 64 * NGV;
+  const int o_kz = o_ks + 512;
+
+  long long pos = st;
+  while (pos < en) {
+    // ---- locate the pair holding unit `pos` ----
+    int lo = 0, hi = B;  // largest b with prefix[b] <= pos
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= pos) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int units = (prefix[b + 1] - prefix[b]) / H;
+    const int h = (int)((pos - prefix[b]) / units);
+    const long long pair_start = prefix[b] + (long long)h * units;
+    const long long seg_end = min(en, pair_start + units);
+    const int ua = (int)(pos - pair_start), ue = (int)(seg_end - pair_start);
+
+    SegInfo sg;
+    sg.b = b;
+    sg.h = h;
+    sg.ts = split_tokens(seq_tokens(b), L);
+    sg.nbf = (sg.ts.n_sink + sg.ts.r + 15) >> 4;
+    sg.nq = (sg.ts.qn + 15) >> 4;
+    const int nbf_tok = sg.ts.n_sink + sg.ts.r;
+    const int wbf = p.bf_weight;
+
+    // ---- query of the g heads of kv head h -> smem (zero rows for r >= g) ----
+    for (int i = tid; i < 8 * 128; i += kThreads) {
+      const int hr = i >> 7, c = i & 127;
+      float v = 0.f;
+      if (hr < g) v = __bfloat162float(qg[((long long)b * p.Hq + h * g + hr) * 128 + c]);
+      q_s[(hr * 4 + (c >> 5)) * kQStride + (c & 31)] = v;
+    }
+    __syncthreads();
+
+    // ---- this warp's unit range and tiles ----
+    const int wa = ua + (int)((long long)(ue - ua) * warp / kNW);
+    const int we = ua + (int)((long long)(ue - ua) * (warp + 1) / kNW);
+    const int bf_first = (wa + wbf - 1) / wbf;
+    const int bf_last = min(sg.nbf, (we + wbf - 1) / wbf);  // exclusive
+    const int qbase = sg.nbf * wbf;
+    const int q_first = max(0, wa - qbase);
+    const int q_last = min(sg.nq, max(0, we - qbase));     // exclusive
+    const int nq_w = max(0, q_last - q_first);
+
+    // the lane's 32 query values of head r (fixed for the segment)
+    const float* qrow = q_s + (r * 4 + q) * kQStride;
+
+    WarpState<NGV> stt;
+    state_init(stt);
+
+    // ---- producer: issue the copies of quantized tile (q_first + k) into stage s ----
+    uint32_t valid_bits = 0, pending_bits = 0;
+    bool alive = true;
+    auto issue = [&](int k, int s) {
+      const int qi = q_first + k;
+      const long long x0 = (long long)qi * 16;
+      const QuantAddr a = quant_addr(L, p.C, b, h, x0, lane == 0 ? p.status : nullptr);
+      if (!a.ok) {
+        valid_bits &= ~(1u << s);
+        return;
+      }
+      valid_bits |= 1u << s;
+      pending_bits |= 1u << s;
+      if (lane == 0) {
+        uint8_t* dst = my_stages + (size_t)s * p.stage_bytes;
+        const uint32_t bar = smem_addr(&my_bars[s]);
+        const bool need_ks = F::kInt && (k == 0 || ((x0 % L.G) == 0));
+        uint32_t bytes = 2 * F::kTile;
+        if constexpr (F::kInt) bytes += 128 * NGV + (need_ks ? 1024 : 0);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_copy_g2s(smem_addr(dst), a.kc, F::kTile, bar);
+        bulk_copy_g2s(smem_addr(dst + o_vc), a.vt, F::kTile, bar);
+        if constexpr (F::kInt) {
+          bulk_copy_g2s(smem_addr(dst + o_vs), a.vs, 64 * NGV, bar);
+          bulk_copy_g2s(smem_addr(dst + o_vz), a.vz, 64 * NGV, bar);
+          if (need_ks) {
+            bulk_copy_g2s(smem_addr(dst + o_ks), a.ks, 512, bar);
+            bulk_copy_g2s(smem_addr(dst + o_kz), a.kz, 512, bar);
+          }
+        }
+      }
+    };
+    for (int k = 0; k < min(nq_w, p.nst); ++k) issue(k, k);
+
+    // =========================== bf16 tiles ===============================
+    for (int bt = bf_first; bt < bf_last; ++bt) {
+      // QK: B = K rows (bf16, natural channel pairs), A = q (bf16, exact)
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int xb = bt * 16 + nt * 8 + r;
+        uint32_t R[16];
+        if (xb < nbf_tok) {
+          const __nv_bfloat16* row = bf16_row(L, sink_k, ring_k, b, h, xb, sg.ts) + 32 * q;
+          const uint4* r4 = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = r4[i];
+            R[4 * i] = v.x; R[4 * i + 1] = v.y; R[4 * i + 2] = v.z; R[4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) R[i] = 0u;
+        }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s);
+          const uint32_t a0 = pack_bf16(qq.x, qq.y);
+          const uint32_t a2 = pack_bf16(qq.z, qq.w);
+          mma_bf16(acc[nt], a0, 0u, a2, 0u, R[2 * s], R[2 * s + 1]);
+        }
+      }
+      // V rows -> warp scratch (zeros past the end), then transposed loads
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int id = lane + 32 * k;
+        const int row = id >> 4, col = id & 15;
+        const int xb = bt * 16 + row;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (xb < nbf_tok) v = reinterpret_cast<const uint4*>(bf16_row(L, sink_v, ring_v, b, h, xb, sg.ts))[col];
+        *reinterpret_cast<uint4*>(my_scratch + row * kBfRow + col * 16) = v;
+      }
+      __syncwarp();
+      float sig[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = bt * 16 + (e >> 1) * 8 + 2 * q + (e & 1);
+        sig[e] = (t < nbf_tok) ? acc[e >> 1][e & 1] * p.scale_log2 : -INFINITY;
+      }
+      float pr[4];
+      const float inv_s = softmax_step(stt, sig, 1.f, pr);
+      uint32_t ah0, al0, ah1, al1;
+      split_bf16(pr[0] * inv_s, pr[1] * inv_s, ah0, al0);
+      split_bf16(pr[2] * inv_s, pr[3] * inv_s, ah1, al1);
+      const uint32_t sbase = smem_addr(my_scratch);
+#pragma unroll
+      for (int jp = 0; jp < 8; ++jp) {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = 8 * (mi & 1) + rr;
+        const uint32_t addr = sbase + tok * kBfRow + (2 * jp + (mi >> 1)) * 16;
+        uint32_t v0, v1, v2, v3;
+        ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+        mma_bf16(stt.o[2 * jp], ah0, al0, ah1, al1, v0, v1);
+        mma_bf16(stt.o[2 * jp + 1], ah0, al0, ah1, al1, v2, v3);
+      }
+      __syncwarp();
+    }
+
+    // ========================= quantized tiles ============================
+    uint32_t A[8][4];
+    float kfac = 0.f, cterm = 0.f;
+    if constexpr (F::kFp8) {
+      // A = q * 2^E (exact in f16), E from the head's largest |q|
+      float mx = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(qrow[i]));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      int ex = 0;
+      if (mx > 0.f) (void)frexpf(mx, &ex);        // mx in [2^(ex-1), 2^ex)
+      const float sc = mx > 0.f ? ldexpf(1.f, 15 - ex) : 1.f;  // max |q| * sc in [2^14, 2^15)
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s);
+        A[s][0] = pack_f16(qq.x * sc, qq.y * sc);
+        A[s][1] = 0u;
+        A[s][2] = pack_f16(qq.z * sc, qq.w * sc);
+        A[s][3] = 0u;
+      }
+      kfac = p.scale_log2 * __ldg(p.C.k_tscale) / sc;
+    }
+    const float s_v8 = F::kFp8 ? __ldg(p.C.v_tscale) : 1.f;
+
+    for (int k = 0; k < nq_w; ++k) {
+      const int s = k % p.nst;
+      const int qi = q_first + k;
+      if ((valid_bits >> s) & 1u) {
+        bool ok = alive && mbar_wait_bounded(smem_addr(&my_bars[s]), (phase_bits >> s) & 1u, kWaitLimitCycles);
+        ok = __all_sync(kFull, ok);
+        if (ok) {
+          phase_bits ^= 1u << s;
+          pending_bits &= ~(1u << s);
+        } else if (alive) {
+          alive = false;
+          if (lane == 0) report(p.status, KVQ_DEV_TIMEOUT);
+        }
+        if (alive) {
+          const uint8_t* stg = my_stages + (size_t)s * p.stage_bytes;
+          if constexpr (F::kInt) {
+            if (k == 0 || (((long long)qi * 16) % L.G) == 0)
+              build_a_int<FMT>(qrow, reinterpret_cast<const float*>(stg + o_ks),
+                               reinterpret_cast<const float*>(stg + o_kz), q, p.scale_log2, A, kfac, cterm);
+          }
+          // ---- QK ----
+          float acc[2][2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[nt][c][e] = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t R[16];
+            unpack_k<FMT>(stg + (nt * 8 + r) * F::kRB + q * F::kKChunk, R);
+#pragma unroll
+            for (int s2 = 0; s2 < 8; ++s2)
+              mma_f16(acc[nt][s2 & 1], A[s2][0], A[s2][1], A[s2][2], A[s2][3], R[2 * s2], R[2 * s2 + 1]);
+          }
+          const int tok_valid = min(16, sg.ts.qn - qi * 16);  // < 16 only for a partial FP8 tile
+          float sig[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int nt = e >> 1, c = e & 1;
+            const float dot = (acc[nt][0][c] + acc[nt][1][c]) + (acc[nt][0][c + 2] + acc[nt][1][c + 2]);
+            const int t = nt * 8 + 2 * q + c;
+            sig[e] = (t < tok_valid) ? fmaf(dot, kfac, cterm) : -INFINITY;
+          }
+          // ---- Value scales of the lane's 4 tokens ----
+          float vs[4][NGV], vz[4][NGV];
+          float smax = s_v8;
+          if constexpr (F::kInt) {
+            const float* vsp = reinterpret_cast<const float*>(stg + o_vs);
+            const float* vzp = reinterpret_cast<const float*>(stg + o_vz);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = (e >> 1) * 8 + 2 * q + (e & 1);
+#pragma unroll
+              for (int j = 0; j < NGV; ++j) {
+                vs[e][j] = vsp[t * NGV + j];
+                vz[e][j] = vzp[t * NGV + j];
+                smax = fmaxf(smax, vs[e][j]);
+              }
+            }
+          }
+          float pr[4];
+          const float inv_s = softmax_step(stt, sig, smax, pr);
+          // ---- PV ----
+          uint32_t W[F::kVChunk / 4];
+          {
+            const uint4* vp = reinterpret_cast<const uint4*>(stg + o_vc + lane * F::kVChunk);
+#pragma unroll
+            for (int i = 0; i < F::kVChunk / 16; ++i) {
+              const uint4 v = vp[i];
+              W[4 * i] = v.x; W[4 * i + 1] = v.y; W[4 * i + 2] = v.z; W[4 * i + 3] = v.w;
+            }
+          }
+          if (tok_valid < 16) {
+            // partial tile: tokens past the end may hold stale bytes -> zero the lane's invalid tokens
+            // (lane's tokens: e -> 2q + (e&1) + 8(e>>1); byte/bit positions from the fragment order)
+            const bool v0 = 2 * q < tok_valid, v1 = 2 * q + 1 < tok_valid;
+            const bool v2 = 8 + 2 * q < tok_valid, v3 = 9 + 2 * q < tok_valid;
+            if constexpr (F::kFp8 || FMT == 8) {
+              // byte e of word jt (FP8) or byte {0,2,1,3}[e] (INT8)
+              uint32_t mk = 0;
+              if (F::kFp8) mk = (v0 ? 0xFFu : 0u) | (v1 ? 0xFF00u : 0u) | (v2 ? 0xFF0000u : 0u) | (v3 ? 0xFF000000u : 0u);
+              else mk = (v0 ? 0xFFu : 0u) | (v1 ? 0xFF0000u : 0u) | (v2 ? 0xFF00u : 0u) | (v3 ? 0xFF000000u : 0u);
+#pragma unroll
+              for (int i = 0; i < F::kVChunk / 4; ++i) W[i] &= mk;
+            }
+          }
+          if constexpr (F::kFp8) {
+            uint32_t ah0, al0, ah1, al1;
+            const float f = s_v8 * inv_s;
+            split_f16(pr[0] * f, pr[1] * f, ah0, al0);
+            split_f16(pr[2] * f, pr[3] * f, ah1, al1);
+#pragma unroll
+            for (int jt = 0; jt < 16; ++jt) {
+              uint32_t b01, b23;
+              switch (jt) {
+#define KVQ_V(J) case J: unpack_v<FMT, J>(W, b01, b23); break;
+                KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
+                KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
+              }
+              mma_f16(stt.o[jt], ah0, al0, ah1, al1, b01, b23);
+            }
+          } else {
+            constexpr int kTilesPerGroup = 16 / NGV;  // n-tiles of 8 channels per Value group
+            constexpr float kH = (float)F::kHalf;
+#pragma unroll
+            for (int j = 0; j < NGV; ++j) {
+              float w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                w[e] = (vs[e][j] * inv_s) * pr[e];
+                stt.zacc[j] = fmaf(w[e], kH - vz[e][j], stt.zacc[j]);
+              }
+              uint32_t ah0, al0, ah1, al1;
+              split_f16(w[0], w[1], ah0, al0);
+              split_f16(w[2], w[3], ah1, al1);
+#pragma unroll
+              for (int jj = 0; jj < kTilesPerGroup; ++jj) {
+                uint32_t b01, b23;
+                switch (j * kTilesPerGroup + jj) {
+                  KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
+                  KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
+#undef KVQ_V
+                }
+                mma_f16(stt.o[j * kTilesPerGroup + jj], ah0, al0, ah1, al1, b01, b23);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (alive && k + p.nst < nq_w) issue(k + p.nst, s);
+    }
+    // drain copies still in flight after a timeout (bounded)
+    if (pending_bits) {
+      for (int s = 0; s < p.nst; ++s)
+        if ((pending_bits >> s) & 1u) {
+          mbar_wait_bounded(smem_addr(&my_bars[s]), (phase_bits >> s) & 1u, kWaitLimitCycles);
+          phase_bits ^= 1u << s;
+        }
+      pending_bits = 0;
+    }
+
+    // ---- finalise the warp's state and publish it ----
+    float l = stt.l;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    float zs[NGV];
+#pragma unroll
+    for (int j = 0; j < NGV; ++j) {
+      float z = stt.zacc[j];
+      z += __shfl_xor_sync(kFull, z, 1);
+      z += __shfl_xor_sync(kFull, z, 2);
+      zs[j] = z;
+    }
+    __syncwarp();
+    float* rec = reinterpret_cast<float*>(my_scratch);
+    if (r < g) {
+      const float unit = stt.S / kPrescale;
+      float* rr = rec + r * kMergeStride;
+      if (q == 0) {
+        rr[0] = stt.m;
+        rr[1] = l;
+      }
+#pragma unroll
+      for (int jt = 0; jt < 16; ++jt) {
+        const float z = F::kInt ? zs[jt / (16 / NGV)] : 0.f;
+        float2 v;
+        v.x = (stt.o[jt][0] + stt.o[jt][2] + z) * unit;
+        v.y = (stt.o[jt][1] + stt.o[jt][3] + z) * unit;
+        if (stt.m == -INFINITY) v.x = v.y = 0.f;
+        *reinterpret_cast<float2*>(rr + 4 + jt * 8 + 2 * q) = v;
+      }
+    }
+    __syncthreads();
+    // ---- merge the warps, write the partial of (b, h) ----
+    {
+      const long long slot = (long long)blockIdx.x + (long long)b * H + h;
+      const float* recs = reinterpret_cast<const float*>(scratch);
+      for (int i = tid; i < g * 128; i += kThreads) {
+        const int hr = i >> 7, c = i & 127;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) M = fmaxf(M, recs[w * (kWarpScratch / 4) + hr * kMergeStride]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kNW; ++w) {
+            const float* rw = recs + w * (kWarpScratch / 4) + hr * kMergeStride;
+            const float f = exp2f(rw[0] - M);  // 0 for an empty warp (m = -inf)
+            Lsum = fmaf(rw[1], f, Lsum);
+            O = fmaf(rw[4 + c], f, O);
+          }
+        }
+        const bool empty = !(Lsum > 0.f);
+        p.ws_o[(slot * g + hr) * 128 + c] = empty ? 0.f : O / Lsum;
+        if (c == 0) p.ws_lse[slot * g + hr] = empty ? -INFINITY : M + log2f(Lsum);
+      }
+    }
+    __syncthreads();
+    pos = seg_end;
+  }
+}
+
+template <int FMT, int NGV>
+cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
+  auto k = decode_kernel<FMT, NGV>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k<<<p.num_ctas, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int FMT, int NGV>
+cudaError_t occupancy_t(int smem, int* n) {
+  auto k = decode_kernel<FMT, NGV>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k, kThreads, smem);
+}
+
+}  // namespace kvq

@@ -1,0 +1,27 @@
+// Decode-attention instantiations for the 2-bit affine format, one per
+// number of Value groups per token (d / Gv).
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+cudaError_t launch_decode_int2(const DecodeParams& p, int smem, cudaStream_t s) {
+  switch (p.L.ngv) {
+    case 1: return launch_decode_t<2, 1>(p, smem, s);
+    case 2: return launch_decode_t<2, 2>(p, smem, s);
+    case 4: return launch_decode_t<2, 4>(p, smem, s);
+    case 8: return launch_decode_t<2, 8>(p, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t occupancy_decode_int2(int ngv, int smem, int* n) {
+  switch (ngv) {
+    case 1: return occupancy_t<2, 1>(smem, n);
+    case 2: return occupancy_t<2, 2>(smem, n);
+    case 4: return occupancy_t<2, 4>(smem, n);
+    case 8: return occupancy_t<2, 8>(smem, n);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,78 @@
+// Export of the dequantized cache as fp32 (sm_103a).
+//
+// "KV Cache Quantization Analysis", section 2: x_hat = s (q - z); section 4:
+// an FP8 value times its fp32 scale.  Evaluated as two IEEE fp32 operations
+// (q - z, then times s), or one (s times the exact E4M3 value), so the result
+// is reproducible bit for bit.  Sink and residual tokens are their bf16 values.
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+  const uint32_t h = e4m3x2_to_f16x2((uint32_t)c);
+  return unpack_f16(h).x;
+}
+
+// grid: (batch * H, ceil(max_tokens / 16)); block: 128 threads (one channel each)
+__global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
+  const LayerDesc& L = p.L;
+  const int b = blockIdx.x / L.H, h = blockIdx.x % L.H;
+  const int c = threadIdx.x;
+  const long long pair = (long long)b * L.H + h;
+  long long T = p.seq_lens[b];
+  const long long cap = max_tokens(L) < p.max_tokens ? max_tokens(L) : p.max_tokens;
+  if (T > cap) {
+    if (blockIdx.y == 0 && c == 0) report(p.status, KVQ_DEV_CAPACITY);
+    T = cap;
+  }
+  if (T < 0) T = 0;
+  const TokenSplit ts = split_tokens((int)T, L);
+  const __nv_bfloat16* sink_k = reinterpret_cast<const __nv_bfloat16*>(p.C.sink_k);
+  const __nv_bfloat16* sink_v = reinterpret_cast<const __nv_bfloat16*>(p.C.sink_v);
+  const __nv_bfloat16* ring_k = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_k);
+  const __nv_bfloat16* ring_v = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_v);
+  const int per_byte = 8 / L.bits;
+  const uint32_t cmask = (1u << L.bits) - 1u;
+  for (int tt = 0; tt < 16; ++tt) {
+    const long long t = (long long)blockIdx.y * 16 + tt;
+    if (t >= p.max_tokens) break;
+    float kx = 0.f, vx = 0.f;
+    if (t < ts.n_sink) {
+      kx = __bfloat162float(sink_k[(pair * L.S + t) * L.d + c]);
+      vx = __bfloat162float(sink_v[(pair * L.S + t) * L.d + c]);
+    } else if (t < ts.n_sink + ts.qn) {
+      const long long x = t - L.S;
+      const QuantAddr a = quant_addr(L, p.C, b, h, x, c == 0 ? p.status : nullptr);
+      if (a.ok) {
+        int byte, bit;
+        vtile_pos(L.bits, L.fp8 != 0, (int)(x % 16), c, byte, bit);
+        if (L.fp8) {
+          kx = __fmul_rn(*p.C.k_tscale, e4m3_value(a.kc[c]));
+          vx = __fmul_rn(*p.C.v_tscale, e4m3_value(a.vt[byte]));
+        } else {
+          const uint32_t kcode = (a.kc[c / per_byte] >> ((c % per_byte) * L.bits)) & cmask;
+          const uint32_t vcode = (a.vt[byte] >> bit) & cmask;
+          const int j = c / L.Gv;
+          kx = __fmul_rn(a.ks[c], __fsub_rn((float)kcode, a.kz[c]));
+          vx = __fmul_rn(a.vs[j], __fsub_rn((float)vcode, a.vz[j]));
+        }
+      }
+    } else if (t < T) {
+      const long long slot = (t - L.S) % L.W;
+      kx = __bfloat162float(ring_k[(pair * L.W + slot) * L.d + c]);
+      vx = __bfloat162float(ring_v[(pair * L.W + slot) * L.d + c]);
+    }
+    const long long o = (pair * p.max_tokens + t) * L.d + c;
+    p.k_out[o] = kx;
+    p.v_out[o] = vx;
+  }
+}
+
+cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream) {
+  if (p.batch * p.L.H == 0 || p.max_tokens == 0) return cudaSuccess;
+  dim3 grid(p.batch * p.L.H, (p.max_tokens + 15) / 16);
+  dequant_kernel<<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,108 @@
+// Internal descriptors shared by the host API (kvq_api.cpp) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxGqa = 8;
+constexpr int kMaxBatch = 2048;
+
+// Validated, derived form of kvq_layer_config.
+struct LayerDesc {
+  int H, d, fmt, bits, fp8;
+  int G, Gv, ngv, R, S, W;  // W = R + G ring slots (0 for FP8)
+  int paged, P, cap, num_blocks, mbps;
+  int rb;  // bytes of one token row of codes (d * bits / 8)
+  long long slab_bytes, block_bytes;
+  int off_kc, off_vc, off_ks, off_kz, off_vs, off_vz;  // inside a paged head slab
+};
+
+struct CachePtrs {
+  void* k_codes;
+  void* v_codes;
+  float* k_scale;
+  float* k_zero;
+  float* v_scale;
+  float* v_zero;
+  void* block_pool;
+  const int32_t* block_table;
+  void* resid_k;
+  void* resid_v;
+  void* sink_k;
+  void* sink_v;
+  const float* k_tscale;
+  const float* v_tscale;
+};
+
+struct DecodeParams {
+  LayerDesc L;
+  CachePtrs C;
+  const void* q;  // bf16 [B][Hq][d]
+  int Hq, g, batch;
+  const int32_t* seq_lens;
+  float scale_log2;  // softmax_scale * log2(e)
+  int num_ctas;      // CTAs of the decode grid (partial slot space = num_ctas + batch*H)
+  int nst;           // pipeline stages per warp
+  int stage_bytes;   // bytes of one stage
+  int bf_weight;     // work units charged to a bf16 tile (quantized tiles cost 1)
+  float* ws_o;       // [slots][g][d] normalised partial outputs
+  float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial
+  int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
+  uint32_t* status;
+};
+
+struct CombineParams {
+  int H, g, Hq, batch, num_ctas;
+  const int* ws_prefix;
+  const float* ws_o;
+  const float* ws_lse;
+  void* out;
+  int out_bf16;
+  float* lse;
+};
+
+struct AppendParams {
+  LayerDesc L;
+  CachePtrs C;
+  const void* k_new;  // bf16 [B][H][n_new][d]
+  const void* v_new;
+  int n_new, batch;
+  const int32_t* seq_lens;
+  uint32_t* status;
+};
+
+struct DequantParams {
+  LayerDesc L;
+  CachePtrs C;
+  const int32_t* seq_lens;
+  int batch, max_tokens;
+  float* k_out;
+  float* v_out;
+  uint32_t* status;
+};
+
+// ---- launchers (defined in the .cu files) --------------------------------
+// decode: one kernel instantiation per (format, Value groups per token)
+cudaError_t decode_smem_and_occupancy(const LayerDesc& L, int batch, int* smem_bytes, int* nst, int* stage_bytes,
+                                      int* ctas_per_sm);
+cudaError_t launch_decode(const DecodeParams& p, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_decode_int2(const DecodeParams& p, int smem, cudaStream_t s);
+cudaError_t launch_decode_int4(const DecodeParams& p, int smem, cudaStream_t s);
+cudaError_t launch_decode_int8(const DecodeParams& p, int smem, cudaStream_t s);
+cudaError_t launch_decode_fp8(const DecodeParams& p, int smem, cudaStream_t s);
+cudaError_t occupancy_decode_int2(int ngv, int smem, int* n);
+cudaError_t occupancy_decode_int4(int ngv, int smem, int* n);
+cudaError_t occupancy_decode_int8(int ngv, int smem, int* n);
+cudaError_t occupancy_decode_fp8(int ngv, int smem, int* n);
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_fp8_calibrate(const void* x, size_t n, float* scale_out, cudaStream_t stream);
+cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,277 @@
+"""Test helpers: drive libkvq through its C ABI and read its buffers back.
+
+The physical-layout decoder below restates the layout contract written in
+include/kvq.h (it is test code, independent of the CUDA sources); the oracle
+side is oracle/kvq_oracle.py.  No expected value here comes from the GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+from oracle import kvq_oracle as O
+
+F32 = np.float32
+BITS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8}
+
+
+# --------------------------------------------------------------------------- #
+# layout contract (include/kvq.h), restated for reading buffers back
+# --------------------------------------------------------------------------- #
+
+
+def vtile_positions(fmt: str):
+    """(byte[16,128], bit[16,128]) of element (token, channel) in a 16-token Value tile."""
+    t = np.arange(16)[:, None]
+    c = np.arange(128)[None, :]
+    n, j = c % 8, c // 8
+    q, e = (t % 8) // 2, (t % 2) + 2 * (t // 8)
+    lane = 4 * n + q
+    if fmt == "fp8_e4m3":
+        return lane * 64 + 4 * j + e + 0 * c, np.zeros((16, 128), int)
+    if fmt == "int8":
+        return lane * 64 + 4 * j + np.array([0, 2, 1, 3])[e], np.zeros((16, 128), int)
+    if fmt == "int4":
+        o = np.array([0, 16, 4, 20])[e] + 8 * (j % 2)
+        return lane * 32 + 4 * (j // 2) + o // 8, o % 8
+    o = 2 * (2 * (j % 4) + e // 2) + 16 * (e % 2)
+    return lane * 16 + 4 * (j // 4) + o // 8, o % 8
+
+
+def unpack_k_rows(raw: np.ndarray, fmt: str) -> np.ndarray:
+    """Key code rows [n, rb] bytes -> codes [n, 128] (little-endian packing along d)."""
+    b = BITS[fmt]
+    per = 8 // b
+    raw = raw.astype(np.uint32)
+    out = np.zeros((raw.shape[0], 128), np.uint8)
+    for c in range(128):
+        out[:, c] = (raw[:, c // per] >> ((c % per) * b)) & ((1 << b) - 1)
+    return out
+
+
+def unpack_v_tiles(raw: np.ndarray, fmt: str) -> np.ndarray:
+    """Value tiles [ntiles, 16*rb] bytes -> codes [ntiles*16, 128]."""
+    b = BITS[fmt]
+    byte, bit = vtile_positions(fmt)
+    raw = raw.astype(np.uint32)
+    vals = (raw[:, byte] >> bit[None]) & ((1 << b) - 1)   # [ntiles, 16, 128]
+    return vals.reshape(-1, 128).astype(np.uint8)
+
+
+def bf16_bits(x_f32: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x_f32, dtype=np.float32).view(np.uint32) >> 16
+
+
+# --------------------------------------------------------------------------- #
+# a GPU cache built through kvq_quantize_append
+# --------------------------------------------------------------------------- #
+
+
+class GpuLayer:
+    """One layer's cache on the GPU for B sequences, with its oracle twin."""
+
+    def __init__(self, fmt: str, H: int, lens: Sequence[int], G: int, Gv: int, R: int, S: int, *,
+                 paged: bool = False, block_tokens: int = 16, spare_blocks: int = 3, seed: int = 0,
+                 extra_capacity: int = 0, device="cuda"):
+        import torch
+        from quantized_kv_cache_decode_gb300 import kvq
+        self.torch, self.kvq = torch, kvq
+        self.fmt, self.H, self.lens = fmt, H, list(lens)
+        self.B = len(lens)
+        self.fp8 = fmt == "fp8_e4m3"
+        self.G = 1 if self.fp8 else G
+        self.Gv = 128 if self.fp8 else Gv
+        self.R = 0 if self.fp8 else R
+        self.S = S
+        self.spec = O.Spec(fmt, d=128, G=self.G, Gv=self.Gv, R=self.R, S=S)
+        self.device = device
+        self.paged = paged
+        maxq = max([O.token_split(T + extra_capacity, self.spec)[1] for T in self.lens] + [0])
+        unit = 16 if self.fp8 else max(16, self.G)
+        if paged:
+            self.P = block_tokens if self.fp8 else self.G
+            blocks_per_seq = [math.ceil(O.token_split(T + extra_capacity, self.spec)[1] / self.P) for T in self.lens]
+            self.mbps = max(blocks_per_seq + [1])
+            nblocks = sum(blocks_per_seq) + spare_blocks
+            self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, paged=True, block_tokens=self.P,
+                                       num_blocks=nblocks, max_blocks_per_seq=self.mbps)
+        else:
+            cap = max(unit, math.ceil(maxq / unit) * unit)
+            self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, capacity_tokens=cap)
+        self.layer = kvq.CacheLayer(self.cfg, self.B, device=device)
+        if paged:
+            rng = np.random.default_rng(seed + 77)
+            perm = rng.permutation(nblocks).astype(np.int32)
+            table = np.full((self.B, self.mbps), -1, np.int32)
+            k = 0
+            for b, nb in enumerate(blocks_per_seq):
+                table[b, :nb] = perm[k:k + nb]
+                k += nb
+            self.table_np = table
+            self.layer.block_table.copy_(torch.from_numpy(table))
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    # -- per-sequence view of the cache struct (batch = 1 calls) --
+    def seq_struct(self, b: int):
+        c = self.layer.struct()
+        sz = self.layer.sizes
+        per = {n: sz[n] // self.B for n in sz}
+        for n in ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "resid_k", "resid_v", "sink_k",
+                  "sink_v"):
+            if getattr(c, n):
+                setattr(c, n, getattr(c, n) + b * per[n])
+        if self.paged:
+            c.block_table = c.block_table + b * self.mbps * 4
+        return c
+
+    def calibrate_fp8(self, k_all_bits: np.ndarray, v_all_bits: np.ndarray):
+        torch = self.torch
+        kd = torch.from_numpy(k_all_bits.astype(np.int16)).to(self.device)
+        vd = torch.from_numpy(v_all_bits.astype(np.int16)).to(self.device)
+        self.kvq.fp8_calibrate(kd, kd.numel(), self.layer.k_tensor_scale)
+        self.kvq.fp8_calibrate(vd, vd.numel(), self.layer.v_tensor_scale)
+        torch.cuda.synchronize()
+
+    def append(self, b: int, k_bits: np.ndarray, v_bits: np.ndarray, T_before: int):
+        """Append tokens [n, d] (bf16 bits) to every kv head of sequence b (k_bits: [H, n, d])."""
+        torch = self.torch
+        n = k_bits.shape[1]
+        kd = torch.from_numpy(np.ascontiguousarray(k_bits).astype(np.int16)).to(self.device)
+        vd = torch.from_numpy(np.ascontiguousarray(v_bits).astype(np.int16)).to(self.device)
+        sl = torch.tensor([T_before], dtype=torch.int32, device=self.device)
+        self.kvq.quantize_append(self.cfg, self.seq_struct(b), kd, vd, n, sl, 1, self.status)
+
+    def seq_lens_dev(self, lens=None):
+        return self.torch.tensor(self.lens if lens is None else lens, dtype=self.torch.int32, device=self.device)
+
+    def raw(self, name: str) -> np.ndarray:
+        return self.layer.buf[name].cpu().numpy()
+
+    def status_value(self) -> int:
+        return int(self.status.item())
+
+    def decode(self, q_bits: np.ndarray, out_bf16: bool = False, lens=None, scale=None):
+        torch = self.torch
+        B, Hq, _ = q_bits.shape
+        qd = torch.from_numpy(q_bits.astype(np.int16)).to(self.device)
+        out = torch.zeros((B, Hq, 128), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=self.device)
+        lse = torch.zeros((B, Hq), dtype=torch.float32, device=self.device)
+        wsb = self.kvq.decode_workspace_size(self.cfg, B, Hq)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=self.device)
+        sl = self.seq_lens_dev(lens)
+        sc = 1.0 / math.sqrt(128) if scale is None else scale
+        self.kvq.decode_attention(self.cfg, self.layer.struct(), qd, Hq, sl, B, sc, out, out_bf16, lse, ws, wsb,
+                                  self.status)
+        torch.cuda.synchronize()
+        return out, lse
+
+    def dequantize(self, max_tokens: int, lens=None):
+        torch = self.torch
+        ko = torch.full((self.B, self.H, max_tokens, 128), 7.0, dtype=torch.float32, device=self.device)
+        vo = torch.full_like(ko, 7.0)
+        self.kvq.dequantize(self.cfg, self.layer.struct(), self.seq_lens_dev(lens), self.B, max_tokens, ko, vo,
+                            self.status)
+        torch.cuda.synchronize()
+        return ko.cpu().numpy(), vo.cpu().numpy()
+
+    # -- read the stored cache of (b, h) back into the oracle's logical form --
+    def logical(self, b: int, h: int, T: int) -> Dict[str, np.ndarray]:
+        n_sink, qn, r = O.token_split(T, self.spec)
+        out = {}
+        rb = 128 * BITS[self.fmt] // 8
+        if self.paged:
+            pool = self.raw("block_pool")
+            slab_fields = self._slab_fields()
+            kc, vt, ks, kz, vs, vz = [], [], [], [], [], []
+            for bi in range(math.ceil(qn / self.P)):
+                blk = int(self.table_np[b, bi])
+                base = blk * self.block_bytes + h * self.slab_bytes
+                f = {k: pool[base + o: base + o + n] for k, (o, n) in slab_fields.items()}
+                kc.append(f["kc"].reshape(self.P, rb))
+                vt.append(f["vc"].reshape(self.P // 16, 16 * rb))
+                if not self.fp8:
+                    ks.append(f["ks"].view(F32).reshape(-1, 128))
+                    kz.append(f["kz"].view(F32).reshape(-1, 128))
+                    vs.append(f["vs"].view(F32).reshape(self.P, -1))
+                    vz.append(f["vz"].view(F32).reshape(self.P, -1))
+            kc = np.concatenate(kc)[:qn] if kc else np.zeros((0, rb), np.uint8)
+            vt = np.concatenate(vt) if vt else np.zeros((0, 16 * rb), np.uint8)
+            if not self.fp8:
+                out["k_s"] = np.concatenate(ks)[:qn // self.G] if ks else np.zeros((0, 128), F32)
+                out["k_z"] = np.concatenate(kz)[:qn // self.G] if kz else np.zeros((0, 128), F32)
+                out["v_s"] = np.concatenate(vs)[:qn] if vs else np.zeros((0, 128 // self.Gv), F32)
+                out["v_z"] = np.concatenate(vz)[:qn] if vz else np.zeros((0, 128 // self.Gv), F32)
+        else:
+            cap = self.cfg.capacity_tokens
+            pair = b * self.H + h
+            kc = self.raw("k_codes").reshape(self.B * self.H, cap, rb)[pair, :qn]
+            vt = self.raw("v_codes").reshape(self.B * self.H, cap // 16, 16 * rb)[pair]
+            if not self.fp8:
+                ng = cap // self.G
+                out["k_s"] = self.raw("k_scale").view(F32).reshape(self.B * self.H, ng, 128)[pair, :qn // self.G]
+                out["k_z"] = self.raw("k_zero").view(F32).reshape(self.B * self.H, ng, 128)[pair, :qn // self.G]
+                out["v_s"] = self.raw("v_scale").view(F32).reshape(self.B * self.H, cap, -1)[pair, :qn]
+                out["v_z"] = self.raw("v_zero").view(F32).reshape(self.B * self.H, cap, -1)[pair, :qn]
+        out["k_codes"] = unpack_k_rows(kc, self.fmt)
+        out["v_codes"] = unpack_v_tiles(vt, self.fmt)[:qn] if len(vt) else np.zeros((0, 128), np.uint8)
+        # bf16 parts
+        pair = b * self.H + h
+        if n_sink:
+            sk = self.raw("sink_k").view(np.uint16).reshape(self.B * self.H, self.S, 128)[pair, :n_sink]
+            sv = self.raw("sink_v").view(np.uint16).reshape(self.B * self.H, self.S, 128)[pair, :n_sink]
+            out["sink_k"], out["sink_v"] = sk, sv
+        if not self.fp8:
+            W = self.R + self.G
+            ring_k = self.raw("resid_k").view(np.uint16).reshape(self.B * self.H, W, 128)[pair]
+            ring_v = self.raw("resid_v").view(np.uint16).reshape(self.B * self.H, W, 128)[pair]
+            slots = [(qn + i) % W for i in range(r)]
+            out["resid_k"], out["resid_v"] = ring_k[slots], ring_v[slots]
+        return out
+
+    def _slab_fields(self):
+        rb = 128 * BITS[self.fmt] // 8
+        P = self.P
+        f, o = {}, 0
+        f["kc"] = (o, P * rb); o += P * rb
+        f["vc"] = (o, P * rb); o += P * rb
+        if not self.fp8:
+            ngv = 128 // self.Gv
+            f["ks"] = (o, (P // self.G) * 512); o += (P // self.G) * 512
+            f["kz"] = (o, (P // self.G) * 512); o += (P // self.G) * 512
+            f["vs"] = (o, P * ngv * 4); o += P * ngv * 4
+            f["vz"] = (o, P * ngv * 4); o += P * ngv * 4
+        self.slab_bytes = (o + 15) // 16 * 16
+        self.block_bytes = self.slab_bytes * self.H
+        return f
+
+
+def compare_logical(gpu: Dict[str, np.ndarray], hc: "O.HeadCache"):
+    """Bit-exact comparison of a GPU head cache (logical form) with the oracle's."""
+    assert np.array_equal(gpu["k_codes"], hc.k_codes), "K codes differ"
+    assert np.array_equal(gpu["v_codes"], hc.v_codes), "V codes differ"
+    if hc.k_s is not None:
+        for f in ("k_s", "k_z", "v_s", "v_z"):
+            g, o = gpu[f], getattr(hc, f)
+            assert g.shape == o.shape and np.array_equal(g.view(np.uint32), o.astype(F32).view(np.uint32)), f
+    if len(hc.sink_k):
+        assert np.array_equal(gpu["sink_k"], bf16_bits(hc.sink_k)) and np.array_equal(gpu["sink_v"], bf16_bits(hc.sink_v))
+    if hc.k_s is not None:
+        assert np.array_equal(gpu["resid_k"], bf16_bits(hc.resid_k)), "residual K differs"
+        assert np.array_equal(gpu["resid_v"], bf16_bits(hc.resid_v)), "residual V differs"
+
+
+def check_attention(out_gpu: np.ndarray, lse_gpu: np.ndarray, out_ref: np.ndarray, lse_ref: np.ndarray,
+                    rel: float = 2e-3, lse_tol: float = 1e-4):
+    """The parity bar: max|out - ref| <= rel * max|ref| over the tensor; |lse - ref| <= lse_tol."""
+    finite = np.isfinite(lse_ref)
+    scale = np.max(np.abs(out_ref)) if out_ref.size else 0.0
+    err = np.max(np.abs(out_gpu.astype(np.float64) - out_ref)) if out_ref.size else 0.0
+    assert err <= rel * scale + 1e-30, f"max |out err| {err:.3e} > {rel} * {scale:.3e}"
+    if finite.any():
+        lerr = np.max(np.abs(lse_gpu.astype(np.float64)[finite] - lse_ref[finite]))
+        assert lerr <= lse_tol, f"max |lse err| {lerr:.3e} > {lse_tol}"
+    assert np.all(np.isneginf(lse_gpu[~finite])), "empty sequences must give lse = -inf"
+    return err / scale if scale else 0.0, (np.max(np.abs(lse_gpu[finite] - lse_ref[finite])) if finite.any() else 0.0)

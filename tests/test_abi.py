@@ -1,0 +1,104 @@
+"""The C-ABI library: it loads, exports every entry point include/kvq.h declares,
+and its host-side validation and layout arithmetic work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import quantized_kv_cache_decode_gb300 as pkg
+    pkg.build()
+    from quantized_kv_cache_decode_gb300 import kvq as mod
+    return mod
+
+
+def test_exports_every_declared_symbol(kvq):
+    declared = kvq.declared_symbols()
+    assert set(declared) >= {"kvq_quantize_append", "kvq_decode_attention", "kvq_dequantize",
+                             "kvq_cache_layout", "kvq_decode_workspace_size", "kvq_fp8_calibrate",
+                             "kvq_status_string"}
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(kvq):
+    for code, name in kvq.STATUS.items():
+        assert kvq.status_string(code).startswith(name)
+
+
+def test_cache_layout_sizes(kvq):
+    # Llama-3-70B-shaped INT4 layer, contiguous: codes 0.5 B per element, fp32 s/z per 128-token
+    # K group and per token V group, bf16 ring of R + G tokens
+    cfg = kvq.make_config("int4", 8, 128, 128, 128, 0, capacity_tokens=8064)
+    sz = kvq.cache_layout(cfg, 16)
+    pairs = 16 * 8
+    assert sz["k_codes"] == pairs * 8064 * 64 and sz["v_codes"] == sz["k_codes"]
+    assert sz["k_scale"] == pairs * (8064 // 128) * 128 * 4 == sz["k_zero"]
+    assert sz["v_scale"] == pairs * 8064 * 1 * 4 == sz["v_zero"]
+    assert sz["resid_k"] == pairs * 256 * 128 * 2 and sz["sink_k"] == 0 and sz["block_pool"] == 0
+    # paged INT4, block 16 = G: slab = K codes 1024 + V codes 1024 + K s/z 1024 + V s/z 128 = 3200 B
+    cfg = kvq.make_config("int4", 8, 16, 128, 64, 1, paged=True, block_tokens=16, num_blocks=10,
+                          max_blocks_per_seq=4)
+    sz = kvq.cache_layout(cfg, 2)
+    assert sz["block_pool"] == 10 * 8 * 3200
+    assert sz["sink_k"] == 2 * 8 * 1 * 128 * 2
+    # FP8: 1 B per element, no scales, no ring
+    cfg = kvq.make_config("fp8_e4m3", 8, 1, 128, 0, 0, capacity_tokens=8192)
+    sz = kvq.cache_layout(cfg, 16)
+    assert sz["k_codes"] == 16 * 8 * 8192 * 128 and sz["k_scale"] == 0 and sz["resid_k"] == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt="int4", num_kv_heads=0, G=32, Gv=128, R=0, S=0, capacity_tokens=64), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=24, Gv=128, R=0, S=0, capacity_tokens=48), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=48, R=0, S=0, capacity_tokens=64), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=-1, S=0, capacity_tokens=64), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=40), -1),
+    (dict(fmt="fp8_e4m3", num_kv_heads=2, G=16, Gv=128, R=0, S=0, capacity_tokens=64), -1),
+    (dict(fmt="fp8_e4m3", num_kv_heads=2, G=1, Gv=128, R=8, S=0, capacity_tokens=64), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, paged=True, block_tokens=16, num_blocks=4,
+          max_blocks_per_seq=2), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, head_dim=64), -2),
+])
+def test_config_validation(kvq, kw, status):
+    kw = dict(kw)
+    cfg = kvq.make_config(kw.pop("fmt"), kw.pop("num_kv_heads"), kw.pop("G"), kw.pop("Gv"), kw.pop("R"),
+                          kw.pop("S"), **kw)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.cache_layout(cfg, 1)
+    assert e.value.status == status
+
+
+def test_calls_reject_bad_arguments_before_any_launch(kvq):
+    cfg = kvq.make_config("int4", 2, 32, 128, 32, 0, capacity_tokens=64)
+    cache = kvq.LayerCache()  # all NULL
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.quantize_append(cfg, cache, 0, 0, 1, 0, 1, stream=0)
+    assert e.value.status == -1
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.decode_attention(cfg, cache, 0, 8, 0, 1, 0.1, 0, False, 0, 0, 0, stream=0)
+    assert e.value.status == -1
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.dequantize(cfg, cache, 0, 1, 16, 0, 0, stream=0)
+    assert e.value.status == -1
+
+
+def test_fragment_order_is_a_bijection():
+    # every bit of a 16-token Value tile holds exactly one (token, channel) code
+    import numpy as np
+    import kvq_testlib as TL
+    for fmt, bits in (("int2", 2), ("int4", 4), ("int8", 8), ("fp8_e4m3", 8)):
+        byte, bit = TL.vtile_positions(fmt)
+        tile_bytes = 16 * 128 * bits // 8
+        used = np.zeros(tile_bytes * 8, int)
+        for t in range(16):
+            for c in range(128):
+                for k in range(bits):
+                    used[byte[t, c] * 8 + bit[t, c] + k] += 1
+        assert used.min() == 1 and used.max() == 1, fmt

@@ -1,0 +1,191 @@
+"""GPU parity of libkvq against the CPU oracle, through the C ABI.
+
+Small shapes that still span several 16-token tiles, several CTAs and ragged
+tails, over every format, both layouts, GQA ratios 1..8 and edge lengths.
+  * codes, scales, zero-points, sink and residual window: bit-exact;
+  * kvq_dequantize export: bit-exact;
+  * attention: max|out - ref| <= 2e-3 * max|ref| (fp32 output),
+    |lse - ref| <= 1e-4, bf16 output == round-to-nearest-even of the fp32 output.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+from quantized_kv_cache_decode_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import kvq_testlib as TL  # noqa: E402
+
+
+def make_inputs(seed, H, g, lens, outliers=4, scale=10.0):
+    rng = np.random.default_rng(seed)
+    chans = rng.choice(128, size=outliers, replace=False)
+    mask = np.zeros(128, bool)
+    mask[chans] = True
+    kv = {}
+    for b, T in enumerate(lens):
+        for h in range(H):
+            k = I.random_bf16(seed * 1000 + 2 * (b * H + h), (T, 128), outlier_mask=mask, outlier_scale=scale)
+            v = I.random_bf16(seed * 1000 + 2 * (b * H + h) + 1, (T, 128))
+            kv[b, h] = (k, v)
+    q = I.random_bf16(seed * 7 + 3, (len(lens), H * g, 128))
+    return kv, q
+
+
+def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=None):
+    gl = TL.GpuLayer(fmt, H, lens, G, Gv, R, S, paged=paged, block_tokens=block_tokens, seed=seed)
+    kv, q = make_inputs(seed, H, g, lens)
+    ks = vs = None
+    if gl.fp8:
+        kall = np.concatenate([kv[k][0].reshape(-1) for k in kv] + [np.zeros(0, np.uint16)])
+        vall = np.concatenate([kv[k][1].reshape(-1) for k in kv] + [np.zeros(0, np.uint16)])
+        gl.calibrate_fp8(kall, vall)
+        ks = O.fp8_tensor_scale(O.bf16_to_f32(kall))
+        vs = O.fp8_tensor_scale(O.bf16_to_f32(vall))
+        assert gl.layer.k_tensor_scale.item() == float(ks) and gl.layer.v_tensor_scale.item() == float(vs)
+    for b, T in enumerate(lens):
+        if T == 0:
+            continue
+        kb = np.stack([kv[b, h][0] for h in range(H)])
+        vb = np.stack([kv[b, h][1] for h in range(H)])
+        steps = chunks(T) if chunks else [T]
+        t0 = 0
+        for n in steps:
+            gl.append(b, kb[:, t0:t0 + n], vb[:, t0:t0 + n], t0)
+            t0 += n
+        assert t0 == T
+    torch.cuda.synchronize()
+    caches = [[O.build_head_cache(O.bf16_to_f32(kv[b, h][0]), O.bf16_to_f32(kv[b, h][1]), gl.spec, ks, vs)
+               for h in range(H)] for b in range(len(lens))]
+    return gl, caches, q
+
+
+CASES = [
+    # fmt, H, g, lens, G, Gv, R, S, paged, block
+    ("int4", 2, 4, [512], 32, 128, 32, 0, False, 16),
+    ("int4", 2, 4, [0, 1, 31, 63, 64, 65, 700], 32, 128, 32, 0, False, 16),
+    ("int2", 3, 1, [1000, 129, 160, 161, 5], 32, 32, 128, 0, False, 16),
+    ("int8", 2, 6, [300, 17, 80, 81, 2], 16, 128, 64, 1, False, 16),
+    ("int4", 2, 8, [777, 2000, 1], 128, 64, 128, 2, False, 16),
+    ("int2", 1, 5, [600, 47], 16, 16, 0, 0, False, 16),
+    ("fp8_e4m3", 2, 4, [0, 1, 15, 16, 17, 333], 1, 128, 0, 0, False, 16),
+    ("fp8_e4m3", 2, 3, [100, 257, 3], 1, 128, 0, 1, False, 16),
+    ("int4", 2, 6, [300, 1000, 17, 81], 16, 128, 64, 1, True, 16),
+    ("int8", 3, 2, [250, 96, 97], 16, 32, 64, 1, True, 16),
+    ("int2", 2, 2, [900, 33], 32, 16, 32, 0, True, 32),
+    ("fp8_e4m3", 2, 4, [500, 7, 48], 1, 128, 0, 1, True, 16),
+    ("fp8_e4m3", 1, 8, [400, 31], 1, 128, 0, 0, True, 32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-H{c[1]}g{c[2]}-G{c[4]}Gv{c[5]}R{c[6]}S{c[7]}"
+                                             f"{'-paged' if c[8] else ''}" for c in CASES])
+def test_parity(case):
+    fmt, H, g, lens, G, Gv, R, S, paged, blk = case
+    seed = abs(hash(str(case))) % 10000
+    gl, caches, q = build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=blk)
+    B = len(lens)
+    # stored cache, bit-exact
+    for b, T in enumerate(lens):
+        for h in range(H):
+            TL.compare_logical(gl.logical(b, h, T), caches[b][h])
+    # dequantized export, bit-exact
+    Tmax = max(lens) + 3
+    ko, vo = gl.dequantize(Tmax)
+    for b, T in enumerate(lens):
+        for h in range(H):
+            kr, vr = O.dequantized_f32(caches[b][h])
+            assert np.array_equal(ko[b, h, :T].view(np.uint32), kr.view(np.uint32))
+            assert np.array_equal(vo[b, h, :T].view(np.uint32), vr.view(np.uint32))
+            assert np.all(ko[b, h, T:] == 0) and np.all(vo[b, h, T:] == 0)
+    # attention
+    qf = O.bf16_to_f32(q)
+    out_ref, lse_ref = O.decode_attention(qf, caches)
+    out, lse = gl.decode(q)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+    out16, lse16 = gl.decode(q, out_bf16=True)
+    assert torch.equal(out16, out.to(torch.bfloat16))
+    assert torch.equal(lse16, lse)
+    assert gl.status_value() == 0
+
+
+@pytest.mark.parametrize("fmt,G,Gv,R,S", [("int4", 32, 128, 32, 0), ("int2", 32, 32, 64, 1),
+                                          ("int8", 16, 64, 16, 2), ("fp8_e4m3", 1, 128, 0, 1)])
+def test_incremental_appends_equal_bulk(fmt, G, Gv, R, S):
+    lens = [203, 77]
+
+    def chunks(T):
+        out, t, i = [], 0, 0
+        pattern = [1, 1, 5, 1, 40, 1, 1, 33, 2]
+        while t < T:
+            n = min(pattern[i % len(pattern)], T - t)
+            out.append(n)
+            t += n
+            i += 1
+        return out
+
+    gl, caches, q = build(fmt, 2, 3, lens, G, Gv, R, S, False, 123, chunks=chunks)
+    for b, T in enumerate(lens):
+        for h in range(2):
+            TL.compare_logical(gl.logical(b, h, T), caches[b][h])
+    out, lse = gl.decode(q)
+    out_ref, lse_ref = O.decode_attention(O.bf16_to_f32(q), caches)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+    assert gl.status_value() == 0
+
+
+@pytest.mark.parametrize("fmt", ["int4", "fp8_e4m3"])
+def test_paged_equals_contiguous_and_permutation_invariant(fmt):
+    lens = [700, 129, 64]
+    G = 1 if fmt == "fp8_e4m3" else 16
+    gc, _, q = build(fmt, 2, 4, lens, G, 128, 32 if G > 1 else 0, 1, False, 5)
+    gp, _, _ = build(fmt, 2, 4, lens, G, 128, 32 if G > 1 else 0, 1, True, 5)
+    oc, lc = gc.decode(q)
+    op, lp = gp.decode(q)
+    assert torch.equal(oc, op) and torch.equal(lc, lp)
+    gp2, _, _ = build(fmt, 2, 4, lens, G, 128, 32 if G > 1 else 0, 1, True, 6)  # other block permutation
+    assert not np.array_equal(gp2.table_np, gp.table_np)
+    # same data, different table: outputs identical bit for bit
+    gp3, _, _ = build(fmt, 2, 4, lens, G, 128, 32 if G > 1 else 0, 1, True, 5)
+    o3, l3 = gp3.decode(q)
+    assert torch.equal(o3, op) and torch.equal(l3, lp)
+
+
+def test_bad_block_and_capacity_are_reported_not_faulted():
+    from quantized_kv_cache_decode_gb300 import kvq
+    lens = [300, 200]
+    gl, caches, q = build("int4", 2, 4, lens, 16, 128, 32, 0, True, 9)
+    # corrupt one block-table entry (host-made fault): the kernel must skip that tile and report
+    bad = gl.table_np.copy()
+    bad[0, 3] = gl.cfg.num_blocks + 5
+    gl.layer.block_table.copy_(torch.from_numpy(bad))
+    gl.status.zero_()
+    out, lse = gl.decode(q)
+    assert gl.status_value() & kvq.DEV_BAD_BLOCK
+    assert torch.isfinite(out).all()
+    # a length beyond the capacity: reported and clamped
+    gl.layer.block_table.copy_(torch.from_numpy(gl.table_np))
+    gl.status.zero_()
+    out, lse = gl.decode(q, lens=[300, 10 ** 6])
+    assert gl.status_value() & kvq.DEV_CAPACITY
+    assert torch.isfinite(out).all()
+
+
+def test_workspace_too_small_is_rejected():
+    from quantized_kv_cache_decode_gb300 import kvq
+    gl, _, q = build("int4", 1, 2, [64], 16, 128, 16, 0, False, 3)
+    wsb = kvq.decode_workspace_size(gl.cfg, 1, 2)
+    ws = torch.empty(wsb - 16, dtype=torch.uint8, device="cuda")
+    out = torch.empty((1, 2, 128), dtype=torch.float32, device="cuda")
+    sl = torch.tensor([64], dtype=torch.int32, device="cuda")
+    qd = torch.from_numpy(q.astype(np.int16)).cuda()
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.decode_attention(gl.cfg, gl.layer.struct(), qd, 2, sl, 1, 0.1, out, False, None, ws, wsb - 16)
+    assert e.value.status == -4
