@@ -216,3 +216,40 @@ def random_bf16(seed: int, shape, scale: float = 1.0, outlier_mask: Optional[np.
     if outlier_mask is not None:
         x = np.where(outlier_mask, x * np.float32(outlier_scale), x).astype(np.float32)
     return f32_to_bf16_bits(x)
+
+
+# --------------------------------------------------------------------------- #
+# Device-side draws for full-size workloads (timing; sampled parity)
+# --------------------------------------------------------------------------- #
+
+
+def device_kv_bf16(w: Workload, layer: int, T: int, device, batch: Optional[int] = None, seed_offset: int = 0):
+    """K, V of one layer for all sequences and kv heads: torch bf16 [B, H, T, d] on ``device``.
+
+    Seeded torch generator on the device; outlier channels as in ``outlier_channels``.
+    The bf16 values are the inputs: tests copy sampled (sequence, head) slices back to
+    the host for the oracle.
+    """
+    import torch
+    B = w.batch if batch is None else batch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed * 100003 + layer * 7919 + seed_offset)
+    shape = (B, w.num_kv_heads, T, w.head_dim)
+    k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    km = torch.from_numpy(outlier_channels(w, "k", layer)).to(device)
+    vm = torch.from_numpy(outlier_channels(w, "v", layer)).to(device)
+    scale = float(w.outlier_scale)
+    k = torch.where(km[None, :, None, :], k * scale, k)
+    v = torch.where(vm[None, :, None, :], v * scale, v)
+    return k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def device_q_bf16(w: Workload, layer: int, device, batch: Optional[int] = None, seed_offset: int = 0):
+    """Decode queries of one layer: torch bf16 [B, Hq, d] on ``device`` (seeded)."""
+    import torch
+    B = w.batch if batch is None else batch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed * 100019 + layer * 104729 + seed_offset + 1)
+    q = torch.randn((B, w.num_q_heads, w.head_dim), generator=gen, device=device, dtype=torch.float32)
+    return q.to(torch.bfloat16)
