@@ -1,0 +1,551 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized KV-cache decode step on GB300 (one JSON line).
+
+A step is one decode step of the whole hot path for every layer of the
+workload: quantize-on-append of the new token of every sequence (bf16 residual
+write, group spill or FP8 encode), then fused decode attention over the whole
+cache (split pass + log-sum-exp combine).  Inputs are seeded synthetic tensors
+already resident in HBM; the cache is built before the timed region.
+
+Metric: effective KV GB/s = algorithmic bytes of one step (codes + scales and
+zero-points + bf16 sink/residual + q + out + lse + append traffic, every KV head
+read once) / step time.  Also reported: % of the measured HBM peak, tokens/s
+(sequences decoded per second).
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own
+GPU (the path shards by sequence with no exchange: weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle baseline is timed single-threaded (set before numpy loads BLAS)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse
+import datetime
+import json
+import math
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_kv_cache_decode_gb300 import inputs as I  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama3_8b_fp8_e4m3"
+L2_BYTES = 129 * 2 ** 20
+
+
+# --------------------------------------------------------------------------- #
+# byte accounting (algorithmic bytes; the roofline numerator)
+# --------------------------------------------------------------------------- #
+
+
+def split_tokens(T, fmt):
+    n_sink = min(T, fmt.S)
+    n = T - n_sink
+    if fmt.fmt == "fp8_e4m3":
+        return n_sink, n, 0
+    qn = max(0, (n - fmt.R) // fmt.G) * fmt.G
+    return n_sink, qn, n - qn
+
+
+def attention_bytes(fmt, T, H, d=128):
+    """Bytes one (sequence, kv head) must read for attention over T tokens."""
+    bits = 8 if fmt.fmt == "fp8_e4m3" else I.FORMAT_BITS[fmt.fmt]
+    n_sink, qn, r = split_tokens(T, fmt)
+    b = 2 * qn * d * bits // 8
+    if fmt.fmt != "fp8_e4m3":
+        b += (qn // fmt.G) * d * 8 + qn * (d // fmt.Gv) * 8
+    b += (n_sink + r) * d * 2 * 2
+    return b * H
+
+
+def append_bytes(fmt, T_before, n, H, d=128):
+    """Bytes moved by appending n tokens to one sequence (all heads)."""
+    bits = 8 if fmt.fmt == "fp8_e4m3" else I.FORMAT_BITS[fmt.fmt]
+    b = 2 * n * d * 2  # read new K, V
+    if fmt.fmt == "fp8_e4m3":
+        return H * (b + 2 * n * d)
+    _, q0, _ = split_tokens(T_before, fmt)
+    n_sink1, q1, r1 = split_tokens(T_before + n, fmt)
+    spilled = q1 - q0
+    b += 2 * n * d * 2  # ring write (upper bound: every new token)
+    b += spilled * 2 * d * 2  # spilled tokens read back (bf16 K, V)
+    b += 2 * spilled * d * bits // 8 + (spilled // fmt.G) * d * 8 + spilled * (d // fmt.Gv) * 8
+    return H * b
+
+
+def step_bytes(w, lens_after, n_app):
+    total = 0
+    for l, fmt in enumerate(w.layer_formats):
+        for T in lens_after:
+            total += attention_bytes(fmt, int(T), w.num_kv_heads)
+            total += append_bytes(fmt, int(T) - n_app, n_app, w.num_kv_heads)
+        B = len(lens_after)
+        total += B * w.num_q_heads * 128 * 2  # q
+        total += B * w.num_q_heads * 128 * 2  # out (bf16)
+        total += B * w.num_q_heads * 4        # lse
+    return total
+
+
+# --------------------------------------------------------------------------- #
+# clocks
+# --------------------------------------------------------------------------- #
+
+
+class ClockSampler:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, t0: float, t1: float):
+        """Median SM clock and active throttle reasons of the samples taken in [t0, t1] (epoch s)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(p[2]), float(p[3]), p[6:10]))
+                except ValueError:
+                    continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "warmup+timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3][i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------- #
+# the GPU workload
+# --------------------------------------------------------------------------- #
+
+
+class Layer:
+    """One layer's cache (one replica) with its step inputs and outputs."""
+
+    def __init__(self, kvq, torch, w, l, fmt, lens_before, n_app, dev, seed_offset):
+        self.kvq, self.torch = kvq, torch
+        B, H, Hq = len(lens_before), w.num_kv_heads, w.num_q_heads
+        self.B, self.H, self.Hq, self.fmt = B, H, Hq, fmt
+        lens_after = [int(t) + n_app for t in lens_before]
+        fp8 = fmt.fmt == "fp8_e4m3"
+        G = 1 if fp8 else fmt.G
+        qmax = [split_tokens(t, fmt)[1] for t in lens_after]
+        if w.paged:
+            P = w.block_tokens
+            nblk = [math.ceil(q / P) for q in qmax]
+            mbps = max(nblk + [1])
+            self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, paged=True, block_tokens=P,
+                                       num_blocks=max(1, sum(nblk)), max_blocks_per_seq=mbps)
+        else:
+            unit = 16 if fp8 else max(16, G)
+            cap = max(unit, math.ceil(max(qmax) / unit) * unit)
+            self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, capacity_tokens=cap)
+        self.cache = kvq.CacheLayer(self.cfg, B, device=dev, zero=False)
+        if w.paged:
+            perm = torch.from_numpy(I.block_permutation(w, max(1, sum(nblk)), l)).to(dev)
+            table = torch.full((B, mbps), -1, dtype=torch.int32, device=dev)
+            k = 0
+            for b, nb in enumerate(nblk):
+                table[b, :nb] = perm[k:k + nb]
+                k += nb
+            self.cache.block_table.copy_(table)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.lens_before = torch.tensor(lens_before, dtype=torch.int32, device=dev)
+        self.lens_after = torch.tensor(lens_after, dtype=torch.int32, device=dev)
+        self.n_app = n_app
+        # build: the cache holds lens_before tokens; the step appends n_app more
+        Tmax = max(lens_after)
+        uniform = len(set(lens_after)) == 1
+        if uniform:
+            k, v = I.device_kv_bf16(w, l, Tmax, dev, batch=B, seed_offset=seed_offset)
+            self._calibrate(fp8, k, v)
+            Tb = lens_before[0]
+            if Tb > 0:
+                zero = torch.zeros(B, dtype=torch.int32, device=dev)
+                kvq.quantize_append(self.cfg, self.cache.struct(), k[:, :, :Tb].contiguous(),
+                                    v[:, :, :Tb].contiguous(), Tb, zero, B, self.status)
+            self.k_new = k[:, :, Tb:Tb + n_app].contiguous()
+            self.v_new = v[:, :, Tb:Tb + n_app].contiguous()
+            del k, v
+        else:
+            if fp8:
+                raise NotImplementedError("per-tensor FP8 calibration over ragged batches")
+            self.k_new = torch.empty((B, H, n_app, 128), dtype=torch.bfloat16, device=dev)
+            self.v_new = torch.empty_like(self.k_new)
+            zero1 = torch.zeros(1, dtype=torch.int32, device=dev)
+            for b in range(B):
+                wb = I.Workload(**{**w.__dict__, "batch": 1})
+                k, v = I.device_kv_bf16(wb, l, lens_after[b], dev, batch=1, seed_offset=seed_offset + 7 * b)
+                Tb = lens_before[b]
+                kvq.quantize_append(self.cfg, self.cache.seq_struct(b), k[:, :, :Tb].contiguous(),
+                                    v[:, :, :Tb].contiguous(), Tb, zero1, 1, self.status)
+                self.k_new[b] = k[0, :, Tb:Tb + n_app]
+                self.v_new[b] = v[0, :, Tb:Tb + n_app]
+                del k, v
+        self.q = I.device_q_bf16(w, l, dev, batch=B, seed_offset=seed_offset)
+        self.out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.wsb = kvq.decode_workspace_size(self.cfg, B, Hq)
+        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device=dev)
+        self.struct = self.cache.struct()
+        self.scale = 1.0 / math.sqrt(128)
+
+    def _calibrate(self, fp8, k, v):
+        if fp8:
+            self.kvq.fp8_calibrate(k, k.numel(), self.cache.k_tensor_scale)
+            self.kvq.fp8_calibrate(v, v.numel(), self.cache.v_tensor_scale)
+
+    def append(self, stream=None):
+        self.kvq.quantize_append(self.cfg, self.struct, self.k_new, self.v_new, self.n_app, self.lens_before,
+                                 self.B, self.status, stream)
+
+    def partials(self, stream=None):
+        self.kvq.decode_partials(self.cfg, self.struct, self.q, self.Hq, self.lens_after, self.B, self.scale,
+                                 self.ws, self.wsb, self.status, stream)
+
+    def combine(self, stream=None):
+        self.kvq.decode_combine(self.cfg, self.Hq, self.B, self.out, True, self.lse, self.ws, self.wsb, stream)
+
+
+def count_launches(w):
+    # per layer: append (1 kernel), decode split pass (1), combine (1)
+    return 3 * len(w.layer_formats)
+
+
+def run_gpu(args, w, rank, world):
+    import torch
+    from quantized_kv_cache_decode_gb300 import kvq
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    n_app = max(1, w.append_tokens)
+    lens_after = I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
+    lens_before = [int(t) - n_app for t in lens_after]
+    sbytes = step_bytes(w, lens_after, n_app)
+    replicas = args.replicas or max(1, min(4, math.ceil(3 * L2_BYTES / sbytes)))
+    reps = []
+    for rep in range(replicas):
+        reps.append([Layer(kvq, torch, w, l, f, lens_before, n_app, dev, seed_offset=1000 * rep + 17 * rank)
+                     for l, f in enumerate(w.layer_formats)])
+    torch.cuda.synchronize()
+    for rep in reps:
+        for lay in rep:
+            assert lay.status.item() == 0, f"device status {lay.status.item()} while building"
+    stream = torch.cuda.current_stream()
+    dist = world > 1
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+
+    def step(i, ev=None):
+        rep = reps[i % replicas]
+        for j, lay in enumerate(rep):
+            lay.append()
+            if ev is not None:
+                ev[0][j].record(stream)
+            lay.partials()
+            if ev is not None:
+                ev[1][j].record(stream)
+            lay.combine()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    clk = ClockSampler(dev.index if dev.index is not None else 0, os.path.join(ROOT, "gpurun_out",
+                                                                                f"clocks_rank{rank}.csv")) \
+        if rank == 0 else None
+    time.sleep(0.15 if clk else 0)
+    # ---- timed region: exactly K steps; per-launch events around the decode split pass ----
+    K = args.steps
+    nl = len(w.layer_formats)
+    evs = [([torch.cuda.Event(enable_timing=True) for _ in range(nl)],
+            [torch.cuda.Event(enable_timing=True) for _ in range(nl)]) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier()
+    ms = t_start.elapsed_time(t_end)
+    kern_ms = [evs[i][0][j].elapsed_time(evs[i][1][j]) for i in range(K) for j in range(nl)]
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / K
+    # ---- end to end through the public API, host buffers, copies inside the timed region ----
+    E = args.e2e_steps or K
+    rep0 = reps[0]
+    h_q = [lay.q.cpu().pin_memory() for lay in rep0]
+    h_k = [lay.k_new.cpu().pin_memory() for lay in rep0]
+    h_v = [lay.v_new.cpu().pin_memory() for lay in rep0]
+    h_out = [torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory() for lay in rep0]
+    h_lse = [torch.empty(lay.lse.shape, dtype=lay.lse.dtype).pin_memory() for lay in rep0]
+    h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v)
+    d2h = sum(x.numel() * x.element_size() for x in h_out + h_lse)
+
+    def e2e_step():
+        for j, lay in enumerate(rep0):
+            lay.q.copy_(h_q[j], non_blocking=True)
+            lay.k_new.copy_(h_k[j], non_blocking=True)
+            lay.v_new.copy_(h_v[j], non_blocking=True)
+            lay.append()
+            lay.partials()
+            lay.combine()
+            h_out[j].copy_(lay.out, non_blocking=True)
+            h_lse[j].copy_(lay.lse, non_blocking=True)
+
+    for _ in range(min(3, E)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = (time.perf_counter() - e0) * 1e3 / E
+    if dist:
+        t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(t.item())
+    clocks = None
+    if clk:
+        clk.stop()
+        clocks = clk.summary(wall0, wall1)
+    for rep in reps:
+        for lay in rep:
+            assert lay.status.item() == 0, f"device status {lay.status.item()}"
+    return dict(ms_step=ms_step, kern_ms=float(np.mean(kern_ms)), kern_ms_all=kern_ms, sbytes=sbytes,
+                replicas=replicas, e2e_ms=e_ms, h2d=h2d, d2h=d2h, clocks=clocks, wall_ms=(wall1 - wall0) * 1e3,
+                lens_after=lens_after, n_app=n_app,
+                attn_bytes_first_layer=sum(attention_bytes(w.layer_formats[0], int(T), w.num_kv_heads)
+                                           for T in lens_after) + len(lens_after) * w.num_q_heads * 128 * 2)
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle (baseline and the reference arm)
+# --------------------------------------------------------------------------- #
+
+
+def oracle_sample(w, max_pairs):
+    """Host inputs and prebuilt oracle caches for a bounded sample of (layer 0, sequence, head) pairs."""
+    from oracle import kvq_oracle as O
+    fmt = w.layer_formats[0]
+    lens_after = I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
+    n_app = max(1, w.append_tokens)
+    spec = O.Spec(fmt.fmt, d=128, G=1 if fmt.fmt == "fp8_e4m3" else fmt.G, Gv=fmt.Gv,
+                  R=0 if fmt.fmt == "fp8_e4m3" else fmt.R, S=fmt.S)
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)][:max_pairs]
+    q = O.bf16_to_f32(I.q_bf16(w, 0))
+    items = []
+    for b, h in pairs:
+        T = int(lens_after[b])
+        k, v = I.kv_bf16(w, 0, b, h, T)
+        kf, vf = O.bf16_to_f32(k), O.bf16_to_f32(v)
+        ks = O.fp8_tensor_scale(kf) if spec.is_fp8 else None
+        vs = O.fp8_tensor_scale(vf) if spec.is_fp8 else None
+        hc = O.build_head_cache(kf[:T - n_app], vf[:T - n_app], spec, ks, vs)
+        items.append((b, h, T, hc, kf[T - n_app:], vf[T - n_app:], q[b, h * w.gqa:(h + 1) * w.gqa]))
+    return O, spec, items, n_app
+
+
+def oracle_step(O, items):
+    """One oracle decode step over the sample: append the new tokens, attend for the g heads."""
+    import copy
+    for (b, h, T, hc, kn, vn, qh) in items:
+        c = copy.copy(hc)
+        for t in range(len(kn)):
+            O.append_token(c, kn[t], vn[t])
+        kh, vh = O.dequantized_f64(c)
+        for j in range(qh.shape[0]):
+            O.attend_head(qh[j], kh, vh, 1.0 / math.sqrt(128))
+
+
+def sample_bytes(w, items, n_app):
+    fmt = w.layer_formats[0]
+    tot = 0
+    for (b, h, T, hc, kn, vn, qh) in items:
+        tot += attention_bytes(fmt, T, 1) + append_bytes(fmt, T - n_app, n_app, 1)
+        tot += qh.shape[0] * (128 * 2 * 2 + 4)
+    return tot
+
+
+def cpu_baseline(w, budget_s=12.0):
+    O, spec, items, n_app = oracle_sample(w, max_pairs=w.batch * w.num_kv_heads)
+    # grow the sample until ~budget_s of CPU work, bounded by the whole first layer
+    t0 = time.perf_counter()
+    done = []
+    for it in items:
+        oracle_step(O, [it])
+        done.append(it)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    gbs = sample_bytes(w, done, n_app) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"layer 0, {len(done)} of {w.batch * w.num_kv_heads} (sequence, kv head) pairs, "
+                      f"append + attention, numpy fp64 single thread, {dt:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    O, spec, items, n_app = oracle_sample(w, max_pairs=w.batch * w.num_kv_heads)
+    # a step = the oracle over a bounded sample of pairs, sized to ~1 s
+    t0 = time.perf_counter()
+    oracle_step(O, items[:1])
+    per_pair = max(1e-3, time.perf_counter() - t0)
+    n = max(1, min(len(items), int(1.0 / per_pair)))
+    sample = items[:n]
+    for _ in range(args.warmup):
+        oracle_step(O, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(O, sample)
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = sample_bytes(w, sample, n_app) / dt / 1e9
+    return gbs, dt, n
+
+
+# --------------------------------------------------------------------------- #
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--replicas", type=int, default=0, help="cache copies cycled to defeat L2 (0: auto)")
+    ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    w = I.WORKLOADS[args.workload]()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    config = {"workload": w.name, "layers": len(w.layer_formats), "batch": w.batch, "q_heads": w.num_q_heads,
+              "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+              "seq_len": w.seq_len if w.seq_len else f"log-uniform {tuple(w.seq_len_range)}",
+              "formats": sorted({f.fmt for f in w.layer_formats}), "append_tokens_per_step": max(1, w.append_tokens),
+              "paged": w.paged}
+    metric = "effective KV GB/s (quantized decode step)"
+
+    if args.impl == "reference":
+        r = run_reference(args, w, rank, world)
+        if rank == 0:
+            gbs, dt, n = r
+            cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"layer 0, {n} (sequence, kv head) pairs per step, append + attention, numpy fp64"}
+            line = {"impl": "reference", "metric": metric, "value": round(gbs, 4), "unit": "GB/s",
+                    "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                    "data": "synthetic", "config": config, "cpu_baseline": cpu,
+                    "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ["LOCAL_RANK"])))
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    r = run_gpu(args, w, rank, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    gbs = r["sbytes"] * world / (r["ms_step"] * 1e-3) / 1e9
+    kern_gbs = r["attn_bytes_first_layer"] / (r["kern_ms"] * 1e-3) / 1e9 if len(w.layer_formats) == 1 else None
+    if kern_gbs is None:
+        # multi-layer: bytes of every layer's attention over the mean launch duration
+        per_layer = [sum(attention_bytes(f, int(T), w.num_kv_heads) for T in r["lens_after"]) +
+                     len(r["lens_after"]) * w.num_q_heads * 256 for f in w.layer_formats]
+        kern_gbs = float(np.mean(per_layer)) / (r["kern_ms"] * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("bytes_per_launch")
+    line = {
+        "metric": metric, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16/f32 (fp8/int codes)", "data": "synthetic",
+        "config": {**config, "l2": f"{r['replicas']} rotating cache copies, {r['replicas'] * r['sbytes'] / 1e6:.0f} MB"
+                   f" cycled (L2 {L2_BYTES / 2 ** 20:.0f} MiB)", "bytes_per_step": r["sbytes"]},
+        "pct_hbm_peak": round(100 * gbs / world / hbm_peak, 2),
+        "tokens_per_s": round(len(r["lens_after"]) * world / (r["ms_step"] * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(kern_gbs / hbm_peak, 4), "traffic": traffic,
+                     "kernel": "decode_kernel (split pass)", "peak_source": peak_src,
+                     "mean_launch_us": round(r["kern_ms"] * 1e3, 2)},
+        "e2e": {"value": round(r["sbytes"] * world / (r["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 4)},
+        "gpu_launches": count_launches(w) * args.steps,
+        "clocks": r["clocks"],
+        "wall_ms_timed": round(r["wall_ms"], 2),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

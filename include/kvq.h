@@ -227,6 +227,26 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
                                 uint32_t* dev_status, void* stream);
 
 /*
+ * kvq_decode_partials / kvq_decode_combine -- the two passes of
+ * kvq_decode_attention, callable separately (same arguments, same workspace).
+ * kvq_decode_partials runs the split pass: every CTA of the grid reads an equal
+ * share of the cache and writes, into the workspace, one partial per (sequence,
+ * kv head) it touches: the output normalised by its own softmax sum and its
+ * log-sum-exp.  kvq_decode_combine merges the partials of each (sequence, query
+ * head) by their log-sum-exp weights into out and lse.  Call them on the same
+ * device and stream, with the same config, batch and query-head count, and
+ * combine before the workspace is reused.  A caller that splits one sequence
+ * over several devices can merge the per-device results with the same
+ * log-sum-exp rule.  Errors as for kvq_decode_attention.
+ */
+kvq_status kvq_decode_partials(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                               int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, uint32_t* dev_status, void* stream);
+kvq_status kvq_decode_combine(const kvq_layer_config* cfg, int32_t num_q_heads, int32_t batch, void* out,
+                              int32_t out_bf16, float* lse, const void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * kvq_dequantize -- export the dequantized cache as fp32.
  * Source: [KVQA] s2 (x_hat = s(q - z)), s4 (FP8 value times its scale).
  *   k_out, v_out  device f32 [batch][H][max_tokens][d]; token t < seq_lens[b]

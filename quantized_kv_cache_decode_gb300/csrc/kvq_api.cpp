@@ -244,19 +244,29 @@ kvq_status kvq_decode_workspace_size(const kvq_layer_config* cfg, int32_t batch,
   return KVQ_OK;
 }
 
-kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+}  // extern "C"
+
+namespace kvq {
+namespace {
+
+kvq_status check_decode_args(const kvq_layer_config* cfg, int32_t num_q_heads, int32_t batch, LayerDesc* L) {
+  kvq_status st = make_desc(cfg, L);
+  if (st != KVQ_OK) return st;
+  if (batch < 0 || batch > kMaxBatch || num_q_heads < L->H || num_q_heads % L->H != 0 ||
+      num_q_heads / L->H > kMaxGqa)
+    return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
                                 int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
-                                void* out, int32_t out_bf16, float* lse, void* workspace, size_t workspace_bytes,
-                                uint32_t* dev_status, void* stream) {
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t s) {
   LayerDesc L;
-  kvq_status st = make_desc(cfg, &L);
+  kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
   if ((st = check_cache(L, cache)) != KVQ_OK) return st;
-  if (batch < 0 || batch > kMaxBatch || num_q_heads < L.H || num_q_heads % L.H != 0 ||
-      num_q_heads / L.H > kMaxGqa || (out_bf16 != 0 && out_bf16 != 1))
-    return KVQ_ERR_INVALID_ARG;
   if (batch == 0) return KVQ_OK;
-  if (!q || !seq_lens || !out || !workspace || !aligned16(workspace) || !(softmax_scale == softmax_scale))
+  if (!q || !seq_lens || !workspace || !aligned16(workspace) || !(softmax_scale == softmax_scale))
     return KVQ_ERR_INVALID_ARG;
   const int g = num_q_heads / L.H;
   DecodeGeom G;
@@ -282,7 +292,6 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
   p.ws_lse = reinterpret_cast<float*>(ws + G.off_lse);
   p.ws_prefix = reinterpret_cast<int*>(ws + G.off_prefix);
   p.status = dev_status;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (L.fmt) {
     case KVQ_FMT_INT2: e = launch_decode_int2(p, G.smem, s); break;
@@ -290,21 +299,71 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
     case KVQ_FMT_INT8: e = launch_decode_int8(p, G.smem, s); break;
     default: e = launch_decode_fp8(p, G.smem, s); break;
   }
-  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status decode_combine_impl(const kvq_layer_config* cfg, int32_t num_q_heads, int32_t batch, void* out,
+                               int32_t out_bf16, float* lse, const void* workspace, size_t workspace_bytes,
+                               cudaStream_t s) {
+  LayerDesc L;
+  kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
+  if (st != KVQ_OK) return st;
+  if (out_bf16 != 0 && out_bf16 != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (!out || !workspace || !aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+  const int g = num_q_heads / L.H;
+  DecodeGeom G;
+  if ((st = decode_geometry(L, batch, g, &G)) != KVQ_OK) return st;
+  if (workspace_bytes < G.ws_bytes) return KVQ_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   CombineParams c;
   c.H = L.H;
   c.g = g;
   c.Hq = num_q_heads;
   c.batch = batch;
   c.num_ctas = G.num_ctas;
-  c.ws_prefix = p.ws_prefix;
-  c.ws_o = p.ws_o;
-  c.ws_lse = p.ws_lse;
+  c.ws_prefix = reinterpret_cast<const int*>(ws + G.off_prefix);
+  c.ws_o = reinterpret_cast<const float*>(ws);
+  c.ws_lse = reinterpret_cast<const float*>(ws + G.off_lse);
   c.out = out;
   c.out_bf16 = out_bf16;
   c.lse = lse;
-  if (launch_combine(c, s) != cudaSuccess) return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  return launch_combine(c, s) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" {
+
+kvq_status kvq_decode_partials(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                               int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+  return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
+                              workspace_bytes, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_combine(const kvq_layer_config* cfg, int32_t num_q_heads, int32_t batch, void* out,
+                              int32_t out_bf16, float* lse, const void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return decode_combine_impl(cfg, num_q_heads, batch, out, out_bf16, lse, workspace, workspace_bytes,
+                             static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
+                                void* out, int32_t out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, void* stream) {
+  LayerDesc L;
+  kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
+  if (st != KVQ_OK) return st;
+  if (out_bf16 != 0 && out_bf16 != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch > 0 && !out) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace, workspace_bytes,
+                            dev_status, s);
+  if (st != KVQ_OK) return st;
+  return decode_combine_impl(cfg, num_q_heads, batch, out, out_bf16, lse, workspace, workspace_bytes, s);
 }
 
 kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const int32_t* seq_lens,

@@ -59,11 +59,14 @@ _lib.kvq_quantize_append.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_vp
 _lib.kvq_decode_workspace_size.argtypes = [_P(LayerConfig), c_i32, c_i32, _P(c_sz)]
 _lib.kvq_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
                                       c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
+_lib.kvq_decode_partials.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
+                                     c_vp, c_sz, c_vp, c_vp]
+_lib.kvq_decode_combine.argtypes = [_P(LayerConfig), c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]
 _lib.kvq_dequantize.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]
 _lib.kvq_status_string.argtypes = [c_i32]
 _lib.kvq_status_string.restype = ctypes.c_char_p
 for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_quantize_append", "kvq_decode_workspace_size",
-            "kvq_decode_attention", "kvq_dequantize"):
+            "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize"):
     getattr(_lib, _fn).restype = c_i32
 
 
@@ -141,6 +144,21 @@ def decode_attention(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, s
                                      workspace_bytes, _ptr(dev_status), _stream_ptr(stream)))
 
 
+def decode_partials(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, seq_lens, batch: int,
+                    softmax_scale: float, workspace, workspace_bytes: int, dev_status=None, stream=None) -> None:
+    _check("kvq_decode_partials",
+           _lib.kvq_decode_partials(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads, _ptr(seq_lens),
+                                    batch, softmax_scale, _ptr(workspace), workspace_bytes, _ptr(dev_status),
+                                    _stream_ptr(stream)))
+
+
+def decode_combine(cfg: LayerConfig, num_q_heads: int, batch: int, out, out_bf16: bool, lse, workspace,
+                   workspace_bytes: int, stream=None) -> None:
+    _check("kvq_decode_combine",
+           _lib.kvq_decode_combine(ctypes.byref(cfg), num_q_heads, batch, _ptr(out), int(out_bf16), _ptr(lse),
+                                   _ptr(workspace), workspace_bytes, _stream_ptr(stream)))
+
+
 def dequantize(cfg: LayerConfig, cache: LayerCache, seq_lens, batch: int, max_tokens: int, k_out, v_out,
                dev_status=None, stream=None) -> None:
     _check("kvq_dequantize",
@@ -178,6 +196,16 @@ class CacheLayer:
         c.block_table = _ptr(self.block_table)
         c.k_tensor_scale = _ptr(self.k_tensor_scale)
         c.v_tensor_scale = _ptr(self.v_tensor_scale)
+        return c
+
+    def seq_struct(self, b: int) -> LayerCache:
+        """The cache struct of sequence b alone (pointer offsets), for batch = 1 calls."""
+        c = self.struct()
+        for n in FIELDS:
+            if n != "block_pool" and getattr(c, n):
+                setattr(c, n, getattr(c, n) + b * (self.sizes[n] // self.num_seqs))
+        if self.block_table is not None:
+            c.block_table = c.block_table + b * self.cfg.max_blocks_per_seq * 4
         return c
 
     def nbytes(self) -> int:
