@@ -227,7 +227,7 @@ class Layer:
         self.out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
         self.wsb = kvq.decode_workspace_size(self.cfg, B, Hq)
-        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(self.wsb, dtype=torch.uint8, device=dev)
         self.struct = self.cache.struct()
         self.scale = 1.0 / math.sqrt(128)
 

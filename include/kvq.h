@@ -215,8 +215,13 @@ kvq_status kvq_decode_workspace_size(const kvq_layer_config* cfg, int32_t batch,
  *             (out_bf16 == 1: the round-to-nearest-even of the fp32 result)
  *   lse       device f32 [batch][num_q_heads] natural-log log-sum-exp of the
  *             scaled scores, or NULL
- *   workspace device, at least kvq_decode_workspace_size() bytes, no alignment
- *             beyond 16 bytes, contents need not be initialised
+ *   workspace device, at least kvq_decode_workspace_size() bytes, 16-byte
+ *             aligned.  Zero-fill it once before its first use: its last
+ *             batch*H 32-bit words are arrival counters (the last CTA to finish
+ *             a (sequence, kv head) merges that pair's partials, in the same
+ *             launch) and every call leaves them at zero again.  After a call
+ *             that reported KVQ_DEV_TIMEOUT, zero it again.  Calls that share a
+ *             workspace must not overlap on the GPU.
  * A sequence with 0 tokens gets out = 0, lse = -inf.  Device errors:
  * KVQ_DEV_BAD_BLOCK (tile skipped), KVQ_DEV_CAPACITY (length clamped to the
  * capacity), KVQ_DEV_TIMEOUT.
@@ -227,8 +232,8 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
                                 uint32_t* dev_status, void* stream);
 
 /*
- * kvq_decode_partials / kvq_decode_combine -- the two passes of
- * kvq_decode_attention, callable separately (same arguments, same workspace).
+ * kvq_decode_partials / kvq_decode_combine -- kvq_decode_attention as two
+ * launches (same arguments, same workspace; the counters are not used).
  * kvq_decode_partials runs the split pass: every CTA of the grid reads an equal
  * share of the cache and writes, into the workspace, one partial per (sequence,
  * kv head) it touches: the output normalised by its own softmax sum and its

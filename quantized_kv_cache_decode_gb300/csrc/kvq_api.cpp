@@ -14,7 +14,7 @@ namespace {
 constexpr int kThreadsDecode = 128;  // 4 warps (kvq_decode.cuh)
 constexpr int kMaxStages = 4;
 constexpr int kWarpScratch = 16 * 272;
-constexpr int kSmemPerCtaTarget = 110 * 1024;  // two resident CTAs per SM
+constexpr int kSmemPerCtaTarget = 74 * 1024;  // three resident CTAs per SM
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -122,9 +122,17 @@ int stage_bytes_of(const LayerDesc& L) {
   return b;
 }
 
-int fixed_smem(int batch) {
+// Shared scratch per warp: a padded bf16 tile when the layer keeps bf16 tokens
+// (sink or residual window), else just the warp's merge record (g heads).
+int warp_scratch_of(const LayerDesc& L, int g) {
+  const bool bf16_tiles = L.S > 0 || !L.fp8;
+  const int merge = g * 132 * 4;
+  return bf16_tiles ? std::max(kWarpScratch, merge) : merge;
+}
+
+int fixed_smem(int batch, int warp_scratch) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16;
-  return kThreadsDecode / 32 * kMaxStages * 8 + 8 * 4 * 36 * 4 + kThreadsDecode / 32 * kWarpScratch + prefix;
+  return kThreadsDecode / 32 * kMaxStages * 8 + 8 * 4 * 36 * 4 + kThreadsDecode / 32 * warp_scratch + prefix;
 }
 
 cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
@@ -137,13 +145,14 @@ cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
 }
 
 struct DecodeGeom {
-  int smem, nst, stage_bytes, num_ctas;
-  size_t ws_bytes, off_lse, off_prefix;
+  int smem, nst, stage_bytes, num_ctas, warp_scratch;
+  size_t ws_bytes, off_lse, off_prefix, off_counters;
 };
 
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) {
   const int sb = stage_bytes_of(L);
-  const int fixed = fixed_smem(batch);
+  const int wsc = warp_scratch_of(L, g);
+  const int fixed = fixed_smem(batch, wsc);
   int nst = kMaxStages;
   while (nst > 2 && fixed + (kThreadsDecode / 32) * nst * sb > kSmemPerCtaTarget) --nst;
   const int smem = fixed + (kThreadsDecode / 32) * nst * sb;
@@ -153,6 +162,7 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) 
   if (occupancy(L, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
   if (per_sm < 1) return KVQ_ERR_UNSUPPORTED;
   G->smem = smem;
+  G->warp_scratch = wsc;
   G->nst = nst;
   G->stage_bytes = sb;
   G->num_ctas = sms * per_sm;
@@ -161,7 +171,8 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) 
   const size_t l_bytes = slots * g * sizeof(float);
   G->off_lse = (o_bytes + 255) / 256 * 256;
   G->off_prefix = G->off_lse + (l_bytes + 255) / 256 * 256;
-  G->ws_bytes = G->off_prefix + (size_t)(batch + 1) * sizeof(int);
+  G->off_counters = G->off_prefix + ((size_t)(batch + 1) * sizeof(int) + 255) / 256 * 256;
+  G->ws_bytes = G->off_counters + (size_t)batch * L.H * sizeof(unsigned);
   return KVQ_OK;
 }
 
@@ -260,7 +271,8 @@ kvq_status check_decode_args(const kvq_layer_config* cfg, int32_t num_q_heads, i
 
 kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
                                 int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
-                                void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t s) {
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t s,
+                                void* out = nullptr, int32_t out_bf16 = 0, float* lse = nullptr) {
   LayerDesc L;
   kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
@@ -292,6 +304,12 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.ws_lse = reinterpret_cast<float*>(ws + G.off_lse);
   p.ws_prefix = reinterpret_cast<int*>(ws + G.off_prefix);
   p.status = dev_status;
+  p.warp_scratch = G.warp_scratch;
+  p.fuse = out != nullptr;
+  p.counters = reinterpret_cast<unsigned*>(ws + G.off_counters);
+  p.out = out;
+  p.out_bf16 = out_bf16;
+  p.lse = lse;
   cudaError_t e;
   switch (L.fmt) {
     case KVQ_FMT_INT2: e = launch_decode_int2(p, G.smem, s); break;
@@ -359,11 +377,9 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
   if (st != KVQ_OK) return st;
   if (out_bf16 != 0 && out_bf16 != 1) return KVQ_ERR_INVALID_ARG;
   if (batch > 0 && !out) return KVQ_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace, workspace_bytes,
-                            dev_status, s);
-  if (st != KVQ_OK) return st;
-  return decode_combine_impl(cfg, num_q_heads, batch, out, out_bf16, lse, workspace, workspace_bytes, s);
+  // one launch: the last CTA to finish each (sequence, kv head) merges its partials
+  return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
+                              workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), out, out_bf16, lse);
 }
 
 kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const int32_t* seq_lens,

@@ -40,6 +40,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t lo16) {
   return d;
 }
 
+// four E4M3FN bytes -> two f16x2 (bytes 0,1 -> lo; bytes 2,3 -> hi), exact
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // f32 pair -> packed f16 (lo in the low half), round to nearest even
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   uint32_t d;

@@ -50,6 +50,7 @@ constexpr float kSTau = 4.f;           // a Value scale may exceed its reference
 constexpr int kQStride = 36;           // floats per (head, lane-group) chunk of the query in smem
 constexpr int kBfRow = 272;            // bytes per bf16 row in the warp scratch (256 + 16 pad)
 constexpr int kWarpScratch = 16 * kBfRow;   // 4352 B: bf16 V tile, later the warp's merge record
+                                            // (smaller when the layer has no bf16 tiles: p.warp_scratch)
 constexpr int kMergeStride = 132;      // floats per head in the merge record: m, l, -, -, o[128]
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -157,8 +158,7 @@ __device__ __forceinline__ void unpack_k(const uint8_t* p, uint32_t (&R)[16]) {
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      R[2 * i + 0] = e4m3x2_to_f16x2(w[i] & 0xFFFFu);
-      R[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+      e4m3x4_to_f16x4(w[i], R[2 * i + 0], R[2 * i + 1]);
     }
   }
 }
@@ -181,8 +181,7 @@ __device__ __forceinline__ void unpack_v(const uint32_t (&W)[NWORDS], uint32_t& 
     b01 = int8_lo(W[JT]);
     b23 = int8_lo(W[JT] >> 8);
   } else {
-    b01 = e4m3x2_to_f16x2(W[JT] & 0xFFFFu);
-    b23 = e4m3x2_to_f16x2(W[JT] >> 16);
+    e4m3x4_to_f16x4(W[JT], b01, b23);
   }
 }
 
@@ -304,6 +303,14 @@ __device__ __forceinline__ void build_a_int(const float* qrow, const float* ks, 
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
+// final output of (sequence b, query head hq), channel c; l2 = log2-domain log-sum-exp
+__device__ __forceinline__ void write_out(const DecodeParams& p, int b, int hq, int c, float o, float l2) {
+  const long long oi = ((long long)b * p.Hq + hq) * 128 + c;
+  if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+  else reinterpret_cast<float*>(p.out)[oi] = o;
+  if (p.lse && c == 0) p.lse[(long long)b * p.Hq + hq] = l2 * 0.69314718055994531f;
+}
+
 struct SegInfo {
   int b, h;
   TokenSplit ts;
@@ -311,7 +318,7 @@ struct SegInfo {
 };
 
 template <int FMT, int NGV>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerDesc& L = p.L;
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
   float* q_s = reinterpret_cast<float*>(smem + off);
   off += 8 * 4 * kQStride * sizeof(float);
   uint8_t* scratch = smem + off;
-  off += kNW * kWarpScratch;
+  off += kNW * p.warp_scratch;
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
 
   if (tid == 0) {
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
 
   uint8_t* my_stages = stage_base + (size_t)warp * p.nst * p.stage_bytes;
   uint64_t* my_bars = bars + warp * kMaxStages;
-  uint8_t* my_scratch = scratch + warp * kWarpScratch;
+  uint8_t* my_scratch = scratch + warp * p.warp_scratch;
   uint32_t phase_bits = 0;  // expected parity of each of this warp's stage barriers
 
   // stage sub-buffer offsets
@@ -593,9 +600,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         if (alive) {
           const uint8_t* stg = my_stages + (size_t)s * p.stage_bytes;
           if constexpr (F::kInt) {
-            if (k == 0 || (((long long)qi * 16) % L.G) == 0)
+            // the group's A operand (q * s, hi/lo) is kept in the warp's shared scratch,
+            // 16 words per lane, and reloaded per tile (saves 32 registers)
+            uint4* afr = reinterpret_cast<uint4*>(my_scratch) + lane * 8;
+            if (k == 0 || (((long long)qi * 16) % L.G) == 0) {
               build_a_int<FMT>(qrow, reinterpret_cast<const float*>(stg + o_ks),
                                reinterpret_cast<const float*>(stg + o_kz), q, p.scale_log2, A, kfac, cterm);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) afr[i] = make_uint4(A[i][0], A[i][1], A[i][2], A[i][3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint4 v = afr[i];
+                A[i][0] = v.x; A[i][1] = v.y; A[i][2] = v.z; A[i][3] = v.w;
+              }
+            }
           }
           // ---- QK ----
           float acc[2][2][4];
@@ -622,21 +641,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
             const int t = nt * 8 + 2 * q + c;
             sig[e] = (t < tok_valid) ? fmaf(dot, kfac, cterm) : -INFINITY;
           }
-          // ---- Value scales of the lane's 4 tokens ----
-          float vs[4][NGV], vz[4][NGV];
+          // ---- largest Value scale of the lane's 4 tokens ----
+          const float* vsp = reinterpret_cast<const float*>(stg + o_vs);
+          const float* vzp = reinterpret_cast<const float*>(stg + o_vz);
           float smax = s_v8;
           if constexpr (F::kInt) {
-            const float* vsp = reinterpret_cast<const float*>(stg + o_vs);
-            const float* vzp = reinterpret_cast<const float*>(stg + o_vz);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int t = (e >> 1) * 8 + 2 * q + (e & 1);
 #pragma unroll
-              for (int j = 0; j < NGV; ++j) {
-                vs[e][j] = vsp[t * NGV + j];
-                vz[e][j] = vzp[t * NGV + j];
-                smax = fmaxf(smax, vs[e][j]);
-              }
+              for (int j = 0; j < NGV; ++j) smax = fmaxf(smax, vsp[t * NGV + j]);
             }
           }
           float pr[4];
@@ -688,8 +702,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
               float w[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                w[e] = (vs[e][j] * inv_s) * pr[e];
-                stt.zacc[j] = fmaf(w[e], kH - vz[e][j], stt.zacc[j]);
+                const int t = (e >> 1) * 8 + 2 * q + (e & 1);
+                w[e] = (vsp[t * NGV + j] * inv_s) * pr[e];
+                stt.zacc[j] = fmaf(w[e], kH - vzp[t * NGV + j], stt.zacc[j]);
               }
               uint32_t ah0, al0, ah1, al1;
               split_f16(w[0], w[1], ah0, al0);
@@ -753,28 +768,72 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
       }
     }
     __syncthreads();
-    // ---- merge the warps, write the partial of (b, h) ----
+    // ---- merge the warps; write the partial of (b, h), or the result when this CTA owns the pair ----
     {
-      const long long slot = (long long)blockIdx.x + (long long)b * H + h;
+      const long long pair = (long long)b * H + h;
+      const long long slot = (long long)blockIdx.x + pair;
+      const long long P0 = pair_start, P1 = pair_start + units;
+      const long long c_lo = ((P0 + 1) * C - 1) / U, c_hi = (P1 * C - 1) / U;
+      const bool whole = p.fuse && c_lo == c_hi;  // no other CTA touches this pair
       const float* recs = reinterpret_cast<const float*>(scratch);
       for (int i = tid; i < g * 128; i += kThreads) {
         const int hr = i >> 7, c = i & 127;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kNW; ++w) M = fmaxf(M, recs[w * (kWarpScratch / 4) + hr * kMergeStride]);
+        for (int w = 0; w < kNW; ++w) M = fmaxf(M, recs[w * (p.warp_scratch / 4) + hr * kMergeStride]);
         float Lsum = 0.f, O = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
           for (int w = 0; w < kNW; ++w) {
-            const float* rw = recs + w * (kWarpScratch / 4) + hr * kMergeStride;
+            const float* rw = recs + w * (p.warp_scratch / 4) + hr * kMergeStride;
             const float f = exp2f(rw[0] - M);  // 0 for an empty warp (m = -inf)
             Lsum = fmaf(rw[1], f, Lsum);
             O = fmaf(rw[4 + c], f, O);
           }
         }
         const bool empty = !(Lsum > 0.f);
-        p.ws_o[(slot * g + hr) * 128 + c] = empty ? 0.f : O / Lsum;
-        if (c == 0) p.ws_lse[slot * g + hr] = empty ? -INFINITY : M + log2f(Lsum);
+        const float o = empty ? 0.f : O / Lsum;
+        const float l2 = empty ? -INFINITY : M + log2f(Lsum);
+        if (whole) {
+          write_out(p, b, h * g + hr, c, o, l2);
+        } else {
+          p.ws_o[(slot * g + hr) * 128 + c] = o;
+          if (c == 0) p.ws_lse[slot * g + hr] = l2;
+        }
+      }
+      if (p.fuse && !whole) {
+        // the last CTA to finish this pair merges every partial of it
+        __shared__ int last_flag;
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+          int n = 0;
+          for (long long cc = c_lo; cc <= c_hi; ++cc) n += ((cc * U) / C != ((cc + 1) * U) / C);
+          const unsigned old = atomicAdd(&p.counters[pair], 1u);
+          last_flag = (old + 1u == (unsigned)n);
+          if (last_flag) p.counters[pair] = 0u;  // ready for the next call
+        }
+        __syncthreads();
+        if (last_flag) {
+          __threadfence();
+          for (int i = tid; i < g * 128; i += kThreads) {
+            const int hr = i >> 7, c = i & 127;
+            float M = -INFINITY;
+            for (long long cc = c_lo; cc <= c_hi; ++cc)
+              if ((cc * U) / C != ((cc + 1) * U) / C) M = fmaxf(M, __ldcg(&p.ws_lse[(cc + pair) * g + hr]));
+            float Lsum = 0.f, O = 0.f;
+            if (M != -INFINITY) {
+              for (long long cc = c_lo; cc <= c_hi; ++cc) {
+                if ((cc * U) / C == ((cc + 1) * U) / C) continue;
+                const float f = exp2f(__ldcg(&p.ws_lse[(cc + pair) * g + hr]) - M);
+                Lsum += f;
+                O = fmaf(f, __ldcg(&p.ws_o[((cc + pair) * g + hr) * 128 + c]), O);
+              }
+            }
+            const bool empty = !(Lsum > 0.f);
+            write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+          }
+        }
       }
     }
     __syncthreads();

@@ -54,6 +54,13 @@ struct DecodeParams {
   float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial
   int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
   uint32_t* status;
+  int warp_scratch;  // bytes of shared scratch per warp (bf16 tile staging / merge record)
+  // fused combine: the last CTA to finish a (sequence, kv head) pair merges its partials
+  int fuse;
+  unsigned* counters;  // [batch * H] arrival counters, zero between calls
+  void* out;
+  int out_bf16;
+  float* lse;
 };
 
 struct CombineParams {

@@ -160,7 +160,7 @@ class GpuLayer:
         out = torch.zeros((B, Hq, 128), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=self.device)
         lse = torch.zeros((B, Hq), dtype=torch.float32, device=self.device)
         wsb = self.kvq.decode_workspace_size(self.cfg, B, Hq)
-        ws = torch.empty(wsb, dtype=torch.uint8, device=self.device)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
         sl = self.seq_lens_dev(lens)
         sc = 1.0 / math.sqrt(128) if scale is None else scale
         self.kvq.decode_attention(self.cfg, self.layer.struct(), qd, Hq, sl, B, sc, out, out_bf16, lse, ws, wsb,

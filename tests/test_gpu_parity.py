@@ -189,3 +189,33 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(kvq.KvqError) as e:
         kvq.decode_attention(gl.cfg, gl.layer.struct(), qd, 2, sl, 1, 0.1, out, False, None, ws, wsb - 16)
     assert e.value.status == -4
+
+
+@pytest.mark.parametrize("fmt,lens", [("int4", [2000, 700, 33]), ("fp8_e4m3", [4000, 17, 900])])
+def test_fused_combine_equals_two_launches_and_repeats(fmt, lens):
+    # kvq_decode_attention merges partials inside the decode launch (arrival counters in the
+    # workspace); kvq_decode_partials + kvq_decode_combine do it in two launches.  Same bits,
+    # and the counters are back at zero after every call.
+    from quantized_kv_cache_decode_gb300 import kvq
+    G = 1 if fmt == "fp8_e4m3" else 32
+    gl, caches, q = build(fmt, 2, 4, lens, G, 128, 32 if G > 1 else 0, 0, False, 21)
+    o1, l1 = gl.decode(q)
+    B, Hq = len(lens), 8
+    qd = torch.from_numpy(q.astype(np.int16)).cuda()
+    wsb = kvq.decode_workspace_size(gl.cfg, B, Hq)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    sl = gl.seq_lens_dev()
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        kvq.decode_attention(gl.cfg, gl.layer.struct(), qd, Hq, sl, B, 1 / math.sqrt(128), out, False, lse, ws, wsb)
+        torch.cuda.synchronize()
+        assert torch.equal(out, o1) and torch.equal(lse, l1)
+    cnt = ws[-B * 2 * 4:].view(torch.int32)
+    assert int(cnt.abs().sum()) == 0
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    kvq.decode_partials(gl.cfg, gl.layer.struct(), qd, Hq, sl, B, 1 / math.sqrt(128), ws, wsb)
+    kvq.decode_combine(gl.cfg, Hq, B, out2, False, lse2, ws, wsb)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, o1) and torch.equal(lse2, l1)
