@@ -391,6 +391,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
 
   const long long U = prefix[B];
   const long long C = p.num_ctas;
+  if (p.fuse) {
+    // sequences without tokens belong to no CTA's range: out = 0, lse = -inf
+    for (int b = blockIdx.x; b < B; b += gridDim.x)
+      if (prefix[b + 1] == prefix[b])
+        for (int i = tid; i < p.Hq * 128; i += kThreads) write_out(p, b, i >> 7, i & 127, 0.f, -INFINITY);
+  }
   const long long st = (long long)blockIdx.x * U / C;
   const long long en = (long long)(blockIdx.x + 1) * U / C;
 
