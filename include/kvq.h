@@ -252,6 +252,33 @@ kvq_status kvq_decode_combine(const kvq_layer_config* cfg, int32_t num_q_heads, 
                               void* stream);
 
 /*
+ * kvq_decode_attention_static_scratch -- kvq_decode_attention for callers that
+ * cannot allocate device memory.  (The pages have no counterpart to this call:
+ * it exists for integration, not for the method.)
+ * Who needs it: code hosted in an application that owns all device memory
+ * through its own pool and forbids direct cudaMalloc, loops that cannot accept
+ * the device-wide synchronisation an allocation may cause, or plug-ins with no
+ * allocator at hand.  Instead of a caller workspace it uses one fixed array of
+ * 8 MiB in device global memory inside libkvq, reserved on every GPU that
+ * loads the library until the process exits.  Inputs and outputs are the
+ * caller's, as for kvq_decode_attention (same arguments minus the workspace).
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library call.
+ *   - Returns KVQ_ERR_WORKSPACE when kvq_decode_workspace_size() for this
+ *     config, batch and query-head count exceeds 8 MiB (large batch x heads).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero.  Calls that overlap on the
+ *     GPU (other streams, other threads) race on it: serialise them.
+ *   - Runs as two launches (split pass, then merge).
+ */
+kvq_status kvq_decode_attention_static_scratch(const kvq_layer_config* cfg, const kvq_layer_cache* cache,
+                                               const void* q, int32_t num_q_heads, const int32_t* seq_lens,
+                                               int32_t batch, float softmax_scale, void* out, int32_t out_bf16,
+                                               float* lse, uint32_t* dev_status, void* stream);
+
+/*
  * kvq_dequantize -- export the dequantized cache as fp32.
  * Source: [KVQA] s2 (x_hat = s(q - z)), s4 (FP8 value times its scale).
  *   k_out, v_out  device f32 [batch][H][max_tokens][d]; token t < seq_lens[b]

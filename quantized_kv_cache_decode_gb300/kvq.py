@@ -62,11 +62,14 @@ _lib.kvq_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i
 _lib.kvq_decode_partials.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
                                      c_vp, c_sz, c_vp, c_vp]
 _lib.kvq_decode_combine.argtypes = [_P(LayerConfig), c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]
+_lib.kvq_decode_attention_static_scratch.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32,
+                                                     ctypes.c_float, c_vp, c_i32, c_vp, c_vp, c_vp]
 _lib.kvq_dequantize.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]
 _lib.kvq_status_string.argtypes = [c_i32]
 _lib.kvq_status_string.restype = ctypes.c_char_p
 for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_quantize_append", "kvq_decode_workspace_size",
-            "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize"):
+            "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize",
+            "kvq_decode_attention_static_scratch"):
     getattr(_lib, _fn).restype = c_i32
 
 
@@ -157,6 +160,16 @@ def decode_combine(cfg: LayerConfig, num_q_heads: int, batch: int, out, out_bf16
     _check("kvq_decode_combine",
            _lib.kvq_decode_combine(ctypes.byref(cfg), num_q_heads, batch, _ptr(out), int(out_bf16), _ptr(lse),
                                    _ptr(workspace), workspace_bytes, _stream_ptr(stream)))
+
+
+def decode_attention_static_scratch(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, seq_lens, batch: int,
+                                    softmax_scale: float, out, out_bf16: bool, lse, dev_status=None,
+                                    stream=None) -> None:
+    """Decode attention using the library's fixed device scratch instead of a workspace (allocates nothing)."""
+    _check("kvq_decode_attention_static_scratch",
+           _lib.kvq_decode_attention_static_scratch(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads,
+                                                    _ptr(seq_lens), batch, softmax_scale, _ptr(out), int(out_bf16),
+                                                    _ptr(lse), _ptr(dev_status), _stream_ptr(stream)))
 
 
 def dequantize(cfg: LayerConfig, cache: LayerCache, seq_lens, batch: int, max_tokens: int, k_out, v_out,
