@@ -99,6 +99,28 @@ def step_bytes(w, lens_after, n_app):
 
 
 # --------------------------------------------------------------------------- #
+# multi-rank aggregation (weak scaling: every rank runs its own replica)
+# --------------------------------------------------------------------------- #
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job GB/s: the bytes all ranks processed per step over the slowest rank's step time."""
+    return bytes_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e9
+
+
+# --------------------------------------------------------------------------- #
 # clocks
 # --------------------------------------------------------------------------- #
 
@@ -316,10 +338,7 @@ def run_gpu(args, w, rank, world):
     barrier()
     ms = t_start.elapsed_time(t_end)
     kern_ms = [evs[i][0][j].elapsed_time(evs[i][1][j]) for i in range(K) for j in range(nl)]
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_step = ms / K
     # ---- end to end through the public API, host buffers, copies inside the timed region ----
     E = args.e2e_steps or K
@@ -352,10 +371,7 @@ def run_gpu(args, w, rank, world):
         e2e_step()
     torch.cuda.synchronize()
     e_ms = (time.perf_counter() - e0) * 1e3 / E
-    if dist:
-        t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e_ms, dev)
     clocks = None
     if clk:
         clk.stop()
@@ -516,7 +532,7 @@ def main():
         torch.distributed.destroy_process_group()
     if rank != 0:
         return
-    gbs = r["sbytes"] * world / (r["ms_step"] * 1e-3) / 1e9
+    gbs = job_throughput(r["sbytes"], r["ms_step"], world)
     kern_gbs = r["attn_bytes_first_layer"] / (r["kern_ms"] * 1e-3) / 1e9 if len(w.layer_formats) == 1 else None
     if kern_gbs is None:
         # multi-layer: bytes of every layer's attention over the mean launch duration
@@ -540,7 +556,7 @@ def main():
                      "frac": round(kern_gbs / hbm_peak, 4), "traffic": traffic,
                      "kernel": "decode_kernel (split pass)", "peak_source": peak_src,
                      "mean_launch_us": round(r["kern_ms"] * 1e3, 2)},
-        "e2e": {"value": round(r["sbytes"] * world / (r["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_throughput(r["sbytes"], r["e2e_ms"], world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 4)},
         "gpu_launches": count_launches(w) * args.steps,
         "clocks": r["clocks"],
