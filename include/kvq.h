@@ -90,23 +90,27 @@ typedef struct {
 /*
  * Device buffers of one layer's cache.  Which fields are used depends on the
  * config; unused fields may be NULL.  With B = sequences, H = num_kv_heads,
- * d = 128, b = bits (8 for FP8), rb = d*b/8 bytes per token row, W = R + G:
+ * d = 128, b = bits (8 for FP8), rb = d*b/8 bytes per token row, W = R + G,
+ * ngv = d / Gv.  Only quantized tokens x = t - S live in the quantized store.
  *
- * Contiguous store (paged == 0), cap = capacity_tokens, per (seq, head) in
- * [B][H] order:
- *   k_codes  u8  [B][H][cap][rb]       token x's row; channel c in byte c/(8/b) at bit (c mod (8/b))*b
- *   v_codes  u8  [B][H][cap/16][16*rb] 16-token tiles in "fragment order" (below)
- *   k_scale  f32 [B][H][cap/G][d]      per-channel scale of each G-token Key group   (INT only)
- *   k_zero   f32 [B][H][cap/G][d]      per-channel zero-point                         (INT only)
- *   v_scale  f32 [B][H][cap][d/Gv]     per-token scale of each Gv-channel Value group (INT only)
- *   v_zero   f32 [B][H][cap][d/Gv]                                                    (INT only)
- * Paged store (paged == 1), P = block_tokens: block_pool holds num_blocks blocks
- * of H head slabs; a slab is, in this order:
- *   K codes [P][rb], V codes [P/16][16*rb] (fragment order),
- *   K scale [P/G][d] f32, K zero [P/G][d] f32, V scale [P][d/Gv] f32, V zero [P][d/Gv] f32
- *   (scales and zeros only for INT formats).  Quantized token x (= t - S) of
- *   sequence b lives in block block_table[b*max_blocks_per_seq + x/P], row x mod P.
- * Both stores index quantized tokens x = t - S only.
+ * A 16-token tile (quantized tokens 16i .. 16i+15) is, in this order:
+ *   K codes  [16][rb]     token row; channel c in byte c/(8/b) at bit (c mod (8/b))*b
+ *   V codes  [16*rb]      in "fragment order" (below)
+ *   V scale  [16][ngv] f32, V zero [16][ngv] f32   (INT only: per token, per Gv channels)
+ * tile_bytes = 32*rb (+ 128*ngv for INT).
+ * A record is a header followed by tpg consecutive tiles:
+ *   INT: header = K scale [d] f32, K zero [d] f32 (the per-channel Key group of
+ *        G = 16*tpg tokens, 1024 bytes); tpg = G/16
+ *   FP8: no header; tpg = 1 (contiguous) or P/16 (paged)
+ * record_bytes = header + tpg * tile_bytes.  A run of consecutive tiles is one
+ * contiguous byte range, so the decode kernel fetches it with one bulk copy.
+ *
+ * Contiguous store (paged == 0): qstore holds, for each (seq, head) in [B][H]
+ * order, cap/(16*tpg) records (cap = capacity_tokens).
+ * Paged store (paged == 1), P = block_tokens: block_pool holds num_blocks
+ * blocks; a block is H records, one per head (INT: P == G, so one Key group per
+ * block).  Quantized token x of sequence b lives in block
+ * block_table[b*max_blocks_per_seq + x/P].
  * bf16 parts (both stores):
  *   resid_k, resid_v  bf16 [B][H][W][d]  residual token t in slot (t - S) mod W
  *   sink_k,  sink_v   bf16 [B][H][S][d]
@@ -123,14 +127,9 @@ typedef struct {
  * directly into tensor-core operand registers.
  */
 typedef struct {
-  void* k_codes;
-  void* v_codes;
-  float* k_scale;
-  float* k_zero;
-  float* v_scale;
-  float* v_zero;
-  void* block_pool;
-  const int32_t* block_table;
+  void* qstore;               /* contiguous quantized store (paged == 0) */
+  void* block_pool;           /* paged quantized store (paged == 1) */
+  const int32_t* block_table; /* paged: int32 [B][max_blocks_per_seq] */
   void* resid_k;
   void* resid_v;
   void* sink_k;
@@ -141,12 +140,7 @@ typedef struct {
 
 /* Indices of kvq_cache_layout()'s output array. */
 enum {
-  KVQ_FIELD_K_CODES = 0,
-  KVQ_FIELD_V_CODES,
-  KVQ_FIELD_K_SCALE,
-  KVQ_FIELD_K_ZERO,
-  KVQ_FIELD_V_SCALE,
-  KVQ_FIELD_V_ZERO,
+  KVQ_FIELD_QSTORE = 0,
   KVQ_FIELD_BLOCK_POOL,
   KVQ_FIELD_RESID_K,
   KVQ_FIELD_RESID_V,

@@ -14,7 +14,8 @@ namespace {
 constexpr int kThreadsDecode = 128;  // 4 warps (kvq_decode.cuh)
 constexpr int kMaxStages = 4;
 constexpr int kWarpScratch = 16 * 272;
-constexpr int kSmemPerCtaTarget = 74 * 1024;  // three resident CTAs per SM
+constexpr int kSmem3PerSm = 74 * 1024;          // per-CTA budget for three resident CTAs per SM
+constexpr int kSmem2PerSm = 112 * 1024;         // ... for two
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -50,44 +51,29 @@ kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
   }
   L->ngv = L->d / L->Gv;
   L->paged = cfg->paged ? 1 : 0;
+  L->tile_bytes = 32 * L->rb + (L->fp8 ? 0 : 128 * L->ngv);
+  L->hdr_bytes = L->fp8 ? 0 : 2 * L->d * 4;
   if (L->paged) {
     L->P = cfg->block_tokens;
     L->num_blocks = cfg->num_blocks;
     L->mbps = cfg->max_blocks_per_seq;
     if (L->P < 16 || L->P % 16 != 0 || L->num_blocks < 1 || L->mbps < 1) return KVQ_ERR_INVALID_ARG;
     if (!L->fp8 && L->P != L->G) return KVQ_ERR_INVALID_ARG;
-    long long off = 0;
-    L->off_kc = 0;
-    off += (long long)L->P * L->rb;
-    L->off_vc = (int)off;
-    off += (long long)L->P * L->rb;
-    if (!L->fp8) {
-      L->off_ks = (int)off;
-      off += (long long)(L->P / L->G) * L->d * 4;
-      L->off_kz = (int)off;
-      off += (long long)(L->P / L->G) * L->d * 4;
-      L->off_vs = (int)off;
-      off += (long long)L->P * L->ngv * 4;
-      L->off_vz = (int)off;
-      off += (long long)L->P * L->ngv * 4;
-    }
-    L->slab_bytes = (off + 15) / 16 * 16;
-    L->block_bytes = L->slab_bytes * L->H;
+    L->tpg = L->P / 16;
   } else {
     L->cap = cfg->capacity_tokens;
     if (L->cap < 0 || L->cap % 16 != 0 || (!L->fp8 && L->cap % L->G != 0)) return KVQ_ERR_INVALID_ARG;
+    L->tpg = L->fp8 ? 1 : L->G / 16;
   }
+  L->rec_bytes = L->hdr_bytes + L->tpg * L->tile_bytes;
+  L->nrec = L->paged ? 0 : L->cap / (16 * L->tpg);
+  L->block_bytes = (long long)L->rec_bytes * L->H;
   return KVQ_OK;
 }
 
 CachePtrs make_ptrs(const kvq_layer_cache* c) {
   CachePtrs p;
-  p.k_codes = c->k_codes;
-  p.v_codes = c->v_codes;
-  p.k_scale = c->k_scale;
-  p.k_zero = c->k_zero;
-  p.v_scale = c->v_scale;
-  p.v_zero = c->v_zero;
+  p.qstore = c->qstore;
   p.block_pool = c->block_pool;
   p.block_table = c->block_table;
   p.resid_k = c->resid_k;
@@ -106,9 +92,7 @@ kvq_status check_cache(const LayerDesc& L, const kvq_layer_cache* c) {
   if (L.paged) {
     if (!need(c->block_pool) || !c->block_table) return KVQ_ERR_INVALID_ARG;
   } else if (L.cap > 0) {
-    if (!need(c->k_codes) || !need(c->v_codes)) return KVQ_ERR_INVALID_ARG;
-    if (!L.fp8 && (!need(c->k_scale) || !need(c->k_zero) || !need(c->v_scale) || !need(c->v_zero)))
-      return KVQ_ERR_INVALID_ARG;
+    if (!need(c->qstore)) return KVQ_ERR_INVALID_ARG;
   }
   if (!L.fp8 && (!need(c->resid_k) || !need(c->resid_v))) return KVQ_ERR_INVALID_ARG;
   if (L.S > 0 && (!need(c->sink_k) || !need(c->sink_v))) return KVQ_ERR_INVALID_ARG;
@@ -116,10 +100,20 @@ kvq_status check_cache(const LayerDesc& L, const kvq_layer_cache* c) {
   return KVQ_OK;
 }
 
+// Quantized tiles per pipeline stage: about 8 KB of cache bytes per stage.
+int tiles_per_stage(const LayerDesc& L) {
+  const int per = L.tile_bytes + (L.hdr_bytes + L.tpg - 1) / L.tpg;
+  return std::max(1, std::min(8, (8192 + per / 2) / per));
+}
+
+// A stage holds a header slot, tps tiles and the record headers between them,
+// or one half (K or V rows) of a 16-token bf16 tile at 272 bytes per row.
 int stage_bytes_of(const LayerDesc& L) {
-  int b = 2 * 16 * L.rb;
-  if (!L.fp8) b += 128 * L.ngv + 1024;
-  return b;
+  const int tps = tiles_per_stage(L);
+  const int inline_hdrs = (tps + L.tpg - 1) / L.tpg;
+  const int q = L.hdr_bytes + tps * L.tile_bytes + inline_hdrs * L.hdr_bytes;
+  const int bf = 16 * 272;
+  return (std::max(q, bf) + 127) / 128 * 128;
 }
 
 // Shared scratch per warp: a padded bf16 tile when the layer keeps bf16 tokens
@@ -130,9 +124,12 @@ int warp_scratch_of(const LayerDesc& L, int g) {
   return bf16_tiles ? std::max(kWarpScratch, merge) : merge;
 }
 
+constexpr int kSegTableBytes = 16 * 48;  // kMaxSeg segment records of 48 bytes (kvq_decode.cuh)
+
 int fixed_smem(int batch, int warp_scratch) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16;
-  return kThreadsDecode / 32 * kMaxStages * 8 + 8 * 4 * 36 * 4 + kThreadsDecode / 32 * warp_scratch + prefix;
+  return kThreadsDecode / 32 * kMaxStages * 8 + 8 * 4 * 36 * 4 + kThreadsDecode / 32 * warp_scratch +
+         kSegTableBytes + prefix;
 }
 
 cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
@@ -153,12 +150,23 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) 
   const int sb = stage_bytes_of(L);
   const int wsc = warp_scratch_of(L, g);
   const int fixed = fixed_smem(batch, wsc);
-  int nst = kMaxStages;
-  while (nst > 2 && fixed + (kThreadsDecode / 32) * nst * sb > kSmemPerCtaTarget) --nst;
-  const int smem = fixed + (kThreadsDecode / 32) * nst * sb;
+  // As many stages as fit three CTAs per SM; if the kernel's registers allow only two
+  // CTAs per SM anyway, spend the shared memory of the third on deeper pipelines.
+  auto fit = [&](int budget) {
+    int n = kMaxStages;
+    while (n > 2 && fixed + (kThreadsDecode / 32) * n * sb > budget) --n;
+    return fixed + (kThreadsDecode / 32) * n * sb <= budget ? n : 0;
+  };
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  int nst = fit(kSmem3PerSm);
+  if (nst) {
+    if (occupancy(L, fixed + (kThreadsDecode / 32) * nst * sb, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (per_sm < 3) nst = 0;
+  }
+  if (nst == 0) nst = std::max(2, fit(kSmem2PerSm));
+  const int smem = fixed + (kThreadsDecode / 32) * nst * sb;
   if (occupancy(L, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
   if (per_sm < 1) return KVQ_ERR_UNSUPPORTED;
   G->smem = smem;
@@ -193,14 +201,7 @@ kvq_status kvq_cache_layout(const kvq_layer_config* cfg, int32_t num_seqs, size_
   if (L.paged) {
     bytes[KVQ_FIELD_BLOCK_POOL] = (size_t)L.num_blocks * L.block_bytes;
   } else {
-    bytes[KVQ_FIELD_K_CODES] = pairs * L.cap * L.rb;
-    bytes[KVQ_FIELD_V_CODES] = pairs * L.cap * L.rb;
-    if (!L.fp8) {
-      bytes[KVQ_FIELD_K_SCALE] = pairs * (L.cap / L.G) * L.d * sizeof(float);
-      bytes[KVQ_FIELD_K_ZERO] = bytes[KVQ_FIELD_K_SCALE];
-      bytes[KVQ_FIELD_V_SCALE] = pairs * L.cap * L.ngv * sizeof(float);
-      bytes[KVQ_FIELD_V_ZERO] = bytes[KVQ_FIELD_V_SCALE];
-    }
+    bytes[KVQ_FIELD_QSTORE] = pairs * L.nrec * L.rec_bytes;
   }
   if (!L.fp8) {
     bytes[KVQ_FIELD_RESID_K] = pairs * L.W * L.d * 2;
@@ -296,9 +297,9 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.num_ctas = G.num_ctas;
   p.nst = G.nst;
   p.stage_bytes = G.stage_bytes;
+  p.tps = tiles_per_stage(L);
   // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
-  const int qbytes = 2 * 16 * L.rb + (L.fp8 ? 0 : 128 * L.ngv);
-  p.bf_weight = std::max(1, (8192 + qbytes / 2) / qbytes);
+  p.bf_weight = std::max(1, (8192 + L.tile_bytes / 2) / L.tile_bytes);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_o = reinterpret_cast<float*>(ws);
   p.ws_lse = reinterpret_cast<float*>(ws + G.off_lse);

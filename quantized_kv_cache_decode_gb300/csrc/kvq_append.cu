@@ -37,44 +37,10 @@ __device__ __forceinline__ uint32_t affine_code(float x, float s, float z, int l
   return (uint32_t)qv;
 }
 
-struct GroupDst {
-  uint8_t* kc;    // K codes of the group's first token (rows of rb bytes)
-  uint8_t* vc;    // V tiles of the group (16-token tiles, fragment order)
-  float *ks, *kz; // K scale / zero rows (d floats)
-  float *vs, *vz; // V scale / zero rows of the group's first token (ngv floats per token)
-  bool ok;
-};
-
-__device__ GroupDst group_dst(const LayerDesc& L, const CachePtrs& C, int b, int h, long long x0, uint32_t* status) {
-  GroupDst g;
-  g.ok = true;
-  if (L.paged) {
-    const long long bi = x0 / L.P;
-    const int row = (int)(x0 - bi * L.P);
-    const int blk = C.block_table[(long long)b * L.mbps + bi];
-    if (blk < 0 || blk >= L.num_blocks) {
-      report(status, KVQ_DEV_BAD_BLOCK);
-      g.ok = false;
-      return g;
-    }
-    uint8_t* slab = reinterpret_cast<uint8_t*>(C.block_pool) + (long long)blk * L.block_bytes +
-                    (long long)h * L.slab_bytes;
-    g.kc = slab + L.off_kc + (long long)row * L.rb;
-    g.vc = slab + L.off_vc + (long long)(row / 16) * 16 * L.rb;
-    g.ks = reinterpret_cast<float*>(slab + L.off_ks) + (long long)(row / L.G) * L.d;
-    g.kz = reinterpret_cast<float*>(slab + L.off_kz) + (long long)(row / L.G) * L.d;
-    g.vs = reinterpret_cast<float*>(slab + L.off_vs) + (long long)row * L.ngv;
-    g.vz = reinterpret_cast<float*>(slab + L.off_vz) + (long long)row * L.ngv;
-  } else {
-    const long long pair = (long long)b * L.H + h;
-    g.kc = reinterpret_cast<uint8_t*>(C.k_codes) + (pair * L.cap + x0) * L.rb;
-    g.vc = reinterpret_cast<uint8_t*>(C.v_codes) + (pair * L.cap + (x0 / 16) * 16) * L.rb;
-    g.ks = C.k_scale ? C.k_scale + (pair * (L.cap / L.G) + x0 / L.G) * L.d : nullptr;
-    g.kz = C.k_zero ? C.k_zero + (pair * (L.cap / L.G) + x0 / L.G) * L.d : nullptr;
-    g.vs = C.v_scale ? C.v_scale + (pair * L.cap + x0) * L.ngv : nullptr;
-    g.vz = C.v_zero ? C.v_zero + (pair * L.cap + x0) * L.ngv : nullptr;
-  }
-  return g;
+// Writable record r of (b, h); nullptr (reported) for a bad block.
+__device__ __forceinline__ uint8_t* record_w(const LayerDesc& L, const CachePtrs& C, int b, int h, long long r,
+                                             uint32_t* status) {
+  return const_cast<uint8_t*>(record_addr(L, C, b, h, r, status));
 }
 
 // One CTA per (sequence, kv head).  Dynamic smem: K and V of one group as fp32
@@ -105,15 +71,17 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
     const long long first = T0 > L.S ? T0 : (long long)L.S;
     for (long long t = first; t < T1; ++t) {
       const long long x = t - L.S;
-      const GroupDst g = group_dst(L, p.C, b, h, x, tid == 0 ? p.status : nullptr);
-      if (!g.ok) continue;
+      const long long i = x / 16;
+      uint8_t* rec = record_w(L, p.C, b, h, i / L.tpg, tid == 0 ? p.status : nullptr);
+      if (!rec) continue;
+      uint8_t* tile = rec + L.hdr_bytes + (long long)(i % L.tpg) * L.tile_bytes;
       const int c = tid;
       const float kx = __bfloat162float(knew[(t - T0) * L.d + c]);
       const float vx = __bfloat162float(vnew[(t - T0) * L.d + c]);
-      g.kc[c] = f32_to_e4m3(__fdiv_rn(kx, sk));
+      tile[(x % 16) * L.rb + c] = f32_to_e4m3(__fdiv_rn(kx, sk));
       int byte, bit;
       vtile_pos(8, true, (int)(x % 16), c, byte, bit);
-      g.vc[byte] = f32_to_e4m3(__fdiv_rn(vx, sv));
+      tile[16 * L.rb + byte] = f32_to_e4m3(__fdiv_rn(vx, sv));
     }
   } else {
     const int G = L.G, levels = (1 << L.bits) - 1;
@@ -143,8 +111,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
         vf[i] = vx;
       }
       __syncthreads();
-      const GroupDst g = group_dst(L, p.C, b, h, x0, tid == 0 ? p.status : nullptr);
-      if (g.ok) {
+      // the group is record grp (G = 16 * tpg tokens): header = K scale, K zero; then G/16 tiles
+      uint8_t* rec = record_w(L, p.C, b, h, grp, tid == 0 ? p.status : nullptr);
+      if (rec) {
+        float* ks = reinterpret_cast<float*>(rec);
+        float* kz = ks + 128;
         // Keys: per channel over the G tokens (thread = channel)
         {
           const int c = tid;
@@ -156,8 +127,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
           float z;
           const float s = affine_params(mn, mx, flev, z);
           for (int tt = 0; tt < G; ++tt) kq[tt * 128 + c] = (uint8_t)affine_code(kf[tt * 128 + c], s, z, levels);
-          g.ks[c] = s;
-          g.kz[c] = z;
+          ks[c] = s;
+          kz[c] = z;
         }
         // Values: per token over Gv channels
         for (int item = tid; item < G * L.ngv; item += kAppendThreads) {
@@ -172,16 +143,17 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
           const float s = affine_params(mn, mx, flev, z);
           uint8_t* qrow = vq + tt * 128 + j * L.Gv;
           for (int c = 0; c < L.Gv; ++c) qrow[c] = (uint8_t)affine_code(row[c], s, z, levels);
-          g.vs[(long long)tt * L.ngv + j] = s;
-          g.vz[(long long)tt * L.ngv + j] = z;
+          float* tvs = reinterpret_cast<float*>(rec + L.hdr_bytes + (long long)(tt / 16) * L.tile_bytes + 32 * L.rb);
+          tvs[(tt % 16) * L.ngv + j] = s;
+          tvs[16 * L.ngv + (tt % 16) * L.ngv + j] = z;
         }
         __syncthreads();
-        // K codes, packed little-endian along d
+        // K codes, packed little-endian along d, 16 rows per tile
         for (int i = tid; i < G * L.rb; i += kAppendThreads) {
           const int tt = i / L.rb, kb = i % L.rb;
           uint32_t v = 0;
           for (int e = 0; e < per_byte; ++e) v |= (uint32_t)kq[tt * 128 + kb * per_byte + e] << (e * L.bits);
-          g.kc[(long long)tt * L.rb + kb] = (uint8_t)v;
+          rec[L.hdr_bytes + (long long)(tt / 16) * L.tile_bytes + (tt % 16) * L.rb + kb] = (uint8_t)v;
         }
         // V codes, 16-token tiles in fragment order
         const int tile_words = 16 * L.rb / 4;
@@ -195,7 +167,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
             atomicOr(&tile[byte >> 2], (uint32_t)vq[(t16 * 16 + tt) * 128 + c] << ((byte & 3) * 8 + bit));
           }
           __syncthreads();
-          uint32_t* dst = reinterpret_cast<uint32_t*>(g.vc + (long long)t16 * 16 * L.rb);
+          uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes + 16 * L.rb);
           for (int i = tid; i < tile_words; i += kAppendThreads) dst[i] = tile[i];
           __syncthreads();
         }

@@ -180,50 +180,26 @@ __host__ __device__ __forceinline__ long long max_tokens(const LayerDesc& L) {
   return L.S + qcap + L.R + L.G - 1;
 }
 
-// Addresses of quantized token x of (b, h): codes row, V tile, scale rows.
-struct QuantAddr {
-  const uint8_t* kc;  // K codes row of token x
-  const uint8_t* vt;  // V tile holding x (fragment order)
-  const float* ks;    // K scale row of x's group (INT)
-  const float* kz;
-  const float* vs;  // V scale row of token x (INT)
-  const float* vz;
-  bool ok;
-};
-
-__device__ __forceinline__ QuantAddr quant_addr(const LayerDesc& L, const CachePtrs& C, int b, int h, long long x,
-                                                uint32_t* status) {
-  QuantAddr a;
-  a.ok = true;
+// Record r of (sequence b, kv head h) in the quantized store, or nullptr (with
+// KVQ_DEV_BAD_BLOCK reported) when its block-table entry is outside the pool.
+// A record is [header (INT: K scale, K zero)][tpg tiles]; see include/kvq.h.
+__device__ __forceinline__ const uint8_t* record_addr(const LayerDesc& L, const CachePtrs& C, int b, int h,
+                                                     long long r, uint32_t* status) {
   if (L.paged) {
-    const long long bi = x / L.P;
-    const int row = (int)(x - bi * L.P);
-    const int blk = C.block_table[(long long)b * L.mbps + bi];
+    const int blk = C.block_table[(long long)b * L.mbps + r];
     if (blk < 0 || blk >= L.num_blocks) {
       report(status, KVQ_DEV_BAD_BLOCK);
-      a.ok = false;
-      a.kc = a.vt = nullptr;
-      a.ks = a.kz = a.vs = a.vz = nullptr;
-      return a;
+      return nullptr;
     }
-    const uint8_t* slab = reinterpret_cast<const uint8_t*>(C.block_pool) + (long long)blk * L.block_bytes +
-                          (long long)h * L.slab_bytes;
-    a.kc = slab + L.off_kc + (long long)row * L.rb;
-    a.vt = slab + L.off_vc + (long long)(row / 16) * 16 * L.rb;
-    a.ks = reinterpret_cast<const float*>(slab + L.off_ks) + (long long)(row / L.G) * L.d;
-    a.kz = reinterpret_cast<const float*>(slab + L.off_kz) + (long long)(row / L.G) * L.d;
-    a.vs = reinterpret_cast<const float*>(slab + L.off_vs) + (long long)row * L.ngv;
-    a.vz = reinterpret_cast<const float*>(slab + L.off_vz) + (long long)row * L.ngv;
-  } else {
-    const long long pair = (long long)b * L.H + h;
-    a.kc = reinterpret_cast<const uint8_t*>(C.k_codes) + (pair * L.cap + x) * L.rb;
-    a.vt = reinterpret_cast<const uint8_t*>(C.v_codes) + (pair * L.cap + (x / 16) * 16) * L.rb;
-    a.ks = C.k_scale ? C.k_scale + (pair * (L.cap / L.G) + x / L.G) * L.d : nullptr;
-    a.kz = C.k_zero ? C.k_zero + (pair * (L.cap / L.G) + x / L.G) * L.d : nullptr;
-    a.vs = C.v_scale ? C.v_scale + (pair * L.cap + x) * L.ngv : nullptr;
-    a.vz = C.v_zero ? C.v_zero + (pair * L.cap + x) * L.ngv : nullptr;
+    return reinterpret_cast<const uint8_t*>(C.block_pool) + (long long)blk * L.block_bytes +
+           (long long)h * L.rec_bytes;
   }
-  return a;
+  return reinterpret_cast<const uint8_t*>(C.qstore) + (((long long)b * L.H + h) * L.nrec + r) * L.rec_bytes;
+}
+
+// Tile i (quantized tokens 16i .. 16i+15) inside its record.
+__device__ __forceinline__ const uint8_t* tile_in_record(const LayerDesc& L, const uint8_t* rec, long long i) {
+  return rec + L.hdr_bytes + (long long)(i % L.tpg) * L.tile_bytes;
 }
 
 // bf16 row of bf16-list token index xb (sink tokens first, then residual tokens in order)

@@ -195,6 +195,7 @@ struct WarpState {
   float m;           // reference max (log2 domain)
   float l;           // sum of p (thread-partial)
   float S;           // reference Value scale
+  float inv_S;       // 1 / S
 };
 
 template <int NGV>
@@ -208,15 +209,24 @@ __device__ __forceinline__ void state_init(WarpState<NGV>& st) {
   st.m = -INFINITY;
   st.l = 0.f;
   st.S = 0.f;
+  st.inv_S = 0.f;
 }
 
-// Update the running max / scale references for a tile with scores sig[4]
-// (tokens 2q, 2q+1, 8+2q, 9+2q of head r; -inf when masked) and the lane's
-// largest Value scale smax; return p[4] * kPrescale and 1 / S.  A token's PV
-// weight is then (s_t / S) * (p_t * kPrescale) <= 4 * 2^6 * 64 = 2^14.
-template <int NGV>
-__device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&sig)[4], float smax, float (&pr)[4]) {
-  float tmax = fmaxf(fmaxf(sig[0], sig[1]), fmaxf(sig[2], sig[3]));
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Update the running max / scale references for a stage with scores sig[N]
+// (the lane's tokens of head r, 4 per 16-token tile; -inf when masked) and the
+// lane's largest Value scale smax; return p[N] * kPrescale and 1 / S.  A token's
+// PV weight is then (s_t / S) * (p_t * kPrescale) <= 4 * 2^6 * 64 = 2^14.
+template <int NGV, int N>
+__device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&sig)[N], float smax, float (&pr)[N]) {
+  float tmax = sig[0];
+#pragma unroll
+  for (int e = 1; e < N; ++e) tmax = fmaxf(tmax, sig[e]);
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
   smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
@@ -226,7 +236,7 @@ __device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&
   if (__any_sync(kFull, bump_m || bump_s)) {
     const float m_new = bump_m ? tmax : st.m;
     const float S_new = bump_s ? smax : st.S;
-    const float a = (st.m == -INFINITY) ? 0.f : exp2f(st.m - m_new);
+    const float a = (st.m == -INFINITY) ? 0.f : fast_exp2(st.m - m_new);
     const float ao = (S_new > 0.f) ? a * (st.S / S_new) : 0.f;
     st.l *= a;
 #pragma unroll
@@ -237,13 +247,17 @@ __device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&
     for (int j = 0; j < NGV; ++j) st.zacc[j] *= ao;
     st.m = m_new;
     st.S = S_new;
+    st.inv_S = 1.f / S_new;
   }
+  float lsum = 0.f;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) pr[e] = (sig[e] == -INFINITY) ? 0.f : exp2f(sig[e] - st.m);
-  st.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) pr[e] *= kPrescale;
-  return 1.f / st.S;
+  for (int e = 0; e < N; ++e) {
+    pr[e] = (sig[e] == -INFINITY) ? 0.f : fast_exp2(sig[e] - st.m);
+    lsum += pr[e];
+    pr[e] *= kPrescale;
+  }
+  st.l += lsum;
+  return st.inv_S;
 }
 
 // --------------------------------------------------------------------------
@@ -255,39 +269,35 @@ __device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&
 template <int FMT>
 __device__ __forceinline__ void build_a_int(const float* qrow, const float* ks, const float* kz, int q,
                                             float scale_log2, uint32_t (&A)[8][4], float& kfac, float& cterm) {
-  float qv[32], sv[32], zv[32];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 q4 = *reinterpret_cast<const float4*>(qrow + 4 * i);
-    qv[4 * i + 0] = q4.x; qv[4 * i + 1] = q4.y; qv[4 * i + 2] = q4.z; qv[4 * i + 3] = q4.w;
-    const float4 s4 = *reinterpret_cast<const float4*>(ks + 32 * q + 4 * i);
-    const float4 z4 = *reinterpret_cast<const float4*>(kz + 32 * q + 4 * i);
-    sv[4 * i + 0] = s4.x; sv[4 * i + 1] = s4.y; sv[4 * i + 2] = s4.z; sv[4 * i + 3] = s4.w;
-    zv[4 * i + 0] = z4.x; zv[4 * i + 1] = z4.y; zv[4 * i + 2] = z4.z; zv[4 * i + 3] = z4.w;
-  }
+  // pass 1: largest |q_c s_c| of the head (sets the f16 range) and the zero-point term
   constexpr float kH = (float)FT<FMT>::kHalf;
-  float x[32];
+  const float* ksq = ks + 32 * q;
+  const float* kzq = kz + 32 * q;
   float mx = 0.f, cz = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int c0 = kchan0<FMT>(j), c1 = kchan1<FMT>(j);
-    const float x0 = qv[c0] * sv[c0];
-    const float x1 = qv[c1] * sv[c1];
-    x[2 * j] = x0;
-    x[2 * j + 1] = x1;
-    mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
-    cz = fmaf(x0, kH - zv[c0], cz);
-    cz = fmaf(x1, kH - zv[c1], cz);
+  for (int i = 0; i < 8; ++i) {
+    const int ci = 4 * ((i + q) & 7);  // rotated per lane group: the 4 groups hit different banks
+    const float4 q4 = *reinterpret_cast<const float4*>(qrow + ci);
+    const float4 s4 = *reinterpret_cast<const float4*>(ksq + ci);
+    const float4 z4 = *reinterpret_cast<const float4*>(kzq + ci);
+    const float x0 = q4.x * s4.x, x1 = q4.y * s4.y, x2 = q4.z * s4.z, x3 = q4.w * s4.w;
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
+    cz = fmaf(x0, kH - z4.x, cz);
+    cz = fmaf(x1, kH - z4.y, cz);
+    cz = fmaf(x2, kH - z4.z, cz);
+    cz = fmaf(x3, kH - z4.w, cz);
   }
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
   cz += __shfl_xor_sync(kFull, cz, 1);
   cz += __shfl_xor_sync(kFull, cz, 2);
   const float kappa = mx > 0.f ? 16384.f / mx : 1.f;
+  // pass 2: A = hi/lo split of q_c s_c kappa, in the channel order the Key unpacking produces
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
+    const int c0 = kchan0<FMT>(j), c1 = kchan1<FMT>(j);
     uint32_t hi, lo;
-    split_f16(x[2 * j] * kappa, x[2 * j + 1] * kappa, hi, lo);
+    split_f16(qrow[c0] * ksq[c0] * kappa, qrow[c1] * ksq[c1] * kappa, hi, lo);
     if ((j & 1) == 0) {
       A[j >> 1][0] = hi;
       A[j >> 1][1] = lo;
@@ -311,31 +321,63 @@ __device__ __forceinline__ void write_out(const DecodeParams& p, int b, int hq, 
   if (p.lse && c == 0) p.lse[(long long)b * p.Hq + hq] = l2 * 0.69314718055994531f;
 }
 
-struct SegInfo {
-  int b, h;
-  TokenSplit ts;
-  int nbf, nq;  // bf16 tiles, quantized tiles
+// One (sequence, kv head) pair's share of this CTA's unit range.
+struct SegRec {
+  long long pair_start;  // first unit of the pair in the flat unit list
+  int b, h, ua, ue, units;
+  int n_sink, qn, r, nbf, nq;
+};
+constexpr int kMaxSeg = 16;  // segments per table batch
+constexpr int kChunk = 2;    // quantized tiles per softmax step
+
+// This warp's part of a segment: bf16 tiles [bf0, bf0 + nbf_w), quantized tiles
+// [q0, q0 + nq_w); stages: two per bf16 tile (its K rows, then its V rows), then
+// ceil(nq_w / tps) quantized stages.
+struct WarpPart {
+  int bf0, nbf_w, q0, nq_w, nstage;
 };
 
+__device__ __forceinline__ WarpPart warp_part(const SegRec& sg, int warp, int wbf, int tps) {
+  WarpPart w;
+  const int wa = sg.ua + (int)((long long)(sg.ue - sg.ua) * warp / kNW);
+  const int we = sg.ua + (int)((long long)(sg.ue - sg.ua) * (warp + 1) / kNW);
+  const int bf0 = (wa + wbf - 1) / wbf;
+  const int bf1 = min(sg.nbf, (we + wbf - 1) / wbf);
+  w.bf0 = bf0;
+  w.nbf_w = max(0, bf1 - bf0);
+  const int qbase = sg.nbf * wbf;
+  w.q0 = max(0, wa - qbase);
+  const int q1 = min(sg.nq, max(0, we - qbase));
+  w.nq_w = max(0, q1 - w.q0);
+  w.nstage = 2 * w.nbf_w + (w.nq_w + tps - 1) / tps;
+  return w;
+}
+
 template <int FMT, int NGV>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
+  constexpr int kHdr = F::kInt ? 1024 : 0;  // every stage starts with a header slot (INT)
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerDesc& L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, q = lane & 3;
   const int B = p.batch, H = L.H, g = p.g;
+  const int tps = p.tps, nst = p.nst, wbf = p.bf_weight;
 
   // ---- shared memory carve-up ----
   uint8_t* stage_base = smem;
-  size_t off = (size_t)kNW * p.nst * p.stage_bytes;
+  size_t off = (size_t)kNW * nst * p.stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
   off += kNW * kMaxStages * sizeof(uint64_t);
   float* q_s = reinterpret_cast<float*>(smem + off);
   off += 8 * 4 * kQStride * sizeof(float);
   uint8_t* scratch = smem + off;
-  off += kNW * p.warp_scratch;
+  off += (size_t)kNW * p.warp_scratch;
+  SegRec* segs = reinterpret_cast<SegRec*>(smem + off);
+  off += kMaxSeg * sizeof(SegRec);
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
+  __shared__ int seg_count;
+  __shared__ long long batch_end;
 
   if (tid == 0) {
     for (int i = 0; i < kNW * kMaxStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
@@ -354,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
     const TokenSplit ts = split_tokens(seq_tokens(b), L);
     const int nbf = (ts.n_sink + ts.r + 15) >> 4;
     const int nq = (ts.qn + 15) >> 4;
-    return nbf * p.bf_weight + nq;
+    return nbf * wbf + nq;
   };
   {
     const int per = (B + kThreads - 1) / kThreads;
@@ -364,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
       prefix[b] = local;
       local += seq_units(b) * H;
     }
-    // exclusive scan of `local` over the block
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -379,7 +420,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
     const int excl = wbase + incl - local;
     for (int b = b0; b < b1; ++b) prefix[b] += excl;
     if (tid == kThreads - 1) prefix[B] = wbase + incl;
-    // lengths beyond the capacity are reported once, by CTA 0
     if (blockIdx.x == 0) {
       for (int b = tid; b < B; b += kThreads)
         if (p.seq_lens[b] > tmax_tok) report(p.status, KVQ_DEV_CAPACITY);
@@ -406,444 +446,528 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams 
   const __nv_bfloat16* ring_k = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_k);
   const __nv_bfloat16* ring_v = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_v);
 
-  uint8_t* my_stages = stage_base + (size_t)warp * p.nst * p.stage_bytes;
+  uint8_t* my_stages = stage_base + (size_t)warp * nst * p.stage_bytes;
   uint64_t* my_bars = bars + warp * kMaxStages;
   uint8_t* my_scratch = scratch + warp * p.warp_scratch;
-  uint32_t phase_bits = 0;  // expected parity of each of this warp's stage barriers
+  const float* qrow = q_s + (r * 4 + q) * kQStride;  // the lane's 32 query values of head r
+  uint32_t phase_bits = 0;  // expected parity of each stage barrier of this warp
+  uint32_t slot_valid = 0;  // lane 0: 8 bits per slot, the tiles its stage holds
+  uint32_t pending = 0;     // slots with copies in flight
+  bool alive = true;
+  int n_issued = 0, n_consumed = 0;
+  const float s_v8 = F::kFp8 ? __ldg(p.C.v_tscale) : 1.f;
 
-  // stage sub-buffer offsets
-  const int o_vc = F::kTile;
-  const int o_vs = 2 * F::kTile;
-  const int o_vz = o_vs + 64 * NGV;
-  const int o_ks = o_vz + 64 * NGV;
-  const int o_kz = o_ks + 512;
-
-  long long pos = st;
-  while (pos < en) {
-    // ---- locate the pair holding unit `pos` ----
-    int lo = 0, hi = B;  // largest b with prefix[b] <= pos
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= pos) lo = mid; else hi = mid - 1;
-    }
-    const int b = lo;
-    const int units = (prefix[b + 1] - prefix[b]) / H;
-    const int h = (int)((pos - prefix[b]) / units);
-    const long long pair_start = prefix[b] + (long long)h * units;
-    const long long seg_end = min(en, pair_start + units);
-    const int ua = (int)(pos - pair_start), ue = (int)(seg_end - pair_start);
-
-    SegInfo sg;
-    sg.b = b;
-    sg.h = h;
-    sg.ts = split_tokens(seq_tokens(b), L);
-    sg.nbf = (sg.ts.n_sink + sg.ts.r + 15) >> 4;
-    sg.nq = (sg.ts.qn + 15) >> 4;
-    const int nbf_tok = sg.ts.n_sink + sg.ts.r;
-    const int wbf = p.bf_weight;
-
-    // ---- query of the g heads of kv head h -> smem (zero rows for r >= g) ----
+  auto load_q = [&](const SegRec& sg) {
     for (int i = tid; i < 8 * 128; i += kThreads) {
       const int hr = i >> 7, c = i & 127;
       float v = 0.f;
-      if (hr < g) v = __bfloat162float(qg[((long long)b * p.Hq + h * g + hr) * 128 + c]);
+      if (hr < g) v = __bfloat162float(qg[((long long)sg.b * p.Hq + sg.h * g + hr) * 128 + c]);
       q_s[(hr * 4 + (c >> 5)) * kQStride + (c & 31)] = v;
     }
+  };
+
+  long long pos = st;
+  while (pos < en) {
+    // ---- the next batch of segments of this CTA's range ----
+    __syncthreads();
+    if (tid == 0) {
+      int ns = 0;
+      long long pp = pos;
+      while (pp < en && ns < kMaxSeg) {
+        int lo = 0, hi = B;  // largest b with prefix[b] <= pp
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= pp) lo = mid; else hi = mid - 1;
+        }
+        SegRec sg;
+        sg.b = lo;
+        sg.units = (prefix[lo + 1] - prefix[lo]) / H;
+        sg.h = (int)((pp - prefix[lo]) / sg.units);
+        sg.pair_start = prefix[lo] + (long long)sg.h * sg.units;
+        const long long se = min(en, sg.pair_start + sg.units);
+        sg.ua = (int)(pp - sg.pair_start);
+        sg.ue = (int)(se - sg.pair_start);
+        const TokenSplit ts = split_tokens(seq_tokens(lo), L);
+        sg.n_sink = ts.n_sink;
+        sg.qn = ts.qn;
+        sg.r = ts.r;
+        sg.nbf = (ts.n_sink + ts.r + 15) >> 4;
+        sg.nq = (ts.qn + 15) >> 4;
+        segs[ns++] = sg;
+        pp = se;
+      }
+      seg_count = ns;
+      batch_end = pp;
+    }
+    __syncthreads();
+    const int nseg = seg_count;
+    load_q(segs[0]);
     __syncthreads();
 
-    // ---- this warp's unit range and tiles ----
-    const int wa = ua + (int)((long long)(ue - ua) * warp / kNW);
-    const int we = ua + (int)((long long)(ue - ua) * (warp + 1) / kNW);
-    const int bf_first = (wa + wbf - 1) / wbf;
-    const int bf_last = min(sg.nbf, (we + wbf - 1) / wbf);  // exclusive
-    const int qbase = sg.nbf * wbf;
-    const int q_first = max(0, wa - qbase);
-    const int q_last = min(sg.nq, max(0, we - qbase));     // exclusive
-    const int nq_w = max(0, q_last - q_first);
-
-    // the lane's 32 query values of head r (fixed for the segment)
-    const float* qrow = q_s + (r * 4 + q) * kQStride;
-
-    WarpState<NGV> stt;
-    state_init(stt);
-
-    // ---- producer: issue the copies of quantized tile (q_first + k) into stage s ----
-    uint32_t valid_bits = 0, pending_bits = 0;
-    bool alive = true;
-    auto issue = [&](int k, int s) {
-      const int qi = q_first + k;
-      const long long x0 = (long long)qi * 16;
-      const QuantAddr a = quant_addr(L, p.C, b, h, x0, lane == 0 ? p.status : nullptr);
-      if (!a.ok) {
-        valid_bits &= ~(1u << s);
-        return;
-      }
-      valid_bits |= 1u << s;
-      pending_bits |= 1u << s;
+    // ---- producer (lane 0 copies; every lane keeps the same cursor) ----
+    int ps = 0, pj = 0;
+    WarpPart pw = warp_part(segs[0], warp, wbf, tps);
+    while (ps < nseg && pw.nstage == 0) {
+      ++ps;
+      if (ps < nseg) pw = warp_part(segs[ps], warp, wbf, tps);
+    }
+    auto issue_next = [&]() {
+      const int slot = n_issued % nst;
+      uint32_t vm = 0;
       if (lane == 0) {
-        uint8_t* dst = my_stages + (size_t)s * p.stage_bytes;
-        const uint32_t bar = smem_addr(&my_bars[s]);
-        const bool need_ks = F::kInt && (k == 0 || ((x0 % L.G) == 0));
-        uint32_t bytes = 2 * F::kTile;
-        if constexpr (F::kInt) bytes += 128 * NGV + (need_ks ? 1024 : 0);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_g2s(smem_addr(dst), a.kc, F::kTile, bar);
-        bulk_copy_g2s(smem_addr(dst + o_vc), a.vt, F::kTile, bar);
-        if constexpr (F::kInt) {
-          bulk_copy_g2s(smem_addr(dst + o_vs), a.vs, 64 * NGV, bar);
-          bulk_copy_g2s(smem_addr(dst + o_vz), a.vz, 64 * NGV, bar);
-          if (need_ks) {
-            bulk_copy_g2s(smem_addr(dst + o_ks), a.ks, 512, bar);
-            bulk_copy_g2s(smem_addr(dst + o_kz), a.kz, 512, bar);
+        const SegRec& sg = segs[ps];
+        uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
+        const uint32_t bar = smem_addr(&my_bars[slot]);
+        if (pj < 2 * pw.nbf_w) {
+          // bf16 tile: its 16 K rows (even stage) or V rows (odd stage), one 256-byte copy per row
+          const int bt = pw.bf0 + pj / 2;
+          const int rows = min(16, sg.n_sink + sg.r - bt * 16);
+          const TokenSplit ts = {sg.n_sink, sg.qn, sg.r};
+          mbar_arrive_expect_tx(bar, 256u * rows);
+          for (int rr = 0; rr < rows; ++rr) {
+            const __nv_bfloat16* src = (pj & 1) ? bf16_row(L, sink_v, ring_v, sg.b, sg.h, bt * 16 + rr, ts)
+                                                : bf16_row(L, sink_k, ring_k, sg.b, sg.h, bt * 16 + rr, ts);
+            bulk_copy_g2s(smem_addr(dst + rr * kBfRow), src, 256, bar);
           }
+          vm = 1;
+        } else {
+          // quantized tiles [i0, i0 + n): one contiguous range per record touched
+          const int qs = pj - 2 * pw.nbf_w;
+          const long long i0 = pw.q0 + (long long)qs * tps;
+          const int n = (int)min((long long)tps, (long long)(pw.q0 + pw.nq_w) - i0);
+          const long long last = i0 + n - 1;
+          const bool hdr0 = F::kInt && qs == 0 && (i0 % L.tpg) != 0;
+          if (!L.paged) {
+            const uint8_t* base = reinterpret_cast<const uint8_t*>(p.C.qstore) +
+                                  ((long long)sg.b * H + sg.h) * L.nrec * L.rec_bytes;
+            const uint8_t* rec0 = base + (i0 / L.tpg) * L.rec_bytes;
+            const uint8_t* start = (F::kInt && i0 % L.tpg == 0) ? rec0 : rec0 + L.hdr_bytes + (i0 % L.tpg) * L.tile_bytes;
+            const uint8_t* end = base + (last / L.tpg) * L.rec_bytes + L.hdr_bytes + (last % L.tpg + 1) * L.tile_bytes;
+            const uint32_t len = (uint32_t)(end - start);
+            mbar_arrive_expect_tx(bar, len + (hdr0 ? 1024u : 0u));
+            bulk_copy_g2s(smem_addr(dst + kHdr), start, len, bar);
+            if (hdr0) bulk_copy_g2s(smem_addr(dst), rec0, 1024, bar);
+            vm = (1u << n) - 1u;
+          } else {
+            uint32_t bytes = 0;
+            for (long long rr = i0 / L.tpg; rr <= last / L.tpg; ++rr) {
+              const uint8_t* rec = record_addr(L, p.C, sg.b, sg.h, rr, p.status);
+              const long long a0 = max(i0, rr * L.tpg), a1 = min(last, rr * L.tpg + L.tpg - 1);
+              if (!rec) continue;
+              for (long long i = a0; i <= a1; ++i) vm |= 1u << (int)(i - i0);
+              const bool with_hdr = F::kInt && (a0 % L.tpg) == 0;
+              bytes += (uint32_t)((with_hdr ? L.hdr_bytes : 0) + (a1 - a0 + 1) * L.tile_bytes);
+              if (hdr0 && rr == i0 / L.tpg) bytes += 1024;
+            }
+            if (vm) {
+              mbar_arrive_expect_tx(bar, bytes);
+              uint32_t so = kHdr;
+              for (long long rr = i0 / L.tpg; rr <= last / L.tpg; ++rr) {
+                const long long a0 = max(i0, rr * L.tpg), a1 = min(last, rr * L.tpg + L.tpg - 1);
+                const bool with_hdr = F::kInt && (a0 % L.tpg) == 0;
+                const uint32_t len = (uint32_t)((with_hdr ? L.hdr_bytes : 0) + (a1 - a0 + 1) * L.tile_bytes);
+                const uint8_t* rec = record_addr(L, p.C, sg.b, sg.h, rr, nullptr);
+                if (rec) {
+                  const uint8_t* src = with_hdr ? rec : rec + L.hdr_bytes + (a0 % L.tpg) * L.tile_bytes;
+                  bulk_copy_g2s(smem_addr(dst + so), src, len, bar);
+                  if (hdr0 && rr == i0 / L.tpg) bulk_copy_g2s(smem_addr(dst), rec, 1024, bar);
+                }
+                so += len;
+              }
+            }
+          }
+        }
+        slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
+      }
+      vm = __shfl_sync(kFull, vm, 0);
+      if (vm) pending |= 1u << slot;
+      ++n_issued;
+      if (++pj == pw.nstage) {
+        pj = 0;
+        ++ps;
+        while (ps < nseg) {
+          pw = warp_part(segs[ps], warp, wbf, tps);
+          if (pw.nstage) break;
+          ++ps;
         }
       }
     };
-    for (int k = 0; k < min(nq_w, p.nst); ++k) issue(k, k);
+    while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
 
-    // =========================== bf16 tiles ===============================
-    for (int bt = bf_first; bt < bf_last; ++bt) {
-      // QK: B = K rows (bf16, natural channel pairs), A = q (bf16, exact)
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- consumer ----
+    for (int s = 0; s < nseg; ++s) {
+      const SegRec sg = segs[s];
+      const WarpPart wp = warp_part(sg, warp, wbf, tps);
+      const int nbf_tok = sg.n_sink + sg.r;
+      WarpState<NGV> stt;
+      state_init(stt);
+      uint32_t A[8][4];
+      float kfac = 0.f, cterm = 0.f;
+      if constexpr (F::kFp8) {
+        // A = q * 2^E (exact in f16), E from the head's largest |q|
+        float mx = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int xb = bt * 16 + nt * 8 + r;
-        uint32_t R[16];
-        if (xb < nbf_tok) {
-          const __nv_bfloat16* row = bf16_row(L, sink_k, ring_k, b, h, xb, sg.ts) + 32 * q;
-          const uint4* r4 = reinterpret_cast<const uint4*>(row);
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(qrow[i]));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        int ex = 0;
+        if (mx > 0.f) (void)frexpf(mx, &ex);
+        const float sc = mx > 0.f ? ldexpf(1.f, 15 - ex) : 1.f;  // max |q| * sc in [2^14, 2^15)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 v = r4[i];
-            R[4 * i] = v.x; R[4 * i + 1] = v.y; R[4 * i + 2] = v.z; R[4 * i + 3] = v.w;
+        for (int s2 = 0; s2 < 8; ++s2) {
+          const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s2);
+          A[s2][0] = pack_f16(qq.x * sc, qq.y * sc);
+          A[s2][1] = 0u;
+          A[s2][2] = pack_f16(qq.z * sc, qq.w * sc);
+          A[s2][3] = 0u;
+        }
+        kfac = p.scale_log2 * __ldg(p.C.k_tscale) / sc;
+      }
+      float sig_bf[4];  // scores of a bf16 tile between its K and V stages
+
+      for (int j = 0; j < wp.nstage; ++j) {
+        const int slot = n_consumed % nst;
+        const uint32_t vmask = (__shfl_sync(kFull, slot_valid, 0) >> (8 * slot)) & 0xFFu;
+        if (vmask) {
+          bool ok = alive && mbar_wait_bounded(smem_addr(&my_bars[slot]), (phase_bits >> slot) & 1u, kWaitLimitCycles);
+          ok = __all_sync(kFull, ok);
+          if (ok) {
+            phase_bits ^= 1u << slot;
+            pending &= ~(1u << slot);
+          } else if (alive) {
+            alive = false;
+            if (lane == 0) report(p.status, KVQ_DEV_TIMEOUT);
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) R[i] = 0u;
         }
+        const uint8_t* stg = my_stages + (size_t)slot * p.stage_bytes;
+        if (vmask && alive && j < 2 * wp.nbf_w) {
+          const int bt = wp.bf0 + j / 2;
+          const int rows = min(16, nbf_tok - bt * 16);
+          if ((j & 1) == 0) {
+            // ---- bf16 tile, K rows: QK with A = q (bf16, exact) ----
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s);
-          const uint32_t a0 = pack_bf16(qq.x, qq.y);
-          const uint32_t a2 = pack_bf16(qq.z, qq.w);
-          mma_bf16(acc[nt], a0, 0u, a2, 0u, R[2 * s], R[2 * s + 1]);
-        }
-      }
-      // V rows -> warp scratch (zeros past the end), then transposed loads
+            for (int nt = 0; nt < 2; ++nt) {
+              const int row = nt * 8 + r;
+              uint32_t R[16];
+              if (row < rows) {
+                const uint4* r4 = reinterpret_cast<const uint4*>(stg + row * kBfRow + 64 * q);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int id = lane + 32 * k;
-        const int row = id >> 4, col = id & 15;
-        const int xb = bt * 16 + row;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (xb < nbf_tok) v = reinterpret_cast<const uint4*>(bf16_row(L, sink_v, ring_v, b, h, xb, sg.ts))[col];
-        *reinterpret_cast<uint4*>(my_scratch + row * kBfRow + col * 16) = v;
-      }
-      __syncwarp();
-      float sig[4];
+                for (int i = 0; i < 4; ++i) {
+                  const uint4 v = r4[i];
+                  R[4 * i] = v.x; R[4 * i + 1] = v.y; R[4 * i + 2] = v.z; R[4 * i + 3] = v.w;
+                }
+              } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = bt * 16 + (e >> 1) * 8 + 2 * q + (e & 1);
-        sig[e] = (t < nbf_tok) ? acc[e >> 1][e & 1] * p.scale_log2 : -INFINITY;
-      }
-      float pr[4];
-      const float inv_s = softmax_step(stt, sig, 1.f, pr);
-      uint32_t ah0, al0, ah1, al1;
-      split_bf16(pr[0] * inv_s, pr[1] * inv_s, ah0, al0);
-      split_bf16(pr[2] * inv_s, pr[3] * inv_s, ah1, al1);
-      const uint32_t sbase = smem_addr(my_scratch);
+                for (int i = 0; i < 16; ++i) R[i] = 0u;
+              }
 #pragma unroll
-      for (int jp = 0; jp < 8; ++jp) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int tok = 8 * (mi & 1) + rr;
-        const uint32_t addr = sbase + tok * kBfRow + (2 * jp + (mi >> 1)) * 16;
-        uint32_t v0, v1, v2, v3;
-        ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-        mma_bf16(stt.o[2 * jp], ah0, al0, ah1, al1, v0, v1);
-        mma_bf16(stt.o[2 * jp + 1], ah0, al0, ah1, al1, v2, v3);
-      }
-      __syncwarp();
-    }
-
-    // ========================= quantized tiles ============================
-    uint32_t A[8][4];
-    float kfac = 0.f, cterm = 0.f;
-    if constexpr (F::kFp8) {
-      // A = q * 2^E (exact in f16), E from the head's largest |q|
-      float mx = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(qrow[i]));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-      int ex = 0;
-      if (mx > 0.f) (void)frexpf(mx, &ex);        // mx in [2^(ex-1), 2^ex)
-      const float sc = mx > 0.f ? ldexpf(1.f, 15 - ex) : 1.f;  // max |q| * sc in [2^14, 2^15)
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s);
-        A[s][0] = pack_f16(qq.x * sc, qq.y * sc);
-        A[s][1] = 0u;
-        A[s][2] = pack_f16(qq.z * sc, qq.w * sc);
-        A[s][3] = 0u;
-      }
-      kfac = p.scale_log2 * __ldg(p.C.k_tscale) / sc;
-    }
-    const float s_v8 = F::kFp8 ? __ldg(p.C.v_tscale) : 1.f;
-
-    for (int k = 0; k < nq_w; ++k) {
-      const int s = k % p.nst;
-      const int qi = q_first + k;
-      if ((valid_bits >> s) & 1u) {
-        bool ok = alive && mbar_wait_bounded(smem_addr(&my_bars[s]), (phase_bits >> s) & 1u, kWaitLimitCycles);
-        ok = __all_sync(kFull, ok);
-        if (ok) {
-          phase_bits ^= 1u << s;
-          pending_bits &= ~(1u << s);
-        } else if (alive) {
-          alive = false;
-          if (lane == 0) report(p.status, KVQ_DEV_TIMEOUT);
-        }
-        if (alive) {
-          const uint8_t* stg = my_stages + (size_t)s * p.stage_bytes;
-          if constexpr (F::kInt) {
-            // the group's A operand (q * s, hi/lo) is kept in the warp's shared scratch,
-            // 16 words per lane, and reloaded per tile (saves 32 registers)
-            uint4* afr = reinterpret_cast<uint4*>(my_scratch) + lane * 8;
-            if (k == 0 || (((long long)qi * 16) % L.G) == 0) {
-              build_a_int<FMT>(qrow, reinterpret_cast<const float*>(stg + o_ks),
-                               reinterpret_cast<const float*>(stg + o_kz), q, p.scale_log2, A, kfac, cterm);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) afr[i] = make_uint4(A[i][0], A[i][1], A[i][2], A[i][3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const uint4 v = afr[i];
-                A[i][0] = v.x; A[i][1] = v.y; A[i][2] = v.z; A[i][3] = v.w;
+              for (int s2 = 0; s2 < 8; ++s2) {
+                const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s2);
+                mma_bf16(acc[nt], pack_bf16(qq.x, qq.y), 0u, pack_bf16(qq.z, qq.w), 0u, R[2 * s2], R[2 * s2 + 1]);
               }
             }
-          }
-          // ---- QK ----
-          float acc[2][2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc[nt][c][e] = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            uint32_t R[16];
-            unpack_k<FMT>(stg + (nt * 8 + r) * F::kRB + q * F::kKChunk, R);
-#pragma unroll
-            for (int s2 = 0; s2 < 8; ++s2)
-              mma_f16(acc[nt][s2 & 1], A[s2][0], A[s2][1], A[s2][2], A[s2][3], R[2 * s2], R[2 * s2 + 1]);
-          }
-          const int tok_valid = min(16, sg.ts.qn - qi * 16);  // < 16 only for a partial FP8 tile
-          float sig[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int nt = e >> 1, c = e & 1;
-            const float dot = (acc[nt][0][c] + acc[nt][1][c]) + (acc[nt][0][c + 2] + acc[nt][1][c + 2]);
-            const int t = nt * 8 + 2 * q + c;
-            sig[e] = (t < tok_valid) ? fmaf(dot, kfac, cterm) : -INFINITY;
-          }
-          // ---- largest Value scale of the lane's 4 tokens ----
-          const float* vsp = reinterpret_cast<const float*>(stg + o_vs);
-          const float* vzp = reinterpret_cast<const float*>(stg + o_vz);
-          float smax = s_v8;
-          if constexpr (F::kInt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int t = (e >> 1) * 8 + 2 * q + (e & 1);
-#pragma unroll
-              for (int j = 0; j < NGV; ++j) smax = fmaxf(smax, vsp[t * NGV + j]);
-            }
-          }
-          float pr[4];
-          const float inv_s = softmax_step(stt, sig, smax, pr);
-          // ---- PV ----
-          uint32_t W[F::kVChunk / 4];
-          {
-            const uint4* vp = reinterpret_cast<const uint4*>(stg + o_vc + lane * F::kVChunk);
-#pragma unroll
-            for (int i = 0; i < F::kVChunk / 16; ++i) {
-              const uint4 v = vp[i];
-              W[4 * i] = v.x; W[4 * i + 1] = v.y; W[4 * i + 2] = v.z; W[4 * i + 3] = v.w;
-            }
-          }
-          if (tok_valid < 16) {
-            // partial tile: tokens past the end may hold stale bytes -> zero the lane's invalid tokens
-            // (lane's tokens: e -> 2q + (e&1) + 8(e>>1); byte/bit positions from the fragment order)
-            const bool v0 = 2 * q < tok_valid, v1 = 2 * q + 1 < tok_valid;
-            const bool v2 = 8 + 2 * q < tok_valid, v3 = 9 + 2 * q < tok_valid;
-            if constexpr (F::kFp8 || FMT == 8) {
-              // byte e of word jt (FP8) or byte {0,2,1,3}[e] (INT8)
-              uint32_t mk = 0;
-              if (F::kFp8) mk = (v0 ? 0xFFu : 0u) | (v1 ? 0xFF00u : 0u) | (v2 ? 0xFF0000u : 0u) | (v3 ? 0xFF000000u : 0u);
-              else mk = (v0 ? 0xFFu : 0u) | (v1 ? 0xFF0000u : 0u) | (v2 ? 0xFF00u : 0u) | (v3 ? 0xFF000000u : 0u);
-#pragma unroll
-              for (int i = 0; i < F::kVChunk / 4; ++i) W[i] &= mk;
-            }
-          }
-          if constexpr (F::kFp8) {
-            uint32_t ah0, al0, ah1, al1;
-            const float f = s_v8 * inv_s;
-            split_f16(pr[0] * f, pr[1] * f, ah0, al0);
-            split_f16(pr[2] * f, pr[3] * f, ah1, al1);
-#pragma unroll
-            for (int jt = 0; jt < 16; ++jt) {
-              uint32_t b01, b23;
-              switch (jt) {
-#define KVQ_V(J) case J: unpack_v<FMT, J>(W, b01, b23); break;
-                KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
-                KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
-              }
-              mma_f16(stt.o[jt], ah0, al0, ah1, al1, b01, b23);
+              sig_bf[e] = (t < rows) ? acc[e >> 1][e & 1] * p.scale_log2 : -INFINITY;
             }
           } else {
-            constexpr int kTilesPerGroup = 16 / NGV;  // n-tiles of 8 channels per Value group
-            constexpr float kH = (float)F::kHalf;
+            // ---- bf16 tile, V rows: softmax, then PV through transposed loads ----
+            uint8_t* stw = const_cast<uint8_t*>(stg);
+            for (int idx = lane; idx < (16 - rows) * 16; idx += 32)
+              *reinterpret_cast<uint4*>(stw + (rows + idx / 16) * kBfRow + (idx % 16) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+            float pr[4];
+            const float inv_s = softmax_step<NGV, 4>(stt, sig_bf, 1.f, pr);
+            uint32_t ah0, al0, ah1, al1;
+            split_bf16(pr[0] * inv_s, pr[1] * inv_s, ah0, al0);
+            split_bf16(pr[2] * inv_s, pr[3] * inv_s, ah1, al1);
+            const uint32_t sbase = smem_addr(stg);
 #pragma unroll
-            for (int j = 0; j < NGV; ++j) {
-              float w[4];
+            for (int jp = 0; jp < 8; ++jp) {
+              const int mi = lane >> 3, rr = lane & 7;
+              const int tok = 8 * (mi & 1) + rr;
+              const uint32_t addr = sbase + tok * kBfRow + (2 * jp + (mi >> 1)) * 16;
+              uint32_t v0, v1, v2, v3;
+              ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+              mma_bf16(stt.o[2 * jp], ah0, al0, ah1, al1, v0, v1);
+              mma_bf16(stt.o[2 * jp + 1], ah0, al0, ah1, al1, v2, v3);
+            }
+          }
+        } else if (vmask && alive) {
+          // ---- quantized stage: tiles [i0, i0 + n), walked in smem ----
+          const int qs = j - 2 * wp.nbf_w;
+          const long long i0 = wp.q0 + (long long)qs * tps;
+          const int n = (int)min((long long)tps, (long long)(wp.q0 + wp.nq_w) - i0);
+          int walk = kHdr;  // smem offset of the next tile (headers inline at record starts)
+          bool a_ready = false;
+          for (int k = 0; k < n; k += kChunk) {
+            float sig[kChunk * 4];
+            int toff[kChunk];
+            float smax = s_v8;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int t = (e >> 1) * 8 + 2 * q + (e & 1);
-                w[e] = (vsp[t * NGV + j] * inv_s) * pr[e];
-                stt.zacc[j] = fmaf(w[e], kH - vzp[t * NGV + j], stt.zacc[j]);
-              }
-              uint32_t ah0, al0, ah1, al1;
-              split_f16(w[0], w[1], ah0, al0);
-              split_f16(w[2], w[3], ah1, al1);
-#pragma unroll
-              for (int jj = 0; jj < kTilesPerGroup; ++jj) {
-                uint32_t b01, b23;
-                switch (j * kTilesPerGroup + jj) {
-                  KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
-                  KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
-#undef KVQ_V
+            for (int tt = 0; tt < kChunk; ++tt) {
+              const int kk = k + tt;
+              const long long i = i0 + kk;
+              int hoff = 0;
+              toff[tt] = -1;
+              if (kk < n) {
+                if (F::kInt && (i % L.tpg) == 0) {
+                  hoff = walk;
+                  walk += L.hdr_bytes;
                 }
-                mma_f16(stt.o[j * kTilesPerGroup + jj], ah0, al0, ah1, al1, b01, b23);
+                toff[tt] = walk;
+                walk += L.tile_bytes;
+              }
+              const bool present = kk < n && ((vmask >> kk) & 1u);
+              if (!present) toff[tt] = -1;
+              if (present) {
+                if constexpr (F::kInt) {
+                  // the group's A operand (q * s, hi/lo) lives in the warp's shared scratch between chunks
+                  uint4* afr = reinterpret_cast<uint4*>(my_scratch) + lane;  // word i of lane at [i][lane]
+                  if ((i % L.tpg) == 0 || (qs == 0 && kk == 0)) {
+                    build_a_int<FMT>(qrow, reinterpret_cast<const float*>(stg + hoff),
+                                     reinterpret_cast<const float*>(stg + hoff + 512), q, p.scale_log2, A, kfac,
+                                     cterm);
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) afr[32 * i2] = make_uint4(A[i2][0], A[i2][1], A[i2][2], A[i2][3]);
+                    a_ready = true;
+                  } else if (!a_ready || tt == 0) {
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) {
+                      const uint4 v = afr[32 * i2];
+                      A[i2][0] = v.x; A[i2][1] = v.y; A[i2][2] = v.z; A[i2][3] = v.w;
+                    }
+                    a_ready = true;
+                  }
+                }
+                const uint8_t* tile = stg + toff[tt];
+                float acc[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+                  uint32_t R[16];
+                  unpack_k<FMT>(tile + (nt * 8 + r) * F::kRB + q * F::kKChunk, R);
+#pragma unroll
+                  for (int s2 = 0; s2 < 8; ++s2)
+                    mma_f16(acc[nt], A[s2][0], A[s2][1], A[s2][2], A[s2][3], R[2 * s2], R[2 * s2 + 1]);
+                }
+                const int tok_valid = (int)min(16LL, (long long)sg.qn - i * 16);  // < 16 only for a partial FP8 tile
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int nt = e >> 1, c = e & 1;
+                  const float dot = acc[nt][c] + acc[nt][c + 2];
+                  const int t = nt * 8 + 2 * q + c;
+                  sig[tt * 4 + e] = (t < tok_valid) ? fmaf(dot, kfac, cterm) : -INFINITY;
+                }
+                if constexpr (F::kInt) {
+                  const float* vsp = reinterpret_cast<const float*>(tile + 32 * F::kRB);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int t = (e >> 1) * 8 + 2 * q + (e & 1);
+#pragma unroll
+                    for (int jg = 0; jg < NGV; ++jg) smax = fmaxf(smax, vsp[t * NGV + jg]);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sig[tt * 4 + e] = -INFINITY;
+              }
+            }
+            float pr[kChunk * 4];
+            const float inv_s = softmax_step<NGV, kChunk * 4>(stt, sig, smax, pr);
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt) {
+              if (toff[tt] < 0) continue;
+              const long long i = i0 + k + tt;
+              const uint8_t* tile = stg + toff[tt];
+              uint32_t W[F::kVChunk / 4];
+              {
+                const uint4* vp = reinterpret_cast<const uint4*>(tile + F::kTile + lane * F::kVChunk);
+#pragma unroll
+                for (int i2 = 0; i2 < F::kVChunk / 16; ++i2) {
+                  const uint4 v = vp[i2];
+                  W[4 * i2] = v.x; W[4 * i2 + 1] = v.y; W[4 * i2 + 2] = v.z; W[4 * i2 + 3] = v.w;
+                }
+              }
+              if constexpr (F::kFp8) {
+                const int tok_valid = (int)min(16LL, (long long)sg.qn - i * 16);
+                if (tok_valid < 16) {
+                  // partial tile: bytes past the end may be stale; zero the lane's invalid tokens (byte e = token e)
+                  const bool v0 = 2 * q < tok_valid, v1 = 2 * q + 1 < tok_valid;
+                  const bool v2 = 8 + 2 * q < tok_valid, v3 = 9 + 2 * q < tok_valid;
+                  const uint32_t mk =
+                      (v0 ? 0xFFu : 0u) | (v1 ? 0xFF00u : 0u) | (v2 ? 0xFF0000u : 0u) | (v3 ? 0xFF000000u : 0u);
+#pragma unroll
+                  for (int i2 = 0; i2 < F::kVChunk / 4; ++i2) W[i2] &= mk;
+                }
+                uint32_t ah0, al0, ah1, al1;
+                const float f = s_v8 * inv_s;
+                split_f16(pr[tt * 4 + 0] * f, pr[tt * 4 + 1] * f, ah0, al0);
+                split_f16(pr[tt * 4 + 2] * f, pr[tt * 4 + 3] * f, ah1, al1);
+#pragma unroll
+                for (int jt = 0; jt < 16; ++jt) {
+                  uint32_t b01, b23;
+                  switch (jt) {
+#define KVQ_V(J) case J: unpack_v<FMT, J>(W, b01, b23); break;
+                    KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
+                    KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
+                  }
+                  mma_f16(stt.o[jt], ah0, al0, ah1, al1, b01, b23);
+                }
+              } else {
+                constexpr int kTilesPerGroup = 16 / NGV;  // n-tiles of 8 channels per Value group
+                constexpr float kH = (float)F::kHalf;
+                const float* vsp = reinterpret_cast<const float*>(tile + 32 * F::kRB);
+                const float* vzp = vsp + 16 * NGV;
+#pragma unroll
+                for (int jg = 0; jg < NGV; ++jg) {
+                  float w[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int t = (e >> 1) * 8 + 2 * q + (e & 1);
+                    w[e] = (vsp[t * NGV + jg] * inv_s) * pr[tt * 4 + e];
+                    stt.zacc[jg] = fmaf(w[e], kH - vzp[t * NGV + jg], stt.zacc[jg]);
+                  }
+                  uint32_t ah0, al0, ah1, al1;
+                  split_f16(w[0], w[1], ah0, al0);
+                  split_f16(w[2], w[3], ah1, al1);
+#pragma unroll
+                  for (int jj = 0; jj < kTilesPerGroup; ++jj) {
+                    uint32_t b01, b23;
+                    switch (jg * kTilesPerGroup + jj) {
+                      KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
+                      KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
+#undef KVQ_V
+                    }
+                    mma_f16(stt.o[jg * kTilesPerGroup + jj], ah0, al0, ah1, al1, b01, b23);
+                  }
+                }
               }
             }
           }
         }
+        __syncwarp();
+        ++n_consumed;
+        while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
+      }
+
+      // ---- finalise the warp's state and publish it ----
+      float l = stt.l;
+      l += __shfl_xor_sync(kFull, l, 1);
+      l += __shfl_xor_sync(kFull, l, 2);
+      float zs[NGV];
+#pragma unroll
+      for (int jg = 0; jg < NGV; ++jg) {
+        float z = stt.zacc[jg];
+        z += __shfl_xor_sync(kFull, z, 1);
+        z += __shfl_xor_sync(kFull, z, 2);
+        zs[jg] = z;
       }
       __syncwarp();
-      if (alive && k + p.nst < nq_w) issue(k + p.nst, s);
+      float* rec = reinterpret_cast<float*>(my_scratch);
+      if (r < g) {
+        const float unit = stt.S / kPrescale;
+        float* rr = rec + r * kMergeStride;
+        if (q == 0) {
+          rr[0] = stt.m;
+          rr[1] = l;
+        }
+#pragma unroll
+        for (int jt = 0; jt < 16; ++jt) {
+          const float z = F::kInt ? zs[jt / (16 / NGV)] : 0.f;
+          float2 v;
+          v.x = (stt.o[jt][0] + stt.o[jt][2] + z) * unit;
+          v.y = (stt.o[jt][1] + stt.o[jt][3] + z) * unit;
+          if (stt.m == -INFINITY) v.x = v.y = 0.f;
+          *reinterpret_cast<float2*>(rr + 4 + jt * 8 + 2 * q) = v;
+        }
+      }
+      __syncthreads();
+      // ---- merge the warps; write the partial of (b, h), or the result when this CTA owns the pair ----
+      {
+        const int b = sg.b, h = sg.h;
+        const long long pair = (long long)b * H + h;
+        const long long slot = (long long)blockIdx.x + pair;
+        const long long P0 = sg.pair_start, P1 = sg.pair_start + sg.units;
+        const long long c_lo = ((P0 + 1) * C - 1) / U, c_hi = (P1 * C - 1) / U;
+        const bool whole = p.fuse && c_lo == c_hi;  // no other CTA touches this pair
+        const float* recs = reinterpret_cast<const float*>(scratch);
+        for (int i = tid; i < g * 128; i += kThreads) {
+          const int hr = i >> 7, c = i & 127;
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kNW; ++w) M = fmaxf(M, recs[w * (p.warp_scratch / 4) + hr * kMergeStride]);
+          float Lsum = 0.f, O = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+              const float* rw = recs + w * (p.warp_scratch / 4) + hr * kMergeStride;
+              const float f = exp2f(rw[0] - M);  // 0 for an empty warp (m = -inf)
+              Lsum = fmaf(rw[1], f, Lsum);
+              O = fmaf(rw[4 + c], f, O);
+            }
+          }
+          const bool empty = !(Lsum > 0.f);
+          const float o = empty ? 0.f : O / Lsum;
+          const float l2 = empty ? -INFINITY : M + log2f(Lsum);
+          if (whole) {
+            write_out(p, b, h * g + hr, c, o, l2);
+          } else {
+            p.ws_o[(slot * g + hr) * 128 + c] = o;
+            if (c == 0) p.ws_lse[slot * g + hr] = l2;
+          }
+        }
+        if (p.fuse && !whole) {
+          // the last CTA to finish this pair merges every partial of it
+          __shared__ int last_flag;
+          __threadfence();
+          __syncthreads();
+          if (tid == 0) {
+            int nparts = 0;
+            for (long long cc = c_lo; cc <= c_hi; ++cc) nparts += ((cc * U) / C != ((cc + 1) * U) / C);
+            const unsigned old = atomicAdd(&p.counters[pair], 1u);
+            last_flag = (old + 1u == (unsigned)nparts);
+            if (last_flag) p.counters[pair] = 0u;  // ready for the next call
+          }
+          __syncthreads();
+          if (last_flag) {
+            __threadfence();
+            for (int i = tid; i < g * 128; i += kThreads) {
+              const int hr = i >> 7, c = i & 127;
+              float M = -INFINITY;
+              for (long long cc = c_lo; cc <= c_hi; ++cc)
+                if ((cc * U) / C != ((cc + 1) * U) / C) M = fmaxf(M, __ldcg(&p.ws_lse[(cc + pair) * g + hr]));
+              float Lsum = 0.f, O = 0.f;
+              if (M != -INFINITY) {
+                for (long long cc = c_lo; cc <= c_hi; ++cc) {
+                  if ((cc * U) / C == ((cc + 1) * U) / C) continue;
+                  const float f = exp2f(__ldcg(&p.ws_lse[(cc + pair) * g + hr]) - M);
+                  Lsum += f;
+                  O = fmaf(f, __ldcg(&p.ws_o[((cc + pair) * g + hr) * 128 + c]), O);
+                }
+              }
+              const bool empty = !(Lsum > 0.f);
+              write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+            }
+          }
+        }
+        if (s + 1 < nseg) load_q(segs[s + 1]);
+      }
+      __syncthreads();
     }
     // drain copies still in flight after a timeout (bounded)
-    if (pending_bits) {
-      for (int s = 0; s < p.nst; ++s)
-        if ((pending_bits >> s) & 1u) {
-          mbar_wait_bounded(smem_addr(&my_bars[s]), (phase_bits >> s) & 1u, kWaitLimitCycles);
-          phase_bits ^= 1u << s;
+    if (pending) {
+      for (int sl = 0; sl < nst; ++sl)
+        if ((pending >> sl) & 1u) {
+          mbar_wait_bounded(smem_addr(&my_bars[sl]), (phase_bits >> sl) & 1u, kWaitLimitCycles);
+          phase_bits ^= 1u << sl;
         }
-      pending_bits = 0;
+      pending = 0;
     }
-
-    // ---- finalise the warp's state and publish it ----
-    float l = stt.l;
-    l += __shfl_xor_sync(kFull, l, 1);
-    l += __shfl_xor_sync(kFull, l, 2);
-    float zs[NGV];
-#pragma unroll
-    for (int j = 0; j < NGV; ++j) {
-      float z = stt.zacc[j];
-      z += __shfl_xor_sync(kFull, z, 1);
-      z += __shfl_xor_sync(kFull, z, 2);
-      zs[j] = z;
-    }
-    __syncwarp();
-    float* rec = reinterpret_cast<float*>(my_scratch);
-    if (r < g) {
-      const float unit = stt.S / kPrescale;
-      float* rr = rec + r * kMergeStride;
-      if (q == 0) {
-        rr[0] = stt.m;
-        rr[1] = l;
-      }
-#pragma unroll
-      for (int jt = 0; jt < 16; ++jt) {
-        const float z = F::kInt ? zs[jt / (16 / NGV)] : 0.f;
-        float2 v;
-        v.x = (stt.o[jt][0] + stt.o[jt][2] + z) * unit;
-        v.y = (stt.o[jt][1] + stt.o[jt][3] + z) * unit;
-        if (stt.m == -INFINITY) v.x = v.y = 0.f;
-        *reinterpret_cast<float2*>(rr + 4 + jt * 8 + 2 * q) = v;
-      }
-    }
-    __syncthreads();
-    // ---- merge the warps; write the partial of (b, h), or the result when this CTA owns the pair ----
-    {
-      const long long pair = (long long)b * H + h;
-      const long long slot = (long long)blockIdx.x + pair;
-      const long long P0 = pair_start, P1 = pair_start + units;
-      const long long c_lo = ((P0 + 1) * C - 1) / U, c_hi = (P1 * C - 1) / U;
-      const bool whole = p.fuse && c_lo == c_hi;  // no other CTA touches this pair
-      const float* recs = reinterpret_cast<const float*>(scratch);
-      for (int i = tid; i < g * 128; i += kThreads) {
-        const int hr = i >> 7, c = i & 127;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) M = fmaxf(M, recs[w * (p.warp_scratch / 4) + hr * kMergeStride]);
-        float Lsum = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kNW; ++w) {
-            const float* rw = recs + w * (p.warp_scratch / 4) + hr * kMergeStride;
-            const float f = exp2f(rw[0] - M);  // 0 for an empty warp (m = -inf)
-            Lsum = fmaf(rw[1], f, Lsum);
-            O = fmaf(rw[4 + c], f, O);
-          }
-        }
-        const bool empty = !(Lsum > 0.f);
-        const float o = empty ? 0.f : O / Lsum;
-        const float l2 = empty ? -INFINITY : M + log2f(Lsum);
-        if (whole) {
-          write_out(p, b, h * g + hr, c, o, l2);
-        } else {
-          p.ws_o[(slot * g + hr) * 128 + c] = o;
-          if (c == 0) p.ws_lse[slot * g + hr] = l2;
-        }
-      }
-      if (p.fuse && !whole) {
-        // the last CTA to finish this pair merges every partial of it
-        __shared__ int last_flag;
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-          int n = 0;
-          for (long long cc = c_lo; cc <= c_hi; ++cc) n += ((cc * U) / C != ((cc + 1) * U) / C);
-          const unsigned old = atomicAdd(&p.counters[pair], 1u);
-          last_flag = (old + 1u == (unsigned)n);
-          if (last_flag) p.counters[pair] = 0u;  // ready for the next call
-        }
-        __syncthreads();
-        if (last_flag) {
-          __threadfence();
-          for (int i = tid; i < g * 128; i += kThreads) {
-            const int hr = i >> 7, c = i & 127;
-            float M = -INFINITY;
-            for (long long cc = c_lo; cc <= c_hi; ++cc)
-              if ((cc * U) / C != ((cc + 1) * U) / C) M = fmaxf(M, __ldcg(&p.ws_lse[(cc + pair) * g + hr]));
-            float Lsum = 0.f, O = 0.f;
-            if (M != -INFINITY) {
-              for (long long cc = c_lo; cc <= c_hi; ++cc) {
-                if ((cc * U) / C == ((cc + 1) * U) / C) continue;
-                const float f = exp2f(__ldcg(&p.ws_lse[(cc + pair) * g + hr]) - M);
-                Lsum += f;
-                O = fmaf(f, __ldcg(&p.ws_o[((cc + pair) * g + hr) * 128 + c]), O);
-              }
-            }
-            const bool empty = !(Lsum > 0.f);
-            write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
-          }
-        }
-      }
-    }
-    __syncthreads();
-    pos = seg_end;
+    pos = batch_end;
   }
 }
 

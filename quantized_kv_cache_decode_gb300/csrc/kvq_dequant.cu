@@ -42,19 +42,26 @@ __global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
       vx = __bfloat162float(sink_v[(pair * L.S + t) * L.d + c]);
     } else if (t < ts.n_sink + ts.qn) {
       const long long x = t - L.S;
-      const QuantAddr a = quant_addr(L, p.C, b, h, x, c == 0 ? p.status : nullptr);
-      if (a.ok) {
+      const long long i = x / 16;
+      const uint8_t* rec = record_addr(L, p.C, b, h, i / L.tpg, c == 0 ? p.status : nullptr);
+      if (rec) {
+        const uint8_t* tile = tile_in_record(L, rec, i);
+        const int row = (int)(x % 16);
         int byte, bit;
-        vtile_pos(L.bits, L.fp8 != 0, (int)(x % 16), c, byte, bit);
+        vtile_pos(L.bits, L.fp8 != 0, row, c, byte, bit);
         if (L.fp8) {
-          kx = __fmul_rn(*p.C.k_tscale, e4m3_value(a.kc[c]));
-          vx = __fmul_rn(*p.C.v_tscale, e4m3_value(a.vt[byte]));
+          kx = __fmul_rn(*p.C.k_tscale, e4m3_value(tile[row * L.rb + c]));
+          vx = __fmul_rn(*p.C.v_tscale, e4m3_value(tile[16 * L.rb + byte]));
         } else {
-          const uint32_t kcode = (a.kc[c / per_byte] >> ((c % per_byte) * L.bits)) & cmask;
-          const uint32_t vcode = (a.vt[byte] >> bit) & cmask;
+          const float* ks = reinterpret_cast<const float*>(rec);
+          const float* kz = ks + 128;
+          const float* vs = reinterpret_cast<const float*>(tile + 32 * L.rb);
+          const float* vz = vs + 16 * L.ngv;
+          const uint32_t kcode = (tile[row * L.rb + c / per_byte] >> ((c % per_byte) * L.bits)) & cmask;
+          const uint32_t vcode = (tile[16 * L.rb + byte] >> bit) & cmask;
           const int j = c / L.Gv;
-          kx = __fmul_rn(a.ks[c], __fsub_rn((float)kcode, a.kz[c]));
-          vx = __fmul_rn(a.vs[j], __fsub_rn((float)vcode, a.vz[j]));
+          kx = __fmul_rn(ks[c], __fsub_rn((float)kcode, kz[c]));
+          vx = __fmul_rn(vs[row * L.ngv + j], __fsub_rn((float)vcode, vz[row * L.ngv + j]));
         }
       }
     } else if (t < T) {

@@ -17,18 +17,17 @@ struct LayerDesc {
   int H, d, fmt, bits, fp8;
   int G, Gv, ngv, R, S, W;  // W = R + G ring slots (0 for FP8)
   int paged, P, cap, num_blocks, mbps;
-  int rb;  // bytes of one token row of codes (d * bits / 8)
-  long long slab_bytes, block_bytes;
-  int off_kc, off_vc, off_ks, off_kz, off_vs, off_vz;  // inside a paged head slab
+  int rb;          // bytes of one token row of codes (d * bits / 8)
+  int tile_bytes;  // one 16-token tile: K codes, V codes, (INT) V scales, V zeros
+  int hdr_bytes;   // record header: K scale + K zero of the record's Key group (INT: 1024, FP8: 0)
+  int tpg;         // tiles per record
+  int rec_bytes;   // hdr_bytes + tpg * tile_bytes
+  int nrec;        // contiguous: records per (seq, head)
+  long long block_bytes;  // paged: H records
 };
 
 struct CachePtrs {
-  void* k_codes;
-  void* v_codes;
-  float* k_scale;
-  float* k_zero;
-  float* v_scale;
-  float* v_zero;
+  void* qstore;
   void* block_pool;
   const int32_t* block_table;
   void* resid_k;
@@ -49,6 +48,7 @@ struct DecodeParams {
   int num_ctas;      // CTAs of the decode grid (partial slot space = num_ctas + batch*H)
   int nst;           // pipeline stages per warp
   int stage_bytes;   // bytes of one stage
+  int tps;           // quantized tiles per stage
   int bf_weight;     // work units charged to a bf16 tile (quantized tiles cost 1)
   float* ws_o;       // [slots][g][d] normalised partial outputs
   float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial

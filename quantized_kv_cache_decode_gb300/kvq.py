@@ -30,8 +30,7 @@ STATUS = {0: "KVQ_OK", -1: "KVQ_ERR_INVALID_ARG", -2: "KVQ_ERR_UNSUPPORTED", -3:
           -4: "KVQ_ERR_WORKSPACE"}
 DEV_BAD_BLOCK, DEV_CAPACITY, DEV_TIMEOUT = 0x1, 0x2, 0x4
 FORMATS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 16}
-FIELDS = ["k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "block_pool", "resid_k", "resid_v",
-          "sink_k", "sink_v"]
+FIELDS = ["qstore", "block_pool", "resid_k", "resid_v", "sink_k", "sink_v"]
 
 
 class KvqError(RuntimeError):
@@ -47,9 +46,8 @@ class LayerConfig(ctypes.Structure):
 
 
 class LayerCache(ctypes.Structure):
-    _fields_ = [(n, c_vp) for n in ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "block_pool",
-                                    "block_table", "resid_k", "resid_v", "sink_k", "sink_v", "k_tensor_scale",
-                                    "v_tensor_scale")]
+    _fields_ = [(n, c_vp) for n in ("qstore", "block_pool", "block_table", "resid_k", "resid_v", "sink_k", "sink_v",
+                                    "k_tensor_scale", "v_tensor_scale")]
 
 
 _P = ctypes.POINTER

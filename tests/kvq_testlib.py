@@ -116,16 +116,7 @@ class GpuLayer:
 
     # -- per-sequence view of the cache struct (batch = 1 calls) --
     def seq_struct(self, b: int):
-        c = self.layer.struct()
-        sz = self.layer.sizes
-        per = {n: sz[n] // self.B for n in sz}
-        for n in ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "resid_k", "resid_v", "sink_k",
-                  "sink_v"):
-            if getattr(c, n):
-                setattr(c, n, getattr(c, n) + b * per[n])
-        if self.paged:
-            c.block_table = c.block_table + b * self.mbps * 4
-        return c
+        return self.layer.seq_struct(b)
 
     def calibrate_fp8(self, k_all_bits: np.ndarray, v_all_bits: np.ndarray):
         torch = self.torch
@@ -178,46 +169,52 @@ class GpuLayer:
         return ko.cpu().numpy(), vo.cpu().numpy()
 
     # -- read the stored cache of (b, h) back into the oracle's logical form --
-    def logical(self, b: int, h: int, T: int) -> Dict[str, np.ndarray]:
-        n_sink, qn, r = O.token_split(T, self.spec)
-        out = {}
+    def _layout(self):
         rb = 128 * BITS[self.fmt] // 8
+        ngv = 128 // self.Gv
+        tile = 32 * rb + (0 if self.fp8 else 128 * ngv)
+        hdr = 0 if self.fp8 else 1024
+        tpg = (self.P // 16) if self.paged else (1 if self.fp8 else self.G // 16)
+        return rb, ngv, tile, hdr, tpg, hdr + tpg * tile
+
+    def _record(self, b: int, h: int, ri: int) -> np.ndarray:
+        rb, ngv, tile, hdr, tpg, rec = self._layout()
         if self.paged:
             pool = self.raw("block_pool")
-            slab_fields = self._slab_fields()
-            kc, vt, ks, kz, vs, vz = [], [], [], [], [], []
-            for bi in range(math.ceil(qn / self.P)):
-                blk = int(self.table_np[b, bi])
-                base = blk * self.block_bytes + h * self.slab_bytes
-                f = {k: pool[base + o: base + o + n] for k, (o, n) in slab_fields.items()}
-                kc.append(f["kc"].reshape(self.P, rb))
-                vt.append(f["vc"].reshape(self.P // 16, 16 * rb))
-                if not self.fp8:
-                    ks.append(f["ks"].view(F32).reshape(-1, 128))
-                    kz.append(f["kz"].view(F32).reshape(-1, 128))
-                    vs.append(f["vs"].view(F32).reshape(self.P, -1))
-                    vz.append(f["vz"].view(F32).reshape(self.P, -1))
-            kc = np.concatenate(kc)[:qn] if kc else np.zeros((0, rb), np.uint8)
-            vt = np.concatenate(vt) if vt else np.zeros((0, 16 * rb), np.uint8)
+            blk = int(self.table_np[b, ri])
+            base = blk * rec * self.H + h * rec
+            return pool[base:base + rec]
+        store = self.raw("qstore")
+        nrec = self.cfg.capacity_tokens // (16 * tpg)
+        base = ((b * self.H + h) * nrec + ri) * rec
+        return store[base:base + rec]
+
+    def logical(self, b: int, h: int, T: int) -> Dict[str, np.ndarray]:
+        n_sink, qn, r = O.token_split(T, self.spec)
+        rb, ngv, tile, hdr, tpg, rec = self._layout()
+        kc, vt, ks, kz, vs, vz = [], [], [], [], [], []
+        ntiles = (qn + 15) // 16
+        for i in range(ntiles):
+            recb = self._record(b, h, i // tpg)
+            t = recb[hdr + (i % tpg) * tile: hdr + (i % tpg + 1) * tile]
+            kc.append(t[:16 * rb].reshape(16, rb))
+            vt.append(t[16 * rb:32 * rb].reshape(1, 16 * rb))
             if not self.fp8:
-                out["k_s"] = np.concatenate(ks)[:qn // self.G] if ks else np.zeros((0, 128), F32)
-                out["k_z"] = np.concatenate(kz)[:qn // self.G] if kz else np.zeros((0, 128), F32)
-                out["v_s"] = np.concatenate(vs)[:qn] if vs else np.zeros((0, 128 // self.Gv), F32)
-                out["v_z"] = np.concatenate(vz)[:qn] if vz else np.zeros((0, 128 // self.Gv), F32)
-        else:
-            cap = self.cfg.capacity_tokens
-            pair = b * self.H + h
-            kc = self.raw("k_codes").reshape(self.B * self.H, cap, rb)[pair, :qn]
-            vt = self.raw("v_codes").reshape(self.B * self.H, cap // 16, 16 * rb)[pair]
-            if not self.fp8:
-                ng = cap // self.G
-                out["k_s"] = self.raw("k_scale").view(F32).reshape(self.B * self.H, ng, 128)[pair, :qn // self.G]
-                out["k_z"] = self.raw("k_zero").view(F32).reshape(self.B * self.H, ng, 128)[pair, :qn // self.G]
-                out["v_s"] = self.raw("v_scale").view(F32).reshape(self.B * self.H, cap, -1)[pair, :qn]
-                out["v_z"] = self.raw("v_zero").view(F32).reshape(self.B * self.H, cap, -1)[pair, :qn]
+                vs.append(t[32 * rb:32 * rb + 64 * ngv].view(F32).reshape(16, ngv))
+                vz.append(t[32 * rb + 64 * ngv:].view(F32).reshape(16, ngv))
+                if i % tpg == 0:
+                    ks.append(recb[:512].view(F32).reshape(1, 128))
+                    kz.append(recb[512:1024].view(F32).reshape(1, 128))
+        out = {}
+        kc = np.concatenate(kc)[:qn] if kc else np.zeros((0, rb), np.uint8)
+        vt = np.concatenate(vt) if vt else np.zeros((0, 16 * rb), np.uint8)
+        if not self.fp8:
+            out["k_s"] = np.concatenate(ks)[:qn // self.G] if ks else np.zeros((0, 128), F32)
+            out["k_z"] = np.concatenate(kz)[:qn // self.G] if kz else np.zeros((0, 128), F32)
+            out["v_s"] = np.concatenate(vs)[:qn] if vs else np.zeros((0, ngv), F32)
+            out["v_z"] = np.concatenate(vz)[:qn] if vz else np.zeros((0, ngv), F32)
         out["k_codes"] = unpack_k_rows(kc, self.fmt)
         out["v_codes"] = unpack_v_tiles(vt, self.fmt)[:qn] if len(vt) else np.zeros((0, 128), np.uint8)
-        # bf16 parts
         pair = b * self.H + h
         if n_sink:
             sk = self.raw("sink_k").view(np.uint16).reshape(self.B * self.H, self.S, 128)[pair, :n_sink]
@@ -230,22 +227,6 @@ class GpuLayer:
             slots = [(qn + i) % W for i in range(r)]
             out["resid_k"], out["resid_v"] = ring_k[slots], ring_v[slots]
         return out
-
-    def _slab_fields(self):
-        rb = 128 * BITS[self.fmt] // 8
-        P = self.P
-        f, o = {}, 0
-        f["kc"] = (o, P * rb); o += P * rb
-        f["vc"] = (o, P * rb); o += P * rb
-        if not self.fp8:
-            ngv = 128 // self.Gv
-            f["ks"] = (o, (P // self.G) * 512); o += (P // self.G) * 512
-            f["kz"] = (o, (P // self.G) * 512); o += (P // self.G) * 512
-            f["vs"] = (o, P * ngv * 4); o += P * ngv * 4
-            f["vz"] = (o, P * ngv * 4); o += P * ngv * 4
-        self.slab_bytes = (o + 15) // 16 * 16
-        self.block_bytes = self.slab_bytes * self.H
-        return f
 
 
 def compare_logical(gpu: Dict[str, np.ndarray], hc: "O.HeadCache"):

@@ -33,16 +33,15 @@ def test_status_strings(kvq):
 
 
 def test_cache_layout_sizes(kvq):
-    # Llama-3-70B-shaped INT4 layer, contiguous: codes 0.5 B per element, fp32 s/z per 128-token
-    # K group and per token V group, bf16 ring of R + G tokens
+    # Llama-3-70B-shaped INT4 layer, contiguous: a record per 128-token Key group =
+    # 1 KB header (fp32 K scale + zero) + 8 tiles of (2 x 1 KB codes + 16 x (4 + 4) B V scale/zero)
     cfg = kvq.make_config("int4", 8, 128, 128, 128, 0, capacity_tokens=8064)
     sz = kvq.cache_layout(cfg, 16)
     pairs = 16 * 8
-    assert sz["k_codes"] == pairs * 8064 * 64 and sz["v_codes"] == sz["k_codes"]
-    assert sz["k_scale"] == pairs * (8064 // 128) * 128 * 4 == sz["k_zero"]
-    assert sz["v_scale"] == pairs * 8064 * 1 * 4 == sz["v_zero"]
+    tile = 2 * 16 * 64 + 16 * 8
+    assert sz["qstore"] == pairs * (8064 // 128) * (1024 + 8 * tile)
     assert sz["resid_k"] == pairs * 256 * 128 * 2 and sz["sink_k"] == 0 and sz["block_pool"] == 0
-    # paged INT4, block 16 = G: slab = K codes 1024 + V codes 1024 + K s/z 1024 + V s/z 128 = 3200 B
+    # paged INT4, block 16 = G: one record per block and head = 1024 + 2048 + 128 = 3200 B
     cfg = kvq.make_config("int4", 8, 16, 128, 64, 1, paged=True, block_tokens=16, num_blocks=10,
                           max_blocks_per_seq=4)
     sz = kvq.cache_layout(cfg, 2)
@@ -51,7 +50,7 @@ def test_cache_layout_sizes(kvq):
     # FP8: 1 B per element, no scales, no ring
     cfg = kvq.make_config("fp8_e4m3", 8, 1, 128, 0, 0, capacity_tokens=8192)
     sz = kvq.cache_layout(cfg, 16)
-    assert sz["k_codes"] == 16 * 8 * 8192 * 128 and sz["k_scale"] == 0 and sz["resid_k"] == 0
+    assert sz["qstore"] == 16 * 8 * 8192 * 128 * 2 and sz["resid_k"] == 0
 
 
 @pytest.mark.parametrize("kw,status", [
