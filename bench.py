@@ -262,17 +262,15 @@ class Layer:
         self.kvq.quantize_append(self.cfg, self.struct, self.k_new, self.v_new, self.n_app, self.lens_before,
                                  self.B, self.status, stream)
 
-    def partials(self, stream=None):
-        self.kvq.decode_partials(self.cfg, self.struct, self.q, self.Hq, self.lens_after, self.B, self.scale,
-                                 self.ws, self.wsb, self.status, stream)
-
-    def combine(self, stream=None):
-        self.kvq.decode_combine(self.cfg, self.Hq, self.B, self.out, True, self.lse, self.ws, self.wsb, stream)
+    def decode(self, stream=None):
+        # one launch: split pass with the log-sum-exp merge fused in (last CTA per pair)
+        self.kvq.decode_attention(self.cfg, self.struct, self.q, self.Hq, self.lens_after, self.B, self.scale,
+                                  self.out, True, self.lse, self.ws, self.wsb, self.status, stream)
 
 
 def count_launches(w):
-    # per layer: append (1 kernel), decode split pass (1), combine (1)
-    return 3 * len(w.layer_formats)
+    # per layer: append (1 kernel) and decode (1 kernel, merge fused)
+    return 2 * len(w.layer_formats)
 
 
 def run_gpu(args, w, rank, world):
@@ -306,10 +304,9 @@ def run_gpu(args, w, rank, world):
             lay.append()
             if ev is not None:
                 ev[0][j].record(stream)
-            lay.partials()
+            lay.decode()
             if ev is not None:
                 ev[1][j].record(stream)
-            lay.combine()
 
     for i in range(args.warmup):
         step(i)
@@ -357,8 +354,7 @@ def run_gpu(args, w, rank, world):
             lay.k_new.copy_(h_k[j], non_blocking=True)
             lay.v_new.copy_(h_v[j], non_blocking=True)
             lay.append()
-            lay.partials()
-            lay.combine()
+            lay.decode()
             h_out[j].copy_(lay.out, non_blocking=True)
             h_lse[j].copy_(lay.lse, non_blocking=True)
 
@@ -554,7 +550,7 @@ def main():
         "tokens_per_s": round(len(r["lens_after"]) * world / (r["ms_step"] * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(kern_gbs / hbm_peak, 4), "traffic": traffic,
-                     "kernel": "decode_kernel (split pass)", "peak_source": peak_src,
+                     "kernel": "decode_kernel (fused merge)", "peak_source": peak_src,
                      "mean_launch_us": round(r["kern_ms"] * 1e3, 2)},
         "e2e": {"value": round(job_throughput(r["sbytes"], r["e2e_ms"], world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 4)},

@@ -21,8 +21,11 @@
  *   [AIQK] "양자화와 KV 캐시" (ai-trend.me)    PagedAttention: fixed-size blocks and a per-request table
  *
  * Conventions for every entry point
- *   - All buffers are owned by the caller.  The library allocates no memory and
- *     keeps no global state.  Pointers marked "device" are CUDA device pointers.
+ *   - All buffers are owned by the caller.  The library allocates no memory
+ *     (kvq_decode_attention_static_scratch excepted, see there) and keeps no
+ *     state between calls other than per-device caches of launch settings
+ *     (kernel occupancy, shared-memory limits).  Pointers marked "device" are
+ *     CUDA device pointers.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL =
  *     the legacy default stream).  They return once the work is enqueued.
  *   - A host-detectable error (bad sizes, unsupported combination, null pointer,

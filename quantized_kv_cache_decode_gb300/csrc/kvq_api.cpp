@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kvq_internal.h"
 
@@ -132,13 +133,40 @@ int fixed_smem(int batch, int warp_scratch) {
          kSegTableBytes + prefix;
 }
 
-cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
+cudaError_t occupancy_query(const LayerDesc& L, int smem, int* n) {
   switch (L.fmt) {
     case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, smem, n);
     case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, smem, n);
     case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, smem, n);
     default: return occupancy_decode_fp8(L.ngv, smem, n);
   }
+}
+
+// Resident CTAs per SM of the decode kernel for (device, format, Value groups,
+// shared memory), cached: the answer never changes for a given device.
+cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
+  struct Entry {
+    int dev, fmt, ngv, smem, n;
+  };
+  static std::mutex mu;
+  static Entry cache[256];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].dev == dev && cache[i].fmt == L.fmt && cache[i].ngv == L.ngv && cache[i].smem == smem) {
+        *n = cache[i].n;
+        return cudaSuccess;
+      }
+  }
+  e = occupancy_query(L, smem, n);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 256) cache[used++] = Entry{dev, L.fmt, L.ngv, smem, *n};
+  return cudaSuccess;
 }
 
 struct DecodeGeom {

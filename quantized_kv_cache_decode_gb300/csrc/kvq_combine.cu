@@ -29,19 +29,53 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const long long c_lo = ((P0 + 1) * C - 1) / U;
   const long long c_hi = (P1 * C - 1) / U;
   const long long pair = (long long)b * p.H + h;
-  // a CTA whose unit range is empty (fewer units than CTAs) wrote nothing
-  auto active = [&](long long cc) { return (cc * U) / C != ((cc + 1) * U) / C; };
-  float M = -INFINITY;
-  for (long long cc = c_lo; cc <= c_hi; ++cc)
-    if (active(cc)) M = fmaxf(M, p.ws_lse[(cc + pair) * p.g + r]);
-  float Lsum = 0.f, O = 0.f;
-  if (M != -INFINITY) {
+  // the CTAs whose unit range overlaps the pair and is not empty, listed once per block
+  __shared__ int act[64];
+  __shared__ int n_act;
+  if (c == 0) {
+    const long long qd = U / C, rd = U % C;
+    long long qv = (c_lo * U) / C, rv = (c_lo * U) % C;
+    int n = 0;
     for (long long cc = c_lo; cc <= c_hi; ++cc) {
-      if (!active(cc)) continue;
-      const long long slot = cc + pair;
-      const float f = exp2f(p.ws_lse[slot * p.g + r] - M);
-      Lsum += f;
-      O = fmaf(f, p.ws_o[(slot * p.g + r) * 128 + c], O);
+      long long qn = qv + qd, rn = rv + rd;
+      if (rn >= C) {
+        rn -= C;
+        ++qn;
+      }
+      if (qn != qv) {
+        if (n < 64) act[n] = (int)cc;
+        ++n;
+      }
+      qv = qn;
+      rv = rn;
+    }
+    n_act = n;
+  }
+  __syncthreads();
+  const int na = n_act;
+  float M = -INFINITY, Lsum = 0.f, O = 0.f;
+  if (na <= 64) {
+    for (int k = 0; k < na; ++k) M = fmaxf(M, p.ws_lse[((long long)act[k] + pair) * p.g + r]);
+    if (M != -INFINITY) {
+      for (int k = 0; k < na; ++k) {
+        const long long slot = (long long)act[k] + pair;
+        const float f = exp2f(p.ws_lse[slot * p.g + r] - M);
+        Lsum += f;
+        O = fmaf(f, p.ws_o[(slot * p.g + r) * 128 + c], O);
+      }
+    }
+  } else {
+    auto active = [&](long long cc) { return (cc * U) / C != ((cc + 1) * U) / C; };
+    for (long long cc = c_lo; cc <= c_hi; ++cc)
+      if (active(cc)) M = fmaxf(M, p.ws_lse[(cc + pair) * p.g + r]);
+    if (M != -INFINITY) {
+      for (long long cc = c_lo; cc <= c_hi; ++cc) {
+        if (!active(cc)) continue;
+        const long long slot = cc + pair;
+        const float f = exp2f(p.ws_lse[slot * p.g + r] - M);
+        Lsum += f;
+        O = fmaf(f, p.ws_o[(slot * p.g + r) * 128 + c], O);
+      }
     }
   }
   const bool empty = !(Lsum > 0.f);

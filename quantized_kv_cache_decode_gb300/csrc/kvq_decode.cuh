@@ -37,6 +37,8 @@
 // lop3 + one fma.f16x2 into B-operand registers.
 #pragma once
 
+#include <mutex>
+
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -321,6 +323,31 @@ __device__ __forceinline__ void write_out(const DecodeParams& p, int b, int hq, 
   if (p.lse && c == 0) p.lse[(long long)b * p.Hq + hq] = l2 * 0.69314718055994531f;
 }
 
+// CTAs c in [c_lo, c_hi] whose unit range [floor(cU/C), floor((c+1)U/C)) is not
+// empty, written to list[0..n) (at most cap entries; returns the full count).
+// Walks c with a running quotient/remainder: no division per step.
+__device__ __forceinline__ int active_ctas(long long c_lo, long long c_hi, long long U, long long C, int* list,
+                                           int cap) {
+  const long long qd = U / C, rd = U % C;
+  long long qv = (c_lo * U) / C, rv = (c_lo * U) % C;  // floor(c U / C), remainder
+  int n = 0;
+  for (long long c = c_lo; c <= c_hi; ++c) {
+    long long qn = qv + qd, rn = rv + rd;
+    if (rn >= C) {
+      rn -= C;
+      ++qn;
+    }
+    if (qn != qv) {
+      if (n < cap) list[n] = (int)c;
+      ++n;
+    }
+    qv = qn;
+    rv = rn;
+  }
+  return n;
+}
+constexpr int kMaxParts = 64;  // partials of one pair merged from a shared-memory list
+
 // One (sequence, kv head) pair's share of this CTA's unit range.
 struct SegRec {
   long long pair_start;  // first unit of the pair in the flat unit list
@@ -329,6 +356,18 @@ struct SegRec {
 };
 constexpr int kMaxSeg = 16;  // segments per table batch
 constexpr int kChunk = 2;    // quantized tiles per softmax step
+
+// Unit order inside a pair: the nbf bf16 tiles (wbf units each) are spread
+// evenly among the nq quantized tiles (1 unit each): bf16 tile i sits right
+// before quantized tile floor(i * nq / nbf).  Every warp's contiguous unit range
+// then gets its share of the (slower) bf16 tiles.
+__device__ __forceinline__ long long unit_of_bf(int i, int nbf, int nq, int wbf) {
+  return (long long)i * nq / nbf + (long long)i * wbf;
+}
+__device__ __forceinline__ long long unit_of_q(int k, int nbf, int nq, int wbf) {
+  const long long before = nbf == 0 ? 0 : min((long long)nbf, ((long long)(k + 1) * nbf + nq - 1) / nq);
+  return k + wbf * before;
+}
 
 // This warp's part of a segment: bf16 tiles [bf0, bf0 + nbf_w), quantized tiles
 // [q0, q0 + nq_w); stages: two per bf16 tile (its K rows, then its V rows), then
@@ -339,16 +378,29 @@ struct WarpPart {
 
 __device__ __forceinline__ WarpPart warp_part(const SegRec& sg, int warp, int wbf, int tps) {
   WarpPart w;
-  const int wa = sg.ua + (int)((long long)(sg.ue - sg.ua) * warp / kNW);
-  const int we = sg.ua + (int)((long long)(sg.ue - sg.ua) * (warp + 1) / kNW);
-  const int bf0 = (wa + wbf - 1) / wbf;
-  const int bf1 = min(sg.nbf, (we + wbf - 1) / wbf);
-  w.bf0 = bf0;
-  w.nbf_w = max(0, bf1 - bf0);
-  const int qbase = sg.nbf * wbf;
-  w.q0 = max(0, wa - qbase);
-  const int q1 = min(sg.nq, max(0, we - qbase));
-  w.nq_w = max(0, q1 - w.q0);
+  const long long wa = sg.ua + (long long)(sg.ue - sg.ua) * warp / kNW;
+  const long long we = sg.ua + (long long)(sg.ue - sg.ua) * (warp + 1) / kNW;
+  // first bf16 tile / quantized tile whose unit is at or after x
+  auto first_bf = [&](long long x) {
+    int lo = 0, hi = sg.nbf;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (unit_of_bf(mid, sg.nbf, sg.nq, wbf) >= x) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+  };
+  auto first_q = [&](long long x) {
+    int lo = 0, hi = sg.nq;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (unit_of_q(mid, sg.nbf, sg.nq, wbf) >= x) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+  };
+  w.bf0 = first_bf(wa);
+  w.nbf_w = first_bf(we) - w.bf0;
+  w.q0 = first_q(wa);
+  w.nq_w = first_q(we) - w.q0;
   w.nstage = 2 * w.nbf_w + (w.nq_w + tps - 1) / tps;
   return w;
 }
@@ -501,8 +553,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     }
     __syncthreads();
     const int nseg = seg_count;
-    load_q(segs[0]);
-    __syncthreads();
 
     // ---- producer (lane 0 copies; every lane keeps the same cursor) ----
     int ps = 0, pj = 0;
@@ -593,6 +643,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
       }
     };
     while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
+    // the query of the first segment, while the first copies are in flight
+    load_q(segs[0]);
+    __syncthreads();
 
     // ---- consumer ----
     for (int s = 0; s < nseg; ++s) {
@@ -922,31 +975,45 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         }
         if (p.fuse && !whole) {
           // the last CTA to finish this pair merges every partial of it
-          __shared__ int last_flag;
+          __shared__ int last_flag, n_act;
+          __shared__ int act[kMaxParts];
           __threadfence();
           __syncthreads();
           if (tid == 0) {
-            int nparts = 0;
-            for (long long cc = c_lo; cc <= c_hi; ++cc) nparts += ((cc * U) / C != ((cc + 1) * U) / C);
+            const int nparts = active_ctas(c_lo, c_hi, U, C, act, kMaxParts);
             const unsigned old = atomicAdd(&p.counters[pair], 1u);
             last_flag = (old + 1u == (unsigned)nparts);
             if (last_flag) p.counters[pair] = 0u;  // ready for the next call
+            n_act = nparts;
           }
           __syncthreads();
           if (last_flag) {
             __threadfence();
+            const int na = n_act;
             for (int i = tid; i < g * 128; i += kThreads) {
               const int hr = i >> 7, c = i & 127;
-              float M = -INFINITY;
-              for (long long cc = c_lo; cc <= c_hi; ++cc)
-                if ((cc * U) / C != ((cc + 1) * U) / C) M = fmaxf(M, __ldcg(&p.ws_lse[(cc + pair) * g + hr]));
-              float Lsum = 0.f, O = 0.f;
-              if (M != -INFINITY) {
-                for (long long cc = c_lo; cc <= c_hi; ++cc) {
-                  if ((cc * U) / C == ((cc + 1) * U) / C) continue;
-                  const float f = exp2f(__ldcg(&p.ws_lse[(cc + pair) * g + hr]) - M);
-                  Lsum += f;
-                  O = fmaf(f, __ldcg(&p.ws_o[((cc + pair) * g + hr) * 128 + c]), O);
+              float M = -INFINITY, Lsum = 0.f, O = 0.f;
+              if (na <= kMaxParts) {
+                for (int k2 = 0; k2 < na; ++k2) M = fmaxf(M, __ldcg(&p.ws_lse[((long long)act[k2] + pair) * g + hr]));
+                if (M != -INFINITY) {
+                  for (int k2 = 0; k2 < na; ++k2) {
+                    const long long sl = (long long)act[k2] + pair;
+                    const float f = exp2f(__ldcg(&p.ws_lse[sl * g + hr]) - M);
+                    Lsum += f;
+                    O = fmaf(f, __ldcg(&p.ws_o[(sl * g + hr) * 128 + c]), O);
+                  }
+                }
+              } else {
+                // more partials than the list holds (tiny per-CTA ranges): walk [c_lo, c_hi]
+                for (long long cc = c_lo; cc <= c_hi; ++cc)
+                  if ((cc * U) / C != ((cc + 1) * U) / C) M = fmaxf(M, __ldcg(&p.ws_lse[(cc + pair) * g + hr]));
+                if (M != -INFINITY) {
+                  for (long long cc = c_lo; cc <= c_hi; ++cc) {
+                    if ((cc * U) / C == ((cc + 1) * U) / C) continue;
+                    const float f = exp2f(__ldcg(&p.ws_lse[(cc + pair) * g + hr]) - M);
+                    Lsum += f;
+                    O = fmaf(f, __ldcg(&p.ws_o[((cc + pair) * g + hr) * 128 + c]), O);
+                  }
                 }
               }
               const bool empty = !(Lsum > 0.f);
@@ -971,21 +1038,35 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
   }
 }
 
+// Raise the kernel's dynamic shared-memory limit on the current device once per
+// size (the attribute is per device and persists; repeated calls are skipped).
+template <int FMT, int NGV>
+cudaError_t ensure_smem_attr(int smem) {
+  static std::mutex mu;
+  static int set_for[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
+  return e;
+}
+
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
-  auto k = decode_kernel<FMT, NGV>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV>(smem);
   if (e != cudaSuccess) return e;
-  k<<<p.num_ctas, kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV><<<p.num_ctas, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int FMT, int NGV>
 cudaError_t occupancy_t(int smem, int* n) {
-  auto k = decode_kernel<FMT, NGV>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV>, kThreads, smem);
 }
 
 }  // namespace kvq

@@ -46,8 +46,7 @@ def _check_layer(w, l, pairs, seed_offset=0):
     lay = bench.Layer(kvq, torch, w, l, fmt, lens_before, n_app, DEV, seed_offset=seed_offset)
     # one benchmark step
     lay.append()
-    lay.partials()
-    lay.combine()
+    lay.decode()
     torch.cuda.synchronize()
     assert lay.status.item() == 0
     out16 = lay.out.clone()
