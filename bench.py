@@ -291,20 +291,50 @@ def run_gpu(args, w, rank, world):
     for rep in reps:
         for lay in rep:
             assert lay.status.item() == 0, f"device status {lay.status.item()} while building"
-    stream = torch.cuda.current_stream()
     dist = world > 1
 
     def barrier():
         if dist:
             torch.distributed.barrier()
 
+    # Each layer's append and decode launches, captured once into two CUDA graphs per
+    # replica and layer: the timed loop replays them, so the host issues a step in a
+    # few microseconds and the device runs the kernels back to back.  Events between
+    # the graphs bracket each decode launch.
+    for rep in reps:  # first calls outside capture (launch settings, shared-memory limits)
+        for lay in rep:
+            lay.append()
+            lay.decode()
+    torch.cuda.synchronize()
+    graphs = None
+    if not args.no_graphs:
+        graphs = []
+        for rep in reps:
+            gl = []
+            for lay in rep:
+                ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(ga, capture_error_mode="relaxed"):
+                    lay.append()
+                with torch.cuda.graph(gd, capture_error_mode="relaxed"):
+                    lay.decode()
+                gl.append((ga, gd))
+            graphs.append(gl)
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
     def step(i, ev=None):
         rep = reps[i % replicas]
         for j, lay in enumerate(rep):
-            lay.append()
+            if graphs is not None:
+                graphs[i % replicas][j][0].replay()
+            else:
+                lay.append()
             if ev is not None:
                 ev[0][j].record(stream)
-            lay.decode()
+            if graphs is not None:
+                graphs[i % replicas][j][1].replay()
+            else:
+                lay.decode()
             if ev is not None:
                 ev[1][j].record(stream)
 
@@ -484,6 +514,7 @@ def main():
     ap.add_argument("--replicas", type=int, default=0, help="cache copies cycled to defeat L2 (0: auto)")
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true", help="time direct library calls instead of graph replays")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     w = I.WORKLOADS[args.workload]()
@@ -545,7 +576,9 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16/f32 (fp8/int codes)", "data": "synthetic",
         "config": {**config, "l2": f"{r['replicas']} rotating cache copies, {r['replicas'] * r['sbytes'] / 1e6:.0f} MB"
-                   f" cycled (L2 {L2_BYTES / 2 ** 20:.0f} MiB)", "bytes_per_step": r["sbytes"]},
+                   f" cycled (L2 {L2_BYTES / 2 ** 20:.0f} MiB)", "bytes_per_step": r["sbytes"],
+                   "launch": "direct library calls" if args.no_graphs else
+                   "per-layer CUDA graphs of the library calls (append, decode), replayed"},
         "pct_hbm_peak": round(100 * gbs / world / hbm_peak, 2),
         "tokens_per_s": round(len(r["lens_after"]) * world / (r["ms_step"] * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",

@@ -80,7 +80,7 @@ typedef struct {
   int32_t head_dim;           /* d, must be 128 */
   int32_t format;             /* kvq_format */
   int32_t k_group_tokens;     /* G: tokens per Key group (per-channel scale); multiple of 16; 1 for FP8 */
-  int32_t v_group_dims;       /* Gv: channels per Value group (per-token scale); 8,16,32,64,128; FP8: 128 */
+  int32_t v_group_dims;       /* Gv: channels per Value group (per-token scale); 16,32,64,128; FP8: 128 */
   int32_t residual_tokens;    /* R >= 0 bf16 recent tokens kept (0 for FP8) */
   int32_t sink_tokens;        /* S >= 0 bf16 first tokens kept */
   int32_t paged;              /* 0: contiguous store, 1: paged store */
@@ -97,7 +97,7 @@ typedef struct {
  * ngv = d / Gv.  Only quantized tokens x = t - S live in the quantized store.
  *
  * A 16-token tile (quantized tokens 16i .. 16i+15) is, in this order:
- *   K codes  [16][rb]     token row; channel c in byte c/(8/b) at bit (c mod (8/b))*b
+ *   K codes  [16*rb]      in "fragment order" (below)
  *   V codes  [16*rb]      in "fragment order" (below)
  *   V scale  [16][ngv] f32, V zero [16][ngv] f32   (INT only: per token, per Gv channels)
  * tile_bytes = 32*rb (+ 128*ngv for INT).
@@ -120,14 +120,21 @@ typedef struct {
  * FP8: k_tensor_scale, v_tensor_scale point to one device float each (amax/448,
  * see kvq_fp8_calibrate); they stay fixed for later appends.
  *
- * Fragment order of a 16-token Value tile (token t in [0,16), channel c in
- * [0,128)): n = c mod 8, j = c / 8, lane = 4n + (t mod 8)/2, e = (t mod 2) + 2(t / 8).
- *   INT4: byte lane*32 + 4(j/2) + o/8, bits o mod 8, o = {0,16,4,20}[e] + 8(j mod 2)
- *   INT2: byte lane*16 + 4(j/4) + o/8, bits o mod 8, o = 2(2(j mod 4) + e/2) + 16(e mod 2)
- *   INT8: byte lane*64 + 4j + {0,2,1,3}[e]
- *   FP8:  byte lane*64 + 4j + e
- * i.e. each lane of a decode warp reads one contiguous run whose words unpack
- * directly into tensor-core operand registers.
+ * Fragment order.  The K codes and the V codes of a tile are each a 16 x 128
+ * code matrix stored as the register file of a tensor-core A operand
+ * (mma m16n8k16): element (row i, column k) of step s (s in [0,8)) goes to
+ * lane 4(i mod 8) + (k mod 8)/2, register reg = (i / 8) + 2(k / 8), half
+ * h = k mod 2.  For the K codes of token t, channel c: s = c/16, i = t, and
+ * with e = c mod 4, k = 2((c/4) mod 4) + (e mod 2) + 8(e/2).  For the V codes
+ * of token t, channel c: s = c/16, i = c mod 16, k = t.
+ * Lane l owns rb/8 32-bit words; word w of lane l is at byte
+ * ((w/4)*32 + l)*16 + (w mod 4)*4, and (lane, s, reg, h) is placed at
+ *   INT4: word s,               bit 4 reg + 16 h
+ *   INT2: word s/2,             bit 8(s mod 2) + 2 reg + 16 h
+ *   INT8: word 2s + reg/2,      bit 8((reg mod 2) + 2h)
+ *   FP8:  word 2s + reg/2,      bit 8(2(reg mod 2) + h)
+ * so that every lane of a decode warp fetches its words with conflict-free
+ * 16-byte loads and unpacks them in registers.
  */
 typedef struct {
   void* qstore;               /* contiguous quantized store (paged == 0) */

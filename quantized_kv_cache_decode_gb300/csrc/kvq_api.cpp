@@ -14,9 +14,9 @@ namespace {
 
 constexpr int kThreadsDecode = 128;  // 4 warps (kvq_decode.cuh)
 constexpr int kMaxStages = 4;
-constexpr int kWarpScratch = 16 * 272;
-constexpr int kSmem3PerSm = 74 * 1024;          // per-CTA budget for three resident CTAs per SM
-constexpr int kSmem2PerSm = 112 * 1024;         // ... for two
+constexpr int kSmemPerSm = 228 * 1024;          // shared memory of one SM
+constexpr int kSmemReservedPerCta = 1024;         // reserved by the system for each resident CTA
+constexpr int kStaticSmemMargin = 1024;           // the kernel's static __shared__ variables (384 B)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -101,53 +101,56 @@ kvq_status check_cache(const LayerDesc& L, const kvq_layer_cache* c) {
   return KVQ_OK;
 }
 
-// Quantized tiles per pipeline stage: about 8 KB of cache bytes per stage.
-int tiles_per_stage(const LayerDesc& L) {
+// Quantized tiles per pipeline stage: about `target` bytes of cache per stage.
+int tiles_per_stage(const LayerDesc& L, int target) {
   const int per = L.tile_bytes + (L.hdr_bytes + L.tpg - 1) / L.tpg;
-  return std::max(1, std::min(8, (8192 + per / 2) / per));
+  return std::max(1, std::min(8, (target + per / 2) / per));
 }
 
 // A stage holds a header slot, tps tiles and the record headers between them,
-// or one half (K or V rows) of a 16-token bf16 tile at 272 bytes per row.
-int stage_bytes_of(const LayerDesc& L) {
-  const int tps = tiles_per_stage(L);
+// or (layers with bf16 tokens) one half (K or V rows) of a 16-token bf16 tile
+// at 272 bytes per row.
+int stage_bytes_of(const LayerDesc& L, int tps) {
   const int inline_hdrs = (tps + L.tpg - 1) / L.tpg;
   const int q = L.hdr_bytes + tps * L.tile_bytes + inline_hdrs * L.hdr_bytes;
-  const int bf = 16 * 272;
+  const bool bf16_tiles = L.S > 0 || !L.fp8;
+  const int bf = bf16_tiles ? 16 * 272 : 0;
   return (std::max(q, bf) + 127) / 128 * 128;
 }
 
-// Shared scratch per warp: a padded bf16 tile when the layer keeps bf16 tokens
-// (sink or residual window), else just the warp's merge record (g heads).
-int warp_scratch_of(const LayerDesc& L, int g) {
-  const bool bf16_tiles = L.S > 0 || !L.fp8;
-  const int merge = g * 132 * 4;
-  return bf16_tiles ? std::max(kWarpScratch, merge) : merge;
+// The CTA's merge record in shared memory: m, l, -, - and 128 outputs per query head.
+int merge_bytes_of(const LayerDesc& L, int g) {
+  (void)L;
+  return g * 132 * 4;
 }
 
 constexpr int kSegTableBytes = 16 * 48;  // kMaxSeg segment records of 48 bytes (kvq_decode.cuh)
 
-int fixed_smem(int batch, int warp_scratch) {
+int fixed_smem(int batch, int merge_bytes) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16;
-  return kThreadsDecode / 32 * kMaxStages * 8 + 8 * 4 * 36 * 4 + kThreadsDecode / 32 * warp_scratch +
-         kSegTableBytes + prefix;
+  // barriers and block-table windows per warp, the query rows (g + 1), the merge record
+  const int g = merge_bytes / (132 * 4);
+  return kThreadsDecode / 32 * (kMaxStages * 8 + 32 * 4) + (g + 1) * 132 * 4 + merge_bytes + kSegTableBytes +
+         prefix;
 }
 
-cudaError_t occupancy_query(const LayerDesc& L, int smem, int* n) {
+cudaError_t occupancy_query(const LayerDesc& L, int g, int smem, int* n) {
   switch (L.fmt) {
-    case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, smem, n);
-    case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, smem, n);
-    case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, smem, n);
-    default: return occupancy_decode_fp8(L.ngv, smem, n);
+    case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, g, smem, n);
+    case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, g, smem, n);
+    case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, g, smem, n);
+    default: return occupancy_decode_fp8(L.ngv, g, smem, n);
   }
 }
 
 // Resident CTAs per SM of the decode kernel for (device, format, Value groups,
-// shared memory), cached: the answer never changes for a given device.
-cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
+// query column blocks, shared memory), cached: the answer never changes for a
+// given device.
+cudaError_t occupancy(const LayerDesc& L, int g, int smem, int* n) {
   struct Entry {
-    int dev, fmt, ngv, smem, n;
+    int dev, fmt, ngv, nbq, smem, n;
   };
+  const int nbq = g <= 4 ? 1 : 2;
   static std::mutex mu;
   static Entry cache[256];
   static int used = 0;
@@ -157,50 +160,68 @@ cudaError_t occupancy(const LayerDesc& L, int smem, int* n) {
   {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
-      if (cache[i].dev == dev && cache[i].fmt == L.fmt && cache[i].ngv == L.ngv && cache[i].smem == smem) {
+      if (cache[i].dev == dev && cache[i].fmt == L.fmt && cache[i].ngv == L.ngv && cache[i].nbq == nbq &&
+          cache[i].smem == smem) {
         *n = cache[i].n;
         return cudaSuccess;
       }
   }
-  e = occupancy_query(L, smem, n);
+  e = occupancy_query(L, g, smem, n);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (used < 256) cache[used++] = Entry{dev, L.fmt, L.ngv, smem, *n};
+  if (used < 256) cache[used++] = Entry{dev, L.fmt, L.ngv, nbq, smem, *n};
   return cudaSuccess;
 }
 
 struct DecodeGeom {
-  int smem, nst, stage_bytes, num_ctas, warp_scratch;
+  int smem, nst, stage_bytes, tps, num_ctas, merge_bytes;
   size_t ws_bytes, off_lse, off_prefix, off_counters;
 };
 
+// Launch shape: two stages per warp (one being computed on, one in flight),
+// as many resident CTAs per SM as the registers allow (4 for up to 4 query
+// heads per kv head, 3 above) with stages of about 4 KB -- the integer formats
+// are bound by the tensor-core and unpack work per byte, so warps count most --
+// and, for FP8 (the least work per byte), 3 CTAs with stages of about 8 KB.
+// Fewer CTAs or smaller stages when the shared memory does not fit.  (Chosen
+// from a sweep of CTAs x stage size x stage count on GB300.)
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) {
-  const int sb = stage_bytes_of(L);
-  const int wsc = warp_scratch_of(L, g);
+  const int wsc = merge_bytes_of(L, g);
   const int fixed = fixed_smem(batch, wsc);
-  // As many stages as fit three CTAs per SM; if the kernel's registers allow only two
-  // CTAs per SM anyway, spend the shared memory of the third on deeper pipelines.
-  auto fit = [&](int budget) {
-    int n = kMaxStages;
-    while (n > 2 && fixed + (kThreadsDecode / 32) * n * sb > budget) --n;
-    return fixed + (kThreadsDecode / 32) * n * sb <= budget ? n : 0;
-  };
+  const int nw = kThreadsDecode / 32;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  int nst = fit(kSmem3PerSm);
-  if (nst) {
-    if (occupancy(L, fixed + (kThreadsDecode / 32) * nst * sb, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
-    if (per_sm < 3) nst = 0;
+  const int pref_ctas = L.fp8 ? 3 : (g <= 4 ? 4 : 3);
+  const int n = 2;
+  int smem = 0, nst = 0, sb = 0, tps = 0;
+  bool found = false;
+  for (int ctas = pref_ctas; ctas >= 1 && !found; --ctas) {
+    const int budget = std::min(kSmemPerSm / ctas - kSmemReservedPerCta, 227 * 1024) - kStaticSmemMargin;
+    for (int target : {8192, 6144, 4096}) {
+      if (!L.fp8 && target != 4096) continue;
+      const int t = tiles_per_stage(L, target);
+      const int b = stage_bytes_of(L, t);
+      if (fixed + nw * n * b > budget && ctas > 1) continue;
+      if (occupancy(L, g, fixed + nw * n * b, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
+      if (per_sm >= ctas) {
+        smem = fixed + nw * n * b;
+        nst = n;
+        sb = b;
+        tps = t;
+        found = true;
+        break;
+      }
+    }
   }
-  if (nst == 0) nst = std::max(2, fit(kSmem2PerSm));
-  const int smem = fixed + (kThreadsDecode / 32) * nst * sb;
-  if (occupancy(L, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (!found) return KVQ_ERR_UNSUPPORTED;
+  if (occupancy(L, g, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
   if (per_sm < 1) return KVQ_ERR_UNSUPPORTED;
   G->smem = smem;
-  G->warp_scratch = wsc;
+  G->merge_bytes = wsc;
   G->nst = nst;
   G->stage_bytes = sb;
+  G->tps = tps;
   G->num_ctas = sms * per_sm;
   const size_t slots = (size_t)G->num_ctas + (size_t)batch * L.H;
   const size_t o_bytes = slots * g * kHeadDim * sizeof(float);
@@ -325,7 +346,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.num_ctas = G.num_ctas;
   p.nst = G.nst;
   p.stage_bytes = G.stage_bytes;
-  p.tps = tiles_per_stage(L);
+  p.tps = G.tps;
   // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
   p.bf_weight = std::max(1, (8192 + L.tile_bytes / 2) / L.tile_bytes);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -333,7 +354,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.ws_lse = reinterpret_cast<float*>(ws + G.off_lse);
   p.ws_prefix = reinterpret_cast<int*>(ws + G.off_prefix);
   p.status = dev_status;
-  p.warp_scratch = G.warp_scratch;
+  p.merge_bytes = G.merge_bytes;
   p.fuse = out != nullptr;
   p.counters = reinterpret_cast<unsigned*>(ws + G.off_counters);
   p.out = out;

@@ -11,6 +11,8 @@
 // Every arithmetic step of the quantizer is one IEEE fp32 operation with
 // round-to-nearest-even and no contraction (explicit __f*_rn intrinsics), so
 // codes, scales and zero-points are reproducible bit for bit.
+#include <mutex>
+
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -75,12 +77,20 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
       uint8_t* rec = record_w(L, p.C, b, h, i / L.tpg, tid == 0 ? p.status : nullptr);
       if (!rec) continue;
       uint8_t* tile = rec + L.hdr_bytes + (long long)(i % L.tpg) * L.tile_bytes;
+      if (x % 16 == 0) {
+        // a new tile: clear it, so the codes of tokens not yet written read as 0
+        for (int w = tid; w < 2 * 16 * L.rb / 16; w += kAppendThreads)
+          reinterpret_cast<uint4*>(tile)[w] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+      }
       const int c = tid;
+      const int tt = (int)(x % 16);
       const float kx = __bfloat162float(knew[(t - T0) * L.d + c]);
       const float vx = __bfloat162float(vnew[(t - T0) * L.d + c]);
-      tile[(x % 16) * L.rb + c] = f32_to_e4m3(__fdiv_rn(kx, sk));
       int byte, bit;
-      vtile_pos(8, true, (int)(x % 16), c, byte, bit);
+      ktile_pos(8, true, tt, c, byte, bit);
+      tile[byte] = f32_to_e4m3(__fdiv_rn(kx, sk));
+      vtile_pos(8, true, tt, c, byte, bit);
       tile[16 * L.rb + byte] = f32_to_e4m3(__fdiv_rn(vx, sv));
     }
   } else {
@@ -90,8 +100,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
     float* vf = kf + G * 128;                           // [G][128]
     uint8_t* kq = reinterpret_cast<uint8_t*>(vf + G * 128);  // [G][128]
     uint8_t* vq = kq + G * 128;                          // [G][128]
-    uint32_t* tile = reinterpret_cast<uint32_t*>(vq + G * 128);  // one V tile (16 * rb bytes)
-    const int per_byte = 8 / L.bits;
+    uint32_t* tile = reinterpret_cast<uint32_t*>(vq + G * 128);  // one tile's K and V codes (2 * 16 * rb bytes)
     for (int grp = t0s.qn / G; grp < t1s.qn / G; ++grp) {
       const long long x0 = (long long)grp * G;  // first quantized index of the group
       // gather the group's tokens: old ones from the ring, new ones from the input
@@ -148,26 +157,22 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
           tvs[16 * L.ngv + (tt % 16) * L.ngv + j] = z;
         }
         __syncthreads();
-        // K codes, packed little-endian along d, 16 rows per tile
-        for (int i = tid; i < G * L.rb; i += kAppendThreads) {
-          const int tt = i / L.rb, kb = i % L.rb;
-          uint32_t v = 0;
-          for (int e = 0; e < per_byte; ++e) v |= (uint32_t)kq[tt * 128 + kb * per_byte + e] << (e * L.bits);
-          rec[L.hdr_bytes + (long long)(tt / 16) * L.tile_bytes + (tt % 16) * L.rb + kb] = (uint8_t)v;
-        }
-        // V codes, 16-token tiles in fragment order
-        const int tile_words = 16 * L.rb / 4;
+        // K and V codes of each 16-token tile, in fragment order
+        const int tile_words = 2 * 16 * L.rb / 4;  // K part, then V part
+        uint32_t* vtile = tile + 16 * L.rb / 4;
         for (int t16 = 0; t16 < G / 16; ++t16) {
           for (int i = tid; i < tile_words; i += kAppendThreads) tile[i] = 0u;
           __syncthreads();
           for (int i = tid; i < 16 * 128; i += kAppendThreads) {
             const int tt = i >> 7, c = i & 127;
             int byte, bit;
+            ktile_pos(L.bits, false, tt, c, byte, bit);
+            atomicOr(&tile[byte >> 2], (uint32_t)kq[(t16 * 16 + tt) * 128 + c] << ((byte & 3) * 8 + bit));
             vtile_pos(L.bits, false, tt, c, byte, bit);
-            atomicOr(&tile[byte >> 2], (uint32_t)vq[(t16 * 16 + tt) * 128 + c] << ((byte & 3) * 8 + bit));
+            atomicOr(&vtile[byte >> 2], (uint32_t)vq[(t16 * 16 + tt) * 128 + c] << ((byte & 3) * 8 + bit));
           }
           __syncthreads();
-          uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes + 16 * L.rb);
+          uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes);
           for (int i = tid; i < tile_words; i += kAppendThreads) dst[i] = tile[i];
           __syncthreads();
         }
@@ -195,9 +200,21 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int blocks = p.batch * p.L.H;
   if (blocks == 0 || p.n_new == 0) return cudaSuccess;
   size_t smem = 0;
-  if (!p.L.fp8) smem = (size_t)p.L.G * 128 * (4 + 4 + 1 + 1) + 16 * (size_t)p.L.rb;
-  cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  if (!p.L.fp8) smem = (size_t)p.L.G * 128 * (4 + 4 + 1 + 1) + 2 * 16 * (size_t)p.L.rb;
+  {
+    // the limit is a per-device attribute that persists: raise it once per size
+    static std::mutex mu;
+    static int set_for[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64 || set_for[dev] < (int)smem) {
+      e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) set_for[dev] = (int)smem;
+    }
+  }
   append_kernel<<<blocks, kAppendThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -97,6 +97,11 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                                   uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -212,28 +217,48 @@ __device__ __forceinline__ const __nv_bfloat16* bf16_row(const LayerDesc& L, con
   return ring + (pair * L.W + slot) * L.d;
 }
 
-// Byte offset (inside a 16-token V tile in fragment order) and bit position of
-// element (token t, channel c).  Matches the decode kernel's operand unpacking.
-__host__ __device__ __forceinline__ void vtile_pos(int bits, bool fp8, int t, int c, int& byte, int& bit) {
-  const int n = c & 7, j = c >> 3, q = (t & 7) >> 1, e = (t & 1) + 2 * (t >> 3);
-  const int lane = 4 * n + q;
-  if (fp8) {
-    byte = lane * 64 + 4 * j + e;
-    bit = 0;
-  } else if (bits == 8) {
-    const int m[4] = {0, 2, 1, 3};
-    byte = lane * 64 + 4 * j + m[e];
-    bit = 0;
-  } else if (bits == 4) {
-    const int m[4] = {0, 16, 4, 20};
-    const int o = m[e] + 8 * (j & 1);
-    byte = lane * 32 + 4 * (j >> 1) + (o >> 3);
-    bit = o & 7;
-  } else {  // 2 bits
-    const int o = 2 * (2 * (j & 3) + (e >> 1)) + 16 * (e & 1);
-    byte = lane * 16 + 4 * (j >> 2) + (o >> 3);
-    bit = o & 7;
+// --------------------------------------------------------------------------
+// code tiles in fragment order
+// --------------------------------------------------------------------------
+// A 16-token tile stores its Key codes and its Value codes, each a 16 x 128
+// matrix of codes, in the register order of the mma.sync m16n8k16 A operand,
+// so that each lane fetches its own operand words with 16-byte shared-memory
+// loads (consecutive lanes 16 bytes apart: no bank conflicts) and unpacks them
+// in registers.  Step s of the A operand (s = 0..7) gives lane 4r+q four
+// registers, each a pair (half 0, half 1):
+//   reg 0: (row r, col 2q+h)    reg 1: (row r+8, col 2q+h)
+//   reg 2: (row r, col 2q+8+h)  reg 3: (row r+8, col 2q+8+h)
+// Keys:   rows = the 16 tokens, step s covers channels 16s..16s+15, column
+//         2q + (e & 1) + 8 (e >> 1) of the step holding channel 16s + 4q + e.
+// Values: rows = channels 16s + i (i = 0..15), columns = the 16 tokens.
+// Word w of lane l sits at byte ((w >> 2) * 32 + l) * 16 + (w & 3) * 4; a
+// lane owns rb / 8 words (rb = bytes of one token row of codes).
+__host__ __device__ __forceinline__ void frag_pos(int bits, bool fp8, int lane, int step, int reg, int half,
+                                                  int& byte, int& bit) {
+  int w, bitpos;
+  if (bits == 4) {  // one word per step: bits 4*reg + 16*half
+    w = step;
+    bitpos = 4 * reg + 16 * half;
+  } else if (bits == 2) {  // one word per two steps: bits 8*(step&1) + 2*reg + 16*half
+    w = step >> 1;
+    bitpos = 8 * (step & 1) + 2 * reg + 16 * half;
+  } else {  // 8-bit codes: two words per step (regs 0-1, regs 2-3)
+    w = 2 * step + (reg >> 1);
+    bitpos = 8 * (fp8 ? 2 * (reg & 1) + half : (reg & 1) + 2 * half);
   }
+  byte = ((w >> 2) * 32 + lane) * 16 + (w & 3) * 4 + (bitpos >> 3);
+  bit = bitpos & 7;
+}
+
+// Key code of (token t, channel c) inside the tile's Key part
+__host__ __device__ __forceinline__ void ktile_pos(int bits, bool fp8, int t, int c, int& byte, int& bit) {
+  const int e = c & 3;
+  frag_pos(bits, fp8, 4 * (t & 7) + ((c >> 2) & 3), c >> 4, (t >> 3) + 2 * (e >> 1), e & 1, byte, bit);
+}
+// Value code of (token t, channel c) inside the tile's Value part
+__host__ __device__ __forceinline__ void vtile_pos(int bits, bool fp8, int t, int c, int& byte, int& bit) {
+  const int i = c & 15;
+  frag_pos(bits, fp8, 4 * (i & 7) + ((t & 7) >> 1), c >> 4, (i >> 3) + 2 * (t >> 3), t & 1, byte, bit);
 }
 
 }  // namespace kvq

@@ -7,34 +7,36 @@
 // cache, section 1).
 //
 // Work decomposition.  Every (sequence, kv head) pair is a list of work units:
-// 16-token bf16 tiles (sink + residual window, charged `bf_weight` units) and
-// 16-token quantized tiles (1 unit).  The pairs' lists are concatenated and cut
-// into num_ctas equal ranges, one per CTA (num_ctas = SMs x resident CTAs), so
-// every CTA moves the same number of bytes whatever the sequence lengths.  A
-// CTA writes one partial (normalised output + log-sum-exp) per pair it touches,
-// into slot cta + pair; a second kernel merges the partials of each pair.
+// its 16-token bf16 tiles (sink + residual window, charged `bf_weight` units
+// each) followed by its 16-token quantized tiles (1 unit each).  The pairs'
+// lists are concatenated and cut into num_ctas equal ranges, one per CTA
+// (num_ctas = SMs x resident CTAs), so every CTA moves the same number of bytes
+// whatever the sequence lengths.  A CTA writes one partial (normalised output +
+// log-sum-exp) per pair it touches; the last CTA to finish a pair merges them.
 //
-// Inside a CTA each of the 4 warps takes a contiguous sub-range and runs its
-// own pipeline: its lane 0 streams 16-token tiles (codes, scales) into shared
-// memory with bulk asynchronous copies (cp.async.bulk, TMA engine) completing
-// on per-stage mbarriers, several stages ahead of the compute.
+// Inside a CTA the 4 warps split each pair's bf16 tiles and quantized tiles
+// evenly and run their own pipelines: lane 0 of a warp streams stages (tiles
+// with their scales) into shared memory with bulk asynchronous copies
+// (cp.async.bulk, TMA engine) completing on per-stage mbarriers, several stages
+// ahead of the compute.
 //
-// Tensor-core mapping (mma.sync m16n8k16, fp32 accumulate).  The 16 MMA rows
-// are the g <= 8 query heads of the kv head (row r) and, in rows r + 8, the
-// low-order half of a two-term split of the same operand, so operands that are
-// not exactly representable in 16 bits keep ~22 bits:
-//   QK:  D[head][token] += A[head][channel] * B[channel][token]
-//        A = q_c * s_c (Key scale of the channel, hi/lo split), B = centred Key
-//        codes (exact in f16); the zero-point term sum_c q_c s_c (2^(b-1) - z_c)
-//        is added per group in fp32.  FP8: A = q (exact in f16 after a power-of-
-//        two rescale), B = E4M3 codes (exact in f16).  bf16 tiles: A = q, B = K.
-//   PV:  D[head][channel] += A[head][token] * B[token][channel]
-//        A = p_t * s_t (Value scale of the token, hi/lo split), B = centred Value
-//        codes; zero-point term accumulated per Value group in fp32.
-// The score tile of QK comes out of the MMA in exactly the register layout the
-// PV A operand needs, so probabilities never leave registers.  Values are
-// stored in "fragment order" so that each lane's 32-bit words unpack with one
-// lop3 + one fma.f16x2 into B-operand registers.
+// Tensor-core mapping (mma.sync m16n8k16, fp32 accumulate).  The cache tile is
+// the A operand (16 rows), the query side the B operand (8 columns):
+//   QK:  D[token][col] = sum_c K[token][c] * Bq[c][col].  A = centred Key codes
+//        (exact in f16), Bq = q_c s_c kappa (Key scale of the channel), split in
+//        two f16 halves: column 2j holds the high half and column 2j+1 the low
+//        half of query head 4b + j (b = column block), so the score of head
+//        4b + q sits in one lane, ~22 bits exact.  The zero-point term
+//        sum_c q_c s_c (2^(b-1) - z_c) is added per group in fp32.  FP8: A = E4M3
+//        codes (exact in f16), Bq = q kappa.  bf16 tiles: A = K, B = q (bf16).
+//   PV:  D[channel][head] = sum_t V^T[channel][t] * W[t][head], A = centred
+//        Value codes of 16 channels, W = p_t s_t (Value scale of the token and
+//        channel group) in f16; zero-point term accumulated per group in fp32.
+//        bf16 tiles: A = V (bf16), W split in two bf16 terms.
+// The probabilities move from the score layout (lane = head) to the W layout
+// (lane = token pair) with four shuffles per tile.  The codes are stored in the
+// A operand's register order (include/kvq.h, "fragment order"): each lane loads
+// its words with conflict-free 16-byte loads and unpacks them in registers.
 #pragma once
 
 #include <mutex>
@@ -49,11 +51,9 @@ constexpr int kMaxStages = 4;
 constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 range is safe
 constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
 constexpr float kSTau = 4.f;           // a Value scale may exceed its reference 4x before a rescale
-constexpr int kQStride = 36;           // floats per (head, lane-group) chunk of the query in smem
-constexpr int kBfRow = 272;            // bytes per bf16 row in the warp scratch (256 + 16 pad)
-constexpr int kWarpScratch = 16 * kBfRow;   // 4352 B: bf16 V tile, later the warp's merge record
-                                            // (smaller when the layer has no bf16 tiles: p.warp_scratch)
-constexpr int kMergeStride = 132;      // floats per head in the merge record: m, l, -, -, o[128]
+constexpr int kQRow = 132;             // floats per query head in shared memory (128 + 4 pad)
+constexpr int kBfRow = 272;            // bytes per bf16 row in a stage (256 + 16 pad: ldmatrix without conflicts)
+constexpr int kMergeStride = 132;      // floats per head in a warp's merge record: m, l, -, -, o[128]
 constexpr unsigned kFull = 0xffffffffu;
 
 __host__ __device__ constexpr uint32_t f16_bits_of_int(int v) {
@@ -76,29 +76,13 @@ struct FT {
   static constexpr bool kInt = !kFp8;
   static constexpr int kBits = kFp8 ? 8 : FMT;
   static constexpr int kRB = 128 * kBits / 8;   // bytes of one token row of codes
-  static constexpr int kTile = 16 * kRB;        // bytes of 16 rows
-  static constexpr int kKChunk = kRB / 4;       // bytes of a lane's 32 channels in a row
-  static constexpr int kVChunk = kTile / 32;    // bytes of a lane's share of a V tile
+  static constexpr int kTile = 16 * kRB;        // bytes of the 16 x 128 code matrix
+  static constexpr int kWords = kRB / 8;        // operand words of one lane per code matrix
   static constexpr int kHalf = kFp8 ? 0 : (1 << (kBits - 1));
 };
 
-// Channels (relative to the lane's 32-channel window) held in the low / high
-// half of unpacked Key register j.
-template <int FMT>
-__host__ __device__ constexpr int kchan0(int j) {
-  return FMT == 4 ? 8 * (j / 4) + (j % 4)
-       : FMT == 2 ? 16 * (j / 8) + (j % 8)
-       : FMT == 8 ? 4 * (j / 2) + (j % 2)
-                  : 2 * j;  // FP8 and bf16: natural pairs
-}
-template <int FMT>
-__host__ __device__ constexpr int kchan1(int j) {
-  return FMT == 4 ? kchan0<FMT>(j) + 4 : FMT == 2 ? kchan0<FMT>(j) + 8 : FMT == 8 ? kchan0<FMT>(j) + 2
-                                                                                  : kchan0<FMT>(j) + 1;
-}
-
 // --------------------------------------------------------------------------
-// operand unpacking
+// operand unpacking: packed codes -> centred f16 pairs (exact)
 // --------------------------------------------------------------------------
 template <int P>  // 2-bit field at bit 2P of each half -> (n - 2)
 __device__ __forceinline__ uint32_t int2_pair(uint32_t w) {
@@ -116,100 +100,100 @@ __device__ __forceinline__ uint32_t int8_lo(uint32_t w) {  // bytes 0, 2 -> (n -
   return hfma2(lop3_and_or(w, 0x00FF00FFu, kMagic), dup16(f16_bits_of_int(1)), dup16(f16_bits_of_int(-1152)));
 }
 
-// Key row: the lane's 32 channels -> 16 packed f16 pairs (channels kchan0/1(j)).
-template <int FMT>
-__device__ __forceinline__ void unpack_k(const uint8_t* p, uint32_t (&R)[16]) {
+// The lane's operand words of one code matrix (fragment order): kWords words,
+// word w at byte ((w >> 2) * 32 + lane) * 16 + (w & 3) * 4.
+template <int N>
+__device__ __forceinline__ void load_words(const uint8_t* base, int lane, uint32_t (&W)[N]) {
+  const uint4* p = reinterpret_cast<const uint4*>(base) + lane;
+#pragma unroll
+  for (int j = 0; j < N / 4; ++j) {
+    const uint4 v = p[32 * j];
+    W[4 * j] = v.x;
+    W[4 * j + 1] = v.y;
+    W[4 * j + 2] = v.z;
+    W[4 * j + 3] = v.w;
+  }
+}
+
+// A-operand registers of step s (a compile-time constant after unrolling).
+template <int FMT, int N>
+__device__ __forceinline__ void unpack_a(const uint32_t (&W)[N], int s, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                         uint32_t& a3) {
   if constexpr (FMT == 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t s = w[i] >> 8;
-      R[4 * i + 0] = int4_lo(w[i]);
-      R[4 * i + 1] = int4_hi(w[i]);
-      R[4 * i + 2] = int4_lo(s);
-      R[4 * i + 3] = int4_hi(s);
-    }
+    const uint32_t w = W[s], w8 = w >> 8;
+    a0 = int4_lo(w);
+    a1 = int4_hi(w);
+    a2 = int4_lo(w8);
+    a3 = int4_hi(w8);
   } else if constexpr (FMT == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    const uint32_t w[2] = {v.x, v.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t s = w[i] >> 8;
-      R[8 * i + 0] = int2_pair<0>(w[i]);
-      R[8 * i + 1] = int2_pair<1>(w[i]);
-      R[8 * i + 2] = int2_pair<2>(w[i]);
-      R[8 * i + 3] = int2_pair<3>(w[i]);
-      R[8 * i + 4] = int2_pair<0>(s);
-      R[8 * i + 5] = int2_pair<1>(s);
-      R[8 * i + 6] = int2_pair<2>(s);
-      R[8 * i + 7] = int2_pair<3>(s);
-    }
+    const uint32_t w = (s & 1) ? (W[s >> 1] >> 8) : W[s >> 1];
+    a0 = int2_pair<0>(w);
+    a1 = int2_pair<1>(w);
+    a2 = int2_pair<2>(w);
+    a3 = int2_pair<3>(w);
   } else if constexpr (FMT == 8) {
-    const uint4 v0 = *reinterpret_cast<const uint4*>(p);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(p + 16);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      R[2 * i + 0] = int8_lo(w[i]);
-      R[2 * i + 1] = int8_lo(w[i] >> 8);
-    }
+    a0 = int8_lo(W[2 * s]);
+    a1 = int8_lo(W[2 * s] >> 8);
+    a2 = int8_lo(W[2 * s + 1]);
+    a3 = int8_lo(W[2 * s + 1] >> 8);
   } else {  // FP8 E4M3
-    const uint4 v0 = *reinterpret_cast<const uint4*>(p);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(p + 16);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    e4m3x4_to_f16x4(W[2 * s], a0, a1);
+    e4m3x4_to_f16x4(W[2 * s + 1], a2, a3);
+  }
+}
+
+// NGV consecutive floats (a token's Value scales or zero-points of all groups)
+template <int NGV>
+__device__ __forceinline__ void load_row(const float* p, float (&v)[NGV]) {
+  if constexpr (NGV == 1) {
+    v[0] = p[0];
+  } else if constexpr (NGV == 2) {
+    const float2 a = *reinterpret_cast<const float2*>(p);
+    v[0] = a.x;
+    v[1] = a.y;
+  } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      e4m3x4_to_f16x4(w[i], R[2 * i + 0], R[2 * i + 1]);
+    for (int j = 0; j < NGV / 4; ++j) {
+      const float4 a = reinterpret_cast<const float4*>(p)[j];
+      v[4 * j] = a.x;
+      v[4 * j + 1] = a.y;
+      v[4 * j + 2] = a.z;
+      v[4 * j + 3] = a.w;
     }
   }
 }
 
-// Value tile: B-operand registers of n-tile jt from the lane's words W.
-template <int FMT, int JT, int NWORDS>
-__device__ __forceinline__ void unpack_v(const uint32_t (&W)[NWORDS], uint32_t& b01, uint32_t& b23) {
-  if constexpr (FMT == 4) {
-    const uint32_t src = (JT & 1) ? (W[JT / 2] >> 8) : W[JT / 2];
-    b01 = int4_lo(src);
-    b23 = int4_hi(src);
-  } else if constexpr (FMT == 2) {
-    constexpr int a = JT & 3;
-    constexpr int p0 = 2 * a, p1 = 2 * a + 1;
-    const uint32_t w = W[JT / 4];
-    const uint32_t s = w >> 8;
-    b01 = int2_pair<(p0 & 3)>(p0 < 4 ? w : s);
-    b23 = int2_pair<(p1 & 3)>(p1 < 4 ? w : s);
-  } else if constexpr (FMT == 8) {
-    b01 = int8_lo(W[JT]);
-    b23 = int8_lo(W[JT] >> 8);
-  } else {
-    e4m3x4_to_f16x4(W[JT], b01, b23);
-  }
-}
-
 // --------------------------------------------------------------------------
-// per-warp online-softmax state (thread (r, q) holds head r)
+// per-warp online-softmax state
 // --------------------------------------------------------------------------
-template <int NGV>
+// Score layout: lane (r, q) holds, per column block b, query head 4b + q for
+// tokens r and r + 8 of a tile.  Output layout: lane (r, q) holds heads 2q and
+// 2q + 1 of channels 16 mb + r and 16 mb + r + 8 (mb = 0..7).  W layout: lane
+// (r, q) holds head r for tokens 2q, 2q + 1, 2q + 8, 2q + 9.
+template <int NBQ, int NGV>
 struct WarpState {
-  float o[16][4];    // PV accumulators: rows r (hi) in [0..1], rows r+8 (lo) in [2..3]
-  float zacc[NGV];   // zero-point terms per Value group (thread-partial)
-  float m;           // reference max (log2 domain)
-  float l;           // sum of p (thread-partial)
-  float S;           // reference Value scale
+  float o[8][4];     // PV accumulators (output layout): [mb][0/1] = channel 16mb+r, heads 2q / 2q+1;
+                     // [mb][2/3] = channel 16mb+r+8
+  float zacc[NGV];   // zero-point sums per Value group, head r (W layout), thread-partial
+  float m[NBQ];      // reference max of head 4b+q (log2 domain)
+  float l[NBQ];      // sum of p of head 4b+q, thread-partial
+  float S;           // reference Value scale (warp-uniform: Value scales do not depend on the head)
   float inv_S;       // 1 / S
 };
 
-template <int NGV>
-__device__ __forceinline__ void state_init(WarpState<NGV>& st) {
+template <int NBQ, int NGV>
+__device__ __forceinline__ void state_init(WarpState<NBQ, NGV>& st) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
+  for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
 #pragma unroll
   for (int j = 0; j < NGV; ++j) st.zacc[j] = 0.f;
-  st.m = -INFINITY;
-  st.l = 0.f;
+#pragma unroll
+  for (int b = 0; b < NBQ; ++b) {
+    st.m[b] = -INFINITY;
+    st.l[b] = 0.f;
+  }
   st.S = 0.f;
   st.inv_S = 0.f;
 }
@@ -220,96 +204,261 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Update the running max / scale references for a stage with scores sig[N]
-// (the lane's tokens of head r, 4 per 16-token tile; -inf when masked) and the
-// lane's largest Value scale smax; return p[N] * kPrescale and 1 / S.  A token's
-// PV weight is then (s_t / S) * (p_t * kPrescale) <= 4 * 2^6 * 64 = 2^14.
-template <int NGV, int N>
-__device__ __forceinline__ float softmax_step(WarpState<NGV>& st, const float (&sig)[N], float smax, float (&pr)[N]) {
-  float tmax = sig[0];
+// One softmax step over a tile: sig[b][0] / sig[b][1] are the scores (log2
+// domain, -inf when masked) of tokens r / r + 8 for head 4b + q; smax is the
+// largest Value scale among the lane's tokens (warp-uniform already when kVarS
+// is false).  The references m (per head) and S move only when a score exceeds
+// m by 2^kTau or a scale exceeds S by kSTau -- each lane checks its own values
+// and the warp votes; only then are the maxima reduced over the lanes and every
+// accumulator rescaled.  Returns p = 2^(sig - m).
+template <int NBQ, int NGV, bool kVarS>
+__device__ __forceinline__ void softmax_tile(WarpState<NBQ, NGV>& st, const float (&sig)[NBQ][2], float smax, int r,
+                                             int q, float (&pr)[NBQ][2]) {
+  bool bump = smax > st.S * kSTau;
 #pragma unroll
-  for (int e = 1; e < N; ++e) tmax = fmaxf(tmax, sig[e]);
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
-  smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
-  smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 2));
-  const bool bump_m = tmax > st.m + kTau;
-  const bool bump_s = smax > st.S * kSTau;
-  if (__any_sync(kFull, bump_m || bump_s)) {
-    const float m_new = bump_m ? tmax : st.m;
-    const float S_new = bump_s ? smax : st.S;
-    const float a = (st.m == -INFINITY) ? 0.f : fast_exp2(st.m - m_new);
-    const float ao = (S_new > 0.f) ? a * (st.S / S_new) : 0.f;
-    st.l *= a;
+  for (int b = 0; b < NBQ; ++b) bump |= fmaxf(sig[b][0], sig[b][1]) > st.m[b] + kTau;
+  if (__any_sync(kFull, bump)) {
+    float alpha[NBQ];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int b = 0; b < NBQ; ++b) {
+      float t = fmaxf(sig[b][0], sig[b][1]);  // the head's largest score: reduce over the token lanes r
+      t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
+      t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
+      t = fmaxf(t, __shfl_xor_sync(kFull, t, 16));
+      const float mn = t > st.m[b] + kTau ? t : st.m[b];
+      alpha[b] = (st.m[b] == -INFINITY) ? 0.f : fast_exp2(st.m[b] - mn);
+      st.m[b] = mn;
+      st.l[b] *= alpha[b];
+    }
+    if constexpr (kVarS) {  // per-token Value scales: the tile's largest over the token lanes q
+      smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
+      smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 2));
+    }
+    const float S_new = smax > st.S * kSTau ? smax : st.S;
+    const float ratio = S_new > 0.f ? st.S / S_new : 0.f;
+    // output layout: heads 2q, 2q + 1 live in score lanes (2q) & 3, (2q + 1) & 3 of block q >> 1
+    float a0 = __shfl_sync(kFull, alpha[0], (2 * q) & 3), a1 = __shfl_sync(kFull, alpha[0], (2 * q + 1) & 3);
+    // W layout: head r lives in score lane r & 3 of block r >> 2
+    float az = __shfl_sync(kFull, alpha[0], r & 3);
+    if constexpr (NBQ == 2) {
+      const float b0 = __shfl_sync(kFull, alpha[1], (2 * q) & 3), b1 = __shfl_sync(kFull, alpha[1], (2 * q + 1) & 3);
+      const float bz = __shfl_sync(kFull, alpha[1], r & 3);
+      if (q >= 2) {
+        a0 = b0;
+        a1 = b1;
+      }
+      if (r >= 4) az = bz;
+    }
+    a0 *= ratio;
+    a1 *= ratio;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) st.o[j][e] *= ao;
+    for (int mb = 0; mb < 8; ++mb) {
+      st.o[mb][0] *= a0;
+      st.o[mb][2] *= a0;
+      st.o[mb][1] *= a1;
+      st.o[mb][3] *= a1;
+    }
 #pragma unroll
-    for (int j = 0; j < NGV; ++j) st.zacc[j] *= ao;
-    st.m = m_new;
+    for (int j = 0; j < NGV; ++j) st.zacc[j] *= az * ratio;
     st.S = S_new;
     st.inv_S = 1.f / S_new;
   }
-  float lsum = 0.f;
 #pragma unroll
-  for (int e = 0; e < N; ++e) {
-    pr[e] = (sig[e] == -INFINITY) ? 0.f : fast_exp2(sig[e] - st.m);
-    lsum += pr[e];
-    pr[e] *= kPrescale;
+  for (int b = 0; b < NBQ; ++b)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      pr[b][e] = (sig[b][e] == -INFINITY) ? 0.f : fast_exp2(sig[b][e] - st.m[b]);
+      st.l[b] += pr[b][e];
+    }
+}
+
+// p of head r for tokens 2q, 2q + 1, 2q + 8, 2q + 9 of a tile whose score-layout
+// values are pr[b][e] (token r) and pr[b][e + 1] (token r + 8).
+template <int NBQ, int NV>
+__device__ __forceinline__ void p_operand(const float (&pr)[NBQ][NV], int e, int r, int q, float (&pt)[4]) {
+  const int s0 = 8 * q + (r & 3), s1 = s0 + 4;  // score lanes of tokens 2q and 2q + 1, head r (mod 4)
+  pt[0] = __shfl_sync(kFull, pr[0][e], s0);
+  pt[1] = __shfl_sync(kFull, pr[0][e], s1);
+  pt[2] = __shfl_sync(kFull, pr[0][e + 1], s0);
+  pt[3] = __shfl_sync(kFull, pr[0][e + 1], s1);
+  if constexpr (NBQ == 2) {
+    const float u0 = __shfl_sync(kFull, pr[1][e], s0), u1 = __shfl_sync(kFull, pr[1][e], s1);
+    const float u2 = __shfl_sync(kFull, pr[1][e + 1], s0), u3 = __shfl_sync(kFull, pr[1][e + 1], s1);
+    if (r >= 4) {
+      pt[0] = u0;
+      pt[1] = u1;
+      pt[2] = u2;
+      pt[3] = u3;
+    }
+  } else {
+    if (r >= 4) pt[0] = pt[1] = pt[2] = pt[3] = 0.f;  // heads 4..7 do not exist with one block
   }
-  st.l += lsum;
-  return st.inv_S;
 }
 
 // --------------------------------------------------------------------------
-// A operands built from the query
+// QK B operand of the quantized tiles
 // --------------------------------------------------------------------------
-// INT: A = q_c * s_c (this group's Key scales) split hi/lo, plus the group's
-// zero-point term and the score multiplier.  qv: the lane's 32 query values of
-// head r; ks/kz: this group's Key scale / zero row (smem, 128 floats).
-template <int FMT>
-__device__ __forceinline__ void build_a_int(const float* qrow, const float* ks, const float* kz, int q,
-                                            float scale_log2, uint32_t (&A)[8][4], float& kfac, float& cterm) {
-  // pass 1: largest |q_c s_c| of the head (sets the f16 range) and the zero-point term
+// Lane (r, q), column block b: column r = half (r & 1) of query head
+// 4b + (r >> 1), channels 16s + 4q + e.  q_s holds the g query heads and a zero
+// row g for the columns of absent heads.  x_c = q_c s_c (INT; FP8: s_c = 1),
+// kappa = 16384 / max_c |x_c| of the head, B = hi (r even) or lo (r odd) part of
+// x_c kappa.  kfac / cterm return the score multiplier and the zero-point term
+// (both scaled by kfac0 = log2(e) / sqrt(d) [* FP8 Key scale]) for head 4b + q.
+template <int FMT, int NBQ>
+__device__ __forceinline__ void build_bq(const float* q_s, const float* ks, const float* kz, int r, int q, int g,
+                                         float kfac0, uint32_t (&Bq)[NBQ][8][2], float (&kfac)[NBQ],
+                                         float (&cterm)[NBQ]) {
   constexpr float kH = (float)FT<FMT>::kHalf;
-  const float* ksq = ks + 32 * q;
-  const float* kzq = kz + 32 * q;
-  float mx = 0.f, cz = 0.f;
+  const bool lo = (r & 1) != 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int ci = 4 * ((i + q) & 7);  // rotated per lane group: the 4 groups hit different banks
-    const float4 q4 = *reinterpret_cast<const float4*>(qrow + ci);
-    const float4 s4 = *reinterpret_cast<const float4*>(ksq + ci);
-    const float4 z4 = *reinterpret_cast<const float4*>(kzq + ci);
-    const float x0 = q4.x * s4.x, x1 = q4.y * s4.y, x2 = q4.z * s4.z, x3 = q4.w * s4.w;
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
-    cz = fmaf(x0, kH - z4.x, cz);
-    cz = fmaf(x1, kH - z4.y, cz);
-    cz = fmaf(x2, kH - z4.z, cz);
-    cz = fmaf(x3, kH - z4.w, cz);
+  for (int b = 0; b < NBQ; ++b) {
+    const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 4 * q;  // row g is zero
+    float mx = 0.f, cz = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
+      if constexpr (FT<FMT>::kInt) {
+        const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
+        const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
+        x.x *= s4.x;
+        x.y *= s4.y;
+        x.z *= s4.z;
+        x.w *= s4.w;
+        cz = fmaf(x.x, kH - z4.x, cz);
+        cz = fmaf(x.y, kH - z4.y, cz);
+        cz = fmaf(x.z, kH - z4.z, cz);
+        cz = fmaf(x.w, kH - z4.w, cz);
+      }
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+      asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    cz += __shfl_xor_sync(kFull, cz, 1);
+    cz += __shfl_xor_sync(kFull, cz, 2);
+    float kap = 16384.f / mx;
+    if (!(mx > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
+      if constexpr (FT<FMT>::kInt) {
+        const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
+        x.x *= s4.x;
+        x.y *= s4.y;
+        x.z *= s4.z;
+        x.w *= s4.w;
+      }
+      x.x *= kap;
+      x.y *= kap;
+      x.z *= kap;
+      x.w *= kap;
+      uint32_t h01 = pack_f16(x.x, x.y), h23 = pack_f16(x.z, x.w);
+      if (lo) {
+        const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
+        h01 = pack_f16(x.x - f01.x, x.y - f01.y);
+        h23 = pack_f16(x.z - f23.x, x.w - f23.y);
+      }
+      Bq[b][s][0] = h01;
+      Bq[b][s][1] = h23;
+      asm volatile("" ::: "memory");
+    }
+    // to the score layout: head 4b + q is held by the lanes with r = 2q
+    const float kf = kfac0 / kap, ct = kfac0 * cz;
+    kfac[b] = __shfl_sync(kFull, kf, 8 * q);
+    cterm[b] = __shfl_sync(kFull, ct, 8 * q);
   }
-  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-  cz += __shfl_xor_sync(kFull, cz, 1);
-  cz += __shfl_xor_sync(kFull, cz, 2);
-  const float kappa = mx > 0.f ? 16384.f / mx : 1.f;
-  // pass 2: A = hi/lo split of q_c s_c kappa, in the channel order the Key unpacking produces
+}
+
+// Raw scores of one quantized tile: d[b][0] / d[b][1] = tokens r / r + 8, head 4b + q.
+template <int FMT, int NBQ>
+__device__ __forceinline__ void qk_tile(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&Bq)[NBQ][8][2],
+                                        float (&d)[NBQ][2]) {
+  float acc[NBQ][2][4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int c0 = kchan0<FMT>(j), c1 = kchan1<FMT>(j);
-    uint32_t hi, lo;
-    split_f16(qrow[c0] * ksq[c0] * kappa, qrow[c1] * ksq[c1] * kappa, hi, lo);
-    if ((j & 1) == 0) {
-      A[j >> 1][0] = hi;
-      A[j >> 1][1] = lo;
-    } else {
-      A[j >> 1][2] = hi;
-      A[j >> 1][3] = lo;
+  for (int b = 0; b < NBQ; ++b)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[b][c][e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    uint32_t a0, a1, a2, a3;
+    unpack_a<FMT>(KW, s, a0, a1, a2, a3);
+#pragma unroll
+    for (int b = 0; b < NBQ; ++b) mma_f16(acc[b][s & 1], a0, a1, a2, a3, Bq[b][s][0], Bq[b][s][1]);
+  }
+#pragma unroll
+  for (int b = 0; b < NBQ; ++b) {
+    d[b][0] = (acc[b][0][0] + acc[b][1][0]) + (acc[b][0][1] + acc[b][1][1]);
+    d[b][1] = (acc[b][0][2] + acc[b][1][2]) + (acc[b][0][3] + acc[b][1][3]);
+  }
+}
+
+// PV of one quantized tile: o[mb] += V^T(channels 16mb..) * W(group of mb).
+template <int FMT, int NGV>
+__device__ __forceinline__ void pv_tile(const uint32_t (&VW)[FT<FMT>::kWords], const uint32_t (&B0)[NGV],
+                                        const uint32_t (&B1)[NGV], float (&o)[8][4]) {
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb) {
+    uint32_t a0, a1, a2, a3;
+    unpack_a<FMT>(VW, mb, a0, a1, a2, a3);
+    mma_f16(o[mb], a0, a1, a2, a3, B0[mb * NGV / 8], B1[mb * NGV / 8]);
+  }
+}
+
+// Scores of a bf16 tile from its K rows in shared memory (rows past `rows` masked).
+template <int NBQ>
+__device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* q_s, int lane, int r, int q, int g,
+                                        int rows, float scale_log2, float (&sig)[NBQ][2]) {
+  const uint32_t sbase = smem_addr(stg);
+  const uint32_t lbase = sbase + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kBfRow + 16 * (lane >> 4);
+  const bool qcol = (r & 1) == 0;  // even columns carry the query, odd columns are zero
+  float acc[NBQ][2][4];
+#pragma unroll
+  for (int b = 0; b < NBQ; ++b)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[b][c][e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    uint32_t a0, a1, a2, a3;
+    ldmatrix_x4(lbase + 32 * s, a0, a1, a2, a3);
+#pragma unroll
+    for (int b = 0; b < NBQ; ++b) {
+      const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 16 * s + 2 * q;
+      const float2 x0 = *reinterpret_cast<const float2*>(qh);
+      const float2 x1 = *reinterpret_cast<const float2*>(qh + 8);
+      const uint32_t b0 = qcol ? pack_bf16(x0.x, x0.y) : 0u, b1 = qcol ? pack_bf16(x1.x, x1.y) : 0u;
+      mma_bf16(acc[b][s & 1], a0, a1, a2, a3, b0, b1);
     }
   }
-  kfac = scale_log2 / kappa;
-  cterm = scale_log2 * cz;
+#pragma unroll
+  for (int b = 0; b < NBQ; ++b) {
+    const bool hv = 4 * b + q < g;
+    const float d0 = (acc[b][0][0] + acc[b][1][0]) + (acc[b][0][1] + acc[b][1][1]);
+    const float d1 = (acc[b][0][2] + acc[b][1][2]) + (acc[b][0][3] + acc[b][1][3]);
+    sig[b][0] = (hv && r < rows) ? d0 * scale_log2 : -INFINITY;
+    sig[b][1] = (hv && r + 8 < rows) ? d1 * scale_log2 : -INFINITY;
+  }
+}
+
+// PV of a bf16 tile from its V rows (rows past the end zeroed); W = pt * f split
+// into two bf16 terms.
+__device__ __forceinline__ void bf16_pv(const uint8_t* stg, int lane, const float (&pt)[4], float f,
+                                        float (&o)[8][4]) {
+  const int mi = lane >> 3;
+  const uint32_t lbase = smem_addr(stg) + ((lane & 7) + 8 * (mi >> 1)) * kBfRow + 16 * (mi & 1);
+  uint32_t h01, l01, h23, l23;
+  split_bf16(pt[0] * f, pt[1] * f, h01, l01);
+  split_bf16(pt[2] * f, pt[3] * f, h23, l23);
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb) {
+    uint32_t a0, a1, a2, a3;
+    ldmatrix_x4_trans(lbase + 32 * mb, a0, a1, a2, a3);
+    mma_bf16(o[mb], a0, a1, a2, a3, h01, h23);
+    mma_bf16(o[mb], a0, a1, a2, a3, l01, l23);
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -355,60 +504,33 @@ struct SegRec {
   int n_sink, qn, r, nbf, nq;
 };
 constexpr int kMaxSeg = 16;  // segments per table batch
-constexpr int kChunk = 2;    // quantized tiles per softmax step
-
-// Unit order inside a pair: the nbf bf16 tiles (wbf units each) are spread
-// evenly among the nq quantized tiles (1 unit each): bf16 tile i sits right
-// before quantized tile floor(i * nq / nbf).  Every warp's contiguous unit range
-// then gets its share of the (slower) bf16 tiles.
-__device__ __forceinline__ long long unit_of_bf(int i, int nbf, int nq, int wbf) {
-  return (long long)i * nq / nbf + (long long)i * wbf;
-}
-__device__ __forceinline__ long long unit_of_q(int k, int nbf, int nq, int wbf) {
-  const long long before = nbf == 0 ? 0 : min((long long)nbf, ((long long)(k + 1) * nbf + nq - 1) / nq);
-  return k + wbf * before;
-}
 
 // This warp's part of a segment: bf16 tiles [bf0, bf0 + nbf_w), quantized tiles
-// [q0, q0 + nq_w); stages: two per bf16 tile (its K rows, then its V rows), then
+// [q0, q0 + nq_w).  A pair's units are its nbf bf16 tiles (wbf units each) and
+// then its nq quantized tiles (1 unit each); a bf16 tile belongs to the range
+// holding its first unit.  The CTA's tiles of each kind are split evenly among
+// the warps.  Stages: two per bf16 tile (its K rows, then its V rows), then
 // ceil(nq_w / tps) quantized stages.
 struct WarpPart {
   int bf0, nbf_w, q0, nq_w, nstage;
 };
 
 __device__ __forceinline__ WarpPart warp_part(const SegRec& sg, int warp, int wbf, int tps) {
+  const int nbu = sg.nbf * wbf;  // units of the bf16 tiles
+  const int bl = min(sg.nbf, (sg.ua + wbf - 1) / wbf), bh = min(sg.nbf, (sg.ue + wbf - 1) / wbf);
+  const int ql = min(sg.nq, max(0, sg.ua - nbu)), qh = min(sg.nq, max(0, sg.ue - nbu));
   WarpPart w;
-  const long long wa = sg.ua + (long long)(sg.ue - sg.ua) * warp / kNW;
-  const long long we = sg.ua + (long long)(sg.ue - sg.ua) * (warp + 1) / kNW;
-  // first bf16 tile / quantized tile whose unit is at or after x
-  auto first_bf = [&](long long x) {
-    int lo = 0, hi = sg.nbf;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (unit_of_bf(mid, sg.nbf, sg.nq, wbf) >= x) hi = mid; else lo = mid + 1;
-    }
-    return lo;
-  };
-  auto first_q = [&](long long x) {
-    int lo = 0, hi = sg.nq;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (unit_of_q(mid, sg.nbf, sg.nq, wbf) >= x) hi = mid; else lo = mid + 1;
-    }
-    return lo;
-  };
-  w.bf0 = first_bf(wa);
-  w.nbf_w = first_bf(we) - w.bf0;
-  w.q0 = first_q(wa);
-  w.nq_w = first_q(we) - w.q0;
+  w.bf0 = bl + (bh - bl) * warp / kNW;
+  w.nbf_w = bl + (bh - bl) * (warp + 1) / kNW - w.bf0;
+  w.q0 = ql + (qh - ql) * warp / kNW;
+  w.nq_w = ql + (qh - ql) * (warp + 1) / kNW - w.q0;
   w.nstage = 2 * w.nbf_w + (w.nq_w + tps - 1) / tps;
   return w;
 }
 
-template <int FMT, int NGV>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p) {
+template <int FMT, int NGV, int NBQ>
+__global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
-  constexpr int kHdr = F::kInt ? 1024 : 0;  // every stage starts with a header slot (INT)
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerDesc& L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -421,10 +543,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
   size_t off = (size_t)kNW * nst * p.stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
   off += kNW * kMaxStages * sizeof(uint64_t);
-  float* q_s = reinterpret_cast<float*>(smem + off);
-  off += 8 * 4 * kQStride * sizeof(float);
-  uint8_t* scratch = smem + off;
-  off += (size_t)kNW * p.warp_scratch;
+  int* tbl = reinterpret_cast<int*>(smem + off);  // per warp: a window of 32 block-table entries
+  off += kNW * 32 * sizeof(int);
+  float* q_s = reinterpret_cast<float*>(smem + off);  // [g + 1 rows][kQRow]: the query heads, a zero row
+  off += (size_t)(g + 1) * kQRow * sizeof(float);
+  uint8_t* scratch = smem + off;  // the CTA's merge record: [g heads][kMergeStride]
+  off += (size_t)p.merge_bytes;
   SegRec* segs = reinterpret_cast<SegRec*>(smem + off);
   off += kMaxSeg * sizeof(SegRec);
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
@@ -500,8 +624,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
 
   uint8_t* my_stages = stage_base + (size_t)warp * nst * p.stage_bytes;
   uint64_t* my_bars = bars + warp * kMaxStages;
-  uint8_t* my_scratch = scratch + warp * p.warp_scratch;
-  const float* qrow = q_s + (r * 4 + q) * kQStride;  // the lane's 32 query values of head r
+  int* my_tbl = tbl + warp * 32;
   uint32_t phase_bits = 0;  // expected parity of each stage barrier of this warp
   uint32_t slot_valid = 0;  // lane 0: 8 bits per slot, the tiles its stage holds
   uint32_t pending = 0;     // slots with copies in flight
@@ -509,12 +632,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
   int n_issued = 0, n_consumed = 0;
   const float s_v8 = F::kFp8 ? __ldg(p.C.v_tscale) : 1.f;
 
+  // the g query heads of a pair into q_s (row g zero)
   auto load_q = [&](const SegRec& sg) {
-    for (int i = tid; i < 8 * 128; i += kThreads) {
+    for (int i = tid; i < (g + 1) * 128; i += kThreads) {
       const int hr = i >> 7, c = i & 127;
       float v = 0.f;
       if (hr < g) v = __bfloat162float(qg[((long long)sg.b * p.Hq + sg.h * g + hr) * 128 + c]);
-      q_s[(hr * 4 + (c >> 5)) * kQStride + (c & 31)] = v;
+      q_s[hr * kQRow + c] = v;
     }
   };
 
@@ -561,74 +685,115 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
       ++ps;
       if (ps < nseg) pw = warp_part(segs[ps], warp, wbf, tps);
     }
+    // quantized cursor: record and position in it of the next quantized tile of the part
+    int q_rec = pw.q0 / L.tpg, q_pos = pw.q0 - q_rec * L.tpg;
+    int tb_base = -1;  // paged: first record of the block-table window in my_tbl (-1: none)
     auto issue_next = [&]() {
       const int slot = n_issued % nst;
+      const SegRec& sg = segs[ps];
       uint32_t vm = 0;
-      if (lane == 0) {
-        const SegRec& sg = segs[ps];
-        uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
-        const uint32_t bar = smem_addr(&my_bars[slot]);
-        if (pj < 2 * pw.nbf_w) {
+      if (pj < 2 * pw.nbf_w) {
+        if (lane == 0) {
           // bf16 tile: its 16 K rows (even stage) or V rows (odd stage), one 256-byte copy per row
-          const int bt = pw.bf0 + pj / 2;
-          const int rows = min(16, sg.n_sink + sg.r - bt * 16);
-          const TokenSplit ts = {sg.n_sink, sg.qn, sg.r};
+          uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
+          const uint32_t bar = smem_addr(&my_bars[slot]);
+          const int x0 = (pw.bf0 + pj / 2) * 16;  // bf16-list index of the first row (sinks, then residual)
+          const int rows = min(16, sg.n_sink + sg.r - x0);
+          const long long pair = (long long)sg.b * H + sg.h;
+          const __nv_bfloat16* sink = (pj & 1) ? sink_v : sink_k;
+          const __nv_bfloat16* ring = (pj & 1) ? ring_v : ring_k;
           mbar_arrive_expect_tx(bar, 256u * rows);
+          int slot_r = -1;
           for (int rr = 0; rr < rows; ++rr) {
-            const __nv_bfloat16* src = (pj & 1) ? bf16_row(L, sink_v, ring_v, sg.b, sg.h, bt * 16 + rr, ts)
-                                                : bf16_row(L, sink_k, ring_k, sg.b, sg.h, bt * 16 + rr, ts);
+            const int xb = x0 + rr;
+            const __nv_bfloat16* src;
+            if (xb < sg.n_sink) {
+              src = sink + (pair * L.S + xb) * L.d;
+            } else {
+              if (slot_r < 0) slot_r = (sg.qn + xb - sg.n_sink) % L.W;
+              else if (++slot_r == L.W) slot_r = 0;
+              src = ring + (pair * L.W + slot_r) * L.d;
+            }
             bulk_copy_g2s(smem_addr(dst + rr * kBfRow), src, 256, bar);
           }
-          vm = 1;
-        } else {
-          // quantized tiles [i0, i0 + n): one contiguous range per record touched
-          const int qs = pj - 2 * pw.nbf_w;
-          const long long i0 = pw.q0 + (long long)qs * tps;
-          const int n = (int)min((long long)tps, (long long)(pw.q0 + pw.nq_w) - i0);
-          const long long last = i0 + n - 1;
-          const bool hdr0 = F::kInt && qs == 0 && (i0 % L.tpg) != 0;
+        }
+        vm = 1;
+      } else {
+        // quantized tiles: n tiles from (q_rec, q_pos), one contiguous range per record touched
+        const int qs = pj - 2 * pw.nbf_w;
+        const int n = min(tps, pw.nq_w - qs * tps);
+        const bool hdr0 = F::kInt && qs == 0 && q_pos != 0;  // the group's header, copied to slot offset 0
+        int l_rec = q_rec, l_pos = q_pos + n - 1;              // the last tile's record and position
+        while (l_pos >= L.tpg) {
+          l_pos -= L.tpg;
+          ++l_rec;
+        }
+        if (L.paged && (tb_base < 0 || q_rec < tb_base || l_rec >= tb_base + 32)) {
+          // the block-table entries of 32 records from q_rec, one per lane
+          tb_base = q_rec;
+          const int x = q_rec + lane;
+          my_tbl[lane] = x < L.mbps ? __ldg(&p.C.block_table[(long long)sg.b * L.mbps + x]) : -1;
+          __syncwarp();
+        }
+        if (lane == 0) {
+          uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
+          const uint32_t bar = smem_addr(&my_bars[slot]);
           if (!L.paged) {
             const uint8_t* base = reinterpret_cast<const uint8_t*>(p.C.qstore) +
                                   ((long long)sg.b * H + sg.h) * L.nrec * L.rec_bytes;
-            const uint8_t* rec0 = base + (i0 / L.tpg) * L.rec_bytes;
-            const uint8_t* start = (F::kInt && i0 % L.tpg == 0) ? rec0 : rec0 + L.hdr_bytes + (i0 % L.tpg) * L.tile_bytes;
-            const uint8_t* end = base + (last / L.tpg) * L.rec_bytes + L.hdr_bytes + (last % L.tpg + 1) * L.tile_bytes;
+            const uint8_t* rec0 = base + (long long)q_rec * L.rec_bytes;
+            const uint8_t* start = (F::kInt && q_pos == 0) ? rec0 : rec0 + L.hdr_bytes + q_pos * L.tile_bytes;
+            const uint8_t* end = base + (long long)l_rec * L.rec_bytes + L.hdr_bytes + (l_pos + 1) * L.tile_bytes;
             const uint32_t len = (uint32_t)(end - start);
             mbar_arrive_expect_tx(bar, len + (hdr0 ? 1024u : 0u));
-            bulk_copy_g2s(smem_addr(dst + kHdr), start, len, bar);
+            bulk_copy_g2s(smem_addr(dst + (hdr0 ? 1024 : 0)), start, len, bar);
             if (hdr0) bulk_copy_g2s(smem_addr(dst), rec0, 1024, bar);
             vm = (1u << n) - 1u;
           } else {
+            // records q_rec .. l_rec: present ones are copied, missing ones (bad block) leave holes
+            const uint8_t* pool = reinterpret_cast<const uint8_t*>(p.C.block_pool);
             uint32_t bytes = 0;
-            for (long long rr = i0 / L.tpg; rr <= last / L.tpg; ++rr) {
-              const uint8_t* rec = record_addr(L, p.C, sg.b, sg.h, rr, p.status);
-              const long long a0 = max(i0, rr * L.tpg), a1 = min(last, rr * L.tpg + L.tpg - 1);
-              if (!rec) continue;
-              for (long long i = a0; i <= a1; ++i) vm |= 1u << (int)(i - i0);
-              const bool with_hdr = F::kInt && (a0 % L.tpg) == 0;
-              bytes += (uint32_t)((with_hdr ? L.hdr_bytes : 0) + (a1 - a0 + 1) * L.tile_bytes);
-              if (hdr0 && rr == i0 / L.tpg) bytes += 1024;
-            }
-            if (vm) {
-              mbar_arrive_expect_tx(bar, bytes);
-              uint32_t so = kHdr;
-              for (long long rr = i0 / L.tpg; rr <= last / L.tpg; ++rr) {
-                const long long a0 = max(i0, rr * L.tpg), a1 = min(last, rr * L.tpg + L.tpg - 1);
-                const bool with_hdr = F::kInt && (a0 % L.tpg) == 0;
-                const uint32_t len = (uint32_t)((with_hdr ? L.hdr_bytes : 0) + (a1 - a0 + 1) * L.tile_bytes);
-                const uint8_t* rec = record_addr(L, p.C, sg.b, sg.h, rr, nullptr);
-                if (rec) {
-                  const uint8_t* src = with_hdr ? rec : rec + L.hdr_bytes + (a0 % L.tpg) * L.tile_bytes;
-                  bulk_copy_g2s(smem_addr(dst + so), src, len, bar);
-                  if (hdr0 && rr == i0 / L.tpg) bulk_copy_g2s(smem_addr(dst), rec, 1024, bar);
+            for (int pass = 0; pass < 2; ++pass) {
+              uint32_t so = hdr0 ? 1024u : 0u;
+              int t = 0;  // tiles of the stage before record rr
+              for (int rr = q_rec; rr <= l_rec; ++rr) {
+                const int a0 = rr == q_rec ? q_pos : 0;
+                const int cnt = min(L.tpg - a0, n - t);
+                const bool with_hdr = F::kInt && a0 == 0;
+                const uint32_t len = (uint32_t)((with_hdr ? L.hdr_bytes : 0) + cnt * L.tile_bytes);
+                const int blk = my_tbl[rr - tb_base];
+                const bool ok = blk >= 0 && blk < L.num_blocks;
+                if (pass == 0) {
+                  if (ok) {
+                    vm |= ((1u << cnt) - 1u) << t;
+                    bytes += len + ((hdr0 && rr == q_rec) ? 1024u : 0u);
+                  } else {
+                    report(p.status, KVQ_DEV_BAD_BLOCK);
+                  }
+                } else if (ok) {
+                  const uint8_t* rec = pool + (long long)blk * L.block_bytes + (long long)sg.h * L.rec_bytes;
+                  bulk_copy_g2s(smem_addr(dst + so), with_hdr ? rec : rec + L.hdr_bytes + a0 * L.tile_bytes, len, bar);
+                  if (hdr0 && rr == q_rec) bulk_copy_g2s(smem_addr(dst), rec, 1024, bar);
                 }
                 so += len;
+                t += cnt;
+              }
+              if (pass == 0) {
+                if (!vm) break;
+                mbar_arrive_expect_tx(bar, bytes);
               }
             }
           }
         }
-        slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
+        // advance the cursor by n tiles
+        q_rec = l_rec;
+        q_pos = l_pos + 1;
+        if (q_pos == L.tpg) {
+          q_pos = 0;
+          ++q_rec;
+        }
       }
+      if (lane == 0) slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
       vm = __shfl_sync(kFull, vm, 0);
       if (vm) pending |= 1u << slot;
       ++n_issued;
@@ -640,11 +805,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
           if (pw.nstage) break;
           ++ps;
         }
+        if (ps < nseg) {
+          q_rec = pw.q0 / L.tpg;
+          q_pos = pw.q0 - q_rec * L.tpg;
+          tb_base = -1;
+        }
       }
     };
+    // the query of the first segment: loads issued before the first copies, stored after them
+    float qpre[8];
+    {
+      const SegRec& s0 = segs[0];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = tid + k * kThreads, hr = i >> 7, c = i & 127;
+        qpre[k] = hr < g ? __bfloat162float(qg[((long long)s0.b * p.Hq + s0.h * g + hr) * 128 + c]) : 0.f;
+      }
+    }
     while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
-    // the query of the first segment, while the first copies are in flight
-    load_q(segs[0]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = tid + k * kThreads, hr = i >> 7, c = i & 127;
+      if (hr <= g) q_s[hr * kQRow + c] = qpre[k];  // row g stays zero
+    }
     __syncthreads();
 
     // ---- consumer ----
@@ -652,31 +835,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
       const SegRec sg = segs[s];
       const WarpPart wp = warp_part(sg, warp, wbf, tps);
       const int nbf_tok = sg.n_sink + sg.r;
-      WarpState<NGV> stt;
+      WarpState<NBQ, NGV> stt;
       state_init(stt);
-      uint32_t A[8][4];
-      float kfac = 0.f, cterm = 0.f;
+      uint32_t Bq[NBQ][8][2];
+      float kfac[NBQ], cterm[NBQ];
       if constexpr (F::kFp8) {
-        // A = q * 2^E (exact in f16), E from the head's largest |q|
-        float mx = 0.f;
+        build_bq<FMT, NBQ>(q_s, nullptr, nullptr, r, q, g, p.scale_log2 * __ldg(p.C.k_tscale), Bq, kfac, cterm);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(qrow[i]));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-        int ex = 0;
-        if (mx > 0.f) (void)frexpf(mx, &ex);
-        const float sc = mx > 0.f ? ldexpf(1.f, 15 - ex) : 1.f;  // max |q| * sc in [2^14, 2^15)
+        for (int b = 0; b < NBQ; ++b) {
+          kfac[b] = cterm[b] = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
-          const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s2);
-          A[s2][0] = pack_f16(qq.x * sc, qq.y * sc);
-          A[s2][1] = 0u;
-          A[s2][2] = pack_f16(qq.z * sc, qq.w * sc);
-          A[s2][3] = 0u;
+          for (int s2 = 0; s2 < 8; ++s2) Bq[b][s2][0] = Bq[b][s2][1] = 0u;
         }
-        kfac = p.scale_log2 * __ldg(p.C.k_tscale) / sc;
       }
-      float sig_bf[4];  // scores of a bf16 tile between its K and V stages
+      float sig_bf[NBQ][2];  // scores of a bf16 tile between its K and V stages
+
+      // hand the consumed slot back to the producer (shared-memory reads and writes of
+      // the slot ordered before the bulk copies that will overwrite it)
+      auto release = [&]() {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        ++n_consumed;
+        while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
+      };
 
       for (int j = 0; j < wp.nstage; ++j) {
         const int slot = n_consumed % nst;
@@ -697,249 +879,190 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
           const int bt = wp.bf0 + j / 2;
           const int rows = min(16, nbf_tok - bt * 16);
           if ((j & 1) == 0) {
-            // ---- bf16 tile, K rows: QK with A = q (bf16, exact) ----
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              const int row = nt * 8 + r;
-              uint32_t R[16];
-              if (row < rows) {
-                const uint4* r4 = reinterpret_cast<const uint4*>(stg + row * kBfRow + 64 * q);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const uint4 v = r4[i];
-                  R[4 * i] = v.x; R[4 * i + 1] = v.y; R[4 * i + 2] = v.z; R[4 * i + 3] = v.w;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) R[i] = 0u;
-              }
-#pragma unroll
-              for (int s2 = 0; s2 < 8; ++s2) {
-                const float4 qq = *reinterpret_cast<const float4*>(qrow + 4 * s2);
-                mma_bf16(acc[nt], pack_bf16(qq.x, qq.y), 0u, pack_bf16(qq.z, qq.w), 0u, R[2 * s2], R[2 * s2 + 1]);
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = (e >> 1) * 8 + 2 * q + (e & 1);
-              sig_bf[e] = (t < rows) ? acc[e >> 1][e & 1] * p.scale_log2 : -INFINITY;
-            }
+            // ---- bf16 tile, K rows ----
+            bf16_qk<NBQ>(stg, q_s, lane, r, q, g, rows, p.scale_log2, sig_bf);
           } else {
-            // ---- bf16 tile, V rows: softmax, then PV through transposed loads ----
+            // ---- bf16 tile, V rows: softmax, then PV ----
             uint8_t* stw = const_cast<uint8_t*>(stg);
             for (int idx = lane; idx < (16 - rows) * 16; idx += 32)
               *reinterpret_cast<uint4*>(stw + (rows + idx / 16) * kBfRow + (idx % 16) * 16) = make_uint4(0u, 0u, 0u, 0u);
             __syncwarp();
-            float pr[4];
-            const float inv_s = softmax_step<NGV, 4>(stt, sig_bf, 1.f, pr);
-            uint32_t ah0, al0, ah1, al1;
-            split_bf16(pr[0] * inv_s, pr[1] * inv_s, ah0, al0);
-            split_bf16(pr[2] * inv_s, pr[3] * inv_s, ah1, al1);
-            const uint32_t sbase = smem_addr(stg);
-#pragma unroll
-            for (int jp = 0; jp < 8; ++jp) {
-              const int mi = lane >> 3, rr = lane & 7;
-              const int tok = 8 * (mi & 1) + rr;
-              const uint32_t addr = sbase + tok * kBfRow + (2 * jp + (mi >> 1)) * 16;
-              uint32_t v0, v1, v2, v3;
-              ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-              mma_bf16(stt.o[2 * jp], ah0, al0, ah1, al1, v0, v1);
-              mma_bf16(stt.o[2 * jp + 1], ah0, al0, ah1, al1, v2, v3);
-            }
+            float pr[NBQ][2];
+            softmax_tile<NBQ, NGV, false>(stt, sig_bf, 1.f, r, q, pr);
+            float pt[4];
+            p_operand<NBQ, 2>(pr, 0, r, q, pt);
+            bf16_pv(stg, lane, pt, stt.inv_S * kPrescale, stt.o);
           }
         } else if (vmask && alive) {
-          // ---- quantized stage: tiles [i0, i0 + n), walked in smem ----
+          // ---- quantized stage: tiles [i0, i0 + n), walked in smem, one softmax step each ----
           const int qs = j - 2 * wp.nbf_w;
-          const long long i0 = wp.q0 + (long long)qs * tps;
-          const int n = (int)min((long long)tps, (long long)(wp.q0 + wp.nq_w) - i0);
-          int walk = kHdr;  // smem offset of the next tile (headers inline at record starts)
-          bool a_ready = false;
-          for (int k = 0; k < n; k += kChunk) {
-            float sig[kChunk * 4];
-            int toff[kChunk];
+          const int i0 = wp.q0 + qs * tps;
+          const int n = min(tps, wp.q0 + wp.nq_w - i0);
+          int walk = 0;            // smem offset of the next tile (headers inline)
+          int rpos = i0 % L.tpg;   // position of tile i0 + k in its record
+          for (int k = 0; k < n; ++k) {
+            const int i = i0 + k;
+            const bool hdr = F::kInt && (rpos == 0 || (qs == 0 && k == 0));
+            const int hoff = walk;
+            if (hdr) walk += L.hdr_bytes;
+            const uint8_t* tile = stg + walk;
+            walk += L.tile_bytes;
+            if (++rpos == L.tpg) rpos = 0;
+            if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
+            if constexpr (F::kInt) {
+              // the group's B operand (q * s, hi/lo), rebuilt at each record (Key group) start
+              if (hdr)
+                build_bq<FMT, NBQ>(q_s, reinterpret_cast<const float*>(stg + hoff),
+                                   reinterpret_cast<const float*>(stg + hoff + 512), r, q, g, p.scale_log2, Bq, kfac,
+                                   cterm);
+            }
+            // QK
+            float d[NBQ][2];
+            {
+              uint32_t KW[F::kWords];
+              load_words(tile, lane, KW);
+              qk_tile<FMT, NBQ>(KW, Bq, d);
+            }
+            const int tok_valid = min(16, sg.qn - i * 16);  // < 16 only for a partial FP8 tile
+            float sig[NBQ][2];
+#pragma unroll
+            for (int b = 0; b < NBQ; ++b) {
+              const bool hv = 4 * b + q < g;
+              sig[b][0] = (hv && r < tok_valid) ? fmaf(d[b][0], kfac[b], cterm[b]) : -INFINITY;
+              sig[b][1] = (hv && r + 8 < tok_valid) ? fmaf(d[b][1], kfac[b], cterm[b]) : -INFINITY;
+            }
+            const float* vsp = reinterpret_cast<const float*>(tile + 2 * F::kTile);  // INT: Value scales [16][NGV]
+            const float* vzp = vsp + 16 * NGV;                                         // INT: Value zero-points
+            const int tk[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};                // the lane's W tokens
             float smax = s_v8;
+            if constexpr (F::kInt) {
 #pragma unroll
-            for (int tt = 0; tt < kChunk; ++tt) {
-              const int kk = k + tt;
-              const long long i = i0 + kk;
-              int hoff = 0;
-              toff[tt] = -1;
-              if (kk < n) {
-                if (F::kInt && (i % L.tpg) == 0) {
-                  hoff = walk;
-                  walk += L.hdr_bytes;
-                }
-                toff[tt] = walk;
-                walk += L.tile_bytes;
-              }
-              const bool present = kk < n && ((vmask >> kk) & 1u);
-              if (!present) toff[tt] = -1;
-              if (present) {
-                if constexpr (F::kInt) {
-                  // the group's A operand (q * s, hi/lo) lives in the warp's shared scratch between chunks
-                  uint4* afr = reinterpret_cast<uint4*>(my_scratch) + lane;  // word i of lane at [i][lane]
-                  if ((i % L.tpg) == 0 || (qs == 0 && kk == 0)) {
-                    build_a_int<FMT>(qrow, reinterpret_cast<const float*>(stg + hoff),
-                                     reinterpret_cast<const float*>(stg + hoff + 512), q, p.scale_log2, A, kfac,
-                                     cterm);
+              for (int e = 0; e < 4; ++e) {
+                float sv[NGV];
+                load_row<NGV>(vsp + tk[e] * NGV, sv);
 #pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2) afr[32 * i2] = make_uint4(A[i2][0], A[i2][1], A[i2][2], A[i2][3]);
-                    a_ready = true;
-                  } else if (!a_ready || tt == 0) {
-#pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2) {
-                      const uint4 v = afr[32 * i2];
-                      A[i2][0] = v.x; A[i2][1] = v.y; A[i2][2] = v.z; A[i2][3] = v.w;
-                    }
-                    a_ready = true;
-                  }
-                }
-                const uint8_t* tile = stg + toff[tt];
-                float acc[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-                  uint32_t R[16];
-                  unpack_k<FMT>(tile + (nt * 8 + r) * F::kRB + q * F::kKChunk, R);
-#pragma unroll
-                  for (int s2 = 0; s2 < 8; ++s2)
-                    mma_f16(acc[nt], A[s2][0], A[s2][1], A[s2][2], A[s2][3], R[2 * s2], R[2 * s2 + 1]);
-                }
-                const int tok_valid = (int)min(16LL, (long long)sg.qn - i * 16);  // < 16 only for a partial FP8 tile
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int nt = e >> 1, c = e & 1;
-                  const float dot = acc[nt][c] + acc[nt][c + 2];
-                  const int t = nt * 8 + 2 * q + c;
-                  sig[tt * 4 + e] = (t < tok_valid) ? fmaf(dot, kfac, cterm) : -INFINITY;
-                }
-                if constexpr (F::kInt) {
-                  const float* vsp = reinterpret_cast<const float*>(tile + 32 * F::kRB);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const int t = (e >> 1) * 8 + 2 * q + (e & 1);
-#pragma unroll
-                    for (int jg = 0; jg < NGV; ++jg) smax = fmaxf(smax, vsp[t * NGV + jg]);
-                  }
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sig[tt * 4 + e] = -INFINITY;
+                for (int jg = 0; jg < NGV; ++jg) smax = fmaxf(smax, sv[jg]);
               }
             }
-            float pr[kChunk * 4];
-            const float inv_s = softmax_step<NGV, kChunk * 4>(stt, sig, smax, pr);
+            float pr[NBQ][2];
+            softmax_tile<NBQ, NGV, F::kInt>(stt, sig, smax, r, q, pr);
+            // PV
+            float pt[4];
+            p_operand<NBQ, 2>(pr, 0, r, q, pt);
+            uint32_t B0[NGV], B1[NGV];
+            if constexpr (F::kFp8) {
+              const float f = s_v8 * stt.inv_S * kPrescale;
+              B0[0] = pack_f16(pt[0] * f, pt[1] * f);
+              B1[0] = pack_f16(pt[2] * f, pt[3] * f);
+            } else {
+              constexpr float kH = (float)F::kHalf;
+              const float f = stt.inv_S * kPrescale;
 #pragma unroll
-            for (int tt = 0; tt < kChunk; ++tt) {
-              if (toff[tt] < 0) continue;
-              const long long i = i0 + k + tt;
-              const uint8_t* tile = stg + toff[tt];
-              uint32_t W[F::kVChunk / 4];
-              {
-                const uint4* vp = reinterpret_cast<const uint4*>(tile + F::kTile + lane * F::kVChunk);
+              for (int jg = 0; jg < NGV; ++jg) {  // one Value group at a time: few live registers
+                float w[4];
 #pragma unroll
-                for (int i2 = 0; i2 < F::kVChunk / 16; ++i2) {
-                  const uint4 v = vp[i2];
-                  W[4 * i2] = v.x; W[4 * i2 + 1] = v.y; W[4 * i2 + 2] = v.z; W[4 * i2 + 3] = v.w;
+                for (int e = 0; e < 4; ++e) {
+                  w[e] = pt[e] * (vsp[tk[e] * NGV + jg] * f);
+                  stt.zacc[jg] = fmaf(w[e], kH - vzp[tk[e] * NGV + jg], stt.zacc[jg]);
                 }
+                B0[jg] = pack_f16(w[0], w[1]);
+                B1[jg] = pack_f16(w[2], w[3]);
               }
-              if constexpr (F::kFp8) {
-                const int tok_valid = (int)min(16LL, (long long)sg.qn - i * 16);
-                if (tok_valid < 16) {
-                  // partial tile: bytes past the end may be stale; zero the lane's invalid tokens (byte e = token e)
-                  const bool v0 = 2 * q < tok_valid, v1 = 2 * q + 1 < tok_valid;
-                  const bool v2 = 8 + 2 * q < tok_valid, v3 = 9 + 2 * q < tok_valid;
-                  const uint32_t mk =
-                      (v0 ? 0xFFu : 0u) | (v1 ? 0xFF00u : 0u) | (v2 ? 0xFF0000u : 0u) | (v3 ? 0xFF000000u : 0u);
-#pragma unroll
-                  for (int i2 = 0; i2 < F::kVChunk / 4; ++i2) W[i2] &= mk;
-                }
-                uint32_t ah0, al0, ah1, al1;
-                const float f = s_v8 * inv_s;
-                split_f16(pr[tt * 4 + 0] * f, pr[tt * 4 + 1] * f, ah0, al0);
-                split_f16(pr[tt * 4 + 2] * f, pr[tt * 4 + 3] * f, ah1, al1);
-#pragma unroll
-                for (int jt = 0; jt < 16; ++jt) {
-                  uint32_t b01, b23;
-                  switch (jt) {
-#define KVQ_V(J) case J: unpack_v<FMT, J>(W, b01, b23); break;
-                    KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
-                    KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
-                  }
-                  mma_f16(stt.o[jt], ah0, al0, ah1, al1, b01, b23);
-                }
-              } else {
-                constexpr int kTilesPerGroup = 16 / NGV;  // n-tiles of 8 channels per Value group
-                constexpr float kH = (float)F::kHalf;
-                const float* vsp = reinterpret_cast<const float*>(tile + 32 * F::kRB);
-                const float* vzp = vsp + 16 * NGV;
-#pragma unroll
-                for (int jg = 0; jg < NGV; ++jg) {
-                  float w[4];
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const int t = (e >> 1) * 8 + 2 * q + (e & 1);
-                    w[e] = (vsp[t * NGV + jg] * inv_s) * pr[tt * 4 + e];
-                    stt.zacc[jg] = fmaf(w[e], kH - vzp[t * NGV + jg], stt.zacc[jg]);
-                  }
-                  uint32_t ah0, al0, ah1, al1;
-                  split_f16(w[0], w[1], ah0, al0);
-                  split_f16(w[2], w[3], ah1, al1);
-#pragma unroll
-                  for (int jj = 0; jj < kTilesPerGroup; ++jj) {
-                    uint32_t b01, b23;
-                    switch (jg * kTilesPerGroup + jj) {
-                      KVQ_V(0) KVQ_V(1) KVQ_V(2) KVQ_V(3) KVQ_V(4) KVQ_V(5) KVQ_V(6) KVQ_V(7)
-                      KVQ_V(8) KVQ_V(9) KVQ_V(10) KVQ_V(11) KVQ_V(12) KVQ_V(13) KVQ_V(14) KVQ_V(15)
-#undef KVQ_V
-                    }
-                    mma_f16(stt.o[jg * kTilesPerGroup + jj], ah0, al0, ah1, al1, b01, b23);
-                  }
-                }
-              }
+            }
+            {
+              uint32_t VW[F::kWords];
+              load_words(tile + F::kTile, lane, VW);
+              pv_tile<FMT, NGV>(VW, B0, B1, stt.o);
             }
           }
         }
-        __syncwarp();
-        ++n_consumed;
-        while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
+        release();
       }
 
-      // ---- finalise the warp's state and publish it ----
-      float l = stt.l;
-      l += __shfl_xor_sync(kFull, l, 1);
-      l += __shfl_xor_sync(kFull, l, 2);
-      float zs[NGV];
+      // ---- finalise the warp's state (output layout: heads 2q, 2q + 1) ----
+      float lsum[NBQ];
+#pragma unroll
+      for (int b = 0; b < NBQ; ++b) {
+        float l = stt.l[b];
+        l += __shfl_xor_sync(kFull, l, 4);
+        l += __shfl_xor_sync(kFull, l, 8);
+        l += __shfl_xor_sync(kFull, l, 16);
+        lsum[b] = l;
+      }
+      // m and l of heads 2q and 2q + 1 (score lanes (2q) & 3, (2q + 1) & 3 of block q >> 1)
+      float mo[2], lo2[2];
+      mo[0] = __shfl_sync(kFull, stt.m[0], (2 * q) & 3);
+      mo[1] = __shfl_sync(kFull, stt.m[0], (2 * q + 1) & 3);
+      lo2[0] = __shfl_sync(kFull, lsum[0], (2 * q) & 3);
+      lo2[1] = __shfl_sync(kFull, lsum[0], (2 * q + 1) & 3);
+      if constexpr (NBQ == 2) {
+        const float m0 = __shfl_sync(kFull, stt.m[1], (2 * q) & 3), m1 = __shfl_sync(kFull, stt.m[1], (2 * q + 1) & 3);
+        const float l0 = __shfl_sync(kFull, lsum[1], (2 * q) & 3), l1 = __shfl_sync(kFull, lsum[1], (2 * q + 1) & 3);
+        if (q >= 2) {
+          mo[0] = m0;
+          mo[1] = m1;
+          lo2[0] = l0;
+          lo2[1] = l1;
+        }
+      }
+      // zero-point sums: head r in the W layout, summed over the token lanes q; head 2q (+1) is at lane 8q (+4)
+      float zo[2][NGV];
 #pragma unroll
       for (int jg = 0; jg < NGV; ++jg) {
         float z = stt.zacc[jg];
         z += __shfl_xor_sync(kFull, z, 1);
         z += __shfl_xor_sync(kFull, z, 2);
-        zs[jg] = z;
+        zo[0][jg] = __shfl_sync(kFull, z, 8 * q);
+        zo[1][jg] = __shfl_sync(kFull, z, 8 * q + 4);
       }
-      __syncwarp();
-      float* rec = reinterpret_cast<float*>(my_scratch);
-      if (r < g) {
-        const float unit = stt.S / kPrescale;
-        float* rr = rec + r * kMergeStride;
-        if (q == 0) {
-          rr[0] = stt.m;
-          rr[1] = l;
-        }
+      // o = sum of W * (Value operand) with W = p s kPrescale / S
+      const float unit = stt.S / kPrescale;
 #pragma unroll
-        for (int jt = 0; jt < 16; ++jt) {
-          const float z = F::kInt ? zs[jt / (16 / NGV)] : 0.f;
-          float2 v;
-          v.x = (stt.o[jt][0] + stt.o[jt][2] + z) * unit;
-          v.y = (stt.o[jt][1] + stt.o[jt][3] + z) * unit;
-          if (stt.m == -INFINITY) v.x = v.y = 0.f;
-          *reinterpret_cast<float2*>(rr + 4 + jt * 8 + 2 * q) = v;
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          const float z = F::kInt ? zo[e][mb * NGV / 8] : 0.f;
+          stt.o[mb][e] = (stt.o[mb][e] + z) * unit;
+          stt.o[mb][2 + e] = (stt.o[mb][2 + e] + z) * unit;
         }
+      // ---- fold the warps into one record per head (m, l, o[128]), one warp at a time ----
+      float* rec = reinterpret_cast<float*>(scratch);
+      __syncthreads();  // the previous segment's record has been read
+      for (int w = 0; w < kNW; ++w) {
+        if (warp == w) {
+          float mr[2], lr[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int hh = min(2 * q + e, g - 1);
+            mr[e] = w == 0 ? -INFINITY : rec[hh * kMergeStride];
+            lr[e] = w == 0 ? 0.f : rec[hh * kMergeStride + 1];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int hh = 2 * q + e;
+            if (hh < g) {
+              float* rr = rec + hh * kMergeStride;
+              const float M = fmaxf(mr[e], mo[e]);
+              const float ar = mr[e] == -INFINITY ? 0.f : exp2f(mr[e] - M);
+              const float aw = mo[e] == -INFINITY ? 0.f : exp2f(mo[e] - M);
+              if (r == 0) {
+                rr[0] = M;
+                rr[1] = ar * lr[e] + aw * lo2[e];
+              }
+#pragma unroll
+              for (int mb = 0; mb < 8; ++mb) {
+                const int c0 = 4 + 16 * mb + r, c1 = c0 + 8;
+                const float o0 = aw * stt.o[mb][e], o1 = aw * stt.o[mb][2 + e];
+                rr[c0] = w == 0 ? o0 : fmaf(ar, rr[c0], o0);
+                rr[c1] = w == 0 ? o1 : fmaf(ar, rr[c1], o1);
+              }
+            }
+          }
+        }
+        __syncthreads();
       }
-      __syncthreads();
-      // ---- merge the warps; write the partial of (b, h), or the result when this CTA owns the pair ----
+      // ---- write the partial of (b, h), or the result when this CTA owns the pair ----
       {
         const int b = sg.b, h = sg.h;
         const long long pair = (long long)b * H + h;
@@ -947,24 +1070,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         const long long P0 = sg.pair_start, P1 = sg.pair_start + sg.units;
         const long long c_lo = ((P0 + 1) * C - 1) / U, c_hi = (P1 * C - 1) / U;
         const bool whole = p.fuse && c_lo == c_hi;  // no other CTA touches this pair
-        const float* recs = reinterpret_cast<const float*>(scratch);
         for (int i = tid; i < g * 128; i += kThreads) {
           const int hr = i >> 7, c = i & 127;
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kNW; ++w) M = fmaxf(M, recs[w * (p.warp_scratch / 4) + hr * kMergeStride]);
-          float Lsum = 0.f, O = 0.f;
-          if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-              const float* rw = recs + w * (p.warp_scratch / 4) + hr * kMergeStride;
-              const float f = exp2f(rw[0] - M);  // 0 for an empty warp (m = -inf)
-              Lsum = fmaf(rw[1], f, Lsum);
-              O = fmaf(rw[4 + c], f, O);
-            }
-          }
+          const float* rr = rec + hr * kMergeStride;
+          const float M = rr[0], Lsum = rr[1];
           const bool empty = !(Lsum > 0.f);
-          const float o = empty ? 0.f : O / Lsum;
+          const float o = empty ? 0.f : rr[4 + c] / Lsum;
           const float l2 = empty ? -INFINITY : M + log2f(Lsum);
           if (whole) {
             write_out(p, b, h * g + hr, c, o, l2);
@@ -1040,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV>
+template <int FMT, int NGV, int NBQ>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1049,24 +1160,34 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, NBQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
+// One column block for up to 4 query heads per kv head, two for 5..8.
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV>(smem);
-  if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV><<<p.num_ctas, kThreads, smem, stream>>>(p);
+  cudaError_t e;
+  if (p.g <= 4) {
+    if ((e = ensure_smem_attr<FMT, NGV, 1>(smem)) != cudaSuccess) return e;
+    decode_kernel<FMT, NGV, 1><<<p.num_ctas, kThreads, smem, stream>>>(p);
+  } else {
+    if ((e = ensure_smem_attr<FMT, NGV, 2>(smem)) != cudaSuccess) return e;
+    decode_kernel<FMT, NGV, 2><<<p.num_ctas, kThreads, smem, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
 template <int FMT, int NGV>
-cudaError_t occupancy_t(int smem, int* n) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV>(smem);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV>, kThreads, smem);
+cudaError_t occupancy_t(int g, int smem, int* n) {
+  cudaError_t e;
+  if (g <= 4) {
+    if ((e = ensure_smem_attr<FMT, NGV, 1>(smem)) != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 1>, kThreads, smem);
+  }
+  if ((e = ensure_smem_attr<FMT, NGV, 2>(smem)) != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 2>, kThreads, smem);
 }
 
 }  // namespace kvq

@@ -31,7 +31,6 @@ __global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
   const __nv_bfloat16* sink_v = reinterpret_cast<const __nv_bfloat16*>(p.C.sink_v);
   const __nv_bfloat16* ring_k = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_k);
   const __nv_bfloat16* ring_v = reinterpret_cast<const __nv_bfloat16*>(p.C.resid_v);
-  const int per_byte = 8 / L.bits;
   const uint32_t cmask = (1u << L.bits) - 1u;
   for (int tt = 0; tt < 16; ++tt) {
     const long long t = (long long)blockIdx.y * 16 + tt;
@@ -47,17 +46,18 @@ __global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
       if (rec) {
         const uint8_t* tile = tile_in_record(L, rec, i);
         const int row = (int)(x % 16);
-        int byte, bit;
+        int kbyte, kbit, byte, bit;
+        ktile_pos(L.bits, L.fp8 != 0, row, c, kbyte, kbit);
         vtile_pos(L.bits, L.fp8 != 0, row, c, byte, bit);
         if (L.fp8) {
-          kx = __fmul_rn(*p.C.k_tscale, e4m3_value(tile[row * L.rb + c]));
+          kx = __fmul_rn(*p.C.k_tscale, e4m3_value(tile[kbyte]));
           vx = __fmul_rn(*p.C.v_tscale, e4m3_value(tile[16 * L.rb + byte]));
         } else {
           const float* ks = reinterpret_cast<const float*>(rec);
           const float* kz = ks + 128;
           const float* vs = reinterpret_cast<const float*>(tile + 32 * L.rb);
           const float* vz = vs + 16 * L.ngv;
-          const uint32_t kcode = (tile[row * L.rb + c / per_byte] >> ((c % per_byte) * L.bits)) & cmask;
+          const uint32_t kcode = (tile[kbyte] >> kbit) & cmask;
           const uint32_t vcode = (tile[16 * L.rb + byte] >> bit) & cmask;
           const int j = c / L.Gv;
           kx = __fmul_rn(ks[c], __fsub_rn((float)kcode, kz[c]));

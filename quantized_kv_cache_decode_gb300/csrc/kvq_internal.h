@@ -54,7 +54,7 @@ struct DecodeParams {
   float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial
   int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
   uint32_t* status;
-  int warp_scratch;  // bytes of shared scratch per warp (bf16 tile staging / merge record)
+  int merge_bytes;   // bytes of the CTA's merge record in shared memory (g heads)
   // fused combine: the last CTA to finish a (sequence, kv head) pair merges its partials
   int fuse;
   unsigned* counters;  // [batch * H] arrival counters, zero between calls
@@ -103,10 +103,10 @@ cudaError_t launch_decode_int2(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_int4(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_int8(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int smem, cudaStream_t s);
-cudaError_t occupancy_decode_int2(int ngv, int smem, int* n);
-cudaError_t occupancy_decode_int4(int ngv, int smem, int* n);
-cudaError_t occupancy_decode_int8(int ngv, int smem, int* n);
-cudaError_t occupancy_decode_fp8(int ngv, int smem, int* n);
+cudaError_t occupancy_decode_int2(int ngv, int g, int smem, int* n);
+cudaError_t occupancy_decode_int4(int ngv, int g, int smem, int* n);
+cudaError_t occupancy_decode_int8(int ngv, int g, int smem, int* n);
+cudaError_t occupancy_decode_fp8(int ngv, int g, int smem, int* n);
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_fp8_calibrate(const void* x, size_t n, float* scale_out, cudaStream_t stream);

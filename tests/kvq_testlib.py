@@ -23,39 +23,42 @@ BITS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8}
 # --------------------------------------------------------------------------- #
 
 
-def vtile_positions(fmt: str):
-    """(byte[16,128], bit[16,128]) of element (token, channel) in a 16-token Value tile."""
-    t = np.arange(16)[:, None]
-    c = np.arange(128)[None, :]
-    n, j = c % 8, c // 8
-    q, e = (t % 8) // 2, (t % 2) + 2 * (t // 8)
-    lane = 4 * n + q
-    if fmt == "fp8_e4m3":
-        return lane * 64 + 4 * j + e + 0 * c, np.zeros((16, 128), int)
-    if fmt == "int8":
-        return lane * 64 + 4 * j + np.array([0, 2, 1, 3])[e], np.zeros((16, 128), int)
+def _frag_positions(fmt: str, i: np.ndarray, k: np.ndarray, s: np.ndarray):
+    """(byte, bit) of A-operand element (row i, column k) of step s (the header's fragment order)."""
+    lane = 4 * (i % 8) + (k % 8) // 2
+    reg = i // 8 + 2 * (k // 8)
+    h = k % 2
     if fmt == "int4":
-        o = np.array([0, 16, 4, 20])[e] + 8 * (j % 2)
-        return lane * 32 + 4 * (j // 2) + o // 8, o % 8
-    o = 2 * (2 * (j % 4) + e // 2) + 16 * (e % 2)
-    return lane * 16 + 4 * (j // 4) + o // 8, o % 8
+        w, bit = s, 4 * reg + 16 * h
+    elif fmt == "int2":
+        w, bit = s // 2, 8 * (s % 2) + 2 * reg + 16 * h
+    elif fmt == "int8":
+        w, bit = 2 * s + reg // 2, 8 * ((reg % 2) + 2 * h)
+    else:  # fp8_e4m3
+        w, bit = 2 * s + reg // 2, 8 * (2 * (reg % 2) + h)
+    byte = ((w // 4) * 32 + lane) * 16 + (w % 4) * 4 + bit // 8
+    return byte, bit % 8
 
 
-def unpack_k_rows(raw: np.ndarray, fmt: str) -> np.ndarray:
-    """Key code rows [n, rb] bytes -> codes [n, 128] (little-endian packing along d)."""
+def ktile_positions(fmt: str):
+    """(byte[16,128], bit[16,128]) of Key code (token, channel) in a tile's K part."""
+    t = np.arange(16)[:, None] + 0 * np.arange(128)[None, :]
+    c = 0 * np.arange(16)[:, None] + np.arange(128)[None, :]
+    e = c % 4
+    return _frag_positions(fmt, t, 2 * ((c // 4) % 4) + e % 2 + 8 * (e // 2), c // 16)
+
+
+def vtile_positions(fmt: str):
+    """(byte[16,128], bit[16,128]) of Value code (token, channel) in a tile's V part."""
+    t = np.arange(16)[:, None] + 0 * np.arange(128)[None, :]
+    c = 0 * np.arange(16)[:, None] + np.arange(128)[None, :]
+    return _frag_positions(fmt, c % 16, t, c // 16)
+
+
+def unpack_tiles(raw: np.ndarray, fmt: str, positions) -> np.ndarray:
+    """Code matrices of tiles [ntiles, 16*rb] bytes -> codes [ntiles*16, 128]."""
     b = BITS[fmt]
-    per = 8 // b
-    raw = raw.astype(np.uint32)
-    out = np.zeros((raw.shape[0], 128), np.uint8)
-    for c in range(128):
-        out[:, c] = (raw[:, c // per] >> ((c % per) * b)) & ((1 << b) - 1)
-    return out
-
-
-def unpack_v_tiles(raw: np.ndarray, fmt: str) -> np.ndarray:
-    """Value tiles [ntiles, 16*rb] bytes -> codes [ntiles*16, 128]."""
-    b = BITS[fmt]
-    byte, bit = vtile_positions(fmt)
+    byte, bit = positions(fmt)
     raw = raw.astype(np.uint32)
     vals = (raw[:, byte] >> bit[None]) & ((1 << b) - 1)   # [ntiles, 16, 128]
     return vals.reshape(-1, 128).astype(np.uint8)
@@ -197,7 +200,7 @@ class GpuLayer:
         for i in range(ntiles):
             recb = self._record(b, h, i // tpg)
             t = recb[hdr + (i % tpg) * tile: hdr + (i % tpg + 1) * tile]
-            kc.append(t[:16 * rb].reshape(16, rb))
+            kc.append(t[:16 * rb].reshape(1, 16 * rb))
             vt.append(t[16 * rb:32 * rb].reshape(1, 16 * rb))
             if not self.fp8:
                 vs.append(t[32 * rb:32 * rb + 64 * ngv].view(F32).reshape(16, ngv))
@@ -206,15 +209,15 @@ class GpuLayer:
                     ks.append(recb[:512].view(F32).reshape(1, 128))
                     kz.append(recb[512:1024].view(F32).reshape(1, 128))
         out = {}
-        kc = np.concatenate(kc)[:qn] if kc else np.zeros((0, rb), np.uint8)
+        kc = np.concatenate(kc) if kc else np.zeros((0, 16 * rb), np.uint8)
         vt = np.concatenate(vt) if vt else np.zeros((0, 16 * rb), np.uint8)
         if not self.fp8:
             out["k_s"] = np.concatenate(ks)[:qn // self.G] if ks else np.zeros((0, 128), F32)
             out["k_z"] = np.concatenate(kz)[:qn // self.G] if kz else np.zeros((0, 128), F32)
             out["v_s"] = np.concatenate(vs)[:qn] if vs else np.zeros((0, ngv), F32)
             out["v_z"] = np.concatenate(vz)[:qn] if vz else np.zeros((0, ngv), F32)
-        out["k_codes"] = unpack_k_rows(kc, self.fmt)
-        out["v_codes"] = unpack_v_tiles(vt, self.fmt)[:qn] if len(vt) else np.zeros((0, 128), np.uint8)
+        out["k_codes"] = unpack_tiles(kc, self.fmt, ktile_positions)[:qn] if len(kc) else np.zeros((0, 128), np.uint8)
+        out["v_codes"] = unpack_tiles(vt, self.fmt, vtile_positions)[:qn] if len(vt) else np.zeros((0, 128), np.uint8)
         pair = b * self.H + h
         if n_sink:
             sk = self.raw("sink_k").view(np.uint16).reshape(self.B * self.H, self.S, 128)[pair, :n_sink]

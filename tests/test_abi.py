@@ -88,12 +88,14 @@ def test_calls_reject_bad_arguments_before_any_launch(kvq):
     assert e.value.status == -1
 
 
-def test_fragment_order_is_a_bijection():
-    # every bit of a 16-token Value tile holds exactly one (token, channel) code
+@pytest.mark.parametrize("part", ["k", "v"])
+def test_fragment_order_is_a_bijection(part):
+    # every bit of a tile's K (V) code matrix holds exactly one (token, channel) code
     import numpy as np
     import kvq_testlib as TL
+    positions = TL.ktile_positions if part == "k" else TL.vtile_positions
     for fmt, bits in (("int2", 2), ("int4", 4), ("int8", 8), ("fp8_e4m3", 8)):
-        byte, bit = TL.vtile_positions(fmt)
+        byte, bit = positions(fmt)
         tile_bytes = 16 * 128 * bits // 8
         used = np.zeros(tile_bytes * 8, int)
         for t in range(16):
@@ -101,3 +103,18 @@ def test_fragment_order_is_a_bijection():
                 for k in range(bits):
                     used[byte[t, c] * 8 + bit[t, c] + k] += 1
         assert used.min() == 1 and used.max() == 1, fmt
+
+
+def test_fragment_order_lane_words():
+    # lane l's words are the 16-byte chunks l, l + 32, ... of the matrix: the K code of
+    # (token t, channel c) and the V code of (token t, channel c) are held by the lanes
+    # the tensor-core operand layout names (row t mod 8 / channel mod 8, column pair)
+    import numpy as np
+    import kvq_testlib as TL
+    for fmt in ("int2", "int4", "int8", "fp8_e4m3"):
+        kb, _ = TL.ktile_positions(fmt)
+        vb, _ = TL.vtile_positions(fmt)
+        t = np.arange(16)[:, None]
+        c = np.arange(128)[None, :]
+        assert np.array_equal((kb // 16) % 32, 4 * (t % 8) + (c // 4) % 4 + 0 * c)
+        assert np.array_equal((vb // 16) % 32, 4 * (c % 8) + (t % 8) // 2)
