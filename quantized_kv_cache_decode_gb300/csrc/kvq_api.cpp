@@ -12,10 +12,7 @@
 namespace kvq {
 namespace {
 
-constexpr int kThreadsDecode = 128;  // 4 warps (kvq_decode.cuh)
 constexpr int kMaxStages = 4;
-constexpr int kSmemPerSm = 228 * 1024;          // shared memory of one SM
-constexpr int kSmemReservedPerCta = 1024;         // reserved by the system for each resident CTA
 constexpr int kStaticSmemMargin = 1024;           // the kernel's static __shared__ variables (384 B)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -118,20 +115,21 @@ int stage_bytes_of(const LayerDesc& L, int tps) {
   return (std::max(q, bf) + 127) / 128 * 128;
 }
 
-// The CTA's merge record in shared memory: m, l, -, - and 128 outputs per query head.
+// A warp's merge record in shared memory: m, l, -, - and 128 outputs per query head.
 int merge_bytes_of(const LayerDesc& L, int g) {
   (void)L;
   return g * 132 * 4;
 }
 
 constexpr int kSegTableBytes = 16 * 48;  // kMaxSeg segment records of 48 bytes (kvq_decode.cuh)
+constexpr int kSlotTagBytes = 20;        // one pipeline slot's tag (kvq_decode.cuh)
 
-int fixed_smem(int batch, int merge_bytes) {
+int fixed_smem(int batch, int merge_bytes, int nw) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16;
-  // barriers and block-table windows per warp, the query rows (g + 1), the merge record
+  // per warp: barriers, block-table window, slot tags, merge record; the query rows (g + 1)
   const int g = merge_bytes / (132 * 4);
-  return kThreadsDecode / 32 * (kMaxStages * 8 + 32 * 4) + (g + 1) * 132 * 4 + merge_bytes + kSegTableBytes +
-         prefix;
+  const int per_warp = kMaxStages * 8 + 32 * 4 + (kMaxStages * kSlotTagBytes + 15) / 16 * 16 + merge_bytes;
+  return nw * per_warp + (g + 1) * 132 * 4 + kSegTableBytes + prefix;
 }
 
 cudaError_t occupancy_query(const LayerDesc& L, int g, int smem, int* n) {
@@ -178,41 +176,31 @@ struct DecodeGeom {
   size_t ws_bytes, off_lse, off_prefix, off_counters;
 };
 
-// Launch shape: two stages per warp (one being computed on, one in flight),
-// as many resident CTAs per SM as the registers allow (4 for up to 4 query
-// heads per kv head, 3 above) with stages of about 4 KB -- the integer formats
-// are bound by the tensor-core and unpack work per byte, so warps count most --
-// and, for FP8 (the least work per byte), 3 CTAs with stages of about 8 KB.
-// Fewer CTAs or smaller stages when the shared memory does not fit.  (Chosen
-// from a sweep of CTAs x stage size x stage count on GB300.)
+// Launch shape: one CTA per SM (its warps claim work items from a shared
+// counter, so all of them finish together), two stages per warp (one being
+// computed on, one in flight) of the largest size among about 8, 6, 4 and 2 KB
+// that fits the shared memory.
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) {
   const int wsc = merge_bytes_of(L, g);
-  const int fixed = fixed_smem(batch, wsc);
-  const int nw = kThreadsDecode / 32;
+  const int nw = decode_warps(L.fmt, g);
+  const int fixed = fixed_smem(batch, wsc, nw);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  const int pref_ctas = L.fp8 ? 3 : (g <= 4 ? 4 : 3);
   const int n = 2;
+  const int budget = 227 * 1024 - kStaticSmemMargin;
   int smem = 0, nst = 0, sb = 0, tps = 0;
   bool found = false;
-  for (int ctas = pref_ctas; ctas >= 1 && !found; --ctas) {
-    const int budget = std::min(kSmemPerSm / ctas - kSmemReservedPerCta, 227 * 1024) - kStaticSmemMargin;
-    for (int target : {8192, 6144, 4096}) {
-      if (!L.fp8 && target != 4096) continue;
-      const int t = tiles_per_stage(L, target);
-      const int b = stage_bytes_of(L, t);
-      if (fixed + nw * n * b > budget && ctas > 1) continue;
-      if (occupancy(L, g, fixed + nw * n * b, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
-      if (per_sm >= ctas) {
-        smem = fixed + nw * n * b;
-        nst = n;
-        sb = b;
-        tps = t;
-        found = true;
-        break;
-      }
-    }
+  for (int target : {8192, 6144, 4096, 2048}) {
+    const int t = tiles_per_stage(L, target);
+    const int b = stage_bytes_of(L, t);
+    if (fixed + nw * n * b > budget) continue;
+    smem = fixed + nw * n * b;
+    nst = n;
+    sb = b;
+    tps = t;
+    found = true;
+    break;
   }
   if (!found) return KVQ_ERR_UNSUPPORTED;
   if (occupancy(L, g, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -222,7 +210,7 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) 
   G->nst = nst;
   G->stage_bytes = sb;
   G->tps = tps;
-  G->num_ctas = sms * per_sm;
+  G->num_ctas = sms;  // one per SM
   const size_t slots = (size_t)G->num_ctas + (size_t)batch * L.H;
   const size_t o_bytes = slots * g * kHeadDim * sizeof(float);
   const size_t l_bytes = slots * g * sizeof(float);
@@ -347,6 +335,8 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.nst = G.nst;
   p.stage_bytes = G.stage_bytes;
   p.tps = G.tps;
+  // a claimed work item: whole records, at least a stage's worth of tiles
+  p.item_tiles = (std::max(G.tps, L.tpg) + L.tpg - 1) / L.tpg * L.tpg;
   // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
   p.bf_weight = std::max(1, (8192 + L.tile_bytes / 2) / L.tile_bytes);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

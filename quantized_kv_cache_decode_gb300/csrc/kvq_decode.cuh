@@ -9,16 +9,18 @@
 // Work decomposition.  Every (sequence, kv head) pair is a list of work units:
 // its 16-token bf16 tiles (sink + residual window, charged `bf_weight` units
 // each) followed by its 16-token quantized tiles (1 unit each).  The pairs'
-// lists are concatenated and cut into num_ctas equal ranges, one per CTA
-// (num_ctas = SMs x resident CTAs), so every CTA moves the same number of bytes
-// whatever the sequence lengths.  A CTA writes one partial (normalised output +
-// log-sum-exp) per pair it touches; the last CTA to finish a pair merges them.
+// lists are concatenated and cut into num_ctas equal ranges, one per CTA (one
+// CTA per SM), so every SM moves the same number of bytes whatever the sequence
+// lengths.  A CTA writes one partial (normalised output + log-sum-exp) per pair
+// it touches; the last CTA to finish a pair merges them.
 //
-// Inside a CTA the 4 warps split each pair's bf16 tiles and quantized tiles
-// evenly and run their own pipelines: lane 0 of a warp streams stages (tiles
+// Inside a CTA the 12 or 16 warps take a segment's work items (a bf16 tile, or
+// a Key group's quantized tiles) round robin, interleaved over the whole
+// segment, and run their own pipelines: lane 0 of a warp streams stages (tiles
 // with their scales) into shared memory with bulk asynchronous copies
-// (cp.async.bulk, TMA engine) completing on per-stage mbarriers, several stages
-// ahead of the compute.
+// (cp.async.bulk, TMA engine) completing on per-stage mbarriers, a stage ahead
+// of the compute, so the copies of the next items (and segments) overlap the
+// math.
 //
 // Tensor-core mapping (mma.sync m16n8k16, fp32 accumulate).  The cache tile is
 // the A operand (16 rows), the query side the B operand (8 columns):
@@ -45,8 +47,14 @@
 
 namespace kvq {
 
-constexpr int kNW = 4;                 // warps per CTA
-constexpr int kThreads = kNW * 32;
+// Warps per CTA (one CTA per SM): 16 for 2- and 4-bit codes with up to 4 query
+// heads per kv head (128 registers a thread), else 12 (170 registers);
+// decode_warps() in kvq_internal.h states the same rule for the host.
+template <int FMT, int NBQ>
+struct DecodeWarps {
+  static constexpr int kNW = (NBQ == 1 && (FMT == 2 || FMT == 4)) ? 16 : 12;
+  static constexpr int kThreads = kNW * 32;
+};
 constexpr int kMaxStages = 4;
 constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 range is safe
 constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
@@ -496,6 +504,7 @@ __device__ __forceinline__ int active_ctas(long long c_lo, long long c_hi, long 
   return n;
 }
 constexpr int kMaxParts = 64;  // partials of one pair merged from a shared-memory list
+static_assert(kMaxParts + 2 <= kMergeStride, "the merge weights live in a merge-record row");
 
 // One (sequence, kv head) pair's share of this CTA's unit range.
 struct SegRec {
@@ -505,50 +514,68 @@ struct SegRec {
 };
 constexpr int kMaxSeg = 16;  // segments per table batch
 
-// This warp's part of a segment: bf16 tiles [bf0, bf0 + nbf_w), quantized tiles
-// [q0, q0 + nq_w).  A pair's units are its nbf bf16 tiles (wbf units each) and
-// then its nq quantized tiles (1 unit each); a bf16 tile belongs to the range
-// holding its first unit.  The CTA's tiles of each kind are split evenly among
-// the warps.  Stages: two per bf16 tile (its K rows, then its V rows), then
-// ceil(nq_w / tps) quantized stages.
-struct WarpPart {
-  int bf0, nbf_w, q0, nq_w, nstage;
+// Work items of one segment, dealt to the CTA's warps round robin (item t to
+// warp t mod NW: every warp's share is interleaved over the segment, so the
+// warps finish together and each warp's sums run in a fixed order): its
+// bf16 tiles [bl, bl + nbf_items) (a pair's units are its nbf bf16 tiles, wbf
+// units each, then its nq quantized tiles, 1 unit each; a bf16 tile belongs to
+// the range holding its first unit), then its quantized tiles [ql, qh) in items
+// of `it` tiles aligned at multiples of `it` (whole records for the integer
+// formats, so an item starts at a record header except at ql).
+struct SegItems {
+  int bl, nbf_items, ql, qh, al, nq_items;
 };
 
-__device__ __forceinline__ WarpPart warp_part(const SegRec& sg, int warp, int wbf, int tps) {
-  const int nbu = sg.nbf * wbf;  // units of the bf16 tiles
-  const int bl = min(sg.nbf, (sg.ua + wbf - 1) / wbf), bh = min(sg.nbf, (sg.ue + wbf - 1) / wbf);
-  const int ql = min(sg.nq, max(0, sg.ua - nbu)), qh = min(sg.nq, max(0, sg.ue - nbu));
-  WarpPart w;
-  w.bf0 = bl + (bh - bl) * warp / kNW;
-  w.nbf_w = bl + (bh - bl) * (warp + 1) / kNW - w.bf0;
-  w.q0 = ql + (qh - ql) * warp / kNW;
-  w.nq_w = ql + (qh - ql) * (warp + 1) / kNW - w.q0;
-  w.nstage = 2 * w.nbf_w + (w.nq_w + tps - 1) / tps;
-  return w;
+__device__ __forceinline__ SegItems seg_items(const SegRec& sg, int wbf, int it) {
+  SegItems s;
+  const int nbu = sg.nbf * wbf;
+  s.bl = min(sg.nbf, (sg.ua + wbf - 1) / wbf);
+  s.nbf_items = min(sg.nbf, (sg.ue + wbf - 1) / wbf) - s.bl;
+  s.ql = min(sg.nq, max(0, sg.ua - nbu));
+  s.qh = min(sg.nq, max(0, sg.ue - nbu));
+  s.al = s.ql / it * it;
+  s.nq_items = s.qh > s.ql ? (s.qh - s.al + it - 1) / it : 0;
+  return s;
 }
 
+// Tag of a pipeline slot: what its stage holds.  seg: segment index; kind 1/2:
+// K/V rows of bf16 tile `a`; kind 3: n quantized tiles from tile `a` (at
+// position rpos of its record), `first` when the stage starts an item (the Key
+// group's B operand is built there).
+struct SlotTag {
+  int seg, a, rpos;
+  short kind, n;
+  int first;
+};
+static_assert(sizeof(SlotTag) == 20, "the host reserves 20 bytes per slot tag");
+static_assert(sizeof(SegRec) == 48, "the host reserves 48 bytes per segment record");
+
 template <int FMT, int NGV, int NBQ>
-__global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
+  constexpr int NW = DecodeWarps<FMT, NBQ>::kNW;
+  constexpr int NT = NW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerDesc& L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, q = lane & 3;
   const int B = p.batch, H = L.H, g = p.g;
   const int tps = p.tps, nst = p.nst, wbf = p.bf_weight;
+  const int it = p.item_tiles;
 
   // ---- shared memory carve-up ----
   uint8_t* stage_base = smem;
-  size_t off = (size_t)kNW * nst * p.stage_bytes;
+  size_t off = (size_t)NW * nst * p.stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
-  off += kNW * kMaxStages * sizeof(uint64_t);
+  off += NW * kMaxStages * sizeof(uint64_t);
   int* tbl = reinterpret_cast<int*>(smem + off);  // per warp: a window of 32 block-table entries
-  off += kNW * 32 * sizeof(int);
+  off += NW * 32 * sizeof(int);
+  SlotTag* tags = reinterpret_cast<SlotTag*>(smem + off);  // per warp and slot
+  off += NW * kMaxStages * sizeof(SlotTag);
   float* q_s = reinterpret_cast<float*>(smem + off);  // [g + 1 rows][kQRow]: the query heads, a zero row
   off += (size_t)(g + 1) * kQRow * sizeof(float);
-  uint8_t* scratch = smem + off;  // the CTA's merge record: [g heads][kMergeStride]
-  off += (size_t)p.merge_bytes;
+  float* recs = reinterpret_cast<float*>(smem + off);  // per warp: merge record [g heads][kMergeStride]
+  off += (size_t)NW * p.merge_bytes;
   SegRec* segs = reinterpret_cast<SegRec*>(smem + off);
   off += kMaxSeg * sizeof(SegRec);
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
@@ -556,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
   __shared__ long long batch_end;
 
   if (tid == 0) {
-    for (int i = 0; i < kNW * kMaxStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    for (int i = 0; i < NW * kMaxStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_barrier_init();
   }
 
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
     return nbf * wbf + nq;
   };
   {
-    const int per = (B + kThreads - 1) / kThreads;
+    const int per = (B + NT - 1) / NT;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int local = 0;
     for (int b = b0; b < b1; ++b) {
@@ -588,21 +615,21 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
       const int v = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += v;
     }
-    __shared__ int warp_tot[kNW];
+    __shared__ int warp_tot[NW];
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     int wbase = 0;
     for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
     const int excl = wbase + incl - local;
     for (int b = b0; b < b1; ++b) prefix[b] += excl;
-    if (tid == kThreads - 1) prefix[B] = wbase + incl;
+    if (tid == NT - 1) prefix[B] = wbase + incl;
     if (blockIdx.x == 0) {
-      for (int b = tid; b < B; b += kThreads)
+      for (int b = tid; b < B; b += NT)
         if (p.seq_lens[b] > tmax_tok) report(p.status, KVQ_DEV_CAPACITY);
     }
     __syncthreads();
     if (blockIdx.x == 0)
-      for (int b = tid; b <= B; b += kThreads) p.ws_prefix[b] = prefix[b];
+      for (int b = tid; b <= B; b += NT) p.ws_prefix[b] = prefix[b];
   }
 
   const long long U = prefix[B];
@@ -611,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
     // sequences without tokens belong to no CTA's range: out = 0, lse = -inf
     for (int b = blockIdx.x; b < B; b += gridDim.x)
       if (prefix[b + 1] == prefix[b])
-        for (int i = tid; i < p.Hq * 128; i += kThreads) write_out(p, b, i >> 7, i & 127, 0.f, -INFINITY);
+        for (int i = tid; i < p.Hq * 128; i += NT) write_out(p, b, i >> 7, i & 127, 0.f, -INFINITY);
   }
   const long long st = (long long)blockIdx.x * U / C;
   const long long en = (long long)(blockIdx.x + 1) * U / C;
@@ -625,6 +652,8 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
   uint8_t* my_stages = stage_base + (size_t)warp * nst * p.stage_bytes;
   uint64_t* my_bars = bars + warp * kMaxStages;
   int* my_tbl = tbl + warp * 32;
+  SlotTag* my_tags = tags + warp * kMaxStages;
+  float* my_rec = recs + (size_t)warp * (p.merge_bytes / 4);
   uint32_t phase_bits = 0;  // expected parity of each stage barrier of this warp
   uint32_t slot_valid = 0;  // lane 0: 8 bits per slot, the tiles its stage holds
   uint32_t pending = 0;     // slots with copies in flight
@@ -634,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
 
   // the g query heads of a pair into q_s (row g zero)
   auto load_q = [&](const SegRec& sg) {
-    for (int i = tid; i < (g + 1) * 128; i += kThreads) {
+    for (int i = tid; i < (g + 1) * 128; i += NT) {
       const int hr = i >> 7, c = i & 127;
       float v = 0.f;
       if (hr < g) v = __bfloat162float(qg[((long long)sg.b * p.Hq + sg.h * g + hr) * 128 + c]);
@@ -678,30 +707,69 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
     __syncthreads();
     const int nseg = seg_count;
 
-    // ---- producer (lane 0 copies; every lane keeps the same cursor) ----
-    int ps = 0, pj = 0;
-    WarpPart pw = warp_part(segs[0], warp, wbf, tps);
-    while (ps < nseg && pw.nstage == 0) {
-      ++ps;
-      if (ps < nseg) pw = warp_part(segs[ps], warp, wbf, tps);
-    }
-    // quantized cursor: record and position in it of the next quantized tile of the part
-    int q_rec = pw.q0 / L.tpg, q_pos = pw.q0 - q_rec * L.tpg;
-    int tb_base = -1;  // paged: first record of the block-table window in my_tbl (-1: none)
+    // ---- producer: lane 0 copies; every lane keeps the same cursor ----
+    int ps = 0;                  // segment of the producer
+    int pk = 0;                  // kind of the current item: 0 none, 1 bf16, 3 quantized
+    int p_a = 0, p_end = 0;      // bf16: tile and next half (0 K, 1 V, 2 done); quantized: next tile, end
+    bool p_first = false;        // the item's first stage is next
+    int q_rec = 0, q_pos = 0;    // record and position in it of the next quantized tile
+    int tb_base = -1;            // paged: first record of the block-table window in my_tbl (-1: none)
+    int tb_seg = -1;             // ... and its segment
+    int p_claims = 0;            // items taken from segment ps
+    int psi_seg = -1;            // segment whose items psi holds
+    SegItems psi;
+    // the next item with stages left, taken from the segments in order; false when none
+    auto producer_ready = [&]() -> bool {
+      while (ps < nseg) {
+        if (pk == 1 && p_end < 2) return true;
+        if (pk == 3 && p_a < p_end) return true;
+        const int t = warp + NW * (p_claims++);  // items warp, warp + NW, ... of the segment
+        if (psi_seg != ps) {
+          psi = seg_items(segs[ps], wbf, it);
+          psi_seg = ps;
+        }
+        const SegItems& si = psi;
+        if (t < si.nbf_items) {
+          pk = 1;
+          p_a = si.bl + t;
+          p_end = 0;
+        } else if (t - si.nbf_items < si.nq_items) {
+          const int k = t - si.nbf_items;
+          pk = 3;
+          p_a = max(si.ql, si.al + k * it);
+          p_end = min(si.qh, si.al + (k + 1) * it);
+          p_first = true;
+          q_rec = p_a / L.tpg;
+          q_pos = p_a - q_rec * L.tpg;
+        } else {
+          pk = 0;
+          ++ps;
+          p_claims = 0;
+        }
+      }
+      return false;
+    };
     auto issue_next = [&]() {
       const int slot = n_issued % nst;
       const SegRec& sg = segs[ps];
       uint32_t vm = 0;
-      if (pj < 2 * pw.nbf_w) {
+      SlotTag tg;
+      tg.seg = ps;
+      if (pk == 1) {
+        tg.kind = (short)(1 + p_end);
+        tg.a = p_a;
+        tg.rpos = 0;
+        tg.n = 1;
+        tg.first = 0;
         if (lane == 0) {
-          // bf16 tile: its 16 K rows (even stage) or V rows (odd stage), one 256-byte copy per row
+          // bf16 tile: its 16 K rows (first stage) or V rows (second), one 256-byte copy per row
           uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
           const uint32_t bar = smem_addr(&my_bars[slot]);
-          const int x0 = (pw.bf0 + pj / 2) * 16;  // bf16-list index of the first row (sinks, then residual)
+          const int x0 = p_a * 16;  // bf16-list index of the first row (sinks, then residual)
           const int rows = min(16, sg.n_sink + sg.r - x0);
           const long long pair = (long long)sg.b * H + sg.h;
-          const __nv_bfloat16* sink = (pj & 1) ? sink_v : sink_k;
-          const __nv_bfloat16* ring = (pj & 1) ? ring_v : ring_k;
+          const __nv_bfloat16* sink = p_end ? sink_v : sink_k;
+          const __nv_bfloat16* ring = p_end ? ring_v : ring_k;
           mbar_arrive_expect_tx(bar, 256u * rows);
           int slot_r = -1;
           for (int rr = 0; rr < rows; ++rr) {
@@ -718,19 +786,25 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
           }
         }
         vm = 1;
+        ++p_end;
       } else {
-        // quantized tiles: n tiles from (q_rec, q_pos), one contiguous range per record touched
-        const int qs = pj - 2 * pw.nbf_w;
-        const int n = min(tps, pw.nq_w - qs * tps);
-        const bool hdr0 = F::kInt && qs == 0 && q_pos != 0;  // the group's header, copied to slot offset 0
+        // n quantized tiles from (q_rec, q_pos), one contiguous range per record touched
+        const int n = min(tps, p_end - p_a);
+        const bool hdr0 = F::kInt && p_first && q_pos != 0;  // the group's header, copied to slot offset 0
         int l_rec = q_rec, l_pos = q_pos + n - 1;              // the last tile's record and position
         while (l_pos >= L.tpg) {
           l_pos -= L.tpg;
           ++l_rec;
         }
-        if (L.paged && (tb_base < 0 || q_rec < tb_base || l_rec >= tb_base + 32)) {
+        tg.kind = 3;
+        tg.a = p_a;
+        tg.rpos = q_pos;
+        tg.n = (short)n;
+        tg.first = p_first ? 1 : 0;
+        if (L.paged && (tb_seg != ps || tb_base < 0 || q_rec < tb_base || l_rec >= tb_base + 32)) {
           // the block-table entries of 32 records from q_rec, one per lane
           tb_base = q_rec;
+          tb_seg = ps;
           const int x = q_rec + lane;
           my_tbl[lane] = x < L.mbps ? __ldg(&p.C.block_table[(long long)sg.b * L.mbps + x]) : -1;
           __syncwarp();
@@ -786,6 +860,8 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
           }
         }
         // advance the cursor by n tiles
+        p_a += n;
+        p_first = false;
         q_rec = l_rec;
         q_pos = l_pos + 1;
         if (q_pos == L.tpg) {
@@ -793,47 +869,41 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
           ++q_rec;
         }
       }
-      if (lane == 0) slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
+      if (lane == 0) {
+        slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
+        my_tags[slot] = tg;
+      }
       vm = __shfl_sync(kFull, vm, 0);
       if (vm) pending |= 1u << slot;
       ++n_issued;
-      if (++pj == pw.nstage) {
-        pj = 0;
-        ++ps;
-        while (ps < nseg) {
-          pw = warp_part(segs[ps], warp, wbf, tps);
-          if (pw.nstage) break;
-          ++ps;
-        }
-        if (ps < nseg) {
-          q_rec = pw.q0 / L.tpg;
-          q_pos = pw.q0 - q_rec * L.tpg;
-          tb_base = -1;
-        }
-      }
     };
+    auto pump = [&]() {
+      while (alive && n_issued - n_consumed < nst && producer_ready()) issue_next();
+      __syncwarp();
+    };
+
     // the query of the first segment: loads issued before the first copies, stored after them
-    float qpre[8];
+    constexpr int kQPer = (8 * 128 + NT - 1) / NT;
+    float qpre[kQPer];
     {
       const SegRec& s0 = segs[0];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = tid + k * kThreads, hr = i >> 7, c = i & 127;
-        qpre[k] = hr < g ? __bfloat162float(qg[((long long)s0.b * p.Hq + s0.h * g + hr) * 128 + c]) : 0.f;
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = tid + k * NT, hr = i >> 7, c = i & 127;
+        qpre[k] = (i < 8 * 128 && hr < g) ? __bfloat162float(qg[((long long)s0.b * p.Hq + s0.h * g + hr) * 128 + c]) : 0.f;
       }
     }
-    while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
+    pump();
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = tid + k * kThreads, hr = i >> 7, c = i & 127;
-      if (hr <= g) q_s[hr * kQRow + c] = qpre[k];  // row g stays zero
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = tid + k * NT, hr = i >> 7, c = i & 127;
+      if (i < 8 * 128 && hr <= g) q_s[hr * kQRow + c] = qpre[k];  // row g stays zero
     }
     __syncthreads();
 
     // ---- consumer ----
     for (int s = 0; s < nseg; ++s) {
       const SegRec sg = segs[s];
-      const WarpPart wp = warp_part(sg, warp, wbf, tps);
       const int nbf_tok = sg.n_sink + sg.r;
       WarpState<NBQ, NGV> stt;
       state_init(stt);
@@ -851,17 +921,15 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
       }
       float sig_bf[NBQ][2];  // scores of a bf16 tile between its K and V stages
 
-      // hand the consumed slot back to the producer (shared-memory reads and writes of
-      // the slot ordered before the bulk copies that will overwrite it)
-      auto release = [&]() {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        ++n_consumed;
-        while (alive && n_issued - n_consumed < nst && ps < nseg) issue_next();
-      };
-
-      for (int j = 0; j < wp.nstage; ++j) {
+      // this warp's stages of segment s, in the order its producer issued them
+      while (true) {
+        if (n_consumed == n_issued) {
+          pump();
+          if (n_consumed == n_issued) break;  // no work left for this warp in this batch
+        }
         const int slot = n_consumed % nst;
+        const SlotTag tg = my_tags[slot];
+        if (tg.seg != s) break;  // the producer has moved on: segment s is done for this warp
         const uint32_t vmask = (__shfl_sync(kFull, slot_valid, 0) >> (8 * slot)) & 0xFFu;
         if (vmask) {
           bool ok = alive && mbar_wait_bounded(smem_addr(&my_bars[slot]), (phase_bits >> slot) & 1u, kWaitLimitCycles);
@@ -875,10 +943,9 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
           }
         }
         const uint8_t* stg = my_stages + (size_t)slot * p.stage_bytes;
-        if (vmask && alive && j < 2 * wp.nbf_w) {
-          const int bt = wp.bf0 + j / 2;
-          const int rows = min(16, nbf_tok - bt * 16);
-          if ((j & 1) == 0) {
+        if (vmask && alive && tg.kind != 3) {
+          const int rows = min(16, nbf_tok - tg.a * 16);
+          if (tg.kind == 1) {
             // ---- bf16 tile, K rows ----
             bf16_qk<NBQ>(stg, q_s, lane, r, q, g, rows, p.scale_log2, sig_bf);
           } else {
@@ -894,15 +961,13 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
             bf16_pv(stg, lane, pt, stt.inv_S * kPrescale, stt.o);
           }
         } else if (vmask && alive) {
-          // ---- quantized stage: tiles [i0, i0 + n), walked in smem, one softmax step each ----
-          const int qs = j - 2 * wp.nbf_w;
-          const int i0 = wp.q0 + qs * tps;
-          const int n = min(tps, wp.q0 + wp.nq_w - i0);
-          int walk = 0;            // smem offset of the next tile (headers inline)
-          int rpos = i0 % L.tpg;   // position of tile i0 + k in its record
+          // ---- quantized stage: tiles [tg.a, tg.a + n), walked in smem, one softmax step each ----
+          const int n = tg.n;
+          int walk = 0;               // smem offset of the next tile (headers inline)
+          int rpos = tg.rpos;         // position of tile tg.a + k in its record
           for (int k = 0; k < n; ++k) {
-            const int i = i0 + k;
-            const bool hdr = F::kInt && (rpos == 0 || (qs == 0 && k == 0));
+            const int i = tg.a + k;
+            const bool hdr = F::kInt && (rpos == 0 || (tg.first && k == 0));
             const int hoff = walk;
             if (hdr) walk += L.hdr_bytes;
             const uint8_t* tile = stg + walk;
@@ -976,10 +1041,15 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
             }
           }
         }
-        release();
+        // hand the slot back to the producer (shared-memory reads and writes of the slot
+        // ordered before the bulk copies that will overwrite it)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        ++n_consumed;
+        pump();
       }
 
-      // ---- finalise the warp's state (output layout: heads 2q, 2q + 1) ----
+      // ---- finalise the warp's state (output layout: heads 2q, 2q + 1) into its merge record ----
       float lsum[NBQ];
 #pragma unroll
       for (int b = 0; b < NBQ; ++b) {
@@ -1018,51 +1088,25 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
       // o = sum of W * (Value operand) with W = p s kPrescale / S
       const float unit = stt.S / kPrescale;
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          const float z = F::kInt ? zo[e][mb * NGV / 8] : 0.f;
-          stt.o[mb][e] = (stt.o[mb][e] + z) * unit;
-          stt.o[mb][2 + e] = (stt.o[mb][2 + e] + z) * unit;
-        }
-      // ---- fold the warps into one record per head (m, l, o[128]), one warp at a time ----
-      float* rec = reinterpret_cast<float*>(scratch);
-      __syncthreads();  // the previous segment's record has been read
-      for (int w = 0; w < kNW; ++w) {
-        if (warp == w) {
-          float mr[2], lr[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int hh = min(2 * q + e, g - 1);
-            mr[e] = w == 0 ? -INFINITY : rec[hh * kMergeStride];
-            lr[e] = w == 0 ? 0.f : rec[hh * kMergeStride + 1];
+      for (int e = 0; e < 2; ++e) {
+        const int hh = 2 * q + e;
+        if (hh < g) {
+          float* rr = my_rec + hh * kMergeStride;
+          if (r == 0) {
+            rr[0] = mo[e];
+            rr[1] = lo2[e];
           }
-          __syncwarp();
+          const bool empty = mo[e] == -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int hh = 2 * q + e;
-            if (hh < g) {
-              float* rr = rec + hh * kMergeStride;
-              const float M = fmaxf(mr[e], mo[e]);
-              const float ar = mr[e] == -INFINITY ? 0.f : exp2f(mr[e] - M);
-              const float aw = mo[e] == -INFINITY ? 0.f : exp2f(mo[e] - M);
-              if (r == 0) {
-                rr[0] = M;
-                rr[1] = ar * lr[e] + aw * lo2[e];
-              }
-#pragma unroll
-              for (int mb = 0; mb < 8; ++mb) {
-                const int c0 = 4 + 16 * mb + r, c1 = c0 + 8;
-                const float o0 = aw * stt.o[mb][e], o1 = aw * stt.o[mb][2 + e];
-                rr[c0] = w == 0 ? o0 : fmaf(ar, rr[c0], o0);
-                rr[c1] = w == 0 ? o1 : fmaf(ar, rr[c1], o1);
-              }
-            }
+          for (int mb = 0; mb < 8; ++mb) {
+            const float z = F::kInt ? zo[e][mb * NGV / 8] : 0.f;
+            rr[4 + 16 * mb + r] = empty ? 0.f : (stt.o[mb][e] + z) * unit;
+            rr[4 + 16 * mb + r + 8] = empty ? 0.f : (stt.o[mb][2 + e] + z) * unit;
           }
         }
-        __syncthreads();
       }
-      // ---- write the partial of (b, h), or the result when this CTA owns the pair ----
+      __syncthreads();
+      // ---- merge the warps' records; write the partial of (b, h), or the result when this CTA owns the pair ----
       {
         const int b = sg.b, h = sg.h;
         const long long pair = (long long)b * H + h;
@@ -1070,12 +1114,24 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
         const long long P0 = sg.pair_start, P1 = sg.pair_start + sg.units;
         const long long c_lo = ((P0 + 1) * C - 1) / U, c_hi = (P1 * C - 1) / U;
         const bool whole = p.fuse && c_lo == c_hi;  // no other CTA touches this pair
-        for (int i = tid; i < g * 128; i += kThreads) {
+        const int rstride = p.merge_bytes / 4;
+        for (int i = tid; i < g * 128; i += NT) {
           const int hr = i >> 7, c = i & 127;
-          const float* rr = rec + hr * kMergeStride;
-          const float M = rr[0], Lsum = rr[1];
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < NW; ++w) M = fmaxf(M, recs[w * rstride + hr * kMergeStride]);
+          float Lsum = 0.f, O = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+              const float* rw = recs + w * rstride + hr * kMergeStride;
+              const float f = exp2f(rw[0] - M);  // 0 for a warp without tiles (m = -inf)
+              Lsum = fmaf(rw[1], f, Lsum);
+              O = fmaf(rw[4 + c], f, O);
+            }
+          }
           const bool empty = !(Lsum > 0.f);
-          const float o = empty ? 0.f : rr[4 + c] / Lsum;
+          const float o = empty ? 0.f : O / Lsum;
           const float l2 = empty ? -INFINITY : M + log2f(Lsum);
           if (whole) {
             write_out(p, b, h * g + hr, c, o, l2);
@@ -1101,21 +1157,50 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
           if (last_flag) {
             __threadfence();
             const int na = n_act;
-            for (int i = tid; i < g * 128; i += kThreads) {
-              const int hr = i >> 7, c = i & 127;
-              float M = -INFINITY, Lsum = 0.f, O = 0.f;
-              if (na <= kMaxParts) {
-                for (int k2 = 0; k2 < na; ++k2) M = fmaxf(M, __ldcg(&p.ws_lse[((long long)act[k2] + pair) * g + hr]));
-                if (M != -INFINITY) {
+            float* wsc = recs;  // the warps' records are read: reuse the first one for the weights
+            if (na <= kMaxParts) {
+              // every partial's lse at once: row hr, column k
+              for (int i = tid; i < g * na; i += NT) {
+                const int hr = i / na, k2 = i - hr * na;
+                wsc[hr * kMergeStride + k2] = __ldcg(&p.ws_lse[((long long)act[k2] + pair) * g + hr]);
+              }
+              __syncthreads();
+              if (tid < g) {  // per head: the largest lse, the weights 2^(lse - M) and their sum
+                float* wr = wsc + tid * kMergeStride;
+                float M = -INFINITY, Lsum = 0.f;
+                for (int k2 = 0; k2 < na; ++k2) M = fmaxf(M, wr[k2]);
+                if (M != -INFINITY)
                   for (int k2 = 0; k2 < na; ++k2) {
-                    const long long sl = (long long)act[k2] + pair;
-                    const float f = exp2f(__ldcg(&p.ws_lse[sl * g + hr]) - M);
-                    Lsum += f;
-                    O = fmaf(f, __ldcg(&p.ws_o[(sl * g + hr) * 128 + c]), O);
+                    wr[k2] = exp2f(wr[k2] - M);
+                    Lsum += wr[k2];
                   }
-                }
-              } else {
-                // more partials than the list holds (tiny per-CTA ranges): walk [c_lo, c_hi]
+                wr[kMaxParts] = M;
+                wr[kMaxParts + 1] = Lsum;
+              }
+              __syncthreads();
+              for (int i = tid; i < g * 128; i += NT) {
+                const int hr = i >> 7, c = i & 127;
+                const float* wr = wsc + hr * kMergeStride;
+                const float M = wr[kMaxParts], Lsum = wr[kMaxParts + 1];
+                float O = 0.f;
+                if (M != -INFINITY)
+                  for (int k0 = 0; k0 < na; k0 += 8) {  // eight loads in flight, then the sums in order
+                    float v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                      v[j] = k0 + j < na ? __ldcg(&p.ws_o[(((long long)act[k0 + j] + pair) * g + hr) * 128 + c]) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                      if (k0 + j < na) O = fmaf(wr[k0 + j], v[j], O);
+                  }
+                const bool empty = !(Lsum > 0.f);
+                write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+              }
+            } else {
+              // more partials than the list holds (tiny per-CTA ranges): walk [c_lo, c_hi]
+              for (int i = tid; i < g * 128; i += NT) {
+                const int hr = i >> 7, c = i & 127;
+                float M = -INFINITY, Lsum = 0.f, O = 0.f;
                 for (long long cc = c_lo; cc <= c_hi; ++cc)
                   if ((cc * U) / C != ((cc + 1) * U) / C) M = fmaxf(M, __ldcg(&p.ws_lse[(cc + pair) * g + hr]));
                 if (M != -INFINITY) {
@@ -1126,9 +1211,9 @@ __global__ void __launch_bounds__(kThreads, NBQ == 1 ? 4 : 3) decode_kernel(cons
                     O = fmaf(f, __ldcg(&p.ws_o[((cc + pair) * g + hr) * 128 + c]), O);
                   }
                 }
+                const bool empty = !(Lsum > 0.f);
+                write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
               }
-              const bool empty = !(Lsum > 0.f);
-              write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
             }
           }
         }
@@ -1171,10 +1256,10 @@ cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream
   cudaError_t e;
   if (p.g <= 4) {
     if ((e = ensure_smem_attr<FMT, NGV, 1>(smem)) != cudaSuccess) return e;
-    decode_kernel<FMT, NGV, 1><<<p.num_ctas, kThreads, smem, stream>>>(p);
+    decode_kernel<FMT, NGV, 1><<<p.num_ctas, DecodeWarps<FMT, 1>::kThreads, smem, stream>>>(p);
   } else {
     if ((e = ensure_smem_attr<FMT, NGV, 2>(smem)) != cudaSuccess) return e;
-    decode_kernel<FMT, NGV, 2><<<p.num_ctas, kThreads, smem, stream>>>(p);
+    decode_kernel<FMT, NGV, 2><<<p.num_ctas, DecodeWarps<FMT, 2>::kThreads, smem, stream>>>(p);
   }
   return cudaGetLastError();
 }
@@ -1184,10 +1269,12 @@ cudaError_t occupancy_t(int g, int smem, int* n) {
   cudaError_t e;
   if (g <= 4) {
     if ((e = ensure_smem_attr<FMT, NGV, 1>(smem)) != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 1>, kThreads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 1>, DecodeWarps<FMT, 1>::kThreads,
+                                                         smem);
   }
   if ((e = ensure_smem_attr<FMT, NGV, 2>(smem)) != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 2>, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 2>, DecodeWarps<FMT, 2>::kThreads,
+                                                       smem);
 }
 
 }  // namespace kvq

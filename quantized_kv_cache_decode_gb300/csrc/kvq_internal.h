@@ -12,6 +12,13 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGqa = 8;
 constexpr int kMaxBatch = 2048;
 
+// Warps per decode CTA (one CTA per SM): 16 for 2- and 4-bit codes with up to 4
+// query heads per kv head (compute-heavy per byte; 128 registers a thread),
+// else 12 (the kernel's DecodeWarps states the same).
+inline int decode_warps(int fmt, int g) {
+  return (g <= 4 && (fmt == KVQ_FMT_INT2 || fmt == KVQ_FMT_INT4)) ? 16 : 12;
+}
+
 // Validated, derived form of kvq_layer_config.
 struct LayerDesc {
   int H, d, fmt, bits, fp8;
@@ -49,12 +56,13 @@ struct DecodeParams {
   int nst;           // pipeline stages per warp
   int stage_bytes;   // bytes of one stage
   int tps;           // quantized tiles per stage
+  int item_tiles;    // quantized tiles per claimed work item (a multiple of the record size)
   int bf_weight;     // work units charged to a bf16 tile (quantized tiles cost 1)
   float* ws_o;       // [slots][g][d] normalised partial outputs
   float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial
   int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
   uint32_t* status;
-  int merge_bytes;   // bytes of the CTA's merge record in shared memory (g heads)
+  int merge_bytes;   // bytes of one warp's merge record in shared memory (g heads)
   // fused combine: the last CTA to finish a (sequence, kv head) pair merges its partials
   int fuse;
   unsigned* counters;  // [batch * H] arrival counters, zero between calls
