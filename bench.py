@@ -504,6 +504,18 @@ def run_reference(args, w, rank, world):
 # --------------------------------------------------------------------------- #
 
 
+def kernel_sources_sha256() -> str:
+    """Hash of the CUDA sources of the library (decides whether a recorded ncu traffic figure still applies)."""
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "quantized_kv_cache_decode_gb300", "csrc")
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,9 +527,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graphs", action="store_true", help="time direct library calls instead of graph replays")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload (profiling captures; 0: all)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     w = I.WORKLOADS[args.workload]()
+    if args.layers:
+        w.layer_formats = w.layer_formats[:args.layers]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     peaks = {}
@@ -566,11 +582,15 @@ def main():
         per_layer = [sum(attention_bytes(f, int(T), w.num_kv_heads) for T in r["lens_after"]) +
                      len(r["lens_after"]) * w.num_q_heads * 256 for f in w.layer_formats]
         kern_gbs = float(np.mean(per_layer)) / (r["kern_ms"] * 1e-3) / 1e9
+    # DRAM bytes per decode launch from an ncu capture, used only while the kernel sources are
+    # the ones the capture ran (their hash is recorded beside the figure)
     traffic = None
     tpath = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
-            traffic = json.load(f).get("bytes_per_launch")
+            rec = json.load(f)
+        if rec.get("kernel_sources_sha256") == kernel_sources_sha256():
+            traffic = rec.get("bytes_per_launch")
     line = {
         "metric": metric, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 5), "higher_is_better": True, "scaling": "weak",
