@@ -121,11 +121,11 @@ int merge_bytes_of(const LayerDesc& L, int g) {
   return g * 132 * 4;
 }
 
-constexpr int kSegTableBytes = 16 * 48;  // kMaxSeg segment records of 48 bytes (kvq_decode.cuh)
+constexpr int kSegTableBytes = 16 * 80;  // kMaxSeg segment records of 80 bytes (kvq_decode.cuh)
 constexpr int kSlotTagBytes = 20;        // one pipeline slot's tag (kvq_decode.cuh)
 
 int fixed_smem(int batch, int merge_bytes, int nw) {
-  int prefix = ((batch + 1) * 4 + 15) / 16 * 16;
+  int prefix = ((batch + 1) * 4 + 15) / 16 * 16 + (batch * 4 + 15) / 16 * 16;  // unit prefix, token counts
   // per warp: barriers, block-table window, slot tags, merge record; the query rows (g + 1)
   const int g = merge_bytes / (132 * 4);
   const int per_warp = kMaxStages * 8 + 32 * 4 + (kMaxStages * kSlotTagBytes + 15) / 16 * 16 + merge_bytes;

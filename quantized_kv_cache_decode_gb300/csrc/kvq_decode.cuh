@@ -506,27 +506,31 @@ __device__ __forceinline__ int active_ctas(long long c_lo, long long c_hi, long 
 constexpr int kMaxParts = 64;  // partials of one pair merged from a shared-memory list
 static_assert(kMaxParts + 2 <= kMergeStride, "the merge weights live in a merge-record row");
 
-// One (sequence, kv head) pair's share of this CTA's unit range.
-struct SegRec {
-  long long pair_start;  // first unit of the pair in the flat unit list
-  int b, h, ua, ue, units;
-  int n_sink, qn, r, nbf, nq;
-};
-constexpr int kMaxSeg = 16;  // segments per table batch
-
 // Work items of one segment, dealt to the CTA's warps round robin (item t to
 // warp t mod NW: every warp's share is interleaved over the segment, so the
-// warps finish together and each warp's sums run in a fixed order): its
-// bf16 tiles [bl, bl + nbf_items) (a pair's units are its nbf bf16 tiles, wbf
-// units each, then its nq quantized tiles, 1 unit each; a bf16 tile belongs to
-// the range holding its first unit), then its quantized tiles [ql, qh) in items
-// of `it` tiles aligned at multiples of `it` (whole records for the integer
+// warps finish together and each warp's sums run in a fixed order): its bf16
+// tiles [bl, bl + nbf_items) (a pair's units are its nbf bf16 tiles, wbf units
+// each, then its nq quantized tiles, 1 unit each; a bf16 tile belongs to the
+// range holding its first unit), then its quantized tiles [ql, qh) in items of
+// `it` tiles aligned at multiples of `it` (whole records for the integer
 // formats, so an item starts at a record header except at ql).
 struct SegItems {
   int bl, nbf_items, ql, qh, al, nq_items;
 };
 
-__device__ __forceinline__ SegItems seg_items(const SegRec& sg, int wbf, int it) {
+// One (sequence, kv head) pair's share of this CTA's unit range, with its work
+// items and the address of its first record (contiguous store).
+struct SegRec {
+  long long pair_start;  // first unit of the pair in the flat unit list
+  const uint8_t* rec0;   // contiguous store: record 0 of the pair
+  int b, h, ua, ue, units;
+  int n_sink, qn, r, nbf, nq;
+  SegItems it;
+};
+constexpr int kMaxSeg = 16;  // segments per table batch
+
+
+__device__ __forceinline__ SegItems seg_items(const SegRec& sg, int wbf, int it) {  // thread 0, once
   SegItems s;
   const int nbu = sg.nbf * wbf;
   s.bl = min(sg.nbf, (sg.ua + wbf - 1) / wbf);
@@ -548,7 +552,7 @@ struct SlotTag {
   int first;
 };
 static_assert(sizeof(SlotTag) == 20, "the host reserves 20 bytes per slot tag");
-static_assert(sizeof(SegRec) == 48, "the host reserves 48 bytes per segment record");
+static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment record");
 
 template <int FMT, int NGV, int NBQ>
 __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_kernel(const DecodeParams p) {
@@ -579,6 +583,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   SegRec* segs = reinterpret_cast<SegRec*>(smem + off);
   off += kMaxSeg * sizeof(SegRec);
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
+  off += ((size_t)(B + 1) * sizeof(int) + 15) / 16 * 16;
+  int* toks = reinterpret_cast<int*>(smem + off);    // [B]: each sequence's token count (clamped)
   __shared__ int seg_count;
   __shared__ long long batch_end;
 
@@ -595,19 +601,16 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
     if (T > tmax_tok) T = tmax_tok;
     return (int)T;
   };
-  auto seq_units = [&](int b) -> int {
-    const TokenSplit ts = split_tokens(seq_tokens(b), L);
-    const int nbf = (ts.n_sink + ts.r + 15) >> 4;
-    const int nq = (ts.qn + 15) >> 4;
-    return nbf * wbf + nq;
-  };
   {
     const int per = (B + NT - 1) / NT;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int local = 0;
     for (int b = b0; b < b1; ++b) {
+      const int T = seq_tokens(b);
+      toks[b] = T;
       prefix[b] = local;
-      local += seq_units(b) * H;
+      const TokenSplit ts = split_tokens(T, L);
+      local += (((ts.n_sink + ts.r + 15) >> 4) * wbf + ((ts.qn + 15) >> 4)) * H;
     }
     int incl = local;
 #pragma unroll
@@ -659,6 +662,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   uint32_t pending = 0;     // slots with copies in flight
   bool alive = true;
   int n_issued = 0, n_consumed = 0;
+  int p_slot = 0, c_slot = 0;  // the slots of the next copy and of the next stage to consume
   const float s_v8 = F::kFp8 ? __ldg(p.C.v_tscale) : 1.f;
 
   // the g query heads of a pair into q_s (row g zero)
@@ -687,17 +691,21 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         SegRec sg;
         sg.b = lo;
         sg.units = (prefix[lo + 1] - prefix[lo]) / H;
-        sg.h = (int)((pp - prefix[lo]) / sg.units);
+        sg.h = (int)(pp - prefix[lo]) / sg.units;
         sg.pair_start = prefix[lo] + (long long)sg.h * sg.units;
         const long long se = min(en, sg.pair_start + sg.units);
         sg.ua = (int)(pp - sg.pair_start);
         sg.ue = (int)(se - sg.pair_start);
-        const TokenSplit ts = split_tokens(seq_tokens(lo), L);
+        const TokenSplit ts = split_tokens(toks[lo], L);
         sg.n_sink = ts.n_sink;
         sg.qn = ts.qn;
         sg.r = ts.r;
         sg.nbf = (ts.n_sink + ts.r + 15) >> 4;
         sg.nq = (ts.qn + 15) >> 4;
+        sg.it = seg_items(sg, wbf, it);
+        sg.rec0 = L.paged ? nullptr
+                          : reinterpret_cast<const uint8_t*>(p.C.qstore) +
+                                ((long long)sg.b * H + sg.h) * L.nrec * L.rec_bytes;
         segs[ns++] = sg;
         pp = se;
       }
@@ -716,19 +724,13 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
     int tb_base = -1;            // paged: first record of the block-table window in my_tbl (-1: none)
     int tb_seg = -1;             // ... and its segment
     int p_claims = 0;            // items taken from segment ps
-    int psi_seg = -1;            // segment whose items psi holds
-    SegItems psi;
     // the next item with stages left, taken from the segments in order; false when none
     auto producer_ready = [&]() -> bool {
       while (ps < nseg) {
         if (pk == 1 && p_end < 2) return true;
         if (pk == 3 && p_a < p_end) return true;
         const int t = warp + NW * (p_claims++);  // items warp, warp + NW, ... of the segment
-        if (psi_seg != ps) {
-          psi = seg_items(segs[ps], wbf, it);
-          psi_seg = ps;
-        }
-        const SegItems& si = psi;
+        const SegItems si = segs[ps].it;
         if (t < si.nbf_items) {
           pk = 1;
           p_a = si.bl + t;
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       return false;
     };
     auto issue_next = [&]() {
-      const int slot = n_issued % nst;
+      const int slot = p_slot;
       const SegRec& sg = segs[ps];
       uint32_t vm = 0;
       SlotTag tg;
@@ -813,8 +815,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
           const uint32_t bar = smem_addr(&my_bars[slot]);
           if (!L.paged) {
-            const uint8_t* base = reinterpret_cast<const uint8_t*>(p.C.qstore) +
-                                  ((long long)sg.b * H + sg.h) * L.nrec * L.rec_bytes;
+            const uint8_t* base = sg.rec0;
             const uint8_t* rec0 = base + (long long)q_rec * L.rec_bytes;
             const uint8_t* start = (F::kInt && q_pos == 0) ? rec0 : rec0 + L.hdr_bytes + q_pos * L.tile_bytes;
             const uint8_t* end = base + (long long)l_rec * L.rec_bytes + L.hdr_bytes + (l_pos + 1) * L.tile_bytes;
@@ -876,6 +877,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       vm = __shfl_sync(kFull, vm, 0);
       if (vm) pending |= 1u << slot;
       ++n_issued;
+      if (++p_slot == nst) p_slot = 0;
     };
     auto pump = [&]() {
       while (alive && n_issued - n_consumed < nst && producer_ready()) issue_next();
@@ -884,20 +886,21 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
 
     // the query of the first segment: loads issued before the first copies, stored after them
     constexpr int kQPer = (8 * 128 + NT - 1) / NT;
-    float qpre[kQPer];
+    unsigned short qpre[kQPer];  // raw bf16: converted only after the copies are issued
     {
       const SegRec& s0 = segs[0];
+      const unsigned short* qraw = reinterpret_cast<const unsigned short*>(qg);
 #pragma unroll
       for (int k = 0; k < kQPer; ++k) {
         const int i = tid + k * NT, hr = i >> 7, c = i & 127;
-        qpre[k] = (i < 8 * 128 && hr < g) ? __bfloat162float(qg[((long long)s0.b * p.Hq + s0.h * g + hr) * 128 + c]) : 0.f;
+        qpre[k] = (i < 8 * 128 && hr < g) ? qraw[((long long)s0.b * p.Hq + s0.h * g + hr) * 128 + c] : 0;
       }
     }
     pump();
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
       const int i = tid + k * NT, hr = i >> 7, c = i & 127;
-      if (i < 8 * 128 && hr <= g) q_s[hr * kQRow + c] = qpre[k];  // row g stays zero
+      if (i < 8 * 128 && hr <= g) q_s[hr * kQRow + c] = __uint_as_float((unsigned)qpre[k] << 16);  // row g stays zero
     }
     __syncthreads();
 
@@ -927,7 +930,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           pump();
           if (n_consumed == n_issued) break;  // no work left for this warp in this batch
         }
-        const int slot = n_consumed % nst;
+        const int slot = c_slot;
         const SlotTag tg = my_tags[slot];
         if (tg.seg != s) break;  // the producer has moved on: segment s is done for this warp
         const uint32_t vmask = (__shfl_sync(kFull, slot_valid, 0) >> (8 * slot)) & 0xFFu;
@@ -1046,6 +1049,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         ++n_consumed;
+        if (++c_slot == nst) c_slot = 0;
         pump();
       }
 
@@ -1158,7 +1162,35 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
             __threadfence();
             const int na = n_act;
             float* wsc = recs;  // the warps' records are read: reuse the first one for the weights
-            if (na <= kMaxParts) {
+            if (na <= 8) {
+              // few partials: each output loads its head's lse values and its partial outputs in
+              // one round trip, then sums in contributor order
+              for (int i = tid; i < g * 128; i += NT) {
+                const int hr = i >> 7, c = i & 127;
+                float ls[8], v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const long long sl = j < na ? (long long)act[j] + pair : 0;
+                  ls[j] = j < na ? __ldcg(&p.ws_lse[sl * g + hr]) : -INFINITY;
+                  v[j] = j < na ? __ldcg(&p.ws_o[(sl * g + hr) * 128 + c]) : 0.f;
+                }
+                float M = -INFINITY, Lsum = 0.f, O = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (j < na) M = fmaxf(M, ls[j]);
+                if (M != -INFINITY) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (j < na) {
+                      const float f = exp2f(ls[j] - M);
+                      Lsum += f;
+                      O = fmaf(f, v[j], O);
+                    }
+                }
+                const bool empty = !(Lsum > 0.f);
+                write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+              }
+            } else if (na <= kMaxParts) {
               // every partial's lse at once: row hr, column k
               for (int i = tid; i < g * na; i += NT) {
                 const int hr = i / na, k2 = i - hr * na;
