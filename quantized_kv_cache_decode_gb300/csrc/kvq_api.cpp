@@ -126,10 +126,10 @@ constexpr int kSlotTagBytes = 20;        // one pipeline slot's tag (kvq_decode.
 
 int fixed_smem(int batch, int merge_bytes, int nw) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16 + (batch * 4 + 15) / 16 * 16;  // unit prefix, token counts
-  // per warp: barriers, block-table window, slot tags, merge record; the query rows (g + 1)
+  // per warp: barriers, block-table window, slot tags; nw/2 merge records; the query rows (g + 1)
   const int g = merge_bytes / (132 * 4);
-  const int per_warp = kMaxStages * 8 + 32 * 4 + (kMaxStages * kSlotTagBytes + 15) / 16 * 16 + merge_bytes;
-  return nw * per_warp + (g + 1) * 132 * 4 + kSegTableBytes + prefix;
+  const int per_warp = kMaxStages * 8 + 32 * 4 + (kMaxStages * kSlotTagBytes + 15) / 16 * 16;
+  return nw * per_warp + nw / 2 * merge_bytes + (g + 1) * 132 * 4 + kSegTableBytes + prefix;
 }
 
 cudaError_t occupancy_query(const LayerDesc& L, int g, int smem, int* n) {

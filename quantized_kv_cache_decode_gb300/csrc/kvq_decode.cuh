@@ -559,6 +559,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   using F = FT<FMT>;
   constexpr int NW = DecodeWarps<FMT, NBQ>::kNW;
   constexpr int NT = NW * 32;
+  constexpr int NR = NW / 2;  // merge records (warps fold pairwise into them)
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerDesc& L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -578,8 +579,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   off += NW * kMaxStages * sizeof(SlotTag);
   float* q_s = reinterpret_cast<float*>(smem + off);  // [g + 1 rows][kQRow]: the query heads, a zero row
   off += (size_t)(g + 1) * kQRow * sizeof(float);
-  float* recs = reinterpret_cast<float*>(smem + off);  // per warp: merge record [g heads][kMergeStride]
-  off += (size_t)NW * p.merge_bytes;
+  float* recs = reinterpret_cast<float*>(smem + off);  // NW/2 merge records [g heads][kMergeStride]
+  off += (size_t)NR * p.merge_bytes;
   SegRec* segs = reinterpret_cast<SegRec*>(smem + off);
   off += kMaxSeg * sizeof(SegRec);
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
@@ -656,7 +657,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   uint64_t* my_bars = bars + warp * kMaxStages;
   int* my_tbl = tbl + warp * 32;
   SlotTag* my_tags = tags + warp * kMaxStages;
-  float* my_rec = recs + (size_t)warp * (p.merge_bytes / 4);
+  float* my_rec = recs + (size_t)(warp % NR) * (p.merge_bytes / 4);
   uint32_t phase_bits = 0;  // expected parity of each stage barrier of this warp
   uint32_t slot_valid = 0;  // lane 0: 8 bits per slot, the tiles its stage holds
   uint32_t pending = 0;     // slots with copies in flight
@@ -1092,20 +1093,62 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       // o = sum of W * (Value operand) with W = p s kPrescale / S
       const float unit = stt.S / kPrescale;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int hh = 2 * q + e;
-        if (hh < g) {
-          float* rr = my_rec + hh * kMergeStride;
-          if (r == 0) {
-            rr[0] = mo[e];
-            rr[1] = lo2[e];
-          }
-          const bool empty = mo[e] == -INFINITY;
+      for (int e = 0; e < 2; ++e)
 #pragma unroll
-          for (int mb = 0; mb < 8; ++mb) {
-            const float z = F::kInt ? zo[e][mb * NGV / 8] : 0.f;
-            rr[4 + 16 * mb + r] = empty ? 0.f : (stt.o[mb][e] + z) * unit;
-            rr[4 + 16 * mb + r + 8] = empty ? 0.f : (stt.o[mb][2 + e] + z) * unit;
+        for (int mb = 0; mb < 8; ++mb) {
+          const bool empty = mo[e] == -INFINITY;
+          const float z = F::kInt ? zo[e][mb * NGV / 8] : 0.f;
+          stt.o[mb][e] = empty ? 0.f : (stt.o[mb][e] + z) * unit;
+          stt.o[mb][2 + e] = empty ? 0.f : (stt.o[mb][2 + e] + z) * unit;
+        }
+      // ---- fold the warps pairwise into NW/2 merge records: warp w + NW/2 writes record w, then
+      // warp w folds its own state into it ----
+      if (warp >= NR) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hh = 2 * q + e;
+          if (hh < g) {
+            float* rr = my_rec + hh * kMergeStride;
+            if (r == 0) {
+              rr[0] = mo[e];
+              rr[1] = lo2[e];
+            }
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              rr[4 + 16 * mb + r] = stt.o[mb][e];
+              rr[4 + 16 * mb + r + 8] = stt.o[mb][2 + e];
+            }
+          }
+        }
+      }
+      __syncthreads();
+      if (warp < NR) {
+        float mr[2], lr[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hh = min(2 * q + e, g - 1);
+          mr[e] = my_rec[hh * kMergeStride];
+          lr[e] = my_rec[hh * kMergeStride + 1];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hh = 2 * q + e;
+          if (hh < g) {
+            float* rr = my_rec + hh * kMergeStride;
+            const float M = fmaxf(mr[e], mo[e]);
+            const float ar = mr[e] == -INFINITY ? 0.f : exp2f(mr[e] - M);
+            const float aw = mo[e] == -INFINITY ? 0.f : exp2f(mo[e] - M);
+            if (r == 0) {
+              rr[0] = M;
+              rr[1] = ar * lr[e] + aw * lo2[e];
+            }
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              const int c0 = 4 + 16 * mb + r, c1 = c0 + 8;
+              rr[c0] = fmaf(ar, rr[c0], aw * stt.o[mb][e]);
+              rr[c1] = fmaf(ar, rr[c1], aw * stt.o[mb][2 + e]);
+            }
           }
         }
       }
@@ -1123,11 +1166,11 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           const int hr = i >> 7, c = i & 127;
           float M = -INFINITY;
 #pragma unroll
-          for (int w = 0; w < NW; ++w) M = fmaxf(M, recs[w * rstride + hr * kMergeStride]);
+          for (int w = 0; w < NR; ++w) M = fmaxf(M, recs[w * rstride + hr * kMergeStride]);
           float Lsum = 0.f, O = 0.f;
           if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
+            for (int w = 0; w < NR; ++w) {
               const float* rw = recs + w * rstride + hr * kMergeStride;
               const float f = exp2f(rw[0] - M);  // 0 for a warp without tiles (m = -inf)
               Lsum = fmaf(rw[1], f, Lsum);
