@@ -18,7 +18,9 @@ title and section.
 * same page, section 3 "Key=per-channel, Value=per-token": Keys quantized per
   channel (over a group of tokens), Values per token; the most recent tokens
   kept in full precision as a sliding residual window.
-* same page, section 4 "FP8 / INT8": FP8 E4M3 with an fp32 scale.
+* same page, section 4 "FP8 / INT8": the two OCP FP8 formats, E4M3
+  (4 exponent, 3 mantissa bits) and E5M2 (5 exponent, 2 mantissa bits), each
+  with an fp32 scale.
 * same page, section 5 "구현·시스템 고려사항": quantize the new token's K,V
   right after they are computed, store them, dequantize right before attention.
 * same page, closing box "메모리 크기 감각": ``KV_bytes = 2 * L * n_kv_heads *
@@ -29,7 +31,9 @@ title and section.
   formula (about 40 GB in bf16, 20 GB FP8, 10 GB INT4); section
   "오차가 어디서 만나는가": ``softmax(Q K^T / sqrt(d))``; section
   "어떤 레이어가 더 민감한가": the first (sink) token's K/V kept in 16-bit
-  precision, FP8/INT8 on early and late layers and INT4 in the middle.
+  precision, FP8/INT8 on early and late layers and INT4 in the middle;
+  section on the vLLM flags: the ``fp8_e5m2`` KV dtype and "skip layers"
+  whose KV cache is left unquantized.
 
 Readings where the pages leave a step open (each is also listed in the design doc):
 
@@ -42,6 +46,11 @@ Readings where the pages leave a step open (each is also listed in the design doc):
 * FP8 is OCP E4M3FN (largest finite 448), round-to-nearest-even with
   saturation to +-448, the sign of zero kept; the per-tensor scale is
   ``amax / 448`` (``1`` when ``amax == 0``) of the tensor it calibrates;
+* FP8 E5M2 is the OCP E5M2 format (IEEE-style: infinities and NaNs at the top
+  exponent, largest finite 57344), encoded the same way (nearest, ties to the
+  even code, saturating to +-57344) with the scale ``amax / 57344``;
+* a "skip layer" (format ``bf16``) keeps every token's K and V in bf16: no
+  quantized tokens, attention over the stored values;
 * the cache keeps the first S tokens in bf16, quantizes tokens in groups of G
   once R + G tokens are waiting, so at least R recent tokens stay bf16
   (``Q_n = max(0, floor((T - S - R) / G)) * G``); FP8 uses G = 1, R = 0;
@@ -59,6 +68,7 @@ import numpy as np
 F32 = np.float32
 FLT_MIN = np.finfo(np.float32).tiny          # smallest normal fp32
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 # --------------------------------------------------------------------------- #
@@ -133,38 +143,78 @@ def e4m3_decode(codes: np.ndarray) -> np.ndarray:
 _E4M3_POS = e4m3_decode(np.arange(0, 0x7F))   # codes 0x00 .. 0x7E, increasing, 0 .. 448
 
 
-def e4m3_encode(v: np.ndarray) -> np.ndarray:
-    """float32 values -> nearest E4M3FN code, ties to the even code, saturating at +-448.
-
-    The sign bit is the sign of the input (so -0.0 and small negatives give 0x80).
-    """
+def _encode_nearest(v: np.ndarray, pos: np.ndarray) -> np.ndarray:
+    """float32 values -> code of the nearest of the non-negative finite values
+    ``pos`` (indexed by code, increasing), ties to the even code, magnitudes at
+    or beyond the largest value saturating to it; the sign bit is the sign of
+    the input (so -0.0 and small negatives give 0x80)."""
     v = np.asarray(v, dtype=F32).astype(np.float64)
     a = np.abs(v)
-    idx = np.searchsorted(_E4M3_POS, a)                     # first value >= a
-    idx = np.clip(idx, 1, len(_E4M3_POS) - 1)
+    idx = np.searchsorted(pos, a)                            # first value >= a
+    idx = np.clip(idx, 1, len(pos) - 1)
     lo_c = idx - 1
     hi_c = idx
-    d_lo = a - _E4M3_POS[lo_c]
-    d_hi = _E4M3_POS[hi_c] - a
+    d_lo = a - pos[lo_c]
+    d_hi = pos[hi_c] - a
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi_c % 2 == 0))
     mag = np.where(pick_hi, hi_c, lo_c)
-    mag = np.where(a >= E4M3_MAX, 0x7E, mag)                 # saturate (satfinite)
-    mag = np.where(a <= _E4M3_POS[0], 0, mag)
+    mag = np.where(a >= pos[-1], len(pos) - 1, mag)          # saturate (satfinite)
+    mag = np.where(a <= pos[0], 0, mag)
     sign = np.signbit(v).astype(np.int64) << 7
     return (mag | sign).astype(np.uint8)
 
 
-def fp8_tensor_scale(x: np.ndarray) -> np.float32:
-    """Per-tensor fp32 scale amax/448 of a calibration tensor (1 when amax == 0)."""
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """float32 values -> nearest E4M3FN code, ties to the even code, saturating at +-448."""
+    return _encode_nearest(v, _E4M3_POS)
+
+
+# E5M2 (same section; the OCP E5M2 definition): 1 sign bit, 5 exponent bits
+# (bias 15), 2 mantissa bits; exponent field 0 is subnormal (m * 2^-16);
+# exponent field 31 holds +-infinity (m = 0) and NaN; max finite 57344.
+
+
+def e5m2_decode(codes: np.ndarray) -> np.ndarray:
+    """E5M2 code (uint8) -> float64 value (+-inf, NaN for the top exponent)."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 2) & 0x1F
+    m = c & 0x3
+    normal = (1.0 + m / 4.0) * np.power(2.0, e - 15)
+    sub = m * 2.0 ** -16
+    mag = np.where(e == 0, sub, normal)
+    mag = np.where(e == 0x1F, np.where(m == 0, np.inf, np.nan), mag)
+    return sign * mag
+
+
+_E5M2_POS = e5m2_decode(np.arange(0, 0x7C))   # codes 0x00 .. 0x7B, increasing, 0 .. 57344
+
+
+def e5m2_encode(v: np.ndarray) -> np.ndarray:
+    """float32 values -> nearest finite E5M2 code, ties to the even code, saturating at +-57344."""
+    return _encode_nearest(v, _E5M2_POS)
+
+
+FP8_FORMATS = {"fp8_e4m3": (e4m3_encode, e4m3_decode, E4M3_MAX),
+               "fp8_e5m2": (e5m2_encode, e5m2_decode, E5M2_MAX)}
+
+
+def fp8_decode(codes: np.ndarray, fmt: str = "fp8_e4m3") -> np.ndarray:
+    return FP8_FORMATS[fmt][1](codes)
+
+
+def fp8_tensor_scale(x: np.ndarray, fmt: str = "fp8_e4m3") -> np.float32:
+    """Per-tensor fp32 scale amax / (largest finite value of the format) of a
+    calibration tensor (1 when amax == 0): 448 for E4M3, 57344 for E5M2."""
     amax = F32(np.max(np.abs(np.asarray(x, dtype=F32)))) if np.size(x) else F32(0.0)
     if amax == 0:
         return F32(1.0)
-    return F32(amax / F32(E4M3_MAX))
+    return F32(amax / F32(FP8_FORMATS[fmt][2]))
 
 
-def fp8_quantize(x: np.ndarray, s: np.float32) -> np.ndarray:
-    """code = E4M3(fl32(x / s))."""
-    return e4m3_encode((np.asarray(x, dtype=F32) / F32(s)).astype(F32))
+def fp8_quantize(x: np.ndarray, s: np.float32, fmt: str = "fp8_e4m3") -> np.ndarray:
+    """code = FP8(fl32(x / s)) in the given format."""
+    return FP8_FORMATS[fmt][0]((np.asarray(x, dtype=F32) / F32(s)).astype(F32))
 
 
 # --------------------------------------------------------------------------- #
@@ -176,20 +226,25 @@ def fp8_quantize(x: np.ndarray, s: np.float32) -> np.ndarray:
 
 @dataclasses.dataclass(frozen=True)
 class Spec:
-    fmt: str          # "int2" | "int4" | "int8" | "fp8_e4m3"
+    fmt: str          # "int2" | "int4" | "int8" | "fp8_e4m3" | "fp8_e5m2" | "bf16"
     d: int = 128
-    G: int = 32       # Key group (tokens); 1 for FP8
+    G: int = 32       # Key group (tokens); 1 for FP8; unused for bf16
     Gv: int = 128     # Value group (channels)
     R: int = 0        # residual window (bf16)
     S: int = 0        # sink tokens (bf16)
 
     @property
     def bits(self) -> int:
-        return {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8}[self.fmt]
+        return {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8, "fp8_e5m2": 8, "bf16": 16}[self.fmt]
 
     @property
     def is_fp8(self) -> bool:
-        return self.fmt == "fp8_e4m3"
+        return self.fmt in FP8_FORMATS
+
+    @property
+    def is_bf16(self) -> bool:
+        """A skip layer: nothing is quantized, every token stays bf16."""
+        return self.fmt == "bf16"
 
 
 def token_split(T: int, spec: Spec) -> Tuple[int, int, int]:
@@ -198,6 +253,8 @@ def token_split(T: int, spec: Spec) -> Tuple[int, int, int]:
     n = T - n_sink
     if spec.is_fp8:
         return n_sink, n, 0
+    if spec.is_bf16:
+        return n_sink, 0, n
     qn = max(0, (n - spec.R) // spec.G) * spec.G
     return n_sink, qn, n - qn
 
@@ -259,8 +316,11 @@ def build_head_cache(k: np.ndarray, v: np.ndarray, spec: Spec,
     hc = HeadCache(spec, k[:n_sink].copy(), v[:n_sink].copy(), None, None, k[q1:].copy(), v[q1:].copy())
     if spec.is_fp8:
         hc.k_scale, hc.v_scale = F32(k_scale), F32(v_scale)
-        hc.k_codes = fp8_quantize(k[q0:q1], hc.k_scale)
-        hc.v_codes = fp8_quantize(v[q0:q1], hc.v_scale)
+        hc.k_codes = fp8_quantize(k[q0:q1], hc.k_scale, spec.fmt)
+        hc.v_codes = fp8_quantize(v[q0:q1], hc.v_scale, spec.fmt)
+    elif spec.is_bf16:
+        hc.k_codes = np.zeros((0, spec.d), np.uint8)
+        hc.v_codes = np.zeros((0, spec.d), np.uint8)
     else:
         hc.k_codes, hc.k_s, hc.k_z = quantize_key_groups(k[q0:q1], spec)
         hc.v_codes, hc.v_s, hc.v_z = quantize_value_tokens(v[q0:q1], spec)
@@ -274,7 +334,7 @@ def empty_head_cache(spec: Spec, k_scale=None, v_scale=None) -> HeadCache:
                    z.copy(), z.copy())
     if spec.is_fp8:
         hc.k_scale, hc.v_scale = F32(k_scale), F32(v_scale)
-    else:
+    elif not spec.is_bf16:
         hc.k_s = np.zeros((0, d), F32)
         hc.k_z = np.zeros((0, d), F32)
         hc.v_s = np.zeros((0, d // spec.Gv), F32)
@@ -297,12 +357,12 @@ def append_token(hc: HeadCache, k_tok: np.ndarray, v_tok: np.ndarray) -> None:
         hc.sink_v = np.concatenate([hc.sink_v, v_tok])
         return
     if spec.is_fp8:
-        hc.k_codes = np.concatenate([hc.k_codes, fp8_quantize(k_tok, hc.k_scale)])
-        hc.v_codes = np.concatenate([hc.v_codes, fp8_quantize(v_tok, hc.v_scale)])
+        hc.k_codes = np.concatenate([hc.k_codes, fp8_quantize(k_tok, hc.k_scale, spec.fmt)])
+        hc.v_codes = np.concatenate([hc.v_codes, fp8_quantize(v_tok, hc.v_scale, spec.fmt)])
         return
     hc.resid_k = np.concatenate([hc.resid_k, k_tok])
     hc.resid_v = np.concatenate([hc.resid_v, v_tok])
-    if len(hc.resid_k) == spec.R + spec.G:
+    if not spec.is_bf16 and len(hc.resid_k) == spec.R + spec.G:
         kc, ks, kz = quantize_key_groups(hc.resid_k[:spec.G], spec)
         vc, vs, vz = quantize_value_tokens(hc.resid_v[:spec.G], spec)
         hc.k_codes = np.concatenate([hc.k_codes, kc])
@@ -319,8 +379,10 @@ def dequantized_f64(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
     """All T tokens' (k_hat, v_hat) in fp64, in token order [T, d]."""
     spec = hc.spec
     if spec.is_fp8:
-        kq = float(hc.k_scale) * e4m3_decode(hc.k_codes)
-        vq = float(hc.v_scale) * e4m3_decode(hc.v_codes)
+        kq = float(hc.k_scale) * fp8_decode(hc.k_codes, spec.fmt)
+        vq = float(hc.v_scale) * fp8_decode(hc.v_codes, spec.fmt)
+    elif spec.is_bf16:
+        kq = vq = np.zeros((0, spec.d))
     else:
         gk = np.repeat(np.arange(len(hc.k_s)), spec.G)
         kq = affine_dequantize_f64(hc.k_codes, hc.k_s[gk], hc.k_z[gk])
@@ -333,11 +395,13 @@ def dequantized_f64(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
 
 
 def dequantized_f32(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
-    """All T tokens' x_hat as the cache export defines it: fp32 ``s*(q - z)`` or ``s*e4m3(q)``."""
+    """All T tokens' x_hat as the cache export defines it: fp32 ``s*(q - z)`` or ``s*fp8(q)``."""
     spec = hc.spec
     if spec.is_fp8:
-        kq = (hc.k_scale * e4m3_decode(hc.k_codes).astype(F32)).astype(F32)
-        vq = (hc.v_scale * e4m3_decode(hc.v_codes).astype(F32)).astype(F32)
+        kq = (hc.k_scale * fp8_decode(hc.k_codes, spec.fmt).astype(F32)).astype(F32)
+        vq = (hc.v_scale * fp8_decode(hc.v_codes, spec.fmt).astype(F32)).astype(F32)
+    elif spec.is_bf16:
+        kq = vq = np.zeros((0, spec.d), F32)
     else:
         gk = np.repeat(np.arange(len(hc.k_s)), spec.G)
         kq = affine_dequantize_f32(hc.k_codes, hc.k_s[gk], hc.k_z[gk])

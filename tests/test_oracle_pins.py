@@ -216,6 +216,74 @@ def test_fp8_tensor_scale():
 
 
 # --------------------------------------------------------------------------- #
+# FP8 E5M2 (OCP E5M2: the high byte of an IEEE binary16)
+# --------------------------------------------------------------------------- #
+
+
+def _f16_of_e5m2(codes):
+    """Independent decoder: an E5M2 code is the top byte of a binary16 whose low byte is zero."""
+    return (np.asarray(codes, np.uint16) << 8).view(np.float16).astype(np.float64)
+
+
+def test_e5m2_known_values():
+    cases = {0x00: 0.0, 0x01: 2.0 ** -16, 0x03: 3 * 2.0 ** -16, 0x04: 2.0 ** -14, 0x3C: 1.0, 0x3D: 1.25,
+             0x3F: 1.75, 0x40: 2.0, 0x7B: 57344.0, 0x7A: 49152.0, 0xBC: -1.0, 0xFB: -57344.0}
+    for c, v in cases.items():
+        assert O.e5m2_decode(np.array([c]))[0] == v
+    assert O.e5m2_decode(np.array([0x7C]))[0] == np.inf and O.e5m2_decode(np.array([0xFC]))[0] == -np.inf
+    assert np.isnan(O.e5m2_decode(np.array([0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]))).all()
+    assert math.copysign(1.0, O.e5m2_decode(np.array([0x80]))[0]) == -1.0
+
+
+def test_e5m2_decode_matches_binary16_all_codes():
+    codes = np.arange(256)
+    a, b = O.e5m2_decode(codes), _f16_of_e5m2(codes)
+    same = (a == b) | (np.isnan(a) & np.isnan(b))
+    assert same.all()
+    num = ~np.isnan(a)
+    assert np.array_equal(np.signbit(a[num]), np.signbit(b[num]))
+
+
+def test_e5m2_roundtrip_all_finite_codes():
+    codes = np.array([c for c in range(256) if (c & 0x7F) < 0x7C], dtype=np.uint8)
+    vals = O.e5m2_decode(codes).astype(F32)
+    assert np.array_equal(O.e5m2_encode(vals), codes)
+
+
+def test_e5m2_encode_exhaustive_bf16_brute_force():
+    # nearest finite value, ties to the even code, saturate to +-57344, keep the sign of zero;
+    # candidates decoded by the independent binary16 route
+    xs = _bf16_all_finite()
+    table = [(c, float(_f16_of_e5m2(np.array([c]))[0])) for c in range(0x7C)]
+    for scale in (1.0, 0.37, 3.0e-3, 61.0, 1.0e-6):
+        with np.errstate(over="ignore"):
+            v = (xs / F32(scale)).astype(F32)
+        got = O.e5m2_encode(v)
+        a = np.abs(v.astype(np.float64))
+        best_d = np.full(a.shape, np.inf)
+        best_c = np.zeros(a.shape, np.int64)
+        for c, val in table:
+            d = np.abs(a - val)
+            better = (d < best_d) | ((d == best_d) & (c % 2 == 0))
+            best_d = np.where(better, d, best_d)
+            best_c = np.where(better, c, best_c)
+        best_c = np.where(a > 57344.0, 0x7B, best_c)
+        best_c |= np.signbit(v).astype(np.int64) << 7
+        assert np.array_equal(got, best_c.astype(np.uint8)), scale
+
+
+def test_e5m2_tensor_scale():
+    x = np.array([-3.5, 1.0, 2.0], F32)
+    assert O.fp8_tensor_scale(x, "fp8_e5m2") == F32(F32(3.5) / F32(57344))
+    assert O.fp8_tensor_scale(np.zeros(4, F32), "fp8_e5m2") == F32(1.0)
+    s = O.fp8_tensor_scale(x, "fp8_e5m2")
+    assert O.fp8_quantize(x, s, "fp8_e5m2")[0] == 0xFB
+    # E5M2 keeps two mantissa bits: 1 + 1/8 lies halfway between 1 and 1.25 and goes to the even code (1.0)
+    assert O.fp8_quantize(np.array([1.125], F32), F32(1.0), "fp8_e5m2")[0] == 0x3C
+    assert O.fp8_quantize(np.array([1.375], F32), F32(1.0), "fp8_e5m2")[0] == 0x3E
+
+
+# --------------------------------------------------------------------------- #
 # cache state machine
 # --------------------------------------------------------------------------- #
 
@@ -231,6 +299,9 @@ def test_token_split_workloads():
     assert O.token_split(80, sp5) == (1, 0, 79)
     assert O.token_split(81, sp5) == (1, 16, 64)
     assert O.token_split(9, O.Spec("fp8_e4m3", G=1, R=0, S=0)) == (0, 9, 0)
+    assert O.token_split(9, O.Spec("fp8_e5m2", G=1, R=0, S=2)) == (2, 7, 0)
+    # a skip layer never quantizes, however long the sequence
+    assert O.token_split(100000, O.Spec("bf16", G=16, R=0, S=1)) == (1, 0, 99999)
 
 
 def _same_cache(a, b):
@@ -247,14 +318,16 @@ def _same_cache(a, b):
     O.Spec("int2", d=16, G=4, Gv=16, R=8, S=1),
     O.Spec("int8", d=16, G=16, Gv=4, R=0, S=2),
     O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=1),
+    O.Spec("fp8_e5m2", d=16, G=1, Gv=16, R=0, S=0),
+    O.Spec("bf16", d=16, G=16, Gv=16, R=0, S=1),
 ])
 def test_bulk_build_equals_appends(spec):
     rng = np.random.default_rng(7)
     T = 61
     k = rng.standard_normal((T, 16)).astype(F32)
     v = rng.standard_normal((T, 16)).astype(F32)
-    ks = O.fp8_tensor_scale(k) if spec.is_fp8 else None
-    vs = O.fp8_tensor_scale(v) if spec.is_fp8 else None
+    ks = O.fp8_tensor_scale(k, spec.fmt) if spec.is_fp8 else None
+    vs = O.fp8_tensor_scale(v, spec.fmt) if spec.is_fp8 else None
     hc = O.empty_head_cache(spec, ks, vs)
     for t in range(T):
         O.append_token(hc, k[t], v[t])
@@ -262,7 +335,9 @@ def test_bulk_build_equals_appends(spec):
         _same_cache(hc, bulk)
         n_sink, qn, r = O.token_split(t + 1, spec)
         assert (len(hc.sink_k), len(hc.k_codes), len(hc.resid_k)) == (n_sink, qn, r)
-        if not spec.is_fp8:
+        if spec.is_bf16:
+            assert qn == 0 and np.array_equal(hc.resid_k, k[min(t + 1, spec.S):t + 1])
+        elif not spec.is_fp8:
             assert r < spec.R + spec.G
 
 
@@ -289,7 +364,10 @@ def _dequant_brute(hc):
         ks.append(list(map(float, hc.sink_k[t])))
         vs.append(list(map(float, hc.sink_v[t])))
     for t in range(len(hc.k_codes)):
-        if sp.is_fp8:
+        if sp.fmt == "fp8_e5m2":
+            ks.append([float(hc.k_scale) * float(_f16_of_e5m2(np.array([c]))[0]) for c in hc.k_codes[t]])
+            vs.append([float(hc.v_scale) * float(_f16_of_e5m2(np.array([c]))[0]) for c in hc.v_codes[t]])
+        elif sp.is_fp8:
             ks.append([float(hc.k_scale) * float(O.e4m3_decode(np.array([c]))[0]) for c in hc.k_codes[t]])
             vs.append([float(hc.v_scale) * float(O.e4m3_decode(np.array([c]))[0]) for c in hc.v_codes[t]])
         else:
@@ -308,6 +386,8 @@ def _dequant_brute(hc):
     O.Spec("int2", d=16, G=4, Gv=16, R=8, S=0),
     O.Spec("int8", d=16, G=16, Gv=4, R=2, S=0),
     O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=1),
+    O.Spec("fp8_e5m2", d=16, G=1, Gv=16, R=0, S=0),
+    O.Spec("bf16", d=16, G=16, Gv=16, R=0, S=1),
 ])
 def test_attention_brute_force(spec):
     rng = np.random.default_rng(11)
@@ -319,8 +399,8 @@ def test_attention_brute_force(spec):
         for h in range(Hkv):
             k = (rng.standard_normal((T, 16)) * 2).astype(F32)
             v = rng.standard_normal((T, 16)).astype(F32)
-            ks = O.fp8_tensor_scale(k) if spec.is_fp8 else None
-            vs = O.fp8_tensor_scale(v) if spec.is_fp8 else None
+            ks = O.fp8_tensor_scale(k, spec.fmt) if spec.is_fp8 else None
+            vs = O.fp8_tensor_scale(v, spec.fmt) if spec.is_fp8 else None
             row.append(O.build_head_cache(k, v, spec, ks, vs))
         caches.append(row)
     out, lse = O.decode_attention(q, caches)
