@@ -50,21 +50,27 @@ L2_BYTES = 129 * 2 ** 20
 # --------------------------------------------------------------------------- #
 
 
+def is_fp8(fmt):
+    return fmt.fmt in ("fp8_e4m3", "fp8_e5m2")
+
+
 def split_tokens(T, fmt):
     n_sink = min(T, fmt.S)
     n = T - n_sink
-    if fmt.fmt == "fp8_e4m3":
+    if is_fp8(fmt):
         return n_sink, n, 0
+    if fmt.fmt == "bf16":  # skip layer: nothing quantized
+        return n_sink, 0, n
     qn = max(0, (n - fmt.R) // fmt.G) * fmt.G
     return n_sink, qn, n - qn
 
 
 def attention_bytes(fmt, T, H, d=128):
     """Bytes one (sequence, kv head) must read for attention over T tokens."""
-    bits = 8 if fmt.fmt == "fp8_e4m3" else I.FORMAT_BITS[fmt.fmt]
+    bits = I.FORMAT_BITS[fmt.fmt]
     n_sink, qn, r = split_tokens(T, fmt)
     b = 2 * qn * d * bits // 8
-    if fmt.fmt != "fp8_e4m3":
+    if not is_fp8(fmt) and qn:
         b += (qn // fmt.G) * d * 8 + qn * (d // fmt.Gv) * 8
     b += (n_sink + r) * d * 2 * 2
     return b * H
@@ -72,9 +78,9 @@ def attention_bytes(fmt, T, H, d=128):
 
 def append_bytes(fmt, T_before, n, H, d=128):
     """Bytes moved by appending n tokens to one sequence (all heads)."""
-    bits = 8 if fmt.fmt == "fp8_e4m3" else I.FORMAT_BITS[fmt.fmt]
+    bits = I.FORMAT_BITS[fmt.fmt]
     b = 2 * n * d * 2  # read new K, V
-    if fmt.fmt == "fp8_e4m3":
+    if is_fp8(fmt):
         return H * (b + 2 * n * d)
     _, q0, _ = split_tokens(T_before, fmt)
     n_sink1, q1, r1 = split_tokens(T_before + n, fmt)
@@ -190,10 +196,13 @@ class Layer:
         B, H, Hq = len(lens_before), w.num_kv_heads, w.num_q_heads
         self.B, self.H, self.Hq, self.fmt = B, H, Hq, fmt
         lens_after = [int(t) + n_app for t in lens_before]
-        fp8 = fmt.fmt == "fp8_e4m3"
+        fp8 = is_fp8(fmt)
         G = 1 if fp8 else fmt.G
         qmax = [split_tokens(t, fmt)[1] for t in lens_after]
-        if w.paged:
+        if fmt.fmt == "bf16":
+            rows = max([1] + [t - min(t, fmt.S) for t in lens_after])
+            self.cfg = kvq.make_config("bf16", H, 0, 0, 0, fmt.S, capacity_tokens=rows)
+        elif w.paged:
             P = w.block_tokens
             nblk = [math.ceil(q / P) for q in qmax]
             mbps = max(nblk + [1])
@@ -221,7 +230,7 @@ class Layer:
         uniform = len(set(lens_after)) == 1
         if uniform:
             k, v = I.device_kv_bf16(w, l, Tmax, dev, batch=B, seed_offset=seed_offset)
-            self._calibrate(fp8, k, v)
+            self._calibrate(fp8, fmt.fmt, k, v)
             Tb = lens_before[0]
             if Tb > 0:
                 zero = torch.zeros(B, dtype=torch.int32, device=dev)
@@ -253,10 +262,10 @@ class Layer:
         self.struct = self.cache.struct()
         self.scale = 1.0 / math.sqrt(128)
 
-    def _calibrate(self, fp8, k, v):
+    def _calibrate(self, fp8, name, k, v):
         if fp8:
-            self.kvq.fp8_calibrate(k, k.numel(), self.cache.k_tensor_scale)
-            self.kvq.fp8_calibrate(v, v.numel(), self.cache.v_tensor_scale)
+            self.kvq.fp8_calibrate(k, k.numel(), self.cache.k_tensor_scale, fmt=name)
+            self.kvq.fp8_calibrate(v, v.numel(), self.cache.v_tensor_scale, fmt=name)
 
     def append(self, stream=None):
         self.kvq.quantize_append(self.cfg, self.struct, self.k_new, self.v_new, self.n_app, self.lens_before,
@@ -423,8 +432,8 @@ def oracle_items(w):
     fmt = w.layer_formats[0]
     lens_after = I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
     n_app = max(1, w.append_tokens)
-    spec = O.Spec(fmt.fmt, d=128, G=1 if fmt.fmt == "fp8_e4m3" else fmt.G, Gv=fmt.Gv,
-                  R=0 if fmt.fmt == "fp8_e4m3" else fmt.R, S=fmt.S)
+    spec = O.Spec(fmt.fmt, d=128, G=1 if is_fp8(fmt) else fmt.G, Gv=fmt.Gv,
+                  R=0 if is_fp8(fmt) else fmt.R, S=fmt.S)
     q = O.bf16_to_f32(I.q_bf16(w, 0))
 
     def gen():
@@ -433,8 +442,8 @@ def oracle_items(w):
                 T = int(lens_after[b])
                 k, v = I.kv_bf16(w, 0, b, h, T)
                 kf, vf = O.bf16_to_f32(k), O.bf16_to_f32(v)
-                ks = O.fp8_tensor_scale(kf) if spec.is_fp8 else None
-                vs = O.fp8_tensor_scale(vf) if spec.is_fp8 else None
+                ks = O.fp8_tensor_scale(kf, spec.fmt) if spec.is_fp8 else None
+                vs = O.fp8_tensor_scale(vf, spec.fmt) if spec.is_fp8 else None
                 hc = O.build_head_cache(kf[:T - n_app], vf[:T - n_app], spec, ks, vs)
                 yield (b, h, T, hc, kf[T - n_app:], vf[T - n_app:], q[b, h * w.gqa:(h + 1) * w.gqa])
 

@@ -3,21 +3,23 @@
  *
  * The library implements attention decode over a KV cache stored with
  * asymmetric affine quantization (Keys per channel over groups of tokens,
- * Values per token over groups of channels) at 2, 4 or 8 bits, or as FP8 E4M3
- * with a per-tensor fp32 scale; a bf16 residual window of recent tokens and
- * bf16 attention-sink tokens; per-layer formats; contiguous or paged storage.
+ * Values per token over groups of channels) at 2, 4 or 8 bits, or as FP8 (E4M3
+ * or E5M2) with a per-tensor fp32 scale; a bf16 residual window of recent
+ * tokens and bf16 attention-sink tokens; per-layer formats, including bf16
+ * "skip" layers left unquantized; contiguous or paged storage.
  *
  * Sources (web pages; cited by title and section):
  *   [KVQA] "KV Cache Quantization Analysis" (ryotta.opik.net, KV 캐시 양자화 심층 분석)
  *          s2 "양자화 기초 / 핵심 개념"       q = round(x/s + z), x_hat = s(q - z); asymmetric z
  *          s3 "Key=per-channel, Value=per-token" Key per channel, Value per token, residual window
- *          s4 "FP8 / INT8"                    E4M3 with an fp32 scale; INT8 needs scale storage
+ *          s4 "FP8 / INT8"                    E4M3 and E5M2 with an fp32 scale; INT8 needs scale storage
  *          s5 "구현·시스템 고려사항"          quantize the new K,V at write; dequantize right before
  *                                             attention, fused with the matmul; paging is orthogonal
  *          box "메모리 크기 감각"             KV bytes = 2 L H_kv d T B bytes
  *   [W4KV] "W4A16 + KV cache quantization combined accuracy" (hrletsgo.me)
  *          "오차가 어디서 만나는가"           softmax(Q K^T / sqrt(d))
  *          "어떤 레이어가 더 민감한가"        sink token K/V kept 16-bit; FP8/INT8 early/late, INT4 middle
+ *          vLLM flags section                 fp8_e5m2 KV dtype; layers skipped from KV quantization
  *   [AIQK] "양자화와 KV 캐시" (ai-trend.me)    PagedAttention: fixed-size blocks and a per-request table
  *
  * Conventions for every entry point
@@ -42,7 +44,9 @@
  * R residual tokens, K group G):  the first min(T, S) tokens are the sink (bf16);
  * Q_n = max(0, floor((T - S - R) / G)) * G tokens are quantized; the last
  * r = T - S - Q_n tokens are the residual window (bf16).  FP8 layers use G = 1
- * and R = 0 (every token after the sink is quantized at once).
+ * and R = 0 (every token after the sink is quantized at once).  bf16 layers
+ * quantize nothing: Q_n = 0 and every token after the sink is a "residual"
+ * token, so the window holds the whole sequence.
  */
 #ifndef KVQ_H_
 #define KVQ_H_
@@ -63,10 +67,12 @@ typedef enum {
 } kvq_status;
 
 typedef enum {
-  KVQ_FMT_INT2 = 2,     /* 2-bit affine codes, fp32 scale + fp32 zero-point per group */
-  KVQ_FMT_INT4 = 4,     /* 4-bit affine codes */
-  KVQ_FMT_INT8 = 8,     /* 8-bit affine codes */
-  KVQ_FMT_FP8_E4M3 = 16 /* OCP E4M3FN codes, one fp32 scale per tensor (K and V each) */
+  KVQ_FMT_BF16 = 1,      /* no quantization ("skip layer"): every token kept in bf16 */
+  KVQ_FMT_INT2 = 2,      /* 2-bit affine codes, fp32 scale + fp32 zero-point per group */
+  KVQ_FMT_INT4 = 4,      /* 4-bit affine codes */
+  KVQ_FMT_INT8 = 8,      /* 8-bit affine codes */
+  KVQ_FMT_FP8_E4M3 = 16, /* OCP E4M3FN codes, one fp32 scale per tensor (K and V each) */
+  KVQ_FMT_FP8_E5M2 = 17  /* OCP E5M2 codes, one fp32 scale per tensor (K and V each) */
 } kvq_format;
 
 /* bits OR-ed into *dev_status */
@@ -79,13 +85,16 @@ typedef struct {
   int32_t num_kv_heads;       /* H_kv >= 1 */
   int32_t head_dim;           /* d, must be 128 */
   int32_t format;             /* kvq_format */
-  int32_t k_group_tokens;     /* G: tokens per Key group (per-channel scale); multiple of 16; 1 for FP8 */
-  int32_t v_group_dims;       /* Gv: channels per Value group (per-token scale); 16,32,64,128; FP8: 128 */
-  int32_t residual_tokens;    /* R >= 0 bf16 recent tokens kept (0 for FP8) */
+  int32_t k_group_tokens;     /* G: tokens per Key group (per-channel scale); multiple of 16; 1 for FP8;
+                                 ignored for bf16 */
+  int32_t v_group_dims;       /* Gv: channels per Value group (per-token scale); 16,32,64,128; FP8: 128;
+                                 ignored for bf16 */
+  int32_t residual_tokens;    /* R >= 0 bf16 recent tokens kept (0 for FP8; ignored for bf16) */
   int32_t sink_tokens;        /* S >= 0 bf16 first tokens kept */
-  int32_t paged;              /* 0: contiguous store, 1: paged store */
+  int32_t paged;              /* 0: contiguous store, 1: paged store (not for bf16) */
   int32_t block_tokens;       /* paged: tokens per block P (INT: P == G; FP8: multiple of 16) */
-  int32_t capacity_tokens;    /* contiguous: quantized tokens per (seq, head); multiple of 16 and of G */
+  int32_t capacity_tokens;    /* contiguous: quantized tokens per (seq, head); multiple of 16 and of G.
+                                 bf16: tokens after the sink per (seq, head), >= 1 */
   int32_t num_blocks;         /* paged: blocks in the pool */
   int32_t max_blocks_per_seq; /* paged: row length of the block table */
 } kvq_layer_config;
@@ -117,8 +126,12 @@ typedef struct {
  * bf16 parts (both stores):
  *   resid_k, resid_v  bf16 [B][H][W][d]  residual token t in slot (t - S) mod W
  *   sink_k,  sink_v   bf16 [B][H][S][d]
- * FP8: k_tensor_scale, v_tensor_scale point to one device float each (amax/448,
- * see kvq_fp8_calibrate); they stay fixed for later appends.
+ * FP8: k_tensor_scale, v_tensor_scale point to one device float each (amax/448
+ * for E4M3, amax/57344 for E5M2, see kvq_fp8_calibrate_format); they stay
+ * fixed for later appends.
+ * bf16 layers: no quantized store (qstore, block_pool unused); resid_k and
+ * resid_v are bf16 [B][H][W][d] with W = capacity_tokens, token t >= S in row
+ * t - S (the ring never wraps: a sequence holds at most S + W tokens).
  *
  * Fragment order.  The K codes and the V codes of a tile are each a 16 x 128
  * code matrix stored as the register file of a tensor-core A operand
@@ -132,7 +145,7 @@ typedef struct {
  *   INT4: word s,               bit 4 reg + 16 h
  *   INT2: word s/2,             bit 8(s mod 2) + 2 reg + 16 h
  *   INT8: word 2s + reg/2,      bit 8((reg mod 2) + 2h)
- *   FP8:  word 2s + reg/2,      bit 8(2(reg mod 2) + h)
+ *   FP8:  word 2s + reg/2,      bit 8(2(reg mod 2) + h)     (E4M3 and E5M2)
  * so that every lane of a decode warp fetches its words with conflict-free
  * 16-byte loads and unpacks them in registers.
  */
@@ -177,6 +190,14 @@ kvq_status kvq_cache_layout(const kvq_layer_config* cfg, int32_t num_seqs, size_
 kvq_status kvq_fp8_calibrate(const void* x, size_t n, float* scale_out, void* stream);
 
 /*
+ * kvq_fp8_calibrate_format -- the same for a given FP8 format: s = amax/448
+ * (KVQ_FMT_FP8_E4M3) or amax/57344 (KVQ_FMT_FP8_E5M2; 57344 is the largest
+ * finite OCP E5M2 value).  Source: [KVQA] s4 (both formats take an fp32
+ * scale).  Any other format returns KVQ_ERR_INVALID_ARG.
+ */
+kvq_status kvq_fp8_calibrate_format(const void* x, size_t n, int32_t format, float* scale_out, void* stream);
+
+/*
  * kvq_quantize_append -- write `n_new` new tokens per (sequence, kv head).
  * Source: [KVQA] s5 (quantize the new K,V right after they are computed and
  * store them), s2 (affine formula), s3 (Key per channel over G tokens, Value
@@ -188,8 +209,10 @@ kvq_status kvq_fp8_calibrate(const void* x, size_t n, float* scale_out, void* st
  * ring reaches R + G tokens its oldest G are quantized as one Key group (per
  * channel: s = (max - min)/(2^b - 1), z = -(min/s), q = clamp(rne(x/s + z))
  * in IEEE fp32, s = 1 for a constant group) and G Value tokens (per token and
- * Gv-channel group, same formula).  FP8: code = E4M3 RNE satfinite of
- * fp32(x / s_tensor).  Result identical to n_new single-token appends.
+ * Gv-channel group, same formula).  FP8: code = E4M3 (or E5M2) RNE satfinite
+ * of fp32(x / s_tensor).  bf16 layers: the token is copied to row t - S of the
+ * residual buffers, never quantized.  Result identical to n_new single-token
+ * appends.
  * The caller advances seq_lens by n_new afterwards, and for a paged store has
  * the blocks of every group that spills already in the block table.
  * Device errors: KVQ_DEV_CAPACITY (store full: nothing written for that
@@ -287,7 +310,8 @@ kvq_status kvq_decode_attention_static_scratch(const kvq_layer_config* cfg, cons
  * Source: [KVQA] s2 (x_hat = s(q - z)), s4 (FP8 value times its scale).
  *   k_out, v_out  device f32 [batch][H][max_tokens][d]; token t < seq_lens[b]
  *   gets x_hat (sink / residual: the bf16 value; INT: s*(q - z) as two fp32
- *   operations; FP8: s * E4M3 value in fp32), tokens t >= seq_lens[b] get 0.
+ *   operations; FP8: s * E4M3 / E5M2 value in fp32), tokens t >= seq_lens[b]
+ *   get 0.
  *   seq_lens      device int32 [batch]; a length above max_tokens is an error
  *   (KVQ_DEV_CAPACITY) and is clamped.
  */

@@ -23,16 +23,34 @@ kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
   if (cfg->num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;
   if (cfg->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
   const int f = cfg->format;
-  if (f != KVQ_FMT_INT2 && f != KVQ_FMT_INT4 && f != KVQ_FMT_INT8 && f != KVQ_FMT_FP8_E4M3)
+  if (f != KVQ_FMT_BF16 && f != KVQ_FMT_INT2 && f != KVQ_FMT_INT4 && f != KVQ_FMT_INT8 && f != KVQ_FMT_FP8_E4M3 &&
+      f != KVQ_FMT_FP8_E5M2)
     return KVQ_ERR_INVALID_ARG;
   L->H = cfg->num_kv_heads;
   L->d = kHeadDim;
   L->fmt = f;
-  L->fp8 = (f == KVQ_FMT_FP8_E4M3);
-  L->bits = L->fp8 ? 8 : f;
+  L->fp8 = (f == KVQ_FMT_FP8_E4M3 || f == KVQ_FMT_FP8_E5M2);
+  L->e5m2 = (f == KVQ_FMT_FP8_E5M2);
+  L->bf16 = (f == KVQ_FMT_BF16);
+  L->bits = (L->fp8 || L->bf16) ? 8 : f;  // bf16: nominal, no codes are stored
   L->rb = L->d * L->bits / 8;
   L->S = cfg->sink_tokens;
   if (L->S < 0) return KVQ_ERR_INVALID_ARG;
+  if (L->bf16) {
+    // every token after the sink lives in the bf16 buffers, row t - S; nothing is quantized
+    if (cfg->paged) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->capacity_tokens < 1) return KVQ_ERR_INVALID_ARG;
+    L->G = 16;
+    L->Gv = kHeadDim;
+    L->R = cfg->capacity_tokens;
+    L->W = cfg->capacity_tokens;
+    L->ngv = 1;
+    L->tile_bytes = 32 * L->rb + 128;
+    L->hdr_bytes = 2 * L->d * 4;
+    L->tpg = 1;
+    L->rec_bytes = L->hdr_bytes + L->tile_bytes;
+    return KVQ_OK;  // cap = nrec = 0: no quantized store
+  }
   if (L->fp8) {
     if (cfg->k_group_tokens != 1 || cfg->residual_tokens != 0) return KVQ_ERR_INVALID_ARG;
     L->G = 1;
@@ -133,10 +151,11 @@ int fixed_smem(int batch, int merge_bytes, int nw) {
 }
 
 cudaError_t occupancy_query(const LayerDesc& L, int g, int smem, int* n) {
-  switch (L.fmt) {
+  switch (kernel_format(L.fmt)) {
     case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, g, smem, n);
     case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, g, smem, n);
     case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, g, smem, n);
+    case KVQ_FMT_FP8_E5M2: return occupancy_decode_fp8_e5m2(L.ngv, g, smem, n);
     default: return occupancy_decode_fp8(L.ngv, g, smem, n);
   }
 }
@@ -182,7 +201,7 @@ struct DecodeGeom {
 // that fits the shared memory.
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) {
   const int wsc = merge_bytes_of(L, g);
-  const int nw = decode_warps(L.fmt, g);
+  const int nw = decode_warps(kernel_format(L.fmt), g);
   const int fixed = fixed_smem(batch, wsc, nw);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -249,11 +268,22 @@ kvq_status kvq_cache_layout(const kvq_layer_config* cfg, int32_t num_seqs, size_
   return KVQ_OK;
 }
 
-kvq_status kvq_fp8_calibrate(const void* x, size_t n, float* scale_out, void* stream) {
+kvq_status kvq_fp8_calibrate_format(const void* x, size_t n, int32_t format, float* scale_out, void* stream) {
   if (!scale_out || (n > 0 && !x)) return KVQ_ERR_INVALID_ARG;
-  if (launch_fp8_calibrate(x, n, scale_out, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  float fmax;
+  if (format == KVQ_FMT_FP8_E4M3)
+    fmax = 448.0f;  // largest finite E4M3FN value
+  else if (format == KVQ_FMT_FP8_E5M2)
+    fmax = 57344.0f;  // largest finite E5M2 value
+  else
+    return KVQ_ERR_INVALID_ARG;
+  if (launch_fp8_calibrate(x, n, fmax, scale_out, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+kvq_status kvq_fp8_calibrate(const void* x, size_t n, float* scale_out, void* stream) {
+  return kvq_fp8_calibrate_format(x, n, KVQ_FMT_FP8_E4M3, scale_out, stream);
 }
 
 kvq_status kvq_quantize_append(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* k_new,
@@ -351,10 +381,11 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.out_bf16 = out_bf16;
   p.lse = lse;
   cudaError_t e;
-  switch (L.fmt) {
+  switch (kernel_format(L.fmt)) {
     case KVQ_FMT_INT2: e = launch_decode_int2(p, G.smem, s); break;
     case KVQ_FMT_INT4: e = launch_decode_int4(p, G.smem, s); break;
     case KVQ_FMT_INT8: e = launch_decode_int8(p, G.smem, s); break;
+    case KVQ_FMT_FP8_E5M2: e = launch_decode_fp8_e5m2(p, G.smem, s); break;
     default: e = launch_decode_fp8(p, G.smem, s); break;
   }
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

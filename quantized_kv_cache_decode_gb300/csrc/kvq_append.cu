@@ -24,6 +24,11 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(x));
   return (uint8_t)(v & 0xFFu);
 }
+__device__ __forceinline__ uint8_t f32_to_e5m2(float x) {
+  uint16_t v;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(x));
+  return (uint8_t)(v & 0xFFu);
+}
 
 // s, z of one group from its min and max; returns s (z by reference)
 __device__ __forceinline__ float affine_params(float mn, float mx, float levels, float& z) {
@@ -88,10 +93,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
       const float kx = __bfloat162float(knew[(t - T0) * L.d + c]);
       const float vx = __bfloat162float(vnew[(t - T0) * L.d + c]);
       int byte, bit;
+      const float kd = __fdiv_rn(kx, sk), vd = __fdiv_rn(vx, sv);
       ktile_pos(8, true, tt, c, byte, bit);
-      tile[byte] = f32_to_e4m3(__fdiv_rn(kx, sk));
+      tile[byte] = L.e5m2 ? f32_to_e5m2(kd) : f32_to_e4m3(kd);
       vtile_pos(8, true, tt, c, byte, bit);
-      tile[16 * L.rb + byte] = f32_to_e4m3(__fdiv_rn(vx, sv));
+      tile[16 * L.rb + byte] = L.e5m2 ? f32_to_e5m2(vd) : f32_to_e4m3(vd);
     }
   } else {
     const int G = L.G, levels = (1 << L.bits) - 1;
@@ -200,7 +206,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int blocks = p.batch * p.L.H;
   if (blocks == 0 || p.n_new == 0) return cudaSuccess;
   size_t smem = 0;
-  if (!p.L.fp8) smem = (size_t)p.L.G * 128 * (4 + 4 + 1 + 1) + 2 * 16 * (size_t)p.L.rb;
+  if (!p.L.fp8 && !p.L.bf16) smem = (size_t)p.L.G * 128 * (4 + 4 + 1 + 1) + 2 * 16 * (size_t)p.L.rb;
   {
     // the limit is a per-device attribute that persists: raise it once per size
     static std::mutex mu;
@@ -230,12 +236,12 @@ __global__ void absmax_kernel(const __nv_bfloat16* __restrict__ x, size_t n, uns
   if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));  // m >= 0: bits order like values
 }
 
-__global__ void scale_from_absmax_kernel(float* scale) {
+__global__ void scale_from_absmax_kernel(float* scale, float fmax) {
   const float amax = __uint_as_float(*reinterpret_cast<unsigned int*>(scale));
-  *scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  *scale = amax > 0.f ? __fdiv_rn(amax, fmax) : 1.0f;
 }
 
-cudaError_t launch_fp8_calibrate(const void* x, size_t n, float* scale_out, cudaStream_t stream) {
+cudaError_t launch_fp8_calibrate(const void* x, size_t n, float fmax, float* scale_out, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(scale_out, 0, sizeof(float), stream);
   if (e != cudaSuccess) return e;
   if (n > 0) {
@@ -246,7 +252,7 @@ cudaError_t launch_fp8_calibrate(const void* x, size_t n, float* scale_out, cuda
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  scale_from_absmax_kernel<<<1, 1, 0, stream>>>(scale_out);
+  scale_from_absmax_kernel<<<1, 1, 0, stream>>>(scale_out, fmax);
   return cudaGetLastError();
 }
 

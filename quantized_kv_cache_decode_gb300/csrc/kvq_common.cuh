@@ -47,6 +47,14 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
       : "r"(w));
 }
 
+// Four E5M2 bytes -> two f16x2 (bytes 0,1 -> lo; bytes 2,3 -> hi), exact: an
+// E5M2 code is the high byte of the binary16 with the same value (both have a
+// 5-bit exponent of bias 15), so each byte only moves to the top of its half.
+__device__ __forceinline__ void e5m2x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("prmt.b32 %0, %1, 0, 0x1404;" : "=r"(lo) : "r"(w));
+  asm("prmt.b32 %0, %1, 0, 0x3424;" : "=r"(hi) : "r"(w));
+}
+
 // f32 pair -> packed f16 (lo in the low half), round to nearest even
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   uint32_t d;
@@ -177,6 +185,9 @@ __host__ __device__ __forceinline__ TokenSplit split_tokens(int T, const LayerDe
   if (L.fp8) {
     s.qn = n;
     s.r = 0;
+  } else if (L.bf16) {
+    s.qn = 0;
+    s.r = n;
   } else {
     int k = (n - L.R) >= 0 ? (n - L.R) / L.G : 0;
     s.qn = k * L.G;
@@ -189,6 +200,7 @@ __host__ __device__ __forceinline__ TokenSplit split_tokens(int T, const LayerDe
 __host__ __device__ __forceinline__ long long max_tokens(const LayerDesc& L) {
   long long qcap = L.paged ? (long long)L.mbps * L.P : (long long)L.cap;
   if (L.fp8) return L.S + qcap;
+  if (L.bf16) return (long long)L.S + L.W;
   return L.S + qcap + L.R + L.G - 1;
 }
 

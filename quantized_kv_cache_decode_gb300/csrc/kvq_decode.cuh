@@ -80,7 +80,7 @@ constexpr uint32_t kMagic = 0x64006400u;  // f16 1024.0 in both halves: (1024 | 
 
 template <int FMT>
 struct FT {
-  static constexpr bool kFp8 = FMT == 16;
+  static constexpr bool kFp8 = FMT == 16 || FMT == 17;  // E4M3, E5M2
   static constexpr bool kInt = !kFp8;
   static constexpr int kBits = kFp8 ? 8 : FMT;
   static constexpr int kRB = 128 * kBits / 8;   // bytes of one token row of codes
@@ -144,6 +144,9 @@ __device__ __forceinline__ void unpack_a(const uint32_t (&W)[N], int s, uint32_t
     a1 = int8_lo(W[2 * s] >> 8);
     a2 = int8_lo(W[2 * s + 1]);
     a3 = int8_lo(W[2 * s + 1] >> 8);
+  } else if constexpr (FMT == 17) {  // FP8 E5M2
+    e5m2x4_to_f16x4(W[2 * s], a0, a1);
+    e5m2x4_to_f16x4(W[2 * s + 1], a2, a3);
   } else {  // FP8 E4M3
     e4m3x4_to_f16x4(W[2 * s], a0, a1);
     e4m3x4_to_f16x4(W[2 * s + 1], a2, a3);

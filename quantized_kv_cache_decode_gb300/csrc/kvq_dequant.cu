@@ -2,8 +2,9 @@
 //
 // "KV Cache Quantization Analysis", section 2: x_hat = s (q - z); section 4:
 // an FP8 value times its fp32 scale.  Evaluated as two IEEE fp32 operations
-// (q - z, then times s), or one (s times the exact E4M3 value), so the result
-// is reproducible bit for bit.  Sink and residual tokens are their bf16 values.
+// (q - z, then times s), or one (s times the exact E4M3 / E5M2 value), so the
+// result is reproducible bit for bit.  Sink and residual tokens (every token of
+// a bf16 layer) are their bf16 values.
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -12,6 +13,8 @@ __device__ __forceinline__ float e4m3_value(uint8_t c) {
   const uint32_t h = e4m3x2_to_f16x2((uint32_t)c);
   return unpack_f16(h).x;
 }
+// an E5M2 code is the high byte of the binary16 of the same value
+__device__ __forceinline__ float e5m2_value(uint8_t c) { return unpack_f16((uint32_t)c << 8).x; }
 
 // grid: (batch * H, ceil(max_tokens / 16)); block: 128 threads (one channel each)
 __global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
@@ -50,8 +53,9 @@ __global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
         ktile_pos(L.bits, L.fp8 != 0, row, c, kbyte, kbit);
         vtile_pos(L.bits, L.fp8 != 0, row, c, byte, bit);
         if (L.fp8) {
-          kx = __fmul_rn(*p.C.k_tscale, e4m3_value(tile[kbyte]));
-          vx = __fmul_rn(*p.C.v_tscale, e4m3_value(tile[16 * L.rb + byte]));
+          const uint8_t kc = tile[kbyte], vc = tile[16 * L.rb + byte];
+          kx = __fmul_rn(*p.C.k_tscale, L.e5m2 ? e5m2_value(kc) : e4m3_value(kc));
+          vx = __fmul_rn(*p.C.v_tscale, L.e5m2 ? e5m2_value(vc) : e4m3_value(vc));
         } else {
           const float* ks = reinterpret_cast<const float*>(rec);
           const float* kz = ks + 128;

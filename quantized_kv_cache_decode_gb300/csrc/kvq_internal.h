@@ -19,9 +19,16 @@ inline int decode_warps(int fmt, int g) {
   return (g <= 4 && (fmt == KVQ_FMT_INT2 || fmt == KVQ_FMT_INT4)) ? 16 : 12;
 }
 
+// The decode-kernel instantiation that serves a layer's format.  A bf16 layer
+// has no quantized tiles, so any instantiation runs only its bf16-tile path;
+// the 8-bit one is used.
+inline int kernel_format(int fmt) { return fmt == KVQ_FMT_BF16 ? KVQ_FMT_INT8 : fmt; }
+
 // Validated, derived form of kvq_layer_config.
 struct LayerDesc {
   int H, d, fmt, bits, fp8;
+  int e5m2;        // FP8 layer in E5M2 (else E4M3)
+  int bf16;        // unquantized layer: every token after the sink in the bf16 buffers (W = their rows)
   int G, Gv, ngv, R, S, W;  // W = R + G ring slots (0 for FP8)
   int paged, P, cap, num_blocks, mbps;
   int rb;          // bytes of one token row of codes (d * bits / 8)
@@ -111,13 +118,16 @@ cudaError_t launch_decode_int2(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_int4(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_int8(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int smem, cudaStream_t s);
+cudaError_t launch_decode_fp8_e5m2(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t occupancy_decode_int2(int ngv, int g, int smem, int* n);
 cudaError_t occupancy_decode_int4(int ngv, int g, int smem, int* n);
 cudaError_t occupancy_decode_int8(int ngv, int g, int smem, int* n);
 cudaError_t occupancy_decode_fp8(int ngv, int g, int smem, int* n);
+cudaError_t occupancy_decode_fp8_e5m2(int ngv, int g, int smem, int* n);
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
-cudaError_t launch_fp8_calibrate(const void* x, size_t n, float* scale_out, cudaStream_t stream);
+// scale = amax / fmax (1 when amax == 0), fmax the format's largest finite value
+cudaError_t launch_fp8_calibrate(const void* x, size_t n, float fmax, float* scale_out, cudaStream_t stream);
 cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream);
 
 }  // namespace kvq

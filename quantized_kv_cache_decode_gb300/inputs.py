@@ -46,14 +46,14 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 # Workload descriptions
 # --------------------------------------------------------------------------- #
 
-FORMAT_BITS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8}
+FORMAT_BITS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8, "fp8_e5m2": 8, "bf16": 16}
 
 
 @dataclasses.dataclass(frozen=True)
 class LayerFormat:
     """Quantization layout of one layer's KV cache.
 
-    fmt: "int2" | "int4" | "int8" | "fp8_e4m3"
+    fmt: "int2" | "int4" | "int8" | "fp8_e4m3" | "fp8_e5m2" | "bf16" (a skip layer: nothing quantized)
     G:   Key group length in tokens (per-channel Key quantization); 1 for FP8
     Gv:  Value group width in channels (per-token Value quantization)
     R:   residual window: the most recent tokens kept in bf16
@@ -104,6 +104,19 @@ def llama3_8b_fp8() -> Workload:
     return Workload("llama3_8b_fp8_e4m3", 1, 16, 32, 8, 128, 8192, [fmt], 10, 10, 8.0, "per_layer", seed=1002)
 
 
+def llama3_8b_fp8_e5m2() -> Workload:
+    """The same Llama-3-8B-shaped decode layer with FP8 E5M2 KV (the other OCP FP8 format)."""
+    fmt = LayerFormat("fp8_e5m2", G=1, Gv=128, R=0, S=0)
+    return Workload("llama3_8b_fp8_e5m2", 1, 16, 32, 8, 128, 8192, [fmt], 10, 10, 8.0, "per_layer", seed=1006)
+
+
+def llama3_8b_bf16_skip() -> Workload:
+    """The same layer left unquantized (a skip layer): bf16 K and V for every token, first token as sink."""
+    fmt = LayerFormat("bf16", G=16, Gv=128, R=0, S=1)
+    return Workload("llama3_8b_bf16_skip_layer", 1, 16, 32, 8, 128, 8192, [fmt], 10, 10, 8.0, "per_layer",
+                    seed=1007)
+
+
 def llama3_70b_int4() -> Workload:
     """Llama-3-70B-shaped decode over 80 layers, KIVI INT4 (G=128, Gv=128, R=128)."""
     fmt = LayerFormat("int4", G=128, Gv=128, R=128, S=0)
@@ -130,6 +143,8 @@ def paged_mixed() -> Workload:
 WORKLOADS = {
     "tiny_kivi_int4": tiny_int4,
     "llama3_8b_fp8_e4m3": llama3_8b_fp8,
+    "llama3_8b_fp8_e5m2": llama3_8b_fp8_e5m2,
+    "llama3_8b_bf16_skip_layer": llama3_8b_bf16_skip,
     "llama3_70b_kivi_int4_80l": llama3_70b_int4,
     "llama2_7b_kivi2_int2_32k": llama2_7b_int2,
     "paged_mixed_int8_int4_64l": paged_mixed,

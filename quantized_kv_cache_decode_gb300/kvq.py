@@ -29,7 +29,8 @@ KVQ_OK = 0
 STATUS = {0: "KVQ_OK", -1: "KVQ_ERR_INVALID_ARG", -2: "KVQ_ERR_UNSUPPORTED", -3: "KVQ_ERR_CUDA",
           -4: "KVQ_ERR_WORKSPACE"}
 DEV_BAD_BLOCK, DEV_CAPACITY, DEV_TIMEOUT = 0x1, 0x2, 0x4
-FORMATS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 16}
+FORMATS = {"bf16": 1, "int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 16, "fp8_e5m2": 17}
+FP8_FORMATS = (FORMATS["fp8_e4m3"], FORMATS["fp8_e5m2"])
 FIELDS = ["qstore", "block_pool", "resid_k", "resid_v", "sink_k", "sink_v"]
 
 
@@ -53,6 +54,7 @@ class LayerCache(ctypes.Structure):
 _P = ctypes.POINTER
 _lib.kvq_cache_layout.argtypes = [_P(LayerConfig), c_i32, _P(c_sz)]
 _lib.kvq_fp8_calibrate.argtypes = [c_vp, c_sz, c_vp, c_vp]
+_lib.kvq_fp8_calibrate_format.argtypes = [c_vp, c_sz, c_i32, c_vp, c_vp]
 _lib.kvq_quantize_append.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_vp, c_i32, c_vp, c_i32, c_vp, c_vp]
 _lib.kvq_decode_workspace_size.argtypes = [_P(LayerConfig), c_i32, c_i32, _P(c_sz)]
 _lib.kvq_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
@@ -65,7 +67,8 @@ _lib.kvq_decode_attention_static_scratch.argtypes = [_P(LayerConfig), _P(LayerCa
 _lib.kvq_dequantize.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]
 _lib.kvq_status_string.argtypes = [c_i32]
 _lib.kvq_status_string.restype = ctypes.c_char_p
-for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_quantize_append", "kvq_decode_workspace_size",
+for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_fp8_calibrate_format", "kvq_quantize_append",
+            "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize",
             "kvq_decode_attention_static_scratch"):
     getattr(_lib, _fn).restype = c_i32
@@ -118,8 +121,12 @@ def cache_layout(cfg: LayerConfig, num_seqs: int) -> Dict[str, int]:
     return {n: int(out[i]) for i, n in enumerate(FIELDS)}
 
 
-def fp8_calibrate(x, n: int, scale_out, stream=None) -> None:
-    _check("kvq_fp8_calibrate", _lib.kvq_fp8_calibrate(_ptr(x), n, _ptr(scale_out), _stream_ptr(stream)))
+def fp8_calibrate(x, n: int, scale_out, stream=None, fmt: str = "fp8_e4m3") -> None:
+    if fmt == "fp8_e4m3":
+        _check("kvq_fp8_calibrate", _lib.kvq_fp8_calibrate(_ptr(x), n, _ptr(scale_out), _stream_ptr(stream)))
+    else:
+        _check("kvq_fp8_calibrate_format",
+               _lib.kvq_fp8_calibrate_format(_ptr(x), n, FORMATS[fmt], _ptr(scale_out), _stream_ptr(stream)))
 
 
 def quantize_append(cfg: LayerConfig, cache: LayerCache, k_new, v_new, n_new: int, seq_lens, batch: int,
@@ -196,7 +203,7 @@ class CacheLayer:
         if cfg.paged:
             self.block_table = torch.full((num_seqs, cfg.max_blocks_per_seq), -1, dtype=torch.int32, device=device)
         self.k_tensor_scale = self.v_tensor_scale = None
-        if cfg.format == FORMATS["fp8_e4m3"]:
+        if cfg.format in FP8_FORMATS:
             self.k_tensor_scale = torch.ones(1, dtype=torch.float32, device=device)
             self.v_tensor_scale = torch.ones(1, dtype=torch.float32, device=device)
 

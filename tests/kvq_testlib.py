@@ -15,7 +15,7 @@ import numpy as np
 from oracle import kvq_oracle as O
 
 F32 = np.float32
-BITS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8}
+BITS = {"int2": 2, "int4": 4, "int8": 8, "fp8_e4m3": 8, "fp8_e5m2": 8}
 
 
 # --------------------------------------------------------------------------- #
@@ -34,7 +34,7 @@ def _frag_positions(fmt: str, i: np.ndarray, k: np.ndarray, s: np.ndarray):
         w, bit = s // 2, 8 * (s % 2) + 2 * reg + 16 * h
     elif fmt == "int8":
         w, bit = 2 * s + reg // 2, 8 * ((reg % 2) + 2 * h)
-    else:  # fp8_e4m3
+    else:  # fp8_e4m3, fp8_e5m2
         w, bit = 2 * s + reg // 2, 8 * (2 * (reg % 2) + h)
     byte = ((w // 4) * 32 + lane) * 16 + (w % 4) * 4 + bit // 8
     return byte, bit % 8
@@ -84,17 +84,22 @@ class GpuLayer:
         self.torch, self.kvq = torch, kvq
         self.fmt, self.H, self.lens = fmt, H, list(lens)
         self.B = len(lens)
-        self.fp8 = fmt == "fp8_e4m3"
-        self.G = 1 if self.fp8 else G
-        self.Gv = 128 if self.fp8 else Gv
-        self.R = 0 if self.fp8 else R
+        self.fp8 = fmt in ("fp8_e4m3", "fp8_e5m2")
+        self.bf16 = fmt == "bf16"
+        self.G = 1 if self.fp8 else (16 if self.bf16 else G)
+        self.Gv = 128 if (self.fp8 or self.bf16) else Gv
+        self.R = 0 if (self.fp8 or self.bf16) else R
         self.S = S
         self.spec = O.Spec(fmt, d=128, G=self.G, Gv=self.Gv, R=self.R, S=S)
         self.device = device
         self.paged = paged
         maxq = max([O.token_split(T + extra_capacity, self.spec)[1] for T in self.lens] + [0])
         unit = 16 if self.fp8 else max(16, self.G)
-        if paged:
+        if self.bf16:
+            # every token after the sink in the bf16 buffers, row t - S
+            self.W = max([1] + [T + extra_capacity - min(T + extra_capacity, S) for T in self.lens])
+            self.cfg = kvq.make_config(fmt, H, 0, 0, 0, S, capacity_tokens=self.W)
+        elif paged:
             self.P = block_tokens if self.fp8 else self.G
             blocks_per_seq = [math.ceil(O.token_split(T + extra_capacity, self.spec)[1] / self.P) for T in self.lens]
             self.mbps = max(blocks_per_seq + [1])
@@ -125,8 +130,8 @@ class GpuLayer:
         torch = self.torch
         kd = torch.from_numpy(k_all_bits.astype(np.int16)).to(self.device)
         vd = torch.from_numpy(v_all_bits.astype(np.int16)).to(self.device)
-        self.kvq.fp8_calibrate(kd, kd.numel(), self.layer.k_tensor_scale)
-        self.kvq.fp8_calibrate(vd, vd.numel(), self.layer.v_tensor_scale)
+        self.kvq.fp8_calibrate(kd, kd.numel(), self.layer.k_tensor_scale, fmt=self.fmt)
+        self.kvq.fp8_calibrate(vd, vd.numel(), self.layer.v_tensor_scale, fmt=self.fmt)
         torch.cuda.synchronize()
 
     def append(self, b: int, k_bits: np.ndarray, v_bits: np.ndarray, T_before: int):
@@ -173,7 +178,7 @@ class GpuLayer:
 
     # -- read the stored cache of (b, h) back into the oracle's logical form --
     def _layout(self):
-        rb = 128 * BITS[self.fmt] // 8
+        rb = 128 * BITS.get(self.fmt, 8) // 8
         ngv = 128 // self.Gv
         tile = 32 * rb + (0 if self.fp8 else 128 * ngv)
         hdr = 0 if self.fp8 else 1024
@@ -224,7 +229,7 @@ class GpuLayer:
             sv = self.raw("sink_v").view(np.uint16).reshape(self.B * self.H, self.S, 128)[pair, :n_sink]
             out["sink_k"], out["sink_v"] = sk, sv
         if not self.fp8:
-            W = self.R + self.G
+            W = self.W if self.bf16 else self.R + self.G
             ring_k = self.raw("resid_k").view(np.uint16).reshape(self.B * self.H, W, 128)[pair]
             ring_v = self.raw("resid_v").view(np.uint16).reshape(self.B * self.H, W, 128)[pair]
             slots = [(qn + i) % W for i in range(r)]
@@ -242,7 +247,7 @@ def compare_logical(gpu: Dict[str, np.ndarray], hc: "O.HeadCache"):
             assert g.shape == o.shape and np.array_equal(g.view(np.uint32), o.astype(F32).view(np.uint32)), f
     if len(hc.sink_k):
         assert np.array_equal(gpu["sink_k"], bf16_bits(hc.sink_k)) and np.array_equal(gpu["sink_v"], bf16_bits(hc.sink_v))
-    if hc.k_s is not None:
+    if not hc.spec.is_fp8:
         assert np.array_equal(gpu["resid_k"], bf16_bits(hc.resid_k)), "residual K differs"
         assert np.array_equal(gpu["resid_v"], bf16_bits(hc.resid_v)), "residual V differs"
 

@@ -51,6 +51,14 @@ def test_cache_layout_sizes(kvq):
     cfg = kvq.make_config("fp8_e4m3", 8, 1, 128, 0, 0, capacity_tokens=8192)
     sz = kvq.cache_layout(cfg, 16)
     assert sz["qstore"] == 16 * 8 * 8192 * 128 * 2 and sz["resid_k"] == 0
+    cfg = kvq.make_config("fp8_e5m2", 8, 1, 128, 0, 0, capacity_tokens=8192)
+    assert kvq.cache_layout(cfg, 16) == sz
+    # bf16 skip layer: no quantized store, bf16 rows for every token after the sink
+    cfg = kvq.make_config("bf16", 8, 0, 0, 0, 1, capacity_tokens=8191)
+    sz = kvq.cache_layout(cfg, 16)
+    assert sz["qstore"] == 0 and sz["block_pool"] == 0
+    assert sz["resid_k"] == sz["resid_v"] == 16 * 8 * 8191 * 128 * 2
+    assert sz["sink_k"] == 16 * 8 * 1 * 128 * 2
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -64,6 +72,10 @@ def test_cache_layout_sizes(kvq):
     (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, paged=True, block_tokens=16, num_blocks=4,
           max_blocks_per_seq=2), -1),
     (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, head_dim=64), -2),
+    (dict(fmt="fp8_e5m2", num_kv_heads=2, G=16, Gv=128, R=0, S=0, capacity_tokens=64), -1),
+    (dict(fmt="bf16", num_kv_heads=2, G=0, Gv=0, R=0, S=1, capacity_tokens=0), -1),
+    (dict(fmt="bf16", num_kv_heads=2, G=0, Gv=0, R=0, S=0, paged=True, block_tokens=16, num_blocks=4,
+          max_blocks_per_seq=2), -2),
 ])
 def test_config_validation(kvq, kw, status):
     kw = dict(kw)
@@ -72,6 +84,12 @@ def test_config_validation(kvq, kw, status):
     with pytest.raises(kvq.KvqError) as e:
         kvq.cache_layout(cfg, 1)
     assert e.value.status == status
+
+
+def test_calibrate_rejects_non_fp8_formats(kvq):
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.fp8_calibrate(0, 0, 16, stream=0, fmt="int4")
+    assert e.value.status == -1
 
 
 def test_calls_reject_bad_arguments_before_any_launch(kvq):
@@ -94,7 +112,7 @@ def test_fragment_order_is_a_bijection(part):
     import numpy as np
     import kvq_testlib as TL
     positions = TL.ktile_positions if part == "k" else TL.vtile_positions
-    for fmt, bits in (("int2", 2), ("int4", 4), ("int8", 8), ("fp8_e4m3", 8)):
+    for fmt, bits in (("int2", 2), ("int4", 4), ("int8", 8), ("fp8_e4m3", 8), ("fp8_e5m2", 8)):
         byte, bit = positions(fmt)
         tile_bytes = 16 * 128 * bits // 8
         used = np.zeros(tile_bytes * 8, int)

@@ -47,8 +47,8 @@ def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=Non
         kall = np.concatenate([kv[k][0].reshape(-1) for k in kv] + [np.zeros(0, np.uint16)])
         vall = np.concatenate([kv[k][1].reshape(-1) for k in kv] + [np.zeros(0, np.uint16)])
         gl.calibrate_fp8(kall, vall)
-        ks = O.fp8_tensor_scale(O.bf16_to_f32(kall))
-        vs = O.fp8_tensor_scale(O.bf16_to_f32(vall))
+        ks = O.fp8_tensor_scale(O.bf16_to_f32(kall), fmt)
+        vs = O.fp8_tensor_scale(O.bf16_to_f32(vall), fmt)
         assert gl.layer.k_tensor_scale.item() == float(ks) and gl.layer.v_tensor_scale.item() == float(vs)
     for b, T in enumerate(lens):
         if T == 0:
@@ -82,6 +82,12 @@ CASES = [
     ("int2", 2, 2, [900, 33], 32, 16, 32, 0, True, 32),
     ("fp8_e4m3", 2, 4, [500, 7, 48], 1, 128, 0, 1, True, 16),
     ("fp8_e4m3", 1, 8, [400, 31], 1, 128, 0, 0, True, 32),
+    ("fp8_e5m2", 2, 4, [0, 1, 15, 16, 17, 333], 1, 128, 0, 0, False, 16),
+    ("fp8_e5m2", 2, 6, [500, 7, 48], 1, 128, 0, 1, True, 16),
+    ("fp8_e5m2", 1, 8, [1200, 64], 1, 128, 0, 2, False, 16),
+    ("bf16", 2, 4, [0, 1, 15, 16, 17, 333], 0, 0, 0, 0, False, 16),
+    ("bf16", 2, 8, [700, 31, 2], 0, 0, 0, 1, False, 16),
+    ("bf16", 1, 1, [1500, 160], 0, 0, 0, 3, False, 16),
 ]
 
 
@@ -117,7 +123,8 @@ def test_parity(case):
 
 
 @pytest.mark.parametrize("fmt,G,Gv,R,S", [("int4", 32, 128, 32, 0), ("int2", 32, 32, 64, 1),
-                                          ("int8", 16, 64, 16, 2), ("fp8_e4m3", 1, 128, 0, 1)])
+                                          ("int8", 16, 64, 16, 2), ("fp8_e4m3", 1, 128, 0, 1),
+                                          ("fp8_e5m2", 1, 128, 0, 0), ("bf16", 0, 0, 0, 1)])
 def test_incremental_appends_equal_bulk(fmt, G, Gv, R, S):
     lens = [203, 77]
 

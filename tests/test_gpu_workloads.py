@@ -33,7 +33,7 @@ DEV = torch.device("cuda", 0)
 
 
 def _spec(fmt):
-    fp8 = fmt.fmt == "fp8_e4m3"
+    fp8 = bench.is_fp8(fmt)
     return O.Spec(fmt.fmt, d=128, G=1 if fp8 else fmt.G, Gv=fmt.Gv, R=0 if fp8 else fmt.R, S=fmt.S)
 
 
@@ -67,7 +67,7 @@ def _check_layer(w, l, pairs, seed_offset=0):
         if spec.is_fp8:
             kall = kd.float().cpu().numpy()
             vall = vd.float().cpu().numpy()
-            ks, vs = O.fp8_tensor_scale(kall), O.fp8_tensor_scale(vall)
+            ks, vs = O.fp8_tensor_scale(kall, spec.fmt), O.fp8_tensor_scale(vall, spec.fmt)
             del kall, vall
             assert lay.cache.k_tensor_scale.item() == float(ks)
             assert lay.cache.v_tensor_scale.item() == float(vs)
@@ -112,6 +112,16 @@ def test_tiny_kivi_int4_all_pairs():
 def test_llama3_8b_fp8_sampled():
     w = I.llama3_8b_fp8()
     _check_layer(w, 0, [(0, 0), (7, 3), (15, 7)])
+
+
+def test_llama3_8b_fp8_e5m2_sampled():
+    w = I.llama3_8b_fp8_e5m2()
+    _check_layer(w, 0, [(0, 0), (8, 2), (15, 7)])
+
+
+def test_llama3_8b_bf16_skip_layer_sampled():
+    w = I.llama3_8b_bf16_skip()
+    _check_layer(w, 0, [(0, 0), (11, 6), (15, 7)])
 
 
 @pytest.mark.parametrize("layer", [0, 79])
