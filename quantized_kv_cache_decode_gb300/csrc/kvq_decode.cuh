@@ -767,8 +767,11 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         tg.rpos = 0;
         tg.n = 1;
         tg.first = 0;
-        if (lane == 0) {
-          // bf16 tile: its 16 K rows (first stage) or V rows (second), one 256-byte copy per row
+        {
+          // bf16 tile: its 16 K rows (first stage) or V rows (second).  Every lane copies
+          // 16-byte chunk (lane & 15) of rows (lane >> 4) + 2i with cp.async (coalesced,
+          // the padded row pitch kept) as one commit group; the consumer waits for the
+          // group (cp.async.wait_group), the slot's barrier only keeps the phases in step.
           uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
           const uint32_t bar = smem_addr(&my_bars[slot]);
           const int x0 = p_a * 16;  // bf16-list index of the first row (sinks, then residual)
@@ -776,20 +779,20 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           const long long pair = (long long)sg.b * H + sg.h;
           const __nv_bfloat16* sink = p_end ? sink_v : sink_k;
           const __nv_bfloat16* ring = p_end ? ring_v : ring_k;
-          mbar_arrive_expect_tx(bar, 256u * rows);
-          int slot_r = -1;
-          for (int rr = 0; rr < rows; ++rr) {
-            const int xb = x0 + rr;
-            const __nv_bfloat16* src;
-            if (xb < sg.n_sink) {
-              src = sink + (pair * L.S + xb) * L.d;
-            } else {
-              if (slot_r < 0) slot_r = (sg.qn + xb - sg.n_sink) % L.W;
-              else if (++slot_r == L.W) slot_r = 0;
-              src = ring + (pair * L.W + slot_r) * L.d;
+          const int ch = lane & 15;
+          const int rbase = sg.qn - sg.n_sink + x0;  // ring index of row 0 before the modulo
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = (lane >> 4) + 2 * i;
+            if (rr < rows) {
+              const int xb = x0 + rr;
+              const __nv_bfloat16* src =
+                  xb < sg.n_sink ? sink + (pair * L.S + xb) * L.d : ring + (pair * L.W + (rbase + rr) % L.W) * L.d;
+              cp_async_16(smem_addr(dst + rr * kBfRow + 16 * ch), src + 8 * ch);
             }
-            bulk_copy_g2s(smem_addr(dst + rr * kBfRow), src, 256, bar);
           }
+          cp_async_commit();
+          if (lane == 0) mbar_arrive(bar);
         }
         vm = 1;
         ++p_end;
@@ -951,6 +954,19 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         }
         const uint8_t* stg = my_stages + (size_t)slot * p.stage_bytes;
         if (vmask && alive && tg.kind != 3) {
+          // this stage's cp.async group: complete once at most `newer` groups (the bf16
+          // stages issued after it) are pending; then every lane's copies are visible
+          int newer = 0;
+          for (int j = 1; j < n_issued - n_consumed; ++j) {
+            int sl = slot + j;
+            if (sl >= nst) sl -= nst;
+            newer += my_tags[sl].kind != 3;
+          }
+          if (newer == 0) cp_async_wait<0>();
+          else if (newer == 1) cp_async_wait<1>();
+          else if (newer == 2) cp_async_wait<2>();
+          else cp_async_wait<3>();
+          __syncwarp();
           const int rows = min(16, nbf_tok - tg.a * 16);
           if (tg.kind == 1) {
             // ---- bf16 tile, K rows ----
@@ -1299,6 +1315,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       }
       __syncthreads();
     }
+    cp_async_wait<0>();  // no cp.async left in flight when the warp moves on or exits
     // drain copies still in flight after a timeout (bounded)
     if (pending) {
       for (int sl = 0; sl < nst; ++sl)
