@@ -122,16 +122,21 @@ int tiles_per_stage(const LayerDesc& L, int target) {
   return std::max(1, std::min(8, (target + per / 2) / per));
 }
 
+constexpr int kBfHalfBytes = 16 * 256;  // the K (or V) rows of a 16-token bf16 tile
+
 // A stage holds a header slot, tps tiles and the record headers between them,
-// or (layers with bf16 tokens) one half (K or V rows) of a 16-token bf16 tile
-// at 272 bytes per row.
+// or (layers with bf16 tokens) the K or V rows of a 16-token bf16 tile (both
+// when the stage has room for them: see bf16_joint).  A bf16 layer has only
+// bf16 tiles: its stages hold both halves.
 int stage_bytes_of(const LayerDesc& L, int tps) {
+  if (L.bf16) return 2 * kBfHalfBytes;
   const int inline_hdrs = (tps + L.tpg - 1) / L.tpg;
   const int q = L.hdr_bytes + tps * L.tile_bytes + inline_hdrs * L.hdr_bytes;
   const bool bf16_tiles = L.S > 0 || !L.fp8;
-  const int bf = bf16_tiles ? 16 * 272 : 0;
+  const int bf = bf16_tiles ? kBfHalfBytes : 0;
   return (std::max(q, bf) + 127) / 128 * 128;
 }
+bool bf16_joint(int stage_bytes) { return stage_bytes >= 2 * kBfHalfBytes; }
 
 // A warp's merge record in shared memory: m, l, -, - and 128 outputs per query head.
 int merge_bytes_of(const LayerDesc& L, int g) {
@@ -369,6 +374,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.item_tiles = (std::max(G.tps, L.tpg) + L.tpg - 1) / L.tpg * L.tpg;
   // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
   p.bf_weight = std::max(1, (8192 + L.tile_bytes / 2) / L.tile_bytes);
+  p.bf_joint = bf16_joint(G.stage_bytes) ? 1 : 0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_o = reinterpret_cast<float*>(ws);
   p.ws_lse = reinterpret_cast<float*>(ws + G.off_lse);

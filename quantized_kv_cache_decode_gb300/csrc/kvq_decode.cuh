@@ -60,7 +60,11 @@ constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 r
 constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
 constexpr float kSTau = 4.f;           // a Value scale may exceed its reference 4x before a rescale
 constexpr int kQRow = 132;             // floats per query head in shared memory (128 + 4 pad)
-constexpr int kBfRow = 272;            // bytes per bf16 row in a stage (256 + 16 pad: ldmatrix without conflicts)
+// A bf16 half tile in a stage: 16 rows of 256 bytes, the 16-byte chunk c of row r
+// stored at chunk c ^ (r & 7), so that the 8 rows an ldmatrix reads at one chunk
+// fall in 8 different bank groups.
+constexpr int kBfHalf = 16 * 256;
+__host__ __device__ constexpr int bf_chunk_off(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
 constexpr int kMergeStride = 132;      // floats per head in a warp's merge record: m, l, -, -, o[128]
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -421,8 +425,11 @@ __device__ __forceinline__ void pv_tile(const uint32_t (&VW)[FT<FMT>::kWords], c
 template <int NBQ>
 __device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* q_s, int lane, int r, int q, int g,
                                         int rows, float scale_log2, float (&sig)[NBQ][2]) {
-  const uint32_t sbase = smem_addr(stg);
-  const uint32_t lbase = sbase + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kBfRow + 16 * (lane >> 4);
+  // lane's row (lane & 7) + 8 ((lane >> 3) & 1), chunk 2s + (lane >> 4), swizzled:
+  // (2s + h) ^ x = 2 (s ^ (x >> 1)) + (h ^ (x & 1)) with x = lane & 7
+  const int x = lane & 7;
+  const uint32_t lbase =
+      smem_addr(stg) + ((lane & 7) + 8 * ((lane >> 3) & 1)) * 256 + 16 * ((lane >> 4) ^ (x & 1));
   const bool qcol = (r & 1) == 0;  // even columns carry the query, odd columns are zero
   float acc[NBQ][2][4];
 #pragma unroll
@@ -434,7 +441,7 @@ __device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* q_s, in
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     uint32_t a0, a1, a2, a3;
-    ldmatrix_x4(lbase + 32 * s, a0, a1, a2, a3);
+    ldmatrix_x4(lbase + 32 * (s ^ (x >> 1)), a0, a1, a2, a3);
 #pragma unroll
     for (int b = 0; b < NBQ; ++b) {
       const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 16 * s + 2 * q;
@@ -458,15 +465,15 @@ __device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* q_s, in
 // into two bf16 terms.
 __device__ __forceinline__ void bf16_pv(const uint8_t* stg, int lane, const float (&pt)[4], float f,
                                         float (&o)[8][4]) {
-  const int mi = lane >> 3;
-  const uint32_t lbase = smem_addr(stg) + ((lane & 7) + 8 * (mi >> 1)) * kBfRow + 16 * (mi & 1);
+  const int mi = lane >> 3, x = lane & 7;  // row (lane & 7) + 8 (mi >> 1), chunk 2 mb + (mi & 1), swizzled
+  const uint32_t lbase = smem_addr(stg) + ((lane & 7) + 8 * (mi >> 1)) * 256 + 16 * ((mi & 1) ^ (x & 1));
   uint32_t h01, l01, h23, l23;
   split_bf16(pt[0] * f, pt[1] * f, h01, l01);
   split_bf16(pt[2] * f, pt[3] * f, h23, l23);
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb) {
     uint32_t a0, a1, a2, a3;
-    ldmatrix_x4_trans(lbase + 32 * mb, a0, a1, a2, a3);
+    ldmatrix_x4_trans(lbase + 32 * (mb ^ (x >> 1)), a0, a1, a2, a3);
     mma_bf16(o[mb], a0, a1, a2, a3, h01, h23);
     mma_bf16(o[mb], a0, a1, a2, a3, l01, l23);
   }
@@ -557,7 +564,9 @@ struct SlotTag {
 static_assert(sizeof(SlotTag) == 20, "the host reserves 20 bytes per slot tag");
 static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment record");
 
-template <int FMT, int NGV, int NBQ>
+// BF: the layer may have bf16 tiles (sink or residual tokens); the variant without
+// them (FP8 layers with no sink tokens) carries no bf16-tile code at all.
+template <int FMT, int NGV, int NBQ, bool BF>
 __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
   constexpr int NW = DecodeWarps<FMT, NBQ>::kNW;
@@ -569,6 +578,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   const int r = lane >> 2, q = lane & 3;
   const int B = p.batch, H = L.H, g = p.g;
   const int tps = p.tps, nst = p.nst, wbf = p.bf_weight;
+  const bool bfj = p.bf_joint != 0;  // a bf16 tile's K and V rows share one stage
   const int it = p.item_tiles;
 
   // ---- shared memory carve-up ----
@@ -735,7 +745,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         if (pk == 3 && p_a < p_end) return true;
         const int t = warp + NW * (p_claims++);  // items warp, warp + NW, ... of the segment
         const SegItems si = segs[ps].it;
-        if (t < si.nbf_items) {
+        if (BF && t < si.nbf_items) {
           pk = 1;
           p_a = si.bl + t;
           p_end = 0;
@@ -761,41 +771,69 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       uint32_t vm = 0;
       SlotTag tg;
       tg.seg = ps;
-      if (pk == 1) {
+      if (BF && pk == 1) {
         tg.kind = (short)(1 + p_end);
         tg.a = p_a;
         tg.rpos = 0;
         tg.n = 1;
         tg.first = 0;
         {
-          // bf16 tile: its 16 K rows (first stage) or V rows (second).  Every lane copies
-          // 16-byte chunk (lane & 15) of rows (lane >> 4) + 2i with cp.async (coalesced,
-          // the padded row pitch kept) as one commit group; the consumer waits for the
-          // group (cp.async.wait_group), the slot's barrier only keeps the phases in step.
+          // bf16 tile: its 16 K rows and 16 V rows in one stage (joint), or the K rows in
+          // one stage and the V rows in the next.  Every lane copies 16-byte chunk
+          // (lane & 15) of rows (lane >> 4) + 2i with cp.async (coalesced) as one commit
+          // group; the consumer waits for the group (cp.async.wait_group), the slot's
+          // barrier only keeps the phases in step.
           uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
           const uint32_t bar = smem_addr(&my_bars[slot]);
           const int x0 = p_a * 16;  // bf16-list index of the first row (sinks, then residual)
           const int rows = min(16, sg.n_sink + sg.r - x0);
           const long long pair = (long long)sg.b * H + sg.h;
-          const __nv_bfloat16* sink = p_end ? sink_v : sink_k;
-          const __nv_bfloat16* ring = p_end ? ring_v : ring_k;
-          const int ch = lane & 15;
-          const int rbase = sg.qn - sg.n_sink + x0;  // ring index of row 0 before the modulo
+          const int ch = lane & 15, hi = lane >> 4;
+          // ring slot of the tile's first residual row (one modulo per stage); rows
+          // [nsk, rows) are residual rows, the first nsk (if any) sink rows
+          const int nsk = max(0, min(rows, sg.n_sink - x0));
+          int slot0 = 0;
+          if (rows > nsk) slot0 = (sg.qn - sg.n_sink + x0 + nsk) % L.W;
+          const int hv0 = bfj ? 0 : p_end, hv1 = bfj ? 1 : p_end;
+          if (nsk == 0 && slot0 + rows <= L.W) {
+            // common case: the 16 rows are consecutive ring rows
+            const long long roff = (pair * L.W + slot0) * L.d + 8 * ch;
+            for (int hv = hv0; hv <= hv1; ++hv) {
+              const __nv_bfloat16* src = (hv ? ring_v : ring_k) + roff;
+              const uint32_t half = smem_addr(dst + (bfj ? hv * kBfHalf : 0));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = (lane >> 4) + 2 * i;
-            if (rr < rows) {
-              const int xb = x0 + rr;
-              const __nv_bfloat16* src =
-                  xb < sg.n_sink ? sink + (pair * L.S + xb) * L.d : ring + (pair * L.W + (rbase + rr) % L.W) * L.d;
-              cp_async_16(smem_addr(dst + rr * kBfRow + 16 * ch), src + 8 * ch);
+              for (int i = 0; i < 8; ++i) {
+                const int rr = hi + 2 * i;
+                if (rr < rows) cp_async_16(half + bf_chunk_off(rr, ch), src + rr * 128);
+              }
+            }
+          } else {
+            // sink rows first, or a ring that wraps inside the tile: row by row
+            for (int hv = hv0; hv <= hv1; ++hv) {
+              const __nv_bfloat16* sink = hv ? sink_v : sink_k;
+              const __nv_bfloat16* ring = hv ? ring_v : ring_k;
+              const uint32_t half = smem_addr(dst + (bfj ? hv * kBfHalf : 0));
+              for (int i = 0; i < 8; ++i) {
+                const int rr = hi + 2 * i;
+                if (rr < rows) {
+                  const __nv_bfloat16* src;
+                  if (rr < nsk) {
+                    src = sink + (pair * L.S + x0 + rr) * L.d;
+                  } else {
+                    int sl = slot0 + (rr - nsk);
+                    if (sl >= L.W) sl -= L.W;
+                    src = ring + (pair * L.W + sl) * L.d;
+                  }
+                  cp_async_16(half + bf_chunk_off(rr, ch), src + 8 * ch);
+                }
+              }
             }
           }
           cp_async_commit();
           if (lane == 0) mbar_arrive(bar);
         }
         vm = 1;
-        ++p_end;
+        p_end = bfj ? 2 : p_end + 1;
       } else {
         // n quantized tiles from (q_rec, q_pos), one contiguous range per record touched
         const int n = min(tps, p_end - p_a);
@@ -953,7 +991,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           }
         }
         const uint8_t* stg = my_stages + (size_t)slot * p.stage_bytes;
-        if (vmask && alive && tg.kind != 3) {
+        if (BF && vmask && alive && tg.kind != 3) {
           // this stage's cp.async group: complete once at most `newer` groups (the bf16
           // stages issued after it) are pending; then every lane's copies are visible
           int newer = 0;
@@ -968,20 +1006,25 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           else cp_async_wait<3>();
           __syncwarp();
           const int rows = min(16, nbf_tok - tg.a * 16);
+          // K rows: scores.  V rows (the same stage when joint, else the next one): rows past
+          // the end zeroed (their p is 0, garbage could be NaN), the softmax step, then PV
+          const uint8_t* vst = stg;
+          bool vpart = tg.kind == 2;
           if (tg.kind == 1) {
-            // ---- bf16 tile, K rows ----
             bf16_qk<NBQ>(stg, q_s, lane, r, q, g, rows, p.scale_log2, sig_bf);
-          } else {
-            // ---- bf16 tile, V rows: softmax, then PV ----
-            uint8_t* stw = const_cast<uint8_t*>(stg);
+            vpart = bfj;
+            vst = stg + kBfHalf;
+          }
+          if (vpart) {
+            uint8_t* stw = const_cast<uint8_t*>(vst);
             for (int idx = lane; idx < (16 - rows) * 16; idx += 32)
-              *reinterpret_cast<uint4*>(stw + (rows + idx / 16) * kBfRow + (idx % 16) * 16) = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(stw + (rows + idx / 16) * 256 + (idx % 16) * 16) = make_uint4(0u, 0u, 0u, 0u);
             __syncwarp();
             float pr[NBQ][2];
             softmax_tile<NBQ, NGV, false>(stt, sig_bf, 1.f, r, q, pr);
             float pt[4];
             p_operand<NBQ, 2>(pr, 0, r, q, pt);
-            bf16_pv(stg, lane, pt, stt.inv_S * kPrescale, stt.o);
+            bf16_pv(vst, lane, pt, stt.inv_S * kPrescale, stt.o);
           }
         } else if (vmask && alive) {
           // ---- quantized stage: tiles [tg.a, tg.a + n), walked in smem, one softmax step each ----
@@ -1315,7 +1358,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       }
       __syncthreads();
     }
-    cp_async_wait<0>();  // no cp.async left in flight when the warp moves on or exits
+    if constexpr (BF) cp_async_wait<0>();  // no cp.async left in flight when the warp moves on or exits
     // drain copies still in flight after a timeout (bounded)
     if (pending) {
       for (int sl = 0; sl < nst; ++sl)
@@ -1331,7 +1374,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, int NBQ>
+template <int FMT, int NGV, int NBQ, bool BF>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1340,36 +1383,44 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, NBQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, NBQ, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-// One column block for up to 4 query heads per kv head, two for 5..8.
-template <int FMT, int NGV>
-cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e;
-  if (p.g <= 4) {
-    if ((e = ensure_smem_attr<FMT, NGV, 1>(smem)) != cudaSuccess) return e;
-    decode_kernel<FMT, NGV, 1><<<p.num_ctas, DecodeWarps<FMT, 1>::kThreads, smem, stream>>>(p);
-  } else {
-    if ((e = ensure_smem_attr<FMT, NGV, 2>(smem)) != cudaSuccess) return e;
-    decode_kernel<FMT, NGV, 2><<<p.num_ctas, DecodeWarps<FMT, 2>::kThreads, smem, stream>>>(p);
-  }
+template <int FMT, int NGV, int NBQ, bool BF>
+cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr<FMT, NGV, NBQ, BF>(smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<FMT, NGV, NBQ, BF><<<p.num_ctas, DecodeWarps<FMT, NBQ>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
+// One column block for up to 4 query heads per kv head, two for 5..8; FP8 layers
+// without sink tokens (no bf16 tiles) take the variant without the bf16 path.
+template <int FMT, int NGV>
+cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
+  if constexpr (FT<FMT>::kFp8) {
+    if (p.L.S == 0)
+      return p.g <= 4 ? launch_variant<FMT, NGV, 1, false>(p, smem, stream)
+                      : launch_variant<FMT, NGV, 2, false>(p, smem, stream);
+  }
+  return p.g <= 4 ? launch_variant<FMT, NGV, 1, true>(p, smem, stream)
+                  : launch_variant<FMT, NGV, 2, true>(p, smem, stream);
+}
+
+// Resident CTAs per SM (the variant with the bf16 path: the larger of the two).
 template <int FMT, int NGV>
 cudaError_t occupancy_t(int g, int smem, int* n) {
   cudaError_t e;
   if (g <= 4) {
-    if ((e = ensure_smem_attr<FMT, NGV, 1>(smem)) != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 1>, DecodeWarps<FMT, 1>::kThreads,
-                                                         smem);
+    if ((e = ensure_smem_attr<FMT, NGV, 1, true>(smem)) != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 1, true>,
+                                                         DecodeWarps<FMT, 1>::kThreads, smem);
   }
-  if ((e = ensure_smem_attr<FMT, NGV, 2>(smem)) != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 2>, DecodeWarps<FMT, 2>::kThreads,
-                                                       smem);
+  if ((e = ensure_smem_attr<FMT, NGV, 2, true>(smem)) != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 2, true>,
+                                                       DecodeWarps<FMT, 2>::kThreads, smem);
 }
 
 }  // namespace kvq

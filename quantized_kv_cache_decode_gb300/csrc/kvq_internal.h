@@ -65,6 +65,7 @@ struct DecodeParams {
   int tps;           // quantized tiles per stage
   int item_tiles;    // quantized tiles per claimed work item (a multiple of the record size)
   int bf_weight;     // work units charged to a bf16 tile (quantized tiles cost 1)
+  int bf_joint;      // 1: a bf16 tile's K and V rows (2 x 4 KB) share one stage; 0: one stage each
   float* ws_o;       // [slots][g][d] normalised partial outputs
   float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial
   int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
