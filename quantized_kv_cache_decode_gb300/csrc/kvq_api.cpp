@@ -130,18 +130,29 @@ constexpr int kBfHalfBytes = 16 * 256;  // the K (or V) rows of a 16-token bf16 
 // bf16 tiles: its stages hold both halves.
 int stage_bytes_of(const LayerDesc& L, int tps) {
   if (L.bf16) return 2 * kBfHalfBytes;
-  const int inline_hdrs = (tps + L.tpg - 1) / L.tpg;
-  const int q = L.hdr_bytes + tps * L.tile_bytes + inline_hdrs * L.hdr_bytes;
+  // headers a stage can hold: with one tile per record, every tile's own; with a
+  // stage no longer than a record, one (work items are then whole records, so a
+  // stage never crosses a record boundary: it holds either the inline header of
+  // the record it starts, or the header copied ahead of a mid-record start);
+  // otherwise the header copied ahead plus one per record started inside it
+  int hdrs;
+  if (L.tpg == 1) hdrs = tps;
+  else if (tps <= L.tpg) hdrs = 1;
+  else hdrs = 1 + (tps + L.tpg - 1) / L.tpg;
+  const int q = tps * L.tile_bytes + (L.hdr_bytes ? hdrs * L.hdr_bytes : 0);
   const bool bf16_tiles = L.S > 0 || !L.fp8;
   const int bf = bf16_tiles ? kBfHalfBytes : 0;
   return (std::max(q, bf) + 127) / 128 * 128;
 }
 bool bf16_joint(int stage_bytes) { return stage_bytes >= 2 * kBfHalfBytes; }
 
+constexpr int kMergeFloats = 132;        // floats per query head of a merge record (kvq_decode.cuh)
+constexpr int kQRowFloats = 136;         // floats per query head row in shared memory (kvq_decode.cuh)
+
 // A warp's merge record in shared memory: m, l, -, - and 128 outputs per query head.
 int merge_bytes_of(const LayerDesc& L, int g) {
   (void)L;
-  return g * 132 * 4;
+  return g * kMergeFloats * 4;
 }
 
 constexpr int kSegTableBytes = 16 * 80;  // kMaxSeg segment records of 80 bytes (kvq_decode.cuh)
@@ -150,9 +161,9 @@ constexpr int kSlotTagBytes = 20;        // one pipeline slot's tag (kvq_decode.
 int fixed_smem(int batch, int merge_bytes, int nw) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16 + (batch * 4 + 15) / 16 * 16;  // unit prefix, token counts
   // per warp: barriers, block-table window, slot tags; nw/2 merge records; the query rows (g + 1)
-  const int g = merge_bytes / (132 * 4);
+  const int g = merge_bytes / (kMergeFloats * 4);
   const int per_warp = kMaxStages * 8 + 32 * 4 + (kMaxStages * kSlotTagBytes + 15) / 16 * 16;
-  return nw * per_warp + nw / 2 * merge_bytes + (g + 1) * 132 * 4 + kSegTableBytes + prefix;
+  return nw * per_warp + nw / 2 * merge_bytes + (g + 1) * kQRowFloats * 4 + kSegTableBytes + prefix;
 }
 
 cudaError_t occupancy_query(const LayerDesc& L, int g, int smem, int* n) {

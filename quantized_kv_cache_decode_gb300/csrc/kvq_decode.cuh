@@ -59,7 +59,10 @@ constexpr int kMaxStages = 4;
 constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 range is safe
 constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
 constexpr float kSTau = 4.f;           // a Value scale may exceed its reference 4x before a rescale
-constexpr int kQRow = 132;             // floats per query head in shared memory (128 + 4 pad)
+// floats per query head in shared memory (128 + 8 pad): the rows of four heads start
+// 8 banks apart, so the bf16 path's 8-byte query loads (four heads, four column
+// pairs per step) and build_bq's 16-byte loads are free of bank conflicts
+constexpr int kQRow = 136;
 // A bf16 half tile in a stage: 16 rows of 256 bytes, the 16-byte chunk c of row r
 // stored at chunk c ^ (r & 7), so that the 8 rows an ldmatrix reads at one chunk
 // fall in 8 different bank groups.
@@ -381,6 +384,88 @@ __device__ __forceinline__ void build_bq(const float* q_s, const float* ks, cons
     const float kf = kfac0 / kap, ct = kfac0 * cz;
     kfac[b] = __shfl_sync(kFull, kf, 8 * q);
     cterm[b] = __shfl_sync(kFull, ct, 8 * q);
+  }
+}
+
+// The same B operand for a Key group of an INT layer, in one pass over the
+// channels: kappa = 16384 / (max_c |q_c| * max_c s_c) bounds |x_c kappa| by
+// 16384 without first finding max_c |x_c| (qm[b]: the lane's head max |q_c|, per
+// segment).  A smaller kappa than the exact one only moves the hi/lo split: the
+// two f16 terms still hold x_c kappa to about 22 bits, or to the f16 subnormal
+// step (2^-24, against elements up to 16384 times the bound ratio) for tiny x_c.
+template <int FMT, int NBQ>
+__device__ __forceinline__ void build_bq_group(const float* q_s, const float* ks, const float* kz, int lane, int r,
+                                               int q, int g, float kfac0, const float (&qm)[NBQ],
+                                               uint32_t (&Bq)[NBQ][8][2], float (&kfac)[NBQ], float (&cterm)[NBQ]) {
+  constexpr float kH = (float)FT<FMT>::kHalf;
+  const bool lo = (r & 1) != 0;
+  // the largest Key scale of the group (scales are positive)
+  float sm;
+  {
+    const float4 a = *reinterpret_cast<const float4*>(ks + 4 * lane);
+    sm = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm = fmaxf(sm, __shfl_xor_sync(kFull, sm, o));
+  }
+#pragma unroll
+  for (int b = 0; b < NBQ; ++b) {
+    const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 4 * q;  // row g is zero
+    const float bound = qm[b] * sm;
+    float kap = 16384.f / bound;
+    if (!(bound > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
+    float cz = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
+      const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
+      const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
+      x.x *= s4.x;
+      x.y *= s4.y;
+      x.z *= s4.z;
+      x.w *= s4.w;
+      cz = fmaf(x.x, kH - z4.x, cz);
+      cz = fmaf(x.y, kH - z4.y, cz);
+      cz = fmaf(x.z, kH - z4.z, cz);
+      cz = fmaf(x.w, kH - z4.w, cz);
+      x.x *= kap;
+      x.y *= kap;
+      x.z *= kap;
+      x.w *= kap;
+      uint32_t h01 = pack_f16(x.x, x.y), h23 = pack_f16(x.z, x.w);
+      if (lo) {
+        const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
+        h01 = pack_f16(x.x - f01.x, x.y - f01.y);
+        h23 = pack_f16(x.z - f23.x, x.w - f23.y);
+      }
+      Bq[b][s][0] = h01;
+      Bq[b][s][1] = h23;
+      asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
+    }
+    cz += __shfl_xor_sync(kFull, cz, 1);
+    cz += __shfl_xor_sync(kFull, cz, 2);
+    // to the score layout: head 4b + q is held by the lanes with r = 2q
+    const float kf = kfac0 / kap, ct = kfac0 * cz;
+    kfac[b] = __shfl_sync(kFull, kf, 8 * q);
+    cterm[b] = __shfl_sync(kFull, ct, 8 * q);
+  }
+}
+
+// Max |q_c| over the channels of the lane's head (4b + (r >> 1), row g zero) of each
+// column block: lane q reads channels 32q .. 32q + 31, the four lanes of a head combine.
+template <int NBQ>
+__device__ __forceinline__ void head_qmax(const float* q_s, int r, int q, int g, float (&qm)[NBQ]) {
+#pragma unroll
+  for (int b = 0; b < NBQ; ++b) {
+    const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 32 * q;
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 x = *reinterpret_cast<const float4*>(qh + 4 * j);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+    }
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+    qm[b] = m;
   }
 }
 
@@ -957,9 +1042,11 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       state_init(stt);
       uint32_t Bq[NBQ][8][2];
       float kfac[NBQ], cterm[NBQ];
+      float qm[NBQ];  // INT: the lanes' head max |q_c| (the Key groups' kappa bound)
       if constexpr (F::kFp8) {
         build_bq<FMT, NBQ>(q_s, nullptr, nullptr, r, q, g, p.scale_log2 * __ldg(p.C.k_tscale), Bq, kfac, cterm);
       } else {
+        head_qmax<NBQ>(q_s, r, q, g, qm);
 #pragma unroll
         for (int b = 0; b < NBQ; ++b) {
           kfac[b] = cterm[b] = 0.f;
@@ -1043,9 +1130,9 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
             if constexpr (F::kInt) {
               // the group's B operand (q * s, hi/lo), rebuilt at each record (Key group) start
               if (hdr)
-                build_bq<FMT, NBQ>(q_s, reinterpret_cast<const float*>(stg + hoff),
-                                   reinterpret_cast<const float*>(stg + hoff + 512), r, q, g, p.scale_log2, Bq, kfac,
-                                   cterm);
+                build_bq_group<FMT, NBQ>(q_s, reinterpret_cast<const float*>(stg + hoff),
+                                         reinterpret_cast<const float*>(stg + hoff + 512), lane, r, q, g, p.scale_log2,
+                                         qm, Bq, kfac, cterm);
             }
             // QK
             float d[NBQ][2];
