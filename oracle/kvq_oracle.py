@@ -453,6 +453,34 @@ def decode_attention(q: np.ndarray, caches: List[List[HeadCache]], softmax_scale
     return out, lse
 
 
+def decode_attention_multi(q: np.ndarray, caches: List[List[HeadCache]], softmax_scale: Optional[float] = None):
+    """Several new query tokens per sequence, each attending causally.
+
+    The same score formula ("W4A16 + KV ...", section "오차가 어디서 만나는가")
+    for M query tokens per sequence whose K, V are already the cache's last M
+    tokens: query token i of a sequence with T cached tokens sits at position
+    T - M + i and attends to tokens 0 .. T - M + i of the cache (as dequantized
+    with all T tokens written).  q: [B, M, Hq, d].  Returns out [B, M, Hq, d],
+    lse [B, M, Hq] (a query with no visible token: out 0, lse -inf).
+    """
+    B, M, Hq, d = q.shape
+    Hkv = len(caches[0])
+    g = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else softmax_scale
+    out = np.zeros((B, M, Hq, d))
+    lse = np.zeros((B, M, Hq))
+    for b in range(B):
+        for h in range(Hkv):
+            k_hat, v_hat = dequantized_f64(caches[b][h])
+            T = k_hat.shape[0]
+            for i in range(M):
+                n = max(0, T - M + i + 1)
+                for j in range(g):
+                    hq = h * g + j
+                    out[b, i, hq], lse[b, i, hq] = attend_head(q[b, i, hq], k_hat[:n], v_hat[:n], scale)
+    return out, lse
+
+
 # --------------------------------------------------------------------------- #
 # Byte accounting ("KV Cache Quantization Analysis", box "메모리 크기 감각")
 # --------------------------------------------------------------------------- #

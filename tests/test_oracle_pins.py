@@ -412,6 +412,46 @@ def test_attention_brute_force(spec):
             assert abs(lse[b, hq] - l) < 1e-12
 
 
+@pytest.mark.parametrize("spec", [
+    O.Spec("int4", d=16, G=8, Gv=8, R=4, S=1),
+    O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=0),
+    O.Spec("bf16", d=16, G=16, Gv=16, R=0, S=1),
+])
+def test_multi_query_causal_brute_force(spec):
+    # query i of M sees tokens 0 .. T - M + i of the full cache; checked against the
+    # plain-Python attention over that prefix of the element-wise dequantized tokens
+    rng = np.random.default_rng(5)
+    B, Hkv, g, M = 2, 2, 2, 3
+    lens = [23, 2]  # the second sequence is shorter than M: its first query sees nothing
+    caches = []
+    for b in range(B):
+        row = []
+        for h in range(Hkv):
+            k = rng.standard_normal((lens[b], 16)).astype(F32)
+            v = rng.standard_normal((lens[b], 16)).astype(F32)
+            ks = O.fp8_tensor_scale(k, spec.fmt) if spec.is_fp8 else None
+            vs = O.fp8_tensor_scale(v, spec.fmt) if spec.is_fp8 else None
+            row.append(O.build_head_cache(k, v, spec, ks, vs))
+        caches.append(row)
+    q = rng.standard_normal((B, M, Hkv * g, 16)).astype(F32)
+    out, lse = O.decode_attention_multi(q, caches)
+    for b in range(B):
+        for i in range(M):
+            n = lens[b] - M + i + 1
+            for hq in range(Hkv * g):
+                K, V = _dequant_brute(caches[b][hq // g])
+                if n <= 0:
+                    assert np.all(out[b, i, hq] == 0) and lse[b, i, hq] == -math.inf
+                    continue
+                o, l = _brute_attention(q[b, i, hq], K[:n], V[:n], 1 / math.sqrt(16))
+                assert np.allclose(out[b, i, hq], o, rtol=0, atol=1e-12)
+                assert abs(lse[b, i, hq] - l) < 1e-12
+    # one query token is the plain decode step
+    o1, l1 = O.decode_attention_multi(q[:, -1:], caches)
+    o2, l2 = O.decode_attention(q[:, -1], caches)
+    assert np.array_equal(o1[:, 0], o2) and np.array_equal(l1[:, 0], l2)
+
+
 def test_attention_single_token_and_uniform():
     spec = O.Spec("int4", d=8, G=4, Gv=8, R=4, S=0)
     k = np.array([[1, -2, 0.5, 0, 3, 1, 1, -1]], F32)
