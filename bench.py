@@ -97,7 +97,7 @@ def step_bytes(w, lens_after, n_app):
         for T in lens_after:
             total += attention_bytes(fmt, int(T), w.num_kv_heads)
             total += append_bytes(fmt, int(T) - n_app, n_app, w.num_kv_heads)
-        B = len(lens_after)
+        B = len(lens_after) * w.n_query    # query rows
         total += B * w.num_q_heads * 128 * 2  # q
         total += B * w.num_q_heads * 128 * 2  # out (bf16)
         total += B * w.num_q_heads * 4        # lse
@@ -255,9 +255,11 @@ class Layer:
                 self.v_new[b] = v[0, :, Tb:Tb + n_app]
                 del k, v
         self.q = I.device_q_bf16(w, l, dev, batch=B, seed_offset=seed_offset)
-        self.out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-        self.wsb = kvq.decode_workspace_size(self.cfg, B, Hq)
+        self.nq = w.n_query
+        qrows = (B, Hq) if self.nq == 1 else (B, self.nq, Hq)
+        self.out = torch.empty(qrows + (128,), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(qrows, dtype=torch.float32, device=dev)
+        self.wsb = kvq.decode_workspace_size_multi(self.cfg, B, self.nq, Hq)
         self.ws = torch.zeros(self.wsb, dtype=torch.uint8, device=dev)
         self.struct = self.cache.struct()
         self.scale = 1.0 / math.sqrt(128)
@@ -273,8 +275,13 @@ class Layer:
 
     def decode(self, stream=None):
         # one launch: split pass with the log-sum-exp merge fused in (last CTA per pair)
-        self.kvq.decode_attention(self.cfg, self.struct, self.q, self.Hq, self.lens_after, self.B, self.scale,
-                                  self.out, True, self.lse, self.ws, self.wsb, self.status, stream)
+        if self.nq == 1:
+            self.kvq.decode_attention(self.cfg, self.struct, self.q, self.Hq, self.lens_after, self.B, self.scale,
+                                      self.out, True, self.lse, self.ws, self.wsb, self.status, stream)
+        else:  # the last nq appended tokens' queries, causal among them
+            self.kvq.decode_attention_multi(self.cfg, self.struct, self.q, self.nq, self.Hq, self.lens_after, self.B,
+                                            self.scale, self.out, True, self.lse, self.ws, self.wsb, self.status,
+                                            stream)
 
 
 def count_launches(w):
@@ -418,7 +425,7 @@ def run_gpu(args, w, rank, world):
                 replicas=replicas, e2e_ms=e_ms, h2d=h2d, d2h=d2h, clocks=clocks, wall_ms=(wall1 - wall0) * 1e3,
                 lens_after=lens_after, n_app=n_app,
                 attn_bytes_first_layer=sum(attention_bytes(w.layer_formats[0], int(T), w.num_kv_heads)
-                                           for T in lens_after) + len(lens_after) * w.num_q_heads * 128 * 2)
+                                           for T in lens_after) + len(lens_after) * w.n_query * w.num_q_heads * 128 * 2)
 
 
 # --------------------------------------------------------------------------- #
@@ -445,21 +452,25 @@ def oracle_items(w):
                 ks = O.fp8_tensor_scale(kf, spec.fmt) if spec.is_fp8 else None
                 vs = O.fp8_tensor_scale(vf, spec.fmt) if spec.is_fp8 else None
                 hc = O.build_head_cache(kf[:T - n_app], vf[:T - n_app], spec, ks, vs)
-                yield (b, h, T, hc, kf[T - n_app:], vf[T - n_app:], q[b, h * w.gqa:(h + 1) * w.gqa])
+                qh = q[b, h * w.gqa:(h + 1) * w.gqa] if w.n_query == 1 else q[b, :, h * w.gqa:(h + 1) * w.gqa]
+                yield (b, h, T, hc, kf[T - n_app:], vf[T - n_app:], qh.reshape(-1, 128))
 
     return O, gen(), n_app
 
 
-def oracle_step(O, items):
-    """One oracle decode step over the sample: append the new tokens, attend for the g heads."""
+def oracle_step(O, items, n_query=1):
+    """One oracle decode step over the sample: append the new tokens, attend for the g heads
+    (of each of the n_query query tokens, over its causal prefix)."""
     import copy
     for (b, h, T, hc, kn, vn, qh) in items:
         c = copy.copy(hc)
         for t in range(len(kn)):
             O.append_token(c, kn[t], vn[t])
         kh, vh = O.dequantized_f64(c)
+        per = qh.shape[0] // n_query  # query heads of the pair (rows: query token major)
         for j in range(qh.shape[0]):
-            O.attend_head(qh[j], kh, vh, 1.0 / math.sqrt(128))
+            n = T - n_query + j // per + 1
+            O.attend_head(qh[j], kh[:n], vh[:n], 1.0 / math.sqrt(128))
 
 
 def sample_bytes(w, items, n_app):
@@ -478,7 +489,7 @@ def cpu_baseline(w, budget_s=12.0):
     done = []
     for it in items:
         t0 = time.perf_counter()
-        oracle_step(O, [it])
+        oracle_step(O, [it], w.n_query)
         dt += time.perf_counter() - t0
         done.append(it)
         if dt > budget_s:
@@ -496,15 +507,15 @@ def run_reference(args, w, rank, world):
     # a step = the oracle over a bounded sample of pairs, sized to ~1 s
     first = next(items)
     t0 = time.perf_counter()
-    oracle_step(O, [first])
+    oracle_step(O, [first], w.n_query)
     per_pair = max(1e-3, time.perf_counter() - t0)
     n = max(1, min(w.batch * w.num_kv_heads, int(1.0 / per_pair)))
     sample = [first] + [it for _, it in zip(range(n - 1), items)]
     for _ in range(args.warmup):
-        oracle_step(O, sample)
+        oracle_step(O, sample, w.n_query)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(O, sample)
+        oracle_step(O, sample, w.n_query)
     dt = (time.perf_counter() - t0) / args.steps
     gbs = sample_bytes(w, sample, n_app) / dt / 1e9
     return gbs, dt, n
@@ -556,7 +567,7 @@ def main():
     config = {"workload": w.name, "layers": len(w.layer_formats), "batch": w.batch, "q_heads": w.num_q_heads,
               "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
               "seq_len": w.seq_len if w.seq_len else f"log-uniform {tuple(w.seq_len_range)}",
-              "formats": sorted({f.fmt for f in w.layer_formats}), "append_tokens_per_step": max(1, w.append_tokens),
+              "formats": sorted({f.fmt for f in w.layer_formats}), "append_tokens_per_step": max(1, w.append_tokens), "query_tokens_per_step": w.n_query,
               "paged": w.paged}
     metric = "effective KV GB/s (quantized decode step)"
 
@@ -589,7 +600,7 @@ def main():
     if kern_gbs is None:
         # multi-layer: bytes of every layer's attention over the mean launch duration
         per_layer = [sum(attention_bytes(f, int(T), w.num_kv_heads) for T in r["lens_after"]) +
-                     len(r["lens_after"]) * w.num_q_heads * 256 for f in w.layer_formats]
+                     len(r["lens_after"]) * w.n_query * w.num_q_heads * 256 for f in w.layer_formats]
         kern_gbs = float(np.mean(per_layer)) / (r["kern_ms"] * 1e-3) / 1e9
     # DRAM bytes per decode launch from an ncu capture, used only while the kernel sources are
     # the ones the capture ran (their hash is recorded beside the figure)

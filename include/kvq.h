@@ -259,6 +259,36 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
                                 uint32_t* dev_status, void* stream);
 
 /*
+ * kvq_decode_attention_multi -- attention of n_query new tokens per sequence
+ * (speculative-decoding verification, chunked prefill) over the quantized
+ * cache in one launch.  Source: [W4KV] "오차가 어디서 만나는가" (the score
+ * formula) applied causally to several query positions; the cache and its
+ * formats as for kvq_decode_attention.
+ *   q         device bf16 [batch][n_query][num_q_heads][d]: query token i of
+ *             sequence b sits at position seq_lens[b] - n_query + i
+ *   seq_lens  device int32 [batch]: tokens in the cache, the n_query new tokens
+ *             included (append them with kvq_quantize_append first)
+ *   out       device [batch][n_query][num_q_heads][d] (fp32 or bf16 as above)
+ *   lse       device f32 [batch][n_query][num_q_heads] or NULL
+ *   workspace at least kvq_decode_workspace_size_multi() bytes, zero-filled
+ *             once before first use (the same arrival counters as above)
+ * Query token i attends to tokens 0 .. seq_lens[b] - n_query + i (causal
+ * among the new tokens); a query with no visible token (seq_lens[b] <
+ * n_query - i) gets out = 0, lse = -inf.  Requires 1 <= n_query and
+ * (num_q_heads / H) * n_query <= 8: the kernel runs the n_query query tokens
+ * of a kv head's query heads as that many tensor-core columns.  n_query = 1 is
+ * kvq_decode_attention.  Errors as for kvq_decode_attention.
+ */
+kvq_status kvq_decode_attention_multi(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                      int32_t n_query, int32_t num_q_heads, const int32_t* seq_lens, int32_t batch,
+                                      float softmax_scale, void* out, int32_t out_bf16, float* lse, void* workspace,
+                                      size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/* Workspace bytes kvq_decode_attention_multi needs (same rules as kvq_decode_workspace_size). */
+kvq_status kvq_decode_workspace_size_multi(const kvq_layer_config* cfg, int32_t batch, int32_t n_query,
+                                           int32_t num_q_heads, size_t* bytes);
+
+/*
  * kvq_decode_partials / kvq_decode_combine -- kvq_decode_attention as two
  * launches (same arguments, same workspace; the counters are not used).
  * kvq_decode_partials runs the split pass: every CTA of the grid reads an equal

@@ -166,24 +166,24 @@ int fixed_smem(int batch, int merge_bytes, int nw) {
   return nw * per_warp + nw / 2 * merge_bytes + (g + 1) * kQRowFloats * 4 + kSegTableBytes + prefix;
 }
 
-cudaError_t occupancy_query(const LayerDesc& L, int g, int smem, int* n) {
+cudaError_t occupancy_query(const LayerDesc& L, int g, int multi, int smem, int* n) {
   switch (kernel_format(L.fmt)) {
-    case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, g, smem, n);
-    case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, g, smem, n);
-    case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, g, smem, n);
-    case KVQ_FMT_FP8_E5M2: return occupancy_decode_fp8_e5m2(L.ngv, g, smem, n);
-    default: return occupancy_decode_fp8(L.ngv, g, smem, n);
+    case KVQ_FMT_INT2: return occupancy_decode_int2(L.ngv, g, multi, smem, n);
+    case KVQ_FMT_INT4: return occupancy_decode_int4(L.ngv, g, multi, smem, n);
+    case KVQ_FMT_INT8: return occupancy_decode_int8(L.ngv, g, multi, smem, n);
+    case KVQ_FMT_FP8_E5M2: return occupancy_decode_fp8_e5m2(L.ngv, g, multi, smem, n);
+    default: return occupancy_decode_fp8(L.ngv, g, multi, smem, n);
   }
 }
 
 // Resident CTAs per SM of the decode kernel for (device, format, Value groups,
 // query column blocks, shared memory), cached: the answer never changes for a
 // given device.
-cudaError_t occupancy(const LayerDesc& L, int g, int smem, int* n) {
+cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
   struct Entry {
     int dev, fmt, ngv, nbq, smem, n;
   };
-  const int nbq = g <= 4 ? 1 : 2;
+  const int nbq = multi ? 3 : (g <= 4 ? 1 : 2);  // 3: the multi-query variant
   static std::mutex mu;
   static Entry cache[256];
   static int used = 0;
@@ -199,7 +199,7 @@ cudaError_t occupancy(const LayerDesc& L, int g, int smem, int* n) {
         return cudaSuccess;
       }
   }
-  e = occupancy_query(L, g, smem, n);
+  e = occupancy_query(L, g, multi, smem, n);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (used < 256) cache[used++] = Entry{dev, L.fmt, L.ngv, nbq, smem, *n};
@@ -215,9 +215,9 @@ struct DecodeGeom {
 // counter, so all of them finish together), two stages per warp (one being
 // computed on, one in flight) of the largest size among about 8, 6, 4 and 2 KB
 // that fits the shared memory.
-kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) {
+kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, int multi = 0) {
   const int wsc = merge_bytes_of(L, g);
-  const int nw = decode_warps(kernel_format(L.fmt), g);
+  const int nw = decode_warps(kernel_format(L.fmt), multi ? kMaxGqa : g);  // multi-query: two column blocks
   const int fixed = fixed_smem(batch, wsc, nw);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -238,7 +238,7 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G) 
     break;
   }
   if (!found) return KVQ_ERR_UNSUPPORTED;
-  if (occupancy(L, g, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (occupancy(L, g, multi, smem, &per_sm) != cudaSuccess) return KVQ_ERR_CUDA;
   if (per_sm < 1) return KVQ_ERR_UNSUPPORTED;
   G->smem = smem;
   G->merge_bytes = wsc;
@@ -339,6 +339,20 @@ kvq_status kvq_decode_workspace_size(const kvq_layer_config* cfg, int32_t batch,
   return KVQ_OK;
 }
 
+kvq_status kvq_decode_workspace_size_multi(const kvq_layer_config* cfg, int32_t batch, int32_t n_query,
+                                           int32_t num_q_heads, size_t* bytes) {
+  LayerDesc L;
+  kvq_status st = make_desc(cfg, &L);
+  if (st != KVQ_OK) return st;
+  if (!bytes || batch < 0 || batch > kMaxBatch || n_query < 1 || num_q_heads < L.H || num_q_heads % L.H != 0 ||
+      num_q_heads / L.H * n_query > kMaxGqa)
+    return KVQ_ERR_INVALID_ARG;
+  DecodeGeom G;
+  if ((st = decode_geometry(L, batch, num_q_heads / L.H * n_query, &G, n_query > 1)) != KVQ_OK) return st;
+  *bytes = G.ws_bytes;
+  return KVQ_OK;
+}
+
 }  // extern "C"
 
 namespace kvq {
@@ -356,17 +370,19 @@ kvq_status check_decode_args(const kvq_layer_config* cfg, int32_t num_q_heads, i
 kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
                                 int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
                                 void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t s,
-                                void* out = nullptr, int32_t out_bf16 = 0, float* lse = nullptr) {
+                                void* out = nullptr, int32_t out_bf16 = 0, float* lse = nullptr,
+                                int32_t n_query = 1) {
   LayerDesc L;
   kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
+  if (n_query < 1 || num_q_heads / L.H * n_query > kMaxGqa) return KVQ_ERR_INVALID_ARG;
   if ((st = check_cache(L, cache)) != KVQ_OK) return st;
   if (batch == 0) return KVQ_OK;
   if (!q || !seq_lens || !workspace || !aligned16(workspace) || !(softmax_scale == softmax_scale))
     return KVQ_ERR_INVALID_ARG;
-  const int g = num_q_heads / L.H;
+  const int g = num_q_heads / L.H * n_query;  // query columns per kv head
   DecodeGeom G;
-  if ((st = decode_geometry(L, batch, g, &G)) != KVQ_OK) return st;
+  if ((st = decode_geometry(L, batch, g, &G, n_query > 1)) != KVQ_OK) return st;
   if (workspace_bytes < G.ws_bytes) return KVQ_ERR_WORKSPACE;
   DecodeParams p;
   p.L = L;
@@ -374,6 +390,8 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.q = q;
   p.Hq = num_q_heads;
   p.g = g;
+  p.gh = num_q_heads / L.H;
+  p.n_query = n_query;
   p.batch = batch;
   p.seq_lens = seq_lens;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -468,6 +486,20 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
   // one launch: the last CTA to finish each (sequence, kv head) merges its partials
   return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
                               workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), out, out_bf16, lse);
+}
+
+kvq_status kvq_decode_attention_multi(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                      int32_t n_query, int32_t num_q_heads, const int32_t* seq_lens, int32_t batch,
+                                      float softmax_scale, void* out, int32_t out_bf16, float* lse, void* workspace,
+                                      size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+  LayerDesc L;
+  kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
+  if (st != KVQ_OK) return st;
+  if (out_bf16 != 0 && out_bf16 != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch > 0 && !out) return KVQ_ERR_INVALID_ARG;
+  return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
+                              workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), out, out_bf16, lse,
+                              n_query);
 }
 
 kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const int32_t* seq_lens,

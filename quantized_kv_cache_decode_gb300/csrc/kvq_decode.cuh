@@ -567,12 +567,23 @@ __device__ __forceinline__ void bf16_pv(const uint8_t* stg, int lane, const floa
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-// final output of (sequence b, query head hq), channel c; l2 = log2-domain log-sum-exp
-__device__ __forceinline__ void write_out(const DecodeParams& p, int b, int hq, int c, float o, float l2) {
-  const long long oi = ((long long)b * p.Hq + hq) * 128 + c;
+// Query columns of a kv head h: column j is query token j / gh (of n_query per
+// sequence) of query head h * gh + j % gh.  Its row in q, out and lse
+// ([B][n_query][Hq]) is b * n_query * Hq + (j / gh) * Hq + h * gh + j % gh.
+__device__ __forceinline__ long long query_row(const DecodeParams& p, int b, int h, int j) {
+  const int m = j / p.gh, hr = j - m * p.gh;
+  return ((long long)b * p.n_query + m) * p.Hq + h * p.gh + hr;
+}
+
+// final output of row `row` of out / lse, channel c; l2 = log2-domain log-sum-exp
+__device__ __forceinline__ void write_row(const DecodeParams& p, long long row, int c, float o, float l2) {
+  const long long oi = row * 128 + c;
   if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
   else reinterpret_cast<float*>(p.out)[oi] = o;
-  if (p.lse && c == 0) p.lse[(long long)b * p.Hq + hq] = l2 * 0.69314718055994531f;
+  if (p.lse && c == 0) p.lse[row] = l2 * 0.69314718055994531f;
+}
+__device__ __forceinline__ void write_out(const DecodeParams& p, int b, int h, int j, int c, float o, float l2) {
+  write_row(p, query_row(p, b, h, j), c, o, l2);
 }
 
 // CTAs c in [c_lo, c_hi] whose unit range [floor(cU/C), floor((c+1)U/C)) is not
@@ -650,8 +661,10 @@ static_assert(sizeof(SlotTag) == 20, "the host reserves 20 bytes per slot tag");
 static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment record");
 
 // BF: the layer may have bf16 tiles (sink or residual tokens); the variant without
-// them (FP8 layers with no sink tokens) carries no bf16-tile code at all.
-template <int FMT, int NGV, int NBQ, bool BF>
+// them (FP8 layers with no sink tokens) carries no bf16-tile code at all.  MQ:
+// several query tokens per sequence (causal limits per column); only that
+// variant carries the limit checks.
+template <int FMT, int NGV, int NBQ, bool BF, bool MQ>
 __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
   constexpr int NW = DecodeWarps<FMT, NBQ>::kNW;
@@ -740,7 +753,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
     // sequences without tokens belong to no CTA's range: out = 0, lse = -inf
     for (int b = blockIdx.x; b < B; b += gridDim.x)
       if (prefix[b + 1] == prefix[b])
-        for (int i = tid; i < p.Hq * 128; i += NT) write_out(p, b, i >> 7, i & 127, 0.f, -INFINITY);
+        for (int i = tid; i < p.n_query * p.Hq * 128; i += NT)
+          write_row(p, (long long)b * p.n_query * p.Hq + (i >> 7), i & 127, 0.f, -INFINITY);
   }
   const long long st = (long long)blockIdx.x * U / C;
   const long long en = (long long)(blockIdx.x + 1) * U / C;
@@ -769,7 +783,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
     for (int i = tid; i < (g + 1) * 128; i += NT) {
       const int hr = i >> 7, c = i & 127;
       float v = 0.f;
-      if (hr < g) v = __bfloat162float(qg[((long long)sg.b * p.Hq + sg.h * g + hr) * 128 + c]);
+      if (hr < g) v = __bfloat162float(qg[query_row(p, sg.b, sg.h, hr) * 128 + c]);
       q_s[hr * kQRow + c] = v;
     }
   };
@@ -1023,7 +1037,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
 #pragma unroll
       for (int k = 0; k < kQPer; ++k) {
         const int i = tid + k * NT, hr = i >> 7, c = i & 127;
-        qpre[k] = (i < 8 * 128 && hr < g) ? qraw[((long long)s0.b * p.Hq + s0.h * g + hr) * 128 + c] : 0;
+        qpre[k] = (i < 8 * 128 && hr < g) ? qraw[query_row(p, s0.b, s0.h, hr) * 128 + c] : 0;
       }
     }
     pump();
@@ -1055,6 +1069,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         }
       }
       float sig_bf[NBQ][2];  // scores of a bf16 tile between its K and V stages
+      // several query tokens per sequence: column 4b + q (query token (4b + q) / gh) sees the
+      // tokens t <= T - n_query + (4b + q) / gh (causal: where that query token sits); the
+      // limit is recomputed where it is needed, so one-query decode keeps no registers for it
+      auto col_limit = [&](int b) { return toks[sg.b] - p.n_query + (4 * b + q) / p.gh; };
 
       // this warp's stages of segment s, in the order its producer issued them
       while (true) {
@@ -1099,6 +1117,16 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           bool vpart = tg.kind == 2;
           if (tg.kind == 1) {
             bf16_qk<NBQ>(stg, q_s, lane, r, q, g, rows, p.scale_log2, sig_bf);
+            if (MQ && p.n_query > 1) {  // bf16 list index -> token: sinks first, then the residual window after Q_n
+              const int x0 = 16 * tg.a + r, x1 = x0 + 8;
+              const int t0 = x0 + (x0 >= sg.n_sink ? sg.qn : 0), t1 = x1 + (x1 >= sg.n_sink ? sg.qn : 0);
+#pragma unroll
+              for (int b = 0; b < NBQ; ++b) {
+                const int lim = col_limit(b);
+                if (t0 > lim) sig_bf[b][0] = -INFINITY;
+                if (t1 > lim) sig_bf[b][1] = -INFINITY;
+              }
+            }
             vpart = bfj;
             vst = stg + kBfHalf;
           }
@@ -1148,6 +1176,15 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
               const bool hv = 4 * b + q < g;
               sig[b][0] = (hv && r < tok_valid) ? fmaf(d[b][0], kfac[b], cterm[b]) : -INFINITY;
               sig[b][1] = (hv && r + 8 < tok_valid) ? fmaf(d[b][1], kfac[b], cterm[b]) : -INFINITY;
+            }
+            if (MQ && p.n_query > 1) {
+              const int t0 = L.S + 16 * i + r;  // token of row r (quantized token x = t - S)
+#pragma unroll
+              for (int b = 0; b < NBQ; ++b) {
+                const int lim = col_limit(b);
+                if (t0 > lim) sig[b][0] = -INFINITY;
+                if (t0 + 8 > lim) sig[b][1] = -INFINITY;
+              }
             }
             const float* vsp = reinterpret_cast<const float*>(tile + 2 * F::kTile);  // INT: Value scales [16][NGV]
             const float* vzp = vsp + 16 * NGV;                                         // INT: Value zero-points
@@ -1330,7 +1367,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           const float o = empty ? 0.f : O / Lsum;
           const float l2 = empty ? -INFINITY : M + log2f(Lsum);
           if (whole) {
-            write_out(p, b, h * g + hr, c, o, l2);
+            write_out(p, b, h, hr, c, o, l2);
           } else {
             p.ws_o[(slot * g + hr) * 128 + c] = o;
             if (c == 0) p.ws_lse[slot * g + hr] = l2;
@@ -1380,7 +1417,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
                     }
                 }
                 const bool empty = !(Lsum > 0.f);
-                write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+                write_out(p, b, h, hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
               }
             } else if (na <= kMaxParts) {
               // every partial's lse at once: row hr, column k
@@ -1418,7 +1455,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
                       if (k0 + j < na) O = fmaf(wr[k0 + j], v[j], O);
                   }
                 const bool empty = !(Lsum > 0.f);
-                write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+                write_out(p, b, h, hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
               }
             } else {
               // more partials than the list holds (tiny per-CTA ranges): walk [c_lo, c_hi]
@@ -1436,7 +1473,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
                   }
                 }
                 const bool empty = !(Lsum > 0.f);
-                write_out(p, b, h * g + hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
+                write_out(p, b, h, hr, c, empty ? 0.f : O / Lsum, empty ? -INFINITY : M + log2f(Lsum));
               }
             }
           }
@@ -1461,7 +1498,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, int NBQ, bool BF>
+template <int FMT, int NGV, int NBQ, bool BF, bool MQ>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1470,44 +1507,47 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, NBQ, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, NBQ, BF, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-template <int FMT, int NGV, int NBQ, bool BF>
+template <int FMT, int NGV, int NBQ, bool BF, bool MQ>
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, NBQ, BF>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, NBQ, BF, MQ>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, NBQ, BF><<<p.num_ctas, DecodeWarps<FMT, NBQ>::kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV, NBQ, BF, MQ><<<p.num_ctas, DecodeWarps<FMT, NBQ>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-// One column block for up to 4 query heads per kv head, two for 5..8; FP8 layers
-// without sink tokens (no bf16 tiles) take the variant without the bf16 path.
+// One column block for up to 4 query columns per kv head, two for 5..8; FP8 layers
+// without sink tokens (no bf16 tiles) take the variant without the bf16 path;
+// several query tokens per sequence take the multi-query variant (two blocks).
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
+  if (p.n_query > 1) return launch_variant<FMT, NGV, 2, true, true>(p, smem, stream);
   if constexpr (FT<FMT>::kFp8) {
     if (p.L.S == 0)
-      return p.g <= 4 ? launch_variant<FMT, NGV, 1, false>(p, smem, stream)
-                      : launch_variant<FMT, NGV, 2, false>(p, smem, stream);
+      return p.g <= 4 ? launch_variant<FMT, NGV, 1, false, false>(p, smem, stream)
+                      : launch_variant<FMT, NGV, 2, false, false>(p, smem, stream);
   }
-  return p.g <= 4 ? launch_variant<FMT, NGV, 1, true>(p, smem, stream)
-                  : launch_variant<FMT, NGV, 2, true>(p, smem, stream);
+  return p.g <= 4 ? launch_variant<FMT, NGV, 1, true, false>(p, smem, stream)
+                  : launch_variant<FMT, NGV, 2, true, false>(p, smem, stream);
 }
 
-// Resident CTAs per SM (the variant with the bf16 path: the larger of the two).
+// Resident CTAs per SM (for one query token: the variant with the bf16 path, the
+// larger of the two; several query tokens: the multi-query variant).
+template <int FMT, int NGV, int NBQ, bool MQ>
+cudaError_t occupancy_variant(int smem, int* n) {
+  cudaError_t e = ensure_smem_attr<FMT, NGV, NBQ, true, MQ>(smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, NBQ, true, MQ>,
+                                                       DecodeWarps<FMT, NBQ>::kThreads, smem);
+}
 template <int FMT, int NGV>
-cudaError_t occupancy_t(int g, int smem, int* n) {
-  cudaError_t e;
-  if (g <= 4) {
-    if ((e = ensure_smem_attr<FMT, NGV, 1, true>(smem)) != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 1, true>,
-                                                         DecodeWarps<FMT, 1>::kThreads, smem);
-  }
-  if ((e = ensure_smem_attr<FMT, NGV, 2, true>(smem)) != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, 2, true>,
-                                                       DecodeWarps<FMT, 2>::kThreads, smem);
+cudaError_t occupancy_t(int g, int multi, int smem, int* n) {
+  if (multi) return occupancy_variant<FMT, NGV, 2, true>(smem, n);
+  return g <= 4 ? occupancy_variant<FMT, NGV, 1, false>(smem, n) : occupancy_variant<FMT, NGV, 2, false>(smem, n);
 }
 
 }  // namespace kvq

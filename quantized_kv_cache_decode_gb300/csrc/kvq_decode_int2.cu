@@ -14,12 +14,12 @@ cudaError_t launch_decode_int2(const DecodeParams& p, int smem, cudaStream_t s) 
   }
 }
 
-cudaError_t occupancy_decode_int2(int ngv, int g, int smem, int* n) {
+cudaError_t occupancy_decode_int2(int ngv, int g, int multi, int smem, int* n) {
   switch (ngv) {
-    case 1: return occupancy_t<2, 1>(g, smem, n);
-    case 2: return occupancy_t<2, 2>(g, smem, n);
-    case 4: return occupancy_t<2, 4>(g, smem, n);
-    case 8: return occupancy_t<2, 8>(g, smem, n);
+    case 1: return occupancy_t<2, 1>(g, multi, smem, n);
+    case 2: return occupancy_t<2, 2>(g, multi, smem, n);
+    case 4: return occupancy_t<2, 4>(g, multi, smem, n);
+    case 8: return occupancy_t<2, 8>(g, multi, smem, n);
     default: return cudaErrorInvalidValue;
   }
 }

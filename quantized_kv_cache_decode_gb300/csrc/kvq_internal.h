@@ -56,7 +56,9 @@ struct DecodeParams {
   LayerDesc L;
   CachePtrs C;
   const void* q;  // bf16 [B][Hq][d]
-  int Hq, g, batch;
+  int Hq, g, batch;  // g: query columns per kv head = gh * n_query
+  int gh;            // query heads per kv head
+  int n_query;       // query tokens per sequence (1: plain decode)
   const int32_t* seq_lens;
   float scale_log2;  // softmax_scale * log2(e)
   int num_ctas;      // CTAs of the decode grid (partial slot space = num_ctas + batch*H)
@@ -120,11 +122,12 @@ cudaError_t launch_decode_int4(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_int8(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_fp8_e5m2(const DecodeParams& p, int smem, cudaStream_t s);
-cudaError_t occupancy_decode_int2(int ngv, int g, int smem, int* n);
-cudaError_t occupancy_decode_int4(int ngv, int g, int smem, int* n);
-cudaError_t occupancy_decode_int8(int ngv, int g, int smem, int* n);
-cudaError_t occupancy_decode_fp8(int ngv, int g, int smem, int* n);
-cudaError_t occupancy_decode_fp8_e5m2(int ngv, int g, int smem, int* n);
+// multi: the multi-query variant (several query tokens per sequence, two column blocks)
+cudaError_t occupancy_decode_int2(int ngv, int g, int multi, int smem, int* n);
+cudaError_t occupancy_decode_int4(int ngv, int g, int multi, int smem, int* n);
+cudaError_t occupancy_decode_int8(int ngv, int g, int multi, int smem, int* n);
+cudaError_t occupancy_decode_fp8(int ngv, int g, int multi, int smem, int* n);
+cudaError_t occupancy_decode_fp8_e5m2(int ngv, int g, int multi, int smem, int* n);
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 // scale = amax / fmax (1 when amax == 0), fmax the format's largest finite value

@@ -86,6 +86,7 @@ class Workload:
     append_tokens: int = 0            # tokens appended by the timed decode step
     seq_len_range: Optional[Sequence[int]] = None  # (lo, hi) log-uniform, paged workload
     seed: int = 0
+    n_query: int = 1                  # query tokens per sequence per step (the last n_query appended tokens)
 
     @property
     def gqa(self) -> int:
@@ -117,6 +118,14 @@ def llama3_8b_bf16_skip() -> Workload:
                     seed=1007)
 
 
+def llama3_8b_fp8_2q() -> Workload:
+    """The FP8 E4M3 8B layer verifying 2 speculative tokens per sequence: both are appended, and the
+    2 x 4 query heads of each kv head attend causally in one launch."""
+    fmt = LayerFormat("fp8_e4m3", G=1, Gv=128, R=0, S=0)
+    return Workload("llama3_8b_fp8_e4m3_2q", 1, 16, 32, 8, 128, 8192, [fmt], 10, 10, 8.0, "per_layer",
+                    append_tokens=2, seed=1008, n_query=2)
+
+
 def llama3_70b_int4() -> Workload:
     """Llama-3-70B-shaped decode over 80 layers, KIVI INT4 (G=128, Gv=128, R=128)."""
     fmt = LayerFormat("int4", G=128, Gv=128, R=128, S=0)
@@ -145,6 +154,7 @@ WORKLOADS = {
     "llama3_8b_fp8_e4m3": llama3_8b_fp8,
     "llama3_8b_fp8_e5m2": llama3_8b_fp8_e5m2,
     "llama3_8b_bf16_skip_layer": llama3_8b_bf16_skip,
+    "llama3_8b_fp8_e4m3_2q": llama3_8b_fp8_2q,
     "llama3_70b_kivi_int4_80l": llama3_70b_int4,
     "llama2_7b_kivi2_int2_32k": llama2_7b_int2,
     "paged_mixed_int8_int4_64l": paged_mixed,
@@ -213,7 +223,8 @@ def kv_bf16(w: Workload, layer: int, b: int, h: int, T: int) -> (np.ndarray, np.
 def q_bf16(w: Workload, layer: int) -> np.ndarray:
     """Decode queries of one layer: bf16 bits [B, Hq, d]."""
     rng = _stream(w.seed, f"q-l{layer}")
-    q = rng.standard_normal((w.batch, w.num_q_heads, w.head_dim), dtype=np.float32)
+    shape = (w.batch, w.num_q_heads, w.head_dim) if w.n_query == 1 else (w.batch, w.n_query, w.num_q_heads, w.head_dim)
+    q = rng.standard_normal(shape, dtype=np.float32)
     return f32_to_bf16_bits(q)
 
 
@@ -261,10 +272,11 @@ def device_kv_bf16(w: Workload, layer: int, T: int, device, batch: Optional[int]
 
 
 def device_q_bf16(w: Workload, layer: int, device, batch: Optional[int] = None, seed_offset: int = 0):
-    """Decode queries of one layer: torch bf16 [B, Hq, d] on ``device`` (seeded)."""
+    """Decode queries of one layer: torch bf16 [B, Hq, d] (or [B, n_query, Hq, d]) on ``device`` (seeded)."""
     import torch
     B = w.batch if batch is None else batch
     gen = torch.Generator(device=device)
     gen.manual_seed(w.seed * 100019 + layer * 104729 + seed_offset + 1)
-    q = torch.randn((B, w.num_q_heads, w.head_dim), generator=gen, device=device, dtype=torch.float32)
+    shape = (B, w.num_q_heads, w.head_dim) if w.n_query == 1 else (B, w.n_query, w.num_q_heads, w.head_dim)
+    q = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
     return q.to(torch.bfloat16)

@@ -59,6 +59,9 @@ _lib.kvq_quantize_append.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_vp
 _lib.kvq_decode_workspace_size.argtypes = [_P(LayerConfig), c_i32, c_i32, _P(c_sz)]
 _lib.kvq_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
                                       c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
+_lib.kvq_decode_attention_multi.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_i32, c_vp, c_i32,
+                                            ctypes.c_float, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
+_lib.kvq_decode_workspace_size_multi.argtypes = [_P(LayerConfig), c_i32, c_i32, c_i32, _P(c_sz)]
 _lib.kvq_decode_partials.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
                                      c_vp, c_sz, c_vp, c_vp]
 _lib.kvq_decode_combine.argtypes = [_P(LayerConfig), c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]
@@ -70,6 +73,7 @@ _lib.kvq_status_string.restype = ctypes.c_char_p
 for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_fp8_calibrate_format", "kvq_quantize_append",
             "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize",
+            "kvq_decode_attention_multi", "kvq_decode_workspace_size_multi",
             "kvq_decode_attention_static_scratch"):
     getattr(_lib, _fn).restype = c_i32
 
@@ -150,6 +154,22 @@ def decode_attention(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, s
            _lib.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads, _ptr(seq_lens),
                                      batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse), _ptr(workspace),
                                      workspace_bytes, _ptr(dev_status), _stream_ptr(stream)))
+
+
+def decode_workspace_size_multi(cfg: LayerConfig, batch: int, n_query: int, num_q_heads: int) -> int:
+    out = c_sz(0)
+    _check("kvq_decode_workspace_size_multi",
+           _lib.kvq_decode_workspace_size_multi(ctypes.byref(cfg), batch, n_query, num_q_heads, ctypes.byref(out)))
+    return int(out.value)
+
+
+def decode_attention_multi(cfg: LayerConfig, cache: LayerCache, q, n_query: int, num_q_heads: int, seq_lens,
+                           batch: int, softmax_scale: float, out, out_bf16: bool, lse, workspace, workspace_bytes: int,
+                           dev_status=None, stream=None) -> None:
+    _check("kvq_decode_attention_multi",
+           _lib.kvq_decode_attention_multi(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), n_query, num_q_heads,
+                                           _ptr(seq_lens), batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse),
+                                           _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream_ptr(stream)))
 
 
 def decode_partials(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, seq_lens, batch: int,

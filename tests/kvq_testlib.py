@@ -167,6 +167,21 @@ class GpuLayer:
         torch.cuda.synchronize()
         return out, lse
 
+    def decode_multi(self, q_bits: np.ndarray, out_bf16: bool = False, scale=None):
+        """q_bits [B, M, Hq, d]: the last M cached tokens' queries, attending causally."""
+        torch = self.torch
+        B, M, Hq, _ = q_bits.shape
+        qd = torch.from_numpy(np.ascontiguousarray(q_bits).astype(np.int16)).to(self.device)
+        out = torch.zeros((B, M, Hq, 128), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=self.device)
+        lse = torch.zeros((B, M, Hq), dtype=torch.float32, device=self.device)
+        wsb = self.kvq.decode_workspace_size_multi(self.cfg, B, M, Hq)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        sc = 1.0 / math.sqrt(128) if scale is None else scale
+        self.kvq.decode_attention_multi(self.cfg, self.layer.struct(), qd, M, Hq, self.seq_lens_dev(), B, sc, out,
+                                        out_bf16, lse, ws, wsb, self.status)
+        torch.cuda.synchronize()
+        return out, lse
+
     def dequantize(self, max_tokens: int, lens=None):
         torch = self.torch
         ko = torch.full((self.B, self.H, max_tokens, 128), 7.0, dtype=torch.float32, device=self.device)

@@ -122,6 +122,36 @@ def test_parity(case):
     assert gl.status_value() == 0
 
 
+MULTI = [
+    # fmt, H, query heads per kv head, query tokens M, lens, G, Gv, R, S, paged
+    ("int4", 2, 4, 2, [300, 1, 17, 64], 16, 128, 32, 1, False),
+    ("fp8_e4m3", 2, 2, 4, [500, 3, 48, 1000], 1, 128, 0, 0, False),
+    ("int8", 1, 1, 8, [250, 7, 129], 16, 64, 16, 0, True),
+    ("bf16", 2, 4, 2, [333, 2], 0, 0, 0, 1, False),
+    ("int2", 2, 3, 2, [200, 40], 32, 32, 64, 0, False),
+    ("fp8_e5m2", 1, 1, 3, [70, 2], 1, 128, 0, 1, True),
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[f"{c[0]}-H{c[1]}g{c[2]}M{c[3]}{'-paged' if c[9] else ''}" for c in MULTI])
+def test_multi_query_parity(case):
+    # M query tokens per sequence (the cache's last M tokens), each attending causally
+    fmt, H, gh, M, lens, G, Gv, R, S, paged = case
+    seed = abs(hash(str(case))) % 10000
+    gl, caches, _ = build(fmt, H, gh, lens, G, Gv, R, S, paged, seed)
+    q = I.random_bf16(seed * 3 + 1, (len(lens), M, H * gh, 128))
+    out_ref, lse_ref = O.decode_attention_multi(O.bf16_to_f32(q), caches)
+    out, lse = gl.decode_multi(q)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+    out16, lse16 = gl.decode_multi(q, out_bf16=True)
+    assert torch.equal(out16, out.to(torch.bfloat16)) and torch.equal(lse16, lse)
+    # the last query token alone is the plain decode step, bit for bit
+    o1, l1 = gl.decode(np.ascontiguousarray(q[:, -1]))
+    o2, l2 = gl.decode_multi(np.ascontiguousarray(q[:, -1:]))
+    assert torch.equal(o1, o2[:, 0]) and torch.equal(l1, l2[:, 0])
+    assert gl.status_value() == 0
+
+
 @pytest.mark.parametrize("fmt,G,Gv,R,S", [("int4", 32, 128, 32, 0), ("int2", 32, 32, 64, 1),
                                           ("int8", 16, 64, 16, 2), ("fp8_e4m3", 1, 128, 0, 1),
                                           ("fp8_e5m2", 1, 128, 0, 0), ("bf16", 0, 0, 0, 1)])

@@ -51,10 +51,16 @@ def _check_layer(w, l, pairs, seed_offset=0):
     assert lay.status.item() == 0
     out16 = lay.out.clone()
     # the same cache, fp32 output
-    out32 = torch.empty((lay.B, lay.Hq, 128), dtype=torch.float32, device=DEV)
-    lse32 = torch.empty((lay.B, lay.Hq), dtype=torch.float32, device=DEV)
-    kvq.decode_attention(lay.cfg, lay.struct, lay.q, lay.Hq, lay.lens_after, lay.B, lay.scale, out32, False, lse32,
-                         lay.ws, lay.wsb, lay.status)
+    M = w.n_query
+    rows = (lay.B, lay.Hq) if M == 1 else (lay.B, M, lay.Hq)
+    out32 = torch.empty(rows + (128,), dtype=torch.float32, device=DEV)
+    lse32 = torch.empty(rows, dtype=torch.float32, device=DEV)
+    if M == 1:
+        kvq.decode_attention(lay.cfg, lay.struct, lay.q, lay.Hq, lay.lens_after, lay.B, lay.scale, out32, False,
+                             lse32, lay.ws, lay.wsb, lay.status)
+    else:
+        kvq.decode_attention_multi(lay.cfg, lay.struct, lay.q, M, lay.Hq, lay.lens_after, lay.B, lay.scale, out32,
+                                   False, lse32, lay.ws, lay.wsb, lay.status)
     torch.cuda.synchronize()
     assert torch.equal(out16, out32.to(torch.bfloat16))
     assert torch.equal(lay.lse, lse32)
@@ -93,13 +99,17 @@ def _check_layer(w, l, pairs, seed_offset=0):
         assert np.array_equal(ko[0, h].cpu().numpy().view(np.uint32), kr.view(np.uint32)), (b, h)
         assert np.array_equal(vo[0, h].cpu().numpy().view(np.uint32), vr.view(np.uint32)), (b, h)
         kh, vh = O.dequantized_f64(hc)
-        for j in range(w.gqa):
-            hq = h * w.gqa + j
-            o, ls = O.attend_head(q[b, hq], kh, vh, lay.scale)
-            refs.append(o)
-            olses.append(ls)
-            outs.append(out32[b, hq].cpu().numpy())
-            lses.append(lse32[b, hq].item())
+        for m in range(M):
+            n = T - M + m + 1  # query token m attends to its causal prefix
+            for j in range(w.gqa):
+                hq = h * w.gqa + j
+                qv, ov, lv = (q[b, hq], out32[b, hq], lse32[b, hq]) if M == 1 else \
+                    (q[b, m, hq], out32[b, m, hq], lse32[b, m, hq])
+                o, ls = O.attend_head(qv, kh[:n], vh[:n], lay.scale)
+                refs.append(o)
+                olses.append(ls)
+                outs.append(ov.cpu().numpy())
+                lses.append(lv.item())
     assert lay.status.item() == 0
     TL.check_attention(np.array(outs), np.array(lses), np.array(refs), np.array(olses))
 
@@ -117,6 +127,11 @@ def test_llama3_8b_fp8_sampled():
 def test_llama3_8b_fp8_e5m2_sampled():
     w = I.llama3_8b_fp8_e5m2()
     _check_layer(w, 0, [(0, 0), (8, 2), (15, 7)])
+
+
+def test_llama3_8b_fp8_two_query_tokens_sampled():
+    w = I.llama3_8b_fp8_2q()
+    _check_layer(w, 0, [(0, 0), (5, 1), (15, 7)])
 
 
 def test_llama3_8b_bf16_skip_layer_sampled():
