@@ -1525,12 +1525,14 @@ cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream)
 // several query tokens per sequence take the multi-query variant (two blocks).
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
-  if (p.n_query > 1) return launch_variant<FMT, NGV, 2, true, true>(p, smem, stream);
   if constexpr (FT<FMT>::kFp8) {
-    if (p.L.S == 0)
+    if (p.L.S == 0) {
+      if (p.n_query > 1) return launch_variant<FMT, NGV, 2, false, true>(p, smem, stream);
       return p.g <= 4 ? launch_variant<FMT, NGV, 1, false, false>(p, smem, stream)
                       : launch_variant<FMT, NGV, 2, false, false>(p, smem, stream);
+    }
   }
+  if (p.n_query > 1) return launch_variant<FMT, NGV, 2, true, true>(p, smem, stream);
   return p.g <= 4 ? launch_variant<FMT, NGV, 1, true, false>(p, smem, stream)
                   : launch_variant<FMT, NGV, 2, true, false>(p, smem, stream);
 }
