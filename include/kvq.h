@@ -349,6 +349,26 @@ kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* ca
                           int32_t batch, int32_t max_tokens, float* k_out, float* v_out, uint32_t* dev_status,
                           void* stream);
 
+/*
+ * kvq_lse_merge -- merge attention results computed over disjoint parts of the
+ * same sequences' tokens: the split a sequence-parallel decode makes when one
+ * long sequence's cache is spread over several devices (each part decoded with
+ * kvq_decode_attention and its lse, the results gathered to one device).
+ * Source: [W4KV] "오차가 어디서 만나는가" -- softmax over the union of the
+ * parts, regrouped exactly as lse = log sum_i exp(lse_i) and
+ * out = sum_i exp(lse_i - lse) * o_i.
+ *   o_parts    device f32 [n_parts][rows][128], 16-byte aligned: each part's
+ *              output, normalised by that part's own softmax sum (as
+ *              kvq_decode_attention writes it in fp32)
+ *   lse_parts  device f32 [n_parts][rows], natural log; -inf for a part with no
+ *              tokens (weight 0)
+ *   out        device [rows][128], 16-byte aligned: fp32 (out_bf16 == 0) or
+ *              bf16 (RNE of the fp32 result); lse_out device f32 [rows] or NULL
+ * A row whose parts are all empty gets out = 0, lse = -inf.
+ */
+kvq_status kvq_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t rows, void* out,
+                         int32_t out_bf16, float* lse_out, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvq_status_string(kvq_status status);
 

@@ -526,6 +526,18 @@ kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* ca
   return KVQ_OK;
 }
 
+kvq_status kvq_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t rows, void* out,
+                         int32_t out_bf16, float* lse_out, void* stream) {
+  if (n_parts < 1 || rows < 0 || (out_bf16 != 0 && out_bf16 != 1)) return KVQ_ERR_INVALID_ARG;
+  if (rows == 0) return KVQ_OK;
+  if (rows > ((long long)1 << 40) || !o_parts || !lse_parts || !out || !aligned16(o_parts) || !aligned16(out))
+    return KVQ_ERR_INVALID_ARG;
+  if (launch_lse_merge(o_parts, lse_parts, n_parts, rows, out, out_bf16, lse_out, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
 const char* kvq_status_string(kvq_status status) {
   switch (status) {
     case KVQ_OK: return "KVQ_OK";

@@ -130,6 +130,8 @@ cudaError_t occupancy_decode_fp8(int ngv, int g, int multi, int smem, int* n);
 cudaError_t occupancy_decode_fp8_e5m2(int ngv, int g, int multi, int smem, int* n);
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n_parts, long long rows, void* out,
+                             int out_bf16, float* lse_out, cudaStream_t stream);
 // scale = amax / fmax (1 when amax == 0), fmax the format's largest finite value
 cudaError_t launch_fp8_calibrate(const void* x, size_t n, float fmax, float* scale_out, cudaStream_t stream);
 cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream);

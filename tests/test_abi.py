@@ -92,6 +92,14 @@ def test_calibrate_rejects_non_fp8_formats(kvq):
     assert e.value.status == -1
 
 
+def test_lse_merge_rejects_bad_arguments(kvq):
+    for args in ((16, 16, 0, 4, 16, 0), (16, 16, 2, 4, 16, 2), (0, 16, 2, 4, 16, 0), (16, 16, 2, 4, 8, 0)):
+        o, l, n, rows, out, bf = args
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.lse_merge(o, l, n, rows, out, bf, None, stream=0)
+        assert e.value.status == -1
+
+
 def test_calls_reject_bad_arguments_before_any_launch(kvq):
     cfg = kvq.make_config("int4", 2, 32, 128, 32, 0, capacity_tokens=64)
     cache = kvq.LayerCache()  # all NULL

@@ -152,6 +152,59 @@ def test_multi_query_parity(case):
     assert gl.status_value() == 0
 
 
+@pytest.mark.parametrize("fmt,G,Gv,R,S", [("int4", 32, 128, 32, 1), ("fp8_e4m3", 1, 128, 0, 0), ("bf16", 0, 0, 0, 1),
+                                          ("int2", 16, 32, 16, 0)])
+def test_sequence_split_lse_merge(fmt, G, Gv, R, S):
+    # each sequence's tokens split in two parts held by separate caches (as two devices of a
+    # sequence-parallel decode would hold them; part B has no sink); each part decoded with its
+    # lse, the two merged by kvq_lse_merge == the oracle's attention over all the tokens
+    from quantized_kv_cache_decode_gb300 import kvq
+    H, g = 2, 4
+    la, lb = [700, 33, 200], [301, 64, 0]
+    B, Hq = len(la), H * g
+    kv, q = make_inputs(31, H, g, [a + b for a, b in zip(la, lb)])
+    parts = []
+    for lens, s_sink, off, seed in ((la, S, 0, 3), (lb, 0, 1, 4)):
+        gl = TL.GpuLayer(fmt, H, lens, G, Gv, R, s_sink, seed=seed)
+        sl = [slice(0, la[b]) if off == 0 else slice(la[b], la[b] + lb[b]) for b in range(B)]
+        ks = vs = None
+        if gl.fp8:
+            kall = np.concatenate([kv[b, h][0][sl[b]].reshape(-1) for b in range(B) for h in range(H)])
+            vall = np.concatenate([kv[b, h][1][sl[b]].reshape(-1) for b in range(B) for h in range(H)])
+            gl.calibrate_fp8(kall, vall)
+            ks, vs = O.fp8_tensor_scale(O.bf16_to_f32(kall), fmt), O.fp8_tensor_scale(O.bf16_to_f32(vall), fmt)
+        for b in range(B):
+            if lens[b]:
+                gl.append(b, np.stack([kv[b, h][0][sl[b]] for h in range(H)]),
+                          np.stack([kv[b, h][1][sl[b]] for h in range(H)]), 0)
+        torch.cuda.synchronize()
+        caches = [[O.build_head_cache(O.bf16_to_f32(kv[b, h][0][sl[b]]), O.bf16_to_f32(kv[b, h][1][sl[b]]), gl.spec,
+                                      ks, vs) for h in range(H)] for b in range(B)]
+        o, l = gl.decode(q)
+        assert gl.status_value() == 0
+        parts.append((o, l, caches))
+    o_parts = torch.stack([parts[0][0], parts[1][0]]).contiguous()
+    l_parts = torch.stack([parts[0][1], parts[1][1]]).contiguous()
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    kvq.lse_merge(o_parts, l_parts, 2, B * Hq, out, False, lse)
+    out16 = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    kvq.lse_merge(o_parts, l_parts, 2, B * Hq, out16, True)
+    torch.cuda.synchronize()
+    qf = O.bf16_to_f32(q)
+    ref_o = np.zeros((B, Hq, 128))
+    ref_l = np.zeros((B, Hq))
+    for b in range(B):
+        for h in range(H):
+            ka, va = O.dequantized_f64(parts[0][2][b][h])
+            kb, vb = O.dequantized_f64(parts[1][2][b][h])
+            kh, vh = np.concatenate([ka, kb]), np.concatenate([va, vb])
+            for j in range(g):
+                ref_o[b, h * g + j], ref_l[b, h * g + j] = O.attend_head(qf[b, h * g + j], kh, vh, 1 / math.sqrt(128))
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+    assert torch.equal(out16, out.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("fmt,G,Gv,R,S", [("int4", 32, 128, 32, 0), ("int2", 32, 32, 64, 1),
                                           ("int8", 16, 64, 16, 2), ("fp8_e4m3", 1, 128, 0, 1),
                                           ("fp8_e5m2", 1, 128, 0, 0), ("bf16", 0, 0, 0, 1)])
