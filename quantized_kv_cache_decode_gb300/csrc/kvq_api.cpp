@@ -206,13 +206,28 @@ cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
   return cudaSuccess;
 }
 
+// CTAs of the decode grid.  One per SM, except for layers whose decode is bound by
+// HBM bandwidth alone (FP8 and bf16: a fraction of the SMs already saturates it)
+// when the batch x kv-head pairs split evenly into k pairs per CTA over at least
+// 80 % of the SMs: then every CTA's range is k whole pairs (for equal sequence
+// lengths), so no pair is split and no partial is written, fenced and merged
+// across CTAs.  Measured on GB300 with 128 pairs (B = 16, 8 kv heads, T = 8192):
+// FP8 decode 61.0 -> 52.6 us, bf16 121.2 -> 108.4 us.  The 2/4/8-bit layers
+// are bound by the SMs' instruction issue and keep every SM.
+int grid_ctas(const LayerDesc& L, int batch, int sms) {
+  const long long pairs = (long long)batch * L.H;
+  if (!(L.fp8 || L.bf16) || pairs < 1) return sms;
+  const long long k = (pairs + sms - 1) / sms;  // pairs per CTA
+  if (pairs % k == 0 && (pairs / k) * 5 >= (long long)sms * 4) return (int)(pairs / k);
+  return sms;
+}
+
 struct DecodeGeom {
   int smem, nst, stage_bytes, tps, num_ctas, merge_bytes;
   size_t ws_bytes, off_lse, off_prefix, off_counters;
 };
 
-// Launch shape: one CTA per SM (its warps claim work items from a shared
-// counter, so all of them finish together), two stages per warp (one being
+// Launch shape: one CTA per SM (see grid_ctas), two stages per warp (one being
 // computed on, one in flight) of the largest size among about 8, 6, 4 and 2 KB
 // that fits the shared memory.
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, int multi = 0) {
@@ -245,7 +260,7 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, 
   G->nst = nst;
   G->stage_bytes = sb;
   G->tps = tps;
-  G->num_ctas = sms;  // one per SM
+  G->num_ctas = grid_ctas(L, batch, sms);
   const size_t slots = (size_t)G->num_ctas + (size_t)batch * L.H;
   const size_t o_bytes = slots * g * kHeadDim * sizeof(float);
   const size_t l_bytes = slots * g * sizeof(float);
