@@ -177,6 +177,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// CTAs that share the work units of a decode launch: the grid, or fewer when the
+// units are so few that a CTA would get less than kMinCtaUnits of them (its
+// fixed costs, and the merge of many tiny partials, would outweigh its share);
+// the CTAs beyond that count have empty ranges.  The decode kernel and the
+// two-launch merge both derive it from the unit total U.
+constexpr long long kMinCtaUnits = 16;
+__host__ __device__ __forceinline__ long long working_ctas(long long grid, long long U) {
+  const long long c = U / kMinCtaUnits;
+  return c < 1 ? 1 : (c < grid ? c : grid);
+}
+
 // about one second at GB300 clocks
 constexpr long long kWaitLimitCycles = 2000000000LL;
 

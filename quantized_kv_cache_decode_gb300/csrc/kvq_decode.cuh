@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
   }
 
   const long long U = prefix[B];
-  const long long C = p.num_ctas;
+  const long long C = working_ctas(p.num_ctas, U);
   if (p.fuse) {
     // sequences without tokens belong to no CTA's range: out = 0, lse = -inf
     for (int b = blockIdx.x; b < B; b += gridDim.x)
@@ -756,8 +756,9 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         for (int i = tid; i < p.n_query * p.Hq * 128; i += NT)
           write_row(p, (long long)b * p.n_query * p.Hq + (i >> 7), i & 127, 0.f, -INFINITY);
   }
-  const long long st = (long long)blockIdx.x * U / C;
-  const long long en = (long long)(blockIdx.x + 1) * U / C;
+  // CTAs at or beyond C have nothing to do
+  const long long st = blockIdx.x < C ? (long long)blockIdx.x * U / C : U;
+  const long long en = blockIdx.x < C ? (long long)(blockIdx.x + 1) * U / C : U;
 
   const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q);
   const __nv_bfloat16* sink_k = reinterpret_cast<const __nv_bfloat16*>(p.C.sink_k);
