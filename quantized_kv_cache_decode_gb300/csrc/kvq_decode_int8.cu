@@ -1,8 +1,15 @@
-// Decode-attention instantiations for the 8-bit affine format, one per
-// number of Value groups per token (d / Gv).
+// Decode-attention dispatch for the 8-bit affine format over the number of Value
+// groups per token (d / Gv), and its instantiations for 1 and 2 groups.
 #include "kvq_decode.cuh"
 
 namespace kvq {
+
+// d/Gv = 4 and 8 are instantiated in kvq_decode_int8_wide.cu (a second translation
+// unit, so that the build compiles the two halves in parallel)
+extern template cudaError_t launch_decode_t<8, 4>(const DecodeParams&, int, cudaStream_t);
+extern template cudaError_t launch_decode_t<8, 8>(const DecodeParams&, int, cudaStream_t);
+extern template cudaError_t occupancy_t<8, 4>(int, int, int, int*);
+extern template cudaError_t occupancy_t<8, 8>(int, int, int, int*);
 
 cudaError_t launch_decode_int8(const DecodeParams& p, int smem, cudaStream_t s) {
   switch (p.L.ngv) {
