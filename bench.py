@@ -387,23 +387,43 @@ def run_gpu(args, w, rank, world):
     # ---- end to end through the public API, host buffers, copies inside the timed region ----
     E = args.e2e_steps or K
     rep0 = reps[0]
-    h_q = [lay.q.cpu().pin_memory() for lay in rep0]
-    h_k = [lay.k_new.cpu().pin_memory() for lay in rep0]
-    h_v = [lay.v_new.cpu().pin_memory() for lay in rep0]
-    h_out = [torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory() for lay in rep0]
-    h_lse = [torch.empty(lay.lse.shape, dtype=lay.lse.dtype).pin_memory() for lay in rep0]
-    h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v)
-    d2h = sum(x.numel() * x.element_size() for x in h_out + h_lse)
+
+    def packed(tensors):
+        # one device buffer holding the tensors (256-byte aligned slices); the returned
+        # views replace them, so a step's inputs (outputs) move in one copy per layer
+        sizes = [t.numel() * t.element_size() for t in tensors]
+        offs, o = [], 0
+        for n in sizes:
+            offs.append(o)
+            o += (n + 255) // 256 * 256
+        buf = torch.empty(o, dtype=torch.uint8, device=dev)
+        views = []
+        for t, off, n in zip(tensors, offs, sizes):
+            v = buf[off:off + n].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            views.append(v)
+        return buf, views, sum(sizes)
+
+    d_in, d_out, h_in, h_out = [], [], [], []
+    h2d = d2h = 0
+    for lay in rep0:
+        bi, (lay.q, lay.k_new, lay.v_new), ni = packed([lay.q, lay.k_new, lay.v_new])
+        bo, (lay.out, lay.lse), no = packed([lay.out, lay.lse])
+        d_in.append(bi)
+        d_out.append(bo)
+        h_in.append(bi.cpu().pin_memory())
+        h_out.append(torch.empty(bo.shape, dtype=torch.uint8).pin_memory())
+        h2d += ni
+        d2h += no
 
     def e2e_step():
+        # per layer: the step's q and new K/V from pinned host memory, append + decode,
+        # the output and lse back to pinned host memory
         for j, lay in enumerate(rep0):
-            lay.q.copy_(h_q[j], non_blocking=True)
-            lay.k_new.copy_(h_k[j], non_blocking=True)
-            lay.v_new.copy_(h_v[j], non_blocking=True)
+            d_in[j].copy_(h_in[j], non_blocking=True)
             lay.append()
             lay.decode()
-            h_out[j].copy_(lay.out, non_blocking=True)
-            h_lse[j].copy_(lay.lse, non_blocking=True)
+            h_out[j].copy_(d_out[j], non_blocking=True)
 
     for _ in range(min(3, E)):
         e2e_step()
