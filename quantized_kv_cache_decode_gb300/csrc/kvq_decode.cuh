@@ -1,6 +1,6 @@
 // Fused decode attention over a quantized KV cache (sm_103a).
 //
-// softmax(q K^T / sqrt(d)) V for one new query per head, reading the compressed
+// softmax(q K^T / sqrt(d)) V for the new query (or queries) of each head, reading the compressed
 // cache once ("W4A16 + KV cache quantization combined accuracy", section
 // "오차가 어디서 만나는가"; dequantization fused with the matmuls as "KV Cache
 // Quantization Analysis" section 5 asks, since decode is bound by reading the
@@ -9,10 +9,12 @@
 // Work decomposition.  Every (sequence, kv head) pair is a list of work units:
 // its 16-token bf16 tiles (sink + residual window, charged `bf_weight` units
 // each) followed by its 16-token quantized tiles (1 unit each).  The pairs'
-// lists are concatenated and cut into num_ctas equal ranges, one per CTA (one
-// CTA per SM), so every SM moves the same number of bytes whatever the sequence
-// lengths.  A CTA writes one partial (normalised output + log-sum-exp) per pair
-// it touches; the last CTA to finish a pair merges them.
+// lists are concatenated and cut into equal ranges, one per CTA, so every CTA
+// moves the same number of bytes whatever the sequence lengths.  The grid is one
+// CTA per SM, or for HBM-bound layers one CTA per k whole pairs when that covers
+// most SMs (the host's choice); CTAs past one per kMinCtaUnits units stay idle.
+// A CTA writes one partial (normalised output + log-sum-exp) per pair it shares
+// with another CTA; the last CTA to finish such a pair merges them.
 //
 // Inside a CTA the 12 or 16 warps take a segment's work items (a bf16 tile, or
 // a Key group's quantized tiles) round robin, interleaved over the whole
@@ -47,7 +49,7 @@
 
 namespace kvq {
 
-// Warps per CTA (one CTA per SM): 16 for 2- and 4-bit codes with up to 4 query
+// Warps per CTA (one CTA per SM at most): 16 for 2- and 4-bit codes with up to 4 query
 // heads per kv head (128 registers a thread), else 12 (170 registers);
 // decode_warps() in kvq_internal.h states the same rule for the host.
 template <int FMT, int NBQ>
@@ -318,54 +320,32 @@ __device__ __forceinline__ void p_operand(const float (&pr)[NBQ][NV], int e, int
 // --------------------------------------------------------------------------
 // Lane (r, q), column block b: column r = half (r & 1) of query head
 // 4b + (r >> 1), channels 16s + 4q + e.  q_s holds the g query heads and a zero
-// row g for the columns of absent heads.  x_c = q_c s_c (INT; FP8: s_c = 1),
-// kappa = 16384 / max_c |x_c| of the head, B = hi (r even) or lo (r odd) part of
-// x_c kappa.  kfac / cterm return the score multiplier and the zero-point term
-// (both scaled by kfac0 = log2(e) / sqrt(d) [* FP8 Key scale]) for head 4b + q.
+// row g for the columns of absent heads.  FP8 layers (one build per segment):
+// x_c = q_c, kappa = 16384 / max_c |x_c| of the head, B = hi (r even) or lo
+// (r odd) part of x_c kappa.  kfac / cterm return the score multiplier and the
+// zero-point term (kfac0 = log2(e) / sqrt(d) * the Key scale; no zero-point for
+// FP8) for head 4b + q.
 template <int FMT, int NBQ>
-__device__ __forceinline__ void build_bq(const float* q_s, const float* ks, const float* kz, int r, int q, int g,
-                                         float kfac0, uint32_t (&Bq)[NBQ][8][2], float (&kfac)[NBQ],
-                                         float (&cterm)[NBQ]) {
-  constexpr float kH = (float)FT<FMT>::kHalf;
+__device__ __forceinline__ void build_bq(const float* q_s, int r, int q, int g, float kfac0,
+                                         uint32_t (&Bq)[NBQ][8][2], float (&kfac)[NBQ], float (&cterm)[NBQ]) {
   const bool lo = (r & 1) != 0;
 #pragma unroll
   for (int b = 0; b < NBQ; ++b) {
     const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 4 * q;  // row g is zero
-    float mx = 0.f, cz = 0.f;
+    float mx = 0.f;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
-      if constexpr (FT<FMT>::kInt) {
-        const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
-        const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
-        x.x *= s4.x;
-        x.y *= s4.y;
-        x.z *= s4.z;
-        x.w *= s4.w;
-        cz = fmaf(x.x, kH - z4.x, cz);
-        cz = fmaf(x.y, kH - z4.y, cz);
-        cz = fmaf(x.z, kH - z4.z, cz);
-        cz = fmaf(x.w, kH - z4.w, cz);
-      }
+      const float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
       asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
     }
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    cz += __shfl_xor_sync(kFull, cz, 1);
-    cz += __shfl_xor_sync(kFull, cz, 2);
     float kap = 16384.f / mx;
     if (!(mx > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
-      if constexpr (FT<FMT>::kInt) {
-        const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
-        x.x *= s4.x;
-        x.y *= s4.y;
-        x.z *= s4.z;
-        x.w *= s4.w;
-      }
       x.x *= kap;
       x.y *= kap;
       x.z *= kap;
@@ -381,14 +361,14 @@ __device__ __forceinline__ void build_bq(const float* q_s, const float* ks, cons
       asm volatile("" ::: "memory");
     }
     // to the score layout: head 4b + q is held by the lanes with r = 2q
-    const float kf = kfac0 / kap, ct = kfac0 * cz;
-    kfac[b] = __shfl_sync(kFull, kf, 8 * q);
-    cterm[b] = __shfl_sync(kFull, ct, 8 * q);
+    kfac[b] = __shfl_sync(kFull, kfac0 / kap, 8 * q);
+    cterm[b] = 0.f;
   }
 }
 
-// The same B operand for a Key group of an INT layer, in one pass over the
-// channels: kappa = 16384 / (max_c |q_c| * max_c s_c) bounds |x_c kappa| by
+// The B operand for a Key group of an INT layer, x_c = q_c s_c (s_c: the Key
+// scale of channel c), with the zero-point term sum_c x_c (2^(b-1) - z_c), in one
+// pass over the channels: kappa = 16384 / (max_c |q_c| * max_c s_c) bounds |x_c kappa| by
 // 16384 without first finding max_c |x_c| (qm[b]: the lane's head max |q_c|, per
 // segment).  A smaller kappa than the exact one only moves the hi/lo split: the
 // two f16 terms still hold x_c kappa to about 22 bits, or to the f16 subnormal
@@ -1059,7 +1039,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
       float kfac[NBQ], cterm[NBQ];
       float qm[NBQ];  // INT: the lanes' head max |q_c| (the Key groups' kappa bound)
       if constexpr (F::kFp8) {
-        build_bq<FMT, NBQ>(q_s, nullptr, nullptr, r, q, g, p.scale_log2 * __ldg(p.C.k_tscale), Bq, kfac, cterm);
+        build_bq<FMT, NBQ>(q_s, r, q, g, p.scale_log2 * __ldg(p.C.k_tscale), Bq, kfac, cterm);
       } else {
         head_qmax<NBQ>(q_s, r, q, g, qm);
 #pragma unroll
