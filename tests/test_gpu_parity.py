@@ -69,6 +69,11 @@ def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=Non
 
 CASES = [
     # fmt, H, g, lens, G, Gv, R, S, paged, block
+    # one long sequence over every SM: each pair merges more than 64 partials
+    ("fp8_e4m3", 1, 8, [40000], 1, 128, 0, 1, False, 16),
+    ("int4", 1, 4, [30000], 32, 128, 32, 0, False, 16),
+    # 128 ragged pairs: the pair-aligned FP8 grid with pairs cut across CTAs
+    ("fp8_e4m3", 8, 4, [16 + 37 * i for i in range(16)], 1, 128, 0, 0, False, 16),
     ("int4", 2, 4, [512], 32, 128, 32, 0, False, 16),
     ("int4", 2, 4, [0, 1, 31, 63, 64, 65, 700], 32, 128, 32, 0, False, 16),
     ("int2", 3, 1, [1000, 129, 160, 161, 5], 32, 32, 128, 0, False, 16),
