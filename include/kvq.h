@@ -369,6 +369,23 @@ kvq_status kvq_dequantize(const kvq_layer_config* cfg, const kvq_layer_cache* ca
 kvq_status kvq_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t rows, void* out,
                          int32_t out_bf16, float* lse_out, void* stream);
 
+/*
+ * kvq_selftest_bounded_wait -- self-test of the device error path (no
+ * counterpart in the pages: it exists to show the failure handling works).
+ * Runs kvq_decode_attention (same arguments) with the first bulk copy of one
+ * warp (CTA 0, warp 0) withheld while its stage barrier still expects the bytes,
+ * so that warp's bounded wait (about one second of SM clocks) runs out.  The
+ * launch must then report KVQ_DEV_TIMEOUT in *dev_status (required, not NULL)
+ * and finish (the warp stops issuing copies and drains its own, each wait
+ * bounded); the outputs of the affected pair are not valid.  Zero the workspace
+ * again afterwards, as after any call that reported KVQ_DEV_TIMEOUT.
+ * Contiguous INT and FP8 layers only (KVQ_ERR_UNSUPPORTED otherwise).
+ */
+kvq_status kvq_selftest_bounded_wait(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                     int32_t num_q_heads, const int32_t* seq_lens, int32_t batch,
+                                     float softmax_scale, void* out, int32_t out_bf16, float* lse, void* workspace,
+                                     size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvq_status_string(kvq_status status);
 

@@ -386,7 +386,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
                                 int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
                                 void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t s,
                                 void* out = nullptr, int32_t out_bf16 = 0, float* lse = nullptr,
-                                int32_t n_query = 1) {
+                                int32_t n_query = 1, int32_t withhold_copy = 0) {
   LayerDesc L;
   kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
@@ -425,6 +425,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.ws_prefix = reinterpret_cast<int*>(ws + G.off_prefix);
   p.status = dev_status;
   p.merge_bytes = G.merge_bytes;
+  p.withhold_copy = withhold_copy;
   p.fuse = out != nullptr;
   p.counters = reinterpret_cast<unsigned*>(ws + G.off_counters);
   p.out = out;
@@ -501,6 +502,21 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
   // one launch: the last CTA to finish each (sequence, kv head) merges its partials
   return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
                               workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), out, out_bf16, lse);
+}
+
+kvq_status kvq_selftest_bounded_wait(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,
+                                     int32_t num_q_heads, const int32_t* seq_lens, int32_t batch,
+                                     float softmax_scale, void* out, int32_t out_bf16, float* lse, void* workspace,
+                                     size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+  LayerDesc L;
+  kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
+  if (st != KVQ_OK) return st;
+  if (L.paged || L.bf16) return KVQ_ERR_UNSUPPORTED;
+  if ((out_bf16 != 0 && out_bf16 != 1) || !dev_status) return KVQ_ERR_INVALID_ARG;
+  if (batch > 0 && !out) return KVQ_ERR_INVALID_ARG;
+  return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
+                              workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), out, out_bf16, lse, 1,
+                              1);
 }
 
 kvq_status kvq_decode_attention_multi(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,

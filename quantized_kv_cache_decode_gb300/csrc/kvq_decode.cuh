@@ -946,8 +946,11 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
             const uint8_t* end = base + (long long)l_rec * L.rec_bytes + L.hdr_bytes + (l_pos + 1) * L.tile_bytes;
             const uint32_t len = (uint32_t)(end - start);
             mbar_arrive_expect_tx(bar, len + (hdr0 ? 1024u : 0u));
-            bulk_copy_g2s(smem_addr(dst + (hdr0 ? 1024 : 0)), start, len, bar);
-            if (hdr0) bulk_copy_g2s(smem_addr(dst), rec0, 1024, bar);
+            // (the self-test of the bounded waits withholds CTA 0 / warp 0's first copy)
+            if (!(p.withhold_copy && blockIdx.x == 0 && warp == 0 && n_issued == 0)) {
+              bulk_copy_g2s(smem_addr(dst + (hdr0 ? 1024 : 0)), start, len, bar);
+              if (hdr0) bulk_copy_g2s(smem_addr(dst), rec0, 1024, bar);
+            }
             vm = (1u << n) - 1u;
           } else {
             // records q_rec .. l_rec: present ones are copied, missing ones (bad block) leave holes

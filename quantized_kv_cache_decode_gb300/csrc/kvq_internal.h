@@ -73,6 +73,7 @@ struct DecodeParams {
   int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
   uint32_t* status;
   int merge_bytes;   // bytes of one warp's merge record in shared memory (g heads)
+  int withhold_copy; // self-test only: CTA 0, warp 0 withholds its first bulk copy (its wait must run out)
   // fused combine: the last CTA to finish a (sequence, kv head) pair merges its partials
   int fuse;
   unsigned* counters;  // [batch * H] arrival counters, zero between calls

@@ -62,6 +62,8 @@ _lib.kvq_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i
 _lib.kvq_decode_attention_multi.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_i32, c_vp, c_i32,
                                             ctypes.c_float, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
 _lib.kvq_decode_workspace_size_multi.argtypes = [_P(LayerConfig), c_i32, c_i32, c_i32, _P(c_sz)]
+_lib.kvq_selftest_bounded_wait.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
+                                           c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
 _lib.kvq_lse_merge.argtypes = [c_vp, c_vp, c_i32, ctypes.c_int64, c_vp, c_i32, c_vp, c_vp]
 _lib.kvq_decode_partials.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
                                      c_vp, c_sz, c_vp, c_vp]
@@ -75,6 +77,7 @@ for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_fp8_calibrate_format",
             "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize",
             "kvq_decode_attention_multi", "kvq_decode_workspace_size_multi", "kvq_lse_merge",
+            "kvq_selftest_bounded_wait",
             "kvq_decode_attention_static_scratch"):
     getattr(_lib, _fn).restype = c_i32
 
@@ -171,6 +174,15 @@ def decode_attention_multi(cfg: LayerConfig, cache: LayerCache, q, n_query: int,
            _lib.kvq_decode_attention_multi(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), n_query, num_q_heads,
                                            _ptr(seq_lens), batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse),
                                            _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream_ptr(stream)))
+
+
+def selftest_bounded_wait(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, seq_lens, batch: int,
+                          softmax_scale: float, out, out_bf16: bool, lse, workspace, workspace_bytes: int, dev_status,
+                          stream=None) -> None:
+    _check("kvq_selftest_bounded_wait",
+           _lib.kvq_selftest_bounded_wait(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads,
+                                          _ptr(seq_lens), batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse),
+                                          _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream_ptr(stream)))
 
 
 def lse_merge(o_parts, lse_parts, n_parts: int, rows: int, out, out_bf16: bool, lse_out=None, stream=None) -> None:

@@ -92,6 +92,18 @@ def test_calibrate_rejects_non_fp8_formats(kvq):
     assert e.value.status == -1
 
 
+def test_selftest_rejects_before_any_launch(kvq):
+    cache = kvq.LayerCache()
+    paged = kvq.make_config("int4", 2, 16, 128, 16, 0, paged=True, block_tokens=16, num_blocks=4, max_blocks_per_seq=2)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.selftest_bounded_wait(paged, cache, 0, 8, 0, 1, 0.1, 0, False, 0, 0, 0, 0, stream=0)
+    assert e.value.status == -2
+    cfg = kvq.make_config("fp8_e4m3", 2, 1, 128, 0, 0, capacity_tokens=64)
+    with pytest.raises(kvq.KvqError) as e:  # no status word to report into
+        kvq.selftest_bounded_wait(cfg, cache, 0, 8, 0, 1, 0.1, 16, False, 0, 0, 0, None, stream=0)
+    assert e.value.status == -1
+
+
 def test_lse_merge_rejects_bad_arguments(kvq):
     for args in ((16, 16, 0, 4, 16, 0), (16, 16, 2, 4, 16, 2), (0, 16, 2, 4, 16, 0), (16, 16, 2, 4, 8, 0)):
         o, l, n, rows, out, bf = args

@@ -273,6 +273,33 @@ def test_bad_block_and_capacity_are_reported_not_faulted():
     assert torch.isfinite(out).all()
 
 
+def test_bounded_wait_runs_out_reports_and_context_stays_usable():
+    # self-test hook: one warp's first copy is withheld while its barrier expects the bytes,
+    # so its bounded wait (about a second) gives up; the launch reports KVQ_DEV_TIMEOUT and
+    # finishes, and the next call on the same context gives the oracle's result
+    import time
+    from quantized_kv_cache_decode_gb300 import kvq
+    gl, caches, q = build("fp8_e4m3", 2, 4, [300, 40], 1, 128, 0, 0, False, 41)
+    B, Hq = 2, 8
+    qd = torch.from_numpy(q.astype(np.int16)).cuda()
+    wsb = kvq.decode_workspace_size(gl.cfg, B, Hq)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    gl.status.zero_()
+    t0 = time.time()
+    kvq.selftest_bounded_wait(gl.cfg, gl.layer.struct(), qd, Hq, gl.seq_lens_dev(), B, 1 / math.sqrt(128), out, False,
+                              lse, ws, wsb, gl.status)
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    assert gl.status_value() & kvq.DEV_TIMEOUT
+    assert 0.3 < waited < 30.0, waited
+    gl.status.zero_()
+    o, l = gl.decode(q)
+    TL.check_attention(o.cpu().numpy(), l.cpu().numpy(), *O.decode_attention(O.bf16_to_f32(q), caches))
+    assert gl.status_value() == 0
+
+
 def test_workspace_too_small_is_rejected():
     from quantized_kv_cache_decode_gb300 import kvq
     gl, _, q = build("int4", 1, 2, [64], 16, 128, 16, 0, False, 3)
