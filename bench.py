@@ -42,6 +42,9 @@ sys.path.insert(0, ROOT)
 from quantized_kv_cache_decode_gb300 import inputs as I  # noqa: E402
 
 DEFAULT_WORKLOAD = "llama3_8b_fp8_e4m3"
+# where the raw nvidia-smi clock samples of the timed region are written (the JSON line
+# carries their summary)
+OUT_DIR = os.environ.get("KVQ_BENCH_OUT", os.path.join(ROOT, "bench_out"))
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -359,8 +362,7 @@ def run_gpu(args, w, rank, world):
         step(i)
     torch.cuda.synchronize()
 
-    clk = ClockSampler(dev.index if dev.index is not None else 0, os.path.join(ROOT, "gpurun_out",
-                                                                                f"clocks_rank{rank}.csv")) \
+    clk = ClockSampler(dev.index if dev.index is not None else 0, os.path.join(OUT_DIR, f"clocks_rank{rank}.csv")) \
         if rank == 0 else None
     time.sleep(0.15 if clk else 0)
     # ---- timed region: exactly K steps; per-launch events around the decode split pass ----
@@ -611,7 +613,7 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ["LOCAL_RANK"])))
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    os.makedirs(OUT_DIR, exist_ok=True)
     r = run_gpu(args, w, rank, world)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -35,7 +35,7 @@ title and section.
   section on the vLLM flags: the ``fp8_e5m2`` KV dtype and "skip layers"
   whose KV cache is left unquantized.
 
-Readings where the pages leave a step open (each is also listed in the design doc):
+Readings where the pages leave a step open:
 
 * scale and zero-point of a group come from its min m and max M:
   ``s = (M - m) / (2^b - 1)``, ``z = -(m / s)`` (float zero-point); a group
