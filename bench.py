@@ -648,7 +648,11 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(kern_gbs / hbm_peak, 4), "traffic": traffic,
                      "kernel": "decode_kernel (fused merge)", "peak_source": peak_src,
-                     "mean_launch_us": round(r["kern_ms"] * 1e3, 2)},
+                     "mean_launch_us": round(r["kern_ms"] * 1e3, 2),
+                     "median_launch_us": round(float(np.median(r["kern_ms_all"])) * 1e3, 2),
+                     "min_launch_us": round(float(np.min(r["kern_ms_all"])) * 1e3, 2),
+                     "max_launch_us": round(float(np.max(r["kern_ms_all"])) * 1e3, 2),
+                     "launches_timed": len(r["kern_ms_all"])},
         "e2e": {"value": round(job_throughput(r["sbytes"], r["e2e_ms"], world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 4)},
         "gpu_launches": count_launches(w) * args.steps,
