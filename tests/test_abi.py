@@ -27,6 +27,18 @@ def test_exports_every_declared_symbol(kvq):
         assert hasattr(lib, name), name
 
 
+def test_binding_matches_declared_parameter_counts(kvq):
+    # every entry point of include/kvq.h is bound with as many ctypes arguments as it declares
+    with open(os.path.join(ROOT, "include", "kvq.h")) as f:
+        text = f.read()
+    decls = re.findall(r"^\s*(?:kvq_status|const char\*)\s+(kvq_\w+)\s*\(([^;]*?)\)\s*;", text, re.M | re.S)
+    assert len(decls) == len(kvq.declared_symbols())
+    for name, params in decls:
+        n = len([p for p in params.split(",") if p.strip() and p.strip() != "void"])
+        bound = getattr(kvq._lib, name).argtypes
+        assert bound is not None and len(bound) == n, (name, n, bound)
+
+
 def test_status_strings(kvq):
     for code, name in kvq.STATUS.items():
         assert kvq.status_string(code).startswith(name)
