@@ -130,6 +130,7 @@ def cache_layout(cfg: LayerConfig, num_seqs: int) -> Dict[str, int]:
 
 
 def fp8_calibrate(x, n: int, scale_out, stream=None, fmt: str = "fp8_e4m3") -> None:
+    """Per-tensor FP8 scale amax / (448 for E4M3, 57344 for E5M2) of n bf16 values, on the device."""
     if fmt == "fp8_e4m3":
         _check("kvq_fp8_calibrate", _lib.kvq_fp8_calibrate(_ptr(x), n, _ptr(scale_out), _stream_ptr(stream)))
     else:
@@ -139,6 +140,7 @@ def fp8_calibrate(x, n: int, scale_out, stream=None, fmt: str = "fp8_e4m3") -> N
 
 def quantize_append(cfg: LayerConfig, cache: LayerCache, k_new, v_new, n_new: int, seq_lens, batch: int,
                     dev_status=None, stream=None) -> None:
+    """Write n_new tokens per (sequence, kv head): sink, bf16 window, quantized spills."""
     _check("kvq_quantize_append",
            _lib.kvq_quantize_append(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new), n_new,
                                     _ptr(seq_lens), batch, _ptr(dev_status), _stream_ptr(stream)))
@@ -154,6 +156,7 @@ def decode_workspace_size(cfg: LayerConfig, batch: int, num_q_heads: int) -> int
 def decode_attention(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, seq_lens, batch: int,
                      softmax_scale: float, out, out_bf16: bool, lse, workspace, workspace_bytes: int,
                      dev_status=None, stream=None) -> None:
+    """One decode step of attention over the cache (fused split pass + log-sum-exp merge)."""
     _check("kvq_decode_attention",
            _lib.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads, _ptr(seq_lens),
                                      batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse), _ptr(workspace),
@@ -161,6 +164,7 @@ def decode_attention(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, s
 
 
 def decode_workspace_size_multi(cfg: LayerConfig, batch: int, n_query: int, num_q_heads: int) -> int:
+    """Workspace bytes of decode_attention_multi (kvq_decode_workspace_size_multi)."""
     out = c_sz(0)
     _check("kvq_decode_workspace_size_multi",
            _lib.kvq_decode_workspace_size_multi(ctypes.byref(cfg), batch, n_query, num_q_heads, ctypes.byref(out)))
@@ -170,6 +174,7 @@ def decode_workspace_size_multi(cfg: LayerConfig, batch: int, n_query: int, num_
 def decode_attention_multi(cfg: LayerConfig, cache: LayerCache, q, n_query: int, num_q_heads: int, seq_lens,
                            batch: int, softmax_scale: float, out, out_bf16: bool, lse, workspace, workspace_bytes: int,
                            dev_status=None, stream=None) -> None:
+    """n_query causal query tokens per sequence in one launch; q, out: [B][n_query][Hq][d]."""
     _check("kvq_decode_attention_multi",
            _lib.kvq_decode_attention_multi(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), n_query, num_q_heads,
                                            _ptr(seq_lens), batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse),
@@ -179,6 +184,7 @@ def decode_attention_multi(cfg: LayerConfig, cache: LayerCache, q, n_query: int,
 def selftest_bounded_wait(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, seq_lens, batch: int,
                           softmax_scale: float, out, out_bf16: bool, lse, workspace, workspace_bytes: int, dev_status,
                           stream=None) -> None:
+    """Decode with one bulk copy withheld: must report DEV_TIMEOUT in dev_status and finish."""
     _check("kvq_selftest_bounded_wait",
            _lib.kvq_selftest_bounded_wait(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads,
                                           _ptr(seq_lens), batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse),
@@ -186,6 +192,7 @@ def selftest_bounded_wait(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: i
 
 
 def lse_merge(o_parts, lse_parts, n_parts: int, rows: int, out, out_bf16: bool, lse_out=None, stream=None) -> None:
+    """Merge per-part (out, lse) rows over disjoint token parts; o_parts [n][rows][128] fp32."""
     _check("kvq_lse_merge", _lib.kvq_lse_merge(_ptr(o_parts), _ptr(lse_parts), n_parts, rows, _ptr(out), int(out_bf16),
                                                _ptr(lse_out), _stream_ptr(stream)))
 
