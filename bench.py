@@ -41,7 +41,7 @@ sys.path.insert(0, ROOT)
 
 from quantized_kv_cache_decode_gb300 import inputs as I  # noqa: E402
 
-DEFAULT_WORKLOAD = "llama3_8b_fp8_e4m3"
+DEFAULT_WORKLOAD = "paged_mixed_int8_int4_64l"
 # where the raw nvidia-smi clock samples of the timed region are written (the JSON line
 # carries their summary)
 OUT_DIR = os.environ.get("KVQ_BENCH_OUT", os.path.join(ROOT, "bench_out"))
@@ -298,7 +298,7 @@ def run_gpu(args, w, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     n_app = max(1, w.append_tokens)
-    lens_after = I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
+    lens_after = lens_after_step(w)
     lens_before = [int(t) - n_app for t in lens_after]
     sbytes = step_bytes(w, lens_after, n_app)
     replicas = args.replicas or max(1, min(4, math.ceil(3 * L2_BYTES / sbytes)))
@@ -383,7 +383,7 @@ def run_gpu(args, w, rank, world):
     wall1 = time.time()
     barrier()
     ms = t_start.elapsed_time(t_end)
-    kern_ms = [evs[i][0][j].elapsed_time(evs[i][1][j]) for i in range(K) for j in range(nl)]
+    kern_ms = [[evs[i][0][j].elapsed_time(evs[i][1][j]) for j in range(nl)] for i in range(K)]  # [step][layer]
     ms = max_over_ranks(ms, dev)
     ms_step = ms / K
     # ---- end to end through the public API, host buffers, copies inside the timed region ----
@@ -444,11 +444,9 @@ def run_gpu(args, w, rank, world):
     for rep in reps:
         for lay in rep:
             assert lay.status.item() == 0, f"device status {lay.status.item()}"
-    return dict(ms_step=ms_step, kern_ms=float(np.mean(kern_ms)), kern_ms_all=kern_ms, sbytes=sbytes,
+    return dict(ms_step=ms_step, kern_ms=np.array(kern_ms), sbytes=sbytes,
                 replicas=replicas, e2e_ms=e_ms, h2d=h2d, d2h=d2h, clocks=clocks, wall_ms=(wall1 - wall0) * 1e3,
-                lens_after=lens_after, n_app=n_app,
-                attn_bytes_first_layer=sum(attention_bytes(w.layer_formats[0], int(T), w.num_kv_heads)
-                                           for T in lens_after) + len(lens_after) * w.n_query * w.num_q_heads * 128 * 2)
+                lens_after=lens_after, n_app=n_app)
 
 
 # --------------------------------------------------------------------------- #
@@ -456,29 +454,30 @@ def run_gpu(args, w, rank, world):
 # --------------------------------------------------------------------------- #
 
 
-def oracle_items(w):
-    """Lazily: host inputs and prebuilt oracle caches of (layer 0, sequence, kv head) pairs."""
+def lens_after_step(w):
+    return I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
+
+
+def oracle_pairs(w, layer, pairs):
+    """Host inputs and prebuilt oracle caches of the given (sequence, kv head) pairs of one layer."""
     from oracle import kvq_oracle as O
-    fmt = w.layer_formats[0]
-    lens_after = I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
+    fmt = w.layer_formats[layer]
+    lens_after = lens_after_step(w)
     n_app = max(1, w.append_tokens)
     spec = O.Spec(fmt.fmt, d=128, G=1 if is_fp8(fmt) else fmt.G, Gv=fmt.Gv,
                   R=0 if is_fp8(fmt) else fmt.R, S=fmt.S)
-    q = O.bf16_to_f32(I.q_bf16(w, 0))
-
-    def gen():
-        for b in range(w.batch):
-            for h in range(w.num_kv_heads):
-                T = int(lens_after[b])
-                k, v = I.kv_bf16(w, 0, b, h, T)
-                kf, vf = O.bf16_to_f32(k), O.bf16_to_f32(v)
-                ks = O.fp8_tensor_scale(kf, spec.fmt) if spec.is_fp8 else None
-                vs = O.fp8_tensor_scale(vf, spec.fmt) if spec.is_fp8 else None
-                hc = O.build_head_cache(kf[:T - n_app], vf[:T - n_app], spec, ks, vs)
-                qh = q[b, h * w.gqa:(h + 1) * w.gqa] if w.n_query == 1 else q[b, :, h * w.gqa:(h + 1) * w.gqa]
-                yield (b, h, T, hc, kf[T - n_app:], vf[T - n_app:], qh.reshape(-1, 128))
-
-    return O, gen(), n_app
+    q = O.bf16_to_f32(I.q_bf16(w, layer))
+    items = []
+    for b, h in pairs:
+        T = int(lens_after[b])
+        k, v = I.kv_bf16(w, layer, b, h, T)
+        kf, vf = O.bf16_to_f32(k), O.bf16_to_f32(v)
+        ks = O.fp8_tensor_scale(kf, spec.fmt) if spec.is_fp8 else None
+        vs = O.fp8_tensor_scale(vf, spec.fmt) if spec.is_fp8 else None
+        hc = O.build_head_cache(kf[:T - n_app], vf[:T - n_app], spec, ks, vs)
+        qh = q[b, h * w.gqa:(h + 1) * w.gqa] if w.n_query == 1 else q[b, :, h * w.gqa:(h + 1) * w.gqa]
+        items.append((b, h, T, hc, kf[T - n_app:], vf[T - n_app:], qh.reshape(-1, 128)))
+    return O, items, n_app
 
 
 def oracle_step(O, items, n_query=1):
@@ -496,8 +495,8 @@ def oracle_step(O, items, n_query=1):
             O.attend_head(qh[j], kh[:n], vh[:n], 1.0 / math.sqrt(128))
 
 
-def sample_bytes(w, items, n_app):
-    fmt = w.layer_formats[0]
+def sample_bytes(w, layer, items, n_app):
+    fmt = w.layer_formats[layer]
     tot = 0
     for (b, h, T, hc, kn, vn, qh) in items:
         tot += attention_bytes(fmt, T, 1) + append_bytes(fmt, T - n_app, n_app, 1)
@@ -505,43 +504,139 @@ def sample_bytes(w, items, n_app):
     return tot
 
 
-def cpu_baseline(w, budget_s=12.0):
-    O, items, n_app = oracle_items(w)
-    # grow the sample until ~budget_s of oracle step time, bounded by the whole first layer
-    dt = 0.0
-    done = []
-    for it in items:
-        t0 = time.perf_counter()
-        oracle_step(O, [it], w.n_query)
-        dt += time.perf_counter() - t0
-        done.append(it)
-        if dt > budget_s:
+def sample_pairs(w, layer, token_budget):
+    """(sequence, kv head) pairs of one layer in a seeded random order (so the sample follows the
+    workload's length mix), as many as hold about ``token_budget`` cached tokens (at least one)."""
+    lens_after = lens_after_step(w)
+    rng = np.random.default_rng(w.seed * 31 + layer)
+    order = rng.permutation(w.batch * w.num_kv_heads)
+    out, tok = [], 0
+    for u in order:
+        b, h = divmod(int(u), w.num_kv_heads)
+        out.append((b, h))
+        tok += int(lens_after[b])
+        if tok >= token_budget:
             break
-    gbs = sample_bytes(w, done, n_app) / dt / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"layer 0, {len(done)} of {w.batch * w.num_kv_heads} (sequence, kv head) pairs, "
-                      f"append + attention, numpy fp64 single thread, {dt:.1f} s"}
+    return out
+
+
+def _oracle_worker(wname, layer, pairs, barrier, results):
+    """One CPU worker (its own process, one numpy thread): build its pairs' oracle caches, wait for
+    every worker, then time one oracle step over them."""
+    w = I.WORKLOADS[wname]()
+    O, items, n_app = oracle_pairs(w, layer, pairs)
+    barrier.wait()
+    t0 = time.time()
+    oracle_step(O, items, w.n_query)
+    t1 = time.time()
+    results.put((sample_bytes(w, layer, items, n_app), t0, t1, len(items)))
+
+
+def time_oracle_parallel(w, layer, pairs, workers):
+    """GB/s of the oracle over ``pairs`` spread over ``workers`` processes (spawned, so safe after the
+    GPU run): the sample's bytes over the span from the first worker's start to the last one's end."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    workers = max(1, min(workers, len(pairs)))
+    # deal the pairs so each worker gets a similar number of tokens (longest first)
+    lens_after = lens_after_step(w)
+    order = sorted(pairs, key=lambda bh: -int(lens_after[bh[0]]))
+    shares, load = [[] for _ in range(workers)], [0] * workers
+    for bh in order:
+        i = int(np.argmin(load))
+        shares[i].append(bh)
+        load[i] += int(lens_after[bh[0]])
+    barrier = ctx.Barrier(workers)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w.name, layer, sh, barrier, results)) for sh in shares]
+    for p in procs:
+        p.start()
+    got = [results.get() for _ in procs]
+    for p in procs:
+        p.join()
+    nbytes = sum(g[0] for g in got)
+    span = max(g[2] for g in got) - min(g[1] for g in got)
+    return nbytes / span / 1e9, span, sum(g[3] for g in got)
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            txt = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in txt.splitlines():
+                if line.split(":")[0].strip() == key:
+                    return f"{key}: {line.split(':', 1)[1].strip()}"
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def parity_layers(w):
+    """The layers the oracle is timed on: all of a one-layer workload, else the first, a middle and the
+    last layer (for the paged mix: INT8, INT4, INT8)."""
+    n = len(w.layer_formats)
+    return sorted({0, n // 2 - 1 if n > 2 else 0, n - 1})
+
+
+def cpu_baseline(w, token_budget=400000):
+    """The oracle on the host cores, 1 thread and every core, on a bounded sample of each parity layer;
+    the whole-step figure is extrapolated from the per-format rates (stated as such)."""
+    nproc = os.cpu_count() or 1
+    legs = []
+    lens_after = lens_after_step(w)
+    n_app = max(1, w.append_tokens)
+    for workers in (1, nproc):
+        per_layer = []
+        rate = {}
+        for layer in parity_layers(w):
+            fmt = w.layer_formats[layer].fmt
+            pairs = sample_pairs(w, layer, token_budget * workers)
+            gbs, span, n = time_oracle_parallel(w, layer, pairs, workers)
+            per_layer.append({"layer": layer, "format": fmt, "pairs": n, "of_pairs": w.batch * w.num_kv_heads,
+                              "GB_per_s": round(gbs, 5), "timed_s": round(span, 2)})
+            rate.setdefault(fmt, []).append(gbs)
+        # every layer of the step at its format's measured rate
+        t = 0.0
+        tot = 0
+        for f in w.layer_formats:
+            lb = sum(attention_bytes(f, int(T), w.num_kv_heads) +
+                     append_bytes(f, int(T) - n_app, n_app, w.num_kv_heads) for T in lens_after)
+            lb += len(lens_after) * w.n_query * w.num_q_heads * (128 * 2 * 2 + 4)
+            tot += lb
+            t += lb / (float(np.mean(rate[f.fmt])) * 1e9)
+        legs.append({"cores": workers, "value": round(tot / t / 1e9, 5), "unit": "GB/s", "step_s": round(t, 2),
+                     "extrapolated": len(w.layer_formats) > len(parity_layers(w)), "per_layer": per_layer})
+    best = legs[-1]
+    layers = ", ".join(str(x) for x in parity_layers(w))
+    return {"value": best["value"], "unit": "GB/s", "cores": best["cores"], "kind": "oracle",
+            "sample": f"layer(s) {layers}: a seeded random sample of (sequence, kv head) pairs holding about "
+                      f"{token_budget} cached tokens per worker, append + attention, numpy fp64, one thread per "
+                      f"worker process; " + ("whole-step figure extrapolated from the per-format rates"
+                                             if best["extrapolated"] else "the whole step is that layer"),
+            "cpu_model": cpu_model(), "nproc": nproc, "legs": legs}
 
 
 def run_reference(args, w, rank, world):
     if rank != 0:
         return None
-    O, items, n_app = oracle_items(w)
-    # a step = the oracle over a bounded sample of pairs, sized to ~1 s
-    first = next(items)
+    # a step = the oracle (one thread) over a bounded sample of layer 0's pairs, sized to ~1 s
+    first = sample_pairs(w, 0, 1)
+    O, items, n_app = oracle_pairs(w, 0, first)
     t0 = time.perf_counter()
-    oracle_step(O, [first], w.n_query)
-    per_pair = max(1e-3, time.perf_counter() - t0)
-    n = max(1, min(w.batch * w.num_kv_heads, int(1.0 / per_pair)))
-    sample = [first] + [it for _, it in zip(range(n - 1), items)]
+    oracle_step(O, items, w.n_query)
+    per_tok = max(1e-9, (time.perf_counter() - t0) / items[0][2])
+    pairs = sample_pairs(w, 0, int(1.0 / per_tok))
+    O, sample, n_app = oracle_pairs(w, 0, pairs)
     for _ in range(args.warmup):
         oracle_step(O, sample, w.n_query)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle_step(O, sample, w.n_query)
     dt = (time.perf_counter() - t0) / args.steps
-    gbs = sample_bytes(w, sample, n_app) / dt / 1e9
-    return gbs, dt, n
+    gbs = sample_bytes(w, 0, sample, n_app) / dt / 1e9
+    return gbs, dt, len(sample)
 
 
 # --------------------------------------------------------------------------- #
@@ -600,7 +695,8 @@ def main():
         if rank == 0:
             gbs, dt, n = r
             cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": f"layer 0, {n} (sequence, kv head) pairs per step, append + attention, numpy fp64"}
+                   "sample": f"layer 0, {n} (sequence, kv head) pairs per step (seeded random order), "
+                             f"append + attention, numpy fp64, one thread", "cpu_model": cpu_model()}
             line = {"impl": "reference", "metric": metric, "value": round(gbs, 4), "unit": "GB/s",
                     "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -620,12 +716,22 @@ def main():
     if rank != 0:
         return
     gbs = job_throughput(r["sbytes"], r["ms_step"], world)
-    kern_gbs = r["attn_bytes_first_layer"] / (r["kern_ms"] * 1e-3) / 1e9 if len(w.layer_formats) == 1 else None
-    if kern_gbs is None:
-        # multi-layer: bytes of every layer's attention over the mean launch duration
-        per_layer = [sum(attention_bytes(f, int(T), w.num_kv_heads) for T in r["lens_after"]) +
-                     len(r["lens_after"]) * w.n_query * w.num_q_heads * 256 for f in w.layer_formats]
-        kern_gbs = float(np.mean(per_layer)) / (r["kern_ms"] * 1e-3) / 1e9
+    # roofline of the decode kernel: algorithmic bytes of each layer's launch (codes, scales and
+    # zero-points, bf16 sink/residual, q, bf16 out, lse) over that launch's CUDA-event duration
+    B = len(r["lens_after"])
+    layer_bytes = np.array([sum(attention_bytes(f, int(T), w.num_kv_heads) for T in r["lens_after"]) +
+                            B * w.n_query * w.num_q_heads * (128 * 2 * 2 + 4) for f in w.layer_formats], float)
+    km = r["kern_ms"]  # [steps][layers] ms
+    kern_gbs = layer_bytes.sum() / (km.sum(axis=1).mean() * 1e-3) / 1e9
+    by_format = {}
+    for fname in sorted({f.fmt for f in w.layer_formats}):
+        idx = [j for j, f in enumerate(w.layer_formats) if f.fmt == fname]
+        t = km[:, idx]
+        a = layer_bytes[idx].sum() / (t.sum(axis=1).mean() * 1e-3) / 1e9
+        by_format[fname] = {"layers": len(idx), "achieved": round(a, 1), "frac": round(a / hbm_peak, 4),
+                            "bytes_per_launch": int(layer_bytes[idx].mean()),
+                            "mean_launch_us": round(float(t.mean()) * 1e3, 2),
+                            "median_launch_us": round(float(np.median(t)) * 1e3, 2)}
     # DRAM bytes per decode launch from an ncu capture, used only while the kernel sources are
     # the ones the capture ran (their hash is recorded beside the figure)
     traffic = None
@@ -634,7 +740,12 @@ def main():
         with open(tpath) as f:
             rec = json.load(f)
         if rec.get("kernel_sources_sha256") == kernel_sources_sha256():
-            traffic = rec.get("bytes_per_launch")
+            per_fmt = rec.get("bytes_per_launch_by_format")
+            if per_fmt:  # the step's launches, averaged, each at its format's captured figure
+                if all(f.fmt in per_fmt for f in w.layer_formats):
+                    traffic = int(np.mean([per_fmt[f.fmt] for f in w.layer_formats]))
+            else:
+                traffic = rec.get("bytes_per_launch")
     line = {
         "metric": metric, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 5), "higher_is_better": True, "scaling": "weak",
@@ -648,11 +759,12 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(kern_gbs / hbm_peak, 4), "traffic": traffic,
                      "kernel": "decode_kernel (fused merge)", "peak_source": peak_src,
-                     "mean_launch_us": round(r["kern_ms"] * 1e3, 2),
-                     "median_launch_us": round(float(np.median(r["kern_ms_all"])) * 1e3, 2),
-                     "min_launch_us": round(float(np.min(r["kern_ms_all"])) * 1e3, 2),
-                     "max_launch_us": round(float(np.max(r["kern_ms_all"])) * 1e3, 2),
-                     "launches_timed": len(r["kern_ms_all"])},
+                     "bytes_per_launch": int(layer_bytes.mean()),
+                     "mean_launch_us": round(float(km.mean()) * 1e3, 2),
+                     "median_launch_us": round(float(np.median(km)) * 1e3, 2),
+                     "min_launch_us": round(float(np.min(km)) * 1e3, 2),
+                     "max_launch_us": round(float(np.max(km)) * 1e3, 2),
+                     "launches_timed": int(km.size), "by_format": by_format},
         "e2e": {"value": round(job_throughput(r["sbytes"], r["e2e_ms"], world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 4)},
         "gpu_launches": count_launches(w) * args.steps,

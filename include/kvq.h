@@ -324,7 +324,11 @@ kvq_status kvq_decode_combine(const kvq_layer_config* cfg, int32_t num_q_heads, 
  *     config, batch and query-head count exceeds 8 MiB (large batch x heads).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device.  The address is kept with the
+ *     id of the device's context: after a device reset (cudaDeviceReset) the
+ *     next call looks it up again, and that call too belongs outside capture.
+ *   - Host-detectable errors (out == NULL with batch > 0, out_bf16 not 0 or 1,
+ *     the checks of kvq_decode_attention) return before anything is enqueued.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero.  Calls that overlap on the
  *     GPU (other streams, other threads) race on it: serialise them.

@@ -8,6 +8,7 @@ tails, over every format, both layouts, GQA ratios 1..8 and edge lengths.
     |lse - ref| <= 1e-4, bf16 output == round-to-nearest-even of the fp32 output.
 """
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -100,7 +101,7 @@ CASES = [
                                              f"{'-paged' if c[8] else ''}" for c in CASES])
 def test_parity(case):
     fmt, H, g, lens, G, Gv, R, S, paged, blk = case
-    seed = abs(hash(str(case))) % 10000
+    seed = zlib.crc32(repr(case).encode()) % 10000  # stable across processes
     gl, caches, q = build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=blk)
     B = len(lens)
     # stored cache, bit-exact
@@ -142,7 +143,7 @@ MULTI = [
 def test_multi_query_parity(case):
     # M query tokens per sequence (the cache's last M tokens), each attending causally
     fmt, H, gh, M, lens, G, Gv, R, S, paged = case
-    seed = abs(hash(str(case))) % 10000
+    seed = zlib.crc32(repr(case).encode()) % 10000  # stable across processes
     gl, caches, _ = build(fmt, H, gh, lens, G, Gv, R, S, paged, seed)
     q = I.random_bf16(seed * 3 + 1, (len(lens), M, H * gh, 128))
     out_ref, lse_ref = O.decode_attention_multi(O.bf16_to_f32(q), caches)

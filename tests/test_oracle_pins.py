@@ -489,3 +489,89 @@ def test_gqa_equals_replicated_mha_and_token_order():
         o1, l1 = O.attend_head(q[0, j], kh, vh, 0.25)
         o2, l2 = O.attend_head(q[0, j], kh[perm], vh[perm], 0.25)
         assert np.allclose(o1, o2, atol=1e-13) and abs(l1 - l2) < 1e-13
+
+
+# --------------------------------------------------------------------------- #
+# the fp32 cache export (dequantized_f32): what kvq_dequantize is compared with
+# "KV Cache Quantization Analysis", section 2 (x_hat = s(q - z)); section 4 (FP8 value times its scale)
+# --------------------------------------------------------------------------- #
+
+
+def _on_grid_groups(bits, qn, d, G, Gv, seed):
+    """K and V of qn quantized tokens where every quantization group lies on a grid of its own:
+    s a power of two and z an integer, different for every group, and the group holds the
+    codes 0 and 2^b - 1 (at positions that move with the group).  Every value is s (q - z) with
+    |q - z| < 256, so it is exact in bf16 and fp32.  Returns (k, v, k_s, k_z, v_s, v_z)."""
+    rng = np.random.default_rng(seed)
+    L = 2 ** bits - 1
+    nk = qn // G
+    k_s = np.empty((nk, d)); k_z = np.empty((nk, d))
+    v_s = np.empty((qn, d // Gv)); v_z = np.empty((qn, d // Gv))
+    kq = rng.integers(0, L + 1, size=(qn, d))
+    vq = rng.integers(0, L + 1, size=(qn, d))
+    for j in range(nk):
+        for c in range(d):
+            k_s[j, c] = 2.0 ** -(1 + (c + 2 * j) % 4)
+            k_z[j, c] = (5 * c + 3 * j + 1) % (L + 1)
+            lo, hi = j * G + (c % G), j * G + ((c + 1) % G)
+            kq[lo, c], kq[hi, c] = 0, L
+    for t in range(qn):
+        for j in range(d // Gv):
+            v_s[t, j] = 2.0 ** -(1 + (t + 3 * j) % 4)
+            v_z[t, j] = (3 * t + 7 * j + 2) % (L + 1)
+            lo, hi = j * Gv + (t % Gv), j * Gv + ((t + 1) % Gv)
+            vq[t, lo], vq[t, hi] = 0, L
+    gk = np.arange(qn) // G
+    k = (k_s[gk] * (kq - k_z[gk])).astype(F32)
+    v = (np.repeat(v_s, Gv, axis=1) * (vq - np.repeat(v_z, Gv, axis=1))).astype(F32)
+    return k, v, k_s, k_z, v_s, v_z
+
+
+@pytest.mark.parametrize("bits,G,Gv,R,S", [(2, 8, 16, 5, 1), (4, 16, 32, 3, 2), (8, 4, 8, 7, 0)])
+def test_dequantized_f32_returns_on_grid_inputs_in_token_order(bits, G, Gv, R, S):
+    d, n_groups = 32, 3
+    qn = n_groups * G
+    kq, vq, k_s, k_z, v_s, v_z = _on_grid_groups(bits, qn, d, G, Gv, seed=bits)
+    rng = np.random.default_rng(100 + bits)
+    # sink and residual tokens: arbitrary bf16 values, distinct from the grid values
+    sink_k, sink_v = (O.bf16_to_f32(rng.integers(0x3F80, 0x4100, size=(S, d)).astype(np.uint16)) for _ in range(2))
+    res_k, res_v = (O.bf16_to_f32(rng.integers(0xC000, 0xC100, size=(R, d)).astype(np.uint16)) for _ in range(2))
+    k = np.concatenate([sink_k, kq, res_k]).astype(F32)
+    v = np.concatenate([sink_v, vq, res_v]).astype(F32)
+    spec = O.Spec(f"int{bits}", d=d, G=G, Gv=Gv, R=R, S=S)
+    assert O.token_split(len(k), spec) == (S, qn, R)
+    hc = O.build_head_cache(k, v, spec)
+    # the quantizer recovers every group's grid exactly ...
+    assert np.array_equal(hc.k_s, k_s.astype(F32)) and np.array_equal(hc.k_z, k_z.astype(F32))
+    assert np.array_equal(hc.v_s, v_s.astype(F32)) and np.array_equal(hc.v_z, v_z.astype(F32))
+    # ... and the export returns the inputs themselves, bit for bit, sink first, residual last
+    ko, vo = O.dequantized_f32(hc)
+    assert ko.dtype == np.float32 and vo.dtype == np.float32
+    assert np.array_equal(ko.view(np.uint32), k.view(np.uint32))
+    assert np.array_equal(vo.view(np.uint32), v.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt,codes,k_scale,v_scale,k_expect,v_expect", [
+    # E4M3: 0x38 = 1.0, 0x7E = 448 (largest finite), 0x01 = 2^-9 (smallest subnormal), 0xB8 = -1.0, +-0
+    ("fp8_e4m3", [0x38, 0x7E, 0x01, 0xB8, 0x00, 0x80], 0.5, 2.0,
+     [0.5, 224.0, 2.0 ** -10, -0.5, 0.0, -0.0], [2.0, 896.0, 2.0 ** -8, -2.0, 0.0, -0.0]),
+    # E5M2: 0x3C = 1.0, 0x7B = 57344 (largest finite), 0x01 = 2^-16, 0xBC = -1.0, 0x46 = 6.0
+    ("fp8_e5m2", [0x3C, 0x7B, 0x01, 0xBC, 0x46], 0.25, 4.0,
+     [0.25, 14336.0, 2.0 ** -18, -0.25, 1.5], [4.0, 229376.0, 2.0 ** -14, -4.0, 24.0]),
+])
+def test_dequantized_f32_fp8_worked_values(fmt, codes, k_scale, v_scale, k_expect, v_expect):
+    d = 4
+    spec = O.Spec(fmt, d=d, G=1, Gv=d, R=0, S=1)
+    n = len(codes)
+    cm = np.array([[c] * d for c in codes], np.uint8)           # token t: code codes[t] in every channel
+    sink = np.full((1, d), 3.0, F32)
+    hc = O.HeadCache(spec, sink.copy(), -sink, cm, cm[::-1].copy(), np.zeros((0, d), F32), np.zeros((0, d), F32),
+                     k_scale=F32(k_scale), v_scale=F32(v_scale))
+    ko, vo = O.dequantized_f32(hc)
+    assert ko.shape == (1 + n, d) and ko.dtype == np.float32
+    assert np.array_equal(ko[0], sink[0]) and np.array_equal(vo[0], -sink[0])
+    want_k = np.array(k_expect, F32)
+    want_v = np.array(v_expect, F32)[::-1]
+    assert np.array_equal(ko[1:, 0].view(np.uint32), want_k.view(np.uint32))   # sign of zero included
+    assert np.array_equal(vo[1:, 0].view(np.uint32), want_v.view(np.uint32))
+    assert np.all(ko[1:] == ko[1:, :1]) and np.all(vo[1:] == vo[1:, :1])
