@@ -147,7 +147,7 @@ int stage_bytes_of(const LayerDesc& L, int tps) {
 bool bf16_joint(int stage_bytes) { return stage_bytes >= 2 * kBfHalfBytes; }
 
 constexpr int kMergeFloats = 132;        // floats per query head of a merge record (kvq_decode.cuh)
-constexpr int kQRowFloats = 136;         // floats per query head row in shared memory (kvq_decode.cuh)
+constexpr int kQRowFloats = 144;         // floats per query column row in shared memory (kvq_decode.cuh)
 
 // A warp's merge record in shared memory: m, l, -, - and 128 outputs per query head.
 int merge_bytes_of(const LayerDesc& L, int g) {
@@ -181,9 +181,9 @@ cudaError_t occupancy_query(const LayerDesc& L, int g, int multi, int smem, int*
 // given device.
 cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
   struct Entry {
-    int dev, fmt, ngv, nbq, smem, n;
+    int dev, fmt, ngv, multi, smem, n;
   };
-  const int nbq = multi ? 3 : (g <= 4 ? 1 : 2);  // 3: the multi-query variant
+  const int mq = multi ? 1 : 0;  // the multi-query variant is a kernel of its own
   static std::mutex mu;
   static Entry cache[256];
   static int used = 0;
@@ -193,7 +193,7 @@ cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
   {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
-      if (cache[i].dev == dev && cache[i].fmt == L.fmt && cache[i].ngv == L.ngv && cache[i].nbq == nbq &&
+      if (cache[i].dev == dev && cache[i].fmt == L.fmt && cache[i].ngv == L.ngv && cache[i].multi == mq &&
           cache[i].smem == smem) {
         *n = cache[i].n;
         return cudaSuccess;
@@ -202,7 +202,7 @@ cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
   e = occupancy_query(L, g, multi, smem, n);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (used < 256) cache[used++] = Entry{dev, L.fmt, L.ngv, nbq, smem, *n};
+  if (used < 256) cache[used++] = Entry{dev, L.fmt, L.ngv, mq, smem, *n};
   return cudaSuccess;
 }
 
@@ -232,7 +232,7 @@ struct DecodeGeom {
 // that fits the shared memory.
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, int multi = 0) {
   const int wsc = merge_bytes_of(L, g);
-  const int nw = decode_warps(kernel_format(L.fmt), multi ? kMaxGqa : g);  // multi-query: two column blocks
+  const int nw = decode_warps(kernel_format(L.fmt));
   const int fixed = fixed_smem(batch, wsc, nw);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;

@@ -49,22 +49,22 @@
 
 namespace kvq {
 
-// Warps per CTA (one CTA per SM at most): 16 for 2- and 4-bit codes with up to 4 query
-// heads per kv head (128 registers a thread), else 12 (170 registers);
-// decode_warps() in kvq_internal.h states the same rule for the host.
-template <int FMT, int NBQ>
+// Warps per CTA (one CTA per SM at most): 12 (168 registers a thread; with 16
+// warps and 128 registers the integer variants spill); decode_warps() in
+// kvq_internal.h states the same for the host.
+template <int FMT>
 struct DecodeWarps {
-  static constexpr int kNW = (NBQ == 1 && (FMT == 2 || FMT == 4)) ? 16 : 12;
+  static constexpr int kNW = 12;
   static constexpr int kThreads = kNW * 32;
 };
 constexpr int kMaxStages = 4;
 constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 range is safe
 constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
 constexpr float kSTau = 4.f;           // a Value scale may exceed its reference 4x before a rescale
-// floats per query head in shared memory (128 + 8 pad): the rows of four heads start
-// 8 banks apart, so the bf16 path's 8-byte query loads (four heads, four column
-// pairs per step) and build_bq's 16-byte loads are free of bank conflicts
-constexpr int kQRow = 136;
+// floats per query column in shared memory (128 + 16 pad): the 16-byte loads of the
+// operand builds (column r, channels 16s + 4q ..) of the 8 lanes of a load phase
+// (two columns) fall in different banks
+constexpr int kQRow = 144;
 // A bf16 half tile in a stage: 16 rows of 256 bytes, the 16-byte chunk c of row r
 // stored at chunk c ^ (r & 7), so that the 8 rows an ldmatrix reads at one chunk
 // fall in 8 different bank groups.
@@ -113,8 +113,14 @@ __device__ __forceinline__ uint32_t int4_lo(uint32_t w) {  // nibbles at bits 0,
 __device__ __forceinline__ uint32_t int4_hi(uint32_t w) {  // nibbles at bits 4, 20 -> (n - 8)
   return hfma2(lop3_and_or(w, 0x00F000F0u, kMagic), dup16(f16_bits_pow2(-4)), dup16(f16_bits_of_int(-72)));
 }
-__device__ __forceinline__ uint32_t int8_lo(uint32_t w) {  // bytes 0, 2 -> (n - 128)
-  return hfma2(lop3_and_or(w, 0x00FF00FFu, kMagic), dup16(f16_bits_of_int(1)), dup16(f16_bits_of_int(-1152)));
+// bytes 0, 2 (sel 0x7170) or 1, 3 (sel 0x7371) of w under the f16 exponent byte 0x64, minus 1152 -> (n - 128)
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t int8_pair(uint32_t w) {
+  uint32_t t;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w), "r"(0x64646464u), "n"(SEL));
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(dup16(f16_bits_of_int(1152))));
+  return d;
 }
 
 // The lane's operand words of one code matrix (fragment order): kWords words,
@@ -132,7 +138,9 @@ __device__ __forceinline__ void load_words(const uint8_t* base, int lane, uint32
   }
 }
 
-// A-operand registers of step s (a compile-time constant after unrolling).
+// Fragment registers of step s (a compile-time constant after unrolling): reg 0 =
+// (row r, columns 2q, 2q + 1), reg 1 = (row r + 8, ...), reg 2 = (row r, columns
+// 2q + 8, 2q + 9), reg 3 = (row r + 8, ...) of the stored 16 x 16 code block.
 template <int FMT, int N>
 __device__ __forceinline__ void unpack_a(const uint32_t (&W)[N], int s, uint32_t& a0, uint32_t& a1, uint32_t& a2,
                                          uint32_t& a3) {
@@ -149,10 +157,10 @@ __device__ __forceinline__ void unpack_a(const uint32_t (&W)[N], int s, uint32_t
     a2 = int2_pair<2>(w);
     a3 = int2_pair<3>(w);
   } else if constexpr (FMT == 8) {
-    a0 = int8_lo(W[2 * s]);
-    a1 = int8_lo(W[2 * s] >> 8);
-    a2 = int8_lo(W[2 * s + 1]);
-    a3 = int8_lo(W[2 * s + 1] >> 8);
+    a0 = int8_pair<0x7270>(W[2 * s]);
+    a1 = int8_pair<0x7371>(W[2 * s]);
+    a2 = int8_pair<0x7270>(W[2 * s + 1]);
+    a3 = int8_pair<0x7371>(W[2 * s + 1]);
   } else if constexpr (FMT == 17) {  // FP8 E5M2
     e5m2x4_to_f16x4(W[2 * s], a0, a1);
     e5m2x4_to_f16x4(W[2 * s + 1], a2, a3);
@@ -186,34 +194,31 @@ __device__ __forceinline__ void load_row(const float* p, float (&v)[NGV]) {
 // --------------------------------------------------------------------------
 // per-warp online-softmax state
 // --------------------------------------------------------------------------
-// Score layout: lane (r, q) holds, per column block b, query head 4b + q for
-// tokens r and r + 8 of a tile.  Output layout: lane (r, q) holds heads 2q and
-// 2q + 1 of channels 16 mb + r and 16 mb + r + 8 (mb = 0..7).  W layout: lane
-// (r, q) holds head r for tokens 2q, 2q + 1, 2q + 8, 2q + 9.
-template <int NBQ, int NGV>
+// Score layout: lane (r, q) holds query column r for tokens 2q, 2q + 1, 2q + 8,
+// 2q + 9 of a tile -- which is also the B-operand (W) layout of the PV product.
+// Output layout: lane (r, q) holds columns 2q and 2q + 1 of channels 16 mb + r and
+// 16 mb + r + 8 (mb = 0..7).
+template <int NGV>
 struct WarpState {
-  float o[8][4];     // PV accumulators (output layout): [mb][0/1] = channel 16mb+r, heads 2q / 2q+1;
+  float o[8][4];     // PV accumulators (output layout): [mb][0/1] = channel 16mb+r, columns 2q / 2q+1;
                      // [mb][2/3] = channel 16mb+r+8
-  float zacc[NGV];   // zero-point sums per Value group, head r (W layout), thread-partial
-  float m[NBQ];      // reference max of head 4b+q (log2 domain)
-  float l[NBQ];      // sum of p of head 4b+q, thread-partial
-  float S;           // reference Value scale (warp-uniform: Value scales do not depend on the head)
+  float zacc[NGV];   // zero-point sums per Value group of column r, lane-partial
+  float m;           // reference max of column r (log2 domain), the same in the row's four lanes
+  float l;           // sum of p of column r, lane-partial
+  float S;           // reference Value scale (warp-uniform: Value scales do not depend on the column)
   float inv_S;       // 1 / S
 };
 
-template <int NBQ, int NGV>
-__device__ __forceinline__ void state_init(WarpState<NBQ, NGV>& st) {
+template <int NGV>
+__device__ __forceinline__ void state_init(WarpState<NGV>& st) {
 #pragma unroll
   for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
 #pragma unroll
   for (int j = 0; j < NGV; ++j) st.zacc[j] = 0.f;
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b) {
-    st.m[b] = -INFINITY;
-    st.l[b] = 0.f;
-  }
+  st.m = -INFINITY;
+  st.l = 0.f;
   st.S = 0.f;
   st.inv_S = 0.f;
 }
@@ -224,53 +229,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// One softmax step over a tile: sig[b][0] / sig[b][1] are the scores (log2
-// domain, -inf when masked) of tokens r / r + 8 for head 4b + q; smax is the
-// largest Value scale among the lane's tokens (warp-uniform already when kVarS
-// is false).  The references m (per head) and S move only when a score exceeds
-// m by 2^kTau or a scale exceeds S by kSTau -- each lane checks its own values
-// and the warp votes; only then are the maxima reduced over the lanes and every
-// accumulator rescaled.  Returns p = 2^(sig - m).
-template <int NBQ, int NGV, bool kVarS>
-__device__ __forceinline__ void softmax_tile(WarpState<NBQ, NGV>& st, const float (&sig)[NBQ][2], float smax, int r,
-                                             int q, float (&pr)[NBQ][2]) {
-  bool bump = smax > st.S * kSTau;
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b) bump |= fmaxf(sig[b][0], sig[b][1]) > st.m[b] + kTau;
+// One softmax step over a tile: sig[e] are the scores (log2 domain, -inf when
+// masked) of the lane's four tokens for column r; smax is the largest Value scale
+// among the lane's tokens (warp-uniform already when kVarS is false).  The
+// references m (per column) and S move only when a score exceeds m by 2^kTau or a
+// scale exceeds S by kSTau -- each lane checks its own values and the warp votes;
+// only then are the maxima reduced over the lanes and every accumulator
+// rescaled.  Returns p = 2^(sig - m).
+template <int NGV, bool kVarS>
+__device__ __forceinline__ void softmax_tile(WarpState<NGV>& st, const float (&sig)[4], float smax, int q,
+                                             float (&pr)[4]) {
+  const float mx = fmaxf(fmaxf(sig[0], sig[1]), fmaxf(sig[2], sig[3]));
+  const bool bump = (smax > st.S * kSTau) || (mx > st.m + kTau);
   if (__any_sync(kFull, bump)) {
-    float alpha[NBQ];
-#pragma unroll
-    for (int b = 0; b < NBQ; ++b) {
-      float t = fmaxf(sig[b][0], sig[b][1]);  // the head's largest score: reduce over the token lanes r
-      t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
-      t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
-      t = fmaxf(t, __shfl_xor_sync(kFull, t, 16));
-      const float mn = t > st.m[b] + kTau ? t : st.m[b];
-      alpha[b] = (st.m[b] == -INFINITY) ? 0.f : fast_exp2(st.m[b] - mn);
-      st.m[b] = mn;
-      st.l[b] *= alpha[b];
-    }
+    float t = mx;  // the column's largest score in the tile: reduce over the row's token lanes q
+    t = fmaxf(t, __shfl_xor_sync(kFull, t, 1));
+    t = fmaxf(t, __shfl_xor_sync(kFull, t, 2));
+    const float mn = t > st.m + kTau ? t : st.m;
+    const float alpha = (st.m == -INFINITY) ? 0.f : fast_exp2(st.m - mn);
+    st.m = mn;
+    st.l *= alpha;
     if constexpr (kVarS) {  // per-token Value scales: the tile's largest over the token lanes q
       smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
       smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 2));
     }
     const float S_new = smax > st.S * kSTau ? smax : st.S;
     const float ratio = S_new > 0.f ? st.S / S_new : 0.f;
-    // output layout: heads 2q, 2q + 1 live in score lanes (2q) & 3, (2q + 1) & 3 of block q >> 1
-    float a0 = __shfl_sync(kFull, alpha[0], (2 * q) & 3), a1 = __shfl_sync(kFull, alpha[0], (2 * q + 1) & 3);
-    // W layout: head r lives in score lane r & 3 of block r >> 2
-    float az = __shfl_sync(kFull, alpha[0], r & 3);
-    if constexpr (NBQ == 2) {
-      const float b0 = __shfl_sync(kFull, alpha[1], (2 * q) & 3), b1 = __shfl_sync(kFull, alpha[1], (2 * q + 1) & 3);
-      const float bz = __shfl_sync(kFull, alpha[1], r & 3);
-      if (q >= 2) {
-        a0 = b0;
-        a1 = b1;
-      }
-      if (r >= 4) az = bz;
-    }
-    a0 *= ratio;
-    a1 *= ratio;
+    // output layout: columns 2q, 2q + 1 live in the score lanes of rows 2q, 2q + 1
+    const float a0 = __shfl_sync(kFull, alpha, 8 * q) * ratio, a1 = __shfl_sync(kFull, alpha, 8 * q + 4) * ratio;
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       st.o[mb][0] *= a0;
@@ -279,106 +265,76 @@ __device__ __forceinline__ void softmax_tile(WarpState<NBQ, NGV>& st, const floa
       st.o[mb][3] *= a1;
     }
 #pragma unroll
-    for (int j = 0; j < NGV; ++j) st.zacc[j] *= az * ratio;
+    for (int j = 0; j < NGV; ++j) st.zacc[j] *= alpha * ratio;
     st.S = S_new;
     st.inv_S = 1.f / S_new;
   }
 #pragma unroll
-  for (int b = 0; b < NBQ; ++b)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      pr[b][e] = (sig[b][e] == -INFINITY) ? 0.f : fast_exp2(sig[b][e] - st.m[b]);
-      st.l[b] += pr[b][e];
-    }
-}
-
-// p of head r for tokens 2q, 2q + 1, 2q + 8, 2q + 9 of a tile whose score-layout
-// values are pr[b][e] (token r) and pr[b][e + 1] (token r + 8).
-template <int NBQ, int NV>
-__device__ __forceinline__ void p_operand(const float (&pr)[NBQ][NV], int e, int r, int q, float (&pt)[4]) {
-  const int s0 = 8 * q + (r & 3), s1 = s0 + 4;  // score lanes of tokens 2q and 2q + 1, head r (mod 4)
-  pt[0] = __shfl_sync(kFull, pr[0][e], s0);
-  pt[1] = __shfl_sync(kFull, pr[0][e], s1);
-  pt[2] = __shfl_sync(kFull, pr[0][e + 1], s0);
-  pt[3] = __shfl_sync(kFull, pr[0][e + 1], s1);
-  if constexpr (NBQ == 2) {
-    const float u0 = __shfl_sync(kFull, pr[1][e], s0), u1 = __shfl_sync(kFull, pr[1][e], s1);
-    const float u2 = __shfl_sync(kFull, pr[1][e + 1], s0), u3 = __shfl_sync(kFull, pr[1][e + 1], s1);
-    if (r >= 4) {
-      pt[0] = u0;
-      pt[1] = u1;
-      pt[2] = u2;
-      pt[3] = u3;
-    }
-  } else {
-    if (r >= 4) pt[0] = pt[1] = pt[2] = pt[3] = 0.f;  // heads 4..7 do not exist with one block
+  for (int e = 0; e < 4; ++e) {
+    pr[e] = (sig[e] == -INFINITY) ? 0.f : fast_exp2(sig[e] - st.m);
+    st.l += pr[e];
   }
 }
 
 // --------------------------------------------------------------------------
-// QK B operand of the quantized tiles
+// the query-side A operand of the quantized tiles
 // --------------------------------------------------------------------------
-// Lane (r, q), column block b: column r = half (r & 1) of query head
-// 4b + (r >> 1), channels 16s + 4q + e.  q_s holds the g query heads and a zero
-// row g for the columns of absent heads.  FP8 layers (one build per segment):
-// x_c = q_c, kappa = 16384 / max_c |x_c| of the head, B = hi (r even) or lo
-// (r odd) part of x_c kappa.  kfac / cterm return the score multiplier and the
-// zero-point term (kfac0 = log2(e) / sqrt(d) * the Key scale; no zero-point for
-// FP8) for head 4b + q.
-template <int FMT, int NBQ>
-__device__ __forceinline__ void build_bq(const float* q_s, int r, int q, int g, float kfac0,
-                                         uint32_t (&Bq)[NBQ][8][2], float (&kfac)[NBQ], float (&cterm)[NBQ]) {
-  const bool lo = (r & 1) != 0;
+// Row r of the 16-row A operand is query column r (high f16 half), row r + 8 the
+// same column's low half; its K index follows the Key codes' fragment order
+// (channel 16s + 4q + e at K index 2q + (e & 1) + 8 (e >> 1)), so lane (r, q)
+// holds, per step s, X[s][0] = hi(x_c) and X[s][1] = lo(x_c) of channels
+// 16s + 4q, +1, and X[s][2], X[s][3] the same of channels 16s + 4q + 2, +3.  The
+// lane computes each of its 32 products once and keeps both halves.
+// qrow: the column's query row in shared memory (a zero row for absent columns).
+
+// FP8 layers (one build per segment): x_c = q_c kappa, kappa = 16384 / max_c |q_c|;
+// kfac (the score multiplier) = kfac0 / kappa, kfac0 = log2(e) / sqrt(d) * the Key scale.
+__device__ __forceinline__ void build_x_fp8(const float* qrow, int q, float kfac0, uint32_t (&X)[8][4],
+                                            float& kfac) {
+  float mx = 0.f;
 #pragma unroll
-  for (int b = 0; b < NBQ; ++b) {
-    const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 4 * q;  // row g is zero
-    float mx = 0.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-      asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    float kap = 16384.f / mx;
-    if (!(mx > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
-      x.x *= kap;
-      x.y *= kap;
-      x.z *= kap;
-      x.w *= kap;
-      uint32_t h01 = pack_f16(x.x, x.y), h23 = pack_f16(x.z, x.w);
-      if (lo) {
-        const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
-        h01 = pack_f16(x.x - f01.x, x.y - f01.y);
-        h23 = pack_f16(x.z - f23.x, x.w - f23.y);
-      }
-      Bq[b][s][0] = h01;
-      Bq[b][s][1] = h23;
-      asm volatile("" ::: "memory");
-    }
-    // to the score layout: head 4b + q is held by the lanes with r = 2q
-    kfac[b] = __shfl_sync(kFull, kfac0 / kap, 8 * q);
-    cterm[b] = 0.f;
+  for (int s = 0; s < 8; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
   }
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  float kap = 16384.f / mx;
+  if (!(mx > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
+  const float2 k2 = make_float2(kap, kap);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
+    split_f16x2(mul_f32x2(make_float2(x.x, x.y), k2), X[s][0], X[s][1]);
+    split_f16x2(mul_f32x2(make_float2(x.z, x.w), k2), X[s][2], X[s][3]);
+  }
+  kfac = kfac0 / kap;
 }
 
-// The B operand for a Key group of an INT layer, x_c = q_c s_c (s_c: the Key
-// scale of channel c), with the zero-point term sum_c x_c (2^(b-1) - z_c), in one
-// pass over the channels: kappa = 16384 / (max_c |q_c| * max_c s_c) bounds |x_c kappa| by
-// 16384 without first finding max_c |x_c| (qm[b]: the lane's head max |q_c|, per
-// segment).  A smaller kappa than the exact one only moves the hi/lo split: the
-// two f16 terms still hold x_c kappa to about 22 bits, or to the f16 subnormal
-// step (2^-24, against elements up to 16384 times the bound ratio) for tiny x_c.
-template <int FMT, int NBQ>
-__device__ __forceinline__ void build_bq_group(const float* q_s, const float* ks, const float* kz, int lane, int r,
-                                               int q, int g, float kfac0, const float (&qm)[NBQ],
-                                               uint32_t (&Bq)[NBQ][8][2], float (&kfac)[NBQ], float (&cterm)[NBQ]) {
+// Max |q_c| of the lane's column (lane q reads channels 32q .. 32q + 31; the four lanes of a row combine).
+__device__ __forceinline__ float column_qmax(const float* qrow, int q) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 32 * q + 4 * j);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+  }
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+  return fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+}
+
+// A Key group of an INT layer: x_c = q_c s_c (s_c: the Key scale of channel c),
+// with the zero-point term sum_c x_c (2^(b-1) - z_c), in one pass over the
+// channels: kappa = 16384 / (max_c |q_c| * max_c s_c) bounds |x_c kappa| by 16384
+// without first finding max_c |x_c| (qm: the column's max |q_c|, per segment).  A
+// smaller kappa than the exact one only moves the hi/lo split: the two f16 terms
+// still hold x_c kappa to about 22 bits, or to the f16 subnormal step (2^-24,
+// against elements up to 16384 times the bound ratio) for tiny x_c.
+template <int FMT>
+__device__ __forceinline__ void build_x_group(const float* qrow, const float* ks, const float* kz, int lane, int q,
+                                              float kfac0, float qm, uint32_t (&X)[8][4], float& kfac,
+                                              float& cterm) {
   constexpr float kH = (float)FT<FMT>::kHalf;
-  const bool lo = (r & 1) != 0;
   // the largest Key scale of the group (scales are positive)
   float sm;
   {
@@ -387,91 +343,50 @@ __device__ __forceinline__ void build_bq_group(const float* q_s, const float* ks
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sm = fmaxf(sm, __shfl_xor_sync(kFull, sm, o));
   }
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b) {
-    const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 4 * q;  // row g is zero
-    const float bound = qm[b] * sm;
-    float kap = 16384.f / bound;
-    if (!(bound > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
-    float cz = 0.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      float4 x = *reinterpret_cast<const float4*>(qh + 16 * s);
-      const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
-      const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
-      x.x *= s4.x;
-      x.y *= s4.y;
-      x.z *= s4.z;
-      x.w *= s4.w;
-      cz = fmaf(x.x, kH - z4.x, cz);
-      cz = fmaf(x.y, kH - z4.y, cz);
-      cz = fmaf(x.z, kH - z4.z, cz);
-      cz = fmaf(x.w, kH - z4.w, cz);
-      x.x *= kap;
-      x.y *= kap;
-      x.z *= kap;
-      x.w *= kap;
-      uint32_t h01 = pack_f16(x.x, x.y), h23 = pack_f16(x.z, x.w);
-      if (lo) {
-        const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
-        h01 = pack_f16(x.x - f01.x, x.y - f01.y);
-        h23 = pack_f16(x.z - f23.x, x.w - f23.y);
-      }
-      Bq[b][s][0] = h01;
-      Bq[b][s][1] = h23;
-      asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
-    }
-    cz += __shfl_xor_sync(kFull, cz, 1);
-    cz += __shfl_xor_sync(kFull, cz, 2);
-    // to the score layout: head 4b + q is held by the lanes with r = 2q
-    const float kf = kfac0 / kap, ct = kfac0 * cz;
-    kfac[b] = __shfl_sync(kFull, kf, 8 * q);
-    cterm[b] = __shfl_sync(kFull, ct, 8 * q);
-  }
-}
-
-// Max |q_c| over the channels of the lane's head (4b + (r >> 1), row g zero) of each
-// column block: lane q reads channels 32q .. 32q + 31, the four lanes of a head combine.
-template <int NBQ>
-__device__ __forceinline__ void head_qmax(const float* q_s, int r, int q, int g, float (&qm)[NBQ]) {
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b) {
-    const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 32 * q;
-    float m = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 x = *reinterpret_cast<const float4*>(qh + 4 * j);
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-    }
-    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
-    qm[b] = m;
-  }
-}
-
-// Raw scores of one quantized tile: d[b][0] / d[b][1] = tokens r / r + 8, head 4b + q.
-template <int FMT, int NBQ>
-__device__ __forceinline__ void qk_tile(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&Bq)[NBQ][8][2],
-                                        float (&d)[NBQ][2]) {
-  float acc[NBQ][2][4];
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b)
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[b][c][e] = 0.f;
+  const float bound = qm * sm;
+  float kap = 16384.f / bound;
+  if (!(bound > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
+  const float2 k2 = make_float2(kap, kap), h2 = make_float2(kH, kH);
+  float2 cz = make_float2(0.f, 0.f);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    uint32_t a0, a1, a2, a3;
-    unpack_a<FMT>(KW, s, a0, a1, a2, a3);
-#pragma unroll
-    for (int b = 0; b < NBQ; ++b) mma_f16(acc[b][s & 1], a0, a1, a2, a3, Bq[b][s][0], Bq[b][s][1]);
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
+    const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
+    const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
+    const float2 x01 = mul_f32x2(make_float2(x.x, x.y), make_float2(s4.x, s4.y));
+    const float2 x23 = mul_f32x2(make_float2(x.z, x.w), make_float2(s4.z, s4.w));
+    cz = fma_f32x2(x01, sub_f32x2(h2, make_float2(z4.x, z4.y)), cz);
+    cz = fma_f32x2(x23, sub_f32x2(h2, make_float2(z4.z, z4.w)), cz);
+    split_f16x2(mul_f32x2(x01, k2), X[s][0], X[s][1]);
+    split_f16x2(mul_f32x2(x23, k2), X[s][2], X[s][3]);
+    asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
   }
+  float c = cz.x + cz.y;
+  c += __shfl_xor_sync(kFull, c, 1);
+  c += __shfl_xor_sync(kFull, c, 2);
+  kfac = kfac0 / kap;
+  cterm = kfac0 * c;
+}
+
+// Raw scores of one quantized tile for the lane's column: d[0..3] = tokens 2q, 2q + 1,
+// 2q + 8, 2q + 9.  Two MMAs per step: tokens 0-7 (Key fragment registers 0, 2 as
+// the B operand) and tokens 8-15 (registers 1, 3); D row r holds the high-half
+// product of column r, row r + 8 the low-half one.
+template <int FMT>
+__device__ __forceinline__ void qk_tile(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&X)[8][4],
+                                        float (&d)[4]) {
+  float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int b = 0; b < NBQ; ++b) {
-    d[b][0] = (acc[b][0][0] + acc[b][1][0]) + (acc[b][0][1] + acc[b][1][1]);
-    d[b][1] = (acc[b][0][2] + acc[b][1][2]) + (acc[b][0][3] + acc[b][1][3]);
+  for (int s = 0; s < 8; ++s) {
+    uint32_t k0, k1, k2, k3;
+    unpack_a<FMT>(KW, s, k0, k1, k2, k3);
+    mma_f16(lo, X[s][0], X[s][1], X[s][2], X[s][3], k0, k2);
+    mma_f16(hi, X[s][0], X[s][1], X[s][2], X[s][3], k1, k3);
   }
+  d[0] = lo[0] + lo[2];
+  d[1] = lo[1] + lo[3];
+  d[2] = hi[0] + hi[2];
+  d[3] = hi[1] + hi[3];
 }
 
 // PV of one quantized tile: o[mb] += V^T(channels 16mb..) * W(group of mb).
@@ -486,44 +401,32 @@ __device__ __forceinline__ void pv_tile(const uint32_t (&VW)[FT<FMT>::kWords], c
   }
 }
 
-// Scores of a bf16 tile from its K rows in shared memory (rows past `rows` masked).
-template <int NBQ>
-__device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* q_s, int lane, int r, int q, int g,
-                                        int rows, float scale_log2, float (&sig)[NBQ][2]) {
+// Scores of a bf16 tile from its K rows in shared memory (rows past `rows` masked):
+// the query column (bf16, exact) in A rows 0-7, rows 8-15 zero; the K rows as the B
+// operand through ldmatrix (natural channel order).
+__device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* qrow, int lane, int q, bool hv, int rows,
+                                        float scale_log2, float (&sig)[4]) {
   // lane's row (lane & 7) + 8 ((lane >> 3) & 1), chunk 2s + (lane >> 4), swizzled:
   // (2s + h) ^ x = 2 (s ^ (x >> 1)) + (h ^ (x & 1)) with x = lane & 7
   const int x = lane & 7;
   const uint32_t lbase =
       smem_addr(stg) + ((lane & 7) + 8 * ((lane >> 3) & 1)) * 256 + 16 * ((lane >> 4) ^ (x & 1));
-  const bool qcol = (r & 1) == 0;  // even columns carry the query, odd columns are zero
-  float acc[NBQ][2][4];
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b)
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[b][c][e] = 0.f;
+  float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    uint32_t a0, a1, a2, a3;
-    ldmatrix_x4(lbase + 32 * (s ^ (x >> 1)), a0, a1, a2, a3);
-#pragma unroll
-    for (int b = 0; b < NBQ; ++b) {
-      const float* qh = q_s + min(4 * b + (r >> 1), g) * kQRow + 16 * s + 2 * q;
-      const float2 x0 = *reinterpret_cast<const float2*>(qh);
-      const float2 x1 = *reinterpret_cast<const float2*>(qh + 8);
-      const uint32_t b0 = qcol ? pack_bf16(x0.x, x0.y) : 0u, b1 = qcol ? pack_bf16(x1.x, x1.y) : 0u;
-      mma_bf16(acc[b][s & 1], a0, a1, a2, a3, b0, b1);
-    }
+    uint32_t k0, k1, k2, k3;
+    ldmatrix_x4(lbase + 32 * (s ^ (x >> 1)), k0, k1, k2, k3);
+    const float2 x0 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * q);
+    const float2 x1 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * q + 8);
+    const uint32_t a0 = pack_bf16(x0.x, x0.y), a2 = pack_bf16(x1.x, x1.y);
+    mma_bf16(lo, a0, 0u, a2, 0u, k0, k2);
+    mma_bf16(hi, a0, 0u, a2, 0u, k1, k3);
   }
-#pragma unroll
-  for (int b = 0; b < NBQ; ++b) {
-    const bool hv = 4 * b + q < g;
-    const float d0 = (acc[b][0][0] + acc[b][1][0]) + (acc[b][0][1] + acc[b][1][1]);
-    const float d1 = (acc[b][0][2] + acc[b][1][2]) + (acc[b][0][3] + acc[b][1][3]);
-    sig[b][0] = (hv && r < rows) ? d0 * scale_log2 : -INFINITY;
-    sig[b][1] = (hv && r + 8 < rows) ? d1 * scale_log2 : -INFINITY;
-  }
+  const int t0 = 2 * q;
+  sig[0] = (hv && t0 < rows) ? lo[0] * scale_log2 : -INFINITY;
+  sig[1] = (hv && t0 + 1 < rows) ? lo[1] * scale_log2 : -INFINITY;
+  sig[2] = (hv && t0 + 8 < rows) ? hi[0] * scale_log2 : -INFINITY;
+  sig[3] = (hv && t0 + 9 < rows) ? hi[1] * scale_log2 : -INFINITY;
 }
 
 // PV of a bf16 tile from its V rows (rows past the end zeroed); W = pt * f split
@@ -644,10 +547,10 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // them (FP8 layers with no sink tokens) carries no bf16-tile code at all.  MQ:
 // several query tokens per sequence (causal limits per column); only that
 // variant carries the limit checks.
-template <int FMT, int NGV, int NBQ, bool BF, bool MQ>
-__global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_kernel(const DecodeParams p) {
+template <int FMT, int NGV, bool BF, bool MQ>
+__global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
-  constexpr int NW = DecodeWarps<FMT, NBQ>::kNW;
+  constexpr int NW = DecodeWarps<FMT>::kNW;
   constexpr int NT = NW * 32;
   constexpr int NR = NW / 2;  // merge records (warps fold pairwise into them)
   extern __shared__ __align__(128) uint8_t smem[];
@@ -1036,27 +939,27 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
     for (int s = 0; s < nseg; ++s) {
       const SegRec sg = segs[s];
       const int nbf_tok = sg.n_sink + sg.r;
-      WarpState<NBQ, NGV> stt;
+      WarpState<NGV> stt;
       state_init(stt);
-      uint32_t Bq[NBQ][8][2];
-      float kfac[NBQ], cterm[NBQ];
-      float qm[NBQ];  // INT: the lanes' head max |q_c| (the Key groups' kappa bound)
+      const float* qrow = q_s + min(r, g) * kQRow;  // the lane's query column (row g is zero)
+      const bool hv = r < g;                         // the column exists
+      uint32_t X[8][4];  // query-side A operand (hi/lo rows), rebuilt per Key group for INT layers
+      float kfac = 0.f, cterm = 0.f;
+      float qm = 0.f;    // INT: the column's max |q_c| (the Key groups' kappa bound)
       if constexpr (F::kFp8) {
-        build_bq<FMT, NBQ>(q_s, r, q, g, p.scale_log2 * __ldg(p.C.k_tscale), Bq, kfac, cterm);
+        build_x_fp8(qrow, q, p.scale_log2 * __ldg(p.C.k_tscale), X, kfac);
       } else {
-        head_qmax<NBQ>(q_s, r, q, g, qm);
+        qm = column_qmax(qrow, q);
 #pragma unroll
-        for (int b = 0; b < NBQ; ++b) {
-          kfac[b] = cterm[b] = 0.f;
-#pragma unroll
-          for (int s2 = 0; s2 < 8; ++s2) Bq[b][s2][0] = Bq[b][s2][1] = 0u;
-        }
+        for (int s2 = 0; s2 < 8; ++s2) X[s2][0] = X[s2][1] = X[s2][2] = X[s2][3] = 0u;
       }
-      float sig_bf[NBQ][2];  // scores of a bf16 tile between its K and V stages
-      // several query tokens per sequence: column 4b + q (query token (4b + q) / gh) sees the
-      // tokens t <= T - n_query + (4b + q) / gh (causal: where that query token sits); the
-      // limit is recomputed where it is needed, so one-query decode keeps no registers for it
-      auto col_limit = [&](int b) { return toks[sg.b] - p.n_query + (4 * b + q) / p.gh; };
+      float sig_bf[4];  // scores of a bf16 tile between its K and V stages
+      // the lane's four tokens of a tile (score and W layout)
+      const int tk[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
+      // several query tokens per sequence: column r (query token r / gh) sees the tokens
+      // t <= T - n_query + r / gh (causal: where that query token sits); the limit is
+      // recomputed where it is needed, so one-query decode keeps no registers for it
+      auto col_limit = [&]() { return toks[sg.b] - p.n_query + r / p.gh; };
 
       // this warp's stages of segment s, in the order its producer issued them
       while (true) {
@@ -1100,15 +1003,13 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
           const uint8_t* vst = stg;
           bool vpart = tg.kind == 2;
           if (tg.kind == 1) {
-            bf16_qk<NBQ>(stg, q_s, lane, r, q, g, rows, p.scale_log2, sig_bf);
+            bf16_qk(stg, qrow, lane, q, hv, rows, p.scale_log2, sig_bf);
             if (MQ && p.n_query > 1) {  // bf16 list index -> token: sinks first, then the residual window after Q_n
-              const int x0 = 16 * tg.a + r, x1 = x0 + 8;
-              const int t0 = x0 + (x0 >= sg.n_sink ? sg.qn : 0), t1 = x1 + (x1 >= sg.n_sink ? sg.qn : 0);
+              const int lim = col_limit();
 #pragma unroll
-              for (int b = 0; b < NBQ; ++b) {
-                const int lim = col_limit(b);
-                if (t0 > lim) sig_bf[b][0] = -INFINITY;
-                if (t1 > lim) sig_bf[b][1] = -INFINITY;
+              for (int e = 0; e < 4; ++e) {
+                const int x = 16 * tg.a + tk[e];
+                if (x + (x >= sg.n_sink ? sg.qn : 0) > lim) sig_bf[e] = -INFINITY;
               }
             }
             vpart = bfj;
@@ -1119,11 +1020,9 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
             for (int idx = lane; idx < (16 - rows) * 16; idx += 32)
               *reinterpret_cast<uint4*>(stw + (rows + idx / 16) * 256 + (idx % 16) * 16) = make_uint4(0u, 0u, 0u, 0u);
             __syncwarp();
-            float pr[NBQ][2];
-            softmax_tile<NBQ, NGV, false>(stt, sig_bf, 1.f, r, q, pr);
-            float pt[4];
-            p_operand<NBQ, 2>(pr, 0, r, q, pt);
-            bf16_pv(vst, lane, pt, stt.inv_S * kPrescale, stt.o);
+            float pr[4];
+            softmax_tile<NGV, false>(stt, sig_bf, 1.f, q, pr);
+            bf16_pv(vst, lane, pr, stt.inv_S * kPrescale, stt.o);
           }
         } else if (vmask && alive) {
           // ---- quantized stage: tiles [tg.a, tg.a + n), walked in smem, one softmax step each ----
@@ -1140,39 +1039,31 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
             if (++rpos == L.tpg) rpos = 0;
             if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
             if constexpr (F::kInt) {
-              // the group's B operand (q * s, hi/lo), rebuilt at each record (Key group) start
+              // the group's query-side operand (q * s, hi/lo), rebuilt at each record (Key group) start
               if (hdr)
-                build_bq_group<FMT, NBQ>(q_s, reinterpret_cast<const float*>(stg + hoff),
-                                         reinterpret_cast<const float*>(stg + hoff + 512), lane, r, q, g, p.scale_log2,
-                                         qm, Bq, kfac, cterm);
+                build_x_group<FMT>(qrow, reinterpret_cast<const float*>(stg + hoff),
+                                   reinterpret_cast<const float*>(stg + hoff + 512), lane, q, p.scale_log2, qm, X,
+                                   kfac, cterm);
             }
             // QK
-            float d[NBQ][2];
+            float d[4];
             {
               uint32_t KW[F::kWords];
               load_words(tile, lane, KW);
-              qk_tile<FMT, NBQ>(KW, Bq, d);
+              qk_tile<FMT>(KW, X, d);
             }
             const int tok_valid = min(16, sg.qn - i * 16);  // < 16 only for a partial FP8 tile
-            float sig[NBQ][2];
+            float sig[4];
 #pragma unroll
-            for (int b = 0; b < NBQ; ++b) {
-              const bool hv = 4 * b + q < g;
-              sig[b][0] = (hv && r < tok_valid) ? fmaf(d[b][0], kfac[b], cterm[b]) : -INFINITY;
-              sig[b][1] = (hv && r + 8 < tok_valid) ? fmaf(d[b][1], kfac[b], cterm[b]) : -INFINITY;
-            }
+            for (int e = 0; e < 4; ++e) sig[e] = (hv && tk[e] < tok_valid) ? fmaf(d[e], kfac, cterm) : -INFINITY;
             if (MQ && p.n_query > 1) {
-              const int t0 = L.S + 16 * i + r;  // token of row r (quantized token x = t - S)
+              const int lim = col_limit() - (L.S + 16 * i);  // in tile rows (quantized token x = t - S)
 #pragma unroll
-              for (int b = 0; b < NBQ; ++b) {
-                const int lim = col_limit(b);
-                if (t0 > lim) sig[b][0] = -INFINITY;
-                if (t0 + 8 > lim) sig[b][1] = -INFINITY;
-              }
+              for (int e = 0; e < 4; ++e)
+                if (tk[e] > lim) sig[e] = -INFINITY;
             }
             const float* vsp = reinterpret_cast<const float*>(tile + 2 * F::kTile);  // INT: Value scales [16][NGV]
             const float* vzp = vsp + 16 * NGV;                                         // INT: Value zero-points
-            const int tk[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};                // the lane's W tokens
             float smax = s_v8;
             if constexpr (F::kInt) {
 #pragma unroll
@@ -1183,11 +1074,9 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
                 for (int jg = 0; jg < NGV; ++jg) smax = fmaxf(smax, sv[jg]);
               }
             }
-            float pr[NBQ][2];
-            softmax_tile<NBQ, NGV, F::kInt>(stt, sig, smax, r, q, pr);
-            // PV
             float pt[4];
-            p_operand<NBQ, 2>(pr, 0, r, q, pt);
+            softmax_tile<NGV, F::kInt>(stt, sig, smax, q, pt);
+            // PV: the lane's probabilities are already in the W layout (column r, its four tokens)
             uint32_t B0[NGV], B1[NGV];
             if constexpr (F::kFp8) {
               const float f = s_v8 * stt.inv_S * kPrescale;
@@ -1224,33 +1113,17 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
         pump();
       }
 
-      // ---- finalise the warp's state (output layout: heads 2q, 2q + 1) into its merge record ----
-      float lsum[NBQ];
-#pragma unroll
-      for (int b = 0; b < NBQ; ++b) {
-        float l = stt.l[b];
-        l += __shfl_xor_sync(kFull, l, 4);
-        l += __shfl_xor_sync(kFull, l, 8);
-        l += __shfl_xor_sync(kFull, l, 16);
-        lsum[b] = l;
-      }
-      // m and l of heads 2q and 2q + 1 (score lanes (2q) & 3, (2q + 1) & 3 of block q >> 1)
+      // ---- finalise the warp's state (output layout: columns 2q, 2q + 1) into its merge record ----
+      float lsum = stt.l;  // column r: summed over the row's token lanes q
+      lsum += __shfl_xor_sync(kFull, lsum, 1);
+      lsum += __shfl_xor_sync(kFull, lsum, 2);
+      // m and l of columns 2q and 2q + 1 (held by the score lanes of rows 2q, 2q + 1)
       float mo[2], lo2[2];
-      mo[0] = __shfl_sync(kFull, stt.m[0], (2 * q) & 3);
-      mo[1] = __shfl_sync(kFull, stt.m[0], (2 * q + 1) & 3);
-      lo2[0] = __shfl_sync(kFull, lsum[0], (2 * q) & 3);
-      lo2[1] = __shfl_sync(kFull, lsum[0], (2 * q + 1) & 3);
-      if constexpr (NBQ == 2) {
-        const float m0 = __shfl_sync(kFull, stt.m[1], (2 * q) & 3), m1 = __shfl_sync(kFull, stt.m[1], (2 * q + 1) & 3);
-        const float l0 = __shfl_sync(kFull, lsum[1], (2 * q) & 3), l1 = __shfl_sync(kFull, lsum[1], (2 * q + 1) & 3);
-        if (q >= 2) {
-          mo[0] = m0;
-          mo[1] = m1;
-          lo2[0] = l0;
-          lo2[1] = l1;
-        }
-      }
-      // zero-point sums: head r in the W layout, summed over the token lanes q; head 2q (+1) is at lane 8q (+4)
+      mo[0] = __shfl_sync(kFull, stt.m, 8 * q);
+      mo[1] = __shfl_sync(kFull, stt.m, 8 * q + 4);
+      lo2[0] = __shfl_sync(kFull, lsum, 8 * q);
+      lo2[1] = __shfl_sync(kFull, lsum, 8 * q + 4);
+      // zero-point sums: column r in the W layout, summed over the token lanes q; head 2q (+1) is at lane 8q (+4)
       float zo[2][NGV];
 #pragma unroll
       for (int jg = 0; jg < NGV; ++jg) {
@@ -1482,7 +1355,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT, NBQ>::kThreads, 1) decode_ker
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, int NBQ, bool BF, bool MQ>
+template <int FMT, int NGV, bool BF, bool MQ>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1491,49 +1364,45 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, NBQ, BF, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-template <int FMT, int NGV, int NBQ, bool BF, bool MQ>
+template <int FMT, int NGV, bool BF, bool MQ>
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, NBQ, BF, MQ>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, NBQ, BF, MQ><<<p.num_ctas, DecodeWarps<FMT, NBQ>::kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV, BF, MQ><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-// One column block for up to 4 query columns per kv head, two for 5..8; FP8 layers
-// without sink tokens (no bf16 tiles) take the variant without the bf16 path;
-// several query tokens per sequence take the multi-query variant (two blocks).
+// FP8 layers without sink tokens (no bf16 tiles) take the variant without the bf16
+// path; several query tokens per sequence take the multi-query variant.
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
   if constexpr (FT<FMT>::kFp8) {
-    if (p.L.S == 0) {
-      if (p.n_query > 1) return launch_variant<FMT, NGV, 2, false, true>(p, smem, stream);
-      return p.g <= 4 ? launch_variant<FMT, NGV, 1, false, false>(p, smem, stream)
-                      : launch_variant<FMT, NGV, 2, false, false>(p, smem, stream);
-    }
+    if (p.L.S == 0)
+      return p.n_query > 1 ? launch_variant<FMT, NGV, false, true>(p, smem, stream)
+                           : launch_variant<FMT, NGV, false, false>(p, smem, stream);
   }
-  if (p.n_query > 1) return launch_variant<FMT, NGV, 2, true, true>(p, smem, stream);
-  return p.g <= 4 ? launch_variant<FMT, NGV, 1, true, false>(p, smem, stream)
-                  : launch_variant<FMT, NGV, 2, true, false>(p, smem, stream);
+  return p.n_query > 1 ? launch_variant<FMT, NGV, true, true>(p, smem, stream)
+                       : launch_variant<FMT, NGV, true, false>(p, smem, stream);
 }
 
-// Resident CTAs per SM (for one query token: the variant with the bf16 path, the
-// larger of the two; several query tokens: the multi-query variant).
-template <int FMT, int NGV, int NBQ, bool MQ>
+// Resident CTAs per SM (the variant with the bf16 path, the larger one; several
+// query tokens: the multi-query variant).
+template <int FMT, int NGV, bool MQ>
 cudaError_t occupancy_variant(int smem, int* n) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, NBQ, true, MQ>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, true, MQ>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, NBQ, true, MQ>,
-                                                       DecodeWarps<FMT, NBQ>::kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ>,
+                                                       DecodeWarps<FMT>::kThreads, smem);
 }
 template <int FMT, int NGV>
 cudaError_t occupancy_t(int g, int multi, int smem, int* n) {
-  if (multi) return occupancy_variant<FMT, NGV, 2, true>(smem, n);
-  return g <= 4 ? occupancy_variant<FMT, NGV, 1, false>(smem, n) : occupancy_variant<FMT, NGV, 2, false>(smem, n);
+  (void)g;
+  return multi ? occupancy_variant<FMT, NGV, true>(smem, n) : occupancy_variant<FMT, NGV, false>(smem, n);
 }
 
 }  // namespace kvq

@@ -12,11 +12,11 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGqa = 8;
 constexpr int kMaxBatch = 2048;
 
-// Warps per decode CTA (one CTA per SM): 16 for 2- and 4-bit codes with up to 4
-// query heads per kv head (compute-heavy per byte; 128 registers a thread),
-// else 12 (the kernel's DecodeWarps states the same).
-inline int decode_warps(int fmt, int g) {
-  return (g <= 4 && (fmt == KVQ_FMT_INT2 || fmt == KVQ_FMT_INT4)) ? 16 : 12;
+// Warps per decode CTA (one CTA per SM): 12, at most 168 registers a thread (the
+// kernel's DecodeWarps states the same).
+inline int decode_warps(int fmt) {
+  (void)fmt;
+  return 12;
 }
 
 // The decode-kernel instantiation that serves a layer's format.  A bf16 layer
