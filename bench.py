@@ -27,6 +27,7 @@ os.environ.setdefault("OMP_NUM_THREADS", "1")
 os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
+import dataclasses
 import datetime
 import json
 import math
@@ -249,7 +250,7 @@ class Layer:
             self.v_new = torch.empty_like(self.k_new)
             zero1 = torch.zeros(1, dtype=torch.int32, device=dev)
             for b in range(B):
-                wb = I.Workload(**{**w.__dict__, "batch": 1})
+                wb = dataclasses.replace(w, batch=1)
                 k, v = I.device_kv_bf16(wb, l, lens_after[b], dev, batch=1, seed_offset=seed_offset + 7 * b)
                 Tb = lens_before[b]
                 kvq.quantize_append(self.cfg, self.cache.seq_struct(b), k[:, :, :Tb].contiguous(),
@@ -304,8 +305,9 @@ def run_gpu(args, w, rank, world):
     replicas = args.replicas or max(1, min(4, math.ceil(3 * L2_BYTES / sbytes)))
     reps = []
     for rep in range(replicas):
+        ids = getattr(w, "layer_ids", range(len(w.layer_formats)))
         reps.append([Layer(kvq, torch, w, l, f, lens_before, n_app, dev, seed_offset=1000 * rep + 17 * rank)
-                     for l, f in enumerate(w.layer_formats)])
+                     for l, f in zip(ids, w.layer_formats)])
     torch.cuda.synchronize()
     for rep in reps:
         for lay in rep:
@@ -668,11 +670,17 @@ def main():
                     help="replay per-layer CUDA graphs of the library calls instead of calling the library directly")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (profiling captures; 0: all)")
+    ap.add_argument("--only-layers", default="",
+                    help="comma-separated layer indices to run (profiling captures of chosen layers)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     w = I.WORKLOADS[args.workload]()
     if args.layers:
         w.layer_formats = w.layer_formats[:args.layers]
+    if args.only_layers:
+        ids = [int(x) for x in args.only_layers.split(",")]
+        w.layer_formats = [w.layer_formats[i] for i in ids]
+        w.layer_ids = ids
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     peaks = {}

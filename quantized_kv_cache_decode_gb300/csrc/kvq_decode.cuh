@@ -96,7 +96,24 @@ struct FT {
   static constexpr int kTile = 16 * kRB;        // bytes of the 16 x 128 code matrix
   static constexpr int kWords = kRB / 8;        // operand words of one lane per code matrix
   static constexpr int kHalf = kFp8 ? 0 : (1 << (kBits - 1));
+  // Integer codes can enter the MMAs as f16 subnormals: a b-bit field placed in the
+  // low mantissa bits is exactly field * 2^-24 (one logic operation per two codes,
+  // no centring; the zero-points are applied in fp32 afterwards).  Fields above bit
+  // 0 carry a power-of-two factor, compensated where it lands (Value codes):
+  //   kVHi  the PV product of channels 16mb + 8 .. 15 (rows r + 8) relative to rows r
+  //   kW1   multiplier of the PV weights of tokens 8-15 (INT2: registers 2, 3 carry 16x
+  //         the factor of registers 0, 1)
+  // kKRaw: the Key codes take the subnormal path (else centred normal f16 values,
+  // code - 2^(b-1), with the zero-point term sum_c x_c (2^(b-1) - z_c)).  Measured on
+  // GB300: with 2- and 4-bit codes as subnormal B operands the QK sums lose precision
+  // (lse errors up to 2e-4 for INT2, 2e-5 for INT4, against 1e-6 with centred
+  // values); 8-bit codes keep it (3e-6), so only they take the cheaper path.  The
+  // Value codes (PV) take it for every width: the output error stays at its level.
+  static constexpr bool kKRaw = FMT == 8;
+  static constexpr float kVHi = FMT == 4 ? 16.f : FMT == 2 ? 4.f : 1.f;
+  static constexpr float kW1 = FMT == 2 ? 0.0625f : 1.f;
 };
+constexpr float kCodeUnit = 16777216.f;  // 2^24: a subnormal-placed code n reads as n * 2^-24
 
 // --------------------------------------------------------------------------
 // operand unpacking: packed codes -> centred f16 pairs (exact)
@@ -168,6 +185,45 @@ __device__ __forceinline__ void unpack_a(const uint32_t (&W)[N], int s, uint32_t
     e4m3x4_to_f16x4(W[2 * s], a0, a1);
     e4m3x4_to_f16x4(W[2 * s + 1], a2, a3);
   }
+}
+
+// Integer codes of step s as f16 subnormals (fields in the low mantissa bits), in
+// the same register order as unpack_a; the power-of-two factors of the fields
+// above bit 0 are listed in FT.  FP8 codes: unpack_a.
+template <int FMT, int N>
+__device__ __forceinline__ void unpack_raw(const uint32_t (&W)[N], int s, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                           uint32_t& a3) {
+  if constexpr (FMT == 4) {  // nibbles 0, 4 of each half (x1, x16); then the byte above them
+    const uint32_t w = W[s], w8 = w >> 8;
+    a0 = w & 0x000F000Fu;
+    a1 = w & 0x00F000F0u;
+    a2 = w8 & 0x000F000Fu;
+    a3 = w8 & 0x00F000F0u;
+  } else if constexpr (FMT == 2) {  // 2-bit fields at bits 0, 2, 4, 6 of each half (x1, x4, x16, x64)
+    const uint32_t w = (s & 1) ? (W[s >> 1] >> 8) : W[s >> 1];
+    a0 = w & 0x00030003u;
+    a1 = w & 0x000C000Cu;
+    a2 = w & 0x00300030u;
+    a3 = w & 0x00C000C0u;
+  } else if constexpr (FMT == 8) {  // bytes 0, 2 and bytes 1, 3 (moved down by a byte permute)
+    const uint32_t w0 = W[2 * s], w1 = W[2 * s + 1];
+    a0 = w0 & 0x00FF00FFu;
+    asm("prmt.b32 %0, %1, 0, 0x4341;" : "=r"(a1) : "r"(w0));
+    a2 = w1 & 0x00FF00FFu;
+    asm("prmt.b32 %0, %1, 0, 0x4341;" : "=r"(a3) : "r"(w1));
+  } else {
+    unpack_a<FMT>(W, s, a0, a1, a2, a3);
+  }
+}
+
+// 2^k with k chosen from the exponent of bound (> 0): bound * 2^k < 2^14 (at least
+// 2^13 for a normal bound), so every |x| <= bound scaled by it fits f16 with room;
+// inv = 2^-k.  No division: exponent arithmetic only (k within [-126, 102]).
+__device__ __forceinline__ float pow2_fit_f16(float bound, float& inv) {
+  const int eb = (__float_as_int(bound) >> 23) & 0xFF;  // biased exponent
+  const int ek = max(25, min(253, 267 - eb));           // biased exponent of 2^k = 2^(13 - (eb - 127))
+  inv = __int_as_float((254 - ek) << 23);
+  return __int_as_float(ek << 23);
 }
 
 // NGV consecutive floats (a token's Value scales or zero-points of all groups)
@@ -287,8 +343,9 @@ __device__ __forceinline__ void softmax_tile(WarpState<NGV>& st, const float (&s
 // lane computes each of its 32 products once and keeps both halves.
 // qrow: the column's query row in shared memory (a zero row for absent columns).
 
-// FP8 layers (one build per segment): x_c = q_c kappa, kappa = 16384 / max_c |q_c|;
-// kfac (the score multiplier) = kfac0 / kappa, kfac0 = log2(e) / sqrt(d) * the Key scale.
+// FP8 layers (one build per segment): x_c = q_c kappa, kappa the power of two that
+// brings max_c |q_c| into [2^13, 2^14); kfac (the score multiplier) = kfac0 / kappa,
+// kfac0 = log2(e) / sqrt(d) * the Key scale.
 __device__ __forceinline__ void build_x_fp8(const float* qrow, int q, float kfac0, uint32_t (&X)[8][4],
                                             float& kfac) {
   float mx = 0.f;
@@ -299,8 +356,8 @@ __device__ __forceinline__ void build_x_fp8(const float* qrow, int q, float kfac
   }
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-  float kap = 16384.f / mx;
-  if (!(mx > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
+  float inv;
+  const float kap = pow2_fit_f16(mx, inv);
   const float2 k2 = make_float2(kap, kap);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
@@ -308,7 +365,7 @@ __device__ __forceinline__ void build_x_fp8(const float* qrow, int q, float kfac
     split_f16x2(mul_f32x2(make_float2(x.x, x.y), k2), X[s][0], X[s][1]);
     split_f16x2(mul_f32x2(make_float2(x.z, x.w), k2), X[s][2], X[s][3]);
   }
-  kfac = kfac0 / kap;
+  kfac = kfac0 * inv;
 }
 
 // Max |q_c| of the lane's column (lane q reads channels 32q .. 32q + 31; the four lanes of a row combine).
@@ -324,17 +381,23 @@ __device__ __forceinline__ float column_qmax(const float* qrow, int q) {
 }
 
 // A Key group of an INT layer: x_c = q_c s_c (s_c: the Key scale of channel c),
-// with the zero-point term sum_c x_c (2^(b-1) - z_c), in one pass over the
-// channels: kappa = 16384 / (max_c |q_c| * max_c s_c) bounds |x_c kappa| by 16384
-// without first finding max_c |x_c| (qm: the column's max |q_c|, per segment).  A
-// smaller kappa than the exact one only moves the hi/lo split: the two f16 terms
-// still hold x_c kappa to about 22 bits, or to the f16 subnormal step (2^-24,
-// against elements up to 16384 times the bound ratio) for tiny x_c.
+// with the zero-point term sum_c x_c z_c, in one pass over the channels: kappa,
+// the power of two that brings max_c |q_c| * max_c s_c into [2^13, 2^14), bounds
+// |x_c kappa| by 2^14 without first finding max_c |x_c| (qm: the column's max
+// |q_c|, per segment).  A smaller kappa than the exact one only moves the hi/lo
+// split: the two f16 terms still hold x_c kappa to about 22 bits, or to the f16
+// subnormal step (2^-24, against elements up to 2^14 times the bound ratio) for
+// tiny x_c.  The codes are read as subnormals (n * 2^-24), so the score of a
+// token is (D * 2^24 / kappa - sum_c x_c z_c) * kfac0: kfac and cterm return those
+// two factors (centred codes: D / kappa and z_c - 2^(b-1) in place of z_c).
 template <int FMT>
 __device__ __forceinline__ void build_x_group(const float* qrow, const float* ks, const float* kz, int lane, int q,
                                               float kfac0, float qm, uint32_t (&X)[8][4], float& kfac,
                                               float& cterm) {
-  constexpr float kH = (float)FT<FMT>::kHalf;
+  using F = FT<FMT>;
+  // score = kfac0 (D / kappa(') - sum_c x_c (z_c - zh)): zh = 0 for subnormal codes (D sums
+  // x n), 2^(b-1) for centred codes (D sums x (n - 2^(b-1)))
+  constexpr float zh = F::kKRaw ? 0.f : (float)F::kHalf;
   // the largest Key scale of the group (scales are positive)
   float sm;
   {
@@ -343,10 +406,9 @@ __device__ __forceinline__ void build_x_group(const float* qrow, const float* ks
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sm = fmaxf(sm, __shfl_xor_sync(kFull, sm, o));
   }
-  const float bound = qm * sm;
-  float kap = 16384.f / bound;
-  if (!(bound > 0.f) || !(kap < 3.0e38f)) kap = 1.f;
-  const float2 k2 = make_float2(kap, kap), h2 = make_float2(kH, kH);
+  float inv;
+  const float kap = pow2_fit_f16(qm * sm, inv);
+  const float2 k2 = make_float2(kap, kap);
   float2 cz = make_float2(0.f, 0.f);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
@@ -355,8 +417,8 @@ __device__ __forceinline__ void build_x_group(const float* qrow, const float* ks
     const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
     const float2 x01 = mul_f32x2(make_float2(x.x, x.y), make_float2(s4.x, s4.y));
     const float2 x23 = mul_f32x2(make_float2(x.z, x.w), make_float2(s4.z, s4.w));
-    cz = fma_f32x2(x01, sub_f32x2(h2, make_float2(z4.x, z4.y)), cz);
-    cz = fma_f32x2(x23, sub_f32x2(h2, make_float2(z4.z, z4.w)), cz);
+    cz = fma_f32x2(x01, make_float2(z4.x - zh, z4.y - zh), cz);
+    cz = fma_f32x2(x23, make_float2(z4.z - zh, z4.w - zh), cz);
     split_f16x2(mul_f32x2(x01, k2), X[s][0], X[s][1]);
     split_f16x2(mul_f32x2(x23, k2), X[s][2], X[s][3]);
     asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
@@ -364,39 +426,45 @@ __device__ __forceinline__ void build_x_group(const float* qrow, const float* ks
   float c = cz.x + cz.y;
   c += __shfl_xor_sync(kFull, c, 1);
   c += __shfl_xor_sync(kFull, c, 2);
-  kfac = kfac0 / kap;
-  cterm = kfac0 * c;
+  kfac = kfac0 * (F::kKRaw ? inv * kCodeUnit : inv);
+  cterm = -kfac0 * c;
 }
 
 // Raw scores of one quantized tile for the lane's column: d[0..3] = tokens 2q, 2q + 1,
 // 2q + 8, 2q + 9.  Two MMAs per step: tokens 0-7 (Key fragment registers 0, 2 as
 // the B operand) and tokens 8-15 (registers 1, 3); D row r holds the high-half
-// product of column r, row r + 8 the low-half one.
+// product of column r, row r + 8 the low-half one.  Even and odd steps accumulate
+// apart (four independent MMA chains).  8-bit integer codes are the
+// subnormal-placed ones (FT::kKRaw), narrower ones centred.
 template <int FMT>
 __device__ __forceinline__ void qk_tile(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&X)[8][4],
                                         float (&d)[4]) {
-  float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+  float lo[2][4] = {}, hi[2][4] = {};
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     uint32_t k0, k1, k2, k3;
-    unpack_a<FMT>(KW, s, k0, k1, k2, k3);
-    mma_f16(lo, X[s][0], X[s][1], X[s][2], X[s][3], k0, k2);
-    mma_f16(hi, X[s][0], X[s][1], X[s][2], X[s][3], k1, k3);
+    if constexpr (FT<FMT>::kKRaw) unpack_raw<FMT>(KW, s, k0, k1, k2, k3);
+    else unpack_a<FMT>(KW, s, k0, k1, k2, k3);
+    mma_f16(lo[s & 1], X[s][0], X[s][1], X[s][2], X[s][3], k0, k2);
+    mma_f16(hi[s & 1], X[s][0], X[s][1], X[s][2], X[s][3], k1, k3);
   }
-  d[0] = lo[0] + lo[2];
-  d[1] = lo[1] + lo[3];
-  d[2] = hi[0] + hi[2];
-  d[3] = hi[1] + hi[3];
+  d[0] = (lo[0][0] + lo[0][2]) + (lo[1][0] + lo[1][2]);
+  d[1] = (lo[0][1] + lo[0][3]) + (lo[1][1] + lo[1][3]);
+  d[2] = (hi[0][0] + hi[0][2]) + (hi[1][0] + hi[1][2]);
+  d[3] = (hi[0][1] + hi[0][3]) + (hi[1][1] + hi[1][3]);
 }
 
-// PV of one quantized tile: o[mb] += V^T(channels 16mb..) * W(group of mb).
+// PV of one quantized tile: o[mb] += V^T(channels 16mb..) * W(group of mb).  Integer
+// codes are the subnormal-placed ones: rows r (channels 16mb + r) accumulate
+// n * 2^-24 * W, rows r + 8 FT::kVHi times that (INT2: the weights of tokens 8-15
+// carry FT::kW1).
 template <int FMT, int NGV>
 __device__ __forceinline__ void pv_tile(const uint32_t (&VW)[FT<FMT>::kWords], const uint32_t (&B0)[NGV],
                                         const uint32_t (&B1)[NGV], float (&o)[8][4]) {
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb) {
     uint32_t a0, a1, a2, a3;
-    unpack_a<FMT>(VW, mb, a0, a1, a2, a3);
+    unpack_raw<FMT>(VW, mb, a0, a1, a2, a3);
     mma_f16(o[mb], a0, a1, a2, a3, B0[mb * NGV / 8], B1[mb * NGV / 8]);
   }
 }
@@ -430,7 +498,9 @@ __device__ __forceinline__ void bf16_qk(const uint8_t* stg, const float* qrow, i
 }
 
 // PV of a bf16 tile from its V rows (rows past the end zeroed); W = pt * f split
-// into two bf16 terms.
+// into two bf16 terms.  RH: factor of rows r + 8 (so that the accumulators keep
+// the scale the quantized tiles of the layer give them; f carries the rest).
+template <int RH>
 __device__ __forceinline__ void bf16_pv(const uint8_t* stg, int lane, const float (&pt)[4], float f,
                                         float (&o)[8][4]) {
   const int mi = lane >> 3, x = lane & 7;  // row (lane & 7) + 8 (mi >> 1), chunk 2 mb + (mi & 1), swizzled
@@ -442,6 +512,11 @@ __device__ __forceinline__ void bf16_pv(const uint8_t* stg, int lane, const floa
   for (int mb = 0; mb < 8; ++mb) {
     uint32_t a0, a1, a2, a3;
     ldmatrix_x4_trans(lbase + 32 * (mb ^ (x >> 1)), a0, a1, a2, a3);
+    if constexpr (RH != 1) {  // exact: a power of two on bf16 values
+      constexpr uint32_t kRh = dup16((uint32_t)(127 + (RH == 16 ? 4 : 2)) << 7);  // bf16 bits of 16 or 4
+      asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(a1) : "r"(kRh));
+      asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(a3) : "r"(kRh));
+    }
     mma_bf16(o[mb], a0, a1, a2, a3, h01, h23);
     mma_bf16(o[mb], a0, a1, a2, a3, l01, l23);
   }
@@ -1022,7 +1097,9 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
             __syncwarp();
             float pr[4];
             softmax_tile<NGV, false>(stt, sig_bf, 1.f, q, pr);
-            bf16_pv(vst, lane, pr, stt.inv_S * kPrescale, stt.o);
+            // integer layers: the accumulators hold code units (2^-24, rows r + 8 FT::kVHi more)
+            constexpr float kUnit = F::kInt ? 1.f / kCodeUnit : 1.f;
+            bf16_pv<F::kInt ? (int)F::kVHi : 1>(vst, lane, pr, stt.inv_S * (kPrescale * kUnit), stt.o);
           }
         } else if (vmask && alive) {
           // ---- quantized stage: tiles [tg.a, tg.a + n), walked in smem, one softmax step each ----
@@ -1083,18 +1160,22 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               B0[0] = pack_f16(pt[0] * f, pt[1] * f);
               B1[0] = pack_f16(pt[2] * f, pt[3] * f);
             } else {
-              constexpr float kH = (float)F::kHalf;
               const float f = stt.inv_S * kPrescale;
 #pragma unroll
               for (int jg = 0; jg < NGV; ++jg) {  // one Value group at a time: few live registers
                 float w[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  w[e] = pt[e] * (vsp[tk[e] * NGV + jg] * f);
-                  stt.zacc[jg] = fmaf(w[e], kH - vzp[tk[e] * NGV + jg], stt.zacc[jg]);
-                }
+                for (int e = 0; e < 4; ++e) w[e] = pt[e] * (vsp[tk[e] * NGV + jg] * f);
                 B0[jg] = pack_f16(w[0], w[1]);
-                B1[jg] = pack_f16(w[2], w[3]);
+                B1[jg] = pack_f16(w[2] * F::kW1, w[3] * F::kW1);
+                // the zero-point sum with the weights the MMA multiplies (rounded to f16)
+                const float2 r0 = unpack_f16(B0[jg]), r1 = unpack_f16(B1[jg]);
+                float z = stt.zacc[jg];
+                z = fmaf(r0.x, vzp[tk[0] * NGV + jg], z);
+                z = fmaf(r0.y, vzp[tk[1] * NGV + jg], z);
+                z = fmaf(r1.x * (1.f / F::kW1), vzp[tk[2] * NGV + jg], z);
+                z = fmaf(r1.y * (1.f / F::kW1), vzp[tk[3] * NGV + jg], z);
+                stt.zacc[jg] = z;
               }
             }
             {
@@ -1133,16 +1214,19 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
         zo[0][jg] = __shfl_sync(kFull, z, 8 * q);
         zo[1][jg] = __shfl_sync(kFull, z, 8 * q + 4);
       }
-      // o = sum of W * (Value operand) with W = p s kPrescale / S
+      // o = sum of W * (Value operand) with W = p s kPrescale / S; integer layers: the
+      // accumulators hold code units (2^-24 on rows r, FT::kVHi times that on rows r + 8)
+      // and the zero-point sum sum W z is subtracted
       const float unit = stt.S / kPrescale;
+      constexpr float kC0 = F::kInt ? kCodeUnit : 1.f, kC1 = F::kInt ? kCodeUnit / F::kVHi : 1.f;
 #pragma unroll
       for (int e = 0; e < 2; ++e)
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
           const bool empty = mo[e] == -INFINITY;
           const float z = F::kInt ? zo[e][mb * NGV / 8] : 0.f;
-          stt.o[mb][e] = empty ? 0.f : (stt.o[mb][e] + z) * unit;
-          stt.o[mb][2 + e] = empty ? 0.f : (stt.o[mb][2 + e] + z) * unit;
+          stt.o[mb][e] = empty ? 0.f : fmaf(stt.o[mb][e], kC0, -z) * unit;
+          stt.o[mb][2 + e] = empty ? 0.f : fmaf(stt.o[mb][2 + e], kC1, -z) * unit;
         }
       // ---- fold the warps pairwise into NW/2 merge records: warp w + NW/2 writes record w, then
       // warp w folds its own state into it ----
