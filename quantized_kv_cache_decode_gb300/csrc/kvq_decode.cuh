@@ -621,8 +621,10 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // BF: the layer may have bf16 tiles (sink or residual tokens); the variant without
 // them (FP8 layers with no sink tokens) carries no bf16-tile code at all.  MQ:
 // several query tokens per sequence (causal limits per column); only that
-// variant carries the limit checks.
-template <int FMT, int NGV, bool BF, bool MQ>
+// variant carries the limit checks.  ONE: integer layers whose Key groups are one
+// tile each (G = 16, the paged blocks): every tile rebuilds the query-side
+// operand, in straight-line code.
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE>
 __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
   constexpr int NW = DecodeWarps<FMT>::kNW;
@@ -813,8 +815,13 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           p_a = max(si.ql, si.al + k * it);
           p_end = min(si.qh, si.al + (k + 1) * it);
           p_first = true;
-          q_rec = p_a / L.tpg;
-          q_pos = p_a - q_rec * L.tpg;
+          if (L.tpg == 1) {
+            q_rec = p_a;
+            q_pos = 0;
+          } else {
+            q_rec = p_a / L.tpg;
+            q_pos = p_a - q_rec * L.tpg;
+          }
         } else {
           pk = 0;
           ++ps;
@@ -897,9 +904,14 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
         const int n = min(tps, p_end - p_a);
         const bool hdr0 = F::kInt && p_first && q_pos != 0;  // the group's header, copied to slot offset 0
         int l_rec = q_rec, l_pos = q_pos + n - 1;              // the last tile's record and position
-        while (l_pos >= L.tpg) {
-          l_pos -= L.tpg;
-          ++l_rec;
+        if (L.tpg == 1) {
+          l_rec = q_rec + n - 1;
+          l_pos = 0;
+        } else {
+          while (l_pos >= L.tpg) {
+            l_pos -= L.tpg;
+            ++l_rec;
+          }
         }
         tg.kind = 3;
         tg.a = p_a;
@@ -914,7 +926,26 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           my_tbl[lane] = x < L.mbps ? __ldg(&p.C.block_table[(long long)sg.b * L.mbps + x]) : -1;
           __syncwarp();
         }
-        if (lane == 0) {
+        if (L.paged && L.tpg == 1) {
+          // one tile per record (blocks of 16 tokens): lane j copies record q_rec + j whole
+          // (header inline) to stage offset j * rec_bytes, all lanes at once; the stage
+          // barrier expects the bytes of the records whose block is inside the pool
+          uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
+          const uint32_t bar = smem_addr(&my_bars[slot]);
+          int blk = -1;
+          if (lane < n) blk = my_tbl[q_rec + lane - tb_base];
+          const bool ok = lane < n && blk >= 0 && blk < L.num_blocks;
+          const uint32_t okm = __ballot_sync(kFull, ok);
+          if (lane < n && !ok) report(p.status, KVQ_DEV_BAD_BLOCK);
+          if (lane == 0 && okm) mbar_arrive_expect_tx(bar, (uint32_t)__popc(okm) * (uint32_t)L.rec_bytes);
+          __syncwarp();
+          if (ok)
+            bulk_copy_g2s(smem_addr(dst + lane * L.rec_bytes),
+                          reinterpret_cast<const uint8_t*>(p.C.block_pool) + (long long)blk * L.block_bytes +
+                              (long long)sg.h * L.rec_bytes,
+                          (uint32_t)L.rec_bytes, bar);
+          vm = okm;
+        } else if (lane == 0) {
           uint8_t* dst = my_stages + (size_t)slot * p.stage_bytes;
           const uint32_t bar = smem_addr(&my_bars[slot]);
           if (!L.paged) {
@@ -1102,25 +1133,15 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
             bf16_pv<F::kInt ? (int)F::kVHi : 1>(vst, lane, pr, stt.inv_S * (kPrescale * kUnit), stt.o);
           }
         } else if (vmask && alive) {
-          // ---- quantized stage: tiles [tg.a, tg.a + n), walked in smem, one softmax step each ----
-          const int n = tg.n;
-          int walk = 0;               // smem offset of the next tile (headers inline)
-          int rpos = tg.rpos;         // position of tile tg.a + k in its record
-          for (int k = 0; k < n; ++k) {
-            const int i = tg.a + k;
-            const bool hdr = F::kInt && (rpos == 0 || (tg.first && k == 0));
-            const int hoff = walk;
-            if (hdr) walk += L.hdr_bytes;
-            const uint8_t* tile = stg + walk;
-            walk += L.tile_bytes;
-            if (++rpos == L.tpg) rpos = 0;
-            if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
+          // ---- quantized stage: tiles [tg.a, tg.a + n), one softmax step each ----
+          // tile i at `tile`; INT: `hdrp` the Key-group header, the query-side operand (q * s,
+          // hi/lo) rebuilt from it when `build` (at each record, i.e. Key group, start)
+          auto tile_step = [&](const int i, const uint8_t* tile, const uint8_t* hdrp, const bool build) {
             if constexpr (F::kInt) {
-              // the group's query-side operand (q * s, hi/lo), rebuilt at each record (Key group) start
-              if (hdr)
-                build_x_group<FMT>(qrow, reinterpret_cast<const float*>(stg + hoff),
-                                   reinterpret_cast<const float*>(stg + hoff + 512), lane, q, p.scale_log2, qm, X,
-                                   kfac, cterm);
+              if (build)
+                build_x_group<FMT>(qrow, reinterpret_cast<const float*>(hdrp),
+                                   reinterpret_cast<const float*>(hdrp + 512), lane, q, p.scale_log2, qm, X, kfac,
+                                   cterm);
             }
             // QK
             float d[4];
@@ -1182,6 +1203,29 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               uint32_t VW[F::kWords];
               load_words(tile + F::kTile, lane, VW);
               pv_tile<FMT, NGV>(VW, B0, B1, stt.o);
+            }
+          };
+          const int n = tg.n;
+          if constexpr (ONE) {
+            // one tile per record (16-token Key groups): record k of the stage at k * rec_bytes,
+            // every tile starts a group (straight-line code: the build overlaps the rest)
+            for (int k = 0; k < n; ++k) {
+              if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
+              const uint8_t* rec = stg + k * L.rec_bytes;
+              tile_step(tg.a + k, rec + L.hdr_bytes, rec, true);
+            }
+          } else {
+            int walk = 0;        // smem offset of the next tile (headers inline)
+            int rpos = tg.rpos;  // position of tile tg.a + k in its record
+            for (int k = 0; k < n; ++k) {
+              const bool hdr = F::kInt && (rpos == 0 || (tg.first && k == 0));
+              const int hoff = walk;
+              if (hdr) walk += L.hdr_bytes;
+              const uint8_t* tile = stg + walk;
+              walk += L.tile_bytes;
+              if (++rpos == L.tpg) rpos = 0;
+              if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
+              tile_step(tg.a + k, tile, stg + hoff, hdr);
             }
           }
         }
@@ -1439,7 +1483,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, bool BF, bool MQ>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1448,39 +1492,46 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-template <int FMT, int NGV, bool BF, bool MQ>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE>
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, BF, MQ><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV, BF, MQ, ONE><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 // FP8 layers without sink tokens (no bf16 tiles) take the variant without the bf16
-// path; several query tokens per sequence take the multi-query variant.
+// path; several query tokens per sequence take the multi-query variant; integer
+// layers with one tile per Key group the straight-line variant.
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
   if constexpr (FT<FMT>::kFp8) {
     if (p.L.S == 0)
-      return p.n_query > 1 ? launch_variant<FMT, NGV, false, true>(p, smem, stream)
-                           : launch_variant<FMT, NGV, false, false>(p, smem, stream);
+      return p.n_query > 1 ? launch_variant<FMT, NGV, false, true, false>(p, smem, stream)
+                           : launch_variant<FMT, NGV, false, false, false>(p, smem, stream);
+    return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, false>(p, smem, stream)
+                         : launch_variant<FMT, NGV, true, false, false>(p, smem, stream);
+  } else {
+    if (p.L.tpg == 1)
+      return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, true>(p, smem, stream)
+                           : launch_variant<FMT, NGV, true, false, true>(p, smem, stream);
+    return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, false>(p, smem, stream)
+                         : launch_variant<FMT, NGV, true, false, false>(p, smem, stream);
   }
-  return p.n_query > 1 ? launch_variant<FMT, NGV, true, true>(p, smem, stream)
-                       : launch_variant<FMT, NGV, true, false>(p, smem, stream);
 }
 
 // Resident CTAs per SM (the variant with the bf16 path, the larger one; several
 // query tokens: the multi-query variant).
 template <int FMT, int NGV, bool MQ>
 cudaError_t occupancy_variant(int smem, int* n) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, true, MQ>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, true, MQ, false>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false>,
                                                        DecodeWarps<FMT>::kThreads, smem);
 }
 template <int FMT, int NGV>
