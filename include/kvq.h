@@ -85,8 +85,8 @@ typedef struct {
   int32_t num_kv_heads;       /* H_kv >= 1 */
   int32_t head_dim;           /* d, must be 128 */
   int32_t format;             /* kvq_format */
-  int32_t k_group_tokens;     /* G: tokens per Key group (per-channel scale); multiple of 16; 1 for FP8;
-                                 ignored for bf16 */
+  int32_t k_group_tokens;     /* G: tokens per Key group (per-channel scale); multiple of 16, at most 256
+                                 (KVQ_ERR_UNSUPPORTED above); 1 for FP8; ignored for bf16 */
   int32_t v_group_dims;       /* Gv: channels per Value group (per-token scale); 16,32,64,128; FP8: 128;
                                  ignored for bf16 */
   int32_t residual_tokens;    /* R >= 0 bf16 recent tokens kept (0 for FP8; ignored for bf16) */
@@ -203,7 +203,7 @@ kvq_status kvq_fp8_calibrate_format(const void* x, size_t n, int32_t format, flo
  * store them), s2 (affine formula), s3 (Key per channel over G tokens, Value
  * per token over Gv channels, full-precision residual window), s4 (FP8);
  * [W4KV] (sink tokens kept 16-bit).
- *   k_new, v_new  device bf16 [batch][H][n_new][d]
+ *   k_new, v_new  device bf16 [batch][H][n_new][d], 16-byte aligned
  *   seq_lens      device int32 [batch]: tokens already in the cache (before)
  * Tokens t < S go to the sink; otherwise to the residual ring; every time the
  * ring reaches R + G tokens its oldest G are quantized as one Key group (per
@@ -212,7 +212,7 @@ kvq_status kvq_fp8_calibrate_format(const void* x, size_t n, int32_t format, flo
  * Gv-channel group, same formula).  FP8: code = E4M3 (or E5M2) RNE satfinite
  * of fp32(x / s_tensor).  bf16 layers: the token is copied to row t - S of the
  * residual buffers, never quantized.  Result identical to n_new single-token
- * appends.
+ * appends (integer layers: at most 65535 * G tokens per call).
  * The caller advances seq_lens by n_new afterwards, and for a paged store has
  * the blocks of every group that spills already in the block table.
  * Device errors: KVQ_DEV_CAPACITY (store full: nothing written for that

@@ -62,6 +62,7 @@ kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
     L->Gv = cfg->v_group_dims;
     L->R = cfg->residual_tokens;
     if (L->G < 16 || L->G % 16 != 0 || L->R < 0) return KVQ_ERR_INVALID_ARG;
+    if (L->G > kMaxGroupTokens) return KVQ_ERR_UNSUPPORTED;
     if (L->Gv != 16 && L->Gv != 32 && L->Gv != 64 && L->Gv != 128) return KVQ_ERR_INVALID_ARG;
     L->W = L->R + L->G;
   }
@@ -326,7 +327,8 @@ kvq_status kvq_quantize_append(const kvq_layer_config* cfg, const kvq_layer_cach
   if ((st = check_cache(L, cache)) != KVQ_OK) return st;
   if (batch < 0 || batch > kMaxBatch || n_new < 0) return KVQ_ERR_INVALID_ARG;
   if (batch == 0 || n_new == 0) return KVQ_OK;
-  if (!k_new || !v_new || !seq_lens) return KVQ_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !seq_lens || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  if (!L.fp8 && !L.bf16 && ((long long)n_new + L.G - 1) / L.G > 65535) return KVQ_ERR_UNSUPPORTED;
   AppendParams p;
   p.L = L;
   p.C = make_ptrs(cache);
@@ -416,6 +418,8 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.tps = G.tps;
   // a claimed work item: whole records, at least a stage's worth of tiles
   p.item_tiles = (std::max(G.tps, L.tpg) + L.tpg - 1) / L.tpg * L.tpg;
+  // one tile per Key group: items of two stages (half the claims; a CTA still has hundreds of items)
+  if (!L.fp8 && !L.bf16 && L.tpg == 1) p.item_tiles = 2 * G.tps;
   // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
   p.bf_weight = std::max(1, (8192 + L.tile_bytes / 2) / L.tile_bytes);
   p.bf_joint = bf16_joint(G.stage_bytes) ? 1 : 0;

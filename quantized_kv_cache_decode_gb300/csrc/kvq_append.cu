@@ -18,6 +18,7 @@
 namespace kvq {
 
 constexpr int kAppendThreads = 128;
+constexpr unsigned kFull32 = 0xffffffffu;
 
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   uint16_t v;
@@ -50,10 +51,10 @@ __device__ __forceinline__ uint8_t* record_w(const LayerDesc& L, const CachePtrs
   return const_cast<uint8_t*>(record_addr(L, C, b, h, r, status));
 }
 
-// One CTA per (sequence, kv head).  Dynamic smem: K and V of one group as fp32
-// [G][128] each, their codes [G][128] bytes each, and one V tile staging buffer.
+// One CTA per (sequence, kv head): FP8 tokens (encoded one by one), bf16 rows of
+// the residual window (integer layers: only the tokens that stay there after the
+// groups that spill, which spill_kernel quantizes) and sink rows.
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
   const LayerDesc& L = p.L;
   const int b = blockIdx.x / L.H, h = blockIdx.x % L.H;
   const int tid = threadIdx.x;
@@ -100,92 +101,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
       tile[16 * L.rb + byte] = L.e5m2 ? f32_to_e5m2(vd) : f32_to_e4m3(vd);
     }
   } else {
-    const int G = L.G, levels = (1 << L.bits) - 1;
-    const float flev = (float)levels;
-    float* kf = reinterpret_cast<float*>(smem);         // [G][128]
-    float* vf = kf + G * 128;                           // [G][128]
-    uint8_t* kq = reinterpret_cast<uint8_t*>(vf + G * 128);  // [G][128]
-    uint8_t* vq = kq + G * 128;                          // [G][128]
-    uint32_t* tile = reinterpret_cast<uint32_t*>(vq + G * 128);  // one tile's K and V codes (2 * 16 * rb bytes)
-    for (int grp = t0s.qn / G; grp < t1s.qn / G; ++grp) {
-      const long long x0 = (long long)grp * G;  // first quantized index of the group
-      // gather the group's tokens: old ones from the ring, new ones from the input
-      for (int i = tid; i < G * 128; i += kAppendThreads) {
-        const int tt = i >> 7, c = i & 127;
-        const long long t = L.S + x0 + tt;
-        float kx, vx;
-        if (t < T0) {
-          const long long slot = (t - L.S) % L.W;
-          kx = __bfloat162float(ring_k[(pair * L.W + slot) * L.d + c]);
-          vx = __bfloat162float(ring_v[(pair * L.W + slot) * L.d + c]);
-        } else {
-          kx = __bfloat162float(knew[(t - T0) * L.d + c]);
-          vx = __bfloat162float(vnew[(t - T0) * L.d + c]);
-        }
-        kf[i] = kx;
-        vf[i] = vx;
-      }
-      __syncthreads();
-      // the group is record grp (G = 16 * tpg tokens): header = K scale, K zero; then G/16 tiles
-      uint8_t* rec = record_w(L, p.C, b, h, grp, tid == 0 ? p.status : nullptr);
-      if (rec) {
-        float* ks = reinterpret_cast<float*>(rec);
-        float* kz = ks + 128;
-        // Keys: per channel over the G tokens (thread = channel)
-        {
-          const int c = tid;
-          float mn = kf[c], mx = kf[c];
-          for (int tt = 1; tt < G; ++tt) {
-            mn = fminf(mn, kf[tt * 128 + c]);
-            mx = fmaxf(mx, kf[tt * 128 + c]);
-          }
-          float z;
-          const float s = affine_params(mn, mx, flev, z);
-          for (int tt = 0; tt < G; ++tt) kq[tt * 128 + c] = (uint8_t)affine_code(kf[tt * 128 + c], s, z, levels);
-          ks[c] = s;
-          kz[c] = z;
-        }
-        // Values: per token over Gv channels
-        for (int item = tid; item < G * L.ngv; item += kAppendThreads) {
-          const int tt = item / L.ngv, j = item % L.ngv;
-          const float* row = vf + tt * 128 + j * L.Gv;
-          float mn = row[0], mx = row[0];
-          for (int c = 1; c < L.Gv; ++c) {
-            mn = fminf(mn, row[c]);
-            mx = fmaxf(mx, row[c]);
-          }
-          float z;
-          const float s = affine_params(mn, mx, flev, z);
-          uint8_t* qrow = vq + tt * 128 + j * L.Gv;
-          for (int c = 0; c < L.Gv; ++c) qrow[c] = (uint8_t)affine_code(row[c], s, z, levels);
-          float* tvs = reinterpret_cast<float*>(rec + L.hdr_bytes + (long long)(tt / 16) * L.tile_bytes + 32 * L.rb);
-          tvs[(tt % 16) * L.ngv + j] = s;
-          tvs[16 * L.ngv + (tt % 16) * L.ngv + j] = z;
-        }
-        __syncthreads();
-        // K and V codes of each 16-token tile, in fragment order
-        const int tile_words = 2 * 16 * L.rb / 4;  // K part, then V part
-        uint32_t* vtile = tile + 16 * L.rb / 4;
-        for (int t16 = 0; t16 < G / 16; ++t16) {
-          for (int i = tid; i < tile_words; i += kAppendThreads) tile[i] = 0u;
-          __syncthreads();
-          for (int i = tid; i < 16 * 128; i += kAppendThreads) {
-            const int tt = i >> 7, c = i & 127;
-            int byte, bit;
-            ktile_pos(L.bits, false, tt, c, byte, bit);
-            atomicOr(&tile[byte >> 2], (uint32_t)kq[(t16 * 16 + tt) * 128 + c] << ((byte & 3) * 8 + bit));
-            vtile_pos(L.bits, false, tt, c, byte, bit);
-            atomicOr(&vtile[byte >> 2], (uint32_t)vq[(t16 * 16 + tt) * 128 + c] << ((byte & 3) * 8 + bit));
-          }
-          __syncthreads();
-          uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes);
-          for (int i = tid; i < tile_words; i += kAppendThreads) dst[i] = tile[i];
-          __syncthreads();
-        }
-      }
-      __syncthreads();
-    }
-    // new tokens that stay in the bf16 residual window
+    // integer layers: the groups that spill are quantized by spill_kernel; here only the
+    // new tokens that stay in the bf16 residual window (bf16 layers: every token after the sink)
     const long long rfirst = (T0 > L.S + t1s.qn) ? T0 : (long long)L.S + t1s.qn;
     for (long long t = rfirst; t < T1; ++t) {
       const long long slot = (t - L.S) % L.W;
@@ -202,26 +119,225 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   }
 }
 
-cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
-  const int blocks = p.batch * p.L.H;
-  if (blocks == 0 || p.n_new == 0) return cudaSuccess;
-  size_t smem = 0;
-  if (!p.L.fp8 && !p.L.bf16) smem = (size_t)p.L.G * 128 * (4 + 4 + 1 + 1) + 2 * 16 * (size_t)p.L.rb;
+// ---------------------------------------------------------------------------
+// spill_kernel: the Key groups (and their G Value tokens) that leave the residual
+// window in this append, quantized and written in fragment order.
+// One CTA of 256 threads per (sequence, kv head, spilled group): the group's G
+// bf16 Key and Value rows are staged in shared memory (coalesced 16-byte loads,
+// from the ring for tokens already cached, from the input for new ones); every
+// channel's Key min/max is found by two threads over half the tokens each, every
+// (token, Gv-channel group) Value min/max by a segmented warp-shuffle reduction;
+// then each 32-bit word of the tile's fragment-order code matrices is assembled
+// in registers (the inverse of the layout formula: which (token, channel) each
+// field of the word holds) and stored once, consecutive threads on consecutive
+// words.  The arithmetic of each code is the same IEEE fp32 sequence as above.
+// With `rest` the CTAs of group 0 also write the sink rows and the new rows that
+// stay in the residual window (one-token appends: those rows are never read by
+// the spill of the same call; longer appends write them in a second launch).
+// ---------------------------------------------------------------------------
+constexpr int kSpillThreads = 256;
+
+// (step, reg, half) of the b-bit field at bit bp of operand word w: the inverse
+// of frag_pos for the integer formats
+template <int BITS>
+__device__ __forceinline__ void frag_field(int w, int bp, int& step, int& reg, int& h) {
+  if constexpr (BITS == 4) {
+    step = w;
+    reg = (bp & 15) >> 2;
+    h = bp >> 4;
+  } else if constexpr (BITS == 2) {
+    h = bp >> 4;
+    const int rem = bp & 15;
+    step = 2 * w + (rem >> 3);
+    reg = (rem & 7) >> 1;
+  } else {
+    step = w >> 1;
+    const int bi = bp >> 3;
+    reg = 2 * (w & 1) + (bi & 1);
+    h = bi >> 1;
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams p, int rest) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const LayerDesc& L = p.L;
+  constexpr int kLevels = (1 << BITS) - 1;
+  constexpr float kFLevels = (float)kLevels;
+  constexpr int kRB = 128 * BITS / 8;        // bytes of one token row of codes
+  constexpr int kWPart = 16 * kRB / 4;       // operand words of one code matrix
+  constexpr int kFields = 32 / BITS;         // codes per word
+  const int b = blockIdx.x / L.H, h = blockIdx.x % L.H;
+  const int gi = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long pair = (long long)b * L.H + h;
+  const long long T0 = p.seq_lens[b];
+  const long long T1 = T0 + p.n_new;
+  if (T0 < 0 || T1 > max_tokens(L)) {
+    if (gi == 0 && tid == 0) report(p.status, KVQ_DEV_CAPACITY);
+    return;
+  }
+  const __nv_bfloat16* knew = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + pair * p.n_new * L.d;
+  const __nv_bfloat16* vnew = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + pair * p.n_new * L.d;
+  __nv_bfloat16* ring_k = reinterpret_cast<__nv_bfloat16*>(p.C.resid_k);
+  __nv_bfloat16* ring_v = reinterpret_cast<__nv_bfloat16*>(p.C.resid_v);
+  const TokenSplit t0s = split_tokens((int)T0, L);
+  const TokenSplit t1s = split_tokens((int)T1, L);
+  const int G = L.G, ngv = L.ngv, Gv = L.Gv;
+  const int ng = (t1s.qn - t0s.qn) / G;  // groups that spill in this call
+
+  if (gi < ng) {
+    const int grp = t0s.qn / G + gi;
+    const long long x0 = (long long)grp * G;  // first quantized index of the group
+    uint8_t* rec = record_w(L, p.C, b, h, grp, tid == 0 ? p.status : nullptr);
+    if (rec) {  // (uniform over the CTA)
+      __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem);  // [G][128]
+      __nv_bfloat16* Vs = Ks + G * 128;                             // [G][128]
+      float* ksz = reinterpret_cast<float*>(Vs + G * 128);          // K scale [128], K zero [128]
+      float* red = ksz + 256;                                       // [2 halves][min, max][128]
+      float* vsz = red + 512;                                       // V scale [G][ngv], V zero [G][ngv]
+      // stage the group's rows: 16-byte chunk ch of row tt, K then V
+      for (int idx = tid; idx < 2 * G * 16; idx += kSpillThreads) {
+        const int which = idx >= G * 16, rem = idx - which * G * 16, tt = rem >> 4, ch = rem & 15;
+        const long long t = L.S + x0 + tt;
+        const __nv_bfloat16* src;
+        if (t < T0) src = (which ? ring_v : ring_k) + (pair * L.W + (t - L.S) % L.W) * L.d;
+        else src = (which ? vnew : knew) + (t - T0) * L.d;
+        reinterpret_cast<uint4*>((which ? Vs : Ks) + tt * 128)[ch] = reinterpret_cast<const uint4*>(src)[ch];
+      }
+      __syncthreads();
+      // Keys, per channel over the G tokens: two halves of the tokens, then the pair combined
+      {
+        const int c = tid & 127, half = tid >> 7, h0 = half * (G >> 1), h1 = h0 + (G >> 1);
+        float mn = __bfloat162float(Ks[h0 * 128 + c]), mx = mn;
+        for (int tt = h0 + 1; tt < h1; ++tt) {
+          const float x = __bfloat162float(Ks[tt * 128 + c]);
+          mn = fminf(mn, x);
+          mx = fmaxf(mx, x);
+        }
+        red[half * 256 + c] = mn;
+        red[half * 256 + 128 + c] = mx;
+      }
+      // Values, per token and Gv-channel group: lane holds channels 4 lane .. 4 lane + 3
+      {
+        const int seg = Gv >> 2;  // lanes per Value group
+        for (int tt = warp; tt < G; tt += kSpillThreads / 32) {
+          const uint2 raw = reinterpret_cast<const uint2*>(Vs + tt * 128)[lane];
+          const float2 a = unpack_bf16(raw.x), c2 = unpack_bf16(raw.y);
+          float mn = fminf(fminf(a.x, a.y), fminf(c2.x, c2.y)), mx = fmaxf(fmaxf(a.x, a.y), fmaxf(c2.x, c2.y));
+          for (int o = 1; o < seg; o <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(kFull32, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull32, mx, o));
+          }
+          if ((lane & (seg - 1)) == 0) {
+            const int j = lane / seg;
+            float z;
+            const float sc = affine_params(mn, mx, kFLevels, z);
+            vsz[tt * ngv + j] = sc;
+            vsz[G * ngv + tt * ngv + j] = z;
+            float* tv = reinterpret_cast<float*>(rec + L.hdr_bytes + (long long)(tt >> 4) * L.tile_bytes + 32 * kRB);
+            tv[(tt & 15) * ngv + j] = sc;
+            tv[16 * ngv + (tt & 15) * ngv + j] = z;
+          }
+        }
+      }
+      __syncthreads();
+      if (tid < 128) {
+        const float mn = fminf(red[tid], red[256 + tid]), mx = fmaxf(red[128 + tid], red[384 + tid]);
+        float z;
+        const float sc = affine_params(mn, mx, kFLevels, z);
+        ksz[tid] = sc;
+        ksz[128 + tid] = z;
+        reinterpret_cast<float*>(rec)[tid] = sc;         // header: K scale [128]
+        reinterpret_cast<float*>(rec)[128 + tid] = z;    //         K zero  [128]
+      }
+      __syncthreads();
+      // the codes, word by word in memory order (word m of a part: lane (m >> 2) & 31,
+      // operand word ((m >> 7) << 2) | (m & 3))
+      for (int t16 = 0; t16 < (G >> 4); ++t16) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes);
+        for (int m = tid; m < 2 * kWPart; m += kSpillThreads) {
+          const int part = m >= kWPart, mm = m - part * kWPart;
+          const int l = (mm >> 2) & 31, w = ((mm >> 7) << 2) | (mm & 3);
+          uint32_t word = 0;
+#pragma unroll
+          for (int f = 0; f < kFields; ++f) {
+            int step, reg, hh;
+            frag_field<BITS>(w, f * BITS, step, reg, hh);
+            const int i = (l >> 2) + 8 * (reg & 1), k = 2 * (l & 3) + hh + 8 * (reg >> 1);
+            uint32_t code;
+            if (!part) {  // Keys: rows = tokens, column k holds channel 16 step + 4 ((k & 7) >> 1) + (k & 1) + 2 (k >> 3)
+              const int c = 16 * step + 4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3);
+              const float x = __bfloat162float(Ks[(t16 * 16 + i) * 128 + c]);
+              code = affine_code(x, ksz[c], ksz[128 + c], kLevels);
+            } else {      // Values: rows = channels 16 step + i, columns = tokens
+              const int c = 16 * step + i, tt = t16 * 16 + k, j = c / Gv;
+              const float x = __bfloat162float(Vs[tt * 128 + c]);
+              code = affine_code(x, vsz[tt * ngv + j], vsz[G * ngv + tt * ngv + j], kLevels);
+            }
+            word |= code << (f * BITS);
+          }
+          dst[m] = word;
+        }
+      }
+    }
+  }
+  if (rest && gi == 0) {
+    // sink rows, and the new rows that stay in the residual window (16-byte chunks)
+    __nv_bfloat16* sink_k = reinterpret_cast<__nv_bfloat16*>(p.C.sink_k);
+    __nv_bfloat16* sink_v = reinterpret_cast<__nv_bfloat16*>(p.C.sink_v);
+    const long long rfirst = (T0 > L.S + t1s.qn) ? T0 : (long long)L.S + t1s.qn;
+    const int n = (int)(T1 - T0);
+    for (int idx = tid; idx < 2 * n * 16; idx += kSpillThreads) {
+      const int which = idx >= n * 16, rem = idx - which * n * 16, j = rem >> 4, ch = rem & 15;
+      const long long t = T0 + j;
+      const __nv_bfloat16* src = (which ? vnew : knew) + (long long)j * L.d;
+      __nv_bfloat16* dst = nullptr;
+      if (t < L.S) dst = (which ? sink_v : sink_k) + (pair * L.S + t) * L.d;
+      else if (t >= rfirst) dst = (which ? ring_v : ring_k) + (pair * L.W + (t - L.S) % L.W) * L.d;
+      if (dst) reinterpret_cast<uint4*>(dst)[ch] = reinterpret_cast<const uint4*>(src)[ch];
+    }
+  }
+}
+
+template <int BITS>
+cudaError_t launch_spill_t(const AppendParams& p, int groups, int rest, cudaStream_t stream) {
+  const size_t smem = (size_t)p.L.G * 128 * 2 * 2 + (256 + 512) * 4 + (size_t)p.L.G * p.L.ngv * 8;
+  static std::mutex mu;
+  static int set_for[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   {
-    // the limit is a per-device attribute that persists: raise it once per size
-    static std::mutex mu;
-    static int set_for[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 64 || set_for[dev] < (int)smem) {
-      e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(spill_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) set_for[dev] = (int)smem;
     }
   }
-  append_kernel<<<blocks, kAppendThreads, smem, stream>>>(p);
+  spill_kernel<BITS><<<dim3(p.batch * p.L.H, groups), kSpillThreads, smem, stream>>>(p, rest);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
+  const int blocks = p.batch * p.L.H;
+  if (blocks == 0 || p.n_new == 0) return cudaSuccess;
+  if (p.L.fp8 || p.L.bf16) {
+    append_kernel<<<blocks, kAppendThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // integer layers: at most ceil(n_new / G) groups spill per (sequence, head)
+  const int groups = (int)(((long long)p.n_new + p.L.G - 1) / p.L.G);
+  const int fused = p.n_new == 1;  // one new token: its row never aliases a ring row the spill reads
+  cudaError_t e;
+  switch (p.L.bits) {
+    case 2: e = launch_spill_t<2>(p, groups, fused, stream); break;
+    case 4: e = launch_spill_t<4>(p, groups, fused, stream); break;
+    default: e = launch_spill_t<8>(p, groups, fused, stream); break;
+  }
+  if (e != cudaSuccess || fused) return e;
+  append_kernel<<<blocks, kAppendThreads, 0, stream>>>(p);  // window and sink rows after the spills
   return cudaGetLastError();
 }
 

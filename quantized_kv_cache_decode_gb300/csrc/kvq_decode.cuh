@@ -325,9 +325,12 @@ __device__ __forceinline__ void softmax_tile(WarpState<NGV>& st, const float (&s
     st.S = S_new;
     st.inv_S = 1.f / S_new;
   }
+  // ex2(-inf) = +0 for masked scores; the reference is -inf only while every score seen
+  // so far (this tile's included) is -inf, then 0 stands in for it
+  const float ms = st.m == -INFINITY ? 0.f : st.m;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    pr[e] = (sig[e] == -INFINITY) ? 0.f : fast_exp2(sig[e] - st.m);
+    pr[e] = fast_exp2(sig[e] - ms);
     st.l += pr[e];
   }
 }
@@ -390,14 +393,36 @@ __device__ __forceinline__ float column_qmax(const float* qrow, int q) {
 // tiny x_c.  The codes are read as subnormals (n * 2^-24), so the score of a
 // token is (D * 2^24 / kappa - sum_c x_c z_c) * kfac0: kfac and cterm return those
 // two factors (centred codes: D / kappa and z_c - 2^(b-1) in place of z_c).
+template <int FMT, bool SCALE>
+__device__ __forceinline__ void build_x_pass(const float* qrow, const float* ks, const float* kz, int q, float kap,
+                                             uint32_t (&X)[8][4], float2& cz) {
+  using F = FT<FMT>;
+  constexpr float zh = F::kKRaw ? 0.f : (float)F::kHalf;
+  const float2 k2 = make_float2(kap, kap);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
+    const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
+    const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
+    float2 x01 = mul_f32x2(make_float2(x.x, x.y), make_float2(s4.x, s4.y));
+    float2 x23 = mul_f32x2(make_float2(x.z, x.w), make_float2(s4.z, s4.w));
+    cz = fma_f32x2(x01, make_float2(z4.x - zh, z4.y - zh), cz);
+    cz = fma_f32x2(x23, make_float2(z4.z - zh, z4.w - zh), cz);
+    if constexpr (SCALE) {
+      x01 = mul_f32x2(x01, k2);
+      x23 = mul_f32x2(x23, k2);
+    }
+    split_f16x2(x01, X[s][0], X[s][1]);
+    split_f16x2(x23, X[s][2], X[s][3]);
+    asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
+  }
+}
+
 template <int FMT>
 __device__ __forceinline__ void build_x_group(const float* qrow, const float* ks, const float* kz, int lane, int q,
                                               float kfac0, float qm, uint32_t (&X)[8][4], float& kfac,
                                               float& cterm) {
   using F = FT<FMT>;
-  // score = kfac0 (D / kappa(') - sum_c x_c (z_c - zh)): zh = 0 for subnormal codes (D sums
-  // x n), 2^(b-1) for centred codes (D sums x (n - 2^(b-1)))
-  constexpr float zh = F::kKRaw ? 0.f : (float)F::kHalf;
   // the largest Key scale of the group (scales are positive)
   float sm;
   {
@@ -406,28 +431,15 @@ __device__ __forceinline__ void build_x_group(const float* qrow, const float* ks
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sm = fmaxf(sm, __shfl_xor_sync(kFull, sm, o));
   }
+  float2 cz = make_float2(0.f, 0.f);
   float inv;
   const float kap = pow2_fit_f16(qm * sm, inv);
-  const float2 k2 = make_float2(kap, kap);
-  float2 cz = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
-    const float4 s4 = *reinterpret_cast<const float4*>(ks + 16 * s + 4 * q);
-    const float4 z4 = *reinterpret_cast<const float4*>(kz + 16 * s + 4 * q);
-    const float2 x01 = mul_f32x2(make_float2(x.x, x.y), make_float2(s4.x, s4.y));
-    const float2 x23 = mul_f32x2(make_float2(x.z, x.w), make_float2(s4.z, s4.w));
-    cz = fma_f32x2(x01, make_float2(z4.x - zh, z4.y - zh), cz);
-    cz = fma_f32x2(x23, make_float2(z4.z - zh, z4.w - zh), cz);
-    split_f16x2(mul_f32x2(x01, k2), X[s][0], X[s][1]);
-    split_f16x2(mul_f32x2(x23, k2), X[s][2], X[s][3]);
-    asm volatile("" ::: "memory");  // one step's loads at a time: keeps the build's registers few
-  }
+  build_x_pass<FMT, true>(qrow, ks, kz, q, kap, X, cz);
   float c = cz.x + cz.y;
   c += __shfl_xor_sync(kFull, c, 1);
   c += __shfl_xor_sync(kFull, c, 2);
   kfac = kfac0 * (F::kKRaw ? inv * kCodeUnit : inv);
-  cterm = -kfac0 * c;
+  cterm = -kfac0 * c;  // score = (D * kfac) + cterm
 }
 
 // Raw scores of one quantized tile for the lane's column: d[0..3] = tokens 2q, 2q + 1,
@@ -1056,6 +1068,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
         build_x_fp8(qrow, q, p.scale_log2 * __ldg(p.C.k_tscale), X, kfac);
       } else {
         qm = column_qmax(qrow, q);
+
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) X[s2][0] = X[s2][1] = X[s2][2] = X[s2][3] = 0u;
       }
@@ -1153,7 +1166,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
             const int tok_valid = min(16, sg.qn - i * 16);  // < 16 only for a partial FP8 tile
             float sig[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sig[e] = (hv && tk[e] < tok_valid) ? fmaf(d[e], kfac, cterm) : -INFINITY;
+            for (int e = 0; e < 4; ++e)  // integer tiles are always full (Key groups of 16k tokens)
+              sig[e] = (hv && (F::kInt || tk[e] < tok_valid)) ? fmaf(d[e], kfac, cterm) : -INFINITY;
             if (MQ && p.n_query > 1) {
               const int lim = col_limit() - (L.S + 16 * i);  // in tile rows (quantized token x = t - S)
 #pragma unroll

@@ -11,6 +11,7 @@ namespace kvq {
 constexpr int kHeadDim = 128;
 constexpr int kMaxGqa = 8;
 constexpr int kMaxBatch = 2048;
+constexpr int kMaxGroupTokens = 256;  // Key group length the append kernel stages in shared memory
 
 // Warps per decode CTA (one CTA per SM): 12, at most 168 registers a thread (the
 // kernel's DecodeWarps states the same).

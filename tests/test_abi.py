@@ -88,6 +88,8 @@ def test_cache_layout_sizes(kvq):
     (dict(fmt="bf16", num_kv_heads=2, G=0, Gv=0, R=0, S=1, capacity_tokens=0), -1),
     (dict(fmt="bf16", num_kv_heads=2, G=0, Gv=0, R=0, S=0, paged=True, block_tokens=16, num_blocks=4,
           max_blocks_per_seq=2), -2),
+    # Key groups longer than the append kernel stages in shared memory (256 tokens)
+    (dict(fmt="int4", num_kv_heads=2, G=272, Gv=128, R=0, S=0, capacity_tokens=272), -2),
 ])
 def test_config_validation(kvq, kw, status):
     kw = dict(kw)
@@ -168,3 +170,15 @@ def test_fragment_order_lane_words():
         c = np.arange(128)[None, :]
         assert np.array_equal((kb // 16) % 32, 4 * (t % 8) + (c // 4) % 4 + 0 * c)
         assert np.array_equal((vb // 16) % 32, 4 * (c % 8) + (t % 8) // 2)
+
+
+def test_append_rejects_unaligned_inputs_before_any_launch(kvq):
+    # the spill kernel stages new rows with 16-byte loads: k_new / v_new must be 16-byte aligned
+    # (the cache pointers below are fake, aligned and never dereferenced: the call returns first)
+    cfg = kvq.make_config("int4", 2, 32, 128, 32, 0, capacity_tokens=64)
+    cache = kvq.LayerCache()
+    cache.qstore, cache.resid_k, cache.resid_v = 1 << 20, 2 << 20, 3 << 20
+    for kn, vn in ((4096 + 2, 8192), (4096, 8192 + 8)):
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.quantize_append(cfg, cache, kn, vn, 1, 16, 1, stream=0)
+        assert e.value.status == -1
