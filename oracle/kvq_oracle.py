@@ -56,6 +56,13 @@ Readings where the pages leave a step open:
   (``Q_n = max(0, floor((T - S - R) / G)) * G``); FP8 uses G = 1, R = 0;
 * attention is computed in fp64 on the dequantized values ``s*(q - z)``
   (also in fp64), ``lse = max + ln(sum exp(score - max))`` (natural log).
+* pre-RoPE Keys ("KV Cache Quantization Analysis", section 3, the RoPE bullet:
+  the rotation mixes channel pairs and smears the Key outliers, so KVQuant
+  quantizes Keys before RoPE; section 4, KVQuant item (ii)): a layer with
+  ``rope_base > 0`` stores its Keys as given (before the rotation) and attention
+  rotates each dequantized Key at its own position t, rotate-half pairing
+  ``(c, c + d/2)``, angle ``t * rope_base^(-2i/d)`` for pair i, in fp64; the
+  query arrives already rotated at its own position.
 """
 from __future__ import annotations
 
@@ -232,6 +239,7 @@ class Spec:
     Gv: int = 128     # Value group (channels)
     R: int = 0        # residual window (bf16)
     S: int = 0        # sink tokens (bf16)
+    rope_base: float = 0.0  # > 0: Keys stored before RoPE, rotated at their position by attention
 
     @property
     def bits(self) -> int:
@@ -414,6 +422,37 @@ def dequantized_f32(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
 
 
 # --------------------------------------------------------------------------- #
+# pre-RoPE Keys ("KV Cache Quantization Analysis", section 3 RoPE bullet; section 4 KVQuant (ii))
+# --------------------------------------------------------------------------- #
+
+
+def rope_angles(positions: np.ndarray, d: int, base: float) -> np.ndarray:
+    """Angles [len(positions), d/2] in fp64: position t times base^(-2i/d) for pair i."""
+    inv_freq = np.power(float(base), -np.arange(0, d, 2, dtype=np.float64) / d)
+    return np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]
+
+
+def rope_rotate(x: np.ndarray, positions: np.ndarray, base: float) -> np.ndarray:
+    """Rotate-half RoPE of rows x [n, d] at the given positions, in fp64: channel pair
+    (i, i + d/2) turned by the angle of pair i (x_i cos - x_{i+d/2} sin, x_{i+d/2} cos + x_i sin)."""
+    x = np.asarray(x, dtype=np.float64)
+    h = x.shape[-1] // 2
+    a = rope_angles(positions, x.shape[-1], base)
+    c, s_ = np.cos(a), np.sin(a)
+    lo, hi = x[..., :h], x[..., h:]
+    return np.concatenate([lo * c - hi * s_, hi * c + lo * s_], axis=-1)
+
+
+def attention_keys(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
+    """(Keys, Values) in fp64 as attention sees them: the dequantized cache, the Keys
+    rotated at their positions 0 .. T-1 when the layer stores them before RoPE."""
+    k, v = dequantized_f64(hc)
+    if hc.spec.rope_base > 0:
+        k = rope_rotate(k, np.arange(k.shape[0]), hc.spec.rope_base)
+    return k, v
+
+
+# --------------------------------------------------------------------------- #
 # C4 -- decode attention, softmax(q K^T / sqrt(d)) V, in fp64
 # "W4A16 + KV ...", section "오차가 어디서 만나는가" (score formula)
 # --------------------------------------------------------------------------- #
@@ -446,7 +485,7 @@ def decode_attention(q: np.ndarray, caches: List[List[HeadCache]], softmax_scale
     lse = np.zeros((B, Hq))
     for b in range(B):
         for h in range(Hkv):
-            k_hat, v_hat = dequantized_f64(caches[b][h])
+            k_hat, v_hat = attention_keys(caches[b][h])
             for j in range(g):
                 hq = h * g + j
                 out[b, hq], lse[b, hq] = attend_head(q[b, hq], k_hat, v_hat, scale)
@@ -471,7 +510,7 @@ def decode_attention_multi(q: np.ndarray, caches: List[List[HeadCache]], softmax
     lse = np.zeros((B, M, Hq))
     for b in range(B):
         for h in range(Hkv):
-            k_hat, v_hat = dequantized_f64(caches[b][h])
+            k_hat, v_hat = attention_keys(caches[b][h])
             T = k_hat.shape[0]
             for i in range(M):
                 n = max(0, T - M + i + 1)

@@ -575,3 +575,73 @@ def test_dequantized_f32_fp8_worked_values(fmt, codes, k_scale, v_scale, k_expec
     assert np.array_equal(ko[1:, 0].view(np.uint32), want_k.view(np.uint32))   # sign of zero included
     assert np.array_equal(vo[1:, 0].view(np.uint32), want_v.view(np.uint32))
     assert np.all(ko[1:] == ko[1:, :1]) and np.all(vo[1:] == vo[1:, :1])
+
+
+# --------------------------------------------------------------------------- #
+# pre-RoPE Keys ("KV Cache Quantization Analysis", section 3 RoPE bullet; section 4 KVQuant (ii))
+# --------------------------------------------------------------------------- #
+
+
+def _rope_brute(x, t, base):
+    """Rotate-half RoPE of one vector at position t, plain Python (math.cos / math.sin)."""
+    d = len(x)
+    h = d // 2
+    out = [0.0] * d
+    for i in range(h):
+        a = t * base ** (-(2 * i) / d)
+        out[i] = float(x[i]) * math.cos(a) - float(x[i + h]) * math.sin(a)
+        out[i + h] = float(x[i + h]) * math.cos(a) + float(x[i]) * math.sin(a)
+    return out
+
+
+def test_rope_closed_forms():
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((6, 16))
+    base = 10000.0
+    # position 0 is the identity
+    assert np.array_equal(O.rope_rotate(x, np.zeros(6), base), x)
+    # a rotation by t then by -t is the identity; every channel pair keeps its norm
+    t = np.array([1, 5, 17, 300, 4095, 65535], dtype=np.float64)
+    y = O.rope_rotate(x, t, base)
+    assert np.allclose(O.rope_rotate(y, -t, base), x, rtol=0, atol=1e-12)
+    assert np.allclose(y[:, :8] ** 2 + y[:, 8:] ** 2, x[:, :8] ** 2 + x[:, 8:] ** 2, rtol=0, atol=1e-12)
+    # the score of a rotated query and a rotated key depends only on their distance
+    q, k = rng.standard_normal((1, 16)), rng.standard_normal((1, 16))
+    def score(m, n):
+        return float((O.rope_rotate(q, [m], base) @ O.rope_rotate(k, [n], base).T)[0, 0])
+    for m, n in ((5, 2), (40, 37), (1003, 1000)):
+        assert abs(score(m, n) - score(3, 0)) < 1e-12
+    assert abs(score(7, 7) - float((q @ k.T)[0, 0])) < 1e-12
+    # the pairing and the angles against a plain-Python rotation (d = 8)
+    x8 = rng.standard_normal(8)
+    for tt in (0, 1, 9, 1234):
+        assert np.allclose(O.rope_rotate(x8[None], [tt], 500000.0)[0], _rope_brute(x8, tt, 500000.0), rtol=0,
+                           atol=1e-12)
+
+
+@pytest.mark.parametrize("spec", [
+    O.Spec("int4", d=16, G=8, Gv=8, R=4, S=1, rope_base=10000.0),
+    O.Spec("int8", d=16, G=16, Gv=4, R=2, S=0, rope_base=500000.0),
+    O.Spec("int2", d=16, G=4, Gv=16, R=8, S=2, rope_base=10000.0),
+])
+def test_attention_over_pre_rope_keys_brute_force(spec):
+    # every dequantized Key (sink, quantized, residual) is rotated at its own position
+    rng = np.random.default_rng(13)
+    B, Hkv, g, T = 2, 2, 3, 37
+    q = rng.standard_normal((B, Hkv * g, 16)).astype(F32)
+    caches = [[O.build_head_cache((rng.standard_normal((T, 16)) * 2).astype(F32),
+                                  rng.standard_normal((T, 16)).astype(F32), spec) for _ in range(Hkv)]
+              for _ in range(B)]
+    out, lse = O.decode_attention(q, caches)
+    for b in range(B):
+        for hq in range(Hkv * g):
+            K, V = _dequant_brute(caches[b][hq // g])
+            K = [_rope_brute(K[t], t, spec.rope_base) for t in range(T)]
+            o, l = _brute_attention(q[b, hq], K, V, 1 / math.sqrt(16))
+            assert np.allclose(out[b, hq], o, rtol=0, atol=1e-11)
+            assert abs(lse[b, hq] - l) < 1e-11
+    # the stored cache is the same as without RoPE (Keys quantized before the rotation)
+    plain = O.Spec(spec.fmt, d=16, G=spec.G, Gv=spec.Gv, R=spec.R, S=spec.S)
+    k = rng.standard_normal((T, 16)).astype(F32)
+    v = rng.standard_normal((T, 16)).astype(F32)
+    _same_cache(O.build_head_cache(k, v, spec), O.build_head_cache(k, v, plain))
