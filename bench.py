@@ -211,11 +211,12 @@ class Layer:
             nblk = [math.ceil(q / P) for q in qmax]
             mbps = max(nblk + [1])
             self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, paged=True, block_tokens=P,
-                                       num_blocks=max(1, sum(nblk)), max_blocks_per_seq=mbps)
+                                       num_blocks=max(1, sum(nblk)), max_blocks_per_seq=mbps, rope_base=fmt.rope_base)
         else:
             unit = 16 if fp8 else max(16, G)
             cap = max(unit, math.ceil(max(qmax) / unit) * unit)
-            self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, capacity_tokens=cap)
+            self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, capacity_tokens=cap,
+                                       rope_base=fmt.rope_base)
         self.cache = kvq.CacheLayer(self.cfg, B, device=dev, zero=False)
         if w.paged:
             perm = torch.from_numpy(I.block_permutation(w, max(1, sum(nblk)), l)).to(dev)
@@ -467,7 +468,7 @@ def oracle_pairs(w, layer, pairs):
     lens_after = lens_after_step(w)
     n_app = max(1, w.append_tokens)
     spec = O.Spec(fmt.fmt, d=128, G=1 if is_fp8(fmt) else fmt.G, Gv=fmt.Gv,
-                  R=0 if is_fp8(fmt) else fmt.R, S=fmt.S)
+                  R=0 if is_fp8(fmt) else fmt.R, S=fmt.S, rope_base=fmt.rope_base)
     q = O.bf16_to_f32(I.q_bf16(w, layer))
     items = []
     for b, h in pairs:

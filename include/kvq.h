@@ -97,6 +97,12 @@ typedef struct {
                                  bf16: tokens after the sink per (seq, head), >= 1 */
   int32_t num_blocks;         /* paged: blocks in the pool */
   int32_t max_blocks_per_seq; /* paged: row length of the block table */
+  float rope_base;            /* 0: Keys are used as stored.  > 1: pre-RoPE Keys -- the layer's Keys are
+                                 appended (and quantized) before the rotary position embedding, and the
+                                 decode rotates each dequantized Key at its position t: channel pair
+                                 (i, i + 64) turned by t * rope_base^(-2i/128) (rotate-half pairing;
+                                 the query is passed already rotated).  Integer formats with Gv of 64 or
+                                 128, one query token (KVQ_ERR_UNSUPPORTED otherwise). */
 } kvq_layer_config;
 
 /*

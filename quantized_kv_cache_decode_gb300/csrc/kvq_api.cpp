@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "kvq_internal.h"
@@ -36,6 +37,13 @@ kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
   L->rb = L->d * L->bits / 8;
   L->S = cfg->sink_tokens;
   if (L->S < 0) return KVQ_ERR_INVALID_ARG;
+  L->rope_base = cfg->rope_base;
+  L->rope = cfg->rope_base != 0.f;
+  if (L->rope) {
+    if (!(cfg->rope_base > 1.f) || !(cfg->rope_base < 3.0e38f)) return KVQ_ERR_INVALID_ARG;
+    if (f == KVQ_FMT_BF16 || f == KVQ_FMT_FP8_E4M3 || f == KVQ_FMT_FP8_E5M2) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->v_group_dims != 64 && cfg->v_group_dims != 128) return KVQ_ERR_UNSUPPORTED;
+  }
   if (L->bf16) {
     // every token after the sink lives in the bf16 buffers, row t - S; nothing is quantized
     if (cfg->paged) return KVQ_ERR_UNSUPPORTED;
@@ -234,7 +242,8 @@ struct DecodeGeom {
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, int multi = 0) {
   const int wsc = merge_bytes_of(L, g);
   const int nw = decode_warps(kernel_format(L.fmt));
-  const int fixed = fixed_smem(batch, wsc, nw);
+  // pre-RoPE Keys: each warp keeps a copy of its current Key group's header (1 KB)
+  const int fixed = fixed_smem(batch, wsc, nw) + (L.rope ? nw * 1024 : 0);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -393,6 +402,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
   if (n_query < 1 || num_q_heads / L.H * n_query > kMaxGqa) return KVQ_ERR_INVALID_ARG;
+  if (L.rope && n_query > 1) return KVQ_ERR_UNSUPPORTED;
   if ((st = check_cache(L, cache)) != KVQ_OK) return st;
   if (batch == 0) return KVQ_OK;
   if (!q || !seq_lens || !workspace || !aligned16(workspace) || !(softmax_scale == softmax_scale))
@@ -435,6 +445,16 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.out = out;
   p.out_bf16 = out_bf16;
   p.lse = lse;
+  if (L.rope) {
+    // pair i turns by theta_i = base^(-2i/128) per position: its angle in turns, as a 64-bit
+    // fraction, so that t * rope_turn[i] (mod 2^64) is the angle of position t reduced exactly
+    for (int i = 0; i < 64; ++i) {
+      const double theta = std::pow((double)L.rope_base, -2.0 * i / 128.0);
+      double turn = theta / (2.0 * 3.14159265358979323846);
+      turn -= std::floor(turn);
+      p.rope_turn[i] = (unsigned long long)(turn * 18446744073709551616.0);
+    }
+  }
   cudaError_t e;
   switch (kernel_format(L.fmt)) {
     case KVQ_FMT_INT2: e = launch_decode_int2(p, G.smem, s); break;

@@ -535,6 +535,196 @@ __device__ __forceinline__ void bf16_pv(const uint8_t* stg, int lane, const floa
 }
 
 // --------------------------------------------------------------------------
+// pre-RoPE Keys: rotation at the Key's position inside the decode
+// --------------------------------------------------------------------------
+// Keys of a layer with rope_base > 0 are stored before the rotary embedding
+// ("KV Cache Quantization Analysis", section 3, the RoPE bullet: the rotation
+// mixes channel pairs and smears the per-channel outliers, so KVQuant quantizes
+// Keys before it; section 4, KVQuant item (ii)).  The decode dequantizes each Key
+// to fp32, turns channel pair (i, i + 64) by t * theta_i (t: the Key's position),
+// and multiplies the rotated Key, split in two f16 terms, with the query (already
+// rotated by the caller) on the tensor cores.  In the fragment order of the Key
+// codes channel c and c + 64 sit in the same lane (steps s and s + 4), so the
+// rotation needs no data exchange.
+
+// cos and sin of the angle of position t for a pair whose angle per position is
+// `turn` (a turn fraction, 64-bit fixed point): the top 32 bits of t * turn
+// (mod 2^64) are the angle modulo one turn, read as a signed fraction in [-1/2, 1/2)
+__device__ __forceinline__ void rope_cs(unsigned long long turn, int t, float& c, float& s) {
+  const uint32_t fl = (uint32_t)turn, fh = (uint32_t)(turn >> 32);
+  const uint32_t top = __umulhi((uint32_t)t, fl) + (uint32_t)t * fh;
+  const float a = (float)(int32_t)top * 1.46291807926715968e-09f;  // 2 pi / 2^32
+  __sincosf(a, &s, &c);
+}
+
+// the power of two that keeps every rotated Key of a group below 2^14: the group's
+// Keys are s_c (n - z_c) with n in [0, L], so |Key| <= s_c (|z_c| + L) and a
+// rotation grows a component by at most sqrt(2) (lane l reads channels 4l .. 4l + 3)
+template <int FMT>
+__device__ __forceinline__ float rope_group_scale(const float* ks, const float* kz, int lane, float& inv) {
+  constexpr float kL = (float)((1 << FT<FMT>::kBits) - 1);
+  const float4 s4 = *reinterpret_cast<const float4*>(ks + 4 * lane);
+  const float4 z4 = *reinterpret_cast<const float4*>(kz + 4 * lane);
+  float m = fmaxf(fmaxf(s4.x * (fabsf(z4.x) + kL), s4.y * (fabsf(z4.y) + kL)),
+                  fmaxf(s4.z * (fabsf(z4.z) + kL), s4.w * (fabsf(z4.w) + kL)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  return pow2_fit_f16(2.f * m, inv);
+}
+
+// Raw scores (d * kfac: the score in the log2 domain) of one quantized tile with the
+// Keys rotated at positions t0 + token: the same MMA layout as qk_tile, the Key
+// operand being the rotated fp32 Keys scaled by kapk in two f16 terms (four MMAs per step).
+template <int FMT>
+__device__ __forceinline__ void qk_tile_rope(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&X)[8][4],
+                                             const float* ks, const float* kz, const unsigned long long* turn, int t0,
+                                             int r, int q, float kapk, float (&d)[4]) {
+  constexpr float kH = (float)FT<FMT>::kHalf;
+  float lo[2][4] = {}, hi[2][4] = {};
+  const int tpos[2] = {t0 + r, t0 + r + 8};
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t a[4], b[4];
+    unpack_a<FMT>(KW, s, a[0], a[1], a[2], a[3]);      // channels 16s + 4q + e (centred codes)
+    unpack_a<FMT>(KW, s + 4, b[0], b[1], b[2], b[3]);  // channels 16s + 64 + 4q + e
+    const int c0 = 16 * s + 4 * q;
+    const float4 sl = *reinterpret_cast<const float4*>(ks + c0), zl = *reinterpret_cast<const float4*>(kz + c0);
+    const float4 sh = *reinterpret_cast<const float4*>(ks + c0 + 64), zh = *reinterpret_cast<const float4*>(kz + c0 + 64);
+    const float slo[4] = {sl.x, sl.y, sl.z, sl.w}, zlo[4] = {zl.x, zl.y, zl.z, zl.w};
+    const float shi[4] = {sh.x, sh.y, sh.z, sh.w}, zhi[4] = {zh.x, zh.y, zh.z, zh.w};
+    const ulonglong2 u01 = *reinterpret_cast<const ulonglong2*>(turn + c0);
+    const ulonglong2 u23 = *reinterpret_cast<const ulonglong2*>(turn + c0 + 2);
+    const unsigned long long tu[4] = {u01.x, u01.y, u23.x, u23.y};
+    float cs[2][4], sn[2][4];  // [token r / r + 8][channel 4q + e]
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rope_cs(tu[e], tpos[tt], cs[tt][e], sn[tt][e]);
+    uint32_t kh[4][2], kl[4][2];  // register reg of steps s (0) and s + 4 (1), high / low f16 terms
+#pragma unroll
+    for (int reg = 0; reg < 4; ++reg) {
+      const int tt = reg & 1, e0 = 2 * (reg >> 1);
+      const float2 u = unpack_f16(a[reg]), w = unpack_f16(b[reg]);
+      // Keys s (n - z) in fp32 (n - 2^(b-1) is exact in the f16 operand)
+      const float x0 = slo[e0] * ((u.x + kH) - zlo[e0]), x1 = slo[e0 + 1] * ((u.y + kH) - zlo[e0 + 1]);
+      const float y0 = shi[e0] * ((w.x + kH) - zhi[e0]), y1 = shi[e0 + 1] * ((w.y + kH) - zhi[e0 + 1]);
+      const float ca = cs[tt][e0], sa = sn[tt][e0], cb = cs[tt][e0 + 1], sb = sn[tt][e0 + 1];
+      split_f16x2(make_float2((x0 * ca - y0 * sa) * kapk, (x1 * cb - y1 * sb) * kapk), kh[reg][0], kl[reg][0]);
+      split_f16x2(make_float2((y0 * ca + x0 * sa) * kapk, (y1 * cb + x1 * sb) * kapk), kh[reg][1], kl[reg][1]);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int st = s + 4 * j;
+      mma_f16(lo[j], X[st][0], X[st][1], X[st][2], X[st][3], kh[0][j], kh[2][j]);
+      mma_f16(lo[j], X[st][0], X[st][1], X[st][2], X[st][3], kl[0][j], kl[2][j]);
+      mma_f16(hi[j], X[st][0], X[st][1], X[st][2], X[st][3], kh[1][j], kh[3][j]);
+      mma_f16(hi[j], X[st][0], X[st][1], X[st][2], X[st][3], kl[1][j], kl[3][j]);
+    }
+  }
+  d[0] = (lo[0][0] + lo[0][2]) + (lo[1][0] + lo[1][2]);
+  d[1] = (lo[0][1] + lo[0][3]) + (lo[1][1] + lo[1][3]);
+  d[2] = (hi[0][0] + hi[0][2]) + (hi[1][0] + hi[1][2]);
+  d[3] = (hi[0][1] + hi[0][3]) + (hi[1][1] + hi[1][3]);
+}
+
+// Scores of a bf16 tile (sink / residual rows, stored before RoPE) with its Keys
+// rotated at their positions (row r: pos_a, row r + 8: pos_b): K rows through ldmatrix
+// (natural channel order: channel c and c + 64 in steps s and s + 4 of the same lane),
+// rotated in fp32, scaled by a power of two from the tile's largest |Key| and split in
+// two f16 terms; the query column (q * kapq, hi/lo) in A rows r, r + 8.  kfacq:
+// the score multiplier of the query scale.  Rows past `rows` masked.
+__device__ __forceinline__ void bf16_qk_rope(const uint8_t* stg, const float* qrow, int lane, int q, bool hv, int rows,
+                                             float kapq, float kfacq, const unsigned long long* turn, int pos_a,
+                                             int pos_b, float (&sig)[4]) {
+  // the largest |Key| of the tile's rows (16-byte chunk lane + 32 j is in row (lane >> 4) + 2 j)
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if ((lane >> 4) + 2 * j >= rows) continue;
+    const uint4 v = reinterpret_cast<const uint4*>(stg)[lane + 32 * j];
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = unpack_bf16(w4[k]);
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  float invk;
+  const float kapk = pow2_fit_f16(2.f * m, invk);
+  const int x = lane & 7;
+  const uint32_t lbase =
+      smem_addr(stg) + ((lane & 7) + 8 * ((lane >> 3) & 1)) * 256 + 16 * ((lane >> 4) ^ (x & 1));
+  float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+  const int tpos[2] = {pos_a, pos_b};
+  const float2 kq = make_float2(kapq, kapq);
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t a[4], b[4];  // rows r / r + 8, channels 16s + 2q + {0, 1} (regs 0, 1) and 16s + 8 + 2q + {0, 1} (2, 3)
+    ldmatrix_x4(lbase + 32 * (s ^ (x >> 1)), a[0], a[1], a[2], a[3]);
+    ldmatrix_x4(lbase + 32 * ((s + 4) ^ (x >> 1)), b[0], b[1], b[2], b[3]);
+    const int cbase[2] = {16 * s + 2 * q, 16 * s + 8 + 2 * q};
+    float cs[2][4], sn[2][4];  // [row r / r + 8][pair 2h + j: channel cbase[h] + j]
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) rope_cs(turn[cbase[h] + j], tpos[tt], cs[tt][2 * h + j], sn[tt][2 * h + j]);
+    uint32_t kh[4][2], kl[4][2];
+#pragma unroll
+    for (int reg = 0; reg < 4; ++reg) {
+      const int tt = reg & 1, h = reg >> 1;
+      const float2 u = unpack_bf16(a[reg]), w = unpack_bf16(b[reg]);
+      const float ca = cs[tt][2 * h], sa = sn[tt][2 * h], cb = cs[tt][2 * h + 1], sb = sn[tt][2 * h + 1];
+      split_f16x2(make_float2((u.x * ca - w.x * sa) * kapk, (u.y * cb - w.y * sb) * kapk), kh[reg][0], kl[reg][0]);
+      split_f16x2(make_float2((w.x * ca + u.x * sa) * kapk, (w.y * cb + u.y * sb) * kapk), kh[reg][1], kl[reg][1]);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int st = s + 4 * j;
+      uint32_t x0h, x0l, x2h, x2l;  // the query column, channels 16 st + 2q .. and 16 st + 8 + 2q ..
+      const float2 q0 = *reinterpret_cast<const float2*>(qrow + 16 * st + 2 * q);
+      const float2 q2 = *reinterpret_cast<const float2*>(qrow + 16 * st + 8 + 2 * q);
+      split_f16x2(mul_f32x2(q0, kq), x0h, x0l);
+      split_f16x2(mul_f32x2(q2, kq), x2h, x2l);
+      mma_f16(lo, x0h, x0l, x2h, x2l, kh[0][j], kh[2][j]);
+      mma_f16(lo, x0h, x0l, x2h, x2l, kl[0][j], kl[2][j]);
+      mma_f16(hi, x0h, x0l, x2h, x2l, kh[1][j], kh[3][j]);
+      mma_f16(hi, x0h, x0l, x2h, x2l, kl[1][j], kl[3][j]);
+    }
+  }
+  const float f = kfacq * invk;
+  const int t0 = 2 * q;
+  sig[0] = (hv && t0 < rows) ? (lo[0] + lo[2]) * f : -INFINITY;
+  sig[1] = (hv && t0 + 1 < rows) ? (lo[1] + lo[3]) * f : -INFINITY;
+  sig[2] = (hv && t0 + 8 < rows) ? (hi[0] + hi[2]) * f : -INFINITY;
+  sig[3] = (hv && t0 + 9 < rows) ? (hi[1] + hi[3]) * f : -INFINITY;
+}
+
+// The query-side operand of a pre-RoPE layer, once per segment: x_c = q_c kappa (kappa
+// the power of two bringing max |q_c| into [2^13, 2^14)), hi/lo as in build_x_fp8.
+__device__ __forceinline__ void build_x_rope(const float* qrow, int q, uint32_t (&X)[8][4], float& kap, float& inv) {
+  float mx = 0.f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  kap = pow2_fit_f16(mx, inv);
+  const float2 k2 = make_float2(kap, kap);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
+    split_f16x2(mul_f32x2(make_float2(x.x, x.y), k2), X[s][0], X[s][1]);
+    split_f16x2(mul_f32x2(make_float2(x.z, x.w), k2), X[s][2], X[s][3]);
+  }
+}
+
+// --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
 // Query columns of a kv head h: column j is query token j / gh (of n_query per
@@ -635,8 +825,9 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // several query tokens per sequence (causal limits per column); only that
 // variant carries the limit checks.  ONE: integer layers whose Key groups are one
 // tile each (G = 16, the paged blocks): every tile rebuilds the query-side
-// operand, in straight-line code.
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE>
+// operand, in straight-line code.  ROPE: pre-RoPE Keys (integer layers), rotated
+// at their positions.
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE>
 __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
   constexpr int NW = DecodeWarps<FMT>::kNW;
@@ -669,12 +860,21 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   int* prefix = reinterpret_cast<int*>(smem + off);  // [B + 1]
   off += ((size_t)(B + 1) * sizeof(int) + 15) / 16 * 16;
   int* toks = reinterpret_cast<int*>(smem + off);    // [B]: each sequence's token count (clamped)
+  off += ((size_t)B * sizeof(int) + 15) / 16 * 16;
+  // pre-RoPE Keys: per warp, the current Key group's header (K scale [128], K zero [128])
+  float* rope_hdr = ROPE ? reinterpret_cast<float*>(smem + off) + warp * 256 : nullptr;
   __shared__ int seg_count;
   __shared__ long long batch_end;
 
   if (tid == 0) {
     for (int i = 0; i < NW * kMaxStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_barrier_init();
+  }
+  unsigned long long* s_turn = nullptr;  // pre-RoPE Keys: the pairs' angle per position
+  if constexpr (ROPE) {
+    __shared__ unsigned long long turn_tab[64];
+    if (tid < 64) turn_tab[tid] = p.rope_turn[tid];
+    s_turn = turn_tab;
   }
 
   // ---- per-sequence work units and their prefix (units of all H heads) ----
@@ -1064,7 +1264,12 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
       uint32_t X[8][4];  // query-side A operand (hi/lo rows), rebuilt per Key group for INT layers
       float kfac = 0.f, cterm = 0.f;
       float qm = 0.f;    // INT: the column's max |q_c| (the Key groups' kappa bound)
-      if constexpr (F::kFp8) {
+      float kapq = 1.f, kfacq = 0.f;  // pre-RoPE Keys: the query operand's scale and score multiplier
+      if constexpr (ROPE) {
+        float invq;
+        build_x_rope(qrow, q, X, kapq, invq);
+        kfacq = p.scale_log2 * invq;
+      } else if constexpr (F::kFp8) {
         build_x_fp8(qrow, q, p.scale_log2 * __ldg(p.C.k_tscale), X, kfac);
       } else {
         qm = column_qmax(qrow, q);
@@ -1072,6 +1277,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) X[s2][0] = X[s2][1] = X[s2][2] = X[s2][3] = 0u;
       }
+      float kapk = 1.f;  // pre-RoPE Keys: the current group's Key scale
       float sig_bf[4];  // scores of a bf16 tile between its K and V stages
       // the lane's four tokens of a tile (score and W layout)
       const int tk[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
@@ -1122,7 +1328,13 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           const uint8_t* vst = stg;
           bool vpart = tg.kind == 2;
           if (tg.kind == 1) {
-            bf16_qk(stg, qrow, lane, q, hv, rows, p.scale_log2, sig_bf);
+            if constexpr (ROPE) {  // bf16 list index -> position: sinks first, then the window after Q_n
+              const int xa = 16 * tg.a + r, xb = xa + 8;
+              bf16_qk_rope(stg, qrow, lane, q, hv, rows, kapq, kfacq, s_turn, xa + (xa >= sg.n_sink ? sg.qn : 0),
+                           xb + (xb >= sg.n_sink ? sg.qn : 0), sig_bf);
+            } else {
+              bf16_qk(stg, qrow, lane, q, hv, rows, p.scale_log2, sig_bf);
+            }
             if (MQ && p.n_query > 1) {  // bf16 list index -> token: sinks first, then the residual window after Q_n
               const int lim = col_limit();
 #pragma unroll
@@ -1150,7 +1362,18 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           // tile i at `tile`; INT: `hdrp` the Key-group header, the query-side operand (q * s,
           // hi/lo) rebuilt from it when `build` (at each record, i.e. Key group, start)
           auto tile_step = [&](const int i, const uint8_t* tile, const uint8_t* hdrp, const bool build) {
-            if constexpr (F::kInt) {
+            if constexpr (ROPE) {
+              // the group's header to the warp's copy (the tiles of a group may span stages)
+              if (build) {
+                __syncwarp();
+                reinterpret_cast<uint4*>(rope_hdr)[lane] = reinterpret_cast<const uint4*>(hdrp)[lane];
+                reinterpret_cast<uint4*>(rope_hdr)[lane + 32] = reinterpret_cast<const uint4*>(hdrp)[lane + 32];
+                __syncwarp();
+                float invk;
+                kapk = rope_group_scale<FMT>(rope_hdr, rope_hdr + 128, lane, invk);
+                kfac = kfacq * invk;
+              }
+            } else if constexpr (F::kInt) {
               if (build)
                 build_x_group<FMT>(qrow, reinterpret_cast<const float*>(hdrp),
                                    reinterpret_cast<const float*>(hdrp + 512), lane, q, p.scale_log2, qm, X, kfac,
@@ -1161,7 +1384,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
             {
               uint32_t KW[F::kWords];
               load_words(tile, lane, KW);
-              qk_tile<FMT>(KW, X, d);
+              if constexpr (ROPE)
+                qk_tile_rope<FMT>(KW, X, rope_hdr, rope_hdr + 128, s_turn, L.S + 16 * i, r, q, kapk, d);
+              else
+                qk_tile<FMT>(KW, X, d);
             }
             const int tok_valid = min(16, sg.qn - i * 16);  // < 16 only for a partial FP8 tile
             float sig[4];
@@ -1497,7 +1723,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1506,16 +1732,17 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false>
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE, ROPE>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, BF, MQ, ONE><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1531,6 +1758,14 @@ cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream
     return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, false>(p, smem, stream)
                          : launch_variant<FMT, NGV, true, false, false>(p, smem, stream);
   } else {
+    if (p.L.rope) {  // pre-RoPE Keys: Value groups of 64 or 128 channels, one query token (host-checked)
+      if constexpr (NGV <= 2) {
+        return p.L.tpg == 1 ? launch_variant<FMT, NGV, true, false, true, true>(p, smem, stream)
+                            : launch_variant<FMT, NGV, true, false, false, true>(p, smem, stream);
+      } else {
+        return cudaErrorInvalidValue;
+      }
+    }
     if (p.L.tpg == 1)
       return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, true>(p, smem, stream)
                            : launch_variant<FMT, NGV, true, false, true>(p, smem, stream);
@@ -1545,7 +1780,7 @@ template <int FMT, int NGV, bool MQ>
 cudaError_t occupancy_variant(int smem, int* n) {
   cudaError_t e = ensure_smem_attr<FMT, NGV, true, MQ, false>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false, false>,
                                                        DecodeWarps<FMT>::kThreads, smem);
 }
 template <int FMT, int NGV>

@@ -39,6 +39,8 @@ struct LayerDesc {
   int rec_bytes;   // hdr_bytes + tpg * tile_bytes
   int nrec;        // contiguous: records per (seq, head)
   long long block_bytes;  // paged: H records
+  int rope;               // Keys stored before RoPE, rotated at their position by the decode
+  float rope_base;
 };
 
 struct CachePtrs {
@@ -81,6 +83,9 @@ struct DecodeParams {
   void* out;
   int out_bf16;
   float* lse;
+  // pre-RoPE Keys: per rotation pair i, frac(theta_i / 2 pi) * 2^64 (the angle of position t
+  // in turns is t * rope_turn[i] mod 2^64, fixed point)
+  unsigned long long rope_turn[64];
 };
 
 struct CombineParams {

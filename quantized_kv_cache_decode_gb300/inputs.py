@@ -58,6 +58,7 @@ class LayerFormat:
     Gv:  Value group width in channels (per-token Value quantization)
     R:   residual window: the most recent tokens kept in bf16
     S:   sink tokens kept in bf16 at the start of the sequence
+    rope_base: > 0: Keys stored before RoPE and rotated at their position by the decode
     """
 
     fmt: str
@@ -65,6 +66,7 @@ class LayerFormat:
     Gv: int
     R: int
     S: int
+    rope_base: float = 0.0
 
 
 @dataclasses.dataclass
@@ -126,6 +128,14 @@ def llama3_8b_fp8_2q() -> Workload:
                     append_tokens=2, seed=1008, n_query=2)
 
 
+def llama3_8b_int4_prerope() -> Workload:
+    """Llama-3-8B-shaped KIVI INT4 layer (B=16, T=8192, 32/8 heads, G=128, Gv=128, R=128) whose Keys are
+    stored before RoPE (base 500000, Llama 3) and rotated at their positions by the decode."""
+    fmt = LayerFormat("int4", G=128, Gv=128, R=128, S=0, rope_base=500000.0)
+    return Workload("llama3_8b_kivi_int4_prerope", 1, 16, 32, 8, 128, 8192, [fmt], 4, 0, 10.0, "per_head",
+                    seed=1009)
+
+
 def llama3_70b_int4() -> Workload:
     """Llama-3-70B-shaped decode over 80 layers, KIVI INT4 (G=128, Gv=128, R=128)."""
     fmt = LayerFormat("int4", G=128, Gv=128, R=128, S=0)
@@ -155,6 +165,7 @@ WORKLOADS = {
     "llama3_8b_fp8_e5m2": llama3_8b_fp8_e5m2,
     "llama3_8b_bf16_skip_layer": llama3_8b_bf16_skip,
     "llama3_8b_fp8_e4m3_2q": llama3_8b_fp8_2q,
+    "llama3_8b_kivi_int4_prerope": llama3_8b_int4_prerope,
     "llama3_70b_kivi_int4_80l": llama3_70b_int4,
     "llama2_7b_kivi2_int2_32k": llama2_7b_int2,
     "paged_mixed_int8_int4_64l": paged_mixed,

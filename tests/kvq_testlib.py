@@ -78,7 +78,7 @@ class GpuLayer:
 
     def __init__(self, fmt: str, H: int, lens: Sequence[int], G: int, Gv: int, R: int, S: int, *,
                  paged: bool = False, block_tokens: int = 16, spare_blocks: int = 3, seed: int = 0,
-                 extra_capacity: int = 0, device="cuda"):
+                 extra_capacity: int = 0, device="cuda", rope_base: float = 0.0):
         import torch
         from quantized_kv_cache_decode_gb300 import kvq
         self.torch, self.kvq = torch, kvq
@@ -90,7 +90,7 @@ class GpuLayer:
         self.Gv = 128 if (self.fp8 or self.bf16) else Gv
         self.R = 0 if (self.fp8 or self.bf16) else R
         self.S = S
-        self.spec = O.Spec(fmt, d=128, G=self.G, Gv=self.Gv, R=self.R, S=S)
+        self.spec = O.Spec(fmt, d=128, G=self.G, Gv=self.Gv, R=self.R, S=S, rope_base=rope_base)
         self.device = device
         self.paged = paged
         maxq = max([O.token_split(T + extra_capacity, self.spec)[1] for T in self.lens] + [0])
@@ -105,10 +105,10 @@ class GpuLayer:
             self.mbps = max(blocks_per_seq + [1])
             nblocks = sum(blocks_per_seq) + spare_blocks
             self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, paged=True, block_tokens=self.P,
-                                       num_blocks=nblocks, max_blocks_per_seq=self.mbps)
+                                       num_blocks=nblocks, max_blocks_per_seq=self.mbps, rope_base=rope_base)
         else:
             cap = max(unit, math.ceil(maxq / unit) * unit)
-            self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, capacity_tokens=cap)
+            self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, capacity_tokens=cap, rope_base=rope_base)
         self.layer = kvq.CacheLayer(self.cfg, self.B, device=device)
         if paged:
             rng = np.random.default_rng(seed + 77)

@@ -90,6 +90,12 @@ def test_cache_layout_sizes(kvq):
           max_blocks_per_seq=2), -2),
     # Key groups longer than the append kernel stages in shared memory (256 tokens)
     (dict(fmt="int4", num_kv_heads=2, G=272, Gv=128, R=0, S=0, capacity_tokens=272), -2),
+    # pre-RoPE Keys: integer formats with Value groups of 64 or 128 channels; a base above 1
+    (dict(fmt="fp8_e4m3", num_kv_heads=2, G=1, Gv=128, R=0, S=0, capacity_tokens=64, rope_base=1e4), -2),
+    (dict(fmt="bf16", num_kv_heads=2, G=0, Gv=0, R=0, S=1, capacity_tokens=64, rope_base=1e4), -2),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=32, R=0, S=0, capacity_tokens=64, rope_base=1e4), -2),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, rope_base=0.5), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, rope_base=float("nan")), -1),
 ])
 def test_config_validation(kvq, kw, status):
     kw = dict(kw)
@@ -182,3 +188,12 @@ def test_append_rejects_unaligned_inputs_before_any_launch(kvq):
         with pytest.raises(kvq.KvqError) as e:
             kvq.quantize_append(cfg, cache, kn, vn, 1, 16, 1, stream=0)
         assert e.value.status == -1
+
+
+def test_pre_rope_keys_reject_several_query_tokens(kvq):
+    # the multi-query decode does not rotate Keys: refused before anything is enqueued
+    cfg = kvq.make_config("int4", 2, 32, 128, 32, 0, capacity_tokens=64, rope_base=10000.0)
+    cache = kvq.LayerCache()
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.decode_attention_multi(cfg, cache, 0, 2, 8, 0, 1, 0.1, 4096, False, 0, 0, 0, 0, stream=0)
+    assert e.value.status == -2

@@ -40,8 +40,9 @@ def make_inputs(seed, H, g, lens, outliers=4, scale=10.0):
     return kv, q
 
 
-def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=None):
-    gl = TL.GpuLayer(fmt, H, lens, G, Gv, R, S, paged=paged, block_tokens=block_tokens, seed=seed)
+def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=None, rope_base=0.0):
+    gl = TL.GpuLayer(fmt, H, lens, G, Gv, R, S, paged=paged, block_tokens=block_tokens, seed=seed,
+                     rope_base=rope_base)
     kv, q = make_inputs(seed, H, g, lens)
     ks = vs = None
     if gl.fp8:
@@ -342,3 +343,39 @@ def test_fused_combine_equals_two_launches_and_repeats(fmt, lens):
     kvq.decode_combine(gl.cfg, Hq, B, out2, False, lse2, ws, wsb)
     torch.cuda.synchronize()
     assert torch.equal(out2, o1) and torch.equal(lse2, l1)
+
+
+ROPE_CASES = [
+    # fmt, H, g, lens, G, Gv, R, S, paged, block, rope_base: Keys appended before RoPE, rotated at
+    # their positions by the decode ("KV Cache Quantization Analysis", section 3 RoPE bullet)
+    ("int4", 2, 4, [700, 33, 129, 0], 32, 128, 32, 1, False, 16, 10000.0),
+    ("int8", 2, 6, [300, 17, 80, 81, 2], 16, 128, 64, 1, True, 16, 500000.0),
+    ("int2", 3, 1, [1000, 160, 5], 32, 64, 128, 0, False, 16, 10000.0),
+    ("int4", 2, 8, [500, 96], 16, 64, 16, 2, True, 16, 500000.0),
+    # long positions (angles up to 20000 turns of the fastest pair), several CTAs per pair
+    ("int4", 1, 8, [20000], 128, 128, 128, 2, False, 16, 500000.0),
+]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES, ids=[f"{c[0]}-H{c[1]}g{c[2]}-G{c[4]}Gv{c[5]}R{c[6]}S{c[7]}"
+                                                  f"{'-paged' if c[8] else ''}-base{int(c[10])}" for c in ROPE_CASES])
+def test_pre_rope_parity(case):
+    fmt, H, g, lens, G, Gv, R, S, paged, blk, base = case
+    seed = zlib.crc32(repr(case).encode()) % 10000
+    gl, caches, q = build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=blk, rope_base=base)
+    # the stored cache holds the Keys as appended (before the rotation), bit-exact
+    for b, T in enumerate(lens):
+        for h in range(H):
+            TL.compare_logical(gl.logical(b, h, T), caches[b][h])
+    ko, vo = gl.dequantize(max(lens) + 1)
+    for b, T in enumerate(lens):
+        for h in range(H):
+            kr, vr = O.dequantized_f32(caches[b][h])
+            assert np.array_equal(ko[b, h, :T].view(np.uint32), kr.view(np.uint32))
+    # attention over the Keys rotated at their positions
+    out_ref, lse_ref = O.decode_attention(O.bf16_to_f32(q), caches)
+    out, lse = gl.decode(q)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+    out16, lse16 = gl.decode(q, out_bf16=True)
+    assert torch.equal(out16, out.to(torch.bfloat16)) and torch.equal(lse16, lse)
+    assert gl.status_value() == 0
