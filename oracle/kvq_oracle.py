@@ -63,6 +63,14 @@ Readings where the pages leave a step open:
   rotates each dequantized Key at its own position t, rotate-half pairing
   ``(c, c + d/2)``, angle ``t * rope_base^(-2i/d)`` for pair i, in fp64; the
   query arrives already rotated at its own position.
+* dense-and-sparse outliers (same page, section 4, KVQuant item (iv): outliers
+  separated per vector; section 2: a few large values widen the grid and cost
+  the other values their resolution): in a layer with ``k_outliers`` /
+  ``v_outliers`` = n > 0, every quantized Key row and Value row keeps its n
+  entries of largest magnitude (ties: the lower channel) exactly, as bf16, in a
+  sparse list ordered by channel; the dense remainder, those entries set to 0,
+  is quantized as usual (Keys per channel over the group, Values per token);
+  the dequantized value is the dense one plus the sparse one.
 """
 from __future__ import annotations
 
@@ -240,6 +248,8 @@ class Spec:
     R: int = 0        # residual window (bf16)
     S: int = 0        # sink tokens (bf16)
     rope_base: float = 0.0  # > 0: Keys stored before RoPE, rotated at their position by attention
+    k_outliers: int = 0     # per quantized Key row: entries kept apart (sparse, bf16)
+    v_outliers: int = 0     # per quantized Value row
 
     @property
     def bits(self) -> int:
@@ -290,26 +300,51 @@ class HeadCache:
     v_z: Optional[np.ndarray] = None
     k_scale: Optional[np.float32] = None
     v_scale: Optional[np.float32] = None
+    # dense-and-sparse: per quantized row, the outliers' channels (ascending) and bf16 values
+    k_sp_idx: Optional[np.ndarray] = None   # int64 [Q_n, k_outliers]
+    k_sp_val: Optional[np.ndarray] = None   # float32 [Q_n, k_outliers]
+    v_sp_idx: Optional[np.ndarray] = None
+    v_sp_val: Optional[np.ndarray] = None
 
     @property
     def T(self) -> int:
         return len(self.sink_k) + len(self.k_codes) + len(self.resid_k)
 
 
+def split_outliers(x: np.ndarray, n: int):
+    """Dense-and-sparse split of rows x [m, d]: the n entries of largest magnitude of each row
+    (ties: the lower channel) leave it.  Returns (dense: x with them set to 0, idx [m, n] ascending,
+    val [m, n]: their values)."""
+    x = np.asarray(x, dtype=F32)
+    m, d = x.shape
+    if n == 0:
+        return x.copy(), np.zeros((m, 0), np.int64), np.zeros((m, 0), F32)
+    order = np.lexsort((np.arange(d)[None, :].repeat(m, 0), -np.abs(x)), axis=1)  # by |x| desc, then channel
+    idx = np.sort(order[:, :n], axis=1)
+    val = np.take_along_axis(x, idx, axis=1)
+    dense = x.copy()
+    np.put_along_axis(dense, idx, F32(0.0), axis=1)
+    return dense, idx, val
+
+
 def quantize_key_groups(k: np.ndarray, spec: Spec):
-    """Keys per channel: every channel of every G-token group is one quantization group."""
+    """Keys per channel: every channel of every G-token group is one quantization group (of the
+    dense part when the layer keeps outliers apart).  Returns codes, s, z, sparse idx, sparse val."""
     qn, d = k.shape
+    k, sp_idx, sp_val = split_outliers(k, spec.k_outliers)
     g = k.reshape(qn // spec.G, spec.G, d).transpose(0, 2, 1)    # [groups, d, G]
     codes, s, z = affine_quantize(g, spec.bits)
-    return codes.transpose(0, 2, 1).reshape(qn, d), s, z         # s, z: [groups, d]
+    return codes.transpose(0, 2, 1).reshape(qn, d), s, z, sp_idx, sp_val   # s, z: [groups, d]
 
 
 def quantize_value_tokens(v: np.ndarray, spec: Spec):
-    """Values per token: every Gv-channel slice of every token is one quantization group."""
+    """Values per token: every Gv-channel slice of every token is one quantization group (of the
+    dense part when the layer keeps outliers apart).  Returns codes, s, z, sparse idx, sparse val."""
     qn, d = v.shape
+    v, sp_idx, sp_val = split_outliers(v, spec.v_outliers)
     g = v.reshape(qn, d // spec.Gv, spec.Gv)
     codes, s, z = affine_quantize(g, spec.bits)
-    return codes.reshape(qn, d), s, z                            # s, z: [Q_n, d/Gv]
+    return codes.reshape(qn, d), s, z, sp_idx, sp_val            # s, z: [Q_n, d/Gv]
 
 
 def build_head_cache(k: np.ndarray, v: np.ndarray, spec: Spec,
@@ -330,8 +365,8 @@ def build_head_cache(k: np.ndarray, v: np.ndarray, spec: Spec,
         hc.k_codes = np.zeros((0, spec.d), np.uint8)
         hc.v_codes = np.zeros((0, spec.d), np.uint8)
     else:
-        hc.k_codes, hc.k_s, hc.k_z = quantize_key_groups(k[q0:q1], spec)
-        hc.v_codes, hc.v_s, hc.v_z = quantize_value_tokens(v[q0:q1], spec)
+        hc.k_codes, hc.k_s, hc.k_z, hc.k_sp_idx, hc.k_sp_val = quantize_key_groups(k[q0:q1], spec)
+        hc.v_codes, hc.v_s, hc.v_z, hc.v_sp_idx, hc.v_sp_val = quantize_value_tokens(v[q0:q1], spec)
     return hc
 
 
@@ -347,6 +382,8 @@ def empty_head_cache(spec: Spec, k_scale=None, v_scale=None) -> HeadCache:
         hc.k_z = np.zeros((0, d), F32)
         hc.v_s = np.zeros((0, d // spec.Gv), F32)
         hc.v_z = np.zeros((0, d // spec.Gv), F32)
+        hc.k_sp_idx, hc.k_sp_val = np.zeros((0, spec.k_outliers), np.int64), np.zeros((0, spec.k_outliers), F32)
+        hc.v_sp_idx, hc.v_sp_val = np.zeros((0, spec.v_outliers), np.int64), np.zeros((0, spec.v_outliers), F32)
     return hc
 
 
@@ -371,8 +408,10 @@ def append_token(hc: HeadCache, k_tok: np.ndarray, v_tok: np.ndarray) -> None:
     hc.resid_k = np.concatenate([hc.resid_k, k_tok])
     hc.resid_v = np.concatenate([hc.resid_v, v_tok])
     if not spec.is_bf16 and len(hc.resid_k) == spec.R + spec.G:
-        kc, ks, kz = quantize_key_groups(hc.resid_k[:spec.G], spec)
-        vc, vs, vz = quantize_value_tokens(hc.resid_v[:spec.G], spec)
+        kc, ks, kz, ki, kv = quantize_key_groups(hc.resid_k[:spec.G], spec)
+        vc, vs, vz, vi, vv = quantize_value_tokens(hc.resid_v[:spec.G], spec)
+        hc.k_sp_idx, hc.k_sp_val = np.concatenate([hc.k_sp_idx, ki]), np.concatenate([hc.k_sp_val, kv])
+        hc.v_sp_idx, hc.v_sp_val = np.concatenate([hc.v_sp_idx, vi]), np.concatenate([hc.v_sp_val, vv])
         hc.k_codes = np.concatenate([hc.k_codes, kc])
         hc.k_s = np.concatenate([hc.k_s, ks])
         hc.k_z = np.concatenate([hc.k_z, kz])
@@ -397,6 +436,12 @@ def dequantized_f64(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
         vs = np.repeat(hc.v_s, spec.Gv, axis=1)
         vz = np.repeat(hc.v_z, spec.Gv, axis=1)
         vq = affine_dequantize_f64(hc.v_codes, vs, vz)
+        # dense-and-sparse: the kept outliers add to the dense values at their channels
+        rows = np.arange(kq.shape[0])[:, None]
+        if spec.k_outliers:
+            kq[rows, hc.k_sp_idx] += hc.k_sp_val.astype(np.float64)
+        if spec.v_outliers:
+            vq[rows, hc.v_sp_idx] += hc.v_sp_val.astype(np.float64)
     k = np.concatenate([hc.sink_k.astype(np.float64), kq, hc.resid_k.astype(np.float64)])
     v = np.concatenate([hc.sink_v.astype(np.float64), vq, hc.resid_v.astype(np.float64)])
     return k, v
@@ -416,6 +461,12 @@ def dequantized_f32(hc: HeadCache) -> Tuple[np.ndarray, np.ndarray]:
         vs = np.repeat(hc.v_s, spec.Gv, axis=1)
         vz = np.repeat(hc.v_z, spec.Gv, axis=1)
         vq = affine_dequantize_f32(hc.v_codes, vs, vz)
+        # dense-and-sparse: one more fp32 add at each kept outlier's channel
+        rows = np.arange(kq.shape[0])[:, None]
+        if spec.k_outliers:
+            kq[rows, hc.k_sp_idx] = (kq[rows, hc.k_sp_idx] + hc.k_sp_val).astype(F32)
+        if spec.v_outliers:
+            vq[rows, hc.v_sp_idx] = (vq[rows, hc.v_sp_idx] + hc.v_sp_val).astype(F32)
     k = np.concatenate([hc.sink_k, kq, hc.resid_k]).astype(F32)
     v = np.concatenate([hc.sink_v, vq, hc.resid_v]).astype(F32)
     return k, v

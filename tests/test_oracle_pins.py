@@ -140,7 +140,7 @@ def test_key_per_channel_value_per_token_axes():
     rng = np.random.default_rng(5)
     k = rng.standard_normal((24, 16)).astype(F32)
     k[:, 3] *= 50
-    kc, ks, kz = O.quantize_key_groups(k, spec)
+    kc, ks, kz, _, _ = O.quantize_key_groups(k, spec)
     assert ks.shape == (3, 16)
     for gi in range(3):
         blk = k[gi * 8:(gi + 1) * 8]
@@ -149,7 +149,7 @@ def test_key_per_channel_value_per_token_axes():
             assert col[blk[:, c].argmin()] == 0 and col[blk[:, c].argmax()] == 15
             assert ks[gi, c] == F32(F32(blk[:, c].max() - blk[:, c].min()) / F32(15))
     v = rng.standard_normal((24, 16)).astype(F32)
-    vc, vs, vz = O.quantize_value_tokens(v, spec)
+    vc, vs, vz, _, _ = O.quantize_value_tokens(v, spec)
     assert vs.shape == (24, 4)
     for t in range(24):
         for j in range(4):
@@ -305,7 +305,8 @@ def test_token_split_workloads():
 
 
 def _same_cache(a, b):
-    for f in ("sink_k", "sink_v", "k_codes", "v_codes", "resid_k", "resid_v", "k_s", "k_z", "v_s", "v_z"):
+    for f in ("sink_k", "sink_v", "k_codes", "v_codes", "resid_k", "resid_v", "k_s", "k_z", "v_s", "v_z",
+              "k_sp_idx", "k_sp_val", "v_sp_idx", "v_sp_val"):
         x, y = getattr(a, f), getattr(b, f)
         if x is None:
             assert y is None
@@ -320,6 +321,8 @@ def _same_cache(a, b):
     O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=1),
     O.Spec("fp8_e5m2", d=16, G=1, Gv=16, R=0, S=0),
     O.Spec("bf16", d=16, G=16, Gv=16, R=0, S=1),
+    O.Spec("int4", d=16, G=8, Gv=8, R=4, S=1, k_outliers=2, v_outliers=1),
+    O.Spec("int2", d=16, G=4, Gv=16, R=8, S=0, k_outliers=1, v_outliers=3),
 ])
 def test_bulk_build_equals_appends(spec):
     rng = np.random.default_rng(7)
@@ -375,6 +378,10 @@ def _dequant_brute(hc):
             ks.append([float(hc.k_s[g, c]) * (int(hc.k_codes[t, c]) - float(hc.k_z[g, c])) for c in range(sp.d)])
             vs.append([float(hc.v_s[t, c // sp.Gv]) * (int(hc.v_codes[t, c]) - float(hc.v_z[t, c // sp.Gv]))
                        for c in range(sp.d)])
+            for j in range(sp.k_outliers):  # the kept outliers add at their channels
+                ks[-1][int(hc.k_sp_idx[t, j])] += float(hc.k_sp_val[t, j])
+            for j in range(sp.v_outliers):
+                vs[-1][int(hc.v_sp_idx[t, j])] += float(hc.v_sp_val[t, j])
     for t in range(len(hc.resid_k)):
         ks.append(list(map(float, hc.resid_k[t])))
         vs.append(list(map(float, hc.resid_v[t])))
@@ -388,6 +395,8 @@ def _dequant_brute(hc):
     O.Spec("fp8_e4m3", d=16, G=1, Gv=16, R=0, S=1),
     O.Spec("fp8_e5m2", d=16, G=1, Gv=16, R=0, S=0),
     O.Spec("bf16", d=16, G=16, Gv=16, R=0, S=1),
+    O.Spec("int4", d=16, G=8, Gv=8, R=4, S=1, k_outliers=2, v_outliers=2),
+    O.Spec("int8", d=16, G=16, Gv=4, R=0, S=0, k_outliers=1, v_outliers=4),
 ])
 def test_attention_brute_force(spec):
     rng = np.random.default_rng(11)
@@ -645,3 +654,110 @@ def test_attention_over_pre_rope_keys_brute_force(spec):
     k = rng.standard_normal((T, 16)).astype(F32)
     v = rng.standard_normal((T, 16)).astype(F32)
     _same_cache(O.build_head_cache(k, v, spec), O.build_head_cache(k, v, plain))
+
+
+
+# --------------------------------------------------------------------------- #
+# dense-and-sparse outliers ("KV Cache Quantization Analysis", section 4, KVQuant (iv); section 2 outliers)
+# --------------------------------------------------------------------------- #
+
+
+def _top_n_brute(row, n):
+    """Channels of the n largest |x| of a row, ties to the lower channel, plain Python; ascending."""
+    chosen = []
+    for _ in range(n):
+        best = None
+        for c in range(len(row)):
+            if c in chosen:
+                continue
+            if best is None or abs(float(row[c])) > abs(float(row[best])):
+                best = c
+        chosen.append(best)
+    return sorted(chosen)
+
+
+def test_outlier_selection_brute_force():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((40, 16)).astype(F32)
+    x[3, [2, 9, 14]] = 5.0            # ties at the top: the lower channels win
+    x[4, :] = 0.0                     # an all-zero row: channels 0 .. n-1
+    x[5, [1, 7]] = [-3.0, 3.0]        # equal magnitudes, opposite signs
+    for n in (0, 1, 2, 3, 5):
+        dense, idx, val = O.split_outliers(x, n)
+        for i in range(len(x)):
+            want = _top_n_brute(x[i], n)
+            assert list(idx[i]) == want, (n, i)
+            assert np.array_equal(val[i], x[i, want])
+            d = x[i].copy()
+            d[want] = 0.0
+            assert np.array_equal(dense[i], d)
+
+
+@pytest.mark.parametrize("bits,nk,nv", [(2, 1, 2), (4, 2, 1), (8, 3, 3)])
+def test_outliers_reconstruct_exactly_on_grid(bits, nk, nv):
+    # dense rows on a grid of their own per group (power-of-two s, integer z, codes 0 and 2^b - 1
+    # present), planted outliers far above every dense value at positions that are neither a group's
+    # minimum nor its maximum and hold the code z (dense value 0): the split recovers the planted
+    # outliers and the export returns the inputs exactly
+    d, G, Gv, n_groups = 32, 8, 16, 2
+    qn = n_groups * G
+    L = 2 ** bits - 1
+    rng = np.random.default_rng(40 + bits)
+    kq = rng.integers(0, L + 1, size=(qn, d))
+    vq = rng.integers(0, L + 1, size=(qn, d))
+    k_s, k_z = np.empty((n_groups, d)), rng.integers(1, L, size=(n_groups, d))
+    v_s, v_z = np.empty((qn, d // Gv)), rng.integers(1, L, size=(qn, d // Gv))
+    reserved_k = np.zeros((qn, d), bool)   # group minimum / maximum positions
+    reserved_v = np.zeros((qn, d), bool)
+    for j in range(n_groups):
+        for c in range(d):
+            k_s[j, c] = 2.0 ** -(1 + (c + j) % 3)
+            lo, hi = j * G + (c % G), j * G + ((c + 1) % G)
+            kq[lo, c], kq[hi, c] = 0, L
+            reserved_k[lo, c] = reserved_k[hi, c] = True
+    for t in range(qn):
+        for j in range(d // Gv):
+            v_s[t, j] = 2.0 ** -(1 + (t + j) % 3)
+            lo, hi = j * Gv + (t % Gv), j * Gv + ((t + 1) % Gv)
+            vq[t, lo], vq[t, hi] = 0, L
+            reserved_v[t, lo] = reserved_v[t, hi] = True
+    gk = np.arange(qn) // G
+    kidx = np.sort(np.stack([rng.choice(np.flatnonzero(~reserved_k[t]), nk, replace=False) for t in range(qn)]), 1)
+    vidx = np.sort(np.stack([rng.choice(np.flatnonzero(~reserved_v[t]), nv, replace=False) for t in range(qn)]), 1)
+    rows = np.arange(qn)[:, None]
+    kq[rows, kidx] = k_z[gk[:, None], kidx]                     # dense value 0 there
+    vq[rows, vidx] = np.repeat(v_z, Gv, axis=1)[rows, vidx]
+    kd = (k_s[gk] * (kq - k_z[gk])).astype(F32)
+    vd = (np.repeat(v_s, Gv, axis=1) * (vq - np.repeat(v_z, Gv, axis=1))).astype(F32)
+    assert np.all(kd[rows, kidx] == 0) and np.all(vd[rows, vidx] == 0) and np.abs(kd).max() < 200
+    kval = (rng.integers(200, 400, size=(qn, nk)) * np.where(rng.random((qn, nk)) < 0.5, -1, 1)).astype(F32)
+    vval = (rng.integers(200, 400, size=(qn, nv)) * np.where(rng.random((qn, nv)) < 0.5, -1, 1)).astype(F32)
+    k, v = kd.copy(), vd.copy()
+    k[rows, kidx], v[rows, vidx] = kval, vval
+    spec = O.Spec(f"int{bits}", d=d, G=G, Gv=Gv, R=0, S=0, k_outliers=nk, v_outliers=nv)
+    hc = O.build_head_cache(k, v, spec)
+    assert np.array_equal(hc.k_sp_idx, kidx) and np.array_equal(hc.k_sp_val, kval)
+    assert np.array_equal(hc.v_sp_idx, vidx) and np.array_equal(hc.v_sp_val, vval)
+    assert np.array_equal(hc.k_s, k_s.astype(F32)) and np.array_equal(hc.k_z, k_z.astype(F32))
+    assert np.array_equal(hc.v_s, v_s.astype(F32)) and np.array_equal(hc.v_z, v_z.astype(F32))
+    ko, vo = O.dequantized_f32(hc)
+    assert np.array_equal(ko.view(np.uint32), k.view(np.uint32)) and np.array_equal(vo.view(np.uint32), v.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_outlier_split_error_bound(bits):
+    # every entry, kept outlier or not, is within s/2 (of its dense group) of its input
+    rng = np.random.default_rng(60 + bits)
+    d, G, Gv, qn = 16, 8, 8, 32
+    x = (rng.standard_normal((qn, d)) * np.where(rng.random((qn, d)) < 0.05, 30, 1)).astype(F32)
+    v = (rng.standard_normal((qn, d)) * np.where(rng.random((qn, d)) < 0.05, 30, 1)).astype(F32)
+    spec = O.Spec(f"int{bits}", d=d, G=G, Gv=Gv, k_outliers=2, v_outliers=2)
+    hc = O.build_head_cache(x, v, spec)
+    kh, vh = O.dequantized_f64(hc)
+    ks = np.repeat(hc.k_s, G, axis=0).astype(np.float64)
+    vs = np.repeat(hc.v_s, Gv, axis=1).astype(np.float64)
+    assert np.all(np.abs(kh - x) <= ks / 2 * (1 + 1e-5) + 1e-30)
+    assert np.all(np.abs(vh - v) <= vs / 2 * (1 + 1e-5) + 1e-30)
+    # the split narrows the grids: the dense scales never exceed those of the plain quantizer
+    plain = O.build_head_cache(x, v, O.Spec(f"int{bits}", d=d, G=G, Gv=Gv))
+    assert np.all(hc.k_s <= plain.k_s) and np.all(hc.v_s <= plain.v_s)
