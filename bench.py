@@ -76,6 +76,7 @@ def attention_bytes(fmt, T, H, d=128):
     b = 2 * qn * d * bits // 8
     if not is_fp8(fmt) and qn:
         b += (qn // fmt.G) * d * 8 + qn * (d // fmt.Gv) * 8
+        b += qn * 4 * (fmt.k_outliers + fmt.v_outliers)  # dense-and-sparse entries
     b += (n_sink + r) * d * 2 * 2
     return b * H
 
@@ -92,6 +93,7 @@ def append_bytes(fmt, T_before, n, H, d=128):
     b += 2 * n * d * 2  # ring write (upper bound: every new token)
     b += spilled * 2 * d * 2  # spilled tokens read back (bf16 K, V)
     b += 2 * spilled * d * bits // 8 + (spilled // fmt.G) * d * 8 + spilled * (d // fmt.Gv) * 8
+    b += spilled * 4 * (getattr(fmt, "k_outliers", 0) + getattr(fmt, "v_outliers", 0))
     return H * b
 
 
@@ -211,12 +213,13 @@ class Layer:
             nblk = [math.ceil(q / P) for q in qmax]
             mbps = max(nblk + [1])
             self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, paged=True, block_tokens=P,
-                                       num_blocks=max(1, sum(nblk)), max_blocks_per_seq=mbps, rope_base=fmt.rope_base)
+                                       num_blocks=max(1, sum(nblk)), max_blocks_per_seq=mbps, rope_base=fmt.rope_base,
+                                       k_outliers=fmt.k_outliers, v_outliers=fmt.v_outliers)
         else:
             unit = 16 if fp8 else max(16, G)
             cap = max(unit, math.ceil(max(qmax) / unit) * unit)
             self.cfg = kvq.make_config(fmt.fmt, H, G, fmt.Gv, fmt.R, fmt.S, capacity_tokens=cap,
-                                       rope_base=fmt.rope_base)
+                                       rope_base=fmt.rope_base, k_outliers=fmt.k_outliers, v_outliers=fmt.v_outliers)
         self.cache = kvq.CacheLayer(self.cfg, B, device=dev, zero=False)
         if w.paged:
             perm = torch.from_numpy(I.block_permutation(w, max(1, sum(nblk)), l)).to(dev)
@@ -468,7 +471,8 @@ def oracle_pairs(w, layer, pairs):
     lens_after = lens_after_step(w)
     n_app = max(1, w.append_tokens)
     spec = O.Spec(fmt.fmt, d=128, G=1 if is_fp8(fmt) else fmt.G, Gv=fmt.Gv,
-                  R=0 if is_fp8(fmt) else fmt.R, S=fmt.S, rope_base=fmt.rope_base)
+                  R=0 if is_fp8(fmt) else fmt.R, S=fmt.S, rope_base=fmt.rope_base, k_outliers=fmt.k_outliers,
+                  v_outliers=fmt.v_outliers)
     q = O.bf16_to_f32(I.q_bf16(w, layer))
     items = []
     for b, h in pairs:

@@ -103,6 +103,11 @@ typedef struct {
                                  (i, i + 64) turned by t * rope_base^(-2i/128) (rotate-half pairing;
                                  the query is passed already rotated).  Integer formats with Gv of 64 or
                                  128, one query token (KVQ_ERR_UNSUPPORTED otherwise). */
+  int32_t k_outliers;         /* 0..8 dense-and-sparse Keys: per quantized Key row, the k_outliers entries
+                                 of largest magnitude (ties: the lower channel) are kept exactly (bf16)
+                                 in a sparse list and the rest, those entries set to 0, is quantized */
+  int32_t v_outliers;         /* 0..8 the same for the Value rows.  Integer formats with Gv of 64 or
+                                 128, no pre-RoPE Keys, one query token (KVQ_ERR_UNSUPPORTED otherwise) */
 } kvq_layer_config;
 
 /*
@@ -115,7 +120,9 @@ typedef struct {
  *   K codes  [16*rb]      in "fragment order" (below)
  *   V codes  [16*rb]      in "fragment order" (below)
  *   V scale  [16][ngv] f32, V zero [16][ngv] f32   (INT only: per token, per Gv channels)
- * tile_bytes = 32*rb (+ 128*ngv for INT).
+ *   K sparse [16][k_outliers] u32, V sparse [16][v_outliers] u32   (dense-and-sparse layers:
+ *            each token's kept entries in ascending channel order, entry = bf16 bits << 16 | channel)
+ * tile_bytes = 32*rb (+ 128*ngv + 64*(k_outliers + v_outliers) for INT).
  * A record is a header followed by tpg consecutive tiles:
  *   INT: header = K scale [d] f32, K zero [d] f32 (the per-channel Key group of
  *        G = 16*tpg tokens, 1024 bytes); tpg = G/16

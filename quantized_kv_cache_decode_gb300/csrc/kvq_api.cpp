@@ -39,6 +39,13 @@ kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
   if (L->S < 0) return KVQ_ERR_INVALID_ARG;
   L->rope_base = cfg->rope_base;
   L->rope = cfg->rope_base != 0.f;
+  L->k_out = cfg->k_outliers;
+  L->v_out = cfg->v_outliers;
+  if (L->k_out < 0 || L->k_out > 8 || L->v_out < 0 || L->v_out > 8) return KVQ_ERR_INVALID_ARG;
+  if (L->k_out || L->v_out) {
+    if (f == KVQ_FMT_BF16 || f == KVQ_FMT_FP8_E4M3 || f == KVQ_FMT_FP8_E5M2 || L->rope) return KVQ_ERR_UNSUPPORTED;
+    if (cfg->v_group_dims != 64 && cfg->v_group_dims != 128) return KVQ_ERR_UNSUPPORTED;
+  }
   if (L->rope) {
     if (!(cfg->rope_base > 1.f) || !(cfg->rope_base < 3.0e38f)) return KVQ_ERR_INVALID_ARG;
     if (f == KVQ_FMT_BF16 || f == KVQ_FMT_FP8_E4M3 || f == KVQ_FMT_FP8_E5M2) return KVQ_ERR_UNSUPPORTED;
@@ -77,6 +84,8 @@ kvq_status make_desc(const kvq_layer_config* cfg, LayerDesc* L) {
   L->ngv = L->d / L->Gv;
   L->paged = cfg->paged ? 1 : 0;
   L->tile_bytes = 32 * L->rb + (L->fp8 ? 0 : 128 * L->ngv);
+  L->sp_off = L->tile_bytes;  // dense-and-sparse entries after the Value scales and zero-points
+  L->tile_bytes += 64 * (L->k_out + L->v_out);
   L->hdr_bytes = L->fp8 ? 0 : 2 * L->d * 4;
   if (L->paged) {
     L->P = cfg->block_tokens;
@@ -242,8 +251,9 @@ struct DecodeGeom {
 kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, int multi = 0) {
   const int wsc = merge_bytes_of(L, g);
   const int nw = decode_warps(kernel_format(L.fmt));
-  // pre-RoPE Keys: each warp keeps a copy of its current Key group's header (1 KB)
-  const int fixed = fixed_smem(batch, wsc, nw) + (L.rope ? nw * 1024 : 0);
+  // pre-RoPE Keys: each warp keeps a copy of its current Key group's header (1 KB);
+  // dense-and-sparse Values: each warp accumulates the sparse part of its outputs (8 x 128 floats)
+  const int fixed = fixed_smem(batch, wsc, nw) + (L.rope ? nw * 1024 : 0) + (L.v_out ? nw * 4096 : 0);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -402,7 +412,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
   if (n_query < 1 || num_q_heads / L.H * n_query > kMaxGqa) return KVQ_ERR_INVALID_ARG;
-  if (L.rope && n_query > 1) return KVQ_ERR_UNSUPPORTED;
+  if ((L.rope || L.k_out || L.v_out) && n_query > 1) return KVQ_ERR_UNSUPPORTED;
   if ((st = check_cache(L, cache)) != KVQ_OK) return st;
   if (batch == 0) return KVQ_OK;
   if (!q || !seq_lens || !workspace || !aligned16(workspace) || !(softmax_scale == softmax_scale))

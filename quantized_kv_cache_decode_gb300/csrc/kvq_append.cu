@@ -206,6 +206,48 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
         reinterpret_cast<uint4*>((which ? Vs : Ks) + tt * 128)[ch] = reinterpret_cast<const uint4*>(src)[ch];
       }
       __syncthreads();
+      if (L.k_out | L.v_out) {
+        // dense-and-sparse: in each Key and Value row, the n entries of largest magnitude (ties:
+        // the lower channel) go to the tile's sparse list, in channel order, and are set to 0 in
+        // the staged row, which the statistics and codes below then see (one warp per row;
+        // lane l holds channels 4l .. 4l + 3; bf16 magnitude bits order like the magnitudes)
+        for (int row = warp; row < 2 * G; row += kSpillThreads / 32) {
+          const int isv = row >= G, tt = row - isv * G, n = isv ? L.v_out : L.k_out;
+          if (n == 0) continue;
+          uint2* xr = reinterpret_cast<uint2*>((isv ? Vs : Ks) + tt * 128) + lane;
+          const uint2 raw = *xr;
+          uint32_t v4[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+          uint32_t chosen = 0;
+          for (int j = 0; j < n; ++j) {
+            uint32_t best = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (!((chosen >> e) & 1u)) best = max(best, ((v4[e] & 0x7FFFu) << 8) | (255u - (uint32_t)(4 * lane + e)));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(kFull32, best, o));
+            const int c = 255 - (int)(best & 0xFFu);
+            if ((c >> 2) == lane) chosen |= 1u << (c & 3);
+          }
+          // rank of an entry in channel order: the entries of the lower lanes, then the lower bits
+          const int cnt = __popc(chosen);
+          int incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull32, incl, o);
+            if (lane >= o) incl += v;
+          }
+          uint32_t* sp = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)(tt >> 4) * L.tile_bytes +
+                                                     L.sp_off + (isv ? 64 * L.k_out : 0)) + (tt & 15) * n;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if ((chosen >> e) & 1u) {
+              sp[incl - cnt + __popc(chosen & ((1u << e) - 1u))] = (v4[e] << 16) | (uint32_t)(4 * lane + e);
+              v4[e] = 0u;
+            }
+          *xr = make_uint2(v4[0] | (v4[1] << 16), v4[2] | (v4[3] << 16));
+        }
+        __syncthreads();
+      }
       // Keys, per channel over the G tokens: two halves of the tokens, then the pair combined
       {
         const int c = tid & 127, half = tid >> 7, h0 = half * (G >> 1), h1 = h0 + (G >> 1);

@@ -294,7 +294,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // rescaled.  Returns p = 2^(sig - m).
 template <int NGV, bool kVarS>
 __device__ __forceinline__ void softmax_tile(WarpState<NGV>& st, const float (&sig)[4], float smax, int q,
-                                             float (&pr)[4]) {
+                                             float (&pr)[4], float* sp_row = nullptr) {
   const float mx = fmaxf(fmaxf(sig[0], sig[1]), fmaxf(sig[2], sig[3]));
   const bool bump = (smax > st.S * kSTau) || (mx > st.m + kTau);
   if (__any_sync(kFull, bump)) {
@@ -324,6 +324,19 @@ __device__ __forceinline__ void softmax_tile(WarpState<NGV>& st, const float (&s
     for (int j = 0; j < NGV; ++j) st.zacc[j] *= alpha * ratio;
     st.S = S_new;
     st.inv_S = 1.f / S_new;
+    if (sp_row) {  // dense-and-sparse: the column's sparse Value sums (lane q: channels 32q .. 32q + 31)
+      float4* p4 = reinterpret_cast<float4*>(sp_row + 32 * q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 v = p4[i];
+        v.x *= alpha;
+        v.y *= alpha;
+        v.z *= alpha;
+        v.w *= alpha;
+        p4[i] = v;
+      }
+      __syncwarp();
+    }
   }
   // ex2(-inf) = +0 for masked scores; the reference is -inf only while every score seen
   // so far (this tile's included) is -inf, then 0 stands in for it
@@ -826,8 +839,10 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // variant carries the limit checks.  ONE: integer layers whose Key groups are one
 // tile each (G = 16, the paged blocks): every tile rebuilds the query-side
 // operand, in straight-line code.  ROPE: pre-RoPE Keys (integer layers), rotated
-// at their positions.
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE>
+// at their positions.  OUT: dense-and-sparse rows (integer layers): the kept Key
+// entries add q_c x_c to the scores, the kept Value entries p x_c to the outputs
+// (through a per-warp shared-memory sum of 8 columns x 128 channels).
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE, bool OUT>
 __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
   constexpr int NW = DecodeWarps<FMT>::kNW;
@@ -863,6 +878,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   off += ((size_t)B * sizeof(int) + 15) / 16 * 16;
   // pre-RoPE Keys: per warp, the current Key group's header (K scale [128], K zero [128])
   float* rope_hdr = ROPE ? reinterpret_cast<float*>(smem + off) + warp * 256 : nullptr;
+  // dense-and-sparse Values: per warp, the sparse part of the 8 columns' outputs [8][128]
+  float* sp_acc = (OUT && L.v_out) ? reinterpret_cast<float*>(smem + off) + warp * 1024 : nullptr;
   __shared__ int seg_count;
   __shared__ long long batch_end;
 
@@ -1259,6 +1276,12 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
       const int nbf_tok = sg.n_sink + sg.r;
       WarpState<NGV> stt;
       state_init(stt);
+      if (sp_acc) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) reinterpret_cast<float4*>(sp_acc)[lane + 32 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+      }
+      float* sp_row = sp_acc ? sp_acc + r * 128 : nullptr;  // the lane's column
       const float* qrow = q_s + min(r, g) * kQRow;  // the lane's query column (row g is zero)
       const bool hv = r < g;                         // the column exists
       uint32_t X[8][4];  // query-side A operand (hi/lo rows), rebuilt per Key group for INT layers
@@ -1352,7 +1375,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               *reinterpret_cast<uint4*>(stw + (rows + idx / 16) * 256 + (idx % 16) * 16) = make_uint4(0u, 0u, 0u, 0u);
             __syncwarp();
             float pr[4];
-            softmax_tile<NGV, false>(stt, sig_bf, 1.f, q, pr);
+            softmax_tile<NGV, false>(stt, sig_bf, 1.f, q, pr, sp_row);
             // integer layers: the accumulators hold code units (2^-24, rows r + 8 FT::kVHi more)
             constexpr float kUnit = F::kInt ? 1.f / kCodeUnit : 1.f;
             bf16_pv<F::kInt ? (int)F::kVHi : 1>(vst, lane, pr, stt.inv_S * (kPrescale * kUnit), stt.o);
@@ -1394,6 +1417,18 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
 #pragma unroll
             for (int e = 0; e < 4; ++e)  // integer tiles are always full (Key groups of 16k tokens)
               sig[e] = (hv && (F::kInt || tk[e] < tok_valid)) ? fmaf(d[e], kfac, cterm) : -INFINITY;
+            if constexpr (OUT) {  // the tokens' kept Key entries: q_c x_c (exact bf16 x_c)
+              const uint32_t* ksp = reinterpret_cast<const uint32_t*>(tile + L.sp_off);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float a = 0.f;
+                for (int j = 0; j < L.k_out; ++j) {
+                  const uint32_t en = ksp[tk[e] * L.k_out + j];
+                  a = fmaf(qrow[en & 127u], __uint_as_float(en & 0xFFFF0000u), a);
+                }
+                sig[e] = fmaf(a, p.scale_log2, sig[e]);
+              }
+            }
             if (MQ && p.n_query > 1) {
               const int lim = col_limit() - (L.S + 16 * i);  // in tile rows (quantized token x = t - S)
 #pragma unroll
@@ -1413,7 +1448,18 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               }
             }
             float pt[4];
-            softmax_tile<NGV, F::kInt>(stt, sig, smax, q, pt);
+            softmax_tile<NGV, F::kInt>(stt, sig, smax, q, pt, sp_row);
+            if constexpr (OUT) {  // the tokens' kept Value entries: p x_c into the column's sparse sums
+              if (sp_row) {
+                const uint32_t* vsp = reinterpret_cast<const uint32_t*>(tile + L.sp_off + 64 * L.k_out);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  for (int j = 0; j < L.v_out; ++j) {
+                    const uint32_t en = vsp[tk[e] * L.v_out + j];
+                    atomicAdd(sp_row + (en & 127u), pt[e] * __uint_as_float(en & 0xFFFF0000u));
+                  }
+              }
+            }
             // PV: the lane's probabilities are already in the W layout (column r, its four tokens)
             uint32_t B0[NGV], B1[NGV];
             if constexpr (F::kFp8) {
@@ -1512,6 +1558,19 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           stt.o[mb][e] = empty ? 0.f : fmaf(stt.o[mb][e], kC0, -z) * unit;
           stt.o[mb][2 + e] = empty ? 0.f : fmaf(stt.o[mb][2 + e], kC1, -z) * unit;
         }
+      if (sp_acc) {  // dense-and-sparse: the sparse Value sums of columns 2q, 2q + 1
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) {
+            const float* sr = sp_acc + (2 * q + e) * 128 + 16 * mb + r;
+            if (mo[e] != -INFINITY) {
+              stt.o[mb][e] += sr[0];
+              stt.o[mb][2 + e] += sr[8];
+            }
+          }
+      }
       // ---- fold the warps pairwise into NW/2 merge records: warp w + NW/2 writes record w, then
       // warp w folds its own state into it ----
       if (warp >= NR) {
@@ -1723,7 +1782,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool OUT = false>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1732,17 +1791,17 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem);
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool OUT = false>
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE, ROPE>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE, ROPE, OUT>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1758,6 +1817,14 @@ cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream
     return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, false>(p, smem, stream)
                          : launch_variant<FMT, NGV, true, false, false>(p, smem, stream);
   } else {
+    if (p.L.k_out || p.L.v_out) {  // dense-and-sparse: Value groups of 64 or 128 channels, one query token
+      if constexpr (NGV <= 2) {
+        return p.L.tpg == 1 ? launch_variant<FMT, NGV, true, false, true, false, true>(p, smem, stream)
+                            : launch_variant<FMT, NGV, true, false, false, false, true>(p, smem, stream);
+      } else {
+        return cudaErrorInvalidValue;
+      }
+    }
     if (p.L.rope) {  // pre-RoPE Keys: Value groups of 64 or 128 channels, one query token (host-checked)
       if constexpr (NGV <= 2) {
         return p.L.tpg == 1 ? launch_variant<FMT, NGV, true, false, true, true>(p, smem, stream)
@@ -1780,7 +1847,7 @@ template <int FMT, int NGV, bool MQ>
 cudaError_t occupancy_variant(int smem, int* n) {
   cudaError_t e = ensure_smem_attr<FMT, NGV, true, MQ, false>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false, false>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false, false, false>,
                                                        DecodeWarps<FMT>::kThreads, smem);
 }
 template <int FMT, int NGV>

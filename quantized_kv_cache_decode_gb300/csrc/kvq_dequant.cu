@@ -66,6 +66,13 @@ __global__ void __launch_bounds__(128) dequant_kernel(const DequantParams p) {
           const int j = c / L.Gv;
           kx = __fmul_rn(ks[c], __fsub_rn((float)kcode, kz[c]));
           vx = __fmul_rn(vs[row * L.ngv + j], __fsub_rn((float)vcode, vz[row * L.ngv + j]));
+          // dense-and-sparse: a kept entry adds its exact value (one more fp32 add)
+          const uint32_t* ksp = reinterpret_cast<const uint32_t*>(tile + L.sp_off) + row * L.k_out;
+          const uint32_t* vsp = reinterpret_cast<const uint32_t*>(tile + L.sp_off + 64 * L.k_out) + row * L.v_out;
+          for (int e = 0; e < L.k_out; ++e)
+            if ((int)(ksp[e] & 127u) == c) kx = __fadd_rn(kx, __uint_as_float(ksp[e] & 0xFFFF0000u));
+          for (int e = 0; e < L.v_out; ++e)
+            if ((int)(vsp[e] & 127u) == c) vx = __fadd_rn(vx, __uint_as_float(vsp[e] & 0xFFFF0000u));
         }
       }
     } else if (t < T) {

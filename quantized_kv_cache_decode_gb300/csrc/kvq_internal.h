@@ -41,6 +41,8 @@ struct LayerDesc {
   long long block_bytes;  // paged: H records
   int rope;               // Keys stored before RoPE, rotated at their position by the decode
   float rope_base;
+  int k_out, v_out;       // dense-and-sparse: entries kept exactly per quantized Key / Value row
+  int sp_off;             // byte offset of a tile's K sparse entries (the V ones follow, 64 * k_out later)
 };
 
 struct CachePtrs {

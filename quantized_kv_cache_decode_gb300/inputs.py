@@ -59,6 +59,7 @@ class LayerFormat:
     R:   residual window: the most recent tokens kept in bf16
     S:   sink tokens kept in bf16 at the start of the sequence
     rope_base: > 0: Keys stored before RoPE and rotated at their position by the decode
+    k_outliers, v_outliers: dense-and-sparse rows (entries per quantized row kept exactly)
     """
 
     fmt: str
@@ -67,6 +68,8 @@ class LayerFormat:
     R: int
     S: int
     rope_base: float = 0.0
+    k_outliers: int = 0
+    v_outliers: int = 0
 
 
 @dataclasses.dataclass
@@ -136,6 +139,14 @@ def llama3_8b_int4_prerope() -> Workload:
                     seed=1009)
 
 
+def llama3_8b_int4_sparse() -> Workload:
+    """Llama-3-8B-shaped KIVI INT4 layer (B=16, T=8192, 32/8 heads, G=128, Gv=128, R=128) with dense-and-
+    sparse rows: 2 Key and 2 Value entries of every quantized row (about 1.6 %) kept exactly."""
+    fmt = LayerFormat("int4", G=128, Gv=128, R=128, S=0, k_outliers=2, v_outliers=2)
+    return Workload("llama3_8b_kivi_int4_sparse", 1, 16, 32, 8, 128, 8192, [fmt], 4, 0, 10.0, "per_head",
+                    seed=1010)
+
+
 def llama3_70b_int4() -> Workload:
     """Llama-3-70B-shaped decode over 80 layers, KIVI INT4 (G=128, Gv=128, R=128)."""
     fmt = LayerFormat("int4", G=128, Gv=128, R=128, S=0)
@@ -166,6 +177,7 @@ WORKLOADS = {
     "llama3_8b_bf16_skip_layer": llama3_8b_bf16_skip,
     "llama3_8b_fp8_e4m3_2q": llama3_8b_fp8_2q,
     "llama3_8b_kivi_int4_prerope": llama3_8b_int4_prerope,
+    "llama3_8b_kivi_int4_sparse": llama3_8b_int4_sparse,
     "llama3_70b_kivi_int4_80l": llama3_70b_int4,
     "llama2_7b_kivi2_int2_32k": llama2_7b_int2,
     "paged_mixed_int8_int4_64l": paged_mixed,

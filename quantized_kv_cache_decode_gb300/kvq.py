@@ -43,7 +43,8 @@ class KvqError(RuntimeError):
 class LayerConfig(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("num_kv_heads", "head_dim", "format", "k_group_tokens", "v_group_dims",
                                      "residual_tokens", "sink_tokens", "paged", "block_tokens", "capacity_tokens",
-                                     "num_blocks", "max_blocks_per_seq")] + [("rope_base", ctypes.c_float)]
+                                     "num_blocks", "max_blocks_per_seq")] + [("rope_base", ctypes.c_float),
+                                                                             ("k_outliers", c_i32), ("v_outliers", c_i32)]
 
 
 class LayerCache(ctypes.Structure):
@@ -118,10 +119,12 @@ def _stream_ptr(stream) -> Optional[int]:
 
 def make_config(fmt: str, num_kv_heads: int, G: int, Gv: int, R: int, S: int, *, paged: bool = False,
                 block_tokens: int = 0, capacity_tokens: int = 0, num_blocks: int = 0,
-                max_blocks_per_seq: int = 0, head_dim: int = 128, rope_base: float = 0.0) -> LayerConfig:
-    """rope_base > 0: the layer's Keys are appended before RoPE and rotated at their position by the decode."""
+                max_blocks_per_seq: int = 0, head_dim: int = 128, rope_base: float = 0.0, k_outliers: int = 0,
+                v_outliers: int = 0) -> LayerConfig:
+    """rope_base > 0: the layer's Keys are appended before RoPE and rotated at their position by the decode.
+    k_outliers / v_outliers > 0: dense-and-sparse rows (that many entries per row kept exactly)."""
     return LayerConfig(num_kv_heads, head_dim, FORMATS[fmt], G, Gv, R, S, int(paged), block_tokens,
-                       capacity_tokens, num_blocks, max_blocks_per_seq, rope_base)
+                       capacity_tokens, num_blocks, max_blocks_per_seq, rope_base, k_outliers, v_outliers)
 
 
 def cache_layout(cfg: LayerConfig, num_seqs: int) -> Dict[str, int]:

@@ -78,7 +78,8 @@ class GpuLayer:
 
     def __init__(self, fmt: str, H: int, lens: Sequence[int], G: int, Gv: int, R: int, S: int, *,
                  paged: bool = False, block_tokens: int = 16, spare_blocks: int = 3, seed: int = 0,
-                 extra_capacity: int = 0, device="cuda", rope_base: float = 0.0):
+                 extra_capacity: int = 0, device="cuda", rope_base: float = 0.0, k_outliers: int = 0,
+                 v_outliers: int = 0):
         import torch
         from quantized_kv_cache_decode_gb300 import kvq
         self.torch, self.kvq = torch, kvq
@@ -90,7 +91,10 @@ class GpuLayer:
         self.Gv = 128 if (self.fp8 or self.bf16) else Gv
         self.R = 0 if (self.fp8 or self.bf16) else R
         self.S = S
-        self.spec = O.Spec(fmt, d=128, G=self.G, Gv=self.Gv, R=self.R, S=S, rope_base=rope_base)
+        self.spec = O.Spec(fmt, d=128, G=self.G, Gv=self.Gv, R=self.R, S=S, rope_base=rope_base,
+                           k_outliers=k_outliers, v_outliers=v_outliers)
+        self.nk, self.nv = k_outliers, v_outliers
+        out_kw = dict(rope_base=rope_base, k_outliers=k_outliers, v_outliers=v_outliers)
         self.device = device
         self.paged = paged
         maxq = max([O.token_split(T + extra_capacity, self.spec)[1] for T in self.lens] + [0])
@@ -105,10 +109,10 @@ class GpuLayer:
             self.mbps = max(blocks_per_seq + [1])
             nblocks = sum(blocks_per_seq) + spare_blocks
             self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, paged=True, block_tokens=self.P,
-                                       num_blocks=nblocks, max_blocks_per_seq=self.mbps, rope_base=rope_base)
+                                       num_blocks=nblocks, max_blocks_per_seq=self.mbps, **out_kw)
         else:
             cap = max(unit, math.ceil(maxq / unit) * unit)
-            self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, capacity_tokens=cap, rope_base=rope_base)
+            self.cfg = kvq.make_config(fmt, H, self.G, self.Gv, self.R, S, capacity_tokens=cap, **out_kw)
         self.layer = kvq.CacheLayer(self.cfg, self.B, device=device)
         if paged:
             rng = np.random.default_rng(seed + 77)
@@ -195,7 +199,7 @@ class GpuLayer:
     def _layout(self):
         rb = 128 * BITS.get(self.fmt, 8) // 8
         ngv = 128 // self.Gv
-        tile = 32 * rb + (0 if self.fp8 else 128 * ngv)
+        tile = 32 * rb + (0 if self.fp8 else 128 * ngv + 64 * (self.nk + self.nv))
         hdr = 0 if self.fp8 else 1024
         tpg = (self.P // 16) if self.paged else (1 if self.fp8 else self.G // 16)
         return rb, ngv, tile, hdr, tpg, hdr + tpg * tile
@@ -215,7 +219,7 @@ class GpuLayer:
     def logical(self, b: int, h: int, T: int) -> Dict[str, np.ndarray]:
         n_sink, qn, r = O.token_split(T, self.spec)
         rb, ngv, tile, hdr, tpg, rec = self._layout()
-        kc, vt, ks, kz, vs, vz = [], [], [], [], [], []
+        kc, vt, ks, kz, vs, vz, kspl, vspl = [], [], [], [], [], [], [], []
         ntiles = (qn + 15) // 16
         for i in range(ntiles):
             recb = self._record(b, h, i // tpg)
@@ -224,7 +228,10 @@ class GpuLayer:
             vt.append(t[16 * rb:32 * rb].reshape(1, 16 * rb))
             if not self.fp8:
                 vs.append(t[32 * rb:32 * rb + 64 * ngv].view(F32).reshape(16, ngv))
-                vz.append(t[32 * rb + 64 * ngv:].view(F32).reshape(16, ngv))
+                vz.append(t[32 * rb + 64 * ngv:32 * rb + 128 * ngv].view(F32).reshape(16, ngv))
+                sp0 = 32 * rb + 128 * ngv
+                kspl.append(t[sp0:sp0 + 64 * self.nk].view(np.uint32).reshape(16, self.nk))
+                vspl.append(t[sp0 + 64 * self.nk:sp0 + 64 * (self.nk + self.nv)].view(np.uint32).reshape(16, self.nv))
                 if i % tpg == 0:
                     ks.append(recb[:512].view(F32).reshape(1, 128))
                     kz.append(recb[512:1024].view(F32).reshape(1, 128))
@@ -236,6 +243,11 @@ class GpuLayer:
             out["k_z"] = np.concatenate(kz)[:qn // self.G] if kz else np.zeros((0, 128), F32)
             out["v_s"] = np.concatenate(vs)[:qn] if vs else np.zeros((0, ngv), F32)
             out["v_z"] = np.concatenate(vz)[:qn] if vz else np.zeros((0, ngv), F32)
+            # dense-and-sparse entries: bf16 bits << 16 | channel
+            ke = np.concatenate(kspl)[:qn] if kspl else np.zeros((0, self.nk), np.uint32)
+            ve = np.concatenate(vspl)[:qn] if vspl else np.zeros((0, self.nv), np.uint32)
+            out["k_sp_idx"], out["k_sp_bits"] = (ke & 127).astype(np.int64), (ke >> 16).astype(np.uint16)
+            out["v_sp_idx"], out["v_sp_bits"] = (ve & 127).astype(np.int64), (ve >> 16).astype(np.uint16)
         out["k_codes"] = unpack_tiles(kc, self.fmt, ktile_positions)[:qn] if len(kc) else np.zeros((0, 128), np.uint8)
         out["v_codes"] = unpack_tiles(vt, self.fmt, vtile_positions)[:qn] if len(vt) else np.zeros((0, 128), np.uint8)
         pair = b * self.H + h
@@ -260,6 +272,9 @@ def compare_logical(gpu: Dict[str, np.ndarray], hc: "O.HeadCache"):
         for f in ("k_s", "k_z", "v_s", "v_z"):
             g, o = gpu[f], getattr(hc, f)
             assert g.shape == o.shape and np.array_equal(g.view(np.uint32), o.astype(F32).view(np.uint32)), f
+        for kv in ("k", "v"):  # dense-and-sparse lists
+            assert np.array_equal(gpu[kv + "_sp_idx"], getattr(hc, kv + "_sp_idx")), kv + " sparse channels"
+            assert np.array_equal(gpu[kv + "_sp_bits"], bf16_bits(getattr(hc, kv + "_sp_val"))), kv + " sparse values"
     if len(hc.sink_k):
         assert np.array_equal(gpu["sink_k"], bf16_bits(hc.sink_k)) and np.array_equal(gpu["sink_v"], bf16_bits(hc.sink_v))
     if not hc.spec.is_fp8:

@@ -96,6 +96,13 @@ def test_cache_layout_sizes(kvq):
     (dict(fmt="int4", num_kv_heads=2, G=32, Gv=32, R=0, S=0, capacity_tokens=64, rope_base=1e4), -2),
     (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, rope_base=0.5), -1),
     (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, rope_base=float("nan")), -1),
+    # dense-and-sparse rows: 0..8 entries, integer formats, Gv of 64 or 128, not with pre-RoPE Keys
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, k_outliers=9), -1),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, v_outliers=-1), -1),
+    (dict(fmt="fp8_e4m3", num_kv_heads=2, G=1, Gv=128, R=0, S=0, capacity_tokens=64, k_outliers=1), -2),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=16, R=0, S=0, capacity_tokens=64, v_outliers=1), -2),
+    (dict(fmt="int4", num_kv_heads=2, G=32, Gv=128, R=0, S=0, capacity_tokens=64, k_outliers=1,
+          rope_base=1e4), -2),
 ])
 def test_config_validation(kvq, kw, status):
     kw = dict(kw)
@@ -197,3 +204,10 @@ def test_pre_rope_keys_reject_several_query_tokens(kvq):
     with pytest.raises(kvq.KvqError) as e:
         kvq.decode_attention_multi(cfg, cache, 0, 2, 8, 0, 1, 0.1, 4096, False, 0, 0, 0, 0, stream=0)
     assert e.value.status == -2
+
+
+def test_outlier_layout_sizes(kvq):
+    # a dense-and-sparse tile carries 16 x (k + v) entries of 4 bytes after the Value scales
+    cfg = kvq.make_config("int4", 8, 16, 128, 64, 1, paged=True, block_tokens=16, num_blocks=10,
+                          max_blocks_per_seq=4, k_outliers=2, v_outliers=3)
+    assert kvq.cache_layout(cfg, 2)["block_pool"] == 10 * 8 * (3200 + 64 * 5)

@@ -40,9 +40,10 @@ def make_inputs(seed, H, g, lens, outliers=4, scale=10.0):
     return kv, q
 
 
-def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=None, rope_base=0.0):
+def build(fmt, H, g, lens, G, Gv, R, S, paged, seed, block_tokens=16, chunks=None, rope_base=0.0, k_outliers=0,
+          v_outliers=0):
     gl = TL.GpuLayer(fmt, H, lens, G, Gv, R, S, paged=paged, block_tokens=block_tokens, seed=seed,
-                     rope_base=rope_base)
+                     rope_base=rope_base, k_outliers=k_outliers, v_outliers=v_outliers)
     kv, q = make_inputs(seed, H, g, lens)
     ks = vs = None
     if gl.fp8:
@@ -373,6 +374,41 @@ def test_pre_rope_parity(case):
             kr, vr = O.dequantized_f32(caches[b][h])
             assert np.array_equal(ko[b, h, :T].view(np.uint32), kr.view(np.uint32))
     # attention over the Keys rotated at their positions
+    out_ref, lse_ref = O.decode_attention(O.bf16_to_f32(q), caches)
+    out, lse = gl.decode(q)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+    out16, lse16 = gl.decode(q, out_bf16=True)
+    assert torch.equal(out16, out.to(torch.bfloat16)) and torch.equal(lse16, lse)
+    assert gl.status_value() == 0
+
+
+OUTLIER_CASES = [
+    # fmt, H, g, lens, G, Gv, R, S, paged, k_outliers, v_outliers: dense-and-sparse rows
+    # ("KV Cache Quantization Analysis", section 4, KVQuant item (iv))
+    ("int4", 2, 4, [700, 33, 129, 0], 32, 128, 32, 1, False, 2, 2),
+    ("int2", 2, 6, [300, 17, 80, 81, 2], 16, 64, 64, 1, True, 1, 3),
+    ("int8", 3, 1, [1000, 160, 5], 32, 128, 128, 0, False, 8, 0),
+    ("int4", 2, 8, [500, 96], 16, 128, 16, 2, True, 0, 8),
+    ("int4", 1, 8, [20000], 128, 64, 128, 2, False, 3, 1),
+]
+
+
+@pytest.mark.parametrize("case", OUTLIER_CASES, ids=[f"{c[0]}-H{c[1]}g{c[2]}-G{c[4]}Gv{c[5]}R{c[6]}S{c[7]}"
+                                                     f"{'-paged' if c[8] else ''}-k{c[9]}v{c[10]}" for c in OUTLIER_CASES])
+def test_dense_and_sparse_parity(case):
+    fmt, H, g, lens, G, Gv, R, S, paged, nk, nv = case
+    seed = zlib.crc32(repr(case).encode()) % 10000
+    gl, caches, q = build(fmt, H, g, lens, G, Gv, R, S, paged, seed, k_outliers=nk, v_outliers=nv)
+    # codes of the dense part, scales, zero-points and the sparse lists: bit-exact
+    for b, T in enumerate(lens):
+        for h in range(H):
+            TL.compare_logical(gl.logical(b, h, T), caches[b][h])
+    ko, vo = gl.dequantize(max(lens) + 1)
+    for b, T in enumerate(lens):
+        for h in range(H):
+            kr, vr = O.dequantized_f32(caches[b][h])
+            assert np.array_equal(ko[b, h, :T].view(np.uint32), kr.view(np.uint32))
+            assert np.array_equal(vo[b, h, :T].view(np.uint32), vr.view(np.uint32))
     out_ref, lse_ref = O.decode_attention(O.bf16_to_f32(q), caches)
     out, lse = gl.decode(q)
     TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
