@@ -381,11 +381,15 @@ def run_gpu(args, w, rank, world):
     barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
+    if args.profile_range:  # ncu --profile-from-start off then sees only the timed steps
+        torch.cuda.profiler.start()
     t_start.record(stream)
     for i in range(K):
         step(args.warmup + i, evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
+    if args.profile_range:
+        torch.cuda.profiler.stop()
     wall1 = time.time()
     barrier()
     ms = t_start.elapsed_time(t_end)
@@ -677,6 +681,8 @@ def main():
                     help="run only the first N layers of the workload (profiling captures; 0: all)")
     ap.add_argument("--only-layers", default="",
                     help="comma-separated layer indices to run (profiling captures of chosen layers)")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     w = I.WORKLOADS[args.workload]()
