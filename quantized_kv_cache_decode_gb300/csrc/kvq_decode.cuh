@@ -494,6 +494,54 @@ __device__ __forceinline__ void pv_tile(const uint32_t (&VW)[FT<FMT>::kWords], c
   }
 }
 
+// Few query columns (KA: at most 4 heads, one query token): the Key tile is the A
+// operand (rows = tokens r, r + 8 of the lane, K index in the codes' fragment
+// order) and the query side the B operand, whose column n holds head n / 2's high
+// (n even) or low (n odd) f16 half.  The B fragment of lane (r, q) is column r at
+// K indices 2q, 2q + 1, 2q + 8, 2q + 9, i.e. channels 16s + 4q .. 16s + 4q + 3 of
+// head r / 2: the query-rows operand of that head (built by the same builders from
+// its query row), one half of it.  ka_operand keeps the lane's half and moves the
+// per-head score factors (kfac, cterm; built per head r / 2) to the column layout
+// of the scores (column r = head r, taken from lane 8r).
+__device__ __forceinline__ void ka_operand(uint32_t (&X)[8][4], int r, float& kfac, float& cterm) {
+  const bool lo = (r & 1) != 0;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t b0 = lo ? X[s][1] : X[s][0], b1 = lo ? X[s][3] : X[s][2];
+    X[s][0] = b0;
+    X[s][1] = b1;
+  }
+  const int src = 8 * (r & 3);
+  kfac = __shfl_sync(kFull, kfac, src);
+  cterm = __shfl_sync(kFull, cterm, src);
+}
+
+// Raw scores of one quantized tile with the Key tile as the A operand (KA): one
+// MMA per step (8 per tile, two chains); D(token, column) of lane (r, q) holds
+// tokens r, r + 8 of head q, high and low halves in columns 2q, 2q + 1.  Four
+// shuffles bring them to the query-rows layout of qk_tile (column r, tokens 2q,
+// 2q + 1, 2q + 8, 2q + 9): token 2q's score sits in lane 8q + r, token 2q + 1's
+// in lane 8q + 4 + r (columns r >= 4 read some lane's value; they are masked).
+template <int FMT>
+__device__ __forceinline__ void qk_tile_ka(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&X)[8][4],
+                                           int lane, float (&d)[4]) {
+  float acc[2][4] = {};
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    uint32_t a0, a1, a2, a3;
+    if constexpr (FT<FMT>::kKRaw) unpack_raw<FMT>(KW, s, a0, a1, a2, a3);
+    else unpack_a<FMT>(KW, s, a0, a1, a2, a3);
+    mma_f16(acc[s & 1], a0, a1, a2, a3, X[s][0], X[s][1]);
+  }
+  const float t0 = (acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]);  // token r
+  const float t8 = (acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]);  // token r + 8
+  const int src = 8 * (lane & 3) + ((lane >> 2) & 3);
+  d[0] = __shfl_sync(kFull, t0, src);
+  d[1] = __shfl_sync(kFull, t0, src + 4);
+  d[2] = __shfl_sync(kFull, t8, src);
+  d[3] = __shfl_sync(kFull, t8, src + 4);
+}
+
 // Scores of a bf16 tile from its K rows in shared memory (rows past `rows` masked):
 // the query column (bf16, exact) in A rows 0-7, rows 8-15 zero; the K rows as the B
 // operand through ldmatrix (natural channel order).
@@ -841,10 +889,14 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // operand, in straight-line code.  ROPE: pre-RoPE Keys (integer layers), rotated
 // at their positions.  OUT: dense-and-sparse rows (integer layers): the kept Key
 // entries add q_c x_c to the scores, the kept Value entries p x_c to the outputs
-// (through a per-warp shared-memory sum of 8 columns x 128 channels).
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE, bool OUT>
+// (through a per-warp shared-memory sum of 8 columns x 128 channels).  KA: at most
+// four query columns (one query token): the Key tile is the A operand of the QK
+// MMAs and the query side the B operand (qk_tile_ka), half the MMAs of the
+// query-rows form.
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE, bool OUT, bool KA>
 __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using F = FT<FMT>;
+  static_assert(!KA || (!MQ && !ROPE && !OUT), "the Key-as-A form serves one query token, plain Keys");
   constexpr int NW = DecodeWarps<FMT>::kNW;
   constexpr int NT = NW * 32;
   constexpr int NR = NW / 2;  // merge records (warps fold pairwise into them)
@@ -1283,6 +1335,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
       }
       float* sp_row = sp_acc ? sp_acc + r * 128 : nullptr;  // the lane's column
       const float* qrow = q_s + min(r, g) * kQRow;  // the lane's query column (row g is zero)
+      const float* qrow_op = KA ? q_s + min(r >> 1, g) * kQRow : qrow;  // the row the lane's operand is built from
       const bool hv = r < g;                         // the column exists
       uint32_t X[8][4];  // query-side A operand (hi/lo rows), rebuilt per Key group for INT layers
       float kfac = 0.f, cterm = 0.f;
@@ -1293,9 +1346,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
         build_x_rope(qrow, q, X, kapq, invq);
         kfacq = p.scale_log2 * invq;
       } else if constexpr (F::kFp8) {
-        build_x_fp8(qrow, q, p.scale_log2 * __ldg(p.C.k_tscale), X, kfac);
+        build_x_fp8(qrow_op, q, p.scale_log2 * __ldg(p.C.k_tscale), X, kfac);
+        if constexpr (KA) ka_operand(X, r, kfac, cterm);
       } else {
-        qm = column_qmax(qrow, q);
+        qm = column_qmax(qrow_op, q);
 
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) X[s2][0] = X[s2][1] = X[s2][2] = X[s2][3] = 0u;
@@ -1397,10 +1451,12 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
                 kfac = kfacq * invk;
               }
             } else if constexpr (F::kInt) {
-              if (build)
-                build_x_group<FMT>(qrow, reinterpret_cast<const float*>(hdrp),
+              if (build) {
+                build_x_group<FMT>(qrow_op, reinterpret_cast<const float*>(hdrp),
                                    reinterpret_cast<const float*>(hdrp + 512), lane, q, p.scale_log2, qm, X, kfac,
                                    cterm);
+                if constexpr (KA) ka_operand(X, r, kfac, cterm);
+              }
             }
             // QK
             float d[4];
@@ -1409,6 +1465,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               load_words(tile, lane, KW);
               if constexpr (ROPE)
                 qk_tile_rope<FMT>(KW, X, rope_hdr, rope_hdr + 128, s_turn, L.S + 16 * i, r, q, kapk, d);
+              else if constexpr (KA)
+                qk_tile_ka<FMT>(KW, X, lane, d);
               else
                 qk_tile<FMT>(KW, X, d);
             }
@@ -1782,7 +1840,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
 
 // Raise the kernel's dynamic shared-memory limit on the current device once per
 // size (the attribute is per device and persists; repeated calls are skipped).
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool OUT = false>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool OUT = false, bool KA = false>
 cudaError_t ensure_smem_attr(int smem) {
   static std::mutex mu;
   static int set_for[64] = {};
@@ -1791,17 +1849,17 @@ cudaError_t ensure_smem_attr(int smem) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && set_for[dev] >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT>,
+  e = cudaFuncSetAttribute(decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT, KA>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) set_for[dev] = smem;
   return e;
 }
 
-template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool OUT = false>
+template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool OUT = false, bool KA = false>
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE, ROPE, OUT>(smem);
+  cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE, ROPE, OUT, KA>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
+  decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT, KA><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1810,10 +1868,14 @@ cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream)
 // layers with one tile per Key group the straight-line variant.
 template <int FMT, int NGV>
 cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream) {
+  const bool ka = p.n_query == 1 && p.g <= 4;  // few query columns: the Key tile as the A operand
   if constexpr (FT<FMT>::kFp8) {
-    if (p.L.S == 0)
+    if (p.L.S == 0) {
+      if (ka) return launch_variant<FMT, NGV, false, false, false, false, false, true>(p, smem, stream);
       return p.n_query > 1 ? launch_variant<FMT, NGV, false, true, false>(p, smem, stream)
                            : launch_variant<FMT, NGV, false, false, false>(p, smem, stream);
+    }
+    if (ka) return launch_variant<FMT, NGV, true, false, false, false, false, true>(p, smem, stream);
     return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, false>(p, smem, stream)
                          : launch_variant<FMT, NGV, true, false, false>(p, smem, stream);
   } else {
@@ -1833,6 +1895,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream
         return cudaErrorInvalidValue;
       }
     }
+    if (ka)
+      return p.L.tpg == 1 ? launch_variant<FMT, NGV, true, false, true, false, false, true>(p, smem, stream)
+                          : launch_variant<FMT, NGV, true, false, false, false, false, true>(p, smem, stream);
     if (p.L.tpg == 1)
       return p.n_query > 1 ? launch_variant<FMT, NGV, true, true, true>(p, smem, stream)
                            : launch_variant<FMT, NGV, true, false, true>(p, smem, stream);
@@ -1847,7 +1912,7 @@ template <int FMT, int NGV, bool MQ>
 cudaError_t occupancy_variant(int smem, int* n) {
   cudaError_t e = ensure_smem_attr<FMT, NGV, true, MQ, false>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false, false, false>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, decode_kernel<FMT, NGV, true, MQ, false, false, false, false>,
                                                        DecodeWarps<FMT>::kThreads, smem);
 }
 template <int FMT, int NGV>
