@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 // ---------------------------------------------------------------------------
 // spill_kernel: the Key groups (and their G Value tokens) that leave the residual
 // window in this append, quantized and written in fragment order.
-// One CTA of 256 threads per (sequence, kv head, spilled group): the group's G
+// One CTA of NT threads per (sequence, kv head, spilled group): the group's G
 // bf16 Key and Value rows are staged in shared memory (coalesced 16-byte loads,
 // from the ring for tokens already cached, from the input for new ones); every
 // channel's Key min/max is found by two threads over half the tokens each, every
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 // stay in the residual window (one-token appends: those rows are never read by
 // the spill of the same call; longer appends write them in a second launch).
 // ---------------------------------------------------------------------------
-constexpr int kSpillThreads = 256;
+constexpr int kSRow = 136;  // staged row stride (bf16): rows 8 banks apart, so the code pass reads without conflicts
 
 // (step, reg, half) of the b-bit field at bit bp of operand word w: the inverse
 // of frag_pos for the integer formats
@@ -158,8 +158,9 @@ __device__ __forceinline__ void frag_field(int w, int bp, int& step, int& reg, i
   }
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams p, int rest) {
+template <int BITS, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) spill_kernel(const AppendParams p, int rest) {
+  constexpr int kKSegs = NT / 128;  // runs of tokens per Key channel in the min/max pass (G >= 16 >= 2 kKSegs)
   extern __shared__ __align__(16) uint8_t smem[];
   const LayerDesc& L = p.L;
   constexpr int kLevels = (1 << BITS) - 1;
@@ -191,19 +192,19 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
     const long long x0 = (long long)grp * G;  // first quantized index of the group
     uint8_t* rec = record_w(L, p.C, b, h, grp, tid == 0 ? p.status : nullptr);
     if (rec) {  // (uniform over the CTA)
-      __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem);  // [G][128]
-      __nv_bfloat16* Vs = Ks + G * 128;                             // [G][128]
-      float* ksz = reinterpret_cast<float*>(Vs + G * 128);          // K scale [128], K zero [128]
-      float* red = ksz + 256;                                       // [2 halves][min, max][128]
-      float* vsz = red + 512;                                       // V scale [G][ngv], V zero [G][ngv]
+      __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem);  // [G][kSRow]
+      __nv_bfloat16* Vs = Ks + G * kSRow;                           // [G][kSRow]
+      float* ksz = reinterpret_cast<float*>(Vs + G * kSRow);        // K scale [128], K zero [128]
+      float* red = ksz + 256;                                       // [kKSegs][min, max][128]
+      float* vsz = red + kKSegs * 256;                              // V scale [G][ngv], V zero [G][ngv]
       // stage the group's rows: 16-byte chunk ch of row tt, K then V
-      for (int idx = tid; idx < 2 * G * 16; idx += kSpillThreads) {
+      for (int idx = tid; idx < 2 * G * 16; idx += NT) {
         const int which = idx >= G * 16, rem = idx - which * G * 16, tt = rem >> 4, ch = rem & 15;
         const long long t = L.S + x0 + tt;
         const __nv_bfloat16* src;
         if (t < T0) src = (which ? ring_v : ring_k) + (pair * L.W + (t - L.S) % L.W) * L.d;
         else src = (which ? vnew : knew) + (t - T0) * L.d;
-        reinterpret_cast<uint4*>((which ? Vs : Ks) + tt * 128)[ch] = reinterpret_cast<const uint4*>(src)[ch];
+        reinterpret_cast<uint4*>((which ? Vs : Ks) + tt * kSRow)[ch] = reinterpret_cast<const uint4*>(src)[ch];
       }
       __syncthreads();
       if (L.k_out | L.v_out) {
@@ -211,10 +212,10 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
         // the lower channel) go to the tile's sparse list, in channel order, and are set to 0 in
         // the staged row, which the statistics and codes below then see (one warp per row;
         // lane l holds channels 4l .. 4l + 3; bf16 magnitude bits order like the magnitudes)
-        for (int row = warp; row < 2 * G; row += kSpillThreads / 32) {
+        for (int row = warp; row < 2 * G; row += NT / 32) {
           const int isv = row >= G, tt = row - isv * G, n = isv ? L.v_out : L.k_out;
           if (n == 0) continue;
-          uint2* xr = reinterpret_cast<uint2*>((isv ? Vs : Ks) + tt * 128) + lane;
+          uint2* xr = reinterpret_cast<uint2*>((isv ? Vs : Ks) + tt * kSRow) + lane;
           const uint2 raw = *xr;
           uint32_t v4[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
           uint32_t chosen = 0;
@@ -248,23 +249,23 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
         }
         __syncthreads();
       }
-      // Keys, per channel over the G tokens: two halves of the tokens, then the pair combined
+      // Keys, per channel over the G tokens: kKSegs equal runs of tokens, then the runs combined
       {
-        const int c = tid & 127, half = tid >> 7, h0 = half * (G >> 1), h1 = h0 + (G >> 1);
-        float mn = __bfloat162float(Ks[h0 * 128 + c]), mx = mn;
+        const int c = tid & 127, sg = tid >> 7, h0 = sg * (G / kKSegs), h1 = h0 + G / kKSegs;
+        float mn = __bfloat162float(Ks[h0 * kSRow + c]), mx = mn;
         for (int tt = h0 + 1; tt < h1; ++tt) {
-          const float x = __bfloat162float(Ks[tt * 128 + c]);
+          const float x = __bfloat162float(Ks[tt * kSRow + c]);
           mn = fminf(mn, x);
           mx = fmaxf(mx, x);
         }
-        red[half * 256 + c] = mn;
-        red[half * 256 + 128 + c] = mx;
+        red[sg * 256 + c] = mn;
+        red[sg * 256 + 128 + c] = mx;
       }
       // Values, per token and Gv-channel group: lane holds channels 4 lane .. 4 lane + 3
       {
         const int seg = Gv >> 2;  // lanes per Value group
-        for (int tt = warp; tt < G; tt += kSpillThreads / 32) {
-          const uint2 raw = reinterpret_cast<const uint2*>(Vs + tt * 128)[lane];
+        for (int tt = warp; tt < G; tt += NT / 32) {
+          const uint2 raw = reinterpret_cast<const uint2*>(Vs + tt * kSRow)[lane];
           const float2 a = unpack_bf16(raw.x), c2 = unpack_bf16(raw.y);
           float mn = fminf(fminf(a.x, a.y), fminf(c2.x, c2.y)), mx = fmaxf(fmaxf(a.x, a.y), fmaxf(c2.x, c2.y));
           for (int o = 1; o < seg; o <<= 1) {
@@ -285,7 +286,12 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
       }
       __syncthreads();
       if (tid < 128) {
-        const float mn = fminf(red[tid], red[256 + tid]), mx = fmaxf(red[128 + tid], red[384 + tid]);
+        float mn = red[tid], mx = red[128 + tid];
+#pragma unroll
+        for (int sg = 1; sg < kKSegs; ++sg) {
+          mn = fminf(mn, red[sg * 256 + tid]);
+          mx = fmaxf(mx, red[sg * 256 + 128 + tid]);
+        }
         float z;
         const float sc = affine_params(mn, mx, kFLevels, z);
         ksz[tid] = sc;
@@ -294,32 +300,68 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
         reinterpret_cast<float*>(rec)[128 + tid] = z;    //         K zero  [128]
       }
       __syncthreads();
-      // the codes, word by word in memory order (word m of a part: lane (m >> 2) & 31,
-      // operand word ((m >> 7) << 2) | (m & 3))
-      for (int t16 = 0; t16 < (G >> 4); ++t16) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes);
-        for (int m = tid; m < 2 * kWPart; m += kSpillThreads) {
-          const int part = m >= kWPart, mm = m - part * kWPart;
-          const int l = (mm >> 2) & 31, w = ((mm >> 7) << 2) | (mm & 3);
+      // the codes: word m of a tile's code matrices (K words, then V words; memory order: lane
+      // (m >> 2) & 31, operand word ((m >> 7) << 2) | (m & 3)) is assembled in registers for
+      // every 16-token tile of the group by the thread(s) that own position m; a Key word's
+      // channels, with their scales and zero-points, are the same in every tile
+      constexpr int W2 = 2 * kWPart;
+      constexpr int kStride = NT >= W2 ? NT / W2 : 1;  // threads per word position (over the tiles)
+      const int ntile = G >> 4;
+      for (int m = NT >= W2 ? tid % W2 : tid; m < W2; m += NT) {
+        const int part = m >= kWPart, mm = m - part * kWPart;
+        const int l = (mm >> 2) & 31, w = ((mm >> 7) << 2) | (mm & 3);
+        // field f of the word: its staged (row, channel) offset, its Value scale index, its Key channel
+        auto field = [&](int f, int& off, int& vj, int& c) {
+          int step, reg, hh;
+          frag_field<BITS>(w, f * BITS, step, reg, hh);
+          const int i = (l >> 2) + 8 * (reg & 1), k = 2 * (l & 3) + hh + 8 * (reg >> 1);
+          if (!part) {  // Keys: rows = tokens, column k holds channel 16 step + 4 ((k & 7) >> 1) + (k & 1) + 2 (k >> 3)
+            c = 16 * step + 4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3);
+            off = i * kSRow + c;
+            vj = 0;
+          } else {      // Values: rows = channels 16 step + i, columns = tokens
+            c = 16 * step + i;
+            off = k * kSRow + c;
+            vj = k * ngv + c / Gv;
+          }
+        };
+        // 4- and 8-bit words (8 and 4 fields): the fields' offsets and Key scales are kept in
+        // registers over the tiles; 2-bit words (16 fields) recompute them (register budget)
+        constexpr bool kKeep = kFields <= 8;
+        int off[kKeep ? kFields : 1], vj[kKeep ? kFields : 1];
+        float ks[kKeep ? kFields : 1], kz[kKeep ? kFields : 1];
+        if constexpr (kKeep) {
+#pragma unroll
+          for (int f = 0; f < kFields; ++f) {
+            int c;
+            field(f, off[f], vj[f], c);
+            ks[f] = part ? 0.f : ksz[c];
+            kz[f] = part ? 0.f : ksz[128 + c];
+          }
+        }
+        for (int t16 = NT >= W2 ? tid / W2 : 0; t16 < ntile; t16 += kStride) {
+          const __nv_bfloat16* rows = (part ? Vs : Ks) + t16 * 16 * kSRow;
+          const float* vs = vsz + t16 * 16 * ngv;
           uint32_t word = 0;
 #pragma unroll
           for (int f = 0; f < kFields; ++f) {
-            int step, reg, hh;
-            frag_field<BITS>(w, f * BITS, step, reg, hh);
-            const int i = (l >> 2) + 8 * (reg & 1), k = 2 * (l & 3) + hh + 8 * (reg >> 1);
-            uint32_t code;
-            if (!part) {  // Keys: rows = tokens, column k holds channel 16 step + 4 ((k & 7) >> 1) + (k & 1) + 2 (k >> 3)
-              const int c = 16 * step + 4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3);
-              const float x = __bfloat162float(Ks[(t16 * 16 + i) * 128 + c]);
-              code = affine_code(x, ksz[c], ksz[128 + c], kLevels);
-            } else {      // Values: rows = channels 16 step + i, columns = tokens
-              const int c = 16 * step + i, tt = t16 * 16 + k, j = c / Gv;
-              const float x = __bfloat162float(Vs[tt * 128 + c]);
-              code = affine_code(x, vsz[tt * ngv + j], vsz[G * ngv + tt * ngv + j], kLevels);
+            int o, j, c = 0;
+            float sk, zk;
+            if constexpr (kKeep) {
+              o = off[f];
+              j = vj[f];
+              sk = ks[f];
+              zk = kz[f];
+            } else {
+              field(f, o, j, c);
+              sk = part ? 0.f : ksz[c];
+              zk = part ? 0.f : ksz[128 + c];
             }
+            const float x = __bfloat162float(rows[o]);
+            const uint32_t code = part ? affine_code(x, vs[j], vs[G * ngv + j], kLevels) : affine_code(x, sk, zk, kLevels);
             word |= code << (f * BITS);
           }
-          dst[m] = word;
+          reinterpret_cast<uint32_t*>(rec + L.hdr_bytes + (long long)t16 * L.tile_bytes)[m] = word;
         }
       }
     }
@@ -330,7 +372,7 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
     __nv_bfloat16* sink_v = reinterpret_cast<__nv_bfloat16*>(p.C.sink_v);
     const long long rfirst = (T0 > L.S + t1s.qn) ? T0 : (long long)L.S + t1s.qn;
     const int n = (int)(T1 - T0);
-    for (int idx = tid; idx < 2 * n * 16; idx += kSpillThreads) {
+    for (int idx = tid; idx < 2 * n * 16; idx += NT) {
       const int which = idx >= n * 16, rem = idx - which * n * 16, j = rem >> 4, ch = rem & 15;
       const long long t = T0 + j;
       const __nv_bfloat16* src = (which ? vnew : knew) + (long long)j * L.d;
@@ -342,9 +384,10 @@ __global__ void __launch_bounds__(kSpillThreads) spill_kernel(const AppendParams
   }
 }
 
-template <int BITS>
-cudaError_t launch_spill_t(const AppendParams& p, int groups, int rest, cudaStream_t stream) {
-  const size_t smem = (size_t)p.L.G * 128 * 2 * 2 + (256 + 512) * 4 + (size_t)p.L.G * p.L.ngv * 8;
+template <int BITS, int NT>
+cudaError_t launch_spill_nt(const AppendParams& p, int groups, int rest, cudaStream_t stream) {
+  const size_t smem =
+      (size_t)p.L.G * kSRow * 2 * 2 + (256 + (NT / 128) * 256) * 4 + (size_t)p.L.G * p.L.ngv * 8;
   static std::mutex mu;
   static int set_for[64] = {};
   int dev = 0;
@@ -353,13 +396,31 @@ cudaError_t launch_spill_t(const AppendParams& p, int groups, int rest, cudaStre
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 64 || set_for[dev] < (int)smem) {
-      e = cudaFuncSetAttribute(spill_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(spill_kernel<BITS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) set_for[dev] = (int)smem;
     }
   }
-  spill_kernel<BITS><<<dim3(p.batch * p.L.H, groups), kSpillThreads, smem, stream>>>(p, rest);
+  spill_kernel<BITS, NT><<<dim3(p.batch * p.L.H, groups), NT, smem, stream>>>(p, rest);
   return cudaGetLastError();
+}
+
+// Threads per spill CTA: few CTAs (one group per sequence and head, few pairs) get
+// 1024 threads each (2-bit codes: 512), many get 256, so that every SM has work and each CTA's serial
+// passes are short.  Measured on GB300: the 70B INT4 layer's spill (128 CTAs of a
+// 128-token group) 41 -> 26 us from 256 to 1024 threads, the INT2 MHA layer's
+// (1024 CTAs of a 32-token group) 37 -> 76 us the other way.
+template <int BITS>
+cudaError_t launch_spill_t(const AppendParams& p, int groups, int rest, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  const long long ctas = (long long)p.batch * p.L.H * groups;
+  if constexpr (BITS != 2) {  // (2-bit words hold 16 codes: the 1024-thread form would spill registers)
+    if (ctas <= 2LL * sms) return launch_spill_nt<BITS, 1024>(p, groups, rest, stream);
+  }
+  if (ctas <= 4LL * sms) return launch_spill_nt<BITS, 512>(p, groups, rest, stream);
+  return launch_spill_nt<BITS, 256>(p, groups, rest, stream);
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
