@@ -281,6 +281,24 @@ class Layer:
         self.kvq.quantize_append(self.cfg, self.struct, self.k_new, self.v_new, self.n_app, self.lens_before,
                                  self.B, self.status, stream)
 
+    # FP8 layers without sink tokens take the step as one call and one launch
+    # (kvq_append_decode_attention: the decode writes the token's codes itself)
+    @property
+    def fused(self):
+        return is_fp8(self.fmt) and self.fmt.S == 0 and self.nq == 1 and self.n_app == 1
+
+    def step_calls(self, stream=None):
+        if self.fused:
+            self.append_decode(stream)
+        else:
+            self.append(stream)
+            self.decode(stream)
+
+    def append_decode(self, stream=None):
+        self.kvq.append_decode_attention(self.cfg, self.struct, self.k_new, self.v_new, self.lens_before, self.B,
+                                         self.q, self.Hq, self.scale, self.out, True, self.lse, self.ws, self.wsb,
+                                         self.status, stream)
+
     def decode(self, stream=None):
         # one launch: split pass with the log-sum-exp merge fused in (last CTA per pair)
         if self.nq == 1:
@@ -293,8 +311,12 @@ class Layer:
 
 
 def count_launches(w):
-    # per layer: append (1 kernel) and decode (1 kernel, merge fused)
-    return 2 * len(w.layer_formats)
+    # per layer: append (1 kernel) and decode (1 kernel, merge fused); FP8 layers without sink
+    # tokens (one token, one query per step): one kernel, the append folded into the decode
+    n = 0
+    for f in w.layer_formats:
+        n += 1 if (is_fp8(f) and f.S == 0 and w.n_query == 1 and max(1, w.append_tokens) == 1) else 2
+    return n
 
 
 def run_gpu(args, w, rank, world):
@@ -329,8 +351,7 @@ def run_gpu(args, w, rank, world):
     # captures each layer's append and decode once into two graphs and replays them.
     for rep in reps:  # first calls outside capture (launch settings, shared-memory limits)
         for lay in rep:
-            lay.append()
-            lay.decode()
+            lay.step_calls()
     torch.cuda.synchronize()
     graphs = None
     if args.graphs:
@@ -338,11 +359,12 @@ def run_gpu(args, w, rank, world):
         for rep in reps:
             gl = []
             for lay in rep:
-                ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-                with torch.cuda.graph(ga, capture_error_mode="relaxed"):
-                    lay.append()
+                ga, gd = (None if lay.fused else torch.cuda.CUDAGraph()), torch.cuda.CUDAGraph()
+                if ga is not None:
+                    with torch.cuda.graph(ga, capture_error_mode="relaxed"):
+                        lay.append()
                 with torch.cuda.graph(gd, capture_error_mode="relaxed"):
-                    lay.decode()
+                    lay.append_decode() if lay.fused else lay.decode()
                 gl.append((ga, gd))
             graphs.append(gl)
         torch.cuda.synchronize()
@@ -351,14 +373,18 @@ def run_gpu(args, w, rank, world):
     def step(i, ev=None):
         rep = reps[i % replicas]
         for j, lay in enumerate(rep):
+            # events around the decode launch (fused layers: the one launch of the step)
             if graphs is not None:
-                graphs[i % replicas][j][0].replay()
-            else:
+                if graphs[i % replicas][j][0] is not None:
+                    graphs[i % replicas][j][0].replay()
+            elif not lay.fused:
                 lay.append()
             if ev is not None:
                 ev[0][j].record(stream)
             if graphs is not None:
                 graphs[i % replicas][j][1].replay()
+            elif lay.fused:
+                lay.append_decode()
             else:
                 lay.decode()
             if ev is not None:
@@ -433,8 +459,7 @@ def run_gpu(args, w, rank, world):
         # the output and lse back to pinned host memory
         for j, lay in enumerate(rep0):
             d_in[j].copy_(h_in[j], non_blocking=True)
-            lay.append()
-            lay.decode()
+            lay.step_calls()
             h_out[j].copy_(d_out[j], non_blocking=True)
 
     for _ in range(min(3, E)):
@@ -738,8 +763,13 @@ def main():
     # roofline of the decode kernel: algorithmic bytes of each layer's launch (codes, scales and
     # zero-points, bf16 sink/residual, q, bf16 out, lse) over that launch's CUDA-event duration
     B = len(r["lens_after"])
+    # a fused layer's launch (FP8, no sink tokens) also reads the step's K, V rows (bf16) and
+    # writes their codes (1 byte each)
+    fused = [is_fp8(f) and f.S == 0 and w.n_query == 1 and max(1, w.append_tokens) == 1 for f in w.layer_formats]
     layer_bytes = np.array([sum(attention_bytes(f, int(T), w.num_kv_heads) for T in r["lens_after"]) +
-                            B * w.n_query * w.num_q_heads * (128 * 2 * 2 + 4) for f in w.layer_formats], float)
+                            B * w.n_query * w.num_q_heads * (128 * 2 * 2 + 4) +
+                            (B * w.num_kv_heads * 128 * (2 * 2 + 2) if fz else 0)
+                            for f, fz in zip(w.layer_formats, fused)], float)
     km = r["kern_ms"]  # [steps][layers] ms
     kern_gbs = layer_bytes.sum() / (km.sum(axis=1).mean() * 1e-3) / 1e9
     by_format = {}
@@ -777,7 +807,7 @@ def main():
         "tokens_per_s": round(len(r["lens_after"]) * world / (r["ms_step"] * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(kern_gbs / hbm_peak, 4), "traffic": traffic,
-                     "kernel": "decode_kernel (fused merge)", "peak_source": peak_src,
+                     "kernel": "decode_kernel (fused merge; FP8 without sinks: the append folded in)", "peak_source": peak_src,
                      "bytes_per_launch": int(layer_bytes.mean()),
                      "mean_launch_us": round(float(km.mean()) * 1e3, 2),
                      "median_launch_us": round(float(np.median(km)) * 1e3, 2),

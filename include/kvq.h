@@ -272,6 +272,33 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
                                 uint32_t* dev_status, void* stream);
 
 /*
+ * kvq_append_decode_attention -- one whole decode step of a layer: the step's
+ * token is appended to every sequence, then attention runs over all tokens
+ * including it.  Source: [KVQA] s5 (quantize the new K, V when they are
+ * written, dequantize right before attention).  The result equals
+ * kvq_quantize_append(..., n_new = 1, seq_lens, ...) followed by
+ * kvq_decode_attention over seq_lens + 1 tokens (same cache contents, same out
+ * and lse bits).  FP8 layers without sink tokens do it in ONE launch: the warp
+ * that reads the new token's tile encodes the token and writes its codes both
+ * into the cache and into the copy it reads (no other CTA reads that tile), so
+ * the step pays no second launch and no launch gap; other layers run the append
+ * launch(es), then the decode launch.
+ *   k_new, v_new  device bf16 [batch][H][d], 16-byte aligned: the step's token
+ *   seq_lens  device int32 [batch]: tokens in the cache BEFORE this step
+ *   q, num_q_heads, softmax_scale, out, out_bf16, lse, workspace  as for
+ *             kvq_decode_attention (workspace: kvq_decode_workspace_size)
+ * Every host-detectable error is returned before anything is enqueued.  The
+ * caller advances seq_lens by 1 afterwards.  Device errors: those of the two
+ * calls it stands for (KVQ_DEV_CAPACITY: the token is not stored and the
+ * sequence's length is clamped to the capacity).
+ */
+kvq_status kvq_append_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cache* cache,
+                                       const void* k_new, const void* v_new, const int32_t* seq_lens, int32_t batch,
+                                       const void* q, int32_t num_q_heads, float softmax_scale, void* out,
+                                       int32_t out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                       uint32_t* dev_status, void* stream);
+
+/*
  * kvq_decode_attention_multi -- attention of n_query new tokens per sequence
  * (speculative-decoding verification, chunked prefill) over the quantized
  * cache in one launch.  Source: [W4KV] "오차가 어디서 만나는가" (the score

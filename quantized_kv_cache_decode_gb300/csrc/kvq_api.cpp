@@ -407,7 +407,8 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
                                 int32_t num_q_heads, const int32_t* seq_lens, int32_t batch, float softmax_scale,
                                 void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t s,
                                 void* out = nullptr, int32_t out_bf16 = 0, float* lse = nullptr,
-                                int32_t n_query = 1, int32_t withhold_copy = 0) {
+                                int32_t n_query = 1, int32_t withhold_copy = 0, const void* k_new = nullptr,
+                                const void* v_new = nullptr, bool check_only = false) {
   LayerDesc L;
   kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
   if (st != KVQ_OK) return st;
@@ -421,6 +422,7 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   DecodeGeom G;
   if ((st = decode_geometry(L, batch, g, &G, n_query > 1)) != KVQ_OK) return st;
   if (workspace_bytes < G.ws_bytes) return KVQ_ERR_WORKSPACE;
+  if (check_only) return KVQ_OK;
   DecodeParams p;
   p.L = L;
   p.C = make_ptrs(cache);
@@ -431,6 +433,12 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.n_query = n_query;
   p.batch = batch;
   p.seq_lens = seq_lens;
+  // a one-token append before the decode (k_new given): the decode sees seq_lens + 1 tokens; FP8
+  // layers without sink tokens write the token's codes inside this launch (fp8_append_token)
+  p.len_add = k_new ? 1 : 0;
+  p.fp8_append = (k_new && L.fp8 && L.S == 0) ? 1 : 0;
+  p.k_new = k_new;
+  p.v_new = v_new;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.num_ctas = G.num_ctas;
   p.nst = G.nst;
@@ -536,6 +544,31 @@ kvq_status kvq_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cac
   // one launch: the last CTA to finish each (sequence, kv head) merges its partials
   return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
                               workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), out, out_bf16, lse);
+}
+
+kvq_status kvq_append_decode_attention(const kvq_layer_config* cfg, const kvq_layer_cache* cache,
+                                       const void* k_new, const void* v_new, const int32_t* seq_lens, int32_t batch,
+                                       const void* q, int32_t num_q_heads, float softmax_scale, void* out,
+                                       int32_t out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                       uint32_t* dev_status, void* stream) {
+  LayerDesc L;
+  kvq_status st = check_decode_args(cfg, num_q_heads, batch, &L);
+  if (st != KVQ_OK) return st;
+  if (out_bf16 != 0 && out_bf16 != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (!out || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every host check of the decode before anything is enqueued
+  if ((st = decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
+                                 workspace_bytes, dev_status, s, out, out_bf16, lse, 1, 0, k_new, v_new, true)) !=
+      KVQ_OK)
+    return st;
+  if (!(L.fp8 && L.S == 0)) {  // the append as its own launch(es) first (see kvq_quantize_append)
+    if ((st = kvq_quantize_append(cfg, cache, k_new, v_new, 1, seq_lens, batch, dev_status, stream)) != KVQ_OK)
+      return st;
+  }
+  return decode_partials_impl(cfg, cache, q, num_q_heads, seq_lens, batch, softmax_scale, workspace,
+                              workspace_bytes, dev_status, s, out, out_bf16, lse, 1, 0, k_new, v_new);
 }
 
 kvq_status kvq_selftest_bounded_wait(const kvq_layer_config* cfg, const kvq_layer_cache* cache, const void* q,

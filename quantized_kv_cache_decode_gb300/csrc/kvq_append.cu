@@ -20,17 +20,6 @@ namespace kvq {
 constexpr int kAppendThreads = 128;
 constexpr unsigned kFull32 = 0xffffffffu;
 
-__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
-  uint16_t v;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(x));
-  return (uint8_t)(v & 0xFFu);
-}
-__device__ __forceinline__ uint8_t f32_to_e5m2(float x) {
-  uint16_t v;
-  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(x));
-  return (uint8_t)(v & 0xFFu);
-}
-
 // s, z of one group from its min and max; returns s (z by reference)
 __device__ __forceinline__ float affine_params(float mn, float mx, float levels, float& z) {
   float s = __fdiv_rn(__fsub_rn(mx, mn), levels);

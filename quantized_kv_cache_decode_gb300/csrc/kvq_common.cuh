@@ -229,6 +229,18 @@ __host__ __device__ __forceinline__ long long working_ctas(long long grid, long 
 // about one second at GB300 clocks
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// FP8 encode of one fp32 value (round to nearest even, saturating to the largest finite code)
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  uint16_t v;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(x));
+  return (uint8_t)(v & 0xFFu);
+}
+__device__ __forceinline__ uint8_t f32_to_e5m2(float x) {
+  uint16_t v;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(x));
+  return (uint8_t)(v & 0xFFu);
+}
+
 __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

@@ -542,6 +542,52 @@ __device__ __forceinline__ void qk_tile_ka(const uint32_t (&KW)[FT<FMT>::kWords]
   d[3] = __shfl_sync(kFull, t8, src + 4);
 }
 
+// One-token append folded into the decode (FP8 layers without sink tokens): the
+// new token of (sequence b, kv head h) is token tt of quantized tile i, which one
+// warp of the launch reads, from its staged copy `stile`.  That warp encodes the
+// token as the append does (code = FP8(fl32(x / s)) with the tensor's scale s, at
+// the token's positions in the fragment-order K and V parts) and writes the codes
+// into the cache record, for later steps, and into the staged copy it is about to
+// read.  A token that starts a tile clears both copies of the tile first, so the
+// codes of tokens not yet written read as 0.  (Lane l encodes channels 4l .. 4l + 3.)
+__device__ __forceinline__ void fp8_append_token(const DecodeParams& p, uint8_t* stile, int b, int h, long long i,
+                                                 int tt, int lane) {
+  const LayerDesc& L = p.L;
+  const uint8_t* rec = record_addr(L, p.C, b, h, i / L.tpg, nullptr);
+  if (!rec) return;  // a bad block: its tile was not copied either (reported by the producer)
+  uint8_t* gtile = const_cast<uint8_t*>(tile_in_record(L, rec, i));
+  constexpr int kCodeBytes = 2 * 16 * 128;  // K and V codes of a 16-token FP8 tile
+  if (tt == 0) {
+#pragma unroll
+    for (int w = lane; w < kCodeBytes / 16; w += 32) {
+      reinterpret_cast<uint4*>(stile)[w] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(gtile)[w] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+  }
+  const long long pair = (long long)b * L.H + h;
+  const uint2 kr = reinterpret_cast<const uint2*>(p.k_new)[pair * 32 + lane];
+  const uint2 vr = reinterpret_cast<const uint2*>(p.v_new)[pair * 32 + lane];
+  const float sk = __ldg(p.C.k_tscale), sv = __ldg(p.C.v_tscale);
+  const float2 k01 = unpack_bf16(kr.x), k23 = unpack_bf16(kr.y), v01 = unpack_bf16(vr.x), v23 = unpack_bf16(vr.y);
+  const float kx[4] = {k01.x, k01.y, k23.x, k23.y}, vx[4] = {v01.x, v01.y, v23.x, v23.y};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int c = 4 * lane + e;
+    const float kd = __fdiv_rn(kx[e], sk), vd = __fdiv_rn(vx[e], sv);
+    const uint8_t kc = L.e5m2 ? f32_to_e5m2(kd) : f32_to_e4m3(kd);
+    const uint8_t vc = L.e5m2 ? f32_to_e5m2(vd) : f32_to_e4m3(vd);
+    int byte, bit;
+    ktile_pos(8, true, tt, c, byte, bit);
+    stile[byte] = kc;
+    gtile[byte] = kc;
+    vtile_pos(8, true, tt, c, byte, bit);
+    stile[16 * 128 + byte] = vc;
+    gtile[16 * 128 + byte] = vc;
+  }
+  __syncwarp();
+}
+
 // Scores of a bf16 tile from its K rows in shared memory (rows past `rows` masked):
 // the query column (bf16, exact) in A rows 0-7, rows 8-15 zero; the K rows as the B
 // operand through ldmatrix (natural channel order).
@@ -949,7 +995,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   // ---- per-sequence work units and their prefix (units of all H heads) ----
   const long long tmax_tok = max_tokens(L);
   auto seq_tokens = [&](int b) -> int {
-    long long T = p.seq_lens[b];
+    long long T = (long long)p.seq_lens[b] + p.len_add;
     if (T < 0) T = 0;
     if (T > tmax_tok) T = tmax_tok;
     return (int)T;
@@ -981,7 +1027,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
     if (tid == NT - 1) prefix[B] = wbase + incl;
     if (blockIdx.x == 0) {
       for (int b = tid; b < B; b += NT)
-        if (p.seq_lens[b] > tmax_tok) report(p.status, KVQ_DEV_CAPACITY);
+        if ((long long)p.seq_lens[b] + p.len_add > tmax_tok) report(p.status, KVQ_DEV_CAPACITY);
     }
     __syncthreads();
     if (blockIdx.x == 0)
@@ -1569,6 +1615,12 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               walk += L.tile_bytes;
               if (++rpos == L.tpg) rpos = 0;
               if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
+              if constexpr (F::kFp8) {
+                // the step's token (one-token append folded into this launch) lies in the last tile
+                if (p.fp8_append && tg.a + k == ((sg.qn - 1) >> 4) &&
+                    (long long)p.seq_lens[sg.b] + 1 <= tmax_tok)
+                  fp8_append_token(p, const_cast<uint8_t*>(tile), sg.b, sg.h, tg.a + k, (sg.qn - 1) & 15, lane);
+              }
               tile_step(tg.a + k, tile, stg + hoff, hdr);
             }
           }

@@ -65,6 +65,12 @@ struct DecodeParams {
   int gh;            // query heads per kv head
   int n_query;       // query tokens per sequence (1: plain decode)
   const int32_t* seq_lens;
+  int len_add;       // tokens added to each seq_lens[b] (1: the call appended the step's token first)
+  // FP8 layers without sink tokens, one-token append folded into the decode: the warp that
+  // reads the new token's tile writes the token's codes (from k_new, v_new: bf16 [B][H][d])
+  int fp8_append;
+  const void* k_new;
+  const void* v_new;
   float scale_log2;  // softmax_scale * log2(e)
   int num_ctas;      // CTAs of the decode grid (partial slot space = num_ctas + batch*H)
   int nst;           // pipeline stages per warp

@@ -62,6 +62,8 @@ _lib.kvq_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i
                                       c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
 _lib.kvq_decode_attention_multi.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_i32, c_vp, c_i32,
                                             ctypes.c_float, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
+_lib.kvq_append_decode_attention.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_vp, c_vp, c_i32, c_vp,
+                                             c_i32, ctypes.c_float, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
 _lib.kvq_decode_workspace_size_multi.argtypes = [_P(LayerConfig), c_i32, c_i32, c_i32, _P(c_sz)]
 _lib.kvq_selftest_bounded_wait.argtypes = [_P(LayerConfig), _P(LayerCache), c_vp, c_i32, c_vp, c_i32, ctypes.c_float,
                                            c_vp, c_i32, c_vp, c_vp, c_sz, c_vp, c_vp]
@@ -79,7 +81,7 @@ for _fn in ("kvq_cache_layout", "kvq_fp8_calibrate", "kvq_fp8_calibrate_format",
             "kvq_decode_attention", "kvq_decode_partials", "kvq_decode_combine", "kvq_dequantize",
             "kvq_decode_attention_multi", "kvq_decode_workspace_size_multi", "kvq_lse_merge",
             "kvq_selftest_bounded_wait",
-            "kvq_decode_attention_static_scratch"):
+            "kvq_decode_attention_static_scratch", "kvq_append_decode_attention"):
     getattr(_lib, _fn).restype = c_i32
 
 
@@ -165,6 +167,17 @@ def decode_attention(cfg: LayerConfig, cache: LayerCache, q, num_q_heads: int, s
            _lib.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), num_q_heads, _ptr(seq_lens),
                                      batch, softmax_scale, _ptr(out), int(out_bf16), _ptr(lse), _ptr(workspace),
                                      workspace_bytes, _ptr(dev_status), _stream_ptr(stream)))
+
+
+def append_decode_attention(cfg: LayerConfig, cache: LayerCache, k_new, v_new, seq_lens, batch: int, q,
+                            num_q_heads: int, softmax_scale: float, out, out_bf16: bool, lse, workspace,
+                            workspace_bytes: int, dev_status=None, stream=None) -> None:
+    """One whole decode step: append one token per sequence (seq_lens: lengths before it), then attention."""
+    _check("kvq_append_decode_attention",
+           _lib.kvq_append_decode_attention(ctypes.byref(cfg), ctypes.byref(cache), _ptr(k_new), _ptr(v_new),
+                                            _ptr(seq_lens), batch, _ptr(q), num_q_heads, softmax_scale, _ptr(out),
+                                            int(out_bf16), _ptr(lse), _ptr(workspace), workspace_bytes,
+                                            _ptr(dev_status), _stream_ptr(stream)))
 
 
 def decode_workspace_size_multi(cfg: LayerConfig, batch: int, n_query: int, num_q_heads: int) -> int:

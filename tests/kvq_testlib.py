@@ -171,6 +171,23 @@ class GpuLayer:
         torch.cuda.synchronize()
         return out, lse
 
+    def append_decode(self, k_bits: np.ndarray, v_bits: np.ndarray, q_bits: np.ndarray, lens_before,
+                      out_bf16: bool = False):
+        """One whole step (kvq_append_decode_attention): k_bits, v_bits [B, H, d] the step's token."""
+        torch = self.torch
+        B, Hq, _ = q_bits.shape
+        qd = torch.from_numpy(q_bits.astype(np.int16)).to(self.device)
+        kd = torch.from_numpy(np.ascontiguousarray(k_bits).astype(np.int16)).to(self.device)
+        vd = torch.from_numpy(np.ascontiguousarray(v_bits).astype(np.int16)).to(self.device)
+        out = torch.zeros((B, Hq, 128), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=self.device)
+        lse = torch.zeros((B, Hq), dtype=torch.float32, device=self.device)
+        wsb = self.kvq.decode_workspace_size(self.cfg, B, Hq)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        self.kvq.append_decode_attention(self.cfg, self.layer.struct(), kd, vd, self.seq_lens_dev(lens_before), B, qd,
+                                         Hq, 1.0 / math.sqrt(128), out, out_bf16, lse, ws, wsb, self.status)
+        torch.cuda.synchronize()
+        return out, lse
+
     def decode_multi(self, q_bits: np.ndarray, out_bf16: bool = False, scale=None):
         """q_bits [B, M, Hq, d]: the last M cached tokens' queries, attending causally."""
         torch = self.torch

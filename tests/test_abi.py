@@ -197,6 +197,21 @@ def test_append_rejects_unaligned_inputs_before_any_launch(kvq):
         assert e.value.status == -1
 
 
+def test_append_decode_host_errors_come_first(kvq):
+    # kvq_append_decode_attention checks everything the host can before its first launch
+    # (fake aligned pointers, never dereferenced)
+    cfg = kvq.make_config("fp8_e4m3", 2, 1, 128, 0, 0, capacity_tokens=64)
+    cache = kvq.LayerCache()
+    cases = [dict(out_bf16=2), dict(k_new=4096 + 2), dict(v_new=0), dict(out=0)]
+    for bad in cases:
+        a = dict(k_new=4096, v_new=8192, out=12288, out_bf16=0)
+        a.update(bad)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.append_decode_attention(cfg, cache, a["k_new"], a["v_new"], 16, 1, 32, 8, 0.1, a["out"],
+                                        a["out_bf16"], 0, 0, 0, stream=0)
+        assert e.value.status == -1, bad
+
+
 def test_pre_rope_keys_reject_several_query_tokens(kvq):
     # the multi-query decode does not rotate Keys: refused before anything is enqueued
     cfg = kvq.make_config("int4", 2, 32, 128, 32, 0, capacity_tokens=64, rope_base=10000.0)

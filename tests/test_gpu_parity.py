@@ -415,3 +415,58 @@ def test_dense_and_sparse_parity(case):
     out16, lse16 = gl.decode(q, out_bf16=True)
     assert torch.equal(out16, out.to(torch.bfloat16)) and torch.equal(lse16, lse)
     assert gl.status_value() == 0
+
+
+APPEND_DECODE = [
+    # fmt, H, g, lens after the step, G, Gv, R, S, paged, block
+    # FP8 without sink tokens: the append folded into the decode launch; tokens that start a
+    # tile (T = 1, 17, 33) and tokens inside one
+    ("fp8_e4m3", 2, 4, [1, 16, 17, 20, 33, 300], 1, 128, 0, 0, False, 16),
+    ("fp8_e5m2", 2, 4, [1, 17, 48, 129], 1, 128, 0, 0, True, 16),
+    ("fp8_e4m3", 1, 8, [33, 400], 1, 128, 0, 0, True, 32),
+    ("fp8_e4m3", 8, 4, [16 + 37 * i for i in range(16)], 1, 128, 0, 0, False, 16),
+    ("fp8_e4m3", 1, 4, [20001], 1, 128, 0, 0, False, 16),
+    # the other layers: the append launch(es), then the decode
+    ("fp8_e4m3", 2, 4, [1, 2, 300], 1, 128, 0, 1, False, 16),
+    ("int4", 2, 4, [1, 64, 65, 96, 700], 32, 128, 32, 0, False, 16),
+    ("int2", 3, 1, [161, 5], 32, 32, 128, 0, False, 16),
+    ("int8", 2, 6, [81, 2, 144], 16, 128, 64, 1, True, 16),
+    ("bf16", 2, 4, [1, 333], 0, 0, 0, 1, False, 16),
+]
+
+
+@pytest.mark.parametrize("case", APPEND_DECODE, ids=[f"{c[0]}-H{c[1]}g{c[2]}-S{c[7]}{'-paged' if c[8] else ''}-"
+                                                    f"{len(c[3])}seq" for c in APPEND_DECODE])
+def test_append_decode_step(case):
+    """kvq_append_decode_attention: the cache holds T - 1 tokens, the call appends token T - 1 and
+    attends over all T.  The stored cache equals the oracle's over all T tokens (bit-exact), the
+    attention equals the oracle's, and a plain decode over the result gives the same bits."""
+    fmt, H, g, lens, G, Gv, R, S, paged, blk = case
+    seed = zlib.crc32(repr(case).encode()) % 10000
+    gl = TL.GpuLayer(fmt, H, lens, G, Gv, R, S, paged=paged, block_tokens=blk, seed=seed)
+    kv, q = make_inputs(seed, H, g, lens)
+    ks = vs = None
+    if gl.fp8:  # the per-tensor scales from every token of the layer, the step's included
+        kall = np.concatenate([kv[k][0].reshape(-1) for k in kv])
+        vall = np.concatenate([kv[k][1].reshape(-1) for k in kv])
+        gl.calibrate_fp8(kall, vall)
+        ks = O.fp8_tensor_scale(O.bf16_to_f32(kall), fmt)
+        vs = O.fp8_tensor_scale(O.bf16_to_f32(vall), fmt)
+    for b, T in enumerate(lens):
+        if T > 1:
+            gl.append(b, np.stack([kv[b, h][0][:T - 1] for h in range(H)]),
+                      np.stack([kv[b, h][1][:T - 1] for h in range(H)]), 0)
+    torch.cuda.synchronize()
+    knew = np.stack([np.stack([kv[b, h][0][T - 1] for h in range(H)]) for b, T in enumerate(lens)])
+    vnew = np.stack([np.stack([kv[b, h][1][T - 1] for h in range(H)]) for b, T in enumerate(lens)])
+    out, lse = gl.append_decode(knew, vnew, q, [T - 1 for T in lens])
+    assert gl.status_value() == 0
+    caches = [[O.build_head_cache(O.bf16_to_f32(kv[b, h][0]), O.bf16_to_f32(kv[b, h][1]), gl.spec, ks, vs)
+               for h in range(H)] for b in range(len(lens))]
+    for b, T in enumerate(lens):
+        for h in range(H):
+            TL.compare_logical(gl.logical(b, h, T), caches[b][h])
+    out_ref, lse_ref = O.decode_attention(O.bf16_to_f32(q), caches)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+    out2, lse2 = gl.decode(q)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
