@@ -390,13 +390,14 @@ def run_gpu(args, w, rank, world):
             if ev is not None:
                 ev[1][j].record(stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
+    # the clock sampler starts first; the warm-up steps then run right before the timed ones, so
+    # the GPU is not left idle (and its clocks low) between them
     clk = ClockSampler(dev.index if dev.index is not None else 0, os.path.join(OUT_DIR, f"clocks_rank{rank}.csv")) \
         if rank == 0 else None
     time.sleep(0.15 if clk else 0)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
     # ---- timed region: exactly K steps; per-launch events around the decode split pass ----
     K = args.steps
     nl = len(w.layer_formats)

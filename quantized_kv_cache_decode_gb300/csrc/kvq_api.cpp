@@ -13,7 +13,7 @@
 namespace kvq {
 namespace {
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 2;
 constexpr int kStaticSmemMargin = 1024;           // the kernel's static __shared__ variables (384 B)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -257,7 +257,7 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, 
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  const int n = 2;
+  const int n = kMaxStages;  // stages per warp (the kernel sizes its barriers and tags for kMaxStages)
   const int budget = 227 * 1024 - kStaticSmemMargin;
   int smem = 0, nst = 0, sb = 0, tps = 0;
   bool found = false;

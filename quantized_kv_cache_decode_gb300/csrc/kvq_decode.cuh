@@ -57,7 +57,7 @@ struct DecodeWarps {
   static constexpr int kNW = 12;
   static constexpr int kThreads = kNW * 32;
 };
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 2;
 constexpr float kPrescale = 64.f;      // w = p * (s / S_ref) * 64 < 2^14: f16 range is safe
 constexpr float kTau = 6.f;            // score max may exceed its reference by 2^6 before a rescale
 constexpr float kSTau = 4.f;           // a Value scale may exceed its reference 4x before a rescale
@@ -1405,9 +1405,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
       // the lane's four tokens of a tile (score and W layout)
       const int tk[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
       // several query tokens per sequence: column r (query token r / gh) sees the tokens
-      // t <= T - n_query + r / gh (causal: where that query token sits); the limit is
-      // recomputed where it is needed, so one-query decode keeps no registers for it
-      auto col_limit = [&]() { return toks[sg.b] - p.n_query + r / p.gh; };
+      // t <= T - n_query + r / gh (causal: where that query token sits); computed once per
+      // segment, only in the multi-query variant
+      const int mq_lim = MQ ? toks[sg.b] - p.n_query + r / p.gh : 0;
+      auto col_limit = [&]() { return mq_lim; };
 
       // this warp's stages of segment s, in the order its producer issued them
       while (true) {
