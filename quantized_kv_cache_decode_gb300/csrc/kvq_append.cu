@@ -44,6 +44,8 @@ __device__ __forceinline__ uint8_t* record_w(const LayerDesc& L, const CachePtrs
 // the residual window (integer layers: only the tokens that stay there after the
 // groups that spill, which spill_kernel quantizes) and sink rows.
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
+  pdl_wait();  // the previous kernel of the stream has finished (programmatic launch)
+  pdl_trigger();
   const LayerDesc& L = p.L;
   const int b = blockIdx.x / L.H, h = blockIdx.x % L.H;
   const int tid = threadIdx.x;
@@ -149,6 +151,8 @@ __device__ __forceinline__ void frag_field(int w, int bp, int& step, int& reg, i
 
 template <int BITS, int NT>
 __global__ void __launch_bounds__(NT, 1024 / NT) spill_kernel(const AppendParams p, int rest) {
+  pdl_wait();  // the previous kernel of the stream has finished (programmatic launch)
+  pdl_trigger();
   constexpr int kKSegs = NT / 128;  // runs of tokens per Key channel in the min/max pass (G >= 16 >= 2 kKSegs)
   extern __shared__ __align__(16) uint8_t smem[];
   const LayerDesc& L = p.L;
@@ -390,8 +394,7 @@ cudaError_t launch_spill_nt(const AppendParams& p, int groups, int rest, cudaStr
       if (dev >= 0 && dev < 64) set_for[dev] = (int)smem;
     }
   }
-  spill_kernel<BITS, NT><<<dim3(p.batch * p.L.H, groups), NT, smem, stream>>>(p, rest);
-  return cudaGetLastError();
+  return launch_pdl(spill_kernel<BITS, NT>, dim3(p.batch * p.L.H, groups), dim3(NT), smem, stream, p, rest);
 }
 
 // Threads per spill CTA: few CTAs (one group per sequence and head, few pairs) get
@@ -416,8 +419,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int blocks = p.batch * p.L.H;
   if (blocks == 0 || p.n_new == 0) return cudaSuccess;
   if (p.L.fp8 || p.L.bf16) {
-    append_kernel<<<blocks, kAppendThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, dim3(blocks), dim3(kAppendThreads), 0, stream, p);
   }
   // integer layers: at most ceil(n_new / G) groups spill per (sequence, head)
   const int groups = (int)(((long long)p.n_new + p.L.G - 1) / p.L.G);
@@ -429,8 +431,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
     default: e = launch_spill_t<8>(p, groups, fused, stream); break;
   }
   if (e != cudaSuccess || fused) return e;
-  append_kernel<<<blocks, kAppendThreads, 0, stream>>>(p);  // window and sink rows after the spills
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(blocks), dim3(kAppendThreads), 0, stream, p);  // window and sink rows after the spills
 }
 
 // ---------------------------------------------------------------------------

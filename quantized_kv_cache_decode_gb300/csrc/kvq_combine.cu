@@ -10,6 +10,8 @@
 namespace kvq {
 
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  pdl_wait();  // the previous kernel of the stream has finished (programmatic launch)
+  pdl_trigger();
   const int bq = blockIdx.x;
   const int b = bq / p.Hq, hq = bq % p.Hq;
   const int h = hq / p.g, r = hq % p.g;
@@ -87,8 +89,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   if (p.batch * p.Hq == 0) return cudaSuccess;
-  combine_kernel<<<p.batch * p.Hq, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(p.batch * p.Hq), dim3(128), 0, stream, p);
 }
 
 }  // namespace kvq

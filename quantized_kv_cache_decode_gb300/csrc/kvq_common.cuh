@@ -3,6 +3,7 @@
 // f16/bf16 conversions, and the layout arithmetic of the cache.
 #pragma once
 
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -228,6 +229,34 @@ __host__ __device__ __forceinline__ long long working_ctas(long long grid, long 
 
 // about one second at GB300 clocks
 constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// Programmatic dependent launch.  The kernels of a decode step (append, decode,
+// combine) are launched with programmatic stream serialisation allowed: a kernel
+// may be scheduled onto free SMs while the previous kernel of the stream is still
+// finishing.  Each of them first waits (pdl_wait) until the previous kernel has
+// completed and its memory writes are visible -- before touching any global
+// memory -- and then lets the next kernel of the stream be scheduled
+// (pdl_trigger).  The overlap hides the launch and CTA scheduling of a kernel
+// behind the tail of the one before it; the order of memory effects is the plain
+// stream order.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...);
+}
 
 // FP8 encode of one fp32 value (round to nearest even, saturating to the largest finite code)
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {

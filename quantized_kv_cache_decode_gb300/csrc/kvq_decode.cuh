@@ -941,6 +941,8 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // query-rows form.
 template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE, bool OUT, bool KA>
 __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(const DecodeParams p) {
+  pdl_wait();  // the previous kernel of the stream has finished (programmatic launch)
+  pdl_trigger();
   using F = FT<FMT>;
   static_assert(!KA || (!MQ && !ROPE && !OUT), "the Key-as-A form serves one query token, plain Keys");
   constexpr int NW = DecodeWarps<FMT>::kNW;
@@ -1912,8 +1914,8 @@ template <int FMT, int NGV, bool BF, bool MQ, bool ONE, bool ROPE = false, bool 
 cudaError_t launch_variant(const DecodeParams& p, int smem, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr<FMT, NGV, BF, MQ, ONE, ROPE, OUT, KA>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT, KA><<<p.num_ctas, DecodeWarps<FMT>::kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<FMT, NGV, BF, MQ, ONE, ROPE, OUT, KA>, dim3(p.num_ctas),
+                    dim3(DecodeWarps<FMT>::kThreads), (size_t)smem, stream, p);
 }
 
 // FP8 layers without sink tokens (no bf16 tiles) take the variant without the bf16
