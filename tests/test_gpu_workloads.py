@@ -2,7 +2,8 @@
 
 Each layer is built and stepped exactly as the benchmark does (bench.Layer:
 cache of T-1 tokens, one decode step = append of the new token + split pass +
-combine).  The oracle then rebuilds sampled (sequence, kv head) pairs from the
+combine; FP8 layers without sink tokens take the step as one
+kvq_append_decode_attention launch).  The oracle then rebuilds sampled (sequence, kv head) pairs from the
 same seeded inputs and checks, for those pairs:
   * the dequantized export (codes, scales, zero-points, bf16 parts): bit-exact;
   * attention outputs of all query heads of the pair: fp32 within
@@ -34,7 +35,21 @@ DEV = torch.device("cuda", 0)
 
 def _spec(fmt):
     fp8 = bench.is_fp8(fmt)
-    return O.Spec(fmt.fmt, d=128, G=1 if fp8 else fmt.G, Gv=fmt.Gv, R=0 if fp8 else fmt.R, S=fmt.S)
+    return O.Spec(fmt.fmt, d=128, G=1 if fp8 else fmt.G, Gv=fmt.Gv, R=0 if fp8 else fmt.R, S=fmt.S,
+                  rope_base=fmt.rope_base, k_outliers=fmt.k_outliers, v_outliers=fmt.v_outliers)
+
+
+def _pairs(w, n, seed):
+    # n seeded (sequence, kv head) pairs, always with the first and the last pair, and for ragged
+    # batches the shortest and the longest sequence
+    rng = np.random.default_rng(seed)
+    pairs = {(0, 0), (w.batch - 1, w.num_kv_heads - 1)}
+    if w.seq_len_range is not None:
+        lens = I.seq_lens(w)
+        pairs |= {(int(np.argmin(lens)), 1 % w.num_kv_heads), (int(np.argmax(lens)), 2 % w.num_kv_heads)}
+    while len(pairs) < n:
+        pairs.add((int(rng.integers(w.batch)), int(rng.integers(w.num_kv_heads))))
+    return sorted(pairs)
 
 
 def _check_layer(w, l, pairs, seed_offset=0):
@@ -44,9 +59,9 @@ def _check_layer(w, l, pairs, seed_offset=0):
     lens_after = I.seq_lens(w) + w.append_tokens if w.seq_len_range is not None else np.full(w.batch, w.seq_len)
     lens_before = [int(t) - n_app for t in lens_after]
     lay = bench.Layer(kvq, torch, w, l, fmt, lens_before, n_app, DEV, seed_offset=seed_offset)
-    # one benchmark step
-    lay.append()
-    lay.decode()
+    # one benchmark step (the calls the bench makes: FP8 layers without sink tokens in one
+    # kvq_append_decode_attention launch, the others append then decode)
+    lay.step_calls()
     torch.cuda.synchronize()
     assert lay.status.item() == 0
     out16 = lay.out.clone()
@@ -98,7 +113,7 @@ def _check_layer(w, l, pairs, seed_offset=0):
         kr, vr = O.dequantized_f32(hc)
         assert np.array_equal(ko[0, h].cpu().numpy().view(np.uint32), kr.view(np.uint32)), (b, h)
         assert np.array_equal(vo[0, h].cpu().numpy().view(np.uint32), vr.view(np.uint32)), (b, h)
-        kh, vh = O.dequantized_f64(hc)
+        kh, vh = O.attention_keys(hc)  # (pre-RoPE layers: Keys rotated at their positions)
         for m in range(M):
             n = T - M + m + 1  # query token m attends to its causal prefix
             for j in range(w.gqa):
@@ -121,42 +136,49 @@ def test_tiny_kivi_int4_all_pairs():
 
 def test_llama3_8b_fp8_sampled():
     w = I.llama3_8b_fp8()
-    _check_layer(w, 0, [(0, 0), (7, 3), (15, 7)])
+    _check_layer(w, 0, _pairs(w, 8, 1))
 
 
 def test_llama3_8b_fp8_e5m2_sampled():
     w = I.llama3_8b_fp8_e5m2()
-    _check_layer(w, 0, [(0, 0), (8, 2), (15, 7)])
+    _check_layer(w, 0, _pairs(w, 6, 2))
 
 
 def test_llama3_8b_fp8_two_query_tokens_sampled():
     w = I.llama3_8b_fp8_2q()
-    _check_layer(w, 0, [(0, 0), (5, 1), (15, 7)])
+    _check_layer(w, 0, _pairs(w, 6, 3))
 
 
 def test_llama3_8b_bf16_skip_layer_sampled():
     w = I.llama3_8b_bf16_skip()
-    _check_layer(w, 0, [(0, 0), (11, 6), (15, 7)])
+    _check_layer(w, 0, _pairs(w, 6, 4))
+
+
+def test_llama3_8b_int4_pre_rope_sampled():
+    w = I.llama3_8b_int4_prerope()
+    _check_layer(w, 0, _pairs(w, 6, 5))
+
+
+def test_llama3_8b_int4_dense_and_sparse_sampled():
+    w = I.llama3_8b_int4_sparse()
+    _check_layer(w, 0, _pairs(w, 6, 6))
 
 
 @pytest.mark.parametrize("layer", [0, 79])
 def test_llama3_70b_int4_sampled(layer):
     w = I.llama3_70b_int4()
-    _check_layer(w, layer, [(0, 0), (9, 5), (15, 7)])
+    _check_layer(w, layer, _pairs(w, 8, 7 + layer))
 
 
 def test_llama2_7b_int2_append_spill_sampled():
     w = I.llama2_7b_int2()
-    _check_layer(w, 0, [(0, 0), (17, 30), (31, 31)])
+    _check_layer(w, 0, _pairs(w, 10, 9))
 
 
 @pytest.mark.parametrize("layer", [0, 31, 63])
 def test_paged_mixed_sampled(layer):
     w = I.paged_mixed()
-    lens = I.seq_lens(w)
-    order = np.argsort(lens)
-    seqs = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
-    _check_layer(w, layer, [(seqs[0], 0), (seqs[1], 4), (seqs[2], 7)])
+    _check_layer(w, layer, _pairs(w, 12, 10 + layer))
 
 
 def test_max_batch_many_short_sequences():
