@@ -608,10 +608,21 @@ def cpu_model():
     try:
         with open("/proc/cpuinfo") as f:
             txt = f.read()
-        for key in ("model name", "Model", "CPU part"):
+        for key in ("model name", "Model"):
             for line in txt.splitlines():
                 if line.split(":")[0].strip() == key:
                     return f"{key}: {line.split(':', 1)[1].strip()}"
+        # Arm cores name themselves only by implementer and part number (MIDR fields)
+        fields = {}
+        for line in txt.splitlines():
+            k, _, v = line.partition(":")
+            fields.setdefault(k.strip(), v.strip())
+        arm_parts = {"0xd40": "Arm Neoverse V1", "0xd49": "Arm Neoverse N2", "0xd4f": "Arm Neoverse V2 (as in NVIDIA Grace)",
+                     "0xd0c": "Arm Neoverse N1", "0xd8e": "Arm Neoverse N3", "0xd84": "Arm Neoverse V3"}
+        part = fields.get("CPU part")
+        if part:
+            name = arm_parts.get(part.lower()) if fields.get("CPU implementer", "").lower() == "0x41" else None
+            return f"{name} (CPU part {part})" if name else f"CPU part: {part}"
     except OSError:
         pass
     import platform
