@@ -286,7 +286,8 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, 
   const size_t l_bytes = slots * g * sizeof(float);
   G->off_lse = (o_bytes + 255) / 256 * 256;
   G->off_prefix = G->off_lse + (l_bytes + 255) / 256 * 256;
-  G->off_counters = G->off_prefix + ((size_t)(batch + 1) * sizeof(int) + 255) / 256 * 256;
+  // unit prefix [batch + 1] and the split pass's CTA count
+  G->off_counters = G->off_prefix + ((size_t)(batch + 2) * sizeof(int) + 255) / 256 * 256;
   G->ws_bytes = G->off_counters + (size_t)batch * L.H * sizeof(unsigned);
   return KVQ_OK;
 }
@@ -446,8 +447,12 @@ kvq_status decode_partials_impl(const kvq_layer_config* cfg, const kvq_layer_cac
   p.tps = G.tps;
   // a claimed work item: whole records, at least a stage's worth of tiles
   p.item_tiles = (std::max(G.tps, L.tpg) + L.tpg - 1) / L.tpg * L.tpg;
-  // one tile per Key group: items of two stages (half the claims; a CTA still has hundreds of items)
-  if (!L.fp8 && !L.bf16 && L.tpg == 1) p.item_tiles = 2 * G.tps;
+  // integer layers whose stages hold more than a record (their stage sizes budget a header for
+  // every record a stage touches, see stage_bytes_of): items of at least two stages, whole records
+  // (half the claims; measured on GB300: INT2 MHA layer 1555 -> 1498 us).  A stage no longer than a
+  // record must not cross one, so there items stay single records.
+  if (!L.fp8 && !L.bf16 && (L.tpg == 1 || G.tps > L.tpg))
+    p.item_tiles = (std::max(2 * G.tps, L.tpg) + L.tpg - 1) / L.tpg * L.tpg;
   // a 16-token bf16 tile reads 8 KB; charge it in units of a quantized tile's bytes
   p.bf_weight = std::max(1, (8192 + L.tile_bytes / 2) / L.tile_bytes);
   p.bf_joint = bf16_joint(G.stage_bytes) ? 1 : 0;

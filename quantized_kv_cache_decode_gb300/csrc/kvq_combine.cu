@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     if (p.lse && c == 0) p.lse[(long long)b * p.Hq + hq] = -INFINITY;
     return;
   }
-  const long long C = working_ctas(p.num_ctas, U);
+  const long long C = p.ws_prefix[p.batch + 1];  // the split pass's choice (range_ctas)
   const long long P0 = p.ws_prefix[b] + (long long)h * units;
   const long long P1 = P0 + units;
   const long long c_lo = ((P0 + 1) * C - 1) / U;

@@ -1037,7 +1037,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   }
 
   const long long U = prefix[B];
-  const long long C = working_ctas(p.num_ctas, U);
+  bool same_len = true;  // every sequence holds the same number of units
+  for (int b = tid; b < B; b += NT) same_len &= (prefix[b + 1] - prefix[b]) == (prefix[1] - prefix[0]);
+  const long long C = range_ctas(p.num_ctas, U, (long long)B * H, __syncthreads_and(same_len) != 0);
+  if (blockIdx.x == 0 && tid == 0) p.ws_prefix[B + 1] = (int)C;  // for the two-launch merge
   if (p.fuse) {
     // sequences without tokens belong to no CTA's range: out = 0, lse = -inf
     for (int b = blockIdx.x; b < B; b += gridDim.x)

@@ -81,7 +81,7 @@ struct DecodeParams {
   int bf_joint;      // 1: a bf16 tile's K and V rows (2 x 4 KB) share one stage; 0: one stage each
   float* ws_o;       // [slots][g][d] normalised partial outputs
   float* ws_lse;     // [slots][g] log2-domain log-sum-exp of each partial
-  int* ws_prefix;    // [batch + 1] per-sequence unit prefix (written by CTA 0 for the combine)
+  int* ws_prefix;    // [batch + 2]: per-sequence unit prefix, then the CTA count (written by CTA 0 for the combine)
   uint32_t* status;
   int merge_bytes;   // bytes of one warp's merge record in shared memory (g heads)
   int withhold_copy; // self-test only: CTA 0, warp 0 withholds its first bulk copy (its wait must run out)
