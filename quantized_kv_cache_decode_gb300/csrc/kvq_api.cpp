@@ -174,13 +174,12 @@ int merge_bytes_of(const LayerDesc& L, int g) {
 }
 
 constexpr int kSegTableBytes = 16 * 80;  // kMaxSeg segment records of 80 bytes (kvq_decode.cuh)
-constexpr int kSlotTagBytes = 20;        // one pipeline slot's tag (kvq_decode.cuh)
 
 int fixed_smem(int batch, int merge_bytes, int nw) {
   int prefix = ((batch + 1) * 4 + 15) / 16 * 16 + (batch * 4 + 15) / 16 * 16;  // unit prefix, token counts
-  // per warp: barriers, block-table window, slot tags; nw/2 merge records; the query rows (g + 1)
+  // per warp: barriers, block-table window; nw/2 merge records; the query rows (g + 1)
   const int g = merge_bytes / (kMergeFloats * 4);
-  const int per_warp = kMaxStages * 8 + 32 * 4 + (kMaxStages * kSlotTagBytes + 15) / 16 * 16;
+  const int per_warp = kMaxStages * 8 + 32 * 4;
   return nw * per_warp + nw / 2 * merge_bytes + (g + 1) * kQRowFloats * 4 + kSegTableBytes + prefix;
 }
 

@@ -924,7 +924,6 @@ struct SlotTag {
   short kind, n;
   int first;
 };
-static_assert(sizeof(SlotTag) == 20, "the host reserves 20 bytes per slot tag");
 static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment record");
 
 // BF: the layer may have bf16 tiles (sink or residual tokens); the variant without
@@ -964,8 +963,6 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   off += NW * kMaxStages * sizeof(uint64_t);
   int* tbl = reinterpret_cast<int*>(smem + off);  // per warp: a window of 32 block-table entries
   off += NW * 32 * sizeof(int);
-  SlotTag* tags = reinterpret_cast<SlotTag*>(smem + off);  // per warp and slot
-  off += NW * kMaxStages * sizeof(SlotTag);
   float* q_s = reinterpret_cast<float*>(smem + off);  // [g + 1 rows][kQRow]: the query heads, a zero row
   off += (size_t)(g + 1) * kQRow * sizeof(float);
   float* recs = reinterpret_cast<float*>(smem + off);  // NW/2 merge records [g heads][kMergeStride]
@@ -1061,10 +1058,13 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   uint8_t* my_stages = stage_base + (size_t)warp * nst * p.stage_bytes;
   uint64_t* my_bars = bars + warp * kMaxStages;
   int* my_tbl = tbl + warp * 32;
-  SlotTag* my_tags = tags + warp * kMaxStages;
   float* my_rec = recs + (size_t)(warp % NR) * (p.merge_bytes / 4);
   uint32_t phase_bits = 0;  // expected parity of each stage barrier of this warp
-  uint32_t slot_valid = 0;  // lane 0: 8 bits per slot, the tiles its stage holds
+  uint32_t slot_valid = 0;  // 8 bits per slot: the tiles its stage holds (every lane keeps the same)
+  // the two slots' tags, kept in registers by every lane (the producer's cursor is the same in all
+  // lanes): the first tile (a), and seg | kind << 8 | n << 12 | rpos << 16 | first << 24
+  uint32_t tga0 = 0, tgb0 = 0, tga1 = 0, tgb1 = 0;
+  static_assert(kMaxStages == 2, "two slots per warp: two register sets of tags");
   uint32_t pending = 0;     // slots with copies in flight
   bool alive = true;
   int n_issued = 0, n_consumed = 0;
@@ -1339,11 +1339,13 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           ++q_rec;
         }
       }
-      if (lane == 0) {
-        slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
-        my_tags[slot] = tg;
+      {
+        const uint32_t pk2 = (uint32_t)tg.seg | ((uint32_t)tg.kind << 8) | ((uint32_t)tg.n << 12) |
+                             ((uint32_t)tg.rpos << 16) | ((uint32_t)tg.first << 24);
+        if (slot) { tga1 = (uint32_t)tg.a; tgb1 = pk2; } else { tga0 = (uint32_t)tg.a; tgb0 = pk2; }
       }
       vm = __shfl_sync(kFull, vm, 0);
+      slot_valid = (slot_valid & ~(0xFFu << (8 * slot))) | (vm << (8 * slot));
       if (vm) pending |= 1u << slot;
       ++n_issued;
       if (++p_slot == nst) p_slot = 0;
@@ -1422,9 +1424,18 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           if (n_consumed == n_issued) break;  // no work left for this warp in this batch
         }
         const int slot = c_slot;
-        const SlotTag tg = my_tags[slot];
+        SlotTag tg;
+        {
+          const uint32_t w = slot ? tgb1 : tgb0;
+          tg.a = (int)(slot ? tga1 : tga0);
+          tg.seg = (int)(w & 0xFFu);
+          tg.kind = (short)((w >> 8) & 0xFu);
+          tg.n = (short)((w >> 12) & 0xFu);
+          tg.rpos = (int)((w >> 16) & 0xFFu);
+          tg.first = (int)(w >> 24);
+        }
         if (tg.seg != s) break;  // the producer has moved on: segment s is done for this warp
-        const uint32_t vmask = (__shfl_sync(kFull, slot_valid, 0) >> (8 * slot)) & 0xFFu;
+        const uint32_t vmask = (slot_valid >> (8 * slot)) & 0xFFu;
         if (vmask) {
           bool ok = alive && mbar_wait_bounded(smem_addr(&my_bars[slot]), (phase_bits >> slot) & 1u, kWaitLimitCycles);
           ok = __all_sync(kFull, ok);
@@ -1444,7 +1455,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           for (int j = 1; j < n_issued - n_consumed; ++j) {
             int sl = slot + j;
             if (sl >= nst) sl -= nst;
-            newer += my_tags[sl].kind != 3;
+            newer += (((sl ? tgb1 : tgb0) >> 8) & 0xFu) != 3u;
           }
           if (newer == 0) cp_async_wait<0>();
           else if (newer == 1) cp_async_wait<1>();
