@@ -316,7 +316,10 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == -4
 
 
-@pytest.mark.parametrize("fmt,lens", [("int4", [2000, 700, 33]), ("fp8_e4m3", [4000, 17, 900])])
+@pytest.mark.parametrize("fmt,lens", [("int4", [2000, 700, 33]), ("fp8_e4m3", [4000, 17, 900]),
+                                      # equal lengths: whole pairs per CTA (128 pairs: one each; 256: two each)
+                                      ("int4", [300] * 64), ("int4", [100] * 128), ("fp8_e4m3", [200] * 64)],
+                         ids=["int4-ragged", "fp8-ragged", "int4-128pairs", "int4-256pairs", "fp8-128pairs"])
 def test_fused_combine_equals_two_launches_and_repeats(fmt, lens):
     # kvq_decode_attention merges partials inside the decode launch (arrival counters in the
     # workspace); kvq_decode_partials + kvq_decode_combine do it in two launches.  Same bits,
@@ -326,6 +329,7 @@ def test_fused_combine_equals_two_launches_and_repeats(fmt, lens):
     gl, caches, q = build(fmt, 2, 4, lens, G, 128, 32 if G > 1 else 0, 0, False, 21)
     o1, l1 = gl.decode(q)
     B, Hq = len(lens), 8
+    TL.check_attention(o1.cpu().numpy(), l1.cpu().numpy(), *O.decode_attention(O.bf16_to_f32(q), caches))
     qd = torch.from_numpy(q.astype(np.int16)).cuda()
     wsb = kvq.decode_workspace_size(gl.cfg, B, Hq)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
