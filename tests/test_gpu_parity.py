@@ -276,6 +276,27 @@ def test_bad_block_and_capacity_are_reported_not_faulted():
     assert torch.isfinite(out).all()
 
 
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "int4"])
+def test_append_decode_past_capacity_is_reported_not_stored(fmt):
+    # a full store: the step's token cannot be stored; the call reports
+    # KVQ_DEV_CAPACITY, writes nothing, and attends over the tokens the store holds
+    from quantized_kv_cache_decode_gb300 import kvq
+    G = 1 if fmt == "fp8_e4m3" else 16
+    lens = [32, 32] if fmt == "fp8_e4m3" else [47, 47]  # the most each store holds (INT4: 32 + a 15-token window)
+    gl, caches, q = build(fmt, 2, 4, lens, G, 128, 0, 0, False, 31)
+    names = ("qstore",) if fmt == "fp8_e4m3" else ("qstore", "resid_k", "resid_v")
+    before = {name: gl.raw(name).copy() for name in names}
+    kb = I.random_bf16(77, (len(lens), 2, 128))
+    vb = I.random_bf16(78, (len(lens), 2, 128))
+    gl.status.zero_()
+    out, lse = gl.append_decode(kb, vb, q, lens)
+    assert gl.status_value() & kvq.DEV_CAPACITY
+    for name, raw in before.items():
+        assert np.array_equal(gl.raw(name), raw)
+    out_ref, lse_ref = O.decode_attention(O.bf16_to_f32(q), caches)
+    TL.check_attention(out.cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref)
+
+
 def test_bounded_wait_runs_out_reports_and_context_stays_usable():
     # self-test hook: one warp's first copy is withheld while its barrier expects the bytes,
     # so its bounded wait (about a second) gives up; the launch reports KVQ_DEV_TIMEOUT and
