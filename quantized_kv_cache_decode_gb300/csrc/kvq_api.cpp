@@ -229,8 +229,10 @@ cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
 // 80 % of the SMs: then every CTA's range is k whole pairs (for equal sequence
 // lengths), so no pair is split and no partial is written, fenced and merged
 // across CTAs.  Measured on GB300 with 128 pairs (B = 16, 8 kv heads, T = 8192):
-// FP8 decode 61.0 -> 52.6 us, bf16 121.2 -> 108.4 us.  The 2/4/8-bit layers
-// are bound by the SMs' instruction issue and keep every SM.
+// FP8 decode 61.0 -> 52.6 us, bf16 121.2 -> 108.4 us.  The 2/4/8-bit layers are
+// bound by their warps' dependency chains and keep every SM: the kernel itself
+// gives whole pairs to the CTAs when the lengths turn out equal (range_ctas), and
+// a ragged batch uses them all.
 int grid_ctas(const LayerDesc& L, int batch, int sms) {
   const long long pairs = (long long)batch * L.H;
   if (!(L.fp8 || L.bf16) || pairs < 1) return sms;

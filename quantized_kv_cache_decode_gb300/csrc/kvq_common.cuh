@@ -219,8 +219,8 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 // CTAs that share the work units of a decode launch: the grid, or fewer when the
 // units are so few that a CTA would get less than kMinCtaUnits of them (its
 // fixed costs, and the merge of many tiny partials, would outweigh its share);
-// the CTAs beyond that count have empty ranges.  The decode kernel and the
-// two-launch merge both derive it from the unit total U.
+// the CTAs beyond that count have empty ranges (see range_ctas for the choice
+// the decode kernel makes, which it records for the two-launch merge).
 constexpr long long kMinCtaUnits = 16;
 __host__ __device__ __forceinline__ long long working_ctas(long long grid, long long U) {
   const long long c = U / kMinCtaUnits;
