@@ -698,15 +698,39 @@ def run_reference(args, w, rank, world):
 # --------------------------------------------------------------------------- #
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank space (string literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":  # literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sources_sha256() -> str:
-    """Hash of the CUDA sources of the library (decides whether a recorded ncu traffic figure still applies)."""
+    """Hash of the code of the library's CUDA sources, comments and blank space left out (decides
+    whether a recorded ncu traffic figure still applies: a comment edit does not change a kernel)."""
     import hashlib
     h = hashlib.sha256()
     src = os.path.join(ROOT, "quantized_kv_cache_decode_gb300", "csrc")
     for name in sorted(os.listdir(src)):
         if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(src, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 
