@@ -680,14 +680,19 @@ __device__ __forceinline__ float rope_group_scale(const float* ks, const float* 
 }
 
 // Raw scores (d * kfac: the score in the log2 domain) of one quantized tile with the
-// Keys rotated at positions t0 + token: the same MMA layout as qk_tile, the Key
-// operand being the rotated fp32 Keys scaled by kapk in two f16 terms (four MMAs per step).
+// Keys rotated at positions t0 + token.  The rotated fp32 Keys, scaled by kapk and
+// split in two f16 terms, are the A operand (the fragment order of the codes: rows =
+// tokens r, r + 8 of the lane) and the query the B operand: column n holds query
+// head n (exact in one f16 term: q is bf16), so one pair of MMAs per step covers the
+// 16 tokens for up to 8 heads (16 MMAs per tile).  D(token, head) of lane (r, q) holds
+// tokens r, r + 8 of heads 2q, 2q + 1; eight shuffles bring the scores to the
+// query-rows layout of qk_tile (head r, tokens 2q, 2q + 1, 2q + 8, 2q + 9).
 template <int FMT>
 __device__ __forceinline__ void qk_tile_rope(const uint32_t (&KW)[FT<FMT>::kWords], const uint32_t (&X)[8][4],
                                              const float* ks, const float* kz, const unsigned long long* turn, int t0,
                                              int r, int q, float kapk, float (&d)[4]) {
   constexpr float kH = (float)FT<FMT>::kHalf;
-  float lo[2][4] = {}, hi[2][4] = {};
+  float acc[2][4] = {};
   const int tpos[2] = {t0 + r, t0 + r + 8};
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -722,16 +727,27 @@ __device__ __forceinline__ void qk_tile_rope(const uint32_t (&KW)[FT<FMT>::kWord
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int st = s + 4 * j;
-      mma_f16(lo[j], X[st][0], X[st][1], X[st][2], X[st][3], kh[0][j], kh[2][j]);
-      mma_f16(lo[j], X[st][0], X[st][1], X[st][2], X[st][3], kl[0][j], kl[2][j]);
-      mma_f16(hi[j], X[st][0], X[st][1], X[st][2], X[st][3], kh[1][j], kh[3][j]);
-      mma_f16(hi[j], X[st][0], X[st][1], X[st][2], X[st][3], kl[1][j], kl[3][j]);
+      mma_f16(acc[j], kh[0][j], kh[1][j], kh[2][j], kh[3][j], X[st][0], X[st][1]);
+      mma_f16(acc[j], kl[0][j], kl[1][j], kl[2][j], kl[3][j], X[st][0], X[st][1]);
     }
   }
-  d[0] = (lo[0][0] + lo[0][2]) + (lo[1][0] + lo[1][2]);
-  d[1] = (lo[0][1] + lo[0][3]) + (lo[1][1] + lo[1][3]);
-  d[2] = (hi[0][0] + hi[0][2]) + (hi[1][0] + hi[1][2]);
-  d[3] = (hi[0][1] + hi[0][3]) + (hi[1][1] + hi[1][3]);
+  const float a0 = acc[0][0] + acc[1][0], a1 = acc[0][1] + acc[1][1];  // token r: heads 2q, 2q + 1
+  const float a8 = acc[0][2] + acc[1][2], a9 = acc[0][3] + acc[1][3];  // token r + 8
+  // head r, token 2q (2q + 8) sits in lane 8q + r / 2 as its head (r & 1) of row 2q; token
+  // 2q + 1 (2q + 9) in lane 8q + 4 + r / 2
+  const int src = 8 * q + (r >> 1);
+  const bool odd = (r & 1) != 0;
+  float v0 = __shfl_sync(kFull, a0, src), v1 = __shfl_sync(kFull, a1, src);
+  d[0] = odd ? v1 : v0;
+  v0 = __shfl_sync(kFull, a0, src + 4);
+  v1 = __shfl_sync(kFull, a1, src + 4);
+  d[1] = odd ? v1 : v0;
+  v0 = __shfl_sync(kFull, a8, src);
+  v1 = __shfl_sync(kFull, a9, src);
+  d[2] = odd ? v1 : v0;
+  v0 = __shfl_sync(kFull, a8, src + 4);
+  v1 = __shfl_sync(kFull, a9, src + 4);
+  d[3] = odd ? v1 : v0;
 }
 
 // Scores of a bf16 tile (sink / residual rows, stored before RoPE) with its Keys
@@ -812,6 +828,9 @@ __device__ __forceinline__ void bf16_qk_rope(const uint8_t* stg, const float* qr
 
 // The query-side operand of a pre-RoPE layer, once per segment: x_c = q_c kappa (kappa
 // the power of two bringing max |q_c| into [2^13, 2^14)), hi/lo as in build_x_fp8.
+// Query operand of pre-RoPE layers (qk_tile_rope's B operand, column = the lane's
+// head r): channels 16s + 4q, +1 in X[s][0] and 16s + 4q + 2, +3 in X[s][1], the
+// bf16 query times a power of two kap (one f16 term, exact: max |q| kap < 2^14).
 __device__ __forceinline__ void build_x_rope(const float* qrow, int q, uint32_t (&X)[8][4], float& kap, float& inv) {
   float mx = 0.f;
 #pragma unroll
@@ -822,12 +841,12 @@ __device__ __forceinline__ void build_x_rope(const float* qrow, int q, uint32_t 
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
   kap = pow2_fit_f16(mx, inv);
-  const float2 k2 = make_float2(kap, kap);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const float4 x = *reinterpret_cast<const float4*>(qrow + 16 * s + 4 * q);
-    split_f16x2(mul_f32x2(make_float2(x.x, x.y), k2), X[s][0], X[s][1]);
-    split_f16x2(mul_f32x2(make_float2(x.z, x.w), k2), X[s][2], X[s][3]);
+    X[s][0] = pack_f16(x.x * kap, x.y * kap);
+    X[s][1] = pack_f16(x.z * kap, x.w * kap);
+    X[s][2] = X[s][3] = 0u;
   }
 }
 
