@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 // One CTA of NT threads per (sequence, kv head, spilled group): the group's G
 // bf16 Key and Value rows are staged in shared memory (coalesced 16-byte loads,
 // from the ring for tokens already cached, from the input for new ones); every
-// channel's Key min/max is found by two threads over half the tokens each, every
+// channel's Key min/max is found by NT/128 threads over runs of the tokens, every
 // (token, Gv-channel group) Value min/max by a segmented warp-shuffle reduction;
 // then each 32-bit word of the tile's fragment-order code matrices is assembled
 // in registers (the inverse of the layout formula: which (token, channel) each
@@ -190,14 +190,38 @@ __global__ void __launch_bounds__(NT, 1024 / NT) spill_kernel(const AppendParams
       float* ksz = reinterpret_cast<float*>(Vs + G * kSRow);        // K scale [128], K zero [128]
       float* red = ksz + 256;                                       // [kKSegs][min, max][128]
       float* vsz = red + kKSegs * 256;                              // V scale [G][ngv], V zero [G][ngv]
-      // stage the group's rows: 16-byte chunk ch of row tt, K then V
-      for (int idx = tid; idx < 2 * G * 16; idx += NT) {
-        const int which = idx >= G * 16, rem = idx - which * G * 16, tt = rem >> 4, ch = rem & 15;
-        const long long t = L.S + x0 + tt;
-        const __nv_bfloat16* src;
-        if (t < T0) src = (which ? ring_v : ring_k) + (pair * L.W + (t - L.S) % L.W) * L.d;
-        else src = (which ? vnew : knew) + (t - T0) * L.d;
-        reinterpret_cast<uint4*>((which ? Vs : Ks) + tt * kSRow)[ch] = reinterpret_cast<const uint4*>(src)[ch];
+      // stage the group's rows: 16-byte chunk ch of row tt, K then V; each thread issues up to
+      // four loads before their stores (one HBM round trip instead of four), and the ring slot of
+      // row tt is the group's first slot plus tt, wrapped once (tt < G <= W)
+      const int slot0 = (int)(x0 % L.W);
+      constexpr int kBatch = 4;
+      for (int base = tid; base < 2 * G * 16; base += kBatch * NT) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = base + u * NT;
+          if (idx < 2 * G * 16) {
+            const int which = idx >= G * 16, rem = idx - which * G * 16, tt = rem >> 4, ch = rem & 15;
+            const long long t = L.S + x0 + tt;
+            const __nv_bfloat16* src;
+            if (t < T0) {
+              int sl = slot0 + tt;
+              if (sl >= L.W) sl -= L.W;
+              src = (which ? ring_v : ring_k) + (pair * L.W + sl) * L.d;
+            } else {
+              src = (which ? vnew : knew) + (t - T0) * L.d;
+            }
+            v[u] = reinterpret_cast<const uint4*>(src)[ch];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = base + u * NT;
+          if (idx < 2 * G * 16) {
+            const int which = idx >= G * 16, rem = idx - which * G * 16, tt = rem >> 4, ch = rem & 15;
+            reinterpret_cast<uint4*>((which ? Vs : Ks) + tt * kSRow)[ch] = v[u];
+          }
+        }
       }
       __syncthreads();
       if (L.k_out | L.v_out) {
