@@ -1633,8 +1633,16 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           };
           const int n = tg.n;
           if constexpr (ONE) {
-            // one tile per record (16-token Key groups): record k of the stage at k * rec_bytes,
-            // every tile starts a group (straight-line code: the build overlaps the rest)
+            // one tile per record (16-token Key groups, or FP8 tiles): record k of the stage at
+            // k * rec_bytes, every integer tile starts a group (straight-line code: the build
+            // overlaps the rest)
+            if constexpr (F::kFp8) {  // the step's token (one-token append folded into this launch)
+              const int inew = (sg.qn - 1) >> 4;
+              if (p.fp8_append && inew >= tg.a && inew < tg.a + n && ((vmask >> (inew - tg.a)) & 1u) &&
+                  (long long)p.seq_lens[sg.b] + 1 <= tmax_tok)
+                fp8_append_token(p, const_cast<uint8_t*>(stg + (inew - tg.a) * L.rec_bytes + L.hdr_bytes), sg.b,
+                                 sg.h, inew, (sg.qn - 1) & 15, lane);
+            }
             if (n == 2 && vmask == 3u) {
               // the common stage, two tiles as straight-line code: the second tile's operand build
               // and Key unpack fill the first tile's MMA latencies (paged INT4 layer 537 -> 525 us)
@@ -1966,7 +1974,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, int smem, cudaStream_t stream
   const bool ka = p.n_query == 1 && p.g <= 4;  // few query columns: the Key tile as the A operand
   if constexpr (FT<FMT>::kFp8) {
     if (p.L.S == 0) {
-      if (ka) return launch_variant<FMT, NGV, false, false, false, false, false, true>(p, smem, stream);
+      if (ka)  // one tile per record (contiguous store): the straight-line variant
+        return p.L.tpg == 1 ? launch_variant<FMT, NGV, false, false, true, false, false, true>(p, smem, stream)
+                            : launch_variant<FMT, NGV, false, false, false, false, false, true>(p, smem, stream);
       return p.n_query > 1 ? launch_variant<FMT, NGV, false, true, false>(p, smem, stream)
                            : launch_variant<FMT, NGV, false, false, false>(p, smem, stream);
     }
