@@ -54,7 +54,9 @@ namespace kvq {
 // kvq_internal.h states the same for the host.
 template <int FMT>
 struct DecodeWarps {
-  static constexpr int kNW = 12;
+  // 8-bit codes: 8 warps of up to 255 registers (measured on GB300: the paged INT8 layers
+  // 643 -> 600 us; the 2/4-bit and FP8 layers are faster with 12)
+  static constexpr int kNW = FMT == 8 ? 8 : 12;
   static constexpr int kThreads = kNW * 32;
 };
 constexpr int kMaxStages = 2;

@@ -13,17 +13,14 @@ constexpr int kMaxGqa = 8;
 constexpr int kMaxBatch = 2048;
 constexpr int kMaxGroupTokens = 256;  // Key group length the append kernel stages in shared memory
 
-// Warps per decode CTA (one CTA per SM): 12, at most 168 registers a thread (the
-// kernel's DecodeWarps states the same).
-inline int decode_warps(int fmt) {
-  (void)fmt;
-  return 12;
-}
+// Warps per decode CTA (one CTA per SM; the kernel's DecodeWarps states the same):
+// 8 for 8-bit codes, else 12 (at most 168 registers a thread).
+inline int decode_warps(int fmt) { return fmt == KVQ_FMT_INT8 ? 8 : 12; }
 
 // The decode-kernel instantiation that serves a layer's format.  A bf16 layer
 // has no quantized tiles, so any instantiation runs only its bf16-tile path;
-// the 8-bit one is used.
-inline int kernel_format(int fmt) { return fmt == KVQ_FMT_BF16 ? KVQ_FMT_INT8 : fmt; }
+// the 4-bit one (12 warps) is used.
+inline int kernel_format(int fmt) { return fmt == KVQ_FMT_BF16 ? KVQ_FMT_INT4 : fmt; }
 
 // Validated, derived form of kvq_layer_config.
 struct LayerDesc {
