@@ -9,38 +9,38 @@
 // Work decomposition.  Every (sequence, kv head) pair is a list of work units:
 // its 16-token bf16 tiles (sink + residual window, charged `bf_weight` units
 // each) followed by its 16-token quantized tiles (1 unit each).  The pairs'
-// lists are concatenated and cut into equal ranges, one per CTA, so every CTA
-// moves the same number of bytes whatever the sequence lengths.  The grid is one
-// CTA per SM, or for HBM-bound layers one CTA per k whole pairs when that covers
-// most SMs (the host's choice); CTAs past one per kMinCtaUnits units stay idle.
-// A CTA writes one partial (normalised output + log-sum-exp) per pair it shares
-// with another CTA; the last CTA to finish such a pair merges them.
+// lists are concatenated and cut into equal ranges, one per working CTA, so every
+// CTA moves the same number of bytes whatever the sequence lengths; when every
+// sequence holds the same number of units, each working CTA takes whole pairs
+// instead (range_ctas).  A CTA writes one partial (normalised output +
+// log-sum-exp) per pair it shares with another CTA; the last CTA to finish such
+// a pair merges them.
 //
-// Inside a CTA the 12 or 16 warps take a segment's work items (a bf16 tile, or
-// a Key group's quantized tiles) round robin, interleaved over the whole
-// segment, and run their own pipelines: lane 0 of a warp streams stages (tiles
-// with their scales) into shared memory with bulk asynchronous copies
-// (cp.async.bulk, TMA engine) completing on per-stage mbarriers, a stage ahead
-// of the compute, so the copies of the next items (and segments) overlap the
-// math.
+// Inside a CTA the warps (12; 8 for 8-bit codes) take a segment's work items (a
+// bf16 tile, or whole records of quantized tiles) round robin, interleaved over
+// the whole segment, and run their own two-stage pipelines: a warp streams
+// stages (tiles with their scales and Key-group headers) into shared memory with
+// bulk asynchronous copies (cp.async.bulk, TMA engine; in the paged one-tile
+// case every lane copies one record) completing on per-stage mbarriers, a stage
+// ahead of the compute.  Every lane keeps the same producer cursor, so the slots'
+// tags live in registers.
 //
-// Tensor-core mapping (mma.sync m16n8k16, fp32 accumulate).  The cache tile is
-// the A operand (16 rows), the query side the B operand (8 columns):
-//   QK:  D[token][col] = sum_c K[token][c] * Bq[c][col].  A = centred Key codes
-//        (exact in f16), Bq = q_c s_c kappa (Key scale of the channel), split in
-//        two f16 halves: column 2j holds the high half and column 2j+1 the low
-//        half of query head 4b + j (b = column block), so the score of head
-//        4b + q sits in one lane, ~22 bits exact.  The zero-point term
-//        sum_c q_c s_c (2^(b-1) - z_c) is added per group in fp32.  FP8: A = E4M3
-//        codes (exact in f16), Bq = q kappa.  bf16 tiles: A = K, B = q (bf16).
-//   PV:  D[channel][head] = sum_t V^T[channel][t] * W[t][head], A = centred
-//        Value codes of 16 channels, W = p_t s_t (Value scale of the token and
-//        channel group) in f16; zero-point term accumulated per group in fp32.
-//        bf16 tiles: A = V (bf16), W split in two bf16 terms.
-// The probabilities move from the score layout (lane = head) to the W layout
-// (lane = token pair) with four shuffles per tile.  The codes are stored in the
-// A operand's register order (include/kvq.h, "fragment order"): each lane loads
-// its words with conflict-free 16-byte loads and unpacks them in registers.
+// Tensor-core mapping (mma.sync m16n8k16, fp32 accumulate), query rows: the A
+// operand is the query side -- row r (r < 8) the high f16 half, row r + 8 the
+// low half of x_c = q_c s_c kappa of query column r (s_c the Key group's
+// per-channel scale, kappa a power of two) -- and the B operand the Key codes
+// themselves, in their stored fragment order, as f16 values (subnormal
+// placement for 8-bit codes, centred values for 2- and 4-bit ones).  The scores
+// of column r land in lane (r, q) for tokens 2q, 2q + 1, 2q + 8, 2q + 9: the
+// layout of the PV B operand, so the online softmax needs no shuffles.  PV: A =
+// the Value codes (V^T fragment order, subnormal placement), B = W = p s_V (one
+// f16 term); the zero-point sums are kept in fp32 with the rounded weights.
+// With at most four query columns (one query token) the Key tile is the A
+// operand and the query the B operand instead (qk_tile_ka: half the MMAs);
+// pre-RoPE Keys take that form too (qk_tile_rope).  bf16 tiles: the same
+// layouts with ldmatrix loads.  The codes are stored in an A operand's register
+// order (include/kvq.h, "fragment order"): each lane loads its words with
+// conflict-free 16-byte loads and unpacks them in registers.
 #pragma once
 
 #include <mutex>
@@ -50,8 +50,8 @@
 namespace kvq {
 
 // Warps per CTA (one CTA per SM at most): 12 (168 registers a thread; with 16
-// warps and 128 registers the integer variants spill); decode_warps() in
-// kvq_internal.h states the same for the host.
+// warps and 128 registers the integer variants spill), 8 for 8-bit codes;
+// decode_warps() in kvq_internal.h states the same for the host.
 template <int FMT>
 struct DecodeWarps {
   // 8-bit codes: 8 warps of up to 255 registers (measured on GB300: the paged INT8 layers
@@ -950,9 +950,9 @@ static_assert(sizeof(SegRec) == 80, "the host reserves 80 bytes per segment reco
 // BF: the layer may have bf16 tiles (sink or residual tokens); the variant without
 // them (FP8 layers with no sink tokens) carries no bf16-tile code at all.  MQ:
 // several query tokens per sequence (causal limits per column); only that
-// variant carries the limit checks.  ONE: integer layers whose Key groups are one
-// tile each (G = 16, the paged blocks): every tile rebuilds the query-side
-// operand, in straight-line code.  ROPE: pre-RoPE Keys (integer layers), rotated
+// variant carries the limit checks.  ONE: one tile per record -- integer layers
+// whose Key groups are one tile each (G = 16, the paged blocks: every tile rebuilds
+// the query-side operand) and contiguous FP8 stores -- in straight-line code.  ROPE: pre-RoPE Keys (integer layers), rotated
 // at their positions.  OUT: dense-and-sparse rows (integer layers): the kept Key
 // entries add q_c x_c to the scores, the kept Value entries p x_c to the outputs
 // (through a per-warp shared-memory sum of 8 columns x 128 channels).  KA: at most
@@ -1522,7 +1522,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
           // ---- quantized stage: tiles [tg.a, tg.a + n), one softmax step each ----
           // tile i at `tile`; INT: `hdrp` the Key-group header, the query-side operand (q * s,
           // hi/lo) rebuilt from it when `build` (at each record, i.e. Key group, start)
-          auto tile_step = [&](const int i, const uint8_t* tile, const uint8_t* hdrp, const bool build) {
+          // a tile's step in two halves: tile_qk, the scores of the lane's column for its four tokens;
+          // tile_sv, the online softmax step and PV
+          auto tile_qk = [&](const int i, const uint8_t* tile, const uint8_t* hdrp, const bool build,
+                             float (&sig)[4]) {
             if constexpr (ROPE) {
               // the group's header to the warp's copy (the tiles of a group may span stages)
               if (build) {
@@ -1555,7 +1558,6 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
                 qk_tile<FMT>(KW, X, d);
             }
             const int tok_valid = min(16, sg.qn - i * 16);  // < 16 only for a partial FP8 tile
-            float sig[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)  // integer tiles are always full (Key groups of 16k tokens)
               sig[e] = (hv && (F::kInt || tk[e] < tok_valid)) ? fmaf(d[e], kfac, cterm) : -INFINITY;
@@ -1577,6 +1579,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               for (int e = 0; e < 4; ++e)
                 if (tk[e] > lim) sig[e] = -INFINITY;
             }
+          };
+          auto tile_sv = [&](const uint8_t* tile, float (&sig)[4]) {
             const float* vsp = reinterpret_cast<const float*>(tile + 2 * F::kTile);  // INT: Value scales [16][NGV]
             const float* vzp = vsp + 16 * NGV;                                         // INT: Value zero-points
             float smax = s_v8;
@@ -1633,6 +1637,11 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
               pv_tile<FMT, NGV>(VW, B0, B1, stt.o);
             }
           };
+          auto tile_step = [&](const int i, const uint8_t* tile, const uint8_t* hdrp, const bool build) {
+            float sig[4];
+            tile_qk(i, tile, hdrp, build, sig);
+            tile_sv(tile, sig);
+          };
           const int n = tg.n;
           if constexpr (ONE) {
             // one tile per record (16-token Key groups, or FP8 tiles): record k of the stage at
@@ -1648,8 +1657,18 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
             if (n == 2 && vmask == 3u) {
               // the common stage, two tiles as straight-line code: the second tile's operand build
               // and Key unpack fill the first tile's MMA latencies (paged INT4 layer 537 -> 525 us)
-              tile_step(tg.a, stg + L.hdr_bytes, stg, true);
-              tile_step(tg.a + 1, stg + L.rec_bytes + L.hdr_bytes, stg + L.rec_bytes, true);
+              if constexpr (FMT == 8) {
+                // 8-bit codes (8 warps, registers to spare): both tiles' scores first, so the second
+                // tile's QK MMAs are in flight during the first tile's softmax (INT8 599 -> 586 us)
+                float s0[4], s1[4];
+                tile_qk(tg.a, stg + L.hdr_bytes, stg, true, s0);
+                tile_qk(tg.a + 1, stg + L.rec_bytes + L.hdr_bytes, stg + L.rec_bytes, true, s1);
+                tile_sv(stg + L.hdr_bytes, s0);
+                tile_sv(stg + L.rec_bytes + L.hdr_bytes, s1);
+              } else {
+                tile_step(tg.a, stg + L.hdr_bytes, stg, true);
+                tile_step(tg.a + 1, stg + L.rec_bytes + L.hdr_bytes, stg + L.rec_bytes, true);
+              }
             } else {
               for (int k = 0; k < n; ++k) {
                 if (!((vmask >> k) & 1u)) continue;  // tile of a missing block
