@@ -134,7 +134,7 @@ cudaError_t launch_decode_int4(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_int8(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int smem, cudaStream_t s);
 cudaError_t launch_decode_fp8_e5m2(const DecodeParams& p, int smem, cudaStream_t s);
-// multi: the multi-query variant (several query tokens per sequence, two column blocks)
+// multi: the multi-query variant (several query tokens per sequence)
 cudaError_t occupancy_decode_int2(int ngv, int g, int multi, int smem, int* n);
 cudaError_t occupancy_decode_int4(int ngv, int g, int multi, int smem, int* n);
 cudaError_t occupancy_decode_int8(int ngv, int g, int multi, int smem, int* n);
