@@ -194,7 +194,7 @@ cudaError_t occupancy_query(const LayerDesc& L, int g, int multi, int smem, int*
 }
 
 // Resident CTAs per SM of the decode kernel for (device, format, Value groups,
-// query column blocks, shared memory), cached: the answer never changes for a
+// single- or multi-query variant, shared memory), cached: the answer never changes for a
 // given device.
 cudaError_t occupancy(const LayerDesc& L, int g, int multi, int smem, int* n) {
   struct Entry {
