@@ -96,6 +96,10 @@ CASES = [
     ("bf16", 2, 4, [0, 1, 15, 16, 17, 333], 0, 0, 0, 0, False, 16),
     ("bf16", 2, 8, [700, 31, 2], 0, 0, 0, 1, False, 16),
     ("bf16", 1, 1, [1500, 160], 0, 0, 0, 3, False, 16),
+    # the largest Key groups (256 tokens: 16 tiles per record, the spill's largest staging)
+    ("int4", 1, 4, [1200, 300, 511, 512], 256, 128, 256, 0, False, 16),
+    ("int8", 2, 8, [900, 767], 256, 64, 32, 1, False, 16),
+    ("int2", 1, 2, [1300, 40], 256, 32, 0, 0, False, 16),
 ]
 
 
