@@ -75,6 +75,7 @@ CASES = [
     # one long sequence over every SM: each pair merges more than 64 partials
     ("fp8_e4m3", 1, 8, [40000], 1, 128, 0, 1, False, 16),
     ("int4", 1, 4, [30000], 32, 128, 32, 0, False, 16),
+    ("int8", 1, 6, [25000], 16, 128, 64, 1, False, 16),  # 8-warp CTAs, one-tile records, many partials
     # 128 ragged pairs: the pair-aligned FP8 grid with pairs cut across CTAs
     ("fp8_e4m3", 8, 4, [16 + 37 * i for i in range(16)], 1, 128, 0, 0, False, 16),
     ("int4", 2, 4, [512], 32, 128, 32, 0, False, 16),
