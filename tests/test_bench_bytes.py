@@ -69,3 +69,13 @@ def test_llama2_7b_int2_step_with_spill():
     app = pairs * (512 + 512 + 32 * 128 * 2 * 2 + 2 * 32 * 128 // 4 + 128 * 8 + 32 * 4 * 8)
     assert app == 22020096
     assert bench.step_bytes(w, np.full(32, 32768), 1) == attn + app == 4367847424
+
+
+def test_launch_count_claim():
+    # the bench's gpu_launches: append + decode per layer, one launch for FP8 layers without
+    # sink tokens stepped through kvq_append_decode_attention (one token, one query)
+    assert bench.count_launches(I.llama3_8b_fp8()) == 1
+    assert bench.count_launches(I.llama3_8b_fp8_e5m2()) == 1
+    assert bench.count_launches(I.llama3_8b_fp8_2q()) == 2
+    assert bench.count_launches(I.llama3_70b_int4()) == 160
+    assert bench.count_launches(I.paged_mixed()) == 128
