@@ -451,33 +451,50 @@ def run_gpu(args, w, rank, world):
             views.append(v)
         return buf, views, sum(sizes)
 
-    d_in, d_out, h_in, h_out = [], [], [], []
-    h2d = d2h = 0
-    for lay in rep0:
-        bi, (lay.q, lay.k_new, lay.v_new), ni = packed([lay.q, lay.k_new, lay.v_new])
-        bo, (lay.out, lay.lse), no = packed([lay.out, lay.lse])
-        d_in.append(bi)
-        d_out.append(bo)
-        h_in.append(bi.cpu().pin_memory())
-        h_out.append(torch.empty(bo.shape, dtype=torch.uint8).pin_memory())
-        h2d += ni
-        d2h += no
+    # Two sets of device buffers, used by alternate steps, each holding the inputs (outputs) of all
+    # the step's layers in one buffer: a step moves its inputs in with one copy and its results out
+    # with one copy.  The copies run on their own stream, so the inputs of step i + 1 move to the
+    # device while step i computes and the results of step i move back while step i + 1 computes;
+    # every step's copies still lie inside the timed region.  The compute stream waits for them
+    # once per step (its kernels then run back to back).
+    sets = []  # [set] = (input buffer, output buffer, [layer] = (q, k_new, v_new, out, lse))
+    for sidx in range(2):
+        bi, vi, h2d = packed([t for lay in rep0 for t in (lay.q, lay.k_new, lay.v_new)])
+        bo, vo, d2h = packed([t for lay in rep0 for t in (lay.out, lay.lse)])
+        sets.append((bi, bo, [tuple(vi[3 * j:3 * j + 3]) + tuple(vo[2 * j:2 * j + 2]) for j in range(len(rep0))]))
+    h_in = sets[0][0].cpu().pin_memory()
+    h_out = [torch.empty(sets[s][1].shape, dtype=torch.uint8).pin_memory() for s in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # a set's inputs are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # a set's step has finished computing
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # a set's results are on the host
+    compute = torch.cuda.current_stream()
 
-    def e2e_step():
-        # per layer: the step's q and new K/V from pinned host memory, append + decode,
-        # the output and lse back to pinned host memory
-        for j, lay in enumerate(rep0):
-            d_in[j].copy_(h_in[j], non_blocking=True)
+    def e2e_step(i):
+        sidx = i % 2
+        bi, bo, views = sets[sidx]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_done[sidx])  # the set's last step has read its inputs
+            bi.copy_(h_in, non_blocking=True)
+            ev_in[sidx].record(copy_stream)
+        compute.wait_event(ev_in[sidx])
+        compute.wait_event(ev_out[sidx])  # the set's last results have left its output buffer
+        for lay, v in zip(rep0, views):
+            lay.q, lay.k_new, lay.v_new, lay.out, lay.lse = v
             lay.step_calls()
-            h_out[j].copy_(d_out[j], non_blocking=True)
+        ev_done[sidx].record(compute)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_done[sidx])
+            h_out[sidx].copy_(bo, non_blocking=True)
+            ev_out[sidx].record(copy_stream)
 
-    for _ in range(min(3, E)):
-        e2e_step()
+    for i in range(min(3, E)):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier()
     e0 = time.perf_counter()
-    for _ in range(E):
-        e2e_step()
+    for i in range(E):
+        e2e_step(i)
     torch.cuda.synchronize()
     e_ms = (time.perf_counter() - e0) * 1e3 / E
     e_ms = max_over_ranks(e_ms, dev)
