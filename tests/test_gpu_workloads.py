@@ -167,18 +167,18 @@ def test_llama3_8b_int4_dense_and_sparse_sampled():
 @pytest.mark.parametrize("layer", [0, 79])
 def test_llama3_70b_int4_sampled(layer):
     w = I.llama3_70b_int4()
-    _check_layer(w, layer, _pairs(w, 8, 7 + layer))
+    _check_layer(w, layer, _pairs(w, 16, 7 + layer))
 
 
 def test_llama2_7b_int2_append_spill_sampled():
     w = I.llama2_7b_int2()
-    _check_layer(w, 0, _pairs(w, 10, 9))
+    _check_layer(w, 0, _pairs(w, 16, 9))
 
 
 @pytest.mark.parametrize("layer", [0, 31, 63])
 def test_paged_mixed_sampled(layer):
     w = I.paged_mixed()
-    _check_layer(w, layer, _pairs(w, 12, 10 + layer))
+    _check_layer(w, layer, _pairs(w, 16, 10 + layer))
 
 
 def test_max_batch_many_short_sequences():
