@@ -470,31 +470,40 @@ def run_gpu(args, w, rank, world):
     ev_out = [torch.cuda.Event() for _ in range(2)]   # a set's results are on the host
     compute = torch.cuda.current_stream()
 
-    def e2e_step(i):
-        sidx = i % 2
-        bi, bo, views = sets[sidx]
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(ev_done[sidx])  # the set's last step has read its inputs
-            bi.copy_(h_in, non_blocking=True)
-            ev_in[sidx].record(copy_stream)
-        compute.wait_event(ev_in[sidx])
-        compute.wait_event(ev_out[sidx])  # the set's last results have left its output buffer
-        for lay, v in zip(rep0, views):
-            lay.q, lay.k_new, lay.v_new, lay.out, lay.lse = v
-            lay.step_calls()
-        ev_done[sidx].record(compute)
-        with torch.cuda.stream(copy_stream):
+    def copy_in(sidx):  # on the copy stream: the inputs of the next step that uses set sidx
+        copy_stream.wait_event(ev_done[sidx])  # the set's last step has read its inputs
+        sets[sidx][0].copy_(h_in, non_blocking=True)
+        ev_in[sidx].record(copy_stream)
+
+    def e2e_steps(n):
+        # step i computes on set i % 2; after its kernels are queued, the copy stream moves the
+        # inputs of step i + 1 in (they wait only for step i - 1, so they overlap step i's
+        # kernels) and then step i's results out
+        torch.cuda.set_stream(copy_stream)
+        copy_in(0)
+        for i in range(n):
+            sidx = i % 2
+            bi, bo, views = sets[sidx]
+            torch.cuda.set_stream(compute)
+            compute.wait_event(ev_in[sidx])
+            compute.wait_event(ev_out[sidx])  # the set's last results have left its output buffer
+            for lay, v in zip(rep0, views):
+                lay.q, lay.k_new, lay.v_new, lay.out, lay.lse = v
+                lay.step_calls(compute)
+            ev_done[sidx].record(compute)
+            torch.cuda.set_stream(copy_stream)
+            if i + 1 < n:
+                copy_in(1 - sidx)
             copy_stream.wait_event(ev_done[sidx])
             h_out[sidx].copy_(bo, non_blocking=True)
             ev_out[sidx].record(copy_stream)
+        torch.cuda.set_stream(compute)
 
-    for i in range(min(3, E)):
-        e2e_step(i)
+    e2e_steps(min(3, E))
     torch.cuda.synchronize()
     barrier()
     e0 = time.perf_counter()
-    for i in range(E):
-        e2e_step(i)
+    e2e_steps(E)
     torch.cuda.synchronize()
     e_ms = (time.perf_counter() - e0) * 1e3 / E
     e_ms = max_over_ranks(e_ms, dev)
