@@ -253,8 +253,9 @@ kvq_status decode_geometry(const LayerDesc& L, int batch, int g, DecodeGeom* G, 
   const int wsc = merge_bytes_of(L, g);
   const int nw = decode_warps(kernel_format(L.fmt));
   // pre-RoPE Keys: each warp keeps a copy of its current Key group's header (1 KB);
-  // dense-and-sparse Values: each warp accumulates the sparse part of its outputs (8 x 128 floats)
-  const int fixed = fixed_smem(batch, wsc, nw) + (L.rope ? nw * 1024 : 0) + (L.v_out ? nw * 4096 : 0);
+  // dense-and-sparse Values: each warp accumulates the sparse part of its outputs (8 x kSparseRow floats)
+  const int fixed = fixed_smem(batch, wsc, nw) + (L.rope ? nw * 1024 : 0) +
+                    (L.v_out ? nw * 8 * kSparseRow * (int)sizeof(float) : 0);
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;

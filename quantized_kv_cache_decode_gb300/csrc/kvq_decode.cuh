@@ -996,8 +996,8 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
   off += ((size_t)B * sizeof(int) + 15) / 16 * 16;
   // pre-RoPE Keys: per warp, the current Key group's header (K scale [128], K zero [128])
   float* rope_hdr = ROPE ? reinterpret_cast<float*>(smem + off) + warp * 256 : nullptr;
-  // dense-and-sparse Values: per warp, the sparse part of the 8 columns' outputs [8][128]
-  float* sp_acc = (OUT && L.v_out) ? reinterpret_cast<float*>(smem + off) + warp * 1024 : nullptr;
+  // dense-and-sparse Values: per warp, the sparse part of the 8 columns' outputs [8][kSparseRow]
+  float* sp_acc = (OUT && L.v_out) ? reinterpret_cast<float*>(smem + off) + warp * 8 * kSparseRow : nullptr;
   __shared__ int seg_count;
   __shared__ long long batch_end;
 
@@ -1404,10 +1404,10 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
       state_init(stt);
       if (sp_acc) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) reinterpret_cast<float4*>(sp_acc)[lane + 32 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < 8; ++i) reinterpret_cast<float4*>(sp_acc + i * kSparseRow)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncwarp();
       }
-      float* sp_row = sp_acc ? sp_acc + r * 128 : nullptr;  // the lane's column
+      float* sp_row = sp_acc ? sp_acc + r * kSparseRow : nullptr;  // the lane's column
       const float* qrow = q_s + min(r, g) * kQRow;  // the lane's query column (row g is zero)
       const float* qrow_op = KA ? q_s + min(r >> 1, g) * kQRow : qrow;  // the row the lane's operand is built from
       const bool hv = r < g;                         // the column exists
@@ -1746,7 +1746,7 @@ __global__ void __launch_bounds__(DecodeWarps<FMT>::kThreads, 1) decode_kernel(c
         for (int e = 0; e < 2; ++e)
 #pragma unroll
           for (int mb = 0; mb < 8; ++mb) {
-            const float* sr = sp_acc + (2 * q + e) * 128 + 16 * mb + r;
+            const float* sr = sp_acc + (2 * q + e) * kSparseRow + 16 * mb + r;
             if (mo[e] != -INFINITY) {
               stt.o[mb][e] += sr[0];
               stt.o[mb][2 + e] += sr[8];

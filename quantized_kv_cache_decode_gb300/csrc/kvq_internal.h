@@ -12,6 +12,9 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGqa = 8;
 constexpr int kMaxBatch = 2048;
 constexpr int kMaxGroupTokens = 256;  // Key group length the append kernel stages in shared memory
+// dense-and-sparse decode: floats per query column of a warp's sparse Value sums in shared
+// memory (128 channels + 4 pad, so that the 8 columns' rows start in different banks)
+constexpr int kSparseRow = 132;
 
 // Warps per decode CTA (one CTA per SM; the kernel's DecodeWarps states the same):
 // 8 for 8-bit codes, else 12 (at most 168 registers a thread).
