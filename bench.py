@@ -10,7 +10,10 @@ already resident in HBM; the cache is built before the timed region.
 Metric: effective KV GB/s = algorithmic bytes of one step (codes + scales and
 zero-points + bf16 sink/residual + q + out + lse + append traffic, every KV head
 read once) / step time.  Also reported: % of the measured HBM peak, tokens/s
-(sequences decoded per second).
+(sequences decoded per second), and the same metric end to end ("e2e"): every
+step's inputs copied in from pinned host memory and its results copied back,
+on a copy stream that overlaps them with the neighbouring steps' kernels, all
+inside the timed region.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
